@@ -1,0 +1,132 @@
+"""fp64 CPU oracle for the delta-rule linear-attention family.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg import this package; the product path (the CUDA library and
+its Python binding) never does, and this package imports nothing from it.
+
+The arithmetic lives in ``ldn_oracle.c`` (plain C, fp64, token by token); this
+module only builds it with gcc, loads it with ctypes and marshals numpy arrays.
+Every function's passage is cited in the C source.
+
+Parity status: pinned.  The pins are in tests/test_oracle_pins.py: the worked
+example of the linear-attention notes (Sec. 2.3), the exact write at beta = 1,
+the Gated DeltaNet prediction-correction identity of the Residual Linear
+Attention notes (Sec. 1.2), closed forms for orthonormal / axis keys, the
+linear-attention limit, orthogonal invariance and per-value-channel
+independence from the state-reduction notes (Sec. 2.5, Prop. 3.1), the rank
+bound (Eq. 3), the contraction of (I - beta k k^T), state passing, and a brute
+force by explicit matrix products at d = 4, T = 8.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ldn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libldn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MODE_DELTANET, MODE_GDN, MODE_KDA = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile ldn_oracle.c into libldn_oracle.so beside it (gcc, no fast-math,
+    no FMA contraction, so the fp64 rounding is the same on every host)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-pthread", "-D_POSIX_C_SOURCE=200809L", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # LDN_ORACLE_LIB points the tests' mutation check at a deliberately
+            # broken copy of this oracle; nothing else sets it.
+            path = os.environ.get("LDN_ORACLE_LIB") or build()
+            lib = ctypes.CDLL(path)
+            f = lib.ldn_oracle_fwd
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)]
+            lib.ldn_oracle_default_threads.restype = ctypes.c_int
+            lib.ldn_oracle_default_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return int(_load().ldn_oracle_default_threads())
+
+
+def _f32(x, name):
+    if x is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    if not np.all(np.isfinite(a)):
+        raise ValueError(f"oracle input {name} has non-finite values")
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def fwd(q, k, v, beta, gate=None, S0=None, mode=MODE_DELTANET, nthreads=0,
+        want_state=True, return_threads=False):
+    """Token-by-token recurrence in fp64.
+
+    q, k: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H];
+    gate (natural-log decay): [B, T, H] for Gated DeltaNet, [B, T, H, dk] for
+    KDA, ignored for DeltaNet; S0: [B, H, dk, dv] (memory orientation, i.e. the
+    transpose of the d_v x d_k math state) or None for zeros.
+    Returns (o [B, T, H, dv] float64, S_final [B, H, dk, dv] float64 or None).
+    """
+    q, k, v, beta = _f32(q, "q"), _f32(k, "k"), _f32(v, "v"), _f32(beta, "beta")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, T, H) or beta.shape != (B, T, H):
+        raise ValueError("oracle: inconsistent shapes")
+    if mode == MODE_DELTANET:
+        gate = None
+    else:
+        gate = _f32(gate, "gate")
+        want = (B, T, H) if mode == MODE_GDN else (B, T, H, dk)
+        if gate is None or gate.shape != want:
+            raise ValueError(f"oracle: gate must have shape {want}")
+    S0 = _f32(S0, "S0")
+    if S0 is not None and S0.shape != (B, H, dk, dv):
+        raise ValueError("oracle: S0 must be [B, H, dk, dv]")
+    out = np.empty((B, T, H, dv), dtype=np.float64)
+    sf = np.empty((B, H, dk, dv), dtype=np.float64) if want_state else None
+    used = ctypes.c_int(0)
+    rc = _load().ldn_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S0),
+                                _ptr(out), _ptr(sf), B, T, H, dk, dv, int(mode), int(nthreads),
+                                ctypes.byref(used))
+    if rc != 0:
+        raise RuntimeError(f"ldn_oracle_fwd failed with {rc}")
+    if return_threads:
+        return out, sf, int(used.value)
+    return out, sf
+
+
+def decode(q, k, v, beta, gate, S0, mode=MODE_GDN, nthreads=0):
+    """Consecutive single-token steps: inputs [steps, B, H, d], state [B, H, dk, dv].
+
+    A decode step is the same recurrence applied to one token; ``steps``
+    consecutive steps equal one pass over a sequence of that length, so this
+    transposes the step axis next to the batch axis and calls ``fwd``.
+    Returns (o [steps, B, H, dv], S_final [B, H, dk, dv])."""
+    tr = lambda a: None if a is None else np.ascontiguousarray(np.swapaxes(np.asarray(a), 0, 1))
+    o, sf = fwd(tr(q), tr(k), tr(v), tr(beta), tr(gate), S0, mode=mode, nthreads=nthreads)
+    return np.ascontiguousarray(np.swapaxes(o, 0, 1)), sf

@@ -1,0 +1,54 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/ldn_oracle.c (a sign, a
+dropped factor, a transposed index, a wrong operand), builds it into a
+temporary library on the CPU, and runs the pin suite against it in a child
+process.  The pin suite must fail for every mutant.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "ldn_oracle.c")
+
+MUTANTS = {
+    # the error is written with the wrong sign
+    "update_sign": ("W[(size_t)i * dk + c] += r * (double)k[c];",
+                    "W[(size_t)i * dk + c] -= r * (double)k[c];"),
+    # the write strength beta is dropped
+    "drop_beta": ("const double r = beta * (", "const double r = 1.0 * ("),
+    # the scalar forget gate is ignored
+    "drop_alpha": ("const double alpha = exp((double)J->gate[tok]);", "const double alpha = 1.0;"),
+    # the per-channel decay acts on the value side instead of the key side
+    "kda_left": ("const double a = exp((double)g[c]);\n                for (int i = 0; i < dv; ++i) W[(size_t)i * dk + c] *= a;",
+                 "for (int i = 0; i < dv; ++i) W[(size_t)i * dk + c] *= exp((double)g[i % dk]);"),
+    # the output reads the memory with the key instead of the query
+    "read_with_key": ("s += W[(size_t)i * dk + c] * (double)q[c];",
+                      "s += W[(size_t)i * dk + c] * (double)k[c];"),
+    # the initial state is read without the transpose
+    "s0_orientation": ("W[(size_t)i * dk + c] = (double)s0[(size_t)c * dv + i];",
+                       "W[(size_t)i * dk + c] = (double)s0[(size_t)i * dk + c];"),
+    # the prediction uses the query instead of the key
+    "predict_with_query": ("for (int c = 0; c < dk; ++c) s += W[(size_t)i * dk + c] * (double)k[c];\n            pred[i] = s;",
+                           "for (int c = 0; c < dk; ++c) s += W[(size_t)i * dk + c] * (double)q[c];\n            pred[i] = s;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    "-D_POSIX_C_SOURCE=200809L", str(mutant_c), "-o", str(lib), "-lm"], check=True)
+    env = dict(os.environ, LDN_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
