@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunkwise Gated DeltaNet forward (and the decode step).
+
+One step = one ldn_chunk_fwd over the workload
+gdn_bf16_b4_t2048_h16_d128 (B=4, T=2048, H=16, dk=dv=128, chunk 64, bf16
+q/k/v/out, fp32 beta/gates/state), inputs resident in HBM.  L2 is flushed
+(a 512 MiB device write) before every timed launch; each launch is timed with
+CUDA events on the stream it runs on.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on the host cores over a bounded sample of the same workload.
+Under torchrun each rank runs the same per-GPU workload (independent
+sequences: weak scaling) and the max time over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s chunkwise GDN fwd (H=16,dk=dv=128) + % roofline; decode GB/s"
+WORKLOAD = "gdn_bf16_b4_t2048_h16_d128"
+DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000")
+FLUSH_BYTES = 512 << 20          # > 129 MB L2
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work
+def chunk_bytes(B, T, H, dk, dv, el_bytes, mode, s0, s_final):
+    """Bytes a chunk forward must move at least: q, k, v read, o written,
+    beta and gate read (fp32), initial / final state (fp32)."""
+    n = B * T * H
+    gate = 0 if mode == 0 else (4 if mode == 1 else 4 * dk)
+    b = n * (el_bytes * (2 * dk + 2 * dv) + 4 + gate)
+    st = B * H * dk * dv * 4
+    return b + (st if s0 else 0) + (st if s_final else 0)
+
+
+def chunk_flops(B, T, H, dk, dv, C=64):
+    """Algorithmic flops of the chunk form per token-head, causal halves counted
+    once: 6 dk dv (state read/write products) + C (3 dk + 2 dv) + C^2 / 3."""
+    return B * T * H * (6 * dk * dv + C * (3 * dk + 2 * dv) + C * C / 3)
+
+
+def decode_bytes(B, H, dk, dv, mode):
+    gate = 0 if mode == 0 else (4 if mode == 1 else 4 * dk)
+    return B * H * (2 * dk * dv * 4 + 2 * dk * 4 + 2 * dv * 4 + 4 + gate)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gated_delta_rule_chunkwise_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key, src_hash):
+    """dram bytes per launch from a committed ncu summary, only if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_hash") == src_hash:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            self.out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(self.out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, row[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    """fp64 CPU oracle, timed on this host's cores over a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from gated_delta_rule_chunkwise_gb300 import workloads as wl
+    w = wl.make_chunk(args.workload)
+    threads = oracle.default_threads()
+    # calibrate one (b, h) chain, then size the per-step sample to ~1.5 s of wall time
+    t0 = time.perf_counter()
+    oracle.fwd(w.q[:1, :, :1], w.k[:1, :, :1], w.v[:1, :, :1], w.beta[:1, :, :1],
+               None if w.gate is None else w.gate[:1, :, :1], None, mode=w.mode, nthreads=1)
+    t1 = time.perf_counter() - t0
+    units = int(max(1, min(w.B * w.H, round(1.5 * threads / max(t1, 1e-6)))))
+    nb = max(1, min(w.B, units // w.H)) if units >= w.H else 1
+    nh = w.H if units >= w.H else units
+    sub = lambda a: None if a is None else np.ascontiguousarray(a[:nb, :, :nh])
+    q, k, v, beta, gate = sub(w.q), sub(w.k), sub(w.v), sub(w.beta), sub(w.gate)
+    used = threads
+    for _ in range(args.warmup):
+        oracle.fwd(q, k, v, beta, gate, None, mode=w.mode, want_state=True)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, _, used = oracle.fwd(q, k, v, beta, gate, None, mode=w.mode, want_state=True, return_threads=True)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    tokens = nb * w.T * nh              # token-heads of the sample, expressed per H heads below
+    value = (nb * w.T) * (nh / w.H) / (ms / 1e3)
+    sample = (f"{nb} of {w.B} sequences x {nh} of {w.H} heads x T={w.T} per step "
+              f"({tokens} token-heads; tokens/s scaled to H={w.H} heads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded recipe, no dataset)",
+            "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": 64, "mode": "gdn"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(w):
+    """The oracle as it stands, on this host's cores, over ~10-20 s of work."""
+    import numpy as np
+    import oracle
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.fwd(w.q[:1, :, :1], w.k[:1, :, :1], w.v[:1, :, :1], w.beta[:1, :, :1],
+               None if w.gate is None else w.gate[:1, :, :1], None, mode=w.mode, nthreads=1)
+    t1 = time.perf_counter() - t0
+    units = int(max(1, min(w.B * w.H, round(12.0 * threads / max(t1, 1e-6)))))
+    nb = max(1, min(w.B, units // w.H)) if units >= w.H else 1
+    nh = w.H if units >= w.H else units
+    sub = lambda a: None if a is None else np.ascontiguousarray(a[:nb, :, :nh])
+    t0 = time.perf_counter()
+    _, _, used = oracle.fwd(sub(w.q), sub(w.k), sub(w.v), sub(w.beta), sub(w.gate), None, mode=w.mode,
+                            return_threads=True)
+    dt = time.perf_counter() - t0
+    value = (nb * w.T) * (nh / w.H) / dt
+    return {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"{nb} of {w.B} sequences x {nh} of {w.H} heads x T={w.T} ({nb * nh * w.T} token-heads, "
+                      f"{dt:.1f} s wall); tokens/s scaled to H={w.H} heads"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    from gated_delta_rule_chunkwise_gb300 import build as ldn_build
+    ldn_build.build()
+    import gated_delta_rule_chunkwise_gb300 as ldn
+    from gated_delta_rule_chunkwise_gb300 import workloads as wl
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    # ---------------- chunk forward (the headline) ----------------
+    w = wl.make_chunk(args.workload, seed=rank)
+    t = w.torch_inputs("cuda")
+    el = 2 if w.dtype == "bf16" else 4
+    dtype_code = ldn.LDN_BF16 if w.dtype == "bf16" else ldn.LDN_F32
+    out = torch.empty((w.B, w.T, w.H, w.dv), dtype=t["q"].dtype, device="cuda")
+    S_final = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    P = lambda x: 0 if x is None else x.data_ptr()
+    args_ptrs = (P(t["q"]), P(t["k"]), P(t["v"]), P(t["beta"]), P(t["gate"]), P(t["S0"]), P(out), P(S_final))
+
+    def step():
+        st = ldn.ldn_chunk_fwd_variant(*args_ptrs, w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, dtype_code,
+                                       args.variant, sh)
+        if st != ldn.LDN_OK:
+            raise ldn.LdnError(st, "ldn_chunk_fwd")
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    if ldn.device_status() != ldn.LDN_OK:
+        raise RuntimeError("device status not ok after warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    wall0 = time.perf_counter()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    launches = args.steps
+    if ldn.device_status() != ldn.LDN_OK:
+        raise RuntimeError("device status not ok after the timed region")
+    per = [e0.elapsed_time(e1) for e0, e1 in evs]
+    ms = max_over_ranks(statistics.mean(per))
+    tokens = w.B * w.T
+    value = world * tokens / (ms / 1e3)
+    nbytes = chunk_bytes(w.B, w.T, w.H, w.dk, w.dv, el, w.mode, False, True)
+    flops = chunk_flops(w.B, w.T, w.H, w.dk, w.dv)
+    achieved_gbs = nbytes / (ms / 1e3) / 1e9
+    from_variant = "tcgen05" if (args.variant == ldn.LDN_VARIANT_TENSOR or
+                                 (args.variant == ldn.LDN_VARIANT_AUTO and w.dtype == "bf16" and
+                                  _tc_enabled(ldn))) else "simt"
+    src = ["chunk_tc.cu"] if from_variant == "tcgen05" else ["chunk_simt.cu"]
+    kernel_key = f"chunk_{from_variant}:{args.workload}"
+    src_hash = kernel_source_hash(src)
+    traffic = recorded_traffic(kernel_key, src_hash)
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+                "algorithmic_bytes_per_launch": nbytes, "kernel": f"chunk_{from_variant}",
+                "tensor": {"achieved_tflops": flops / (ms / 1e3) / 1e12, "peak_tflops": bf16_peak,
+                           "frac": flops / (ms / 1e3) / 1e12 / bf16_peak, "algorithmic_flops_per_launch": flops},
+                "roofline_time_us": 1e6 * max(nbytes / (hbm_peak * 1e9), flops / (bf16_peak * 1e12)),
+                "frac_of_roofline_time": 1e6 * max(nbytes / (hbm_peak * 1e9), flops / (bf16_peak * 1e12)) / (ms * 1e3)}
+
+    # ---------------- end to end through the public API, host buffers ----------------
+    e2e = None
+    if not args.no_e2e:
+        host = {k_: (None if v_ is None else v_.cpu().pin_memory()) for k_, v_ in t.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        sf_h = torch.empty(S_final.shape, dtype=S_final.dtype).pin_memory()
+        h2d = sum(v_.numel() * v_.element_size() for v_ in host.values() if v_ is not None)
+        d2h = out.numel() * out.element_size() + S_final.numel() * 4
+
+        def e2e_step():
+            for k_, v_ in host.items():
+                if v_ is not None:
+                    t[k_].copy_(v_, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            sf_h.copy_(S_final, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier()
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for e0, e1 in ee:
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+        barrier()
+        launches += args.steps
+        ems = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in ee))
+        e2e = {"value": world * tokens / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+        del host, out_h, sf_h
+
+    # ---------------- decode step (bandwidth) ----------------
+    decode = None
+    if not args.no_decode:
+        decode = {}
+        del t, out, S_final
+        for name in DECODE_WORKLOADS:
+            d = wl.make_decode(name, seed=rank)
+            td = d.torch_inputs("cuda")
+            S = td["S0"].clone()
+            o = torch.empty((d.B, d.H, d.dv), dtype=torch.float32, device="cuda")
+            steps = d.T
+            ptr = [(td["q"][i].data_ptr(), td["k"][i].data_ptr(), td["v"][i].data_ptr(), td["beta"][i].data_ptr(),
+                    td["gate"][i].data_ptr()) for i in range(steps)]
+
+            def dstep(i):
+                qp, kp, vp, bp, gp = ptr[i]
+                st = ldn.ldn_decode_step(qp, kp, vp, bp, gp, S.data_ptr(), o.data_ptr(), d.B, d.H, d.dk, d.dv,
+                                         d.mode, ldn.LDN_F32, sh)
+                if st != ldn.LDN_OK:
+                    raise ldn.LdnError(st, "ldn_decode_step")
+
+            for i in range(5):
+                dstep(i)
+            S.copy_(td["S0"])
+            barrier()
+            cold = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for i, (e0, e1) in enumerate(cold):
+                flush.zero_()
+                e0.record(stream)
+                dstep(i)
+                e1.record(stream)
+            barrier()
+            cold_ms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in cold))
+            S.copy_(td["S0"])
+            barrier()
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0.record(stream)
+            for i in range(steps):
+                dstep(i)
+            w1.record(stream)
+            barrier()
+            warm_ms = max_over_ranks(w0.elapsed_time(w1) / steps)
+            launches += 2 * steps
+            if ldn.device_status() != ldn.LDN_OK:
+                raise RuntimeError("decode: device status not ok")
+            db = decode_bytes(d.B, d.H, d.dk, d.dv, d.mode)
+            decode[name] = {"steps": steps, "bytes_per_step": db,
+                            "cold_l2": {"us_per_step": cold_ms * 1e3, "GB/s": db / (cold_ms / 1e3) / 1e9,
+                                        "frac_hbm": db / (cold_ms / 1e3) / 1e9 / hbm_peak},
+                            "warm_back_to_back": {"us_per_step": warm_ms * 1e3, "GB/s": db / (warm_ms / 1e3) / 1e9},
+                            "tokens_per_s": world * d.B / (cold_ms / 1e3)}
+            del td, S, o, ptr
+
+    line = {"impl": "ours", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded numpy recipe: L2-normalised Gaussian q,k; Gaussian v; sigmoid beta; "
+                    "-0.1*softplus log-decay); no dataset",
+            "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": 64, "mode": "gdn", "kernel": f"chunk_{from_variant}",
+                       "l2": "flushed before every timed launch (512 MiB device write)",
+                       "parallelism": f"replica x{world} (independent sequences per GPU)"},
+            "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
+            "wall_s_timed_region": wall, "decode": decode}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _tc_enabled(ldn):
+    """Whether the library's automatic choice for bf16 GDN is the tensor-core kernel."""
+    return ldn.ldn_chunk_fwd_select(128, 128, 64, ldn.LDN_GDN, ldn.LDN_BF16) == ldn.LDN_VARIANT_TENSOR
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 SIMT fp32, 2 tcgen05")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

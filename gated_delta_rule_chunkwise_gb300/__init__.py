@@ -1,0 +1,14 @@
+"""GB300 (sm_103a) chunkwise delta-rule linear attention: DeltaNet, Gated
+DeltaNet and KDA forward, plus the single-token recurrent decode step.
+
+The computation lives in CUDA kernels behind the C ABI of include/ldn.h
+(lib/libldn.so, built by ``build.build()``); this package holds the ctypes
+binding (``_native``) and the seeded synthetic workloads (``workloads``).
+"""
+from ._native import (  # noqa: F401
+    EXPORTS, LDN_BF16, LDN_DELTANET, LDN_ERR_CUDA, LDN_ERR_INVALID_ARG, LDN_ERR_TIMEOUT,
+    LDN_ERR_UNSUPPORTED, LDN_F32, LDN_GDN, LDN_KDA, LDN_OK, LDN_VARIANT_AUTO, LDN_VARIANT_SIMT,
+    LDN_VARIANT_TENSOR, LIB_PATH, MODES, LdnError, chunk_fwd, decode_step, device_status,
+    ldn_chunk_fwd, ldn_chunk_fwd_select, ldn_chunk_fwd_variant, ldn_decode_step, ldn_get_device_status,
+    ldn_status_string, ldn_version, load,
+)

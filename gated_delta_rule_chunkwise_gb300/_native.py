@@ -1,0 +1,201 @@
+"""Thin ctypes binding of libldn (include/ldn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of lib/libldn.so.  There is no CPU fallback: if the library has not
+been built, or no GPU is present, the calls raise.
+
+Two layers:
+  * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_decode_step``,
+    ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
+    entry points under the same names, taking raw integer pointers;
+  * ``chunk_fwd`` and ``decode_step``: the same calls on torch CUDA tensors,
+    with shape / dtype checks and output allocation (torch is used for device
+    memory and the current stream only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libldn.so")
+
+LDN_DELTANET, LDN_GDN, LDN_KDA = 0, 1, 2
+LDN_F32, LDN_BF16 = 0, 1
+LDN_OK, LDN_ERR_INVALID_ARG, LDN_ERR_UNSUPPORTED, LDN_ERR_CUDA, LDN_ERR_TIMEOUT = 0, 1, 2, 3, 4
+LDN_VARIANT_AUTO, LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR = 0, 1, 2
+
+MODES = {"deltanet": LDN_DELTANET, "gdn": LDN_GDN, "kda": LDN_KDA}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LdnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({ldn_status_string(status)})" if what else
+                         f"status {status} ({ldn_status_string(status)})")
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGNATURES = {
+    "ldn_chunk_fwd": ([_P] * 8 + [_I] * 8 + [_P], _I),
+    "ldn_chunk_fwd_variant": ([_P] * 8 + [_I] * 9 + [_P], _I),
+    "ldn_chunk_fwd_select": ([_I] * 5, _I),
+    "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
+    "ldn_get_device_status": ([_P], _I),
+    "ldn_status_string": ([_I], ctypes.c_char_p),
+    "ldn_version": ([], _I),
+}
+EXPORTS = tuple(_SIGNATURES)
+
+
+def load(path: str | None = None):
+    """Load libldn.so (raises if it is missing: build it first)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libldn.so not found at {p}; run __graft_entry__.build() "
+                                   "(or gated_delta_rule_chunkwise_gb300.build.build()) first")
+            lib = ctypes.CDLL(p)
+            for name, (args, res) in _SIGNATURES.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+# --- C entry points under their own names ---------------------------------
+def ldn_chunk_fwd(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, stream):
+    return load().ldn_chunk_fwd(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk,
+                                mode, dtype, stream)
+
+
+def ldn_chunk_fwd_variant(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode,
+                          dtype, variant, stream):
+    return load().ldn_chunk_fwd_variant(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv,
+                                        chunk, mode, dtype, variant, stream)
+
+
+def ldn_chunk_fwd_select(dk, dv, chunk, mode, dtype):
+    return load().ldn_chunk_fwd_select(dk, dv, chunk, mode, dtype)
+
+
+def ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream):
+    return load().ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream)
+
+
+def ldn_get_device_status(stream):
+    return load().ldn_get_device_status(stream)
+
+
+def ldn_status_string(status: int) -> str:
+    try:
+        return load().ldn_status_string(int(status)).decode()
+    except RuntimeError:
+        return "libldn not loaded"
+
+
+def ldn_version() -> int:
+    return load().ldn_version()
+
+
+# --- torch-tensor convenience layer ---------------------------------------
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return LDN_F32
+    if t.dtype == torch.bfloat16:
+        return LDN_BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _check(t, name, shape=None, dtype=None):
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def chunk_fwd(q, k, v, beta, gate=None, S0=None, *, mode, chunk=64, out=None, S_final=None,
+              want_state=True, variant=LDN_VARIANT_AUTO, stream=None):
+    """Chunkwise forward on torch CUDA tensors (see ldn_chunk_fwd in include/ldn.h).
+
+    q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16, same dtype);
+    beta [B,T,H] float32; gate [B,T,H] (gdn) or [B,T,H,dk] (kda) float32;
+    S0 [B,H,dk,dv] float32 or None.  Returns (out, S_final or None)."""
+    import torch
+    mode = MODES.get(mode, mode)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q"); _check(k, "k", q.shape, q.dtype); _check(v, "v", (B, T, H, dv), q.dtype)
+    _check(beta, "beta", (B, T, H), torch.float32)
+    if mode == LDN_DELTANET:
+        gate = None
+    else:
+        _check(gate, "gate", (B, T, H) if mode == LDN_GDN else (B, T, H, dk), torch.float32)
+    _check(S0, "S0", (B, H, dk, dv), torch.float32)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", (B, T, H, dv), q.dtype)
+    if S_final is None and want_state:
+        S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check(S_final, "S_final", (B, H, dk, dv), torch.float32)
+    st = ldn_chunk_fwd_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S0),
+                               _ptr(out), _ptr(S_final), B, T, H, dk, dv, chunk, mode,
+                               _dtype_code(q), variant, _stream_handle(stream))
+    if st != LDN_OK:
+        raise LdnError(st, "ldn_chunk_fwd")
+    return out, S_final
+
+
+def decode_step(q, k, v, beta, gate, S, *, mode, out=None, stream=None):
+    """One recurrent step on torch CUDA tensors; S [B,H,dk,dv] float32 is updated
+    in place.  q, k [B,H,dk], v [B,H,dv]; beta [B,H]; gate [B,H] / [B,H,dk]."""
+    import torch
+    mode = MODES.get(mode, mode)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q"); _check(k, "k", q.shape, q.dtype); _check(v, "v", (B, H, dv), q.dtype)
+    _check(beta, "beta", (B, H), torch.float32)
+    if mode == LDN_DELTANET:
+        gate = None
+    else:
+        _check(gate, "gate", (B, H) if mode == LDN_GDN else (B, H, dk), torch.float32)
+    _check(S, "S", (B, H, dk, dv), torch.float32)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", (B, H, dv), q.dtype)
+    st = ldn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S), _ptr(out),
+                         B, H, dk, dv, mode, _dtype_code(q), _stream_handle(stream))
+    if st != LDN_OK:
+        raise LdnError(st, "ldn_decode_step")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and read/clear the device status word."""
+    return ldn_get_device_status(_stream_handle(stream))

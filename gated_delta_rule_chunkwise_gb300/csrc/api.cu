@@ -1,0 +1,152 @@
+// C ABI of libldn: argument validation, kernel-family dispatch, status word.
+// The operations and their sources are documented in include/ldn.h.
+#include "ldn_internal.cuh"
+
+namespace ldn {
+__device__ int g_status = 0;
+
+__global__ void copy_state_kernel(const float *__restrict__ S0, float *__restrict__ S_final, long long n)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        S_final[i] = S0 ? S0[i] : 0.0f;
+}
+
+cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cudaStream_t stream)
+{
+    if (n == 0) return cudaSuccess;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    copy_state_kernel<<<(unsigned)blocks, 256, 0, stream>>>(S0, S_final, n);
+    return cudaGetLastError();
+}
+}  // namespace ldn
+
+using namespace ldn;
+
+// Address of g_status on the current device, resolved once per device.
+static int *status_word()
+{
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        addr[dev] = (int *)p;
+    }
+    return addr[dev];
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static bool supported_dim(int d) { return d == 64 || d == 128; }
+
+static int validate_common(int mode, int dtype, int dk, int dv)
+{
+    if (mode < LDN_DELTANET || mode > LDN_KDA) return LDN_ERR_INVALID_ARG;
+    if (dtype != LDN_F32 && dtype != LDN_BF16) return LDN_ERR_INVALID_ARG;
+    if (dk < 1 || dv < 1) return LDN_ERR_INVALID_ARG;
+    if (!supported_dim(dk) || !supported_dim(dv)) return LDN_ERR_UNSUPPORTED;
+    return LDN_OK;
+}
+
+extern "C" int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v, const float *beta,
+                                     const float *gate, const float *S0, void *out, float *S_final,
+                                     int B, int T, int H, int dk, int dv, int chunk, int mode,
+                                     int dtype, int variant, void *stream)
+{
+    int st = validate_common(mode, dtype, dk, dv);
+    if (st != LDN_OK) return st;
+    if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
+    if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_TENSOR) return LDN_ERR_INVALID_ARG;
+    if (chunk != 64) return LDN_ERR_UNSUPPORTED;
+    // Sizes: token-head count and state element count must stay well inside int64
+    // and the grid limits.
+    const long long units = (long long)B * H;
+    if (units > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
+    if ((long long)B * T * H * (dk > dv ? dk : dv) > (1LL << 40)) return LDN_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        if (S0 && !aligned16(S0)) return LDN_ERR_INVALID_ARG;
+        if (S_final && !aligned16(S_final)) return LDN_ERR_INVALID_ARG;
+        if (!S_final) return LDN_OK;
+        return launch_copy_state(S0, S_final, units * dk * dv, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+    }
+    if (!q || !k || !v || !beta || !out) return LDN_ERR_INVALID_ARG;
+    if (mode != LDN_DELTANET && !gate) return LDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, gate, S0, out, S_final};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return LDN_ERR_INVALID_ARG;
+
+    ChunkArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S0, out, S_final,
+                B, T, H, dk, dv, chunk, mode, dtype, nullptr};
+    if (variant == LDN_VARIANT_AUTO)
+        variant = (dtype == LDN_BF16 && chunk_tc_supported(a)) ? LDN_VARIANT_TENSOR : LDN_VARIANT_SIMT;
+    if (variant == LDN_VARIANT_TENSOR && !chunk_tc_supported(a)) return LDN_ERR_UNSUPPORTED;
+    a.status = status_word();
+    if (!a.status) return LDN_ERR_CUDA;
+    const cudaError_t err = variant == LDN_VARIANT_TENSOR ? launch_chunk_tc(a, s) : launch_chunk_simt(a, s);
+    return err == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
+extern "C" int ldn_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
+                             const float *gate, const float *S0, void *out, float *S_final,
+                             int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                             void *stream)
+{
+    return ldn_chunk_fwd_variant(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk,
+                                 mode, dtype, LDN_VARIANT_AUTO, stream);
+}
+
+extern "C" int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype)
+{
+    const int st = validate_common(mode, dtype, dk, dv);
+    if (st != LDN_OK) return -st;
+    if (chunk != 64) return -LDN_ERR_UNSUPPORTED;
+    ChunkArgs a{};
+    a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = 1; a.T = 1; a.H = 1;
+    return (dtype == LDN_BF16 && chunk_tc_supported(a)) ? LDN_VARIANT_TENSOR : LDN_VARIANT_SIMT;
+}
+
+extern "C" int ldn_decode_step(const void *q, const void *k, const void *v, const float *beta,
+                               const float *gate, float *S, void *out,
+                               int B, int H, int dk, int dv, int mode, int dtype, void *stream)
+{
+    int st = validate_common(mode, dtype, dk, dv);
+    if (st != LDN_OK) return st;
+    if (B < 1 || H < 1) return LDN_ERR_INVALID_ARG;
+    if ((long long)B * H > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !beta || !S || !out) return LDN_ERR_INVALID_ARG;
+    if (mode != LDN_DELTANET && !gate) return LDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, gate, S, out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return LDN_ERR_INVALID_ARG;
+    int *sw = status_word();
+    if (!sw) return LDN_ERR_CUDA;
+    DecodeArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S, out, B, H, dk, dv, mode, dtype, sw};
+    return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
+extern "C" int ldn_get_device_status(void *stream)
+{
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LDN_ERR_CUDA;
+    int h = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&h, g_status, sizeof(int)) != cudaSuccess) return LDN_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return LDN_ERR_CUDA;
+    if (h & (1 << LDN_ERR_TIMEOUT)) return LDN_ERR_TIMEOUT;
+    return h ? LDN_ERR_CUDA : LDN_OK;
+}
+
+extern "C" const char *ldn_status_string(int status)
+{
+    switch (status) {
+    case LDN_OK: return "ok";
+    case LDN_ERR_INVALID_ARG: return "invalid argument (NULL or misaligned pointer, bad enum or size)";
+    case LDN_ERR_UNSUPPORTED: return "unsupported configuration (dk/dv not in {64,128}, chunk != 64, or variant)";
+    case LDN_ERR_CUDA: return "CUDA runtime or launch error";
+    case LDN_ERR_TIMEOUT: return "a kernel abandoned a bounded wait; outputs are incomplete";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int ldn_version(void) { return LDN_VERSION; }

@@ -1,0 +1,138 @@
+// Single-token recurrent decode step, fp32 state streamed once through HBM.
+//
+// For one token per (b, h) the step is, in memory orientation H = S^T
+// ([dk][dv], fp32):
+//   H' = alpha H (Gated DeltaNet) | Diag(a) H (KDA) | H (DeltaNet)
+//   p  = H'^T k,  s = H'^T q                      (one pass over H')
+//   r  = beta (v - p),  o = s + r (k . q)         (prediction-correction form,
+//                                                   Residual Linear Attention
+//                                                   notes, Sec. 1.2)
+//   H  <- H' + k r^T                              (in place)
+// Decay before the error follows the linear-attention notes, Sec. 2.4 Eqs.
+// 15-17; the KDA decay acts on the key rows of H (Sec. 2.5, Eqs. 18-20).
+//
+// Work split: one CTA per (b, h, 64-column slice of dv).  Columns are
+// independent (each value channel is its own linear system, state-reduction
+// notes Sec. 2.5), so slices need no communication.  128 threads: 16 threads
+// cover one 256-byte row of the slice with float4 loads, 8 row groups stride
+// over dk, and each thread keeps its dk/8 float4 of H' in registers between
+// the read pass and the write pass, so H is read once and written once.
+#include "ldn_internal.cuh"
+
+namespace ldn {
+namespace {
+
+constexpr int kDecThreads = 128;
+constexpr int kDecCols = 64;                   // dv columns per CTA
+constexpr int kTPR = kDecCols / 4;             // threads per row (float4 each)
+constexpr int kRowsPerPass = kDecThreads / kTPR;
+
+template <int DK, typename TIn, int MODE>
+__global__ void __launch_bounds__(kDecThreads)
+decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
+              const float *__restrict__ beta, const float *__restrict__ gate,
+              float *__restrict__ S, TIn *__restrict__ out, int dv)
+{
+    constexpr int RPT = DK / kRowsPerPass;     // rows held per thread
+    __shared__ float qs[DK], ks[DK], as[DK];
+    __shared__ __align__(16) float red_p[kRowsPerPass][kDecCols];
+    __shared__ __align__(16) float red_s[kRowsPerPass][kDecCols];
+    __shared__ __align__(16) float rs[kDecCols];
+    __shared__ float kq_part[kDecThreads / 32];
+
+    const int slices = dv / kDecCols;
+    const int unit = blockIdx.x / slices;      // (b, h) pair, b * H + h
+    const int col0 = (blockIdx.x % slices) * kDecCols;
+    const int tid = threadIdx.x;
+
+    float kq = 0.0f;
+    if (tid < DK) {
+        const float qv = load_in(q, (size_t)unit * DK + tid);
+        const float kv = load_in(k, (size_t)unit * DK + tid);
+        qs[tid] = qv;
+        ks[tid] = kv;
+        if (MODE == LDN_KDA) as[tid] = expf(gate[(size_t)unit * DK + tid]);
+        kq = qv * kv;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+    if ((tid & 31) == 0) kq_part[tid >> 5] = kq;
+    const float alpha = (MODE == LDN_GDN) ? expf(gate[unit]) : 1.0f;
+    __syncthreads();
+
+    const int cg = tid % kTPR;                 // float4 column group
+    const int rg = tid / kTPR;                 // first row of this thread
+    float *Sbase = S + (size_t)unit * DK * dv + col0 + 4 * cg;
+
+    float4 h[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+        h[i] = *reinterpret_cast<const float4 *>(Sbase + (size_t)(rg + i * kRowsPerPass) * dv);
+
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), s = p;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        const int row = rg + i * kRowsPerPass;
+        const float d = (MODE == LDN_KDA) ? as[row] : alpha;
+        if (MODE != LDN_DELTANET) { h[i].x *= d; h[i].y *= d; h[i].z *= d; h[i].w *= d; }
+        const float kr = ks[row], qr = qs[row];
+        p.x += h[i].x * kr; p.y += h[i].y * kr; p.z += h[i].z * kr; p.w += h[i].w * kr;
+        s.x += h[i].x * qr; s.y += h[i].y * qr; s.z += h[i].z * qr; s.w += h[i].w * qr;
+    }
+    *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = p;
+    *reinterpret_cast<float4 *>(&red_s[rg][4 * cg]) = s;
+    __syncthreads();
+
+    if (tid < kDecCols) {
+        float pp = 0.f, ss = 0.f, kqt = 0.f;
+#pragma unroll
+        for (int g = 0; g < kRowsPerPass; ++g) { pp += red_p[g][tid]; ss += red_s[g][tid]; }
+#pragma unroll
+        for (int w = 0; w < kDecThreads / 32; ++w) kqt += kq_part[w];
+        const size_t vi = (size_t)unit * dv + col0 + tid;
+        const float r = beta[unit] * (load_in(v, vi) - pp);
+        rs[tid] = r;
+        store_out(out, vi, ss + r * kqt);
+    }
+    __syncthreads();
+
+    const float4 r4 = *reinterpret_cast<const float4 *>(&rs[4 * cg]);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        const float kr = ks[rg + i * kRowsPerPass];
+        float4 o = h[i];
+        o.x += kr * r4.x; o.y += kr * r4.y; o.z += kr * r4.z; o.w += kr * r4.w;
+        *reinterpret_cast<float4 *>(Sbase + (size_t)(rg + i * kRowsPerPass) * dv) = o;
+    }
+}
+
+template <int DK, typename TIn>
+cudaError_t launch_dk(const DecodeArgs &a, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDecCols));
+    const TIn *q = (const TIn *)a.q, *k = (const TIn *)a.k, *v = (const TIn *)a.v;
+    TIn *o = (TIn *)a.out;
+    switch (a.mode) {
+    case LDN_DELTANET:
+        decode_kernel<DK, TIn, LDN_DELTANET><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        break;
+    case LDN_GDN:
+        decode_kernel<DK, TIn, LDN_GDN><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        break;
+    default:
+        decode_kernel<DK, TIn, LDN_KDA><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st)
+{
+    if (a.dtype == LDN_BF16)
+        return a.dk == 128 ? launch_dk<128, __nv_bfloat16>(a, st) : launch_dk<64, __nv_bfloat16>(a, st);
+    return a.dk == 128 ? launch_dk<128, float>(a, st) : launch_dk<64, float>(a, st);
+}
+
+}  // namespace ldn

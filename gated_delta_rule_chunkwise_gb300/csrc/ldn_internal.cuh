@@ -1,0 +1,47 @@
+// Internal declarations shared by the CUDA translation units of libldn.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/ldn.h"
+
+namespace ldn {
+
+// Device status word: kernels atomically OR (1 << LDN_ERR_*) into it when they
+// abandon a bounded wait.  It is a __device__ variable of api.cu (no
+// allocation); api.cu resolves its address per device and hands it to the
+// launchers, and ldn_get_device_status() reads and clears it.
+struct ChunkArgs {
+    const void *q, *k, *v;
+    const float *beta, *gate, *S0;
+    void *out;
+    float *S_final;
+    int B, T, H, dk, dv, chunk, mode, dtype;
+    int *status;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *beta, *gate;
+    float *S;
+    void *out;
+    int B, H, dk, dv, mode, dtype;
+    int *status;
+};
+
+// Launchers: return cudaSuccess or the launch error.  Arguments are validated
+// by the caller (api.cu).
+cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
+bool chunk_tc_supported(const ChunkArgs &a);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cudaStream_t stream);
+
+// Loads of q/k/v in either element type, widened to fp32.
+__device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void store_out(float *p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+
+}  // namespace ldn

@@ -1,0 +1,136 @@
+"""Seeded synthetic inputs for the delta-rule kernels and the oracle.
+
+This module holds input generation only (none of the method's arithmetic):
+both the CUDA path and the fp64 oracle consume the same arrays from here.
+
+Recipe (every named workload):
+  * numpy ``Generator(PCG64(seed))``, seed 0 unless given; draws in this order:
+    q, k, v, beta-logits, gate noise, per-head gate bias b_h (KDA), S0;
+  * q, k ~ N(0, 1) then L2-normalised over d_k per (b, t, h) in fp32 (the
+    method sources normalise q and k per head); v ~ N(0, 1);
+  * beta = sigmoid(N(0, 1)) per (b, t, h);
+  * Gated DeltaNet log-decay g = -softplus(N(0, 1)) * 0.1 per (b, t, h);
+    KDA log-decay g = -softplus(N(0, 1) + b_h) * 0.1 per (b, t, h, c) with one
+    b_h ~ N(0, 0.5^2) per head (0.5 read as the standard deviation);
+  * S0 ~ N(0, 0.02^2) where the workload has a nonzero initial state, else none;
+  * for bf16 workloads q, k, v are rounded to bf16 (round to nearest even)
+    AFTER normalisation; beta, gates and states stay fp32.
+Arrays are returned as float32 numpy arrays holding exactly the values the
+kernels see (bf16 values are exact in fp32).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+MODE_DELTANET, MODE_GDN, MODE_KDA = 0, 1, 2
+
+# name -> recipe.  Sizes are the benchmark workloads; tests shrink them with overrides.
+CHUNK_WORKLOADS = {
+    "deltanet_fp32_b1_t256_h1_d64": dict(mode=MODE_DELTANET, dtype="f32", B=1, T=256, H=1, dk=64, dv=64, s0=False),
+    "gdn_bf16_b4_t2048_h16_d128": dict(mode=MODE_GDN, dtype="bf16", B=4, T=2048, H=16, dk=128, dv=128, s0=False),
+    "kda_bf16_b8_t4096_h16_d128": dict(mode=MODE_KDA, dtype="bf16", B=8, T=4096, H=16, dk=128, dv=128, s0=False),
+    "gdn_bf16_long_b1_t8192_h16_d128": dict(mode=MODE_GDN, dtype="bf16", B=1, T=8192, H=16, dk=128, dv=128, s0=True),
+    "gdn_bf16_long_b1_t32768_h16_d128": dict(mode=MODE_GDN, dtype="bf16", B=1, T=32768, H=16, dk=128, dv=128, s0=True),
+    "gdn_bf16_long_b1_t65536_h16_d128": dict(mode=MODE_GDN, dtype="bf16", B=1, T=65536, H=16, dk=128, dv=128, s0=True),
+}
+DECODE_WORKLOADS = {
+    "gdn_decode_b64_h16_dk128_dv128_steps1000": dict(mode=MODE_GDN, dtype="f32", B=64, H=16, dk=128, dv=128, steps=1000),
+    "gdn_decode_b64_h16_dk64_dv128_steps1000": dict(mode=MODE_GDN, dtype="f32", B=64, H=16, dk=64, dv=128, steps=1000),
+}
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 -> nearest bf16 (ties to even), returned as fp32 values (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def _l2norm(x: np.ndarray) -> np.ndarray:
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True, dtype=np.float32))
+    return (x / n).astype(np.float32)
+
+
+def _softplus(x: np.ndarray) -> np.ndarray:
+    return np.logaddexp(np.float32(0), x).astype(np.float32)
+
+
+def _sigmoid(x: np.ndarray) -> np.ndarray:
+    return (1.0 / (1.0 + np.exp(-x))).astype(np.float32)
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    mode: int
+    dtype: str              # "f32" or "bf16": element type of q, k, v, out
+    B: int
+    T: int                  # tokens per sequence (decode: number of steps)
+    H: int
+    dk: int
+    dv: int
+    q: np.ndarray           # chunk: [B,T,H,dk]   decode: [steps,B,H,dk]
+    k: np.ndarray
+    v: np.ndarray
+    beta: np.ndarray
+    gate: Optional[np.ndarray]
+    S0: Optional[np.ndarray]  # [B,H,dk,dv]
+    chunk: int = 64
+    decode: bool = False
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.T
+
+    def torch_inputs(self, device="cuda"):
+        """The inputs as torch tensors on `device` in the kernel dtypes."""
+        import torch
+        el = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        cv = lambda a, dt: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dt)
+        return dict(q=cv(self.q, el), k=cv(self.k, el), v=cv(self.v, el), beta=cv(self.beta, torch.float32),
+                    gate=cv(self.gate, torch.float32), S0=cv(self.S0, torch.float32))
+
+
+def _draw(rng, lead, mode, dtype, H, dk, dv, s0, B):
+    """Draws in the documented order; `lead` is the leading shape ([B,T] or [steps,B])."""
+    f32 = np.float32
+    q = _l2norm(rng.standard_normal((*lead, H, dk), dtype=f32))
+    k = _l2norm(rng.standard_normal((*lead, H, dk), dtype=f32))
+    v = rng.standard_normal((*lead, H, dv), dtype=f32)
+    beta = _sigmoid(rng.standard_normal((*lead, H), dtype=f32))
+    gate = None
+    if mode == MODE_GDN:
+        gate = (-_softplus(rng.standard_normal((*lead, H), dtype=f32)) * f32(0.1)).astype(f32)
+    elif mode == MODE_KDA:
+        noise = rng.standard_normal((*lead, H, dk), dtype=f32)
+        b_h = (rng.standard_normal(H, dtype=f32) * f32(0.5)).astype(f32)
+        gate = (-_softplus(noise + b_h[:, None]) * f32(0.1)).astype(f32)
+    S0 = (rng.standard_normal((B, H, dk, dv), dtype=f32) * f32(0.02)).astype(f32) if s0 else None
+    if dtype == "bf16":
+        q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)
+    return q, k, v, beta, gate, S0
+
+
+def make_chunk(name: str = "gdn_bf16_b4_t2048_h16_d128", seed: int = 0, **over) -> Workload:
+    """A chunkwise-forward workload; keyword overrides (B, T, H, dk, dv, mode,
+    dtype, s0) shrink or vary it while keeping the recipe."""
+    r = dict(CHUNK_WORKLOADS[name]); r.update(over)
+    rng = np.random.default_rng(seed)
+    q, k, v, beta, gate, S0 = _draw(rng, (r["B"], r["T"]), r["mode"], r["dtype"], r["H"], r["dk"],
+                                    r["dv"], r["s0"], r["B"])
+    return Workload(name=name, mode=r["mode"], dtype=r["dtype"], B=r["B"], T=r["T"], H=r["H"],
+                    dk=r["dk"], dv=r["dv"], q=q, k=k, v=v, beta=beta, gate=gate, S0=S0)
+
+
+def make_decode(name: str = "gdn_decode_b64_h16_dk128_dv128_steps1000", seed: int = 0, **over) -> Workload:
+    """A decode workload: `steps` consecutive tokens per sequence, drawn as
+    [steps, B, H, .] in one go, from a random S0 ~ N(0, 0.02^2)."""
+    r = dict(DECODE_WORKLOADS[name]); r.update(over)
+    rng = np.random.default_rng(seed)
+    q, k, v, beta, gate, S0 = _draw(rng, (r["steps"], r["B"]), r["mode"], r["dtype"], r["H"], r["dk"],
+                                    r["dv"], True, r["B"])
+    return Workload(name=name, mode=r["mode"], dtype=r["dtype"], B=r["B"], T=r["steps"], H=r["H"],
+                    dk=r["dk"], dv=r["dv"], q=q, k=k, v=v, beta=beta, gate=gate, S0=S0, decode=True)

@@ -1,0 +1,139 @@
+/*
+ * ldn.h -- C ABI of the GB300 (sm_103a) delta-rule linear-attention library.
+ *
+ * Operations (math orientation: the memory S is d_v x d_k, column vectors):
+ *
+ *   DeltaNet   S_t = S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   Gated DN   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   KDA        S_t = S_{t-1} Diag(a_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   output     o_t = S_t q_t            (the query reads the UPDATED memory)
+ *
+ * as defined in "Linear Attention Architectures: Mechanisms, Trade-offs, and
+ * Cross-Layer Routing" (reading notes), Sec. 2.1 Eq. 8, Sec. 2.3 Eqs. 9-10/14,
+ * Sec. 2.4 Eqs. 15-17 (decay before the error), Sec. 2.5 Eqs. 18-20 (Diag(a)
+ * on the key side), and in "State reduction by key/query channel pruning"
+ * (reading notes), Sec. 2.1 Eqs. 1-2.  The decode step is the same rule for one
+ * token, written in the prediction-correction form of the Residual Linear
+ * Attention notes, Sec. 1.2.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers q, k, v, beta, gate, S0, S, out, S_final are DEVICE pointers,
+ *     contiguous, row-major, 16-byte aligned.  The caller owns every buffer;
+ *     the library allocates no device memory per call.
+ *   - Gates are natural-log decays: alpha_t = exp(gate), a_t = exp(gate[c]).
+ *     A positive log-gate is accepted (it is not clamped); beta is not clamped.
+ *   - q is not scaled and q, k are not normalised by the library (scale = 1).
+ *   - The state is stored in memory orientation H = S^T, fp32, [B][H][dk][dv]
+ *     ("K x V"), i.e. element (c, i) of head (b, h) is S[i][c].
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous.  Argument errors are detected and returned
+ *     synchronously before anything is enqueued.  A launch failure returns
+ *     LDN_ERR_CUDA.  Device-side faults that a kernel detects itself (a wait
+ *     that ran out of its iteration limit) are recorded in a device status
+ *     word and read with ldn_get_device_status().
+ *   - Not thread-safe across concurrent calls that share an output buffer;
+ *     otherwise re-entrant.
+ */
+#ifndef LDN_H
+#define LDN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LDN_VERSION 1
+
+typedef enum { LDN_DELTANET = 0, LDN_GDN = 1, LDN_KDA = 2 } ldn_mode;
+
+/* Element type of q, k, v and out.  beta, gate and every state are fp32. */
+typedef enum { LDN_F32 = 0, LDN_BF16 = 1 } ldn_dtype;
+
+typedef enum {
+    LDN_OK = 0,
+    LDN_ERR_INVALID_ARG = 1, /* NULL / misaligned pointer, bad enum, negative size */
+    LDN_ERR_UNSUPPORTED = 2, /* valid but not implemented: dk/dv, chunk, variant  */
+    LDN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed              */
+    LDN_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (device word)  */
+} ldn_status;
+
+/* Kernel family for ldn_chunk_fwd_variant. */
+typedef enum {
+    LDN_VARIANT_AUTO = 0,   /* bf16 -> tensor-core kernel, fp32 -> fp32 SIMT kernel */
+    LDN_VARIANT_SIMT = 1,   /* fp32 CUDA-core kernel, either dtype                 */
+    LDN_VARIANT_TENSOR = 2  /* tcgen05 / TMEM kernel, bf16 only                     */
+} ldn_variant;
+
+/*
+ * ldn_chunk_fwd -- chunkwise-parallel forward over a whole sequence.
+ *
+ * Computes, for every (b, h), the outputs o_t of the recurrence above for
+ * t = 1..T starting from S0, and the final state S_T.  The sequence is cut
+ * into chunks of `chunk` tokens; inside a chunk the recurrence is solved in
+ * closed form (the UT/WY transform: a unit-lower-triangular solve with
+ * (I + strict_tril(Diag(beta) K^ K~^T))), chunk outputs are formed from the
+ * incoming state plus the masked, decay-weighted intra-chunk interactions,
+ * and only the chunk-to-chunk state update is sequential.  The result equals
+ * the token recurrence up to floating-point rounding.
+ *
+ *   q, k     [B][T][H][dk]  dtype        v, out [B][T][H][dv] dtype
+ *   beta     [B][T][H]      fp32
+ *   gate     mode GDN: [B][T][H] fp32; mode KDA: [B][T][H][dk] fp32;
+ *            mode DELTANET: ignored, may be NULL
+ *   S0       [B][H][dk][dv] fp32, or NULL for a zero initial state
+ *   S_final  [B][H][dk][dv] fp32, or NULL to skip writing it
+ *            (S_final may alias S0: every block reads its slice of S0 before
+ *            it writes the same slice of S_final)
+ *   B, H >= 1; T >= 0 (T = 0 only copies S0, or zeros, to S_final);
+ *   dk, dv in {64, 128}; chunk == 64; mode in ldn_mode; dtype in ldn_dtype.
+ * Returns LDN_OK or an error code; out and S_final are written asynchronously.
+ */
+int ldn_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
+                  const float *gate, const float *S0, void *out, float *S_final,
+                  int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                  void *stream);
+
+/* Same as ldn_chunk_fwd with an explicit kernel family (ldn_variant).
+ * LDN_VARIANT_TENSOR with dtype LDN_F32 returns LDN_ERR_UNSUPPORTED. */
+int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v, const float *beta,
+                          const float *gate, const float *S0, void *out, float *S_final,
+                          int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                          int variant, void *stream);
+
+/* Which kernel family LDN_VARIANT_AUTO runs for these sizes: returns
+ * LDN_VARIANT_SIMT or LDN_VARIANT_TENSOR, or -LDN_ERR_* for arguments that
+ * ldn_chunk_fwd would reject.  Pure host function: touches no device. */
+int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype);
+
+/*
+ * ldn_decode_step -- one recurrent step for every (b, h), state updated in place.
+ *
+ * For one token per sequence it forms the decayed state S' = alpha S (GDN),
+ * S Diag(a) (KDA) or S (DeltaNet), the key prediction p = S' k and the query
+ * read s = S' q in one pass over the state, then r = beta (v - p),
+ * o = s + r (k^T q) (the prediction-correction form) and writes
+ * S <- S' + r k^T back.
+ *
+ *   q, k  [B][H][dk] dtype      v, out [B][H][dv] dtype
+ *   beta  [B][H] fp32           gate   GDN [B][H], KDA [B][H][dk] fp32, DN ignored
+ *   S     [B][H][dk][dv] fp32, read and overwritten in place
+ *   B, H >= 1; dk, dv in {64, 128}.
+ */
+int ldn_decode_step(const void *q, const void *k, const void *v, const float *beta,
+                    const float *gate, float *S, void *out,
+                    int B, int H, int dk, int dv, int mode, int dtype, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word on the
+ * current device.  Returns LDN_OK, LDN_ERR_TIMEOUT (a kernel abandoned a
+ * bounded wait and left its outputs incomplete) or LDN_ERR_CUDA. */
+int ldn_get_device_status(void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *ldn_status_string(int status);
+
+/* LDN_VERSION of the loaded library. */
+int ldn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LDN_H */

@@ -1,0 +1,119 @@
+"""CPU-side checks of the C ABI: the library loads without a GPU, exports
+every entry point include/ldn.h declares, and rejects bad arguments
+synchronously (these paths run before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_chunkwise_gb300 as ldn
+from gated_delta_rule_chunkwise_gb300 import build as ldn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ldn_build.build()
+    return ldn.load()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(ldn_\w+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert {"ldn_chunk_fwd", "ldn_decode_step"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(ldn.EXPORTS) == declared
+
+
+def test_version_and_status_strings(lib):
+    assert ldn.ldn_version() == 1
+    for st in range(5):
+        assert isinstance(ldn.ldn_status_string(st), str) and ldn.ldn_status_string(st)
+    assert "unknown" in ldn.ldn_status_string(99)
+
+
+FAKE = 1 << 20          # a 16-byte aligned, never dereferenced address
+
+
+def _chunk(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, gate=FAKE, S0=None, out=FAKE, S_final=None,
+             B=1, T=64, H=1, dk=64, dv=64, chunk=64, mode=1, dtype=1, variant=0, stream=None)
+    a.update(kw)
+    return ldn.ldn_chunk_fwd_variant(a["q"], a["k"], a["v"], a["beta"], a["gate"], a["S0"], a["out"],
+                                     a["S_final"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"],
+                                     a["mode"], a["dtype"], a["variant"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(k=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(v=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(beta=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(out=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None, mode=1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None, mode=2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 4), ldn.LDN_ERR_INVALID_ARG),            # misaligned
+    (dict(S0=FAKE + 8), ldn.LDN_ERR_INVALID_ARG),
+    (dict(mode=3), ldn.LDN_ERR_INVALID_ARG),
+    (dict(mode=-1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dtype=2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(B=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(H=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(T=-1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(variant=3), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dk=96), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(dv=32), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(dk=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(chunk=32), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(variant=2, dtype=0), ldn.LDN_ERR_UNSUPPORTED),    # tensor cores need bf16
+])
+def test_chunk_rejects_bad_arguments(lib, kw, want):
+    assert _chunk(**kw) == want
+
+
+def _decode(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, gate=FAKE, S=FAKE, out=FAKE, B=1, H=1, dk=64, dv=64,
+             mode=1, dtype=0, stream=None)
+    a.update(kw)
+    return ldn.ldn_decode_step(a["q"], a["k"], a["v"], a["beta"], a["gate"], a["S"], a["out"], a["B"],
+                               a["H"], a["dk"], a["dv"], a["mode"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(S=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(S=FAKE + 4), ldn.LDN_ERR_INVALID_ARG),
+    (dict(B=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(mode=7), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dk=32), ldn.LDN_ERR_UNSUPPORTED),
+])
+def test_decode_rejects_bad_arguments(lib, kw, want):
+    assert _decode(**kw) == want
+
+
+def test_binding_without_library_fails_loudly(tmp_path, monkeypatch):
+    import gated_delta_rule_chunkwise_gb300._native as nat
+    monkeypatch.setattr(nat, "_lib", None)
+    with pytest.raises(RuntimeError, match="libldn.so not found"):
+        nat.load(str(tmp_path / "missing.so"))
+
+
+def test_select_reports_kernel_family(lib):
+    assert ldn.ldn_chunk_fwd_select(64, 64, 64, 0, ldn.LDN_F32) == ldn.LDN_VARIANT_SIMT
+    assert ldn.ldn_chunk_fwd_select(128, 128, 64, 1, ldn.LDN_BF16) in (ldn.LDN_VARIANT_SIMT, ldn.LDN_VARIANT_TENSOR)
+    assert ldn.ldn_chunk_fwd_select(96, 128, 64, 1, ldn.LDN_BF16) == -ldn.LDN_ERR_UNSUPPORTED
+    assert ldn.ldn_chunk_fwd_select(128, 128, 32, 1, ldn.LDN_BF16) == -ldn.LDN_ERR_UNSUPPORTED
+    assert ldn.ldn_chunk_fwd_select(128, 128, 64, 5, ldn.LDN_BF16) == -ldn.LDN_ERR_INVALID_ARG

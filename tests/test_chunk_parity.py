@@ -1,0 +1,173 @@
+"""GPU parity of ldn_chunk_fwd against the fp64 oracle, element by element.
+
+Sizes span several 64-token chunks and a ragged tail; each case compares every
+output and the final state with max|gpu - oracle| / RMS(oracle) within 1e-4
+(fp32 inputs) or 2e-2 (bf16 inputs, fp32 state)."""
+import numpy as np
+import pytest
+
+import gated_delta_rule_chunkwise_gb300 as ldn
+from gated_delta_rule_chunkwise_gb300 import workloads as wl
+from tests._helpers import TOL, oracle_chunk, rel_err
+
+pytestmark = pytest.mark.gpu
+
+BASE = {0: "deltanet_fp32_b1_t256_h1_d64", 1: "gdn_bf16_b4_t2048_h16_d128", 2: "kda_bf16_b8_t4096_h16_d128"}
+MODE_NAME = {0: "deltanet", 1: "gdn", 2: "kda"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gated_delta_rule_chunkwise_gb300 import build
+    build.build()
+    ldn.load()
+
+
+def run_gpu(w, variant=ldn.LDN_VARIANT_AUTO, S0=True, want_state=True):
+    import torch
+    t = w.torch_inputs("cuda")
+    out, sf = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"] if S0 else None,
+                            mode=w.mode, variant=variant, want_state=want_state)
+    assert ldn.device_status() == ldn.LDN_OK
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), (None if sf is None else sf.cpu().numpy())
+
+
+def check(w, variant=ldn.LDN_VARIANT_AUTO, tol=None):
+    tol = tol or TOL[w.dtype]
+    o, s = run_gpu(w, variant)
+    ro, rs = oracle_chunk(w)
+    eo, es = rel_err(o, ro), rel_err(s, rs)
+    assert eo <= tol and es <= tol, f"{w.name} {w.dtype} variant={variant}: out {eo:.3g} state {es:.3g} (tol {tol})"
+    return eo, es
+
+
+# ---- every mode x dtype x head size, ragged tails, with and without S0 ----
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_parity_modes_dtypes_dims(mode, dtype, dk, dv):
+    w = wl.make_chunk(BASE[mode], B=2, T=200, H=3, dk=dk, dv=dv, mode=mode, dtype=dtype, s0=True)
+    check(w)
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129, 321])
+@pytest.mark.parametrize("mode", [1, 2])
+def test_parity_lengths(T, mode):
+    w = wl.make_chunk(BASE[mode], B=1, T=T, H=2, s0=(T % 2 == 1))
+    check(w)
+
+
+@pytest.mark.parametrize("variant", [ldn.LDN_VARIANT_SIMT])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_simt_variant_on_bf16(variant, mode):
+    w = wl.make_chunk(BASE[mode], B=2, T=150, H=2, mode=mode, dtype="bf16", s0=True)
+    check(w, variant)
+
+
+def test_config_deltanet_fp32_full():
+    """The fp32 DeltaNet workload at its full size (B=1, T=256, H=1, d=64)."""
+    w = wl.make_chunk("deltanet_fp32_b1_t256_h1_d64")
+    check(w)
+
+
+def test_zero_length_copies_state():
+    import torch
+    w = wl.make_chunk(BASE[1], B=2, T=3, H=2, s0=True)
+    t = w.torch_inputs("cuda")
+    S_final = torch.full_like(t["S0"], 7.0)
+    st = ldn.ldn_chunk_fwd(0, 0, 0, 0, 0, t["S0"].data_ptr(), 0, S_final.data_ptr(), 2, 0, 2, 128, 128,
+                           64, 1, 1, torch.cuda.current_stream().cuda_stream)
+    assert st == ldn.LDN_OK
+    torch.cuda.synchronize()
+    assert torch.equal(S_final, t["S0"])
+    st = ldn.ldn_chunk_fwd(0, 0, 0, 0, 0, 0, 0, S_final.data_ptr(), 2, 0, 2, 128, 128, 64, 1, 1,
+                           torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == ldn.LDN_OK and float(S_final.abs().max()) == 0.0
+
+
+def test_no_state_output_and_null_s0():
+    w = wl.make_chunk(BASE[2], B=1, T=100, H=2, s0=False)
+    o, s = run_gpu(w, want_state=False)
+    assert s is None
+    ro, _ = oracle_chunk(w)
+    assert rel_err(o, ro) <= TOL["bf16"]
+
+
+def test_state_output_may_alias_initial_state():
+    import torch
+    w = wl.make_chunk(BASE[1], B=2, T=130, H=2, s0=True)
+    t = w.torch_inputs("cuda")
+    S = t["S0"].clone()
+    out, sf = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], S, mode=1, S_final=S)
+    torch.cuda.synchronize()
+    ro, rs = oracle_chunk(w)
+    assert rel_err(out.float().cpu().numpy(), ro) <= TOL["bf16"]
+    assert rel_err(S.cpu().numpy(), rs) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_state_passing_split_equals_full(mode):
+    """Resume: S_final of the first part seeds the second part."""
+    import torch
+    w = wl.make_chunk(BASE[mode], B=2, T=300, H=2, s0=True)
+    t = w.torch_inputs("cuda")
+    cut = 130
+    sl = lambda x, a, b: None if x is None else x[:, a:b].contiguous()
+    o1, s1 = ldn.chunk_fwd(sl(t["q"], 0, cut), sl(t["k"], 0, cut), sl(t["v"], 0, cut), sl(t["beta"], 0, cut),
+                           sl(t["gate"], 0, cut), t["S0"], mode=mode)
+    o2, s2 = ldn.chunk_fwd(sl(t["q"], cut, None), sl(t["k"], cut, None), sl(t["v"], cut, None),
+                           sl(t["beta"], cut, None), sl(t["gate"], cut, None), s1, mode=mode)
+    torch.cuda.synchronize()
+    ro, rs = oracle_chunk(w)
+    o = torch.cat([o1, o2], dim=1).float().cpu().numpy()
+    assert rel_err(o, ro) <= TOL["bf16"]
+    assert rel_err(s2.cpu().numpy(), rs) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_degenerate_beta(mode):
+    """beta = 0 (memory only decays) and beta = 1 (exact overwrite along k)."""
+    for bval in (0.0, 1.0):
+        w = wl.make_chunk(BASE[mode], B=1, T=140, H=2, mode=mode, s0=True)
+        w.beta = np.full_like(w.beta, bval)
+        check(w)
+
+
+def test_strong_gdn_gates():
+    """Large per-token decays (log alpha ~ -2): the decayed chunk products stay finite
+    for a scalar gate because only e^{g_r - g_j}, r >= j, is ever needed."""
+    w = wl.make_chunk(BASE[1], B=1, T=200, H=2, s0=True)
+    w.gate = (w.gate * 20).astype(np.float32)
+    check(w)
+
+
+# ---- full-size workloads in the benchmark's launch configuration, sampled ----
+def _sampled(name, picks, **over):
+    import torch
+    w = wl.make_chunk(name, **over)
+    o, s = run_gpu(w)
+    for b, h in picks:
+        sub = wl.Workload(name=w.name, mode=w.mode, dtype=w.dtype, B=1, T=w.T, H=1, dk=w.dk, dv=w.dv,
+                          q=w.q[b:b + 1, :, h:h + 1], k=w.k[b:b + 1, :, h:h + 1], v=w.v[b:b + 1, :, h:h + 1],
+                          beta=w.beta[b:b + 1, :, h:h + 1],
+                          gate=None if w.gate is None else w.gate[b:b + 1, :, h:h + 1],
+                          S0=None if w.S0 is None else w.S0[b:b + 1, h:h + 1])
+        ro, rs = oracle_chunk(sub)
+        eo = rel_err(o[b:b + 1, :, h:h + 1], ro)
+        es = rel_err(s[b:b + 1, h:h + 1], rs)
+        assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], f"{name} (b={b},h={h}): out {eo:.3g} state {es:.3g}"
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
+
+
+def test_full_gdn_bf16_b4_t2048_sampled():
+    _sampled("gdn_bf16_b4_t2048_h16_d128", [(0, 0), (1, 7), (3, 15)])
+
+
+def test_full_kda_bf16_b8_t4096_sampled():
+    _sampled("kda_bf16_b8_t4096_h16_d128", [(0, 3), (7, 12)])
+
+
+def test_full_gdn_long_t65536_sampled():
+    _sampled("gdn_bf16_long_b1_t65536_h16_d128", [(0, 5)])
