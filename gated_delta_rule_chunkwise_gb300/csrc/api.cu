@@ -39,6 +39,7 @@ static int *status_word()
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 static bool supported_dim(int d) { return d == 64 || d == 128; }
 
 static int validate_common(int mode, int dtype, int dk, int dv)
@@ -74,9 +75,12 @@ extern "C" int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v
     }
     if (!q || !k || !v || !beta || !out) return LDN_ERR_INVALID_ARG;
     if (mode != LDN_DELTANET && !gate) return LDN_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, beta, gate, S0, out, S_final};
-    for (const void *p : ptrs)
+    // Tiles of q, k, v, out and the states move in 16-byte vectors (TMA,
+    // float4); beta and gates are read as scalars.
+    const void *vec_ptrs[] = {q, k, v, S0, out, S_final};
+    for (const void *p : vec_ptrs)
         if (p && !aligned16(p)) return LDN_ERR_INVALID_ARG;
+    if (!aligned(beta, 4) || (gate && !aligned(gate, 4))) return LDN_ERR_INVALID_ARG;
 
     ChunkArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S0, out, S_final,
                 B, T, H, dk, dv, chunk, mode, dtype, nullptr};
@@ -118,9 +122,13 @@ extern "C" int ldn_decode_step(const void *q, const void *k, const void *v, cons
     if ((long long)B * H > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
     if (!q || !k || !v || !beta || !S || !out) return LDN_ERR_INVALID_ARG;
     if (mode != LDN_DELTANET && !gate) return LDN_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, beta, gate, S, out};
-    for (const void *p : ptrs)
-        if (p && !aligned16(p)) return LDN_ERR_INVALID_ARG;
+    // The state moves in float4 rows; everything else is read element-wise.
+    const uintptr_t el = dtype == LDN_BF16 ? 2 : 4;
+    if (!aligned16(S)) return LDN_ERR_INVALID_ARG;
+    const void *el_ptrs[] = {q, k, v, out};
+    for (const void *p : el_ptrs)
+        if (!aligned(p, el)) return LDN_ERR_INVALID_ARG;
+    if (!aligned(beta, 4) || (gate && !aligned(gate, 4))) return LDN_ERR_INVALID_ARG;
     int *sw = status_word();
     if (!sw) return LDN_ERR_CUDA;
     DecodeArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S, out, B, H, dk, dv, mode, dtype, sw};

@@ -17,9 +17,12 @@
  * Attention notes, Sec. 1.2.
  *
  * Conventions shared by every entry point
- *   - Pointers q, k, v, beta, gate, S0, S, out, S_final are DEVICE pointers,
- *     contiguous, row-major, 16-byte aligned.  The caller owns every buffer;
- *     the library allocates no device memory per call.
+ *   - Pointers q, k, v, beta, gate, S0, S, out, S_final are DEVICE pointers to
+ *     contiguous, row-major arrays.  Alignment: ldn_chunk_fwd needs q, k, v,
+ *     out, S0 and S_final 16-byte aligned; ldn_decode_step needs S 16-byte
+ *     aligned and q, k, v, out aligned to their element size; beta and gate
+ *     are 4-byte aligned everywhere.  The caller owns every buffer; the
+ *     library allocates no device memory per call.
  *   - Gates are natural-log decays: alpha_t = exp(gate), a_t = exp(gate[c]).
  *     A positive log-gate is accepted (it is not clamped); beta is not clamped.
  *   - q is not scaled and q, k are not normalised by the library (scale = 1).

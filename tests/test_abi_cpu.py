@@ -66,6 +66,9 @@ def _chunk(**kw):
     (dict(gate=None, mode=2), ldn.LDN_ERR_INVALID_ARG),
     (dict(q=FAKE + 4), ldn.LDN_ERR_INVALID_ARG),            # misaligned
     (dict(S0=FAKE + 8), ldn.LDN_ERR_INVALID_ARG),
+    (dict(out=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(beta=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=FAKE + 1), ldn.LDN_ERR_INVALID_ARG),
     (dict(mode=3), ldn.LDN_ERR_INVALID_ARG),
     (dict(mode=-1), ldn.LDN_ERR_INVALID_ARG),
     (dict(dtype=2), ldn.LDN_ERR_INVALID_ARG),
@@ -96,6 +99,8 @@ def _decode(**kw):
     (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
     (dict(gate=None), ldn.LDN_ERR_INVALID_ARG),
     (dict(S=FAKE + 4), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),             # fp32 q needs 4-byte alignment
+    (dict(beta=FAKE + 1), ldn.LDN_ERR_INVALID_ARG),
     (dict(B=0), ldn.LDN_ERR_INVALID_ARG),
     (dict(mode=7), ldn.LDN_ERR_INVALID_ARG),
     (dict(dk=32), ldn.LDN_ERR_UNSUPPORTED),
