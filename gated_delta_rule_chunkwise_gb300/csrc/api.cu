@@ -20,12 +20,8 @@ cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cuda
     copy_state_kernel<<<(unsigned)blocks, 256, 0, stream>>>(S0, S_final, n);
     return cudaGetLastError();
 }
-}  // namespace ldn
-
-using namespace ldn;
-
 // Address of g_status on the current device, resolved once per device.
-static int *status_word()
+int *status_word_ptr()
 {
     static int *addr[64] = {nullptr};
     int dev = 0;
@@ -37,6 +33,9 @@ static int *status_word()
     }
     return addr[dev];
 }
+}  // namespace ldn
+
+using namespace ldn;
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
@@ -87,7 +86,7 @@ extern "C" int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v
     if (variant == LDN_VARIANT_AUTO)
         variant = (dtype == LDN_BF16 && chunk_tc_supported(a)) ? LDN_VARIANT_TENSOR : LDN_VARIANT_SIMT;
     if (variant == LDN_VARIANT_TENSOR && !chunk_tc_supported(a)) return LDN_ERR_UNSUPPORTED;
-    a.status = status_word();
+    a.status = status_word_ptr();
     if (!a.status) return LDN_ERR_CUDA;
     const cudaError_t err = variant == LDN_VARIANT_TENSOR ? launch_chunk_tc(a, s) : launch_chunk_simt(a, s);
     return err == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
@@ -129,7 +128,7 @@ extern "C" int ldn_decode_step(const void *q, const void *k, const void *v, cons
     for (const void *p : el_ptrs)
         if (!aligned(p, el)) return LDN_ERR_INVALID_ARG;
     if (!aligned(beta, 4) || (gate && !aligned(gate, 4))) return LDN_ERR_INVALID_ARG;
-    int *sw = status_word();
+    int *sw = status_word_ptr();
     if (!sw) return LDN_ERR_CUDA;
     DecodeArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S, out, B, H, dk, dv, mode, dtype, sw};
     return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;

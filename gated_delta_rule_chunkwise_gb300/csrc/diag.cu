@@ -1,0 +1,158 @@
+// Diagnostic entry points (include/ldn_diag.h): check, on tiny matrices, the
+// building blocks the tensor-core kernels rely on -- SWIZZLE_128B placement
+// of TMA loads, shared-memory / instruction descriptors for K-major and
+// MN-major bf16 operands, and the TMEM row layout of M = 64 and M = 128
+// accumulators.  They exist so that tests can pin these encodings directly.
+#include "ldn_internal.cuh"
+#include "sm100_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace ldn {
+namespace {
+using namespace sm100;
+
+constexpr uint64_t kDiagTimeoutNs = 2000000000ull;   // 2 s
+constexpr float kSentinel = -12345.0f;
+
+// One MMA chain D = A * B^T over K, A [M][K], B [N][K] (row-major bf16 in
+// global memory), placed in shared memory K-major or MN-major; the whole
+// 128-lane x N TMEM region is dumped to D_out [128][N] after being prefilled
+// with a sentinel, so a test can see which lanes the accumulator occupies.
+__global__ void __launch_bounds__(128)
+diag_umma_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__restrict__ B, float *__restrict__ D,
+                 int M, int N, int K, int a_mn, int b_mn, uint32_t tmem_cols, int *status)
+{
+    extern __shared__ uint8_t dsmem[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);
+    uint8_t *As = base;                    // up to 128 x 128 bf16
+    uint8_t *Bs = base + 32768;            // up to 256 x 128 bf16
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    for (int e = tid; e < M * K; e += 128) {
+        const int m = e / K, k = e % K;
+        const uint32_t off = a_mn ? (m >> 6) * (uint32_t)K * 128u + sw128_offset(k, m & 63)
+                                  : (k >> 6) * (uint32_t)M * 128u + sw128_offset(m, k & 63);
+        *reinterpret_cast<__nv_bfloat16 *>(As + off) = A[e];
+    }
+    for (int e = tid; e < N * K; e += 128) {
+        const int n = e / K, k = e % K;
+        const uint32_t off = b_mn ? (n >> 6) * (uint32_t)K * 128u + sw128_offset(k, n & 63)
+                                  : (k >> 6) * (uint32_t)N * 128u + sw128_offset(n, k & 63);
+        *reinterpret_cast<__nv_bfloat16 *>(Bs + off) = B[e];
+    }
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_s, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_s;
+
+    float sent[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sent[i] = kSentinel;
+    for (int c = 0; c < N; c += 16) tmem_st16(tmem_addr(tbase, 32 * warp, c), sent);
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (tid == 0) {
+        const uint32_t idesc = idesc_bf16_f32(M, N, a_mn, b_mn);
+        const uint32_t a0 = smem_u32(As), b0 = smem_u32(Bs);
+        for (int s = 0; s < K / 16; ++s) {
+            const uint64_t ad = a_mn ? mnmajor_desc(a0, K, s) : kmajor_desc(a0, M, s);
+            const uint64_t bd = b_mn ? mnmajor_desc(b0, K, s) : kmajor_desc(b0, N, s);
+            umma_bf16(tbase, ad, bd, idesc, s > 0);
+        }
+        umma_commit(&bar);
+    }
+    const bool ok = mbar_wait(&bar, 0, kDiagTimeoutNs);
+    if (!ok && lane == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+    tc_fence_after();
+    if (ok) {
+        for (int c = 0; c < N; c += 16) {
+            float v[16];
+            tmem_ld16(tmem_addr(tbase, 32 * warp, c), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[(size_t)(32 * warp + lane) * N + c + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, tmem_cols);
+}
+
+// TMA load of a 64-row x 64-column bf16 box (SWIZZLE_128B) at (row0, col0)
+// of a [rows][cols] matrix, then a raw byte dump of the 8 KiB tile.
+__global__ void __launch_bounds__(128)
+diag_tma_kernel(const __grid_constant__ CUtensorMap map, uint8_t *__restrict__ out, int col0, int row0, int *status)
+{
+    __shared__ __align__(1024) uint8_t tile[8192];
+    __shared__ uint64_t bar;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar, 8192);
+        tma_load_4d(tile, &map, &bar, col0, 0, row0, 0);
+    }
+    const bool ok = mbar_wait(&bar, 0, kDiagTimeoutNs);
+    if (!ok) {
+        if (tid == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        return;
+    }
+    for (int i = tid; i < 8192 / 16; i += 128)
+        reinterpret_cast<uint4 *>(out)[i] = reinterpret_cast<const uint4 *>(tile)[i];
+}
+
+}  // namespace
+}  // namespace ldn
+
+using namespace ldn;
+
+extern "C" int ldn_diag_umma(const void *A, const void *B, float *D, int M, int N, int K, int a_mn, int b_mn,
+                             void *stream)
+{
+    if (!A || !B || !D) return LDN_ERR_INVALID_ARG;
+    if (M != 64 && M != 128) return LDN_ERR_UNSUPPORTED;
+    if (N < 16 || N > 256 || N % 16 != 0) return LDN_ERR_UNSUPPORTED;
+    if (K < 16 || K > 128 || K % 16 != 0) return LDN_ERR_UNSUPPORTED;
+    if ((a_mn && (M % 64 != 0 || K % 8 != 0)) || (b_mn && N % 64 != 0)) return LDN_ERR_UNSUPPORTED;
+    int *sw = status_word_ptr();
+    if (!sw) return LDN_ERR_CUDA;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)N) cols <<= 1;
+    const size_t smem = 32768 + 65536 + 1024;
+    if (cudaFuncSetAttribute(diag_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return LDN_ERR_CUDA;
+    diag_umma_kernel<<<1, 128, smem, (cudaStream_t)stream>>>((const __nv_bfloat16 *)A, (const __nv_bfloat16 *)B,
+                                                             D, M, N, K, a_mn, b_mn, cols, sw);
+    return cudaGetLastError() == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
+extern "C" int ldn_diag_tma_sw128(const void *src, void *dst, int rows, int cols, int row0, int col0, void *stream)
+{
+    if (!src || !dst) return LDN_ERR_INVALID_ARG;
+    if (((uintptr_t)src & 15u) || rows < 1 || cols < 64 || cols % 8 != 0) return LDN_ERR_INVALID_ARG;
+    if (col0 < 0 || col0 % 64 != 0 || col0 + 64 > cols || row0 < 0) return LDN_ERR_INVALID_ARG;
+    int *sw = status_word_ptr();
+    if (!sw) return LDN_ERR_CUDA;
+    CUtensorMap map;
+    if (!make_tmap_bf16_4d(&map, src, (uint64_t)cols, 1, (uint64_t)rows, 1, 64, 64)) return LDN_ERR_CUDA;
+    diag_tma_kernel<<<1, 128, 0, (cudaStream_t)stream>>>(map, (uint8_t *)dst, col0, row0, sw);
+    return cudaGetLastError() == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "../../include/ldn.h"
+#include "../../include/ldn_diag.h"
 
 namespace ldn {
 
@@ -36,6 +37,7 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs &a);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+int *status_word_ptr();   // address of the device status word on the current device
 cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cudaStream_t stream);
 
 // Loads of q/k/v in either element type, widened to fp32.

@@ -1,0 +1,41 @@
+/*
+ * ldn_diag.h -- diagnostic entry points of libldn.
+ *
+ * These do not compute the method; they expose, on tiny inputs, the hardware
+ * building blocks the tensor-core kernels of ldn.h are made of, so that tests
+ * can check each encoding against a plain matrix product.  Pointers are
+ * device pointers; calls are asynchronous on `stream`; argument errors return
+ * synchronously (LDN_ERR_* of ldn.h); a kernel that abandons a bounded wait
+ * sets LDN_ERR_TIMEOUT in the status word read by ldn_get_device_status().
+ */
+#ifndef LDN_DIAG_H
+#define LDN_DIAG_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One tcgen05.mma chain (kind::f16, bf16 inputs, fp32 accumulate in TMEM),
+ * D = A * B^T over K, with A [M][K] and B [N][K] bf16 row-major in global
+ * memory placed in shared memory with 128-byte swizzle, K-major (a_mn / b_mn
+ * = 0) or MN-major (= 1).  The accumulator's TMEM region is prefilled with
+ * -12345.0 and then dumped whole: D_out [128][N] fp32, row = TMEM lane.
+ * M in {64, 128}; N in [16, 256], N % 16 == 0 (N % 64 == 0 if b_mn);
+ * K in [16, 128], K % 16 == 0.
+ */
+int ldn_diag_umma(const void *A, const void *B, float *D_out, int M, int N, int K, int a_mn, int b_mn,
+                  void *stream);
+
+/*
+ * TMA tiled load (SWIZZLE_128B, box 64 x 64) of rows [row0, row0 + 64) and
+ * columns [col0, col0 + 64) of a bf16 matrix src [rows][cols]; rows past the
+ * end read as zero.  The 8192 bytes of the shared-memory tile are copied to
+ * dst unchanged.  src 16-byte aligned, cols % 8 == 0, col0 % 64 == 0.
+ */
+int ldn_diag_tma_sw128(const void *src, void *dst, int rows, int cols, int row0, int col0, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LDN_DIAG_H */
