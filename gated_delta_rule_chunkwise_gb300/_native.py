@@ -49,7 +49,7 @@ _SIGNATURES = {
     "ldn_get_device_status": ([_P], _I),
     "ldn_status_string": ([_I], ctypes.c_char_p),
     "ldn_version": ([], _I),
-    "ldn_diag_umma": ([_P] * 3 + [_I] * 5 + [_P], _I),
+    "ldn_diag_umma": ([_P] * 3 + [_I] * 6 + [_P], _I),
     "ldn_diag_tma_sw128": ([_P] * 2 + [_I] * 4 + [_P], _I),
 }
 EXPORTS = tuple(_SIGNATURES)
@@ -108,8 +108,8 @@ def ldn_version() -> int:
     return load().ldn_version()
 
 
-def ldn_diag_umma(A, B, D, M, N, K, a_mn, b_mn, stream):
-    return load().ldn_diag_umma(A, B, D, M, N, K, a_mn, b_mn, stream)
+def ldn_diag_umma(A, B, D, M, N, K, a_mn, b_mn, fmt, stream):
+    return load().ldn_diag_umma(A, B, D, M, N, K, a_mn, b_mn, fmt, stream)
 
 
 def ldn_diag_tma_sw128(src, dst, rows, cols, row0, col0, stream):

@@ -1,6 +1,14 @@
-// Chunkwise forward on the 5th-generation tensor cores (tcgen05, bf16
+// Chunkwise forward on the 5th-generation tensor cores (tcgen05, fp16
 // operands, fp32 accumulators in TMEM), fp32 state, for bf16 q/k/v with
 // dk = 128 and dv a multiple of 64; DeltaNet and Gated DeltaNet.
+//
+// Operand precision: the bf16 q/k/v tiles are converted to fp16 in shared
+// memory on arrival (exact for the magnitudes of normalised activations), and
+// every intermediate operand (P, T, P T, Q~, W, the state copy, U~) is
+// rounded to fp16 rather than bf16: 2^-11 instead of 2^-8 relative rounding,
+// which keeps the chunk result within a few 1e-3 of the exact recurrence on
+// a max-error / RMS scale.  Accumulation, the inverse and the state are fp32.
+// Intermediates and inputs must stay below the fp16 range (65504).
 //
 // Chunk algebra (exact; derived from the per-token rules of the
 // linear-attention notes, Sec. 2.3-2.4, which give no chunk form).  Memory
@@ -99,23 +107,55 @@ __device__ __forceinline__ void st_bf16x8(uint8_t *p, const float *v)
     *reinterpret_cast<uint4 *>(p) = u;
 }
 
+__device__ __forceinline__ void st_f16x8(uint8_t *p, const float *v)
+{
+    __half2 h0 = __floats2half2_rn(v[0], v[1]);
+    __half2 h1 = __floats2half2_rn(v[2], v[3]);
+    __half2 h2 = __floats2half2_rn(v[4], v[5]);
+    __half2 h3 = __floats2half2_rn(v[6], v[7]);
+    uint4 u;
+    u.x = *reinterpret_cast<uint32_t *>(&h0);
+    u.y = *reinterpret_cast<uint32_t *>(&h1);
+    u.z = *reinterpret_cast<uint32_t *>(&h2);
+    u.w = *reinterpret_cast<uint32_t *>(&h3);
+    *reinterpret_cast<uint4 *>(p) = u;
+}
+
 // Store 16 consecutive columns [col, col+16) of row `row` into a SWIZZLE_128B
-// block (col % 16 == 0, col < 64).
+// block of fp16 operands (col % 16 == 0, col < 64).
 __device__ __forceinline__ void st_row16(uint8_t *block, int row, int col, const float *v)
 {
-    st_bf16x8(block + sw128_offset(row, col), v);
-    st_bf16x8(block + sw128_offset(row, col + 8), v + 8);
+    st_f16x8(block + sw128_offset(row, col), v);
+    st_f16x8(block + sw128_offset(row, col + 8), v + 8);
 }
 
 __device__ __forceinline__ void ld_row8(const uint8_t *block, int row, int col, float *v)
 {
     const uint4 u = *reinterpret_cast<const uint4 *>(block + sw128_offset(row, col));
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
+        const float2 f = __half22float2(h[i]);
         v[2 * i] = f.x;
         v[2 * i + 1] = f.y;
+    }
+}
+
+// In-place bf16 -> fp16 conversion of `bytes` of swizzled tile (all threads).
+// Exact for |x| in [2^-14, 65504]; smaller magnitudes keep an absolute error
+// below 2^-25.
+__device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int tid)
+{
+    for (int o = tid * 16; o < bytes; o += kThreads * 16) {
+        uint4 u = *reinterpret_cast<const uint4 *>(p + o);
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&w[i]);
+            __half2 h2 = __float22half2_rn(__bfloat1622float2(b2));
+            w[i] = *reinterpret_cast<uint32_t *>(&h2);
+        }
+        *reinterpret_cast<uint4 *>(p + o) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -215,10 +255,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return S.fail == 0;
     };
 
-    const uint32_t id_n64 = idesc_bf16_f32(128, 64, 0, 0);     // K-major A, K-major B
-    const uint32_t id_mn_n128 = idesc_bf16_f32(128, 128, 0, 1); // K-major A, MN-major B
-    const uint32_t id_mn_n64 = idesc_bf16_f32(128, 64, 0, 1);
-    const uint32_t id_amn_n64 = idesc_bf16_f32(128, 64, 1, 1);  // MN-major A and B
+    // Every operand of every MMA is fp16 (the q/k/v tiles are converted in place
+    // on arrival), so no MMA mixes element types.
+    const uint32_t id_n64 = idesc_f16kind_f32(128, 64, 0, 0, kMmaF16);      // K-major A, K-major B
+    const uint32_t id_mn_n128 = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16);  // K-major A, MN-major B
+    const uint32_t id_mn_n64 = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);
+    const uint32_t id_amn_n64 = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);   // MN-major A and B
 
     for (int c = 0; c < nchunks; ++c) {
         const int st = c & 1;
@@ -252,6 +294,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncthreads();
         if (S.fail) break;
         if (tid == 0) pending[st] = -1;
+        tile_bf16_to_f16(QK, kQKBytes, tid);
+        tile_bf16_to_f16(Vt, kVBytes, tid);
+        fence_proxy_async_smem();
+        __syncthreads();
         if (tid == 0) {
             tc_fence_after();
             for (int s = 0; s < kDK / 16; ++s)

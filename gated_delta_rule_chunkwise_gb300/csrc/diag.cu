@@ -19,8 +19,8 @@ constexpr float kSentinel = -12345.0f;
 // 128-lane x N TMEM region is dumped to D_out [128][N] after being prefilled
 // with a sentinel, so a test can see which lanes the accumulator occupies.
 __global__ void __launch_bounds__(128)
-diag_umma_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__restrict__ B, float *__restrict__ D,
-                 int M, int N, int K, int a_mn, int b_mn, uint32_t tmem_cols, int *status)
+diag_umma_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B, float *__restrict__ D,
+                 int M, int N, int K, int a_mn, int b_mn, uint32_t fmt, uint32_t tmem_cols, int *status)
 {
     extern __shared__ uint8_t dsmem[];
     uint8_t *base = (uint8_t *)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);
@@ -34,13 +34,13 @@ diag_umma_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__res
         const int m = e / K, k = e % K;
         const uint32_t off = a_mn ? (m >> 6) * (uint32_t)K * 128u + sw128_offset(k, m & 63)
                                   : (k >> 6) * (uint32_t)M * 128u + sw128_offset(m, k & 63);
-        *reinterpret_cast<__nv_bfloat16 *>(As + off) = A[e];
+        *reinterpret_cast<uint16_t *>(As + off) = A[e];
     }
     for (int e = tid; e < N * K; e += 128) {
         const int n = e / K, k = e % K;
         const uint32_t off = b_mn ? (n >> 6) * (uint32_t)K * 128u + sw128_offset(k, n & 63)
                                   : (k >> 6) * (uint32_t)N * 128u + sw128_offset(n, k & 63);
-        *reinterpret_cast<__nv_bfloat16 *>(Bs + off) = B[e];
+        *reinterpret_cast<uint16_t *>(Bs + off) = B[e];
     }
     fence_proxy_async_smem();
     if (tid == 0) {
@@ -66,7 +66,7 @@ diag_umma_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__res
     tc_fence_after();
 
     if (tid == 0) {
-        const uint32_t idesc = idesc_bf16_f32(M, N, a_mn, b_mn);
+        const uint32_t idesc = idesc_f16kind_f32(M, N, a_mn, b_mn, fmt);
         const uint32_t a0 = smem_u32(As), b0 = smem_u32(Bs);
         for (int s = 0; s < K / 16; ++s) {
             const uint64_t ad = a_mn ? mnmajor_desc(a0, K, s) : kmajor_desc(a0, M, s);
@@ -123,10 +123,11 @@ diag_tma_kernel(const __grid_constant__ CUtensorMap map, uint8_t *__restrict__ o
 
 using namespace ldn;
 
-extern "C" int ldn_diag_umma(const void *A, const void *B, float *D, int M, int N, int K, int a_mn, int b_mn,
+extern "C" int ldn_diag_umma(const void *A, const void *B, float *D, int M, int N, int K, int a_mn, int b_mn, int fmt,
                              void *stream)
 {
     if (!A || !B || !D) return LDN_ERR_INVALID_ARG;
+    if (fmt != 0 && fmt != 1) return LDN_ERR_INVALID_ARG;
     if (M != 64 && M != 128) return LDN_ERR_UNSUPPORTED;
     if (N < 16 || N > 256 || N % 16 != 0) return LDN_ERR_UNSUPPORTED;
     if (K < 16 || K > 128 || K % 16 != 0) return LDN_ERR_UNSUPPORTED;
@@ -139,8 +140,8 @@ extern "C" int ldn_diag_umma(const void *A, const void *B, float *D, int M, int 
     if (cudaFuncSetAttribute(diag_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return LDN_ERR_CUDA;
-    diag_umma_kernel<<<1, 128, smem, (cudaStream_t)stream>>>((const __nv_bfloat16 *)A, (const __nv_bfloat16 *)B,
-                                                             D, M, N, K, a_mn, b_mn, cols, sw);
+    diag_umma_kernel<<<1, 128, smem, (cudaStream_t)stream>>>((const uint16_t *)A, (const uint16_t *)B,
+                                                             D, M, N, K, a_mn, b_mn, (uint32_t)fmt, cols, sw);
     return cudaGetLastError() == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 

@@ -181,14 +181,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulate.
-// a_mn / b_mn: operand is MN-major (1) or K-major (0).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn)
+// Instruction descriptor, kind::f16 with fp32 accumulate.  `fmt` is the
+// element type of BOTH A and B (kMmaF16 or kMmaBF16: one MMA never mixes
+// them).  a_mn / b_mn: operand is MN-major (1) or K-major (0).
+constexpr uint32_t kMmaF16 = 0;
+constexpr uint32_t kMmaBF16 = 1;
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn,
+                                                         uint32_t fmt)
 {
     return (1u << 4)            // D: f32
-           | (1u << 7)          // A: bf16
-           | (1u << 10)         // B: bf16
+           | (fmt << 7)         // A type
+           | (fmt << 10)        // B type (same as A)
            | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn)
+{
+    return idesc_f16kind_f32(M, N, a_mn, b_mn, kMmaBF16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.

@@ -16,16 +16,16 @@ extern "C" {
 #endif
 
 /*
- * One tcgen05.mma chain (kind::f16, bf16 inputs, fp32 accumulate in TMEM),
- * D = A * B^T over K, with A [M][K] and B [N][K] bf16 row-major in global
- * memory placed in shared memory with 128-byte swizzle, K-major (a_mn / b_mn
- * = 0) or MN-major (= 1).  The accumulator's TMEM region is prefilled with
+ * One tcgen05.mma chain (kind::f16, fp32 accumulate in TMEM), D = A * B^T
+ * over K, with A [M][K] and B [N][K] 16-bit row-major in global memory --
+ * both fp16 (fmt = 0) or both bf16 (fmt = 1) -- placed in shared memory with
+ * 128-byte swizzle, K-major (a_mn / b_mn = 0) or MN-major (= 1).  The accumulator's TMEM region is prefilled with
  * -12345.0 and then dumped whole: D_out [128][N] fp32, row = TMEM lane.
  * M in {64, 128}; N in [16, 256], N % 16 == 0 (N % 64 == 0 if b_mn);
  * K in [16, 128], K % 16 == 0.
  */
 int ldn_diag_umma(const void *A, const void *B, float *D_out, int M, int N, int K, int a_mn, int b_mn,
-                  void *stream);
+                  int fmt, void *stream);
 
 /*
  * TMA tiled load (SWIZZLE_128B, box 64 x 64) of rows [row0, row0 + 64) and

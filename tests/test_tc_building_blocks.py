@@ -51,21 +51,24 @@ def test_tma_swizzle_128b_placement(row0, col0):
     np.testing.assert_array_equal(got, want)
 
 
-CASES = [  # M, N, K, a_mn, b_mn
-    (128, 64, 128, 0, 0), (128, 128, 64, 0, 1), (128, 64, 64, 1, 1), (128, 128, 128, 1, 0),
-    (128, 256, 64, 0, 1), (64, 128, 64, 0, 1), (64, 64, 128, 0, 0), (64, 128, 64, 1, 1), (128, 16, 32, 0, 0),
+CASES = [  # M, N, K, a_mn, b_mn, fmt (0 fp16, 1 bf16)
+    (128, 64, 128, 0, 0, 1), (128, 128, 64, 0, 1, 1), (128, 64, 64, 1, 1, 1), (128, 128, 128, 1, 0, 1),
+    (128, 256, 64, 0, 1, 1), (64, 128, 64, 0, 1, 1), (64, 64, 128, 0, 0, 1), (64, 128, 64, 1, 1, 1),
+    (128, 16, 32, 0, 0, 1),
+    (128, 64, 128, 0, 0, 0), (128, 128, 64, 0, 1, 0), (128, 64, 64, 1, 1, 0), (128, 128, 128, 1, 0, 0),
 ]
 
 
-@pytest.mark.parametrize("M,N,K,a_mn,b_mn", CASES)
-def test_umma_bf16_layouts(M, N, K, a_mn, b_mn):
+@pytest.mark.parametrize("M,N,K,a_mn,b_mn,fmt", CASES)
+def test_umma_f16kind_layouts(M, N, K, a_mn, b_mn, fmt):
     import torch
-    g = torch.Generator().manual_seed(M * 1000 + N + K + 7 * a_mn + 13 * b_mn)
-    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
-    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    g = torch.Generator().manual_seed(M * 1000 + N + K + 7 * a_mn + 13 * b_mn + 17 * fmt)
+    dt = torch.bfloat16 if fmt == 1 else torch.float16
+    A = torch.randn(M, K, generator=g).to(dt)
+    B = torch.randn(N, K, generator=g).to(dt)
     D = torch.empty(128, N, dtype=torch.float32, device="cuda")
     Ad, Bd = A.cuda(), B.cuda()
-    st = ldn.ldn_diag_umma(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, a_mn, b_mn, _stream())
+    st = ldn.ldn_diag_umma(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, a_mn, b_mn, fmt, _stream())
     assert st == ldn.LDN_OK
     assert ldn.device_status() == ldn.LDN_OK
     got = D.cpu().numpy().astype(np.float64)
