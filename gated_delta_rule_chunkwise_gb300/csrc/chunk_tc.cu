@@ -2,14 +2,6 @@
 // operands, fp32 accumulators in TMEM), fp32 state, for bf16 q/k/v with
 // dk = 128 and dv a multiple of 64; DeltaNet and Gated DeltaNet.
 //
-// Operand precision: the bf16 q/k/v tiles are converted to fp16 in shared
-// memory on arrival (exact for the magnitudes of normalised activations), and
-// every intermediate operand (P, T, P T, Q~, W, the state copy, U~) is
-// rounded to fp16 rather than bf16: 2^-11 instead of 2^-8 relative rounding,
-// which keeps the chunk result within a few 1e-3 of the exact recurrence on
-// a max-error / RMS scale.  Accumulation, the inverse and the state are fp32.
-// Intermediates and inputs must stay below the fp16 range (65504).
-//
 // Chunk algebra (exact; derived from the per-token rules of the
 // linear-attention notes, Sec. 2.3-2.4, which give no chunk form).  Memory
 // orientation H = S^T ([dk][dv]).  For a chunk of C = 64 rows with incoming
@@ -20,27 +12,40 @@
 //   U'  = Tu V,   W = Tw K,   Q~ = Diag(e^{g}) Q - P W
 //   O   = P U' + Q~ H0
 //   U   = U' - W H0,   H1 = e^{g_C} H0 + K^T Diag(e^{g_C - g}) U
-// Every contraction runs as an M = 128 tcgen05.mma by stacking two 64-row
-// operands that share the right-hand side:
-//   MMA1  [Q ; K] K^T              -> P_raw (rows 0-63), (K K^T) (rows 64-127)
-//   MMA2  [P ; I] [Tu | Tw]        -> [P Tu | P Tw], [Tu | Tw]
-//   MMA3  [P Tu ; Tu] V            -> P U' (= intra-chunk output), U'
-//   MMA4  [Tw ; -P Tw] K           -> W, -P W
-//   MMA5  accumulate [Q~ ; -W] H0 onto MMA3's result -> O (rows 0-63), U (rows 64-127)
-//   MMA6  K^T U~                   -> K^T Diag(e^{g_C - g}) U (state increment)
-// Only MMA5, MMA6 and the register update of H depend on the incoming state.
-// The unit-lower-triangular inverse is computed on CUDA cores in fp32 by 16x16
-// blocks (diagonal blocks by substitution, off-diagonal blocks by block
-// substitution).
+// Only the last two lines depend on the incoming state.
 //
-// Work split: one CTA per (b, h, 64-wide slice of dv) -- value columns are
-// independent (state-reduction notes, Sec. 2.5) -- with 128 threads; thread t
-// owns TMEM lane t, i.e. row t of every accumulator, and row t of the fp32
-// state slice H[t][0:64] in registers.  q/k/v chunk tiles arrive by TMA
-// (128-byte swizzle, two stages); all other operands are written by the
-// threads into swizzled shared memory.  One elected thread issues TMA and MMA.
-// Every mbarrier wait is bounded in time; a timeout sets LDN_ERR_TIMEOUT in
-// the status word, abandons the remaining chunks, frees TMEM and returns.
+// Warp roles (384 threads, one CTA per (b, h, 64-wide slice of dv); value
+// columns are independent, state-reduction notes Sec. 2.5):
+//   * 8 PREP warps compute everything that does not depend on the state for
+//     chunk c + 1 while
+//   * 4 SERIAL warps run the state step of chunk c (thread = TMEM lane = row
+//     of the fp32 state slice H[row][0:64], held in registers).
+// Contractions (tcgen05.mma, fp16 operands, fp32 TMEM accumulators):
+//   MMA1 [Q ; K] K^T            M=128  bf16 tiles as loaded  -> P_raw, K K^T
+//   MMA2 P [Tu | Tw]            M=64                         -> P Tu, P Tw
+//   MMA3 [P Tu ; Tu] V          M=128                        -> P U', U'
+//   MMA4 [-P Tw ; Tw] K         M=128                        -> -P W, W
+//   MMA5 RV += [Q~ ; -W] H0     M=128  (serial)              -> O, U
+//   MMA6 K^T U~                 M=128  (serial)              -> state increment
+// Hand-offs use mbarriers: prep -> serial "chunk ready" (double-buffered
+// MMA3 accumulators), serial -> prep "A5 operand free" (an MMA commit) and
+// "accumulator read"; the serial warps issue the TMA loads of chunk c + 2 as
+// soon as the state step of chunk c has released its tiles.
+//
+// The unit-lower-triangular inverse is a blocked fp32 substitution on CUDA
+// cores.  Decay ratios are applied as row / column factors around the chunk's
+// middle row (e^{g_r - m} * e^{m - g_j}), each factor within e^{60}; chunks
+// whose log-decay span exceeds that use one exponential per entry instead.
+//
+// Operand precision: MMA1 runs on the bf16 tiles as loaded; the k and v tiles
+// are then converted to fp16 in place, and every computed operand (P, T,
+// P T, Q~, W, the state copy, U~) is rounded to fp16 (2^-11), which keeps the
+// result within a few 1e-3 of the exact recurrence on a max-error / RMS scale.
+// Inputs and intermediates must stay below the fp16 range (65504).
+//
+// Every mbarrier wait is bounded in time (2 s); a timeout sets LDN_ERR_TIMEOUT
+// in the status word, both roles abandon their loops, in-flight copies and
+// MMAs are drained with bounded waits, TMEM is freed and the CTA returns.
 #include "ldn_internal.cuh"
 #include "sm100_ptx.cuh"
 #include "tma_host.cuh"
@@ -52,108 +57,103 @@ using namespace sm100;
 constexpr int kC = 64;
 constexpr int kDK = 128;
 constexpr int kDVS = 64;
-constexpr int kThreads = 128;
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, far above any legitimate latency
+constexpr int kPrepThreads = 256;
+constexpr int kSerialThreads = 128;
+constexpr int kThreads = kPrepThreads + kSerialThreads;
+constexpr uint32_t kBarPrep = 1, kBarSerial = 2;   // named barrier ids
+constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
+constexpr float kMaxLogSpan = 60.f;                // factored decay limit (e^60 per factor)
 
 // TMEM columns (fp32, 128 lanes).
-constexpr uint32_t kColD1 = 0;      // 64
-constexpr uint32_t kColDP = 64;     // 128
-constexpr uint32_t kColRV = 192;    // 64
-constexpr uint32_t kColDK = 256;    // 128
-constexpr uint32_t kColD6 = 384;    // 64
+constexpr uint32_t kColD1 = 0;      // 64   MMA1
+constexpr uint32_t kColDP = 64;     // 128  MMA2 (M = 64 layout)
+constexpr uint32_t kColDK = 192;    // 128  MMA4
+constexpr uint32_t kColRV = 320;    // 2 x 64  MMA3 / MMA5 (double-buffered)
+constexpr uint32_t kColD6 = 448;    // 64   MMA6
 constexpr uint32_t kTmemCols = 512;
 
-// Shared-memory plan (bytes from a 1024-aligned base).
-constexpr uint32_t kQKBytes = 2 * 16384;      // [Q;K] K-major, 2 blocks of 128 rows x 128 B
+// Shared memory (bytes from a 1024-aligned base).
+constexpr uint32_t kQKBytes = 2 * 16384;      // [Q;K], 2 blocks of 128 rows x 128 B
 constexpr uint32_t kVBytes = 8192;            // V slice, 64 rows x 128 B
 constexpr uint32_t kOffQK0 = 0;
 constexpr uint32_t kOffQK1 = kOffQK0 + kQKBytes;
 constexpr uint32_t kOffV0 = kOffQK1 + kQKBytes;
 constexpr uint32_t kOffV1 = kOffV0 + kVBytes;
-constexpr uint32_t kOffPI = kOffV1 + kVBytes;          // [P ; I] K-major 128 x 64
-constexpr uint32_t kOffTT = kOffPI + 16384;            // [Tu | Tw] MN-major 64 x 128  (later [Tw ; -P Tw])
-constexpr uint32_t kOffAV = kOffTT + 16384;            // [P Tu ; Tu] K-major 128 x 64
-constexpr uint32_t kOffA5 = kOffAV + 16384;            // [Q~ ; -W] K-major 128 x 128
-constexpr uint32_t kOffHB = kOffA5 + 32768;            // H bf16, MN-major 128 x 64
-constexpr uint32_t kOffF = kOffHB + 16384;             // fp32 A [64][65] (later U~ bf16 64 x 64)
-constexpr uint32_t kOffTf = kOffF + 64 * 65 * 4;       // fp32 T [64][65]
-constexpr uint32_t kOffX = kOffTf + 64 * 65 * 4;       // fp32 block-inverse scratch [3][16][16]
+constexpr uint32_t kOffPI = kOffV1 + kVBytes;      // P, K-major 64 x 64                (8 KB)
+constexpr uint32_t kOffTT = kOffPI + 8192;         // [Tu | Tw] MN-major, then [-P Tw ; Tw] (16 KB)
+constexpr uint32_t kOffAV = kOffTT + 16384;        // [P Tu ; Tu] K-major 128 x 64       (16 KB)
+constexpr uint32_t kOffA5 = kOffAV + 16384;        // [Q~ ; -W] K-major 128 x 128        (32 KB)
+constexpr uint32_t kOffHB = kOffA5 + 32768;        // H fp16, MN-major 128 x 64          (16 KB)
+constexpr uint32_t kOffUB = kOffHB + 16384;        // U~ fp16, MN-major 64 x 64          (8 KB)
+constexpr uint32_t kOffAf = kOffUB + 8192;         // fp32 A [64][65]
+constexpr uint32_t kOffTf = kOffAf + 64 * 65 * 4;  // fp32 T [64][65]
+constexpr uint32_t kOffX = kOffTf + 64 * 65 * 4;   // fp32 block-inverse scratch [3][256]
 constexpr uint32_t kOffSmall = kOffX + 3 * 256 * 4;
-constexpr uint32_t kSmemBytes = kOffSmall + 2048 + 1024;   // + small arrays + alignment slack
+constexpr uint32_t kSmemBytes = kOffSmall + 3072 + 1024;
 
 struct Small {
-    uint64_t bar_load[2];
-    uint64_t bar_mma;
+    uint64_t bar_load[2];     // TMA tiles of stage s landed
+    uint64_t bar_pmma;        // prep MMA commits
+    uint64_t bar_smma;        // serial MMA commits
+    uint64_t bar_ready[2];    // prep -> serial: chunk in RV[s] / A5 ready
+    uint64_t bar_a5free;      // serial MMA5 finished reading A5
+    uint64_t bar_rvfree[2];   // serial finished reading RV[s]
     uint32_t tmem_base;
     int fail;
+    int exact;                // per-entry exponentials for this chunk
     float beta[kC];
-    float g[kC];        // inclusive log-decay prefix
-    float eg[kC];       // e^{g_r}
-    float egc[kC];      // e^{g_C - g_r}
-    float gC;           // e^{g_C}
+    float g[kC];              // inclusive log-decay prefix
+    float fr[kC];             // e^{g_r - m}
+    float fc[kC];             // e^{m - g_j}
+    float eg[kC];             // e^{g_r}
+    float egc[2][kC];         // e^{g_C - g_r}, per stage (read by the serial warps)
+    float gC[2];              // e^{g_C}, per stage
 };
 
-__device__ __forceinline__ void st_bf16x8(uint8_t *p, const float *v)
+__device__ __forceinline__ uint32_t pack_h2(float a, float b)
 {
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
-    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
-    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
-    uint4 u;
-    u.x = *reinterpret_cast<uint32_t *>(&h0);
-    u.y = *reinterpret_cast<uint32_t *>(&h1);
-    u.z = *reinterpret_cast<uint32_t *>(&h2);
-    u.w = *reinterpret_cast<uint32_t *>(&h3);
-    *reinterpret_cast<uint4 *>(p) = u;
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ void st_f16x8(uint8_t *p, const float *v)
-{
-    __half2 h0 = __floats2half2_rn(v[0], v[1]);
-    __half2 h1 = __floats2half2_rn(v[2], v[3]);
-    __half2 h2 = __floats2half2_rn(v[4], v[5]);
-    __half2 h3 = __floats2half2_rn(v[6], v[7]);
-    uint4 u;
-    u.x = *reinterpret_cast<uint32_t *>(&h0);
-    u.y = *reinterpret_cast<uint32_t *>(&h1);
-    u.z = *reinterpret_cast<uint32_t *>(&h2);
-    u.w = *reinterpret_cast<uint32_t *>(&h3);
-    *reinterpret_cast<uint4 *>(p) = u;
-}
-
-// Store 16 consecutive columns [col, col+16) of row `row` into a SWIZZLE_128B
-// block of fp16 operands (col % 16 == 0, col < 64).
+// 16 consecutive columns [col, col + 16) of row `row` of a SWIZZLE_128B block,
+// as fp16 (col % 16 == 0, col < 64).
 __device__ __forceinline__ void st_row16(uint8_t *block, int row, int col, const float *v)
 {
-    st_f16x8(block + sw128_offset(row, col), v);
-    st_f16x8(block + sw128_offset(row, col + 8), v + 8);
+    *reinterpret_cast<uint4 *>(block + sw128_offset(row, col)) =
+        make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
+    *reinterpret_cast<uint4 *>(block + sw128_offset(row, col + 8)) =
+        make_uint4(pack_h2(v[8], v[9]), pack_h2(v[10], v[11]), pack_h2(v[12], v[13]), pack_h2(v[14], v[15]));
 }
 
-__device__ __forceinline__ void ld_row8(const uint8_t *block, int row, int col, float *v)
+// 8 bf16 values of a swizzled tile (as loaded by TMA), widened to fp32.
+__device__ __forceinline__ void ld_row8_bf16(const uint8_t *block, int row, int col, float *v)
 {
     const uint4 u = *reinterpret_cast<const uint4 *>(block + sw128_offset(row, col));
-    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h[i]);
+        const float2 f = __bfloat1622float2(h[i]);
         v[2 * i] = f.x;
         v[2 * i + 1] = f.y;
     }
 }
 
-// In-place bf16 -> fp16 conversion of `bytes` of swizzled tile (all threads).
-// Exact for |x| in [2^-14, 65504]; smaller magnitudes keep an absolute error
-// below 2^-25.
-__device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int tid)
+// In-place bf16 -> fp16 conversion of `bytes` of a tile by `n` threads.
+__device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int t, int n)
 {
-    for (int o = tid * 16; o < bytes; o += kThreads * 16) {
+    for (int o = t * 16; o < bytes; o += n * 16) {
         uint4 u = *reinterpret_cast<const uint4 *>(p + o);
         uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&w[i]);
-            __half2 h2 = __float22half2_rn(__bfloat1622float2(b2));
-            w[i] = *reinterpret_cast<uint32_t *>(&h2);
+            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[i]));
+            w[i] = pack_h2(f.x, f.y);
         }
         *reinterpret_cast<uint4 *>(p + o) = make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -169,24 +169,31 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     extern __shared__ uint8_t dsmem[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);
     Small &S = *reinterpret_cast<Small *>(sm + kOffSmall);
-    float *Af = reinterpret_cast<float *>(sm + kOffF);
+    float *Af = reinterpret_cast<float *>(sm + kOffAf);
     float *Tf = reinterpret_cast<float *>(sm + kOffTf);
     float *Xs = reinterpret_cast<float *>(sm + kOffX);
-    uint8_t *PI = sm + kOffPI, *TT = sm + kOffTT, *AV = sm + kOffAV, *A5 = sm + kOffA5, *HB = sm + kOffHB;
-    uint8_t *UB = sm + kOffF;   // U~ (bf16) reuses the fp32 A buffer after the inverse
+    uint8_t *PI = sm + kOffPI, *TT = sm + kOffTT, *AV = sm + kOffAV, *A5 = sm + kOffA5;
+    uint8_t *HB = sm + kOffHB, *UB = sm + kOffUB;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slices = dv / kDVS;
     const int unit = blockIdx.x / slices;
     const int b = unit / H, h = unit % H;
     const int n0 = (blockIdx.x % slices) * kDVS;
     const int nchunks = (T + kC - 1) / kC;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t quad = (uint32_t)(warp & 3);          // TMEM lane quadrant of this warp
+    const uint32_t lane_base = (32u * quad) << 16;
 
     if (tid == 0) {
         mbar_init(&S.bar_load[0], 1);
         mbar_init(&S.bar_load[1], 1);
-        mbar_init(&S.bar_mma, 1);
+        mbar_init(&S.bar_pmma, 1);
+        mbar_init(&S.bar_smma, 1);
+        mbar_init(&S.bar_ready[0], 1);
+        mbar_init(&S.bar_ready[1], 1);
+        mbar_init(&S.bar_a5free, 1);
+        mbar_init(&S.bar_rvfree[0], 1);
+        mbar_init(&S.bar_rvfree[1], 1);
         fence_mbar_init();
         S.fail = 0;
         tma_prefetch_desc(&tm_q);
@@ -197,370 +204,426 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_alloc(&S.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    // Identity rows 64..127 of [P ; I] (constant for the whole sequence).
-    {
-        const int r = tid - 64;
-        if (r >= 0)
-            for (int c = 0; c < 64; c += 16) {
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = (c + i == r) ? 1.f : 0.f;
-                st_row16(PI, tid, c, v);
-            }
-    }
-    // Incoming state: row c = tid of the slice, fp32 in registers, bf16 copy in HB.
-    float Hreg[kDVS];
-    {
-        const float *src = S0 ? S0 + ((size_t)unit * kDK + tid) * dv + n0 : nullptr;
-#pragma unroll
-        for (int n = 0; n < kDVS; n += 4) {
-            float4 x = src ? *reinterpret_cast<const float4 *>(src + n) : make_float4(0.f, 0.f, 0.f, 0.f);
-            Hreg[n] = x.x; Hreg[n + 1] = x.y; Hreg[n + 2] = x.z; Hreg[n + 3] = x.w;
-        }
-#pragma unroll
-        for (int n = 0; n < kDVS; n += 16) st_row16(HB, tid, n, &Hreg[n]);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
 
-    int pending[2] = {-1, -1};   // chunk whose TMA load is in flight per stage (thread 0)
-    auto issue_load = [&](int c) {
-        const int st = c & 1;
-        pending[st] = c;
-        uint8_t *qk = sm + (st ? kOffQK1 : kOffQK0);
-        uint8_t *vv = sm + (st ? kOffV1 : kOffV0);
-        mbar_arrive_expect_tx(&S.bar_load[st], 2 * 16384 + 8192);
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_4d(qk + kb * 16384, &tm_q, &S.bar_load[st], kb * 64, h, c * kC, b);
-            tma_load_4d(qk + kb * 16384 + 8192, &tm_k, &S.bar_load[st], kb * 64, h, c * kC, b);
-        }
-        tma_load_4d(vv, &tm_v, &S.bar_load[st], n0, h, c * kC, b);
-    };
-    if (tid == 0) {
-        issue_load(0);
-        if (nchunks > 1) issue_load(1);
-    }
-
-    uint32_t mma_phase = 0;
-    // Wait for the MMA commit; every thread calls it.  Returns false (in every
-    // thread alike) if any thread gave up on the wait.
-    auto wait_mma = [&]() -> bool {
-        if (!mbar_wait(&S.bar_mma, mma_phase, kWaitNs)) S.fail = 1;
-        mma_phase ^= 1u;
-        tc_fence_after();
-        __syncthreads();
-        return S.fail == 0;
-    };
-
-    // Every operand of every MMA is fp16 (the q/k/v tiles are converted in place
-    // on arrival), so no MMA mixes element types.
-    const uint32_t id_n64 = idesc_f16kind_f32(128, 64, 0, 0, kMmaF16);      // K-major A, K-major B
-    const uint32_t id_mn_n128 = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16);  // K-major A, MN-major B
-    const uint32_t id_mn_n64 = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);
-    const uint32_t id_amn_n64 = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);   // MN-major A and B
-
-    for (int c = 0; c < nchunks; ++c) {
-        const int st = c & 1;
-        const int t0 = c * kC;
-        const int L = min(kC, T - t0);
-        uint8_t *QK = sm + (st ? kOffQK1 : kOffQK0);
-        uint8_t *Vt = sm + (st ? kOffV1 : kOffV0);
-        const uint32_t qk_s = smem_u32(QK), k_s = qk_s + 8192, v_s = smem_u32(Vt);
-
-        // ---- gates and beta of this chunk (tail rows: beta 0, no decay)
-        if (tid < kC) {
-            const size_t i = ((size_t)b * T + t0 + tid) * H + h;
-            S.beta[tid] = tid < L ? beta[i] : 0.f;
-            S.g[tid] = (MODE == LDN_GDN && tid < L) ? gate[i] : 0.f;
-        }
-        __syncthreads();
-        if (MODE == LDN_GDN && tid == 0) {
-            float acc = 0.f;
-            for (int r = 0; r < kC; ++r) { acc += S.g[r]; S.g[r] = acc; }
-            S.gC = expf(acc);
-        }
-        __syncthreads();
-        if (tid < kC) {
-            S.eg[tid] = MODE == LDN_GDN ? expf(S.g[tid]) : 1.f;
-            S.egc[tid] = MODE == LDN_GDN ? expf(S.g[kC - 1] - S.g[tid]) : 1.f;
-        }
-        const float gC = MODE == LDN_GDN ? S.gC : 1.f;
-
-        // ---- MMA1: [Q ; K] K^T
-        if (!mbar_wait(&S.bar_load[st], (c >> 1) & 1, kWaitNs)) S.fail = 1;
-        __syncthreads();
-        if (S.fail) break;
-        if (tid == 0) pending[st] = -1;
-        tile_bf16_to_f16(QK, kQKBytes, tid);
-        tile_bf16_to_f16(Vt, kVBytes, tid);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+    if (tid < kPrepThreads) {
+        // ============================== PREP ==============================
+        const int pt = tid;
+        const int half = pt >> 7;                  // column half handled in TMEM reads
+        const int row = 32 * quad + lane;          // TMEM lane of this thread
+        const bool issuer = (pt == 32);
+        uint32_t pphase = 0;
+        auto prep_vote = [&](bool ok) -> bool {
+            if (!ok) S.fail = 1;
+            named_sync(kBarPrep, kPrepThreads);
+            return S.fail == 0;
+        };
+        auto wait_pmma = [&]() -> bool {
+            const bool ok = mbar_wait(&S.bar_pmma, pphase, kWaitNs);
+            pphase ^= 1u;
             tc_fence_after();
-            for (int s = 0; s < kDK / 16; ++s)
-                umma_bf16(tbase + kColD1, kmajor_desc(qk_s, 128, s), kmajor_desc(k_s, 128, s), id_n64, s > 0);
-            umma_commit(&S.bar_mma);
-        }
-        if (!wait_mma()) break;
+            return prep_vote(ok);
+        };
+        const uint32_t id_m128_n64 = idesc_f16kind_f32(128, 64, 0, 0, kMmaBF16);   // MMA1 (bf16)
+        const uint32_t id_m64_n128 = idesc_f16kind_f32(64, 128, 0, 1, kMmaF16);    // MMA2
+        const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16); // MMA3
+        const uint32_t id_m128_n128_mn = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16);// MMA4
 
-        // ---- A (fp32, for the inverse) and P (bf16 operand), gated and masked
-        {
-            const bool isP = tid < 64;
-            const int r = isP ? tid : tid - 64;
-            const float gr = S.g[r], br = S.beta[r];
-            for (int j0 = 0; j0 < kC; j0 += 16) {
-                float v[16];
-                tmem_ld16(tbase + lane_base + kColD1 + j0, v);
-                tmem_ld_wait();
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
+            uint8_t *QK = sm + (s ? kOffQK1 : kOffQK0);
+            uint8_t *Vt = sm + (s ? kOffV1 : kOffV0);
+            const uint32_t qk_s = smem_u32(QK), k_s = qk_s + 8192, v_s = smem_u32(Vt);
+
+            // ---- P1: tiles of chunk c; MMA1 on the bf16 tiles as loaded
+            if (!prep_vote(mbar_wait(&S.bar_load[s], (c >> 1) & 1, kWaitNs))) break;
+            if (issuer) {
+                tc_fence_after();
+                for (int k = 0; k < kDK / 16; ++k)
+                    umma_bf16(tbase + kColD1, kmajor_desc(qk_s, 128, k), kmajor_desc(k_s, 128, k), id_m128_n64,
+                              k > 0);
+                umma_commit(&S.bar_pmma);
+            }
+            // ---- P2: beta, gate prefix (warp 0, two rows per lane) and decay factors
+            if (warp == 0) {
+                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+                const int r0 = 2 * lane, r1 = r0 + 1;
+                const size_t i0 = ((size_t)b * T + t0 + r0) * H + h, i1 = i0 + H;
+                if (r0 < L) { b0 = beta[i0]; if (MODE == LDN_GDN) a0 = gate[i0]; }
+                if (r1 < L) { b1 = beta[i1]; if (MODE == LDN_GDN) a1 = gate[i1]; }
+                float incl = a0 + a1;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = j0 + i;
-                    const bool keep = isP ? (j <= r) : (j < r);
-                    float x = keep ? v[i] : 0.f;
-                    if (MODE == LDN_GDN && keep) x *= expf(gr - S.g[j]);
-                    if (!isP) x *= br;
-                    v[i] = x;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
                 }
-                if (isP) st_row16(PI, r, j0, v);
-                else
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) Af[r * 65 + j0 + i] = v[i];
+                const float g1 = incl, g0 = incl - a1;
+                const float m = __shfl_sync(0xffffffffu, g1, 15);        // g at row 31
+                const float gc = __shfl_sync(0xffffffffu, g1, 31);       // g at row 63
+                S.beta[r0] = b0; S.beta[r1] = b1;
+                S.g[r0] = g0; S.g[r1] = g1;
+                if (MODE == LDN_GDN) {
+                    S.fr[r0] = expf(g0 - m); S.fr[r1] = expf(g1 - m);
+                    S.fc[r0] = expf(m - g0); S.fc[r1] = expf(m - g1);
+                    S.eg[r0] = expf(g0); S.eg[r1] = expf(g1);
+                    S.egc[s][r0] = expf(gc - g0); S.egc[s][r1] = expf(gc - g1);
+                    if (lane == 0) {
+                        S.gC[s] = expf(gc);
+                        S.exact = (-m > kMaxLogSpan || m - gc > kMaxLogSpan) ? 1 : 0;
+                    }
+                } else {
+                    S.fr[r0] = S.fr[r1] = S.fc[r0] = S.fc[r1] = 1.f;
+                    S.eg[r0] = S.eg[r1] = 1.f;
+                    S.egc[s][r0] = S.egc[s][r1] = 1.f;
+                    if (lane == 0) { S.gC[s] = 1.f; S.exact = 0; }
+                }
             }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
+            named_sync(kBarPrep, kPrepThreads);
+            if (!wait_pmma()) break;
 
-        // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by column substitution
-        if (tid < 64) {
-            const int blk = tid >> 4, col = tid & 15, o = blk * 16;
-            float x[16];
+            // ---- P4: P (fp16 operand) and A (fp32) from MMA1; k, v tiles -> fp16
+            {
+                const bool isP = row < 64;
+                const int r = isP ? row : row - 64;
+                const float frr = S.fr[r], br = S.beta[r], gr = S.g[r];
+                const bool exact = S.exact != 0;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = (r == col) ? 1.f : 0.f;
+                for (int jj = 0; jj < 32; jj += 16) {
+                    const int j0 = 32 * half + jj;
+                    float v[16];
+                    tmem_ld16(tbase + lane_base + kColD1 + j0, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < r; ++j) acc -= Af[(o + r) * 65 + o + j] * x[j];
-                x[r] = (r < col) ? 0.f : acc;
+                    for (int i = 0; i < 16; ++i) {
+                        const int j = j0 + i;
+                        const bool keep = isP ? (j <= r) : (j < r);
+                        float x = 0.f;
+                        if (keep) {
+                            x = v[i];
+                            if (MODE == LDN_GDN) x = exact ? x * expf(gr - S.g[j]) : (frr * x) * S.fc[j];
+                            if (!isP) x *= br;
+                        }
+                        v[i] = x;
+                    }
+                    if (isP) st_row16(PI, r, j0, v);
+                    else
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) Af[r * 65 + j0 + i] = v[i];
+                }
+                tile_bf16_to_f16(QK + 8192, 8192, pt, kPrepThreads);           // K, block 0
+                tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt, kPrepThreads);   // K, block 1
+                tile_bf16_to_f16(Vt, kVBytes, pt, kPrepThreads);
             }
+            fence_proxy_async_smem();
+            named_sync(kBarPrep, kPrepThreads);
+
+            // ---- P5: T = (I + A)^{-1}: 16x16 diagonal blocks, then block substitution
+            if (pt < 64) {
+                const int blk = pt >> 4, col = pt & 15, o = blk * 16;
+                float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) Tf[(o + r) * 65 + o + col] = x[r];
-        }
-        // zero the strictly-upper blocks of T
-        for (int e = tid; e < 64 * 64; e += kThreads) {
-            const int r = e >> 6, j = e & 63;
-            if ((j >> 4) > (r >> 4)) Tf[r * 65 + j] = 0.f;
-        }
-        __syncthreads();
-        // off-diagonal blocks by block distance d: T_{i+d,i} = -T_{i+d,i+d} sum_k A_{i+d,k} T_{k,i}
-        for (int d = 1; d < 4; ++d) {
-            const int nb = 4 - d;
-            for (int e = tid; e < nb * 256; e += kThreads) {
-                const int i = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int ro = (i + d) * 16, co = i * 16;
-                float acc = 0.f;
-                for (int kb = i; kb < i + d; ++kb)
+                for (int r = 0; r < 16; ++r) {
+                    float acc = (r == col) ? 1.f : 0.f;
+#pragma unroll
+                    for (int j = 0; j < r; ++j) acc -= Af[(o + r) * 65 + o + j] * x[j];
+                    x[r] = (r < col) ? 0.f : acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tf[(o + r) * 65 + o + col] = x[r];
+            }
+            for (int e = pt; e < 64 * 64; e += kPrepThreads) {
+                const int r = e >> 6, j = e & 63;
+                if ((j >> 4) > (r >> 4)) Tf[r * 65 + j] = 0.f;
+            }
+            named_sync(kBarPrep, kPrepThreads);
+            for (int d = 1; d < 4; ++d) {
+                const int nb = 4 - d;
+                for (int e = pt; e < nb * 256; e += kPrepThreads) {
+                    const int i = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                    const int ro = (i + d) * 16, co = i * 16;
+                    float acc = 0.f;
+                    for (int kb = i; kb < i + d; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk)
+                            acc += Af[(ro + rr) * 65 + kb * 16 + kk] * Tf[(kb * 16 + kk) * 65 + co + cc];
+                    Xs[e] = acc;
+                }
+                named_sync(kBarPrep, kPrepThreads);
+                for (int e = pt; e < nb * 256; e += kPrepThreads) {
+                    const int i = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                    const int ro = (i + d) * 16, co = i * 16;
+                    float acc = 0.f;
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
-                        acc += Af[(ro + rr) * 65 + kb * 16 + kk] * Tf[(kb * 16 + kk) * 65 + co + cc];
-                Xs[e] = acc;
+                        acc -= Tf[(ro + rr) * 65 + ro + kk] * Xs[(i << 8) + kk * 16 + cc];
+                    Tf[(ro + rr) * 65 + co + cc] = acc;
+                }
+                named_sync(kBarPrep, kPrepThreads);
             }
-            __syncthreads();
-            for (int e = tid; e < nb * 256; e += kThreads) {
-                const int i = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int ro = (i + d) * 16, co = i * 16;
-                float acc = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) acc -= Tf[(ro + rr) * 65 + ro + kk] * Xs[(i << 8) + kk * 16 + cc];
-                Tf[(ro + rr) * 65 + co + cc] = acc;
-            }
-            __syncthreads();
-        }
 
-        // ---- [Tu | Tw] as the MN-major right operand of MMA2 (row j of T scaled by column factors)
-        {
-            const int j = tid & 63;
-            const bool w = tid >= 64;
-            uint8_t *blk = TT + (w ? 8192 : 0);
-            for (int n0c = 0; n0c < kC; n0c += 16) {
-                float v[16];
+            // ---- P6: Tu, Tw rows (fp16): TT = [Tu | Tw] (MN-major B of MMA2, and Tw
+            //      doubles as rows 64..127 of [-P Tw ; Tw]); AV rows 64..127 = Tu
+            {
+                const int j = pt & 63;           // row of T
+                const int q4 = pt >> 6;          // which 16-column group
+                const int n0c = 16 * q4;
+                float vu[16], vw[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int n = n0c + i;
-                    const float f = S.beta[n] * (w ? S.eg[n] : 1.f);
-                    v[i] = Tf[j * 65 + n] * f;
+                    const float t = Tf[j * 65 + n] * S.beta[n];
+                    vu[i] = t;
+                    vw[i] = t * S.eg[n];
                 }
-                st_row16(blk, j, n0c, v);
+                st_row16(TT, j, n0c, vu);
+                st_row16(TT + 8192, j, n0c, vw);
+                st_row16(AV, 64 + j, n0c, vu);
             }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- MMA2: [P ; I] [Tu | Tw]
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t pi_s = smem_u32(PI), tt_s = smem_u32(TT);
-            for (int s = 0; s < kC / 16; ++s)
-                umma_bf16(tbase + kColDP, kmajor_desc(pi_s, 128, s), mnmajor_desc(tt_s, 64, s), id_mn_n128, s > 0);
-            umma_commit(&S.bar_mma);
-        }
-        if (!wait_mma()) break;
-
-        // ---- AV = [P Tu ; Tu] (own row), AK = [Tw ; -P Tw] (rows swap halves) into TT's buffer
-        {
-            const bool top = tid < 64;
-            const int r = tid & 63;
-            for (int j0 = 0; j0 < kC; j0 += 16) {
-                float v[16];
-                tmem_ld16(tbase + lane_base + kColDP + j0, v);
-                tmem_ld_wait();
-                st_row16(AV, tid, j0, v);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarPrep, kPrepThreads);
+            if (issuer) {
+                tc_fence_after();
+                const uint32_t pi_s = smem_u32(PI), tt_s = smem_u32(TT);
+                for (int k = 0; k < kC / 16; ++k)
+                    umma_bf16(tbase + kColDP, kmajor_desc(pi_s, 64, k), mnmajor_desc(tt_s, 64, k), id_m64_n128,
+                              k > 0);
+                umma_commit(&S.bar_pmma);
             }
-            __syncthreads();   // every thread has read [Tu | Tw] from TT before it is overwritten
-            for (int j0 = 0; j0 < kC; j0 += 16) {
-                float v[16];
-                tmem_ld16(tbase + lane_base + kColDP + 64 + j0, v);
-                tmem_ld_wait();
-                if (top) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = -v[i];
-                }
-                st_row16(TT, top ? 64 + r : r, j0, v);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
+            if (!wait_pmma()) break;
 
-        // ---- MMA3: [P Tu ; Tu] V -> RV ;  MMA4: [Tw ; -P Tw] K -> DK
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(TT);
-            for (int s = 0; s < kC / 16; ++s)
-                umma_bf16(tbase + kColRV, kmajor_desc(av_s, 128, s), mnmajor_desc(v_s, 64, s), id_mn_n64, s > 0);
-            for (int s = 0; s < kC / 16; ++s)
-                umma_bf16(tbase + kColDK, kmajor_desc(ak_s, 128, s), mnmajor_desc(k_s, 128, s), id_mn_n128, s > 0);
-            umma_commit(&S.bar_mma);
-        }
-        if (!wait_mma()) break;
-
-        // ---- A5 = [Q~ ; -W]:  rows 0-63 of DK hold W, rows 64-127 hold -P W
-        {
-            const bool top = tid < 64;
-            const int r = tid & 63;
-            const float er = S.eg[r];
-            for (int c0 = 0; c0 < kDK; c0 += 16) {
-                float v[16];
-                tmem_ld16(tbase + lane_base + kColDK + c0, v);
-                tmem_ld_wait();
-                uint8_t *blk = A5 + (c0 >> 6) * 16384;
-                if (top) {
+            // ---- P8: P Tu -> AV rows 0..63;  -P Tw -> TT rows 0..63 (so TT = [-P Tw ; Tw]).
+            //      MMA2 is M = 64: row r sits in TMEM lane 32*(r/16) + r%16.
+            {
+                const int r = 16 * (int)quad + (lane & 15);
+                const bool has = lane < 16;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = -v[i];
-                    st_row16(blk, 64 + r, c0 & 63, v);
-                } else {
-                    float qv[16];
-                    const uint8_t *qblk = QK + (c0 >> 6) * 16384;
-                    ld_row8(qblk, r, c0 & 63, qv);
-                    ld_row8(qblk, r, (c0 & 63) + 8, qv + 8);
+                for (int jj = 0; jj < 64; jj += 16) {
+                    float v[16];
+                    tmem_ld16(tbase + lane_base + kColDP + 64 * half + jj, v);
+                    tmem_ld_wait();
+                    if (has) {
+                        if (half == 0) st_row16(AV, r, jj, v);
+                        else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] += er * qv[i];
-                    st_row16(blk, r, c0 & 63, v);
+                            for (int i = 0; i < 16; ++i) v[i] = -v[i];
+                            st_row16(TT, r, jj, v);
+                        }
+                    }
                 }
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarPrep, kPrepThreads);
+
+            // ---- P9: MMA3 [P Tu ; Tu] V -> RV[s] (once the serial warps released it),
+            //      MMA4 [-P Tw ; Tw] K -> DK
+            if (c >= 2 && !prep_vote(mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs))) break;
+            if (issuer) {
+                tc_fence_after();
+                const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(TT);
+                for (int k = 0; k < kC / 16; ++k)
+                    umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(av_s, 128, k), mnmajor_desc(v_s, 64, k),
+                              id_m128_n64_mn, k > 0);
+                for (int k = 0; k < kC / 16; ++k)
+                    umma_bf16(tbase + kColDK, kmajor_desc(ak_s, 128, k), mnmajor_desc(k_s, 128, k),
+                              id_m128_n128_mn, k > 0);
+                umma_commit(&S.bar_pmma);
+            }
+            if (!wait_pmma()) break;
+
+            // ---- P10: A5 = [Q~ ; -W] (after the serial MMA5 of chunk c-1 has read A5):
+            //      DK rows 0..63 = -P W, rows 64..127 = W.
+            if (c >= 1 && !prep_vote(mbar_wait(&S.bar_a5free, (c - 1) & 1, kWaitNs))) break;
+            {
+                const bool top = row < 64;
+                const int r = top ? row : row - 64;
+                const float er = S.eg[r];
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 16) {
+                    const int c0 = 64 * half + cc;
+                    float v[16];
+                    tmem_ld16(tbase + lane_base + kColDK + c0, v);
+                    tmem_ld_wait();
+                    uint8_t *blk = A5 + half * 16384;
+                    if (top) {
+                        float qv[16];
+                        const uint8_t *qblk = QK + half * 16384;   // Q rows 0..63 (bf16)
+                        ld_row8_bf16(qblk, r, cc, qv);
+                        ld_row8_bf16(qblk, r, cc + 8, qv + 8);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] += er * qv[i];
+                        st_row16(blk, r, cc, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = -v[i];
+                        st_row16(blk, 64 + r, cc, v);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarPrep, kPrepThreads);
+            if (pt == 0) mbar_arrive(&S.bar_ready[s]);
+        }
+    } else {
+        // ============================== SERIAL ==============================
+        const int st = tid - kPrepThreads;   // = TMEM lane = state row
+        uint32_t sphase = 0;
+        auto serial_vote = [&](bool ok) -> bool {
+            if (!ok) S.fail = 1;
+            named_sync(kBarSerial, kSerialThreads);
+            return S.fail == 0;
+        };
+        auto wait_smma = [&]() -> bool {
+            const bool ok = mbar_wait(&S.bar_smma, sphase, kWaitNs);
+            sphase ^= 1u;
+            tc_fence_after();
+            return serial_vote(ok);
+        };
+        int pending[2] = {-1, -1};
+        auto issue_load = [&](int c) {
+            const int s = c & 1;
+            uint8_t *qk = sm + (s ? kOffQK1 : kOffQK0);
+            uint8_t *vv = sm + (s ? kOffV1 : kOffV0);
+            pending[s] = c;
+            mbar_arrive_expect_tx(&S.bar_load[s], 2 * 16384 + 8192);
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_4d(qk + kb * 16384, &tm_q, &S.bar_load[s], kb * 64, h, c * kC, b);
+                tma_load_4d(qk + kb * 16384 + 8192, &tm_k, &S.bar_load[s], kb * 64, h, c * kC, b);
+            }
+            tma_load_4d(vv, &tm_v, &S.bar_load[s], n0, h, c * kC, b);
+        };
+        if (st == 0) {
+            issue_load(0);
+            if (nchunks > 1) issue_load(1);
+        }
+        const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);   // MMA5
+        const uint32_t id_m128_n64_amn = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);  // MMA6
+
+        float Hreg[kDVS];
+        {
+            const float *src = S0 ? S0 + ((size_t)unit * kDK + st) * dv + n0 : nullptr;
+#pragma unroll
+            for (int n = 0; n < kDVS; n += 4) {
+                const float4 x = src ? *reinterpret_cast<const float4 *>(src + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+                Hreg[n] = x.x; Hreg[n + 1] = x.y; Hreg[n + 2] = x.z; Hreg[n + 3] = x.w;
+            }
+#pragma unroll
+            for (int n = 0; n < kDVS; n += 16) st_row16(HB, st, n, &Hreg[n]);
         }
         fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        named_sync(kBarSerial, kSerialThreads);
 
-        // ---- MMA5 (state-dependent): RV += [Q~ ; -W] H0
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t a5_s = smem_u32(A5), hb_s = smem_u32(HB);
-            for (int s = 0; s < kDK / 16; ++s)
-                umma_bf16(tbase + kColRV, kmajor_desc(a5_s, 128, s), mnmajor_desc(hb_s, 128, s), id_mn_n64, 1);
-            umma_commit(&S.bar_mma);
-        }
-        if (!wait_mma()) break;
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
+            const uint8_t *QK = sm + (s ? kOffQK1 : kOffQK0);
+            const uint32_t k_s = smem_u32(QK) + 8192;
 
-        // ---- O rows to global; U~ = Diag(e^{g_C - g}) U into UB
-        {
-            const bool top = tid < 64;
-            const int r = tid & 63;
-            const float f = S.egc[r];
+            // ---- S1: chunk c prepared
+            if (!serial_vote(mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs))) break;
+            const float gC = S.gC[s];
+            const float egc = (st >= 64) ? S.egc[s][st - 64] : 0.f;
+
+            // ---- S2: MMA5: RV[s] += [Q~ ; -W] H0  -> O (rows 0..63), U (rows 64..127)
+            if (st == 0) {
+                tc_fence_after();
+                const uint32_t a5_s = smem_u32(A5), hb_s = smem_u32(HB);
+                for (int k = 0; k < kDK / 16; ++k)
+                    umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(a5_s, 128, k), mnmajor_desc(hb_s, 128, k),
+                              id_m128_n64_mn, 1);
+                umma_commit(&S.bar_smma);
+                umma_commit(&S.bar_a5free);
+            }
+            if (!wait_smma()) break;
+
+            // ---- S3: O -> global (bf16); U~ = Diag(e^{g_C - g}) U -> UB
+            {
+                const bool top = st < 64;
+                const int r = top ? st : st - 64;
+#pragma unroll
+                for (int n = 0; n < kDVS; n += 16) {
+                    float v[16];
+                    tmem_ld16(tbase + lane_base + kColRV + 64 * s + n, v);
+                    tmem_ld_wait();
+                    if (top) {
+                        if (r < L) {
+                            __nv_bfloat16 *dst = out + (((size_t)b * T + t0 + r) * H + h) * dv + n0 + n;
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]),
+                                                                         pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
+                            *reinterpret_cast<uint4 *>(dst + 8) =
+                                make_uint4(pack_bf2(v[8], v[9]), pack_bf2(v[10], v[11]), pack_bf2(v[12], v[13]),
+                                           pack_bf2(v[14], v[15]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= egc;
+                        st_row16(UB, r, n, v);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarSerial, kSerialThreads);
+            if (st == 0) {
+                mbar_arrive(&S.bar_rvfree[s]);
+                // ---- S4: MMA6: K^T U~ -> D6
+                tc_fence_after();
+                const uint32_t ub_s = smem_u32(UB);
+                for (int k = 0; k < kC / 16; ++k)
+                    umma_bf16(tbase + kColD6, mnmajor_desc(k_s, 128, k), mnmajor_desc(ub_s, 64, k), id_m128_n64_amn,
+                              k > 0);
+                umma_commit(&S.bar_smma);
+            }
+            if (!wait_smma()) break;
+            // the tiles of stage s are no longer read by anyone: fetch chunk c + 2 into them
+            if (st == 0 && c + 2 < nchunks) issue_load(c + 2);
+
+            // ---- S5: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
+#pragma unroll
             for (int n = 0; n < kDVS; n += 16) {
                 float v[16];
-                tmem_ld16(tbase + lane_base + kColRV + n, v);
+                tmem_ld16(tbase + lane_base + kColD6 + n, v);
                 tmem_ld_wait();
-                if (top) {
-                    if (r < L) {
-                        __nv_bfloat16 *dst = out + (((size_t)b * T + t0 + r) * H + h) * dv + n0 + n;
-                        uint8_t tmp[32];
-                        st_bf16x8(tmp, v);
-                        st_bf16x8(tmp + 16, v + 8);
-                        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(tmp);
-                        *reinterpret_cast<uint4 *>(dst + 8) = *reinterpret_cast<uint4 *>(tmp + 16);
-                    }
-                } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] *= f;
-                    st_row16(UB, r, n, v);
+                for (int i = 0; i < 16; ++i) {
+                    Hreg[n + i] = gC * Hreg[n + i] + v[i];
+                    v[i] = Hreg[n + i];
                 }
+                st_row16(HB, st, n, v);
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarSerial, kSerialThreads);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
 
-        // ---- MMA6: K^T U~ -> D6
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t ub_s = smem_u32(UB);
-            for (int s = 0; s < kC / 16; ++s)
-                umma_bf16(tbase + kColD6, mnmajor_desc(k_s, 128, s), mnmajor_desc(ub_s, 64, s), id_amn_n64, s > 0);
-            umma_commit(&S.bar_mma);
-        }
-        if (!wait_mma()) break;
-        // this stage's tiles are free: prefetch chunk c + 2 into it
-        if (tid == 0 && c + 2 < nchunks) issue_load(c + 2);
-
-        // ---- H1 = e^{g_C} H0 + D6 (row tid), bf16 copy for the next chunk
+        if (S.fail == 0) {
+            if (S_final) {
+                float *dst = S_final + ((size_t)unit * kDK + st) * dv + n0;
 #pragma unroll
-        for (int n = 0; n < kDVS; n += 16) {
-            float v[16];
-            tmem_ld16(tbase + lane_base + kColD6 + n, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                Hreg[n + i] = gC * Hreg[n + i] + v[i];
-                v[i] = Hreg[n + i];
+                for (int n = 0; n < kDVS; n += 4)
+                    *reinterpret_cast<float4 *>(dst + n) =
+                        make_float4(Hreg[n], Hreg[n + 1], Hreg[n + 2], Hreg[n + 3]);
             }
-            st_row16(HB, tid, n, v);
+        } else if (st == 0) {
+            // Drain this role's in-flight TMA loads and MMAs (bounded) before
+            // shared memory and TMEM are released.
+            for (int s = 0; s < 2; ++s)
+                if (pending[s] >= 0) mbar_wait(&S.bar_load[s], (pending[s] >> 1) & 1, kWaitNs / 4);
+            mbar_wait(&S.bar_smma, sphase ^ 1u, kWaitNs / 4);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
     }
 
-    __syncthreads();
-    if (S.fail) {
-        if (tid == 0) {
-            atomicOr(status, 1 << LDN_ERR_TIMEOUT);
-            // Give outstanding TMA loads and MMAs a bounded chance to land
-            // before the shared memory and TMEM are released.
-            for (int st = 0; st < 2; ++st)
-                if (pending[st] >= 0) mbar_wait(&S.bar_load[st], (pending[st] >> 1) & 1, kWaitNs);
-            mbar_wait(&S.bar_mma, mma_phase ^ 1u, kWaitNs);
-        }
-    } else if (S_final) {
-        float *dst = S_final + ((size_t)unit * kDK + tid) * dv + n0;
-#pragma unroll
-        for (int n = 0; n < kDVS; n += 4)
-            *reinterpret_cast<float4 *>(dst + n) = make_float4(Hreg[n], Hreg[n + 1], Hreg[n + 2], Hreg[n + 3]);
-    }
     tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && S.fail) {
+        atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        mbar_wait(&S.bar_pmma, 0, kWaitNs / 8);   // best effort: a prep MMA may still be in flight
+        mbar_wait(&S.bar_pmma, 1, kWaitNs / 8);
+    }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
