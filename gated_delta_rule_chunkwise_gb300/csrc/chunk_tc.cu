@@ -22,19 +22,21 @@
 //     of the fp32 state slice H[row][0:64], held in registers).
 // Contractions (tcgen05.mma, fp16 operands, fp32 TMEM accumulators):
 //   MMA1 [Q ; K] K^T            M=128  bf16 tiles as loaded  -> P_raw, K K^T
-//   MMA2 P [Tu | Tw]            M=64                         -> P Tu, P Tw
 //   MMA3 [P Tu ; Tu] V          M=128                        -> P U', U'
 //   MMA4 [-P Tw ; Tw] K         M=128                        -> -P W, W
 //   MMA5 RV += [Q~ ; -W] H0     M=128  (serial)              -> O, U
 //   MMA6 K^T U~                 M=128  (serial)              -> state increment
+// and, inside the prep warps, P T by TF32 warp MMAs (block lower-triangular).
 // Hand-offs use mbarriers: prep -> serial "chunk ready" (double-buffered
 // MMA3 accumulators), serial -> prep "A5 operand free" (an MMA commit) and
 // "accumulator read"; the serial warps issue the TMA loads of chunk c + 2 as
 // soon as the state step of chunk c has released its tiles.
 //
-// The unit-lower-triangular inverse is a blocked fp32 substitution on CUDA
-// cores.  Decay ratios are applied as row / column factors around the chunk's
-// middle row (e^{g_r - m} * e^{m - g_j}), each factor within e^{60}; chunks
+// The unit-lower-triangular inverse is blocked by 16: the diagonal blocks by
+// fp32 substitution on CUDA cores, the blocks below them by block
+// substitution with TF32 warp MMAs (mma.sync m16n8k8, fp32 accumulate), one
+// warp per column block.  Decay ratios are applied as row / column factors
+// around the chunk's middle row (e^{g_r - m} * e^{m - g_j}), each factor within e^{60}; chunks
 // whose log-decay span exceeds that use one exponential per entry instead.
 //
 // Operand precision: MMA1 runs on the bf16 tiles as loaded; the k and v tiles
@@ -66,7 +68,6 @@ constexpr float kMaxLogSpan = 60.f;                // factored decay limit (e^60
 
 // TMEM columns (fp32, 128 lanes).
 constexpr uint32_t kColD1 = 0;      // 64   MMA1
-constexpr uint32_t kColDP = 64;     // 128  MMA2 (M = 64 layout)
 constexpr uint32_t kColDK = 192;    // 128  MMA4
 constexpr uint32_t kColRV = 320;    // 2 x 64  MMA3 / MMA5 (double-buffered)
 constexpr uint32_t kColD6 = 448;    // 64   MMA6
@@ -79,15 +80,15 @@ constexpr uint32_t kOffQK0 = 0;
 constexpr uint32_t kOffQK1 = kOffQK0 + kQKBytes;
 constexpr uint32_t kOffV0 = kOffQK1 + kQKBytes;
 constexpr uint32_t kOffV1 = kOffV0 + kVBytes;
-constexpr uint32_t kOffPI = kOffV1 + kVBytes;      // P, K-major 64 x 64                (8 KB)
-constexpr uint32_t kOffTT = kOffPI + 8192;         // [Tu | Tw] MN-major, then [-P Tw ; Tw] (16 KB)
-constexpr uint32_t kOffAV = kOffTT + 16384;        // [P Tu ; Tu] K-major 128 x 64       (16 KB)
+constexpr uint32_t kOffAK = kOffV1 + kVBytes;      // [-P Tw ; Tw] K-major 128 x 64      (16 KB)
+constexpr uint32_t kOffAV = kOffAK + 16384;        // [P Tu ; Tu] K-major 128 x 64       (16 KB)
 constexpr uint32_t kOffA5 = kOffAV + 16384;        // [Q~ ; -W] K-major 128 x 128        (32 KB)
 constexpr uint32_t kOffHB = kOffA5 + 32768;        // H fp16, MN-major 128 x 64          (16 KB)
 constexpr uint32_t kOffUB = kOffHB + 16384;        // U~ fp16, MN-major 64 x 64          (8 KB)
 constexpr uint32_t kOffAf = kOffUB + 8192;         // fp32 A [64][65]
 constexpr uint32_t kOffTf = kOffAf + 64 * 65 * 4;  // fp32 T [64][65]
-constexpr uint32_t kOffX = kOffTf + 64 * 65 * 4;   // fp32 block-inverse scratch [3][256]
+constexpr uint32_t kOffPf = kOffTf + 64 * 65 * 4;  // fp32 P [64][65]
+constexpr uint32_t kOffX = kOffPf + 64 * 65 * 4;   // fp32 block-inverse scratch [3][256]
 constexpr uint32_t kOffSmall = kOffX + 3 * 256 * 4;
 constexpr uint32_t kSmemBytes = kOffSmall + 3072 + 1024;
 
@@ -108,6 +109,8 @@ struct Small {
     float eg[kC];             // e^{g_r}
     float egc[2][kC];         // e^{g_C - g_r}, per stage (read by the serial warps)
     float gC[2];              // e^{g_C}, per stage
+    float stg_beta[2][kC];    // beta / log-gate of the next chunk, prefetched by cp.async
+    float stg_gate[2][kC];
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b)
@@ -172,7 +175,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float *Af = reinterpret_cast<float *>(sm + kOffAf);
     float *Tf = reinterpret_cast<float *>(sm + kOffTf);
     float *Xs = reinterpret_cast<float *>(sm + kOffX);
-    uint8_t *PI = sm + kOffPI, *TT = sm + kOffTT, *AV = sm + kOffAV, *A5 = sm + kOffA5;
+    float *Pf = reinterpret_cast<float *>(sm + kOffPf);
+    uint8_t *AK = sm + kOffAK, *AV = sm + kOffAV, *A5 = sm + kOffA5;
     uint8_t *HB = sm + kOffHB, *UB = sm + kOffUB;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,9 +232,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             return prep_vote(ok);
         };
         const uint32_t id_m128_n64 = idesc_f16kind_f32(128, 64, 0, 0, kMmaBF16);   // MMA1 (bf16)
-        const uint32_t id_m64_n128 = idesc_f16kind_f32(64, 128, 0, 1, kMmaF16);    // MMA2
         const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16); // MMA3
         const uint32_t id_m128_n128_mn = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16);// MMA4
+
+        // beta and log-gates of chunk cc into staging slot cc & 1 (warp 0; rows
+        // past T read as zero), asynchronously so the loads overlap a whole chunk.
+        auto prefetch_gates = [&](int cc) {
+            const int tt0 = cc * kC, LL = min(kC, T - tt0);
+            for (int r = lane; r < kC; r += 32) {
+                const bool ok = r < LL;
+                const size_t i = ok ? ((size_t)b * T + tt0 + r) * H + h : 0;
+                cp_async4(&S.stg_beta[cc & 1][r], beta + i, ok ? 4u : 0u);
+                if (MODE == LDN_GDN) cp_async4(&S.stg_gate[cc & 1][r], gate + i, ok ? 4u : 0u);
+            }
+            cp_async_commit();
+        };
+        if (warp == 0) prefetch_gates(0);
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
@@ -249,11 +266,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             // ---- P2: beta, gate prefix (warp 0, two rows per lane) and decay factors
             if (warp == 0) {
-                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+                cp_async_wait<0>();          // this chunk's staged beta / gates
+                __syncwarp();
                 const int r0 = 2 * lane, r1 = r0 + 1;
-                const size_t i0 = ((size_t)b * T + t0 + r0) * H + h, i1 = i0 + H;
-                if (r0 < L) { b0 = beta[i0]; if (MODE == LDN_GDN) a0 = gate[i0]; }
-                if (r1 < L) { b1 = beta[i1]; if (MODE == LDN_GDN) a1 = gate[i1]; }
+                const float b0 = S.stg_beta[s][r0], b1 = S.stg_beta[s][r1];
+                const float a0 = MODE == LDN_GDN ? S.stg_gate[s][r0] : 0.f;
+                const float a1 = MODE == LDN_GDN ? S.stg_gate[s][r1] : 0.f;
+                __syncwarp();
+                if (c + 1 < nchunks) prefetch_gates(c + 1);
                 float incl = a0 + a1;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -288,30 +308,33 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             {
                 const bool isP = row < 64;
                 const int r = isP ? row : row - 64;
-                const float frr = S.fr[r], br = S.beta[r], gr = S.g[r];
-                const bool exact = S.exact != 0;
+                const float frr = S.fr[r] * (isP ? 1.f : S.beta[r]), gr = S.g[r];
+                const float br = isP ? 1.f : S.beta[r];
+                const bool exact = MODE == LDN_GDN && S.exact != 0;
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 16) {
                     const int j0 = 32 * half + jj;
                     float v[16];
                     tmem_ld16(tbase + lane_base + kColD1 + j0, v);
                     tmem_ld_wait();
+                    if (exact) {   // log-decay span too wide for the factored form: one exp per entry
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = j0 + i;
-                        const bool keep = isP ? (j <= r) : (j < r);
-                        float x = 0.f;
-                        if (keep) {
-                            x = v[i];
-                            if (MODE == LDN_GDN) x = exact ? x * expf(gr - S.g[j]) : (frr * x) * S.fc[j];
-                            if (!isP) x *= br;
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = j0 + i;
+                            const bool keep = isP ? (j <= r) : (j < r);
+                            v[i] = keep ? v[i] * br * expf(gr - S.g[j]) : 0.f;
                         }
-                        v[i] = x;
-                    }
-                    if (isP) st_row16(PI, r, j0, v);
-                    else
+                    } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) Af[r * 65 + j0 + i] = v[i];
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = j0 + i;
+                            const bool keep = isP ? (j <= r) : (j < r);
+                            v[i] = keep ? (frr * v[i]) * S.fc[j] : 0.f;
+                        }
+                    }
+                    float *dst = (isP ? Pf : Af) + r * 65 + j0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dst[i] = v[i];
                 }
                 tile_bf16_to_f16(QK + 8192, 8192, pt, kPrepThreads);           // K, block 0
                 tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt, kPrepThreads);   // K, block 1
@@ -334,42 +357,76 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int r = 0; r < 16; ++r) Tf[(o + r) * 65 + o + col] = x[r];
             }
-            for (int e = pt; e < 64 * 64; e += kPrepThreads) {
-                const int r = e >> 6, j = e & 63;
-                if ((j >> 4) > (r >> 4)) Tf[r * 65 + j] = 0.f;
+            else {   // the other prep threads zero the strictly-upper blocks meanwhile
+                for (int e = pt - 64; e < 64 * 64; e += kPrepThreads - 64) {
+                    const int r = e >> 6, j = e & 63;
+                    if ((j >> 4) > (r >> 4)) Tf[r * 65 + j] = 0.f;
+                }
             }
             named_sync(kBarPrep, kPrepThreads);
-            for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                for (int e = pt; e < nb * 256; e += kPrepThreads) {
-                    const int i = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                    const int ro = (i + d) * 16, co = i * 16;
-                    float acc = 0.f;
-                    for (int kb = i; kb < i + d; ++kb)
+            // Below-diagonal blocks, one warp per 16-column block i (warps 0..2):
+            //   T_{R,i} = -T_{R,R} sum_{k=i}^{R-1} A_{R,k} T_{k,i},   R = i+1 .. 3,
+            // each 16x16 product as two m16n8k8 TF32 warp MMAs per 8-wide K step.
+            if (warp < 3) {
+                const int i = warp, g = lane >> 2, t4 = lane & 3;
+                float *X = Xs + 256 * warp;           // 16x16 scratch of this warp
+                for (int R = i + 1; R < 4; ++R) {
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int kk = 16 * i; kk < 16 * R; kk += 8) {
+                        uint32_t a[4];
+                        const float *ar = Af + (16 * R + g) * 65 + kk + t4;
+                        a[0] = to_tf32(ar[0]); a[1] = to_tf32(ar[8 * 65]);
+                        a[2] = to_tf32(ar[4]); a[3] = to_tf32(ar[8 * 65 + 4]);
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk)
-                            acc += Af[(ro + rr) * 65 + kb * 16 + kk] * Tf[(kb * 16 + kk) * 65 + co + cc];
-                    Xs[e] = acc;
-                }
-                named_sync(kBarPrep, kPrepThreads);
-                for (int e = pt; e < nb * 256; e += kPrepThreads) {
-                    const int i = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                    const int ro = (i + d) * 16, co = i * 16;
-                    float acc = 0.f;
+                        for (int nt = 0; nt < 2; ++nt) {
+                            uint32_t bb[2];
+                            const float *br = Tf + (kk + t4) * 65 + 16 * i + 8 * nt + g;
+                            bb[0] = to_tf32(br[0]); bb[1] = to_tf32(br[4 * 65]);
+                            mma_tf32_16x8x8(acc[nt], a, bb);
+                        }
+                    }
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        acc -= Tf[(ro + rr) * 65 + ro + kk] * Xs[(i << 8) + kk * 16 + cc];
-                    Tf[(ro + rr) * 65 + co + cc] = acc;
+                    for (int nt = 0; nt < 2; ++nt) {
+                        X[g * 16 + 8 * nt + 2 * t4] = acc[nt][0];
+                        X[g * 16 + 8 * nt + 2 * t4 + 1] = acc[nt][1];
+                        X[(g + 8) * 16 + 8 * nt + 2 * t4] = acc[nt][2];
+                        X[(g + 8) * 16 + 8 * nt + 2 * t4 + 1] = acc[nt][3];
+                    }
+                    __syncwarp();
+                    float tacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int ks = 0; ks < 16; ks += 8) {
+                        uint32_t a[4];
+                        const float *ar = Tf + (16 * R + g) * 65 + 16 * R + ks + t4;
+                        a[0] = to_tf32(ar[0]); a[1] = to_tf32(ar[8 * 65]);
+                        a[2] = to_tf32(ar[4]); a[3] = to_tf32(ar[8 * 65 + 4]);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            uint32_t bb[2];
+                            bb[0] = to_tf32(X[(ks + t4) * 16 + 8 * nt + g]);
+                            bb[1] = to_tf32(X[(ks + t4 + 4) * 16 + 8 * nt + g]);
+                            mma_tf32_16x8x8(tacc[nt], a, bb);
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float *tr = Tf + (16 * R + g) * 65 + 16 * i + 8 * nt + 2 * t4;
+                        tr[0] = -tacc[nt][0];
+                        tr[1] = -tacc[nt][1];
+                        tr[8 * 65] = -tacc[nt][2];
+                        tr[8 * 65 + 1] = -tacc[nt][3];
+                    }
+                    __syncwarp();
                 }
-                named_sync(kBarPrep, kPrepThreads);
             }
+            named_sync(kBarPrep, kPrepThreads);
 
-            // ---- P6: Tu, Tw rows (fp16): TT = [Tu | Tw] (MN-major B of MMA2, and Tw
-            //      doubles as rows 64..127 of [-P Tw ; Tw]); AV rows 64..127 = Tu
+            // ---- P6: stacked operands AV = [P Tu ; Tu] and AK = [-P Tw ; Tw] (fp16, K-major).
+            //      Rows 64..127 straight from T; rows 0..63 from P T by TF32 warp MMAs
+            //      over 16x16 blocks, (P T)_{R,i} = sum_{k=i..R} P_{R,k} T_{k,i}.
             {
                 const int j = pt & 63;           // row of T
-                const int q4 = pt >> 6;          // which 16-column group
-                const int n0c = 16 * q4;
+                const int n0c = 16 * (pt >> 6);  // 16-column group
                 float vu[16], vw[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -378,41 +435,64 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     vu[i] = t;
                     vw[i] = t * S.eg[n];
                 }
-                st_row16(TT, j, n0c, vu);
-                st_row16(TT + 8192, j, n0c, vw);
                 st_row16(AV, 64 + j, n0c, vu);
+                st_row16(AK, 64 + j, n0c, vw);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(kBarPrep, kPrepThreads);
-            if (issuer) {
-                tc_fence_after();
-                const uint32_t pi_s = smem_u32(PI), tt_s = smem_u32(TT);
-                for (int k = 0; k < kC / 16; ++k)
-                    umma_bf16(tbase + kColDP, kmajor_desc(pi_s, 64, k), mnmajor_desc(tt_s, 64, k), id_m64_n128,
-                              k > 0);
-                umma_commit(&S.bar_pmma);
-            }
-            if (!wait_pmma()) break;
-
-            // ---- P8: P Tu -> AV rows 0..63;  -P Tw -> TT rows 0..63 (so TT = [-P Tw ; Tw]).
-            //      MMA2 is M = 64: row r sits in TMEM lane 32*(r/16) + r%16.
-            {
-                const int r = 16 * (int)quad + (lane & 15);
-                const bool has = lane < 16;
+            if (warp < 7) {
+                // (R, i) output blocks per warp, balanced by k-block count (20 in all).
+                const int g = lane >> 2, t4 = lane & 3;
+                // block codes 4R + i for this warp (-1: none)
+                int code0 = -1, code1 = -1;
+                switch (warp) {
+                case 0: code0 = 12; break;                  // (3,0)
+                case 1: code0 = 8; break;                   // (2,0)
+                case 2: code0 = 13; break;                  // (3,1)
+                case 3: code0 = 4; code1 = 0; break;        // (1,0) (0,0)
+                case 4: code0 = 9; code1 = 5; break;        // (2,1) (1,1)
+                case 5: code0 = 14; code1 = 15; break;      // (3,2) (3,3)
+                default: code0 = 10; break;                 // (2,2)
+                }
+#pragma unroll 1
+                for (int bi = 0; bi < 2; ++bi) {
+                    const int code = bi == 0 ? code0 : code1;
+                    if (code < 0) break;
+                    const int R = code >> 2, i = code & 3;
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int kk = 16 * i; kk < 16 * (R + 1); kk += 8) {
+                        uint32_t a[4];
+                        const float *ar = Pf + (16 * R + g) * 65 + kk + t4;
+                        a[0] = to_tf32(ar[0]); a[1] = to_tf32(ar[8 * 65]);
+                        a[2] = to_tf32(ar[4]); a[3] = to_tf32(ar[8 * 65 + 4]);
 #pragma unroll
-                for (int jj = 0; jj < 64; jj += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + lane_base + kColDP + 64 * half + jj, v);
-                    tmem_ld_wait();
-                    if (has) {
-                        if (half == 0) st_row16(AV, r, jj, v);
-                        else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = -v[i];
-                            st_row16(TT, r, jj, v);
+                        for (int nt = 0; nt < 2; ++nt) {
+                            uint32_t bb[2];
+                            const float *br = Tf + (kk + t4) * 65 + 16 * i + 8 * nt + g;
+                            bb[0] = to_tf32(br[0]); bb[1] = to_tf32(br[4 * 65]);
+                            mma_tf32_16x8x8(acc[nt], a, bb);
                         }
                     }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int rr = 16 * R + g + 8 * hh, cc = 16 * i + 8 * nt + 2 * t4;
+                            const float p0 = acc[nt][2 * hh], p1 = acc[nt][2 * hh + 1];
+                            const float b0 = S.beta[cc], b1 = S.beta[cc + 1];
+                            *reinterpret_cast<uint32_t *>(AV + sw128_offset(rr, cc)) = pack_h2(p0 * b0, p1 * b1);
+                            *reinterpret_cast<uint32_t *>(AK + sw128_offset(rr, cc)) =
+                                pack_h2(-p0 * b0 * S.eg[cc], -p1 * b1 * S.eg[cc + 1]);
+                        }
+                }
+            } else {
+                // warp 7: the strictly-upper 16x16 blocks of rows 0..63 are zero
+                for (int e = lane; e < 6 * 16 * 2 * 2; e += 32) {
+                    const int blkid = e / 64, rem = e % 64;          // 6 blocks x 16 rows x 2 halves x 2 tiles
+                    // (R, i) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                    const int R = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
+                    const int i = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
+                    const int rr = 16 * R + (rem >> 2), cc = 16 * i + 8 * ((rem >> 1) & 1);
+                    uint8_t *dst = (rem & 1) ? AK : AV;
+                    *reinterpret_cast<uint4 *>(dst + sw128_offset(rr, cc)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
@@ -424,7 +504,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (c >= 2 && !prep_vote(mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs))) break;
             if (issuer) {
                 tc_fence_after();
-                const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(TT);
+                const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(AK);
                 for (int k = 0; k < kC / 16; ++k)
                     umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(av_s, 128, k), mnmajor_desc(v_s, 64, k),
                               id_m128_n64_mn, k > 0);
