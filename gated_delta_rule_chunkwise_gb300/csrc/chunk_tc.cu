@@ -225,11 +225,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             named_sync(kBarPrep, kPrepThreads);
             return S.fail == 0;
         };
+        // MMA-completion and hand-off barriers: one thread polls, the others
+        // block in the role's named barrier; tcgen05 ordering follows the sync.
         auto wait_pmma = [&]() -> bool {
-            const bool ok = mbar_wait(&S.bar_pmma, pphase, kWaitNs);
+            const bool ok = (pt == 0) ? mbar_wait(&S.bar_pmma, pphase, kWaitNs) : true;
             pphase ^= 1u;
+            const bool r = prep_vote(ok);
             tc_fence_after();
-            return prep_vote(ok);
+            return r;
         };
         const uint32_t id_m128_n64 = idesc_f16kind_f32(128, 64, 0, 0, kMmaBF16);   // MMA1 (bf16)
         const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16); // MMA3
@@ -501,7 +504,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
             // ---- P9: MMA3 [P Tu ; Tu] V -> RV[s] (once the serial warps released it),
             //      MMA4 [-P Tw ; Tw] K -> DK
-            if (c >= 2 && !prep_vote(mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs))) break;
+            if (c >= 2 && !prep_vote(pt == 0 ? mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs) : true))
+                break;
             if (issuer) {
                 tc_fence_after();
                 const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(AK);
@@ -517,7 +521,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
             // ---- P10: A5 = [Q~ ; -W] (after the serial MMA5 of chunk c-1 has read A5):
             //      DK rows 0..63 = -P W, rows 64..127 = W.
-            if (c >= 1 && !prep_vote(mbar_wait(&S.bar_a5free, (c - 1) & 1, kWaitNs))) break;
+            if (c >= 1 && !prep_vote(pt == 0 ? mbar_wait(&S.bar_a5free, (c - 1) & 1, kWaitNs) : true)) break;
             {
                 const bool top = row < 64;
                 const int r = top ? row : row - 64;
@@ -559,10 +563,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             return S.fail == 0;
         };
         auto wait_smma = [&]() -> bool {
-            const bool ok = mbar_wait(&S.bar_smma, sphase, kWaitNs);
+            const bool ok = (st == 0) ? mbar_wait(&S.bar_smma, sphase, kWaitNs) : true;
             sphase ^= 1u;
+            const bool r = serial_vote(ok);
             tc_fence_after();
-            return serial_vote(ok);
+            return r;
         };
         int pending[2] = {-1, -1};
         auto issue_load = [&](int c) {
@@ -604,7 +609,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t k_s = smem_u32(QK) + 8192;
 
             // ---- S1: chunk c prepared
-            if (!serial_vote(mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs))) break;
+            if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
+            tc_fence_after();
             const float gC = S.gC[s];
             const float egc = (st >= 64) ? S.egc[s][st - 64] : 0.f;
 
