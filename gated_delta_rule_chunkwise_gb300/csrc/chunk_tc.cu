@@ -170,7 +170,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float *S_final, int T, int H, int dv, int *status)
 {
     extern __shared__ uint8_t dsmem[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
+    // array so that every access below stays a shared-memory access.
+    uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
     Small &S = *reinterpret_cast<Small *>(sm + kOffSmall);
     float *Af = reinterpret_cast<float *>(sm + kOffAf);
     float *Tf = reinterpret_cast<float *>(sm + kOffTf);

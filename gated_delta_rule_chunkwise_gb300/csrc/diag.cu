@@ -23,7 +23,7 @@ diag_umma_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
                  int M, int N, int K, int a_mn, int b_mn, uint32_t fmt, uint32_t tmem_cols, int *status)
 {
     extern __shared__ uint8_t dsmem[];
-    uint8_t *base = (uint8_t *)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);
+    uint8_t *base = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
     uint8_t *As = base;                    // up to 128 x 128 bf16
     uint8_t *Bs = base + 32768;            // up to 256 x 128 bf16
     __shared__ uint64_t bar;

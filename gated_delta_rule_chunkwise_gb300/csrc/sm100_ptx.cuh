@@ -122,10 +122,11 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float *c, const uint32_t *a, con
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).  The
+// non-.aligned form: threads of a warp may arrive from divergent paths.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
