@@ -26,7 +26,7 @@
 //   MMA4 [-P Tw ; Tw] K         M=128                        -> -P W, W
 //   MMA5 RV += [Q~ ; -W] H0     M=128  (serial)              -> O, U
 //   MMA6 K^T U~                 M=128  (serial)              -> state increment
-// and, inside the prep warps, P T by TF32 warp MMAs (block lower-triangular).
+// and, inside the prep warps, P T by fp16 warp MMAs (block lower-triangular).
 // Hand-offs use mbarriers: prep -> serial "chunk ready" (double-buffered
 // MMA3 accumulators), serial -> prep "A5 operand free" (an MMA commit) and
 // "accumulator read"; the serial warps issue the TMA loads of chunk c + 2 as
@@ -34,8 +34,8 @@
 //
 // The unit-lower-triangular inverse is blocked by 16: the diagonal blocks by
 // fp32 substitution on CUDA cores, the blocks below them by block
-// substitution with TF32 warp MMAs (mma.sync m16n8k8, fp32 accumulate), one
-// warp per column block.  Decay ratios are applied as row / column factors
+// substitution with fp16 warp MMAs (mma.sync m16n8k16, fp32 accumulate, ldmatrix
+// operands), one warp per column block.  Decay ratios are applied as row / column factors
 // around the chunk's middle row (e^{g_r - m} * e^{m - g_j}), each factor within e^{60}; chunks
 // whose log-decay span exceeds that use one exponential per entry instead.
 //
@@ -85,11 +85,13 @@ constexpr uint32_t kOffAV = kOffAK + 16384;        // [P Tu ; Tu] K-major 128 x 
 constexpr uint32_t kOffA5 = kOffAV + 16384;        // [Q~ ; -W] K-major 128 x 128        (32 KB)
 constexpr uint32_t kOffHB = kOffA5 + 32768;        // H fp16, MN-major 128 x 64          (16 KB)
 constexpr uint32_t kOffUB = kOffHB + 16384;        // U~ fp16, MN-major 64 x 64          (8 KB)
-constexpr uint32_t kOffAf = kOffUB + 8192;         // fp32 A [64][65]
-constexpr uint32_t kOffTf = kOffAf + 64 * 65 * 4;  // fp32 T [64][65]
-constexpr uint32_t kOffPf = kOffTf + 64 * 65 * 4;  // fp32 P [64][65]
-constexpr uint32_t kOffX = kOffPf + 64 * 65 * 4;   // fp32 block-inverse scratch [3][256]
-constexpr uint32_t kOffSmall = kOffX + 3 * 256 * 4;
+constexpr int kLd16 = 72;                            // fp16 row stride (144 B: ldmatrix conflict-free)
+constexpr uint32_t kOffA16 = kOffUB + 8192;          // fp16 A [64][72]
+constexpr uint32_t kOffP16 = kOffA16 + 64 * kLd16 * 2;  // fp16 P [64][72]
+constexpr uint32_t kOffT16 = kOffP16 + 64 * kLd16 * 2;  // fp16 T [64][72]
+constexpr uint32_t kOffTf = kOffT16 + 64 * kLd16 * 2;   // fp32 T [64][65]
+constexpr uint32_t kOffX = kOffTf + 64 * 65 * 4;     // fp16 16x16 scratch per chain warp [3][16][24]
+constexpr uint32_t kOffSmall = kOffX + 3072;
 constexpr uint32_t kSmemBytes = kOffSmall + 3072 + 1024;
 
 struct Small {
@@ -174,10 +176,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // array so that every access below stays a shared-memory access.
     uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
     Small &S = *reinterpret_cast<Small *>(sm + kOffSmall);
-    float *Af = reinterpret_cast<float *>(sm + kOffAf);
+    __half *A16 = reinterpret_cast<__half *>(sm + kOffA16);
+    __half *P16 = reinterpret_cast<__half *>(sm + kOffP16);
+    __half *T16 = reinterpret_cast<__half *>(sm + kOffT16);
     float *Tf = reinterpret_cast<float *>(sm + kOffTf);
-    float *Xs = reinterpret_cast<float *>(sm + kOffX);
-    float *Pf = reinterpret_cast<float *>(sm + kOffPf);
+    __half *X16 = reinterpret_cast<__half *>(sm + kOffX);
     uint8_t *AK = sm + kOffAK, *AV = sm + kOffAV, *A5 = sm + kOffA5;
     uint8_t *HB = sm + kOffHB, *UB = sm + kOffUB;
 
@@ -337,9 +340,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             v[i] = keep ? (frr * v[i]) * S.fc[j] : 0.f;
                         }
                     }
-                    float *dst = (isP ? Pf : Af) + r * 65 + j0;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[i] = v[i];
+                    uint4 *dst = reinterpret_cast<uint4 *>((isP ? P16 : A16) + r * kLd16 + j0);
+                    dst[0] = make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]),
+                                        pack_h2(v[6], v[7]));
+                    dst[1] = make_uint4(pack_h2(v[8], v[9]), pack_h2(v[10], v[11]), pack_h2(v[12], v[13]),
+                                        pack_h2(v[14], v[15]));
                 }
                 tile_bf16_to_f16(QK + 8192, 8192, pt, kPrepThreads);           // K, block 0
                 tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt, kPrepThreads);   // K, block 1
@@ -355,12 +360,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
                     float acc = (r == col) ? 1.f : 0.f;
+                    const __half *ar = A16 + (o + r) * kLd16 + o;
 #pragma unroll
-                    for (int j = 0; j < r; ++j) acc -= Af[(o + r) * 65 + o + j] * x[j];
+                    for (int j = 0; j < r; ++j) acc -= __half2float(ar[j]) * x[j];
                     x[r] = (r < col) ? 0.f : acc;
                 }
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Tf[(o + r) * 65 + o + col] = x[r];
+                for (int r = 0; r < 16; ++r) {
+                    Tf[(o + r) * 65 + o + col] = x[r];
+                    T16[(o + r) * kLd16 + o + col] = __float2half_rn(x[r]);
+                }
             }
             else {   // the other prep threads zero the strictly-upper blocks meanwhile
                 for (int e = pt - 64; e < 64 * 64; e += kPrepThreads - 64) {
@@ -371,63 +380,53 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             named_sync(kBarPrep, kPrepThreads);
             // Below-diagonal blocks, one warp per 16-column block i (warps 0..2):
             //   T_{R,i} = -T_{R,R} sum_{k=i}^{R-1} A_{R,k} T_{k,i},   R = i+1 .. 3,
-            // each 16x16 product as two m16n8k8 TF32 warp MMAs per 8-wide K step.
+            // each 16x16x16 product as two m16n8k16 fp16 warp MMAs (fp32 accumulate),
+            // operands fetched with ldmatrix (row-major A blocks, transposed B blocks).
             if (warp < 3) {
                 const int i = warp, g = lane >> 2, t4 = lane & 3;
-                float *X = Xs + 256 * warp;           // 16x16 scratch of this warp
+                const int lr = lane & 15, lc = 8 * (lane >> 4);   // ldmatrix row / column of this lane
+                __half *X = X16 + 16 * 24 * warp;                  // 16x16 fp16 scratch, row stride 24
                 for (int R = i + 1; R < 4; ++R) {
                     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int kk = 16 * i; kk < 16 * R; kk += 8) {
-                        uint32_t a[4];
-                        const float *ar = Af + (16 * R + g) * 65 + kk + t4;
-                        a[0] = to_tf32(ar[0]); a[1] = to_tf32(ar[8 * 65]);
-                        a[2] = to_tf32(ar[4]); a[3] = to_tf32(ar[8 * 65 + 4]);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t bb[2];
-                            const float *br = Tf + (kk + t4) * 65 + 16 * i + 8 * nt + g;
-                            bb[0] = to_tf32(br[0]); bb[1] = to_tf32(br[4 * 65]);
-                            mma_tf32_16x8x8(acc[nt], a, bb);
-                        }
+                    for (int kb = i; kb < R; ++kb) {
+                        uint32_t a[4], bq[4];
+                        ldsm_x4(a, A16 + (16 * R + lr) * kLd16 + 16 * kb + lc);
+                        ldsm_x4_trans(bq, T16 + (16 * kb + lr) * kLd16 + 16 * i + lc);
+                        mma_f16_16x8x16(acc[0], a, bq);
+                        mma_f16_16x8x16(acc[1], a, bq + 2);
                     }
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        X[g * 16 + 8 * nt + 2 * t4] = acc[nt][0];
-                        X[g * 16 + 8 * nt + 2 * t4 + 1] = acc[nt][1];
-                        X[(g + 8) * 16 + 8 * nt + 2 * t4] = acc[nt][2];
-                        X[(g + 8) * 16 + 8 * nt + 2 * t4 + 1] = acc[nt][3];
+                        *reinterpret_cast<uint32_t *>(X + g * 24 + 8 * nt + 2 * t4) = pack_h2(acc[nt][0], acc[nt][1]);
+                        *reinterpret_cast<uint32_t *>(X + (g + 8) * 24 + 8 * nt + 2 * t4) =
+                            pack_h2(acc[nt][2], acc[nt][3]);
                     }
                     __syncwarp();
                     float tacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    {
+                        uint32_t a[4], bq[4];
+                        ldsm_x4(a, T16 + (16 * R + lr) * kLd16 + 16 * R + lc);
+                        ldsm_x4_trans(bq, X + lr * 24 + lc);
+                        mma_f16_16x8x16(tacc[0], a, bq);
+                        mma_f16_16x8x16(tacc[1], a, bq + 2);
+                    }
 #pragma unroll
-                    for (int ks = 0; ks < 16; ks += 8) {
-                        uint32_t a[4];
-                        const float *ar = Tf + (16 * R + g) * 65 + 16 * R + ks + t4;
-                        a[0] = to_tf32(ar[0]); a[1] = to_tf32(ar[8 * 65]);
-                        a[2] = to_tf32(ar[4]); a[3] = to_tf32(ar[8 * 65 + 4]);
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t bb[2];
-                            bb[0] = to_tf32(X[(ks + t4) * 16 + 8 * nt + g]);
-                            bb[1] = to_tf32(X[(ks + t4 + 4) * 16 + 8 * nt + g]);
-                            mma_tf32_16x8x8(tacc[nt], a, bb);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int rr = 16 * R + g + 8 * hh, cc = 16 * i + 8 * nt + 2 * t4;
+                            const float t0v = -tacc[nt][2 * hh], t1v = -tacc[nt][2 * hh + 1];
+                            Tf[rr * 65 + cc] = t0v;
+                            Tf[rr * 65 + cc + 1] = t1v;
+                            *reinterpret_cast<uint32_t *>(T16 + rr * kLd16 + cc) = pack_h2(t0v, t1v);
                         }
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        float *tr = Tf + (16 * R + g) * 65 + 16 * i + 8 * nt + 2 * t4;
-                        tr[0] = -tacc[nt][0];
-                        tr[1] = -tacc[nt][1];
-                        tr[8 * 65] = -tacc[nt][2];
-                        tr[8 * 65 + 1] = -tacc[nt][3];
-                    }
                     __syncwarp();
                 }
             }
             named_sync(kBarPrep, kPrepThreads);
 
             // ---- P6: stacked operands AV = [P Tu ; Tu] and AK = [-P Tw ; Tw] (fp16, K-major).
-            //      Rows 64..127 straight from T; rows 0..63 from P T by TF32 warp MMAs
+            //      Rows 64..127 straight from T; rows 0..63 from P T by fp16 warp MMAs
             //      over 16x16 blocks, (P T)_{R,i} = sum_{k=i..R} P_{R,k} T_{k,i}.
             {
                 const int j = pt & 63;           // row of T
@@ -462,19 +461,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const int code = bi == 0 ? code0 : code1;
                     if (code < 0) break;
                     const int R = code >> 2, i = code & 3;
+                    const int lr = lane & 15, lc = 8 * (lane >> 4);
                     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int kk = 16 * i; kk < 16 * (R + 1); kk += 8) {
-                        uint32_t a[4];
-                        const float *ar = Pf + (16 * R + g) * 65 + kk + t4;
-                        a[0] = to_tf32(ar[0]); a[1] = to_tf32(ar[8 * 65]);
-                        a[2] = to_tf32(ar[4]); a[3] = to_tf32(ar[8 * 65 + 4]);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t bb[2];
-                            const float *br = Tf + (kk + t4) * 65 + 16 * i + 8 * nt + g;
-                            bb[0] = to_tf32(br[0]); bb[1] = to_tf32(br[4 * 65]);
-                            mma_tf32_16x8x8(acc[nt], a, bb);
-                        }
+                    for (int kb = i; kb <= R; ++kb) {
+                        uint32_t a[4], bq[4];
+                        ldsm_x4(a, P16 + (16 * R + lr) * kLd16 + 16 * kb + lc);
+                        ldsm_x4_trans(bq, T16 + (16 * kb + lr) * kLd16 + 16 * i + lc);
+                        mma_f16_16x8x16(acc[0], a, bq);
+                        mma_f16_16x8x16(acc[1], a, bq + 2);
                     }
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)

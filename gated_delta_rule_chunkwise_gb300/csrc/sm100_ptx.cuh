@@ -122,6 +122,32 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float *c, const uint32_t *a, con
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// ---------------------------------------------------------------- warp MMA (fp16)
+// Four 8x8 b16 matrices from shared memory; lane l supplies the row address
+// of matrix l / 8.  With .trans each matrix is transposed on the way in.
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, const void *row_addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(row_addr)));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t *r, const void *row_addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(row_addr)));
+}
+// D = A (16x16, row) * B (16x8, col) + C, fp16 inputs, fp32 accumulate
+// (mma.m16n8k16; C/D fragment as in mma_tf32_16x8x8).
+__device__ __forceinline__ void mma_f16_16x8x16(float *c, const uint32_t *a, const uint32_t *b)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).  The
 // non-.aligned form: threads of a warp may arrive from divergent paths.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
