@@ -114,6 +114,8 @@ struct Small {
     float stg_beta[2][kC];    // beta / log-gate of the next chunk, prefetched by cp.async
     float stg_gate[2][kC];
 };
+static_assert(sizeof(Small) <= 3072, "Small does not fit its shared-memory slot");
+static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b)
 {
