@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s chunkwise GDN fwd (H=16,dk=dv=128) + % roofline; decode GB/s"
 WORKLOAD = "gdn_bf16_b4_t2048_h16_d128"
+EXTRA_WORKLOADS = ("kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
+                   "gdn_bf16_long_b1_t65536_h16_d128", "deltanet_fp32_b1_t256_h1_d64")
 DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000")
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
@@ -349,6 +351,43 @@ def run_ours(args):
                "d2h_bytes_per_step": d2h, "ms_per_step": ems}
         del host, out_h, sf_h
 
+    # ---------------- the other chunkwise workloads (secondary lines) ----------------
+    others = None
+    if not args.no_extra:
+        others = {}
+        for name in EXTRA_WORKLOADS:
+            ow = wl.make_chunk(name, seed=rank)
+            ot = ow.torch_inputs("cuda")
+            oel = 2 if ow.dtype == "bf16" else 4
+            oout = torch.empty((ow.B, ow.T, ow.H, ow.dv), dtype=ot["q"].dtype, device="cuda")
+            osf = torch.empty((ow.B, ow.H, ow.dk, ow.dv), dtype=torch.float32, device="cuda")
+            optr = (P(ot["q"]), P(ot["k"]), P(ot["v"]), P(ot["beta"]), P(ot["gate"]), P(ot["S0"]), P(oout), P(osf))
+            odt = ldn.LDN_BF16 if ow.dtype == "bf16" else ldn.LDN_F32
+
+            def ostep():
+                st_ = ldn.ldn_chunk_fwd(*optr, ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt, sh)
+                if st_ != ldn.LDN_OK:
+                    raise ldn.LdnError(st_, "ldn_chunk_fwd")
+
+            ostep()
+            oev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+            for e0, e1 in oev:
+                flush_l2()
+                e0.record(stream)
+                ostep()
+                e1.record(stream)
+            barrier()
+            launches += 4
+            oms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in oev))
+            ob = chunk_bytes(ow.B, ow.T, ow.H, ow.dk, ow.dv, oel, ow.mode, ow.S0 is not None, True)
+            kern = "tcgen05" if ldn.ldn_chunk_fwd_select(ow.dk, ow.dv, 64, ow.mode, odt) == ldn.LDN_VARIANT_TENSOR else "simt"
+            others[name] = {"tokens_per_s": world * ow.B * ow.T / (oms / 1e3), "ms_per_launch": oms,
+                            "kernel": f"chunk_{kern}", "algorithmic_bytes": ob,
+                            "hbm_frac": ob / (oms / 1e3) / 1e9 / hbm_peak}
+            del ot, oout, osf
+        if ldn.device_status() != ldn.LDN_OK:
+            raise RuntimeError("other workloads: device status not ok")
+
     # ---------------- decode step (bandwidth) ----------------
     decode = None
     if not args.no_decode:
@@ -412,6 +451,7 @@ def run_ours(args):
                        "l2": "flushed before every timed launch (512 MiB write, then 512 MiB read of another buffer: cold and clean)",
                        "parallelism": f"replica x{world} (independent sequences per GPU)"},
             "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
+            "other_workloads": others,
             "wall_s_timed_region": wall, "decode": decode}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -438,6 +478,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workload lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

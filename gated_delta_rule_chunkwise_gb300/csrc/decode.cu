@@ -11,39 +11,50 @@
 // Decay before the error follows the linear-attention notes, Sec. 2.4 Eqs.
 // 15-17; the KDA decay acts on the key rows of H (Sec. 2.5, Eqs. 18-20).
 //
-// Work split: one CTA per (b, h, 64-column slice of dv).  Columns are
-// independent (each value channel is its own linear system, state-reduction
-// notes Sec. 2.5), so slices need no communication.  128 threads: 16 threads
-// cover one 256-byte row of the slice with float4 loads, 8 row groups stride
-// over dk, and each thread keeps its dk/8 float4 of H' in registers between
-// the read pass and the write pass, so H is read once and written once.
+// Work split: one CTA of 128 threads per (b, h, DVC-column slice of dv).
+// Columns are independent (each value channel is its own linear system,
+// state-reduction notes Sec. 2.5), so slices need no communication.  A row of
+// the slice is covered by DVC/4 threads with float4 accesses; the row groups
+// stride over dk and each thread keeps its 16 float4 of H' in registers
+// between the read pass and the write pass, so H is read once and written
+// once.  DVC = 64 for dk = 128 and 128 for dk = 64, i.e. 32 KiB of state per
+// CTA either way (enough bytes in flight per thread to stream at HBM rate).
 #include "ldn_internal.cuh"
 
 namespace ldn {
 namespace {
 
 constexpr int kDecThreads = 128;
-constexpr int kDecCols = 64;                   // dv columns per CTA
-constexpr int kTPR = kDecCols / 4;             // threads per row (float4 each)
-constexpr int kRowsPerPass = kDecThreads / kTPR;
 
-template <int DK, typename TIn, int MODE>
+template <int DK, int DVC, typename TIn, int MODE>
 __global__ void __launch_bounds__(kDecThreads)
 decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
               const float *__restrict__ beta, const float *__restrict__ gate,
               float *__restrict__ S, TIn *__restrict__ out, int dv)
 {
-    constexpr int RPT = DK / kRowsPerPass;     // rows held per thread
+    constexpr int TPR = DVC / 4;               // threads per row (float4 each)
+    constexpr int RP = kDecThreads / TPR;      // rows per pass
+    constexpr int RPT = DK / RP;               // rows held per thread
     __shared__ float qs[DK], ks[DK], as[DK];
-    __shared__ __align__(16) float red_p[kRowsPerPass][kDecCols];
-    __shared__ __align__(16) float red_s[kRowsPerPass][kDecCols];
-    __shared__ __align__(16) float rs[kDecCols];
+    __shared__ __align__(16) float red_p[RP][DVC];
+    __shared__ __align__(16) float red_s[RP][DVC];
+    __shared__ __align__(16) float rs[DVC];
     __shared__ float kq_part[kDecThreads / 32];
 
-    const int slices = dv / kDecCols;
+    const int slices = dv / DVC;
     const int unit = blockIdx.x / slices;      // (b, h) pair, b * H + h
-    const int col0 = (blockIdx.x % slices) * kDecCols;
+    const int col0 = (blockIdx.x % slices) * DVC;
     const int tid = threadIdx.x;
+
+    const int cg = tid % TPR;                  // float4 column group
+    const int rg = tid / TPR;                  // first row of this thread
+    float *Sbase = S + (size_t)unit * DK * dv + col0 + 4 * cg;
+
+    // Issue the state loads first: they are the stream; q/k/gates are small.
+    float4 h[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+        h[i] = *reinterpret_cast<const float4 *>(Sbase + (size_t)(rg + i * RP) * dv);
 
     float kq = 0.0f;
     if (tid < DK) {
@@ -60,19 +71,10 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
     const float alpha = (MODE == LDN_GDN) ? expf(gate[unit]) : 1.0f;
     __syncthreads();
 
-    const int cg = tid % kTPR;                 // float4 column group
-    const int rg = tid / kTPR;                 // first row of this thread
-    float *Sbase = S + (size_t)unit * DK * dv + col0 + 4 * cg;
-
-    float4 h[RPT];
-#pragma unroll
-    for (int i = 0; i < RPT; ++i)
-        h[i] = *reinterpret_cast<const float4 *>(Sbase + (size_t)(rg + i * kRowsPerPass) * dv);
-
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), s = p;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const int row = rg + i * kRowsPerPass;
+        const int row = rg + i * RP;
         const float d = (MODE == LDN_KDA) ? as[row] : alpha;
         if (MODE != LDN_DELTANET) { h[i].x *= d; h[i].y *= d; h[i].z *= d; h[i].w *= d; }
         const float kr = ks[row], qr = qs[row];
@@ -83,10 +85,10 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
     *reinterpret_cast<float4 *>(&red_s[rg][4 * cg]) = s;
     __syncthreads();
 
-    if (tid < kDecCols) {
+    if (tid < DVC) {
         float pp = 0.f, ss = 0.f, kqt = 0.f;
 #pragma unroll
-        for (int g = 0; g < kRowsPerPass; ++g) { pp += red_p[g][tid]; ss += red_s[g][tid]; }
+        for (int g = 0; g < RP; ++g) { pp += red_p[g][tid]; ss += red_s[g][tid]; }
 #pragma unroll
         for (int w = 0; w < kDecThreads / 32; ++w) kqt += kq_part[w];
         const size_t vi = (size_t)unit * dv + col0 + tid;
@@ -99,40 +101,46 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
     const float4 r4 = *reinterpret_cast<const float4 *>(&rs[4 * cg]);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const float kr = ks[rg + i * kRowsPerPass];
+        const float kr = ks[rg + i * RP];
         float4 o = h[i];
         o.x += kr * r4.x; o.y += kr * r4.y; o.z += kr * r4.z; o.w += kr * r4.w;
-        *reinterpret_cast<float4 *>(Sbase + (size_t)(rg + i * kRowsPerPass) * dv) = o;
+        *reinterpret_cast<float4 *>(Sbase + (size_t)(rg + i * RP) * dv) = o;
     }
 }
 
-template <int DK, typename TIn>
-cudaError_t launch_dk(const DecodeArgs &a, cudaStream_t st)
+template <int DK, int DVC, typename TIn>
+cudaError_t launch_cfg(const DecodeArgs &a, cudaStream_t st)
 {
-    const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDecCols));
+    const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / DVC));
     const TIn *q = (const TIn *)a.q, *k = (const TIn *)a.k, *v = (const TIn *)a.v;
     TIn *o = (TIn *)a.out;
     switch (a.mode) {
     case LDN_DELTANET:
-        decode_kernel<DK, TIn, LDN_DELTANET><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        decode_kernel<DK, DVC, TIn, LDN_DELTANET><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
         break;
     case LDN_GDN:
-        decode_kernel<DK, TIn, LDN_GDN><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        decode_kernel<DK, DVC, TIn, LDN_GDN><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
         break;
     default:
-        decode_kernel<DK, TIn, LDN_KDA><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        decode_kernel<DK, DVC, TIn, LDN_KDA><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
         break;
     }
     return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st)
+{
+    if (a.dk == 128) return launch_cfg<128, 64, TIn>(a, st);
+    // dk = 64: 128-column slices when dv allows (dv is 64 or 128)
+    return a.dv % 128 == 0 ? launch_cfg<64, 128, TIn>(a, st) : launch_cfg<64, 64, TIn>(a, st);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st)
 {
-    if (a.dtype == LDN_BF16)
-        return a.dk == 128 ? launch_dk<128, __nv_bfloat16>(a, st) : launch_dk<64, __nv_bfloat16>(a, st);
-    return a.dk == 128 ? launch_dk<128, float>(a, st) : launch_dk<64, float>(a, st);
+    return a.dtype == LDN_BF16 ? launch_t<__nv_bfloat16>(a, st) : launch_t<float>(a, st);
 }
 
 }  // namespace ldn
