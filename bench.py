@@ -147,6 +147,26 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+# multi-rank host logic (one process per GPU; no data-path collective)
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own independent sequences: the workload is sharded
+    by batch (weak scaling), rank r uses seed r."""
+    return int(rank)
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the timed region is as slow as
+    the slowest rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
 def run_reference(args):
     """fp64 CPU oracle, timed on this host's cores over a bounded sample."""
     rank = int(os.environ.get("RANK", "0"))
@@ -240,11 +260,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, world, "cuda")
 
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
@@ -260,7 +276,7 @@ def run_ours(args):
         flush_r.sum()
 
     # ---------------- chunk forward (the headline) ----------------
-    w = wl.make_chunk(args.workload, seed=rank)
+    w = wl.make_chunk(args.workload, seed=rank_seed(rank))
     t = w.torch_inputs("cuda")
     el = 2 if w.dtype == "bf16" else 4
     dtype_code = ldn.LDN_BF16 if w.dtype == "bf16" else ldn.LDN_F32

@@ -51,6 +51,7 @@ _SIGNATURES = {
     "ldn_version": ([], _I),
     "ldn_diag_umma": ([_P] * 3 + [_I] * 6 + [_P], _I),
     "ldn_diag_tma_sw128": ([_P] * 2 + [_I] * 4 + [_P], _I),
+    "ldn_diag_wait_timeout": ([ctypes.c_longlong, _P, _P], _I),
 }
 EXPORTS = tuple(_SIGNATURES)
 
@@ -114,6 +115,10 @@ def ldn_diag_umma(A, B, D, M, N, K, a_mn, b_mn, fmt, stream):
 
 def ldn_diag_tma_sw128(src, dst, rows, cols, row0, col0, stream):
     return load().ldn_diag_tma_sw128(src, dst, rows, cols, row0, col0, stream)
+
+
+def ldn_diag_wait_timeout(timeout_ns, waited_ok, stream):
+    return load().ldn_diag_wait_timeout(timeout_ns, waited_ok, stream)
 
 
 # --- torch-tensor convenience layer ---------------------------------------

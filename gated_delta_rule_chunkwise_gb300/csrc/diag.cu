@@ -118,10 +118,36 @@ diag_tma_kernel(const __grid_constant__ CUtensorMap map, uint8_t *__restrict__ o
         reinterpret_cast<uint4 *>(out)[i] = reinterpret_cast<const uint4 *>(tile)[i];
 }
 
+// A bounded wait on an mbarrier that nothing ever arrives on: the kernel must
+// give up after `timeout_ns`, record LDN_ERR_TIMEOUT and return normally.
+__global__ void diag_timeout_kernel(uint64_t timeout_ns, int *status, int *waited_ok)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(&bar, 0, timeout_ns);   // phase 0 never completes
+    if (threadIdx.x == 0) {
+        *waited_ok = ok ? 1 : 0;
+        if (!ok) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+    }
+}
+
 }  // namespace
 }  // namespace ldn
 
 using namespace ldn;
+
+extern "C" int ldn_diag_wait_timeout(long long timeout_ns, int *waited_ok, void *stream)
+{
+    if (!waited_ok || timeout_ns < 0 || timeout_ns > 2000000000LL) return LDN_ERR_INVALID_ARG;
+    int *sw = status_word_ptr();
+    if (!sw) return LDN_ERR_CUDA;
+    diag_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)timeout_ns, sw, waited_ok);
+    return cudaGetLastError() == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
 
 extern "C" int ldn_diag_umma(const void *A, const void *B, float *D, int M, int N, int K, int a_mn, int b_mn, int fmt,
                              void *stream)

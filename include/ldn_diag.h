@@ -35,6 +35,15 @@ int ldn_diag_umma(const void *A, const void *B, float *D_out, int M, int N, int 
  */
 int ldn_diag_tma_sw128(const void *src, void *dst, int rows, int cols, int row0, int col0, void *stream);
 
+/*
+ * Failure-path check of the bounded waits every kernel uses: one CTA waits on
+ * an mbarrier that nothing arrives on, gives up after timeout_ns (at most 2 s),
+ * sets LDN_ERR_TIMEOUT in the status word and returns normally, leaving the
+ * context usable.  *waited_ok (device int) receives 1 if the wait succeeded,
+ * 0 if it timed out.
+ */
+int ldn_diag_wait_timeout(long long timeout_ns, int *waited_ok, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
