@@ -23,14 +23,18 @@
 // Contractions (tcgen05.mma, fp16 operands, fp32 TMEM accumulators):
 //   MMA1 [Q ; K] K^T            M=128  bf16 tiles as loaded  -> P_raw, K K^T
 //   MMA3 [P Tu ; Tu] V          M=128                        -> P U', U'
-//   MMA4 [-P Tw ; Tw] K         M=128                        -> -P W, W
+//   MMA4 [-P Tw ; Tw] K         M=128  (double-buffered)     -> -P W, W
 //   MMA5 RV += [Q~ ; -W] H0     M=128  (serial)              -> O, U
 //   MMA6 K^T U~                 M=128  (serial)              -> state increment
 // and, inside the prep warps, P T by fp16 warp MMAs (block lower-triangular).
-// Hand-offs use mbarriers: prep -> serial "chunk ready" (double-buffered
-// MMA3 accumulators), serial -> prep "A5 operand free" (an MMA commit) and
-// "accumulator read"; the serial warps issue the TMA loads of chunk c + 2 as
-// soon as the state step of chunk c has released its tiles.
+// Hand-offs use mbarriers: prep -> serial "chunk ready" is the commit of
+// MMA3 / MMA4 itself (both accumulators double-buffered in TMEM), serial ->
+// prep "accumulators read".  The serial warps form the MMA5 operand
+// [Q~ ; -W] from the MMA4 accumulator (they are idle most of a chunk, the
+// prep warps are not), and issue the TMA loads of chunk c + 2 as soon as the
+// state step of chunk c has released its tiles.  The prep warps need no wait
+// for MMA3 / MMA4: the commit of the next chunk's MMA1, which they wait on
+// anyway, also covers the earlier MMAs of the same issuing thread.
 //
 // The unit-lower-triangular inverse is blocked by 16: the diagonal blocks by
 // fp32 substitution on CUDA cores, the blocks below them by block
@@ -68,7 +72,8 @@ constexpr float kMaxLogSpan = 60.f;                // factored decay limit (e^60
 
 // TMEM columns (fp32, 128 lanes).
 constexpr uint32_t kColD1 = 0;      // 64   MMA1
-constexpr uint32_t kColDK = 192;    // 128  MMA4
+constexpr uint32_t kColDK1 = 64;    // 128  MMA4, stage 1
+constexpr uint32_t kColDK0 = 192;   // 128  MMA4, stage 0
 constexpr uint32_t kColRV = 320;    // 2 x 64  MMA3 / MMA5 (double-buffered)
 constexpr uint32_t kColD6 = 448;    // 64   MMA6
 constexpr uint32_t kTmemCols = 512;
@@ -92,15 +97,16 @@ constexpr uint32_t kOffT16 = kOffP16 + 64 * kLd16 * 2;  // fp16 T [64][72]
 constexpr uint32_t kOffTf = kOffT16 + 64 * kLd16 * 2;   // fp32 T [64][65]
 constexpr uint32_t kOffX = kOffTf + 64 * 65 * 4;     // fp16 16x16 scratch per chain warp [3][16][24]
 constexpr uint32_t kOffSmall = kOffX + 3072;
-constexpr uint32_t kSmemBytes = kOffSmall + 3072 + 1024;
+constexpr uint32_t kSmallBytes = 4096;
+constexpr uint32_t kSmemBytes = kOffSmall + kSmallBytes + 1024;
 
 struct Small {
     uint64_t bar_load[2];     // TMA tiles of stage s landed
     uint64_t bar_pmma;        // prep MMA commits
     uint64_t bar_smma;        // serial MMA commits
-    uint64_t bar_ready[2];    // prep -> serial: chunk in RV[s] / A5 ready
-    uint64_t bar_a5free;      // serial MMA5 finished reading A5
-    uint64_t bar_rvfree[2];   // serial finished reading RV[s]
+    uint64_t bar_ready[2];    // MMA3 / MMA4 of stage s complete (prep commit)
+    uint64_t bar_rvfree[2];   // serial finished reading RV[s] and DK[s]
+    uint64_t bar_drain[2];    // failure path: last commit of each MMA issuer
     uint32_t tmem_base;
     int fail;
     int exact;                // per-entry exponentials for this chunk
@@ -108,13 +114,13 @@ struct Small {
     float g[kC];              // inclusive log-decay prefix
     float fr[kC];             // e^{g_r - m}
     float fc[kC];             // e^{m - g_j}
-    float eg[kC];             // e^{g_r}
+    float eg[2][kC];          // e^{g_r}, per stage (also read by the serial warps)
     float egc[2][kC];         // e^{g_C - g_r}, per stage (read by the serial warps)
     float gC[2];              // e^{g_C}, per stage
     float stg_beta[2][kC];    // beta / log-gate of the next chunk, prefetched by cp.async
     float stg_gate[2][kC];
 };
-static_assert(sizeof(Small) <= 3072, "Small does not fit its shared-memory slot");
+static_assert(sizeof(Small) <= kSmallBytes, "Small does not fit its shared-memory slot");
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b)
@@ -202,7 +208,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&S.bar_smma, 1);
         mbar_init(&S.bar_ready[0], 1);
         mbar_init(&S.bar_ready[1], 1);
-        mbar_init(&S.bar_a5free, 1);
+        mbar_init(&S.bar_drain[0], 1);
+        mbar_init(&S.bar_drain[1], 1);
         mbar_init(&S.bar_rvfree[0], 1);
         mbar_init(&S.bar_rvfree[1], 1);
         fence_mbar_init();
@@ -219,6 +226,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
+    int pending[2] = {-1, -1};   // chunk whose TMA loads were last issued into stage s (serial thread 0)
 
     if (tid < kPrepThreads) {
         // ============================== PREP ==============================
@@ -298,7 +306,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (MODE == LDN_GDN) {
                     S.fr[r0] = expf(g0 - m); S.fr[r1] = expf(g1 - m);
                     S.fc[r0] = expf(m - g0); S.fc[r1] = expf(m - g1);
-                    S.eg[r0] = expf(g0); S.eg[r1] = expf(g1);
+                    S.eg[s][r0] = expf(g0); S.eg[s][r1] = expf(g1);
                     S.egc[s][r0] = expf(gc - g0); S.egc[s][r1] = expf(gc - g1);
                     if (lane == 0) {
                         S.gC[s] = expf(gc);
@@ -306,7 +314,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 } else {
                     S.fr[r0] = S.fr[r1] = S.fc[r0] = S.fc[r1] = 1.f;
-                    S.eg[r0] = S.eg[r1] = 1.f;
+                    S.eg[s][r0] = S.eg[s][r1] = 1.f;
                     S.egc[s][r0] = S.egc[s][r1] = 1.f;
                     if (lane == 0) { S.gC[s] = 1.f; S.exact = 0; }
                 }
@@ -439,7 +447,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const int n = n0c + i;
                     const float t = Tf[j * 65 + n] * S.beta[n];
                     vu[i] = t;
-                    vw[i] = t * S.eg[n];
+                    vw[i] = t * S.eg[s][n];
                 }
                 st_row16(AV, 64 + j, n0c, vu);
                 st_row16(AK, 64 + j, n0c, vw);
@@ -481,7 +489,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             const float b0 = S.beta[cc], b1 = S.beta[cc + 1];
                             *reinterpret_cast<uint32_t *>(AV + sw128_offset(rr, cc)) = pack_h2(p0 * b0, p1 * b1);
                             *reinterpret_cast<uint32_t *>(AK + sw128_offset(rr, cc)) =
-                                pack_h2(-p0 * b0 * S.eg[cc], -p1 * b1 * S.eg[cc + 1]);
+                                pack_h2(-p0 * b0 * S.eg[s][cc], -p1 * b1 * S.eg[s][cc + 1]);
                         }
                 }
             } else {
@@ -500,8 +508,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_before();
             named_sync(kBarPrep, kPrepThreads);
 
-            // ---- P9: MMA3 [P Tu ; Tu] V -> RV[s] (once the serial warps released it),
-            //      MMA4 [-P Tw ; Tw] K -> DK
+            // ---- P9: MMA3 [P Tu ; Tu] V -> RV[s], MMA4 [-P Tw ; Tw] K -> DK[s] (once the
+            //      serial warps have read both accumulators of chunk c - 2); their
+            //      commit is the serial warps' "chunk ready".
             if (c >= 2 && !prep_vote(pt == 0 ? mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs) : true))
                 break;
             if (issuer) {
@@ -511,45 +520,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(av_s, 128, k), mnmajor_desc(v_s, 64, k),
                               id_m128_n64_mn, k > 0);
                 for (int k = 0; k < kC / 16; ++k)
-                    umma_bf16(tbase + kColDK, kmajor_desc(ak_s, 128, k), mnmajor_desc(k_s, 128, k),
-                              id_m128_n128_mn, k > 0);
-                umma_commit(&S.bar_pmma);
+                    umma_bf16(tbase + (s ? kColDK1 : kColDK0), kmajor_desc(ak_s, 128, k),
+                              mnmajor_desc(k_s, 128, k), id_m128_n128_mn, k > 0);
+                umma_commit(&S.bar_ready[s]);
             }
-            if (!wait_pmma()) break;
-
-            // ---- P10: A5 = [Q~ ; -W] (after the serial MMA5 of chunk c-1 has read A5):
-            //      DK rows 0..63 = -P W, rows 64..127 = W.
-            if (c >= 1 && !prep_vote(pt == 0 ? mbar_wait(&S.bar_a5free, (c - 1) & 1, kWaitNs) : true)) break;
-            {
-                const bool top = row < 64;
-                const int r = top ? row : row - 64;
-                const float er = S.eg[r];
-#pragma unroll
-                for (int cc = 0; cc < 64; cc += 16) {
-                    const int c0 = 64 * half + cc;
-                    float v[16];
-                    tmem_ld16(tbase + lane_base + kColDK + c0, v);
-                    tmem_ld_wait();
-                    uint8_t *blk = A5 + half * 16384;
-                    if (top) {
-                        float qv[16];
-                        const uint8_t *qblk = QK + half * 16384;   // Q rows 0..63 (bf16)
-                        ld_row8_bf16(qblk, r, cc, qv);
-                        ld_row8_bf16(qblk, r, cc + 8, qv + 8);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] += er * qv[i];
-                        st_row16(blk, r, cc, v);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = -v[i];
-                        st_row16(blk, 64 + r, cc, v);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(kBarPrep, kPrepThreads);
-            if (pt == 0) mbar_arrive(&S.bar_ready[s]);
         }
     } else {
         // ============================== SERIAL ==============================
@@ -567,7 +541,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_after();
             return r;
         };
-        int pending[2] = {-1, -1};
         auto issue_load = [&](int c) {
             const int s = c & 1;
             uint8_t *qk = sm + (s ? kOffQK1 : kOffQK0);
@@ -606,13 +579,51 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint8_t *QK = sm + (s ? kOffQK1 : kOffQK0);
             const uint32_t k_s = smem_u32(QK) + 8192;
 
-            // ---- S1: chunk c prepared
+            // ---- S1: MMA3 / MMA4 of chunk c complete (RV[s] = [P U' ; U'], DK[s] = [-P W ; W])
             if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
             tc_fence_after();
             const float gC = S.gC[s];
-            const float egc = (st >= 64) ? S.egc[s][st - 64] : 0.f;
+            const bool top = st < 64;
+            const float egc = top ? 0.f : S.egc[s][st - 64];
 
-            // ---- S2: MMA5: RV[s] += [Q~ ; -W] H0  -> O (rows 0..63), U (rows 64..127)
+            // ---- S2: A5 = [Q~ ; -W] (row st): Q~ = Diag(e^{g}) Q - P W on the top rows
+            //      (Q read from the bf16 tile as loaded), -W on the bottom rows.  The
+            //      previous MMA5, the only reader of A5, completed in the last step.
+            {
+                const float er = top ? S.eg[s][st] : 0.f;
+                const uint32_t dk_col = tbase + lane_base + (s ? kColDK1 : kColDK0);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    uint8_t *blk = A5 + kb * 16384;
+                    const uint8_t *qblk = QK + kb * 16384;   // Q rows 0..63 of this column block
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 32) {
+                        float v[32];
+                        tmem_ld16(dk_col + 64 * kb + cc, v);
+                        tmem_ld16(dk_col + 64 * kb + cc + 16, v + 16);
+                        tmem_ld_wait();
+                        if (top) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                float qv[8];
+                                ld_row8_bf16(qblk, st, cc + j, qv);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) v[j + i] += er * qv[i];
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = -v[i];
+                        }
+                        st_row16(blk, st, cc, v);
+                        st_row16(blk, st, cc + 16, v + 16);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarSerial, kSerialThreads);
+
+            // ---- S3: MMA5: RV[s] += [Q~ ; -W] H0  -> O (rows 0..63), U (rows 64..127)
             if (st == 0) {
                 tc_fence_after();
                 const uint32_t a5_s = smem_u32(A5), hb_s = smem_u32(HB);
@@ -620,13 +631,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(a5_s, 128, k), mnmajor_desc(hb_s, 128, k),
                               id_m128_n64_mn, 1);
                 umma_commit(&S.bar_smma);
-                umma_commit(&S.bar_a5free);
             }
             if (!wait_smma()) break;
 
-            // ---- S3: O -> global (bf16); U~ = Diag(e^{g_C - g}) U -> UB
+            // ---- S4: O -> global (bf16); U~ = Diag(e^{g_C - g}) U -> UB
             {
-                const bool top = st < 64;
                 const int r = top ? st : st - 64;
 #pragma unroll
                 for (int n = 0; n < kDVS; n += 16) {
@@ -654,7 +663,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             named_sync(kBarSerial, kSerialThreads);
             if (st == 0) {
                 mbar_arrive(&S.bar_rvfree[s]);
-                // ---- S4: MMA6: K^T U~ -> D6
+                // ---- S5: MMA6: K^T U~ -> D6
                 tc_fence_after();
                 const uint32_t ub_s = smem_u32(UB);
                 for (int k = 0; k < kC / 16; ++k)
@@ -666,7 +675,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // the tiles of stage s are no longer read by anyone: fetch chunk c + 2 into them
             if (st == 0 && c + 2 < nchunks) issue_load(c + 2);
 
-            // ---- S5: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
+            // ---- S6: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
 #pragma unroll
             for (int n = 0; n < kDVS; n += 16) {
                 float v[16];
@@ -684,29 +693,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             named_sync(kBarSerial, kSerialThreads);
         }
 
-        if (S.fail == 0) {
-            if (S_final) {
-                float *dst = S_final + ((size_t)unit * kDK + st) * dv + n0;
+        if (S.fail == 0 && S_final) {
+            float *dst = S_final + ((size_t)unit * kDK + st) * dv + n0;
 #pragma unroll
-                for (int n = 0; n < kDVS; n += 4)
-                    *reinterpret_cast<float4 *>(dst + n) =
-                        make_float4(Hreg[n], Hreg[n + 1], Hreg[n + 2], Hreg[n + 3]);
-            }
-        } else if (st == 0) {
-            // Drain this role's in-flight TMA loads and MMAs (bounded) before
-            // shared memory and TMEM are released.
-            for (int s = 0; s < 2; ++s)
-                if (pending[s] >= 0) mbar_wait(&S.bar_load[s], (pending[s] >> 1) & 1, kWaitNs / 4);
-            mbar_wait(&S.bar_smma, sphase ^ 1u, kWaitNs / 4);
+            for (int n = 0; n < kDVS; n += 4)
+                *reinterpret_cast<float4 *>(dst + n) = make_float4(Hreg[n], Hreg[n + 1], Hreg[n + 2], Hreg[n + 3]);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && S.fail) {
-        atomicOr(status, 1 << LDN_ERR_TIMEOUT);
-        mbar_wait(&S.bar_pmma, 0, kWaitNs / 8);   // best effort: a prep MMA may still be in flight
-        mbar_wait(&S.bar_pmma, 1, kWaitNs / 8);
+    if (S.fail) {
+        // Drain the in-flight MMAs of both issuers and the TMA loads (bounded)
+        // before shared memory and TMEM are released: a commit tracks every
+        // earlier MMA of the thread that issues it.
+        if (tid == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        if (tid == 32 || tid == kPrepThreads) {
+            const int i = tid == 32 ? 0 : 1;
+            umma_commit(&S.bar_drain[i]);
+            mbar_wait(&S.bar_drain[i], 0, kWaitNs / 4);
+        }
+        if (tid == kPrepThreads)
+            for (int s = 0; s < 2; ++s)
+                if (pending[s] >= 0) mbar_wait(&S.bar_load[s], (pending[s] >> 1) & 1, kWaitNs / 4);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
