@@ -266,6 +266,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             cp_async_commit();
         };
         if (warp == 0) prefetch_gates(0);
+        // The strictly-upper 16x16 blocks of T (fp32 copy) and of the top halves of
+        // AV / AK (the blocks of P T above the diagonal) are zero for every chunk
+        // and nothing else writes them: clear them once.
+        for (int e = pt; e < 64 * 64; e += kPrepThreads) {
+            const int r = e >> 6, j = e & 63;
+            if ((j >> 4) > (r >> 4)) Tf[r * 65 + j] = 0.f;
+        }
+        for (int e = pt; e < 6 * 16 * 2 * 2; e += kPrepThreads) {
+            const int blkid = e / 64, rem = e % 64;          // 6 blocks x 16 rows x 2 halves x 2 tiles
+            // (R, i) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+            const int R = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
+            const int i = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
+            const int rr = 16 * R + (rem >> 2), cc = 16 * i + 8 * ((rem >> 1) & 1);
+            uint8_t *dst = (rem & 1) ? AK : AV;
+            *reinterpret_cast<uint4 *>(dst + sw128_offset(rr, cc)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        named_sync(kBarPrep, kPrepThreads);
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
@@ -322,45 +339,38 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             named_sync(kBarPrep, kPrepThreads);
             if (!wait_pmma()) break;
 
-            // ---- P4: P (fp16 operand) and A (fp32) from MMA1; k, v tiles -> fp16
+            // ---- P4: P and A (fp16) from MMA1, with decay factors, beta and masks
             {
                 const bool isP = row < 64;
                 const int r = isP ? row : row - 64;
                 const float frr = S.fr[r] * (isP ? 1.f : S.beta[r]), gr = S.g[r];
                 const float br = isP ? 1.f : S.beta[r];
                 const bool exact = MODE == LDN_GDN && S.exact != 0;
+                float v[32];
+                tmem_ld16(tbase + lane_base + kColD1 + 32 * half, v);
+                tmem_ld16(tbase + lane_base + kColD1 + 32 * half + 16, v + 16);
+                tmem_ld_wait();
+                if (exact) {   // log-decay span too wide for the factored form: one exp per entry
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 16) {
-                    const int j0 = 32 * half + jj;
-                    float v[16];
-                    tmem_ld16(tbase + lane_base + kColD1 + j0, v);
-                    tmem_ld_wait();
-                    if (exact) {   // log-decay span too wide for the factored form: one exp per entry
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int j = j0 + i;
-                            const bool keep = isP ? (j <= r) : (j < r);
-                            v[i] = keep ? v[i] * br * expf(gr - S.g[j]) : 0.f;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int j = j0 + i;
-                            const bool keep = isP ? (j <= r) : (j < r);
-                            v[i] = keep ? (frr * v[i]) * S.fc[j] : 0.f;
-                        }
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = 32 * half + i;
+                        const bool keep = isP ? (j <= r) : (j < r);
+                        v[i] = keep ? v[i] * br * expf(gr - S.g[j]) : 0.f;
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>((isP ? P16 : A16) + r * kLd16 + j0);
-                    dst[0] = make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]),
-                                        pack_h2(v[6], v[7]));
-                    dst[1] = make_uint4(pack_h2(v[8], v[9]), pack_h2(v[10], v[11]), pack_h2(v[12], v[13]),
-                                        pack_h2(v[14], v[15]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = 32 * half + i;
+                        const bool keep = isP ? (j <= r) : (j < r);
+                        v[i] = keep ? (frr * v[i]) * S.fc[j] : 0.f;
+                    }
                 }
-                tile_bf16_to_f16(QK + 8192, 8192, pt, kPrepThreads);           // K, block 0
-                tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt, kPrepThreads);   // K, block 1
-                tile_bf16_to_f16(Vt, kVBytes, pt, kPrepThreads);
+                uint4 *dst = reinterpret_cast<uint4 *>((isP ? P16 : A16) + r * kLd16 + 32 * half);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    dst[q4] = make_uint4(pack_h2(v[8 * q4], v[8 * q4 + 1]), pack_h2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                                         pack_h2(v[8 * q4 + 4], v[8 * q4 + 5]), pack_h2(v[8 * q4 + 6], v[8 * q4 + 7]));
             }
-            fence_proxy_async_smem();
             named_sync(kBarPrep, kPrepThreads);
 
             // ---- P5: T = (I + A)^{-1}: 16x16 diagonal blocks, then block substitution
@@ -381,11 +391,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     T16[(o + r) * kLd16 + o + col] = __float2half_rn(x[r]);
                 }
             }
-            else {   // the other prep threads zero the strictly-upper blocks meanwhile
-                for (int e = pt - 64; e < 64 * 64; e += kPrepThreads - 64) {
-                    const int r = e >> 6, j = e & 63;
-                    if ((j >> 4) > (r >> 4)) Tf[r * 65 + j] = 0.f;
-                }
+            else {   // the other prep threads convert the k and v tiles to fp16 meanwhile
+                tile_bf16_to_f16(QK + 8192, 8192, pt - 64, kPrepThreads - 64);           // K, block 0
+                tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
+                tile_bf16_to_f16(Vt, kVBytes, pt - 64, kPrepThreads - 64);
             }
             named_sync(kBarPrep, kPrepThreads);
             // Below-diagonal blocks, one warp per 16-column block i (warps 0..2):
@@ -491,17 +500,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             *reinterpret_cast<uint32_t *>(AK + sw128_offset(rr, cc)) =
                                 pack_h2(-p0 * b0 * S.eg[s][cc], -p1 * b1 * S.eg[s][cc + 1]);
                         }
-                }
-            } else {
-                // warp 7: the strictly-upper 16x16 blocks of rows 0..63 are zero
-                for (int e = lane; e < 6 * 16 * 2 * 2; e += 32) {
-                    const int blkid = e / 64, rem = e % 64;          // 6 blocks x 16 rows x 2 halves x 2 tiles
-                    // (R, i) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-                    const int R = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
-                    const int i = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-                    const int rr = 16 * R + (rem >> 2), cc = 16 * i + 8 * ((rem >> 1) & 1);
-                    uint8_t *dst = (rem & 1) ? AK : AV;
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(rr, cc)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
@@ -638,23 +636,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             {
                 const int r = top ? st : st - 64;
 #pragma unroll
-                for (int n = 0; n < kDVS; n += 16) {
-                    float v[16];
+                for (int n = 0; n < kDVS; n += 32) {
+                    float v[32];
                     tmem_ld16(tbase + lane_base + kColRV + 64 * s + n, v);
+                    tmem_ld16(tbase + lane_base + kColRV + 64 * s + n + 16, v + 16);
                     tmem_ld_wait();
                     if (top) {
                         if (r < L) {
-                            __nv_bfloat16 *dst = out + (((size_t)b * T + t0 + r) * H + h) * dv + n0 + n;
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]),
-                                                                         pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
-                            *reinterpret_cast<uint4 *>(dst + 8) =
-                                make_uint4(pack_bf2(v[8], v[9]), pack_bf2(v[10], v[11]), pack_bf2(v[12], v[13]),
-                                           pack_bf2(v[14], v[15]));
+                            uint4 *dst = reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * H + h) * dv + n0 + n);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                dst[q4] = make_uint4(pack_bf2(v[8 * q4], v[8 * q4 + 1]), pack_bf2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                                                     pack_bf2(v[8 * q4 + 4], v[8 * q4 + 5]),
+                                                     pack_bf2(v[8 * q4 + 6], v[8 * q4 + 7]));
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= egc;
+                        for (int i = 0; i < 32; ++i) v[i] *= egc;
                         st_row16(UB, r, n, v);
+                        st_row16(UB, r, n + 16, v + 16);
                     }
                 }
             }
@@ -677,16 +677,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
             // ---- S6: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
 #pragma unroll
-            for (int n = 0; n < kDVS; n += 16) {
-                float v[16];
+            for (int n = 0; n < kDVS; n += 32) {
+                float v[32];
                 tmem_ld16(tbase + lane_base + kColD6 + n, v);
+                tmem_ld16(tbase + lane_base + kColD6 + n + 16, v + 16);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     Hreg[n + i] = gC * Hreg[n + i] + v[i];
                     v[i] = Hreg[n + i];
                 }
                 st_row16(HB, st, n, v);
+                st_row16(HB, st, n + 16, v + 16);
             }
             fence_proxy_async_smem();
             tc_fence_before();
