@@ -92,6 +92,87 @@ diag_umma_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
     if (warp == 0) tmem_dealloc(tbase, tmem_cols);
 }
 
+// The same chain with A (M = 128) held in TMEM instead of shared memory: row r
+// of A goes to lane r as 16-bit pairs, element k in the low (k even) or high
+// (k odd) half of column kAcol + k / 2, written with tcgen05.st.  D occupies
+// columns [0, N); the full 128 x N region is dumped as in diag_umma_kernel.
+constexpr uint32_t kAcol = 256;
+__global__ void __launch_bounds__(128)
+diag_umma_ts_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B, float *__restrict__ D,
+                    int N, int K, int b_mn, uint32_t fmt, int *status)
+{
+    extern __shared__ uint8_t dsmem[];
+    uint8_t *Bs = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);   // up to 256 x 128 16-bit
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base_s;
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    for (int e = tid; e < N * K; e += 128) {
+        const int n = e / K, k = e % K;
+        const uint32_t off = b_mn ? (n >> 6) * (uint32_t)K * 128u + sw128_offset(k, n & 63)
+                                  : (k >> 6) * (uint32_t)N * 128u + sw128_offset(n, k & 63);
+        *reinterpret_cast<uint16_t *>(Bs + off) = B[e];
+    }
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_s, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_s;
+    const uint32_t lane_addr = (uint32_t)(32 * warp) << 16;
+
+    // row tid of A -> lane tid (thread tid of warp w owns lane 32 w + lane)
+    float sent[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sent[i] = kSentinel;
+    for (int c = 0; c < N; c += 16) tmem_st16(tbase + lane_addr + c, sent);
+    for (int c = 0; c < K / 2; c += 16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int k = 2 * (c + i);
+            w[i] = (uint32_t)A[(size_t)tid * K + k] | ((uint32_t)A[(size_t)tid * K + k + 1] << 16);
+        }
+        tmem_st16u(tbase + lane_addr + kAcol + c, w);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (tid == 0) {
+        const uint32_t idesc = idesc_f16kind_f32(128, N, 0, b_mn, fmt);
+        const uint32_t b0 = smem_u32(Bs);
+        for (int s = 0; s < K / 16; ++s) {
+            const uint64_t bd = b_mn ? mnmajor_desc(b0, K, s) : kmajor_desc(b0, N, s);
+            umma_ts(tbase, tbase + kAcol + 8 * s, bd, idesc, s > 0);
+        }
+        umma_commit(&bar);
+    }
+    const bool ok = mbar_wait(&bar, 0, kDiagTimeoutNs);
+    if (!ok && (tid & 31) == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+    tc_fence_after();
+    if (ok) {
+        for (int c = 0; c < N; c += 16) {
+            float v[16];
+            tmem_ld16(tbase + lane_addr + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[(size_t)tid * N + c + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 // TMA load of a 64-row x 64-column bf16 box (SWIZZLE_128B) at (row0, col0)
 // of a [rows][cols] matrix, then a raw byte dump of the 8 KiB tile.
 __global__ void __launch_bounds__(128)
@@ -168,6 +249,25 @@ extern "C" int ldn_diag_umma(const void *A, const void *B, float *D, int M, int 
         return LDN_ERR_CUDA;
     diag_umma_kernel<<<1, 128, smem, (cudaStream_t)stream>>>((const uint16_t *)A, (const uint16_t *)B,
                                                              D, M, N, K, a_mn, b_mn, (uint32_t)fmt, cols, sw);
+    return cudaGetLastError() == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
+extern "C" int ldn_diag_umma_tmem_a(const void *A, const void *B, float *D, int N, int K, int b_mn, int fmt,
+                                    void *stream)
+{
+    if (!A || !B || !D) return LDN_ERR_INVALID_ARG;
+    if (fmt != 0 && fmt != 1) return LDN_ERR_INVALID_ARG;
+    if (N < 16 || N > 256 || N % 16 != 0) return LDN_ERR_UNSUPPORTED;
+    if (K < 32 || K > 128 || K % 32 != 0) return LDN_ERR_UNSUPPORTED;
+    if (b_mn && N % 64 != 0) return LDN_ERR_UNSUPPORTED;
+    int *sw = status_word_ptr();
+    if (!sw) return LDN_ERR_CUDA;
+    const size_t smem = 65536 + 1024;
+    if (cudaFuncSetAttribute(diag_umma_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return LDN_ERR_CUDA;
+    diag_umma_ts_kernel<<<1, 128, smem, (cudaStream_t)stream>>>((const uint16_t *)A, (const uint16_t *)B, D, N, K,
+                                                                b_mn, (uint32_t)fmt, sw);
     return cudaGetLastError() == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 

@@ -28,6 +28,16 @@ int ldn_diag_umma(const void *A, const void *B, float *D_out, int M, int N, int 
                   int fmt, void *stream);
 
 /*
+ * The same chain with A held in tensor memory (M = 128): row r of A [128][K]
+ * is written to TMEM lane r as 16-bit pairs (element k in the low half of a
+ * 32-bit column for even k, the high half for odd k), and tcgen05.mma reads it
+ * from there; B [N][K] is staged as for ldn_diag_umma.  D_out [128][N] fp32.
+ * N in [16, 256], N % 16 == 0 (N % 64 == 0 if b_mn); K in {32, 64, 96, 128}.
+ */
+int ldn_diag_umma_tmem_a(const void *A, const void *B, float *D_out, int N, int K, int b_mn, int fmt,
+                         void *stream);
+
+/*
  * TMA tiled load (SWIZZLE_128B, box 64 x 64) of rows [row0, row0 + 64) and
  * columns [col0, col0 + 64) of a bf16 matrix src [rows][cols]; rows past the
  * end read as zero.  The 8192 bytes of the shared-memory tile are copied to

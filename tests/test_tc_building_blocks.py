@@ -85,3 +85,31 @@ def test_umma_f16kind_layouts(M, N, K, a_mn, b_mn, fmt):
     for lane in range(128):
         if lane not in used and M == 128:
             raise AssertionError("M=128 must use every lane")
+
+
+TMEM_A_CASES = [  # N, K, b_mn, fmt
+    (64, 128, 1, 0), (128, 64, 0, 0), (64, 64, 1, 1), (256, 128, 0, 1), (16, 32, 0, 0),
+]
+
+
+@pytest.mark.parametrize("N,K,b_mn,fmt", TMEM_A_CASES)
+def test_umma_a_operand_in_tmem(N, K, b_mn, fmt):
+    """A (M = 128) read from TMEM as 16-bit pairs: element k of row r in lane r,
+    column k // 2, low half for even k.  On failure, say whether the pairs were
+    read the other way round."""
+    import torch
+    g = torch.Generator().manual_seed(N * 7 + K + 3 * b_mn + 11 * fmt)
+    dt = torch.bfloat16 if fmt == 1 else torch.float16
+    A = torch.randn(128, K, generator=g).to(dt)
+    B = torch.randn(N, K, generator=g).to(dt)
+    D = torch.empty(128, N, dtype=torch.float32, device="cuda")
+    Ad, Bd = A.cuda(), B.cuda()
+    assert ldn.ldn_diag_umma_tmem_a(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), N, K, b_mn, fmt, _stream()) == ldn.LDN_OK
+    assert ldn.device_status() == ldn.LDN_OK
+    got = D.cpu().numpy().astype(np.float64)
+    a, b = A.double().numpy(), B.double().numpy()
+    ref = a @ b.T
+    swapped = a.reshape(128, K // 2, 2)[:, :, ::-1].reshape(128, K) @ b.T
+    err = np.max(np.abs(got - ref)) / (1 + np.abs(ref).max())
+    err_sw = np.max(np.abs(got - swapped)) / (1 + np.abs(ref).max())
+    assert err < 1e-5, f"max rel err {err:.3g} (pair-swapped reading: {err_sw:.3g})"
