@@ -24,15 +24,17 @@
 //   MMA1 [Q ; K] K^T            M=128  bf16 tiles as loaded  -> P_raw, K K^T
 //   MMA3 [P Tu ; Tu] V          M=128                        -> P U', U'
 //   MMA4 [-P Tw ; Tw] K         M=128  (double-buffered)     -> -P W, W
-//   MMA5 RV += [Q~ ; -W] H0     M=128  (serial)              -> O, U
+//   MMA5 RV += [Q~ ; -W] H0     M=128  (serial, A in TMEM)   -> O, U
 //   MMA6 K^T U~                 M=128  (serial)              -> state increment
 // and, inside the prep warps, P T by fp16 warp MMAs (block lower-triangular).
 // Hand-offs use mbarriers: prep -> serial "chunk ready" is the commit of
 // MMA3 / MMA4 itself (both accumulators double-buffered in TMEM), serial ->
 // prep "accumulators read".  The serial warps form the MMA5 operand
-// [Q~ ; -W] from the MMA4 accumulator (they are idle most of a chunk, the
-// prep warps are not), and issue the TMA loads of chunk c + 2 as soon as the
-// state step of chunk c has released its tiles.  The prep warps need no wait
+// [Q~ ; -W] from the MMA4 accumulator and leave it in tensor memory, in place
+// (they are idle most of a chunk, the prep warps are not).  Input tiles sit in
+// a ring of three stages: the serial warps issue the TMA loads of chunk c + 3
+// as soon as the state step of chunk c has released its tiles, so a load has
+// two chunks' time to land before it is needed.  The prep warps need no wait
 // for MMA3 / MMA4: the commit of the next chunk's MMA1, which they wait on
 // anyway, also covers the earlier MMAs of the same issuing thread.
 //
@@ -67,13 +69,15 @@ constexpr int kPrepThreads = 256;
 constexpr int kSerialThreads = 128;
 constexpr int kThreads = kPrepThreads + kSerialThreads;
 constexpr uint32_t kBarPrep = 1, kBarSerial = 2;   // named barrier ids
+constexpr int kIssuer = 96;                        // prep thread issuing every prep MMA (warp 3)
+constexpr int kGateWarp = 4;                       // prep warp computing gate prefixes
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
 constexpr float kMaxLogSpan = 60.f;                // factored decay limit (e^60 per factor)
 
 // TMEM columns (fp32, 128 lanes).
 constexpr uint32_t kColD1 = 0;      // 64   MMA1
-constexpr uint32_t kColDK1 = 64;    // 128  MMA4, stage 1
-constexpr uint32_t kColDK0 = 192;   // 128  MMA4, stage 0
+constexpr uint32_t kColDK1 = 64;    // 128  MMA4, stage 1; then the MMA5 A operand (fp16 pairs, 64)
+constexpr uint32_t kColDK0 = 192;   // 128  MMA4, stage 0; likewise
 constexpr uint32_t kColRV = 320;    // 2 x 64  MMA3 / MMA5 (double-buffered)
 constexpr uint32_t kColD6 = 448;    // 64   MMA6
 constexpr uint32_t kTmemCols = 512;
@@ -81,27 +85,24 @@ constexpr uint32_t kTmemCols = 512;
 // Shared memory (bytes from a 1024-aligned base).
 constexpr uint32_t kQKBytes = 2 * 16384;      // [Q;K], 2 blocks of 128 rows x 128 B
 constexpr uint32_t kVBytes = 8192;            // V slice, 64 rows x 128 B
-constexpr uint32_t kOffQK0 = 0;
-constexpr uint32_t kOffQK1 = kOffQK0 + kQKBytes;
-constexpr uint32_t kOffV0 = kOffQK1 + kQKBytes;
-constexpr uint32_t kOffV1 = kOffV0 + kVBytes;
-constexpr uint32_t kOffAK = kOffV1 + kVBytes;      // [-P Tw ; Tw] K-major 128 x 64      (16 KB)
+constexpr int kStages = 3;                    // ring of input tiles (chunk c in stage c % 3)
+constexpr uint32_t kOffQK = 0;                // kStages x [Q;K]
+constexpr uint32_t kOffV = kOffQK + kStages * kQKBytes;   // kStages x V slice
+constexpr uint32_t kOffAK = kOffV + kStages * kVBytes;    // [-P Tw ; Tw] K-major 128 x 64      (16 KB)
 constexpr uint32_t kOffAV = kOffAK + 16384;        // [P Tu ; Tu] K-major 128 x 64       (16 KB)
-constexpr uint32_t kOffA5 = kOffAV + 16384;        // [Q~ ; -W] K-major 128 x 128        (32 KB)
-constexpr uint32_t kOffHB = kOffA5 + 32768;        // H fp16, MN-major 128 x 64          (16 KB)
+constexpr uint32_t kOffHB = kOffAV + 16384;        // H fp16, MN-major 128 x 64          (16 KB)
 constexpr uint32_t kOffUB = kOffHB + 16384;        // U~ fp16, MN-major 64 x 64          (8 KB)
 constexpr int kLd16 = 72;                            // fp16 row stride (144 B: ldmatrix conflict-free)
 constexpr uint32_t kOffA16 = kOffUB + 8192;          // fp16 A [64][72]
 constexpr uint32_t kOffP16 = kOffA16 + 64 * kLd16 * 2;  // fp16 P [64][72]
 constexpr uint32_t kOffT16 = kOffP16 + 64 * kLd16 * 2;  // fp16 T [64][72]
-constexpr uint32_t kOffTf = kOffT16 + 64 * kLd16 * 2;   // fp32 T [64][65]
-constexpr uint32_t kOffX = kOffTf + 64 * 65 * 4;     // fp16 16x16 scratch per chain warp [3][16][24]
+constexpr uint32_t kOffX = kOffT16 + 64 * kLd16 * 2;  // fp16 16x16 scratch per chain warp [3][16][24]
 constexpr uint32_t kOffSmall = kOffX + 3072;
-constexpr uint32_t kSmallBytes = 4096;
+constexpr uint32_t kSmallBytes = 6144;
 constexpr uint32_t kSmemBytes = kOffSmall + kSmallBytes + 1024;
 
 struct Small {
-    uint64_t bar_load[2];     // TMA tiles of stage s landed
+    uint64_t bar_load[kStages];   // TMA tiles of ring stage ls landed
     uint64_t bar_pmma;        // prep MMA commits
     uint64_t bar_smma;        // serial MMA commits
     uint64_t bar_ready[2];    // MMA3 / MMA4 of stage s complete (prep commit)
@@ -109,19 +110,22 @@ struct Small {
     uint64_t bar_drain[2];    // failure path: last commit of each MMA issuer
     uint32_t tmem_base;
     int fail;
-    int exact;                // per-entry exponentials for this chunk
-    float beta[kC];
-    float g[kC];              // inclusive log-decay prefix
-    float fr[kC];             // e^{g_r - m}
-    float fc[kC];             // e^{m - g_j}
-    float eg[2][kC];          // e^{g_r}, per stage (also read by the serial warps)
-    float egc[2][kC];         // e^{g_C - g_r}, per stage (read by the serial warps)
-    float gC[2];              // e^{g_C}, per stage
+    // Per-chunk gate data, slot = chunk % 3: written one chunk ahead by the gate
+    // warp, read by the prep warps and (eg, egc, gC) by the serial warps.
+    int exact[kStages];       // per-entry exponentials for this chunk
+    float gC[kStages];        // e^{g_C}
+    alignas(16) float beta[kStages][kC];
+    alignas(16) float g[kStages][kC];     // inclusive log-decay prefix
+    alignas(16) float fr[kStages][kC];    // e^{g_r - m}
+    alignas(16) float fc[kStages][kC];    // e^{m - g_j}
+    alignas(16) float eg[kStages][kC];    // e^{g_r}
+    alignas(16) float egc[kStages][kC];   // e^{g_C - g_r}
     float stg_beta[2][kC];    // beta / log-gate of the next chunk, prefetched by cp.async
     float stg_gate[2][kC];
 };
 static_assert(sizeof(Small) <= kSmallBytes, "Small does not fit its shared-memory slot");
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+static_assert(kOffSmall % 16 == 0 && kOffT16 % 16 == 0, "vector accesses need 16-byte aligned buffers");
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b)
 {
@@ -187,9 +191,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __half *A16 = reinterpret_cast<__half *>(sm + kOffA16);
     __half *P16 = reinterpret_cast<__half *>(sm + kOffP16);
     __half *T16 = reinterpret_cast<__half *>(sm + kOffT16);
-    float *Tf = reinterpret_cast<float *>(sm + kOffTf);
     __half *X16 = reinterpret_cast<__half *>(sm + kOffX);
-    uint8_t *AK = sm + kOffAK, *AV = sm + kOffAV, *A5 = sm + kOffA5;
+    uint8_t *AK = sm + kOffAK, *AV = sm + kOffAV;
     uint8_t *HB = sm + kOffHB, *UB = sm + kOffUB;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -202,8 +205,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_base = (32u * quad) << 16;
 
     if (tid == 0) {
-        mbar_init(&S.bar_load[0], 1);
-        mbar_init(&S.bar_load[1], 1);
+        for (int i = 0; i < kStages; ++i) mbar_init(&S.bar_load[i], 1);
         mbar_init(&S.bar_pmma, 1);
         mbar_init(&S.bar_smma, 1);
         mbar_init(&S.bar_ready[0], 1);
@@ -226,14 +228,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
-    int pending[2] = {-1, -1};   // chunk whose TMA loads were last issued into stage s (serial thread 0)
+    int pending[kStages] = {-1, -1, -1};   // chunk last loaded into ring stage ls (serial thread 0)
 
     if (tid < kPrepThreads) {
         // ============================== PREP ==============================
         const int pt = tid;
         const int half = pt >> 7;                  // column half handled in TMEM reads
         const int row = 32 * quad + lane;          // TMEM lane of this thread
-        const bool issuer = (pt == 32);
+        const bool issuer = (pt == kIssuer);
         uint32_t pphase = 0;
         auto prep_vote = [&](bool ok) -> bool {
             if (!ok) S.fail = 1;
@@ -253,7 +255,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16); // MMA3
         const uint32_t id_m128_n128_mn = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16);// MMA4
 
-        // beta and log-gates of chunk cc into staging slot cc & 1 (warp 0; rows
+        // beta and log-gates of chunk cc into staging slot cc & 1 (gate warp; rows
         // past T read as zero), asynchronously so the loads overlap a whole chunk.
         auto prefetch_gates = [&](int cc) {
             const int tt0 = cc * kC, LL = min(kC, T - tt0);
@@ -265,13 +267,67 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             cp_async_commit();
         };
-        if (warp == 0) prefetch_gates(0);
-        // The strictly-upper 16x16 blocks of T (fp32 copy) and of the top halves of
-        // AV / AK (the blocks of P T above the diagonal) are zero for every chunk
-        // and nothing else writes them: clear them once.
+        // Gate prefix and decay factors of chunk cc into slot cc % 3 (gate warp, two
+        // rows per lane); then the staging of chunk cc + 1 is started.
+        auto compute_gates = [&](int cc) {
+            const int sg = cc & 1, gs = cc % kStages;
+            cp_async_wait<0>();          // chunk cc's staged beta / gates
+            __syncwarp();
+            const int r0 = 2 * lane, r1 = r0 + 1;
+            const float b0 = S.stg_beta[sg][r0], b1 = S.stg_beta[sg][r1];
+            const float a0 = MODE == LDN_GDN ? S.stg_gate[sg][r0] : 0.f;
+            const float a1 = MODE == LDN_GDN ? S.stg_gate[sg][r1] : 0.f;
+            __syncwarp();
+            if (cc + 1 < nchunks) prefetch_gates(cc + 1);
+            float incl = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const float g1 = incl, g0 = incl - a1;
+            const float m = __shfl_sync(0xffffffffu, g1, 15);        // g at row 31
+            const float gc = __shfl_sync(0xffffffffu, g1, 31);       // g at row 63
+            S.beta[gs][r0] = b0; S.beta[gs][r1] = b1;
+            S.g[gs][r0] = g0; S.g[gs][r1] = g1;
+            if (MODE == LDN_GDN) {
+                S.fr[gs][r0] = expf(g0 - m); S.fr[gs][r1] = expf(g1 - m);
+                S.fc[gs][r0] = expf(m - g0); S.fc[gs][r1] = expf(m - g1);
+                S.eg[gs][r0] = expf(g0); S.eg[gs][r1] = expf(g1);
+                S.egc[gs][r0] = expf(gc - g0); S.egc[gs][r1] = expf(gc - g1);
+                if (lane == 0) {
+                    S.gC[gs] = expf(gc);
+                    S.exact[gs] = (-m > kMaxLogSpan || m - gc > kMaxLogSpan) ? 1 : 0;
+                }
+            } else {
+                S.fr[gs][r0] = S.fr[gs][r1] = S.fc[gs][r0] = S.fc[gs][r1] = 1.f;
+                S.eg[gs][r0] = S.eg[gs][r1] = 1.f;
+                S.egc[gs][r0] = S.egc[gs][r1] = 1.f;
+                if (lane == 0) { S.gC[gs] = 1.f; S.exact[gs] = 0; }
+            }
+        };
+        // MMA1 [Q ; K] K^T of chunk cc on its bf16 tiles as loaded (issuer thread).
+        auto issue_mma1 = [&](int cc) -> bool {
+            const int ls = cc % kStages;
+            if (!mbar_wait(&S.bar_load[ls], (cc / kStages) & 1, kWaitNs)) return false;
+            tc_fence_after();
+            const uint32_t qk = smem_u32(sm + kOffQK + ls * kQKBytes);
+            for (int k = 0; k < kDK / 16; ++k)
+                umma_bf16(tbase + kColD1, kmajor_desc(qk, 128, k), kmajor_desc(qk + 8192, 128, k), id_m128_n64, k > 0);
+            umma_commit(&S.bar_pmma);
+            return true;
+        };
+        if (warp == kGateWarp) {
+            prefetch_gates(0);
+            compute_gates(0);
+        }
+        if (issuer && !issue_mma1(0)) S.fail = 1;
+        // The strictly-upper 16x16 blocks of T and of the top halves of AV / AK
+        // (the blocks of P T above the diagonal) are zero for every chunk and
+        // nothing else writes them: clear them once.
         for (int e = pt; e < 64 * 64; e += kPrepThreads) {
             const int r = e >> 6, j = e & 63;
-            if ((j >> 4) > (r >> 4)) Tf[r * 65 + j] = 0.f;
+            if ((j >> 4) > (r >> 4)) T16[r * kLd16 + j] = __float2half_rn(0.f);
         }
         for (int e = pt; e < 6 * 16 * 2 * 2; e += kPrepThreads) {
             const int blkid = e / 64, rem = e % 64;          // 6 blocks x 16 rows x 2 halves x 2 tiles
@@ -285,67 +341,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         named_sync(kBarPrep, kPrepThreads);
 
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
-            uint8_t *QK = sm + (s ? kOffQK1 : kOffQK0);
-            uint8_t *Vt = sm + (s ? kOffV1 : kOffV0);
+            const int s = c & 1, ls = c % kStages, gs = ls;
+            uint8_t *QK = sm + kOffQK + ls * kQKBytes;
+            uint8_t *Vt = sm + kOffV + ls * kVBytes;
             const uint32_t qk_s = smem_u32(QK), k_s = qk_s + 8192, v_s = smem_u32(Vt);
 
-            // ---- P1: tiles of chunk c; MMA1 on the bf16 tiles as loaded
-            if (!prep_vote(mbar_wait(&S.bar_load[s], (c >> 1) & 1, kWaitNs))) break;
-            if (issuer) {
-                tc_fence_after();
-                for (int k = 0; k < kDK / 16; ++k)
-                    umma_bf16(tbase + kColD1, kmajor_desc(qk_s, 128, k), kmajor_desc(k_s, 128, k), id_m128_n64,
-                              k > 0);
-                umma_commit(&S.bar_pmma);
-            }
-            // ---- P2: beta, gate prefix (warp 0, two rows per lane) and decay factors
-            if (warp == 0) {
-                cp_async_wait<0>();          // this chunk's staged beta / gates
-                __syncwarp();
-                const int r0 = 2 * lane, r1 = r0 + 1;
-                const float b0 = S.stg_beta[s][r0], b1 = S.stg_beta[s][r1];
-                const float a0 = MODE == LDN_GDN ? S.stg_gate[s][r0] : 0.f;
-                const float a1 = MODE == LDN_GDN ? S.stg_gate[s][r1] : 0.f;
-                __syncwarp();
-                if (c + 1 < nchunks) prefetch_gates(c + 1);
-                float incl = a0 + a1;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const float g1 = incl, g0 = incl - a1;
-                const float m = __shfl_sync(0xffffffffu, g1, 15);        // g at row 31
-                const float gc = __shfl_sync(0xffffffffu, g1, 31);       // g at row 63
-                S.beta[r0] = b0; S.beta[r1] = b1;
-                S.g[r0] = g0; S.g[r1] = g1;
-                if (MODE == LDN_GDN) {
-                    S.fr[r0] = expf(g0 - m); S.fr[r1] = expf(g1 - m);
-                    S.fc[r0] = expf(m - g0); S.fc[r1] = expf(m - g1);
-                    S.eg[s][r0] = expf(g0); S.eg[s][r1] = expf(g1);
-                    S.egc[s][r0] = expf(gc - g0); S.egc[s][r1] = expf(gc - g1);
-                    if (lane == 0) {
-                        S.gC[s] = expf(gc);
-                        S.exact = (-m > kMaxLogSpan || m - gc > kMaxLogSpan) ? 1 : 0;
-                    }
-                } else {
-                    S.fr[r0] = S.fr[r1] = S.fc[r0] = S.fc[r1] = 1.f;
-                    S.eg[s][r0] = S.eg[s][r1] = 1.f;
-                    S.egc[s][r0] = S.egc[s][r1] = 1.f;
-                    if (lane == 0) { S.gC[s] = 1.f; S.exact = 0; }
-                }
-            }
-            named_sync(kBarPrep, kPrepThreads);
+            // ---- P1: MMA1 of chunk c (issued while chunk c - 1 was prepared) complete
             if (!wait_pmma()) break;
 
             // ---- P4: P and A (fp16) from MMA1, with decay factors, beta and masks
             {
                 const bool isP = row < 64;
                 const int r = isP ? row : row - 64;
-                const float frr = S.fr[r] * (isP ? 1.f : S.beta[r]), gr = S.g[r];
-                const float br = isP ? 1.f : S.beta[r];
-                const bool exact = MODE == LDN_GDN && S.exact != 0;
+                const float frr = S.fr[gs][r] * (isP ? 1.f : S.beta[gs][r]), gr = S.g[gs][r];
+                const float br = isP ? 1.f : S.beta[gs][r];
+                const bool exact = MODE == LDN_GDN && S.exact[gs] != 0;
                 float v[32];
                 tmem_ld16(tbase + lane_base + kColD1 + 32 * half, v);
                 tmem_ld16(tbase + lane_base + kColD1 + 32 * half + 16, v + 16);
@@ -355,14 +365,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int i = 0; i < 32; ++i) {
                         const int j = 32 * half + i;
                         const bool keep = isP ? (j <= r) : (j < r);
-                        v[i] = keep ? v[i] * br * expf(gr - S.g[j]) : 0.f;
+                        v[i] = keep ? v[i] * br * expf(gr - S.g[gs][j]) : 0.f;
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int j = 32 * half + i;
                         const bool keep = isP ? (j <= r) : (j < r);
-                        v[i] = keep ? (frr * v[i]) * S.fc[j] : 0.f;
+                        v[i] = keep ? (frr * v[i]) * S.fc[gs][j] : 0.f;
                     }
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>((isP ? P16 : A16) + r * kLd16 + 32 * half);
@@ -371,6 +381,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     dst[q4] = make_uint4(pack_h2(v[8 * q4], v[8 * q4 + 1]), pack_h2(v[8 * q4 + 2], v[8 * q4 + 3]),
                                          pack_h2(v[8 * q4 + 4], v[8 * q4 + 5]), pack_h2(v[8 * q4 + 6], v[8 * q4 + 7]));
             }
+            tc_fence_before();   // D1 has been read: the next MMA1 may overwrite it
             named_sync(kBarPrep, kPrepThreads);
 
             // ---- P5: T = (I + A)^{-1}: 16x16 diagonal blocks, then block substitution
@@ -387,7 +398,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
-                    Tf[(o + r) * 65 + o + col] = x[r];
                     T16[(o + r) * kLd16 + o + col] = __float2half_rn(x[r]);
                 }
             }
@@ -435,14 +445,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int hh = 0; hh < 2; ++hh) {
                             const int rr = 16 * R + g + 8 * hh, cc = 16 * i + 8 * nt + 2 * t4;
                             const float t0v = -tacc[nt][2 * hh], t1v = -tacc[nt][2 * hh + 1];
-                            Tf[rr * 65 + cc] = t0v;
-                            Tf[rr * 65 + cc + 1] = t1v;
                             *reinterpret_cast<uint32_t *>(T16 + rr * kLd16 + cc) = pack_h2(t0v, t1v);
                         }
                     __syncwarp();
                 }
+            } else if (warp == kIssuer / 32) {
+                // look-ahead: MMA1 of chunk c + 1 into D1 (read by P4 above)
+                if (issuer && c + 1 < nchunks && !issue_mma1(c + 1)) S.fail = 1;
+            } else if (warp == kGateWarp) {
+                // The serial warps have read the accumulators and gate slot of chunk
+                // c - 2 (needed before MMA3 / MMA4 of chunk c overwrite RV[s], DK[s],
+                // and before slot (c + 1) % 3 = (c - 2) % 3 is rewritten).
+                bool ok = true;
+                if (c >= 2 && lane == 0) ok = mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) {
+                    if (lane == 0) S.fail = 1;
+                } else if (c + 1 < nchunks) {
+                    compute_gates(c + 1);
+                }
             }
-            named_sync(kBarPrep, kPrepThreads);
+            // MMA3 / MMA4 of chunk c - 1 have finished reading AV / AK before they are rewritten
+            if (!prep_vote(pt == 0 && c >= 1 ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs)
+                                             : true))
+                break;
 
             // ---- P6: stacked operands AV = [P Tu ; Tu] and AK = [-P Tw ; Tw] (fp16, K-major).
             //      Rows 64..127 straight from T; rows 0..63 from P T by fp16 warp MMAs
@@ -451,12 +477,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int j = pt & 63;           // row of T
                 const int n0c = 16 * (pt >> 6);  // 16-column group
                 float vu[16], vw[16];
+                const uint4 *trow = reinterpret_cast<const uint4 *>(T16 + j * kLd16 + n0c);
+                const float4 *bq = reinterpret_cast<const float4 *>(&S.beta[gs][n0c]);
+                const float4 *eq = reinterpret_cast<const float4 *>(&S.eg[gs][n0c]);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int n = n0c + i;
-                    const float t = Tf[j * 65 + n] * S.beta[n];
-                    vu[i] = t;
-                    vw[i] = t * S.eg[s][n];
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    const uint4 u = trow[h8];
+                    const __half2 *t2 = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const float4 bb = bq[2 * h8 + q], ee = eq[2 * h8 + q];
+                        const float2 ta = __half22float2(t2[2 * q]), tb = __half22float2(t2[2 * q + 1]);
+                        const int i = 8 * h8 + 4 * q;
+                        vu[i] = ta.x * bb.x; vu[i + 1] = ta.y * bb.y; vu[i + 2] = tb.x * bb.z; vu[i + 3] = tb.y * bb.w;
+                        vw[i] = vu[i] * ee.x; vw[i + 1] = vu[i + 1] * ee.y;
+                        vw[i + 2] = vu[i + 2] * ee.z; vw[i + 3] = vu[i + 3] * ee.w;
+                    }
                 }
                 st_row16(AV, 64 + j, n0c, vu);
                 st_row16(AK, 64 + j, n0c, vw);
@@ -495,10 +531,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int hh = 0; hh < 2; ++hh) {
                             const int rr = 16 * R + g + 8 * hh, cc = 16 * i + 8 * nt + 2 * t4;
                             const float p0 = acc[nt][2 * hh], p1 = acc[nt][2 * hh + 1];
-                            const float b0 = S.beta[cc], b1 = S.beta[cc + 1];
-                            *reinterpret_cast<uint32_t *>(AV + sw128_offset(rr, cc)) = pack_h2(p0 * b0, p1 * b1);
-                            *reinterpret_cast<uint32_t *>(AK + sw128_offset(rr, cc)) =
-                                pack_h2(-p0 * b0 * S.eg[s][cc], -p1 * b1 * S.eg[s][cc + 1]);
+                            const float2 bb = *reinterpret_cast<const float2 *>(&S.beta[gs][cc]);
+                            const float2 ee = *reinterpret_cast<const float2 *>(&S.eg[gs][cc]);
+                            const float u0 = p0 * bb.x, u1 = p1 * bb.y;
+                            *reinterpret_cast<uint32_t *>(AV + sw128_offset(rr, cc)) = pack_h2(u0, u1);
+                            *reinterpret_cast<uint32_t *>(AK + sw128_offset(rr, cc)) = pack_h2(-u0 * ee.x, -u1 * ee.y);
                         }
                 }
             }
@@ -506,11 +543,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_before();
             named_sync(kBarPrep, kPrepThreads);
 
-            // ---- P9: MMA3 [P Tu ; Tu] V -> RV[s], MMA4 [-P Tw ; Tw] K -> DK[s] (once the
-            //      serial warps have read both accumulators of chunk c - 2); their
+            // ---- P9: MMA3 [P Tu ; Tu] V -> RV[s], MMA4 [-P Tw ; Tw] K -> DK[s] (the
+            //      gate warp saw the serial warps release both for chunk c - 2); their
             //      commit is the serial warps' "chunk ready".
-            if (c >= 2 && !prep_vote(pt == 0 ? mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs) : true))
-                break;
             if (issuer) {
                 tc_fence_after();
                 const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(AK);
@@ -540,21 +575,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             return r;
         };
         auto issue_load = [&](int c) {
-            const int s = c & 1;
-            uint8_t *qk = sm + (s ? kOffQK1 : kOffQK0);
-            uint8_t *vv = sm + (s ? kOffV1 : kOffV0);
-            pending[s] = c;
-            mbar_arrive_expect_tx(&S.bar_load[s], 2 * 16384 + 8192);
+            const int ls = c % kStages;
+            uint8_t *qk = sm + kOffQK + ls * kQKBytes;
+            uint8_t *vv = sm + kOffV + ls * kVBytes;
+            pending[ls] = c;
+            mbar_arrive_expect_tx(&S.bar_load[ls], 2 * 16384 + 8192);
             for (int kb = 0; kb < 2; ++kb) {
-                tma_load_4d(qk + kb * 16384, &tm_q, &S.bar_load[s], kb * 64, h, c * kC, b);
-                tma_load_4d(qk + kb * 16384 + 8192, &tm_k, &S.bar_load[s], kb * 64, h, c * kC, b);
+                tma_load_4d(qk + kb * 16384, &tm_q, &S.bar_load[ls], kb * 64, h, c * kC, b);
+                tma_load_4d(qk + kb * 16384 + 8192, &tm_k, &S.bar_load[ls], kb * 64, h, c * kC, b);
             }
-            tma_load_4d(vv, &tm_v, &S.bar_load[s], n0, h, c * kC, b);
+            tma_load_4d(vv, &tm_v, &S.bar_load[ls], n0, h, c * kC, b);
         };
-        if (st == 0) {
-            issue_load(0);
-            if (nchunks > 1) issue_load(1);
-        }
+        if (st == 0)
+            for (int c = 0; c < kStages && c < nchunks; ++c) issue_load(c);
         const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);   // MMA5
         const uint32_t id_m128_n64_amn = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);  // MMA6
 
@@ -574,25 +607,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
-            const uint8_t *QK = sm + (s ? kOffQK1 : kOffQK0);
+            const uint8_t *QK = sm + kOffQK + (c % kStages) * kQKBytes;
             const uint32_t k_s = smem_u32(QK) + 8192;
 
             // ---- S1: MMA3 / MMA4 of chunk c complete (RV[s] = [P U' ; U'], DK[s] = [-P W ; W])
             if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
             tc_fence_after();
-            const float gC = S.gC[s];
+            const int gs = c % kStages;
+            const float gC = S.gC[gs];
             const bool top = st < 64;
-            const float egc = top ? 0.f : S.egc[s][st - 64];
+            const float egc = top ? 0.f : S.egc[gs][st - 64];
 
             // ---- S2: A5 = [Q~ ; -W] (row st): Q~ = Diag(e^{g}) Q - P W on the top rows
-            //      (Q read from the bf16 tile as loaded), -W on the bottom rows.  The
-            //      previous MMA5, the only reader of A5, completed in the last step.
+            //      (Q read from the bf16 tile as loaded), -W on the bottom rows, packed as
+            //      fp16 pairs into the first 64 columns of DK[s] -- the MMA5 A operand,
+            //      read from tensor memory.  Each thread rewrites only columns of its own
+            //      lane that it has already read.
             {
-                const float er = top ? S.eg[s][st] : 0.f;
+                const float er = top ? S.eg[gs][st] : 0.f;
                 const uint32_t dk_col = tbase + lane_base + (s ? kColDK1 : kColDK0);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
-                    uint8_t *blk = A5 + kb * 16384;
                     const uint8_t *qblk = QK + kb * 16384;   // Q rows 0..63 of this column block
 #pragma unroll
                     for (int cc = 0; cc < 64; cc += 32) {
@@ -612,22 +647,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = -v[i];
                         }
-                        st_row16(blk, st, cc, v);
-                        st_row16(blk, st, cc + 16, v + 16);
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_h2(v[2 * i], v[2 * i + 1]);
+                        tmem_st16u(dk_col + 32 * kb + cc / 2, w);
                     }
                 }
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             named_sync(kBarSerial, kSerialThreads);
 
             // ---- S3: MMA5: RV[s] += [Q~ ; -W] H0  -> O (rows 0..63), U (rows 64..127)
             if (st == 0) {
                 tc_fence_after();
-                const uint32_t a5_s = smem_u32(A5), hb_s = smem_u32(HB);
+                const uint32_t a5_t = tbase + (s ? kColDK1 : kColDK0), hb_s = smem_u32(HB);
                 for (int k = 0; k < kDK / 16; ++k)
-                    umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(a5_s, 128, k), mnmajor_desc(hb_s, 128, k),
-                              id_m128_n64_mn, 1);
+                    umma_ts(tbase + kColRV + 64 * s, a5_t + 8 * k, mnmajor_desc(hb_s, 128, k), id_m128_n64_mn, 1);
                 umma_commit(&S.bar_smma);
             }
             if (!wait_smma()) break;
@@ -672,8 +708,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 umma_commit(&S.bar_smma);
             }
             if (!wait_smma()) break;
-            // the tiles of stage s are no longer read by anyone: fetch chunk c + 2 into them
-            if (st == 0 && c + 2 < nchunks) issue_load(c + 2);
+            // the tiles of chunk c are no longer read by anyone: fetch chunk c + 3 into them
+            if (st == 0 && c + kStages < nchunks) issue_load(c + kStages);
 
             // ---- S6: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
 #pragma unroll
@@ -710,14 +746,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // before shared memory and TMEM are released: a commit tracks every
         // earlier MMA of the thread that issues it.
         if (tid == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
-        if (tid == 32 || tid == kPrepThreads) {
-            const int i = tid == 32 ? 0 : 1;
+        if (tid == kIssuer || tid == kPrepThreads) {
+            const int i = tid == kIssuer ? 0 : 1;
             umma_commit(&S.bar_drain[i]);
             mbar_wait(&S.bar_drain[i], 0, kWaitNs / 4);
         }
         if (tid == kPrepThreads)
-            for (int s = 0; s < 2; ++s)
-                if (pending[s] >= 0) mbar_wait(&S.bar_load[s], (pending[s] >> 1) & 1, kWaitNs / 4);
+            for (int ls = 0; ls < kStages; ++ls)
+                if (pending[ls] >= 0) mbar_wait(&S.bar_load[ls], (pending[ls] / kStages) & 1, kWaitNs / 4);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
