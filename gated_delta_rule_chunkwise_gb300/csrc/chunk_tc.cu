@@ -69,10 +69,12 @@ constexpr int kPrepThreads = 256;
 constexpr int kSerialThreads = 128;
 constexpr int kThreads = kPrepThreads + kSerialThreads;
 constexpr uint32_t kBarPrep = 1, kBarSerial = 2;   // named barrier ids
+constexpr uint32_t kBarBuild = 3, kBarBuildIssue = 4;   // KDA operand build (warps 4-7; + issuer warp 3)
 constexpr int kIssuer = 96;                        // prep thread issuing every prep MMA (warp 3)
 constexpr int kGateWarp = 4;                       // prep warp computing gate prefixes
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
 constexpr float kMaxLogSpan = 60.f;                // factored decay limit (e^60 per factor)
+constexpr float kKdaMaxSpan = 8.f;                 // KDA: fp16 factors e^{+-(G - m)} stay below e^8
 
 // TMEM columns (fp32, 128 lanes).
 constexpr uint32_t kColD1 = 0;      // 64   MMA1
@@ -85,24 +87,37 @@ constexpr uint32_t kTmemCols = 512;
 // Shared memory (bytes from a 1024-aligned base).
 constexpr uint32_t kQKBytes = 2 * 16384;      // [Q;K], 2 blocks of 128 rows x 128 B
 constexpr uint32_t kVBytes = 8192;            // V slice, 64 rows x 128 B
-constexpr int kStages = 3;                    // ring of input tiles (chunk c in stage c % 3)
-constexpr uint32_t kOffQK = 0;                // kStages x [Q;K]
-constexpr uint32_t kOffV = kOffQK + kStages * kQKBytes;   // kStages x V slice
-constexpr uint32_t kOffAK = kOffV + kStages * kVBytes;    // [-P Tw ; Tw] K-major 128 x 64      (16 KB)
-constexpr uint32_t kOffAV = kOffAK + 16384;        // [P Tu ; Tu] K-major 128 x 64       (16 KB)
-constexpr uint32_t kOffHB = kOffAV + 16384;        // H fp16, MN-major 128 x 64          (16 KB)
-constexpr uint32_t kOffUB = kOffHB + 16384;        // U~ fp16, MN-major 64 x 64          (8 KB)
-constexpr int kLd16 = 72;                            // fp16 row stride (144 B: ldmatrix conflict-free)
-constexpr uint32_t kOffA16 = kOffUB + 8192;          // fp16 A [64][72]
-constexpr uint32_t kOffP16 = kOffA16 + 64 * kLd16 * 2;  // fp16 P [64][72]
-constexpr uint32_t kOffT16 = kOffP16 + 64 * kLd16 * 2;  // fp16 T [64][72]
-constexpr uint32_t kOffX = kOffT16 + 64 * kLd16 * 2;  // fp16 16x16 scratch per chain warp [3][16][24]
-constexpr uint32_t kOffSmall = kOffX + 3072;
-constexpr uint32_t kSmallBytes = 6144;
-constexpr uint32_t kSmemBytes = kOffSmall + kSmallBytes + 1024;
+constexpr uint32_t kKBBytes = 16384;          // KDA side tile [64][128] fp16, K-major (2 blocks of 64 rows)
+constexpr int kLd16 = 72;                     // fp16 row stride (144 B: ldmatrix conflict-free)
+constexpr uint32_t kSmallBytes = 11264;
+constexpr int kMaxStages = 3;
+
+// Input tiles sit in a ring (chunk c in stage c % stages): three stages for
+// DeltaNet / Gated DeltaNet; two for KDA, whose two side tiles take the room.
+template <int MODE>
+struct Layout {
+    static constexpr bool kda = MODE == LDN_KDA;
+    static constexpr int stages = kda ? 2 : 3;
+    static constexpr uint32_t qk = 0;                              // stages x [Q;K]
+    static constexpr uint32_t v = qk + stages * kQKBytes;          // stages x V slice
+    static constexpr uint32_t kb = v + stages * kVBytes;           // KDA: 2 x side tile
+    static constexpr uint32_t ak = kb + (kda ? 2 * kKBBytes : 0);  // [-P Tw ; Tw] K-major 128 x 64 (16 KB)
+    static constexpr uint32_t av = ak + 16384;                     // [P Tu ; Tu] K-major 128 x 64  (16 KB)
+    static constexpr uint32_t hb = av + 16384;                     // H fp16, MN-major 128 x 64     (16 KB)
+    static constexpr uint32_t ub = hb + 16384;                     // U~ fp16, MN-major 64 x 64     (8 KB)
+    static constexpr uint32_t a16 = ub + 8192;                     // fp16 A [64][72]
+    static constexpr uint32_t p16 = a16 + 64 * kLd16 * 2;          // fp16 P [64][72]
+    static constexpr uint32_t t16 = p16 + 64 * kLd16 * 2;          // fp16 T [64][72]
+    static constexpr uint32_t x = t16 + 64 * kLd16 * 2;            // fp16 16x16 scratch per chain warp [3][16][24]
+    static constexpr uint32_t small = x + 3072;
+    static constexpr uint32_t bytes = small + kSmallBytes + 1024;
+    static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
+    static_assert(small % 16 == 0 && t16 % 16 == 0 && kb % 1024 == 0 && ak % 1024 == 0,
+                  "buffer alignment (16 B vector accesses, 1024 B swizzled tiles)");
+};
 
 struct Small {
-    uint64_t bar_load[kStages];   // TMA tiles of ring stage ls landed
+    uint64_t bar_load[kMaxStages];   // TMA tiles of ring stage ls landed
     uint64_t bar_pmma;        // prep MMA commits
     uint64_t bar_smma;        // serial MMA commits
     uint64_t bar_ready[2];    // MMA3 / MMA4 of stage s complete (prep commit)
@@ -112,20 +127,24 @@ struct Small {
     int fail;
     // Per-chunk gate data, slot = chunk % 3: written one chunk ahead by the gate
     // warp, read by the prep warps and (eg, egc, gC) by the serial warps.
-    int exact[kStages];       // per-entry exponentials for this chunk
-    float gC[kStages];        // e^{g_C}
-    alignas(16) float beta[kStages][kC];
-    alignas(16) float g[kStages][kC];     // inclusive log-decay prefix
-    alignas(16) float fr[kStages][kC];    // e^{g_r - m}
-    alignas(16) float fc[kStages][kC];    // e^{m - g_j}
-    alignas(16) float eg[kStages][kC];    // e^{g_r}
-    alignas(16) float egc[kStages][kC];   // e^{g_C - g_r}
+    int exact[3];             // per-entry exponentials for this chunk
+    float gC[3];              // e^{g_C}
+    int kflag[3][4];          // KDA: a channel of this chunk exceeds the factored span (one word per build warp)
+    alignas(16) float beta[3][kC];
+    alignas(16) float g[3][kC];      // inclusive log-decay prefix
+    alignas(16) float fr[3][kC];     // e^{g_r - m}
+    alignas(16) float fc[3][kC];     // e^{m - g_j}
+    alignas(16) float eg[3][kC];     // e^{g_r}
+    alignas(16) float egc[3][kC];    // e^{g_C - g_r}
+    // KDA, per key channel: e^{m}, e^{g_C - m}, e^{g_C} (m, g_C: the channel's
+    // log-decay prefix at rows 31 and 63)
+    alignas(16) float em[3][kDK];
+    alignas(16) float egcm[3][kDK];
+    alignas(16) float egC[3][kDK];
     float stg_beta[2][kC];    // beta / log-gate of the next chunk, prefetched by cp.async
     float stg_gate[2][kC];
 };
 static_assert(sizeof(Small) <= kSmallBytes, "Small does not fit its shared-memory slot");
-static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
-static_assert(kOffSmall % 16 == 0 && kOffT16 % 16 == 0, "vector accesses need 16-byte aligned buffers");
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b)
 {
@@ -161,6 +180,41 @@ __device__ __forceinline__ void ld_row8_bf16(const uint8_t *block, int row, int 
     }
 }
 
+// 8 fp16 values of a swizzled tile, widened to fp32.
+__device__ __forceinline__ void ld_row8_f16(const uint8_t *block, int row, int col, float *v)
+{
+    const uint4 u = *reinterpret_cast<const uint4 *>(block + sw128_offset(row, col));
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+// In-place scaling of the fp16 elements of swizzled K-major tiles by a factor per
+// column (key channel): `bytes` of blocks of `rows` rows x 64 columns, block kb
+// covering channels 64 kb .. 64 kb + 63; f[ch] is the factor of channel ch.
+__device__ __forceinline__ void tile_scale_cols_f16(uint8_t *p, int bytes, int rows, const float *f, int t, int n)
+{
+    for (int o = t * 16; o < bytes; o += n * 16) {
+        const int blk = o / (rows * 128), rr = (o % (rows * 128)) >> 7, pc = (o >> 4) & 7;
+        const int col0 = 64 * blk + 8 * (pc ^ (rr & 7));
+        uint4 u = *reinterpret_cast<const uint4 *>(p + o);
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const float4 f0 = *reinterpret_cast<const float4 *>(f + col0);
+        const float4 f1 = *reinterpret_cast<const float4 *>(f + col0 + 4);
+        const float ff[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __half22float2(*reinterpret_cast<__half2 *>(&w[i]));
+            w[i] = pack_h2(x.x * ff[2 * i], x.y * ff[2 * i + 1]);
+        }
+        *reinterpret_cast<uint4 *>(p + o) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // In-place bf16 -> fp16 conversion of `bytes` of a tile by `n` threads.
 __device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int t, int n)
 {
@@ -187,13 +241,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
     // array so that every access below stays a shared-memory access.
     uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
-    Small &S = *reinterpret_cast<Small *>(sm + kOffSmall);
-    __half *A16 = reinterpret_cast<__half *>(sm + kOffA16);
-    __half *P16 = reinterpret_cast<__half *>(sm + kOffP16);
-    __half *T16 = reinterpret_cast<__half *>(sm + kOffT16);
-    __half *X16 = reinterpret_cast<__half *>(sm + kOffX);
-    uint8_t *AK = sm + kOffAK, *AV = sm + kOffAV;
-    uint8_t *HB = sm + kOffHB, *UB = sm + kOffUB;
+    using LY = Layout<MODE>;
+    constexpr int kStages = LY::stages;
+    constexpr bool kKda = MODE == LDN_KDA;
+    Small &S = *reinterpret_cast<Small *>(sm + LY::small);
+    __half *A16 = reinterpret_cast<__half *>(sm + LY::a16);
+    __half *P16 = reinterpret_cast<__half *>(sm + LY::p16);
+    __half *T16 = reinterpret_cast<__half *>(sm + LY::t16);
+    __half *X16 = reinterpret_cast<__half *>(sm + LY::x);
+    uint8_t *AK = sm + LY::ak, *AV = sm + LY::av;
+    uint8_t *HB = sm + LY::hb, *UB = sm + LY::ub;
+    uint8_t *KB = sm + LY::kb;   // KDA side tiles (chunk c in KB + (c & 1) * kKBBytes)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slices = dv / kDVS;
@@ -228,7 +286,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
-    int pending[kStages] = {-1, -1, -1};   // chunk last loaded into ring stage ls (serial thread 0)
+    int pending[kMaxStages] = {-1, -1, -1};   // chunk last loaded into ring stage ls (serial thread 0)
 
     if (tid < kPrepThreads) {
         // ============================== PREP ==============================
@@ -237,10 +295,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int row = 32 * quad + lane;          // TMEM lane of this thread
         const bool issuer = (pt == kIssuer);
         uint32_t pphase = 0;
+        // Every prep thread takes the same decision (an OR over the role's barrier),
+        // whatever the serial warps write to S.fail meanwhile.
         auto prep_vote = [&](bool ok) -> bool {
-            if (!ok) S.fail = 1;
-            named_sync(kBarPrep, kPrepThreads);
-            return S.fail == 0;
+            const bool bad = named_sync_or(kBarPrep, kPrepThreads, !ok || S.fail != 0);
+            if (bad && pt == 0) S.fail = 1;
+            return !bad;
         };
         // MMA-completion and hand-off barriers: one thread polls, the others
         // block in the role's named barrier; tcgen05 ordering follows the sync.
@@ -270,7 +330,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // Gate prefix and decay factors of chunk cc into slot cc % 3 (gate warp, two
         // rows per lane); then the staging of chunk cc + 1 is started.
         auto compute_gates = [&](int cc) {
-            const int sg = cc & 1, gs = cc % kStages;
+            const int sg = cc & 1, gs = cc % 3;
             cp_async_wait<0>();          // chunk cc's staged beta / gates
             __syncwarp();
             const int r0 = 2 * lane, r1 = r0 + 1;
@@ -311,17 +371,114 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int ls = cc % kStages;
             if (!mbar_wait(&S.bar_load[ls], (cc / kStages) & 1, kWaitNs)) return false;
             tc_fence_after();
-            const uint32_t qk = smem_u32(sm + kOffQK + ls * kQKBytes);
+            const uint32_t qk = smem_u32(sm + LY::qk + ls * kQKBytes);
             for (int k = 0; k < kDK / 16; ++k)
                 umma_bf16(tbase + kColD1, kmajor_desc(qk, 128, k), kmajor_desc(qk + 8192, 128, k), id_m128_n64, k > 0);
             umma_commit(&S.bar_pmma);
             return true;
         };
+        auto zero_upper_avak = [&]() {
+            for (int e = pt; e < 6 * 16 * 2 * 2; e += kPrepThreads) {
+                const int blkid = e / 64, rem = e % 64;          // 6 blocks x 16 rows x 2 halves x 2 tiles
+                // (R, i) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                const int R = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
+                const int i = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
+                const int rr = 16 * R + (rem >> 2), cc = 16 * i + 8 * ((rem >> 1) & 1);
+                uint8_t *dst = (rem & 1) ? AK : AV;
+                *reinterpret_cast<uint4 *>(dst + sw128_offset(rr, cc)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        // KDA: per-channel log-decay prefix G of chunk cc and the fp16 MMA1 operands
+        // (build warps 4-7, thread = key channel).  The decay ratio e^{G_r - G_j} of
+        // each channel is split about row 31 (m): the tile's Q and K rows become
+        // Q e^{G - m}, K e^{G - m} in place, the side tile gets K e^{m - G}, so the
+        // products carry exactly the decay of every pair of rows.  If |G - m| of some
+        // channel exceeds kKdaMaxSpan the chunk keeps its bf16 tiles and is formed
+        // entry by entry instead (kflag).  Called after the chunk's tiles landed and,
+        // for warp 4, after the serial warps released gate slot cc % 3.
+        auto kda_build = [&](int cc) {
+            const int ch = pt - 128, ls = cc % kStages, gs = cc % 3, tb = cc * kC, LL = min(kC, T - tb);
+            const float *gp = gate + (((size_t)b * T + tb) * H + h) * kDK + ch;
+            const size_t rstride = (size_t)H * kDK;
+            float G[kC];
+#pragma unroll
+            for (int r = 0; r < kC; ++r) {
+                const float x = __ldg(gp + (size_t)min(r, LL - 1) * rstride);   // rows past T: zero
+                G[r] = r < LL ? x : 0.f;
+            }
+#pragma unroll
+            for (int r = 1; r < kC; ++r) G[r] += G[r - 1];
+            const float m = G[31], gc = G[63];
+            float span = 0.f;
+#pragma unroll
+            for (int r = 0; r < kC; ++r) span = fmaxf(span, fabsf(G[r] - m));
+            const bool wide = !(span <= kKdaMaxSpan);   // NaN gates take the entry-wise path too
+            const bool any = __any_sync(0xffffffffu, wide);
+            if (lane == 0) S.kflag[gs][warp - 4] = any ? 1 : 0;
+            named_sync(kBarBuild, 128);
+            const bool exact = (S.kflag[gs][0] | S.kflag[gs][1] | S.kflag[gs][2] | S.kflag[gs][3]) != 0;
+            S.egC[gs][ch] = expf(gc);
+            if (!exact) {
+                S.em[gs][ch] = expf(m);
+                S.egcm[gs][ch] = expf(gc - m);
+                uint8_t *qk = sm + LY::qk + ls * kQKBytes + (ch >> 6) * 16384;
+                uint8_t *kbt = KB + (cc & 1) * kKBBytes + (ch >> 6) * 8192;
+                const int col = ch & 63;
+#pragma unroll
+                for (int r = 0; r < kC; ++r) {
+                    const float ep = expf(G[r] - m), en = expf(m - G[r]);
+                    uint8_t *qp = qk + sw128_offset(r, col), *kp = qk + sw128_offset(64 + r, col);
+                    const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qp));
+                    const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kp));
+                    *reinterpret_cast<__half *>(qp) = __float2half_rn(qv * ep);
+                    *reinterpret_cast<__half *>(kp) = __float2half_rn(kv * ep);
+                    *reinterpret_cast<__half *>(kbt + sw128_offset(r, col)) = __float2half_rn(kv * en);
+                }
+            }
+            fence_proxy_async_smem();
+        };
+        const uint32_t id_m128_n64_f16 = idesc_f16kind_f32(128, 64, 0, 0, kMmaF16);   // MMA1 (KDA, fp16)
+        auto kda_exact = [&](int cc) -> bool {
+            const int gs = cc % 3;
+            return (S.kflag[gs][0] | S.kflag[gs][1] | S.kflag[gs][2] | S.kflag[gs][3]) != 0;
+        };
+        // KDA MMA1 [Q e^{G-m} ; K e^{G-m}] (K e^{m-G})^T (issuer, after the build);
+        // the commit is made even when the chunk is formed entry by entry.
+        auto kda_issue_mma1 = [&](int cc) {
+            const int ls = cc % kStages;
+            tc_fence_after();
+            if (!kda_exact(cc)) {
+                const uint32_t qk = smem_u32(sm + LY::qk + ls * kQKBytes);
+                const uint32_t kbt = smem_u32(KB + (cc & 1) * kKBBytes);
+                for (int k = 0; k < kDK / 16; ++k)
+                    umma_bf16(tbase + kColD1, kmajor_desc(qk, 128, k), kmajor_desc(kbt, 64, k), id_m128_n64_f16,
+                              k > 0);
+            }
+            umma_commit(&S.bar_pmma);
+        };
+        // build warps: wait for the TMA tiles of chunk cc (one poll per warp)
+        auto build_wait_tiles = [&](int cc) {
+            const int ls = cc % kStages;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&S.bar_load[ls], (cc / kStages) & 1, kWaitNs);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) S.fail = 1;
+        };
         if (warp == kGateWarp) {
             prefetch_gates(0);
             compute_gates(0);
         }
-        if (issuer && !issue_mma1(0)) S.fail = 1;
+        if constexpr (kKda) {
+            if (warp >= 4) {
+                build_wait_tiles(0);
+                kda_build(0);
+                named_sync(kBarBuildIssue, 160);
+            } else if (warp == kIssuer / 32) {
+                named_sync(kBarBuildIssue, 160);
+                if (issuer) kda_issue_mma1(0);
+            }
+        } else {
+            if (issuer && !issue_mma1(0)) S.fail = 1;
+        }
         // The strictly-upper 16x16 blocks of T and of the top halves of AV / AK
         // (the blocks of P T above the diagonal) are zero for every chunk and
         // nothing else writes them: clear them once.
@@ -329,28 +486,93 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int r = e >> 6, j = e & 63;
             if ((j >> 4) > (r >> 4)) T16[r * kLd16 + j] = __float2half_rn(0.f);
         }
-        for (int e = pt; e < 6 * 16 * 2 * 2; e += kPrepThreads) {
-            const int blkid = e / 64, rem = e % 64;          // 6 blocks x 16 rows x 2 halves x 2 tiles
-            // (R, i) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-            const int R = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
-            const int i = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-            const int rr = 16 * R + (rem >> 2), cc = 16 * i + 8 * ((rem >> 1) & 1);
-            uint8_t *dst = (rem & 1) ? AK : AV;
-            *reinterpret_cast<uint4 *>(dst + sw128_offset(rr, cc)) = make_uint4(0u, 0u, 0u, 0u);
-        }
+        zero_upper_avak();
         named_sync(kBarPrep, kPrepThreads);
 
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1, ls = c % kStages, gs = ls;
-            uint8_t *QK = sm + kOffQK + ls * kQKBytes;
-            uint8_t *Vt = sm + kOffV + ls * kVBytes;
+            const int s = c & 1, ls = c % kStages, gs = c % 3;
+            uint8_t *QK = sm + LY::qk + ls * kQKBytes;
+            uint8_t *Vt = sm + LY::v + ls * kVBytes;
             const uint32_t qk_s = smem_u32(QK), k_s = qk_s + 8192, v_s = smem_u32(Vt);
 
             // ---- P1: MMA1 of chunk c (issued while chunk c - 1 was prepared) complete
             if (!wait_pmma()) break;
+            const bool kexact = kKda && kda_exact(c);
+
+            if constexpr (kKda) {
+                if (kexact) {
+                    // ---- P4 (KDA, decay span beyond the fp16 factors): A and P entry by entry.
+                    // AV / AK, free once MMA3 / MMA4 of chunk c - 1 completed, hold the fp32
+                    // per-channel log-decay prefix G [64][128] meanwhile.
+                    if (!prep_vote(pt == 0 && c >= 1 ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1,
+                                                                 kWaitNs)
+                                                     : true))
+                        break;
+                    float *Gs = reinterpret_cast<float *>(AK);
+                    if (pt < kDK) {
+                        const int tb = c * kC, LL = min(kC, T - tb);
+                        const float *gp = gate + (((size_t)b * T + tb) * H + h) * kDK + pt;
+                        float acc = 0.f;
+                        for (int r = 0; r < kC; ++r) {
+                            if (r < LL) acc += __ldg(gp + (size_t)r * H * kDK);
+                            Gs[r * kDK + pt] = acc;
+                        }
+                    }
+                    named_sync(kBarPrep, kPrepThreads);
+                    {   // A_rj = beta_r sum_ch k_r k_j e^{G_r - G_j} (j < r); P_rj = sum_ch q_r k_j e^{G_r - G_j} (j <= r)
+                        const int isA = pt >> 7, r = (pt >> 1) & 63, j0 = 32 * (pt & 1);
+                        const int jmax = isA ? r - 1 : r;
+                        float acc[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                        if (j0 <= jmax) {
+                            for (int ch = 0; ch < kDK; ++ch) {
+                                const uint8_t *blk = QK + (ch >> 6) * 16384;
+                                const int col = ch & 63;
+                                const float xr = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                    blk + sw128_offset(isA ? 64 + r : r, col)));
+                                const float gr = Gs[r * kDK + ch];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    if (j0 + i <= jmax) {
+                                        const float kj = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                            blk + sw128_offset(64 + j0 + i, col)));
+                                        acc[i] += xr * kj * expf(gr - Gs[(j0 + i) * kDK + ch]);
+                                    }
+                                }
+                            }
+                        }
+                        const float sc = isA ? S.beta[gs][r] : 1.f;
+                        __half *dst = (isA ? A16 : P16) + r * kLd16 + j0;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            *reinterpret_cast<uint32_t *>(dst + i) = pack_h2(j0 + i <= jmax ? acc[i] * sc : 0.f,
+                                                                             j0 + i + 1 <= jmax ? acc[i + 1] * sc : 0.f);
+                    }
+                    named_sync(kBarPrep, kPrepThreads);
+                    {   // Q^ = Q e^{G}, K^ = K e^{G} in place; K~ = K e^{G_C - G} into the side tile
+                        uint8_t *kbt = KB + (c & 1) * kKBBytes;
+                        for (int e = pt; e < kC * kDK; e += kPrepThreads) {
+                            const int r = e >> 7, ch = e & 127, col = ch & 63;
+                            uint8_t *blk = QK + (ch >> 6) * 16384;
+                            const float gv = Gs[r * kDK + ch], gcv = Gs[(kC - 1) * kDK + ch];
+                            uint8_t *qp = blk + sw128_offset(r, col), *kp = blk + sw128_offset(64 + r, col);
+                            const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qp));
+                            const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kp));
+                            const float eg = expf(gv);
+                            *reinterpret_cast<__half *>(qp) = __float2half_rn(qv * eg);
+                            *reinterpret_cast<__half *>(kp) = __float2half_rn(kv * eg);
+                            *reinterpret_cast<__half *>(kbt + (ch >> 6) * 8192 + sw128_offset(r, col)) =
+                                __float2half_rn(kv * expf(gcv - gv));
+                        }
+                    }
+                    named_sync(kBarPrep, kPrepThreads);
+                    zero_upper_avak();   // G overwrote the constant zero blocks of AV / AK
+                }
+            }
 
             // ---- P4: P and A (fp16) from MMA1, with decay factors, beta and masks
-            {
+            if (!kexact) {
                 const bool isP = row < 64;
                 const int r = isP ? row : row - 64;
                 const float frr = S.fr[gs][r] * (isP ? 1.f : S.beta[gs][r]), gr = S.g[gs][r];
@@ -402,8 +624,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
             else {   // the other prep threads convert the k and v tiles to fp16 meanwhile
-                tile_bf16_to_f16(QK + 8192, 8192, pt - 64, kPrepThreads - 64);           // K, block 0
-                tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
+                if constexpr (kKda) {
+                    if (!kexact) {
+                        // Q e^{G-m}, K e^{G-m} -> Q^ = Q e^{G}, K^ = K e^{G} (times e^{m});
+                        // K e^{m-G} -> K~ = K e^{G_C - G} (times e^{G_C - m})
+                        tile_scale_cols_f16(QK, kQKBytes, 128, S.em[gs], pt - 64, kPrepThreads - 64);
+                        tile_scale_cols_f16(KB + (c & 1) * kKBBytes, kKBBytes, 64, S.egcm[gs], pt - 64,
+                                            kPrepThreads - 64);
+                    }
+                } else {
+                    tile_bf16_to_f16(QK + 8192, 8192, pt - 64, kPrepThreads - 64);           // K, block 0
+                    tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
+                }
                 tile_bf16_to_f16(Vt, kVBytes, pt - 64, kPrepThreads - 64);
             }
             named_sync(kBarPrep, kPrepThreads);
@@ -451,18 +683,32 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             } else if (warp == kIssuer / 32) {
                 // look-ahead: MMA1 of chunk c + 1 into D1 (read by P4 above)
-                if (issuer && c + 1 < nchunks && !issue_mma1(c + 1)) S.fail = 1;
-            } else if (warp == kGateWarp) {
-                // The serial warps have read the accumulators and gate slot of chunk
-                // c - 2 (needed before MMA3 / MMA4 of chunk c overwrite RV[s], DK[s],
-                // and before slot (c + 1) % 3 = (c - 2) % 3 is rewritten).
-                bool ok = true;
-                if (c >= 2 && lane == 0) ok = mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) {
-                    if (lane == 0) S.fail = 1;
-                } else if (c + 1 < nchunks) {
-                    compute_gates(c + 1);
+                if constexpr (kKda) {
+                    named_sync(kBarBuildIssue, 160);   // operands of chunk c + 1 built
+                    if (issuer && c + 1 < nchunks) kda_issue_mma1(c + 1);
+                } else {
+                    if (issuer && c + 1 < nchunks && !issue_mma1(c + 1)) S.fail = 1;
+                }
+            } else {
+                if (warp == kGateWarp) {
+                    // The serial warps have read the accumulators and gate slot of chunk
+                    // c - 2 (needed before MMA3 / MMA4 of chunk c overwrite RV[s], DK[s],
+                    // and before slot (c + 1) % 3 = (c - 2) % 3 is rewritten).
+                    bool ok = true;
+                    if (c >= 2 && lane == 0) ok = mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) {
+                        if (lane == 0) S.fail = 1;
+                    } else if (c + 1 < nchunks) {
+                        compute_gates(c + 1);
+                    }
+                }
+                if constexpr (kKda) {   // warps 4-7: KDA operands of chunk c + 1
+                    if (c + 1 < nchunks) {
+                        build_wait_tiles(c + 1);
+                        kda_build(c + 1);
+                    }
+                    named_sync(kBarBuildIssue, 160);
                 }
             }
             // MMA3 / MMA4 of chunk c - 1 have finished reading AV / AK before they are rewritten
@@ -563,9 +809,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int st = tid - kPrepThreads;   // = TMEM lane = state row
         uint32_t sphase = 0;
         auto serial_vote = [&](bool ok) -> bool {
-            if (!ok) S.fail = 1;
-            named_sync(kBarSerial, kSerialThreads);
-            return S.fail == 0;
+            const bool bad = named_sync_or(kBarSerial, kSerialThreads, !ok || S.fail != 0);
+            if (bad && st == 0) S.fail = 1;
+            return !bad;
         };
         auto wait_smma = [&]() -> bool {
             const bool ok = (st == 0) ? mbar_wait(&S.bar_smma, sphase, kWaitNs) : true;
@@ -576,8 +822,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         };
         auto issue_load = [&](int c) {
             const int ls = c % kStages;
-            uint8_t *qk = sm + kOffQK + ls * kQKBytes;
-            uint8_t *vv = sm + kOffV + ls * kVBytes;
+            uint8_t *qk = sm + LY::qk + ls * kQKBytes;
+            uint8_t *vv = sm + LY::v + ls * kVBytes;
             pending[ls] = c;
             mbar_arrive_expect_tx(&S.bar_load[ls], 2 * 16384 + 8192);
             for (int kb = 0; kb < 2; ++kb) {
@@ -607,13 +853,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
-            const uint8_t *QK = sm + kOffQK + (c % kStages) * kQKBytes;
+            const uint8_t *QK = sm + LY::qk + (c % kStages) * kQKBytes;
             const uint32_t k_s = smem_u32(QK) + 8192;
 
             // ---- S1: MMA3 / MMA4 of chunk c complete (RV[s] = [P U' ; U'], DK[s] = [-P W ; W])
             if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
             tc_fence_after();
-            const int gs = c % kStages;
+            const int gs = c % 3;
             const float gC = S.gC[gs];
             const bool top = st < 64;
             const float egc = top ? 0.f : S.egc[gs][st - 64];
@@ -624,7 +870,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             //      read from tensor memory.  Each thread rewrites only columns of its own
             //      lane that it has already read.
             {
-                const float er = top ? S.eg[gs][st] : 0.f;
+                const float er = kKda ? 1.f : (top ? S.eg[gs][st] : 0.f);   // KDA: Q^ holds e^{G} already
                 const uint32_t dk_col = tbase + lane_base + (s ? kColDK1 : kColDK0);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
@@ -639,7 +885,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                             for (int j = 0; j < 32; j += 8) {
                                 float qv[8];
-                                ld_row8_bf16(qblk, st, cc + j, qv);
+                                if constexpr (kKda) ld_row8_f16(qblk, st, cc + j, qv);
+                                else ld_row8_bf16(qblk, st, cc + j, qv);
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) v[j + i] += er * qv[i];
                             }
@@ -702,16 +949,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // ---- S5: MMA6: K^T U~ -> D6
                 tc_fence_after();
                 const uint32_t ub_s = smem_u32(UB);
+                // A = K^T (GDN, DeltaNet: U~ carries the decay) or K~^T (KDA, side tile)
+                const uint32_t ka_s = kKda ? smem_u32(KB + (c & 1) * kKBBytes) : k_s;
                 for (int k = 0; k < kC / 16; ++k)
-                    umma_bf16(tbase + kColD6, mnmajor_desc(k_s, 128, k), mnmajor_desc(ub_s, 64, k), id_m128_n64_amn,
-                              k > 0);
+                    umma_bf16(tbase + kColD6, mnmajor_desc(ka_s, kKda ? 64 : 128, k), mnmajor_desc(ub_s, 64, k),
+                              id_m128_n64_amn, k > 0);
                 umma_commit(&S.bar_smma);
             }
             if (!wait_smma()) break;
-            // the tiles of chunk c are no longer read by anyone: fetch chunk c + 3 into them
+            // the tiles of chunk c are no longer read by anyone: fetch chunk c + stages into them
             if (st == 0 && c + kStages < nchunks) issue_load(c + kStages);
 
             // ---- S6: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
+            const float gCr = kKda ? S.egC[gs][st] : gC;   // KDA: decay of key channel st
 #pragma unroll
             for (int n = 0; n < kDVS; n += 32) {
                 float v[32];
@@ -720,7 +970,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    Hreg[n + i] = gC * Hreg[n + i] + v[i];
+                    Hreg[n + i] = gCr * Hreg[n + i] + v[i];
                     v[i] = Hreg[n + i];
                 }
                 st_row16(HB, st, n, v);
@@ -764,7 +1014,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 bool chunk_tc_supported(const ChunkArgs &a)
 {
     return a.dtype == LDN_BF16 && a.dk == kDK && a.dv % kDVS == 0 && a.chunk == kC &&
-           (a.mode == LDN_DELTANET || a.mode == LDN_GDN);
+           (a.mode == LDN_DELTANET || a.mode == LDN_GDN || a.mode == LDN_KDA);
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
@@ -775,11 +1025,18 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
         !make_tmap_bf16_4d(&tv, a.v, a.dv, a.H, a.T, a.B, 64, kC))
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDVS));
-    auto kern = a.mode == LDN_GDN ? chunk_tc_kernel<LDN_GDN> : chunk_tc_kernel<LDN_DELTANET>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto go = [&](auto kern, uint32_t smem) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out, a.S_final,
+                                           a.T, a.H, a.dv, a.status);
+        return cudaSuccess;
+    };
+    cudaError_t e;
+    if (a.mode == LDN_GDN) e = go(chunk_tc_kernel<LDN_GDN>, Layout<LDN_GDN>::bytes);
+    else if (a.mode == LDN_KDA) e = go(chunk_tc_kernel<LDN_KDA>, Layout<LDN_KDA>::bytes);
+    else e = go(chunk_tc_kernel<LDN_DELTANET>, Layout<LDN_DELTANET>::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out, a.S_final,
-                                             a.T, a.H, a.dv, a.status);
     return cudaGetLastError();
 }
 

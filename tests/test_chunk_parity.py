@@ -143,6 +143,33 @@ def test_strong_gdn_gates():
     check(w)
 
 
+@pytest.mark.parametrize("variant", [ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SIMT])
+def test_kda_tensor_and_simt_paths(variant):
+    """KDA through the tensor-core kernel (per-channel decay split about the
+    chunk's middle row) and through the CUDA-core kernel, on the same inputs."""
+    w = wl.make_chunk(BASE[2], B=2, T=333, H=3, s0=True)
+    check(w, variant)
+
+
+def test_kda_strong_channel_gates_entrywise_chunks():
+    """Per-channel decays strong enough (log a ~ -1.2 on a few channels, in some
+    chunks only) that the fp16 decay factors would leave their range: those
+    chunks are formed entry by entry, the others through the factored MMA."""
+    w = wl.make_chunk(BASE[2], B=1, T=320, H=2, s0=True)
+    g = w.gate.copy()
+    g[:, 64:192, :, 5] = -1.2      # chunks 1 and 2, channel 5
+    g[:, 256:300, 1, 100] = -0.9   # chunk 4, head 1, channel 100
+    w.gate = g.astype(np.float32)
+    check(w, ldn.LDN_VARIANT_TENSOR)
+
+
+def test_kda_all_chunks_entrywise():
+    """Every chunk beyond the factored range (log a = -0.6 on every channel)."""
+    w = wl.make_chunk(BASE[2], B=1, T=200, H=2, s0=True)
+    w.gate = np.full_like(w.gate, -0.6)
+    check(w, ldn.LDN_VARIANT_TENSOR)
+
+
 # ---- full-size workloads in the benchmark's launch configuration, sampled ----
 def _sampled(name, picks, **over):
     import torch
