@@ -101,7 +101,8 @@ struct Layout {
     static constexpr uint32_t qk = 0;                              // stages x [Q;K]
     static constexpr uint32_t v = qk + stages * kQKBytes;          // stages x V slice
     static constexpr uint32_t kb = v + stages * kVBytes;           // KDA: 2 x side tile
-    static constexpr uint32_t ak = kb + (kda ? 2 * kKBBytes : 0);  // [-P Tw ; Tw] K-major 128 x 64 (16 KB)
+    static constexpr uint32_t akc = kb + (kda ? 2 * kKBBytes : 0); // KDA: [I ; 0] K-major 128 x 64 (16 KB, constant)
+    static constexpr uint32_t ak = akc + (kda ? 16384 : 0);        // [-P Tw ; Tw] K-major 128 x 64 (16 KB)
     static constexpr uint32_t av = ak + 16384;                     // [P Tu ; Tu] K-major 128 x 64  (16 KB)
     static constexpr uint32_t hb = av + 16384;                     // H fp16, MN-major 128 x 64     (16 KB)
     static constexpr uint32_t ub = hb + 16384;                     // U~ fp16, MN-major 64 x 64     (8 KB)
@@ -112,7 +113,7 @@ struct Layout {
     static constexpr uint32_t small = x + 3072;
     static constexpr uint32_t bytes = small + kSmallBytes + 1024;
     static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
-    static_assert(small % 16 == 0 && t16 % 16 == 0 && kb % 1024 == 0 && ak % 1024 == 0,
+    static_assert(small % 16 == 0 && t16 % 16 == 0 && kb % 1024 == 0 && akc % 1024 == 0 && ak % 1024 == 0,
                   "buffer alignment (16 B vector accesses, 1024 B swizzled tiles)");
 };
 
@@ -123,6 +124,7 @@ struct Small {
     uint64_t bar_ready[2];    // MMA3 / MMA4 of stage s complete (prep commit)
     uint64_t bar_rvfree[2];   // serial finished reading RV[s] and DK[s]
     uint64_t bar_drain[2];    // failure path: last commit of each MMA issuer
+    uint64_t bar_kbfree[2];   // KDA: MMA6 of chunk c finished reading side tile c & 1
     uint32_t tmem_base;
     int fail;
     // Per-chunk gate data, slot = chunk % 3: written one chunk ahead by the gate
@@ -177,41 +179,6 @@ __device__ __forceinline__ void ld_row8_bf16(const uint8_t *block, int row, int 
         const float2 f = __bfloat1622float2(h[i]);
         v[2 * i] = f.x;
         v[2 * i + 1] = f.y;
-    }
-}
-
-// 8 fp16 values of a swizzled tile, widened to fp32.
-__device__ __forceinline__ void ld_row8_f16(const uint8_t *block, int row, int col, float *v)
-{
-    const uint4 u = *reinterpret_cast<const uint4 *>(block + sw128_offset(row, col));
-    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h[i]);
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
-    }
-}
-
-// In-place scaling of the fp16 elements of swizzled K-major tiles by a factor per
-// column (key channel): `bytes` of blocks of `rows` rows x 64 columns, block kb
-// covering channels 64 kb .. 64 kb + 63; f[ch] is the factor of channel ch.
-__device__ __forceinline__ void tile_scale_cols_f16(uint8_t *p, int bytes, int rows, const float *f, int t, int n)
-{
-    for (int o = t * 16; o < bytes; o += n * 16) {
-        const int blk = o / (rows * 128), rr = (o % (rows * 128)) >> 7, pc = (o >> 4) & 7;
-        const int col0 = 64 * blk + 8 * (pc ^ (rr & 7));
-        uint4 u = *reinterpret_cast<const uint4 *>(p + o);
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        const float4 f0 = *reinterpret_cast<const float4 *>(f + col0);
-        const float4 f1 = *reinterpret_cast<const float4 *>(f + col0 + 4);
-        const float ff[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 x = __half22float2(*reinterpret_cast<__half2 *>(&w[i]));
-            w[i] = pack_h2(x.x * ff[2 * i], x.y * ff[2 * i + 1]);
-        }
-        *reinterpret_cast<uint4 *>(p + o) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -272,6 +239,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&S.bar_drain[1], 1);
         mbar_init(&S.bar_rvfree[0], 1);
         mbar_init(&S.bar_rvfree[1], 1);
+        mbar_init(&S.bar_kbfree[0], 1);
+        mbar_init(&S.bar_kbfree[1], 1);
         fence_mbar_init();
         S.fail = 0;
         tma_prefetch_desc(&tm_q);
@@ -388,51 +357,117 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 *reinterpret_cast<uint4 *>(dst + sw128_offset(rr, cc)) = make_uint4(0u, 0u, 0u, 0u);
             }
         };
+        // build warps: wait for the TMA tiles of chunk cc (one poll per warp)
+        auto build_wait_tiles = [&](int cc) {
+            const int ls = cc % kStages;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&S.bar_load[ls], (cc / kStages) & 1, kWaitNs);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) S.fail = 1;
+        };
         // KDA: per-channel log-decay prefix G of chunk cc and the fp16 MMA1 operands
         // (build warps 4-7, thread = key channel).  The decay ratio e^{G_r - G_j} of
         // each channel is split about row 31 (m): the tile's Q and K rows become
         // Q e^{G - m}, K e^{G - m} in place, the side tile gets K e^{m - G}, so the
         // products carry exactly the decay of every pair of rows.  If |G - m| of some
         // channel exceeds kKdaMaxSpan the chunk keeps its bf16 tiles and is formed
-        // entry by entry instead (kflag).  Called after the chunk's tiles landed and,
-        // for warp 4, after the serial warps released gate slot cc % 3.
-        auto kda_build = [&](int cc) {
-            const int ch = pt - 128, ls = cc % kStages, gs = cc % 3, tb = cc * kC, LL = min(kC, T - tb);
-            const float *gp = gate + (((size_t)b * T + tb) * H + h) * kDK + ch;
-            const size_t rstride = (size_t)H * kDK;
-            float G[kC];
+        // entry by entry instead (kflag).  The gate prefix does not need the tiles:
+        // it is formed while they are still landing.  Warp 4 calls this after the
+        // serial warps released gate slot cc % 3.
+        // thread = 8 key channels (ch0..ch0+7) x 8 consecutive rows (r0..r0+7); the 8
+        // row groups of a channel group are 8 consecutive lanes.  The log-gates are
+        // loaded (into G) a phase ahead of the rest, so their latency is hidden.
+        const int kt = pt - 128, kch0 = 8 * (4 * (kt >> 5) + ((lane >> 3) & 3)), krg = lane & 7;
+        auto kda_load_gates = [&](int cc, float (&G)[8][8]) {
+            const int tb = cc * kC, LL = min(kC, T - tb);
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                const float x = __ldg(gp + (size_t)min(r, LL - 1) * rstride);   // rows past T: zero
-                G[r] = r < LL ? x : 0.f;
+            for (int i = 0; i < 8; ++i) {
+                const int r = 8 * krg + i;
+                float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+                if (r < LL) {   // rows past T: zero
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(gate + (((size_t)b * T + tb + r) * H + h) * kDK + kch0);
+                    lo = __ldg(src);
+                    hi = __ldg(src + 1);
+                }
+                G[i][0] = lo.x; G[i][1] = lo.y; G[i][2] = lo.z; G[i][3] = lo.w;
+                G[i][4] = hi.x; G[i][5] = hi.y; G[i][6] = hi.z; G[i][7] = hi.w;
             }
+        };
+        auto kda_build = [&](int cc, float (&G)[8][8]) {
+            const int ch0 = kch0, rg = krg, r0 = 8 * rg, ls = cc % kStages, gs = cc % 3;
+            // inclusive prefix over the rows: within the thread, then across the row groups
 #pragma unroll
-            for (int r = 1; r < kC; ++r) G[r] += G[r - 1];
-            const float m = G[31], gc = G[63];
-            float span = 0.f;
+            for (int i = 1; i < 8; ++i)
 #pragma unroll
-            for (int r = 0; r < kC; ++r) span = fmaxf(span, fabsf(G[r] - m));
-            const bool wide = !(span <= kKdaMaxSpan);   // NaN gates take the entry-wise path too
+                for (int j = 0; j < 8; ++j) G[i][j] += G[i - 1][j];
+            float m[8], gc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float inc = G[7][j];
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, inc, o, 8);
+                    if (rg >= o) inc += y;
+                }
+                const float excl = inc - G[7][j];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) G[i][j] += excl;
+                m[j] = __shfl_sync(0xffffffffu, G[7][j], (lane & ~7) + 3);    // row 31
+                gc[j] = __shfl_sync(0xffffffffu, G[7][j], (lane & ~7) + 7);   // row 63
+            }
+            bool wide = false;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) wide |= !(fabsf(G[i][j] - m[j]) <= kKdaMaxSpan);   // NaN: entry-wise
             const bool any = __any_sync(0xffffffffu, wide);
             if (lane == 0) S.kflag[gs][warp - 4] = any ? 1 : 0;
             named_sync(kBarBuild, 128);
             const bool exact = (S.kflag[gs][0] | S.kflag[gs][1] | S.kflag[gs][2] | S.kflag[gs][3]) != 0;
-            S.egC[gs][ch] = expf(gc);
-            if (!exact) {
-                S.em[gs][ch] = expf(m);
-                S.egcm[gs][ch] = expf(gc - m);
-                uint8_t *qk = sm + LY::qk + ls * kQKBytes + (ch >> 6) * 16384;
-                uint8_t *kbt = KB + (cc & 1) * kKBBytes + (ch >> 6) * 8192;
-                const int col = ch & 63;
+            if (rg == 0) {   // per-channel factors the serial warps apply to MMA4 / MMA6 results
 #pragma unroll
-                for (int r = 0; r < kC; ++r) {
-                    const float ep = expf(G[r] - m), en = expf(m - G[r]);
-                    uint8_t *qp = qk + sw128_offset(r, col), *kp = qk + sw128_offset(64 + r, col);
-                    const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qp));
-                    const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kp));
-                    *reinterpret_cast<__half *>(qp) = __float2half_rn(qv * ep);
-                    *reinterpret_cast<__half *>(kp) = __float2half_rn(kv * ep);
-                    *reinterpret_cast<__half *>(kbt + sw128_offset(r, col)) = __float2half_rn(kv * en);
+                for (int j = 0; j < 8; ++j) {
+                    S.egC[gs][ch0 + j] = expf(gc[j]);
+                    S.em[gs][ch0 + j] = exact ? 1.f : expf(m[j]);
+                    S.egcm[gs][ch0 + j] = exact ? 1.f : expf(gc[j] - m[j]);
+                }
+            }
+            build_wait_tiles(cc);
+            if (cc >= 2) {   // side tile cc & 1: MMA6 of chunk cc - 2 has read it
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(&S.bar_kbfree[cc & 1], ((cc >> 1) - 1) & 1, kWaitNs);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) S.fail = 1;
+            }
+            if (!exact) {
+                uint8_t *qk = sm + LY::qk + ls * kQKBytes + (ch0 >> 6) * 16384;
+                uint8_t *kbt = KB + (cc & 1) * kKBBytes + (ch0 >> 6) * 8192;
+                const int col = ch0 & 63;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + i;
+                    float ep[8], en[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {   // |G - m| <= kKdaMaxSpan; rounded to fp16 below
+                        ep[j] = __expf(G[i][j] - m[j]);
+                        en[j] = __expf(m[j] - G[i][j]);
+                    }
+                    uint4 *qp = reinterpret_cast<uint4 *>(qk + sw128_offset(r, col));
+                    uint4 *kp = reinterpret_cast<uint4 *>(qk + sw128_offset(64 + r, col));
+                    uint4 *bp = reinterpret_cast<uint4 *>(kbt + sw128_offset(r, col));
+                    const uint4 qu = *qp, ku = *kp;
+                    const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qu);
+                    const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ku);
+                    uint32_t wq[4], wk[4], wb[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 qf = __bfloat1622float2(q2[u]), kf = __bfloat1622float2(k2[u]);
+                        wq[u] = pack_h2(qf.x * ep[2 * u], qf.y * ep[2 * u + 1]);
+                        wk[u] = pack_h2(kf.x * ep[2 * u], kf.y * ep[2 * u + 1]);
+                        wb[u] = pack_h2(kf.x * en[2 * u], kf.y * en[2 * u + 1]);
+                    }
+                    *qp = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    *kp = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                    *bp = make_uint4(wb[0], wb[1], wb[2], wb[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -456,29 +491,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             umma_commit(&S.bar_pmma);
         };
-        // build warps: wait for the TMA tiles of chunk cc (one poll per warp)
-        auto build_wait_tiles = [&](int cc) {
-            const int ls = cc % kStages;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(&S.bar_load[ls], (cc / kStages) & 1, kWaitNs);
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) S.fail = 1;
-        };
-        if (warp == kGateWarp) {
-            prefetch_gates(0);
-            compute_gates(0);
-        }
-        if constexpr (kKda) {
-            if (warp >= 4) {
-                build_wait_tiles(0);
-                kda_build(0);
-                named_sync(kBarBuildIssue, 160);
-            } else if (warp == kIssuer / 32) {
-                named_sync(kBarBuildIssue, 160);
-                if (issuer) kda_issue_mma1(0);
-            }
-        } else {
-            if (issuer && !issue_mma1(0)) S.fail = 1;
-        }
+        if (warp == kGateWarp) prefetch_gates(0);
         // The strictly-upper 16x16 blocks of T and of the top halves of AV / AK
         // (the blocks of P T above the diagonal) are zero for every chunk and
         // nothing else writes them: clear them once.
@@ -487,17 +500,37 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if ((j >> 4) > (r >> 4)) T16[r * kLd16 + j] = __float2half_rn(0.f);
         }
         zero_upper_avak();
+        if constexpr (kKda) {
+            // KDA: MMA4 runs over [Q^ ; K^] with A = [[I, -P Tw], [0, Tw]]; its first
+            // 64 columns, [I ; 0], are the same for every chunk
+            uint8_t *akc = sm + LY::akc;
+            for (int e = pt; e < 128 * 8; e += kPrepThreads) {
+                const int rr = e >> 3, c8 = 8 * (e & 7);
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                if (rr < 64 && rr >= c8 && rr < c8 + 8) {
+                    const int j = rr - c8;   // the 1.0 sits in half j of this 16-byte group
+                    w[j >> 1] = (j & 1) ? 0x3C000000u : 0x00003C00u;
+                }
+                *reinterpret_cast<uint4 *>(akc + sw128_offset(rr, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
         named_sync(kBarPrep, kPrepThreads);
 
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1, ls = c % kStages, gs = c % 3;
+        // Iteration c = -1 runs only the look-ahead part (gates, operands and MMA1 of
+        // chunk 0), so that code exists once.
+        for (int c = -1; c < nchunks; ++c) {
+            const int cp = c < 0 ? 0 : c;
+            const int s = cp & 1, ls = cp % kStages, gs = cp % 3;
             uint8_t *QK = sm + LY::qk + ls * kQKBytes;
             uint8_t *Vt = sm + LY::v + ls * kVBytes;
             const uint32_t qk_s = smem_u32(QK), k_s = qk_s + 8192, v_s = smem_u32(Vt);
 
+            const bool kexact = kKda && c >= 0 && kda_exact(c);
+            float Gn[8][8];   // KDA, warps 4-7: log-gates of chunk c + 1
+            if (kKda && warp >= 4 && c + 1 < nchunks) kda_load_gates(c + 1, Gn);
+            if (c >= 0) {
             // ---- P1: MMA1 of chunk c (issued while chunk c - 1 was prepared) complete
             if (!wait_pmma()) break;
-            const bool kexact = kKda && kda_exact(c);
 
             if constexpr (kKda) {
                 if (kexact) {
@@ -624,26 +657,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
             else {   // the other prep threads convert the k and v tiles to fp16 meanwhile
-                if constexpr (kKda) {
-                    if (!kexact) {
-                        // Q e^{G-m}, K e^{G-m} -> Q^ = Q e^{G}, K^ = K e^{G} (times e^{m});
-                        // K e^{m-G} -> K~ = K e^{G_C - G} (times e^{G_C - m})
-                        tile_scale_cols_f16(QK, kQKBytes, 128, S.em[gs], pt - 64, kPrepThreads - 64);
-                        tile_scale_cols_f16(KB + (c & 1) * kKBBytes, kKBBytes, 64, S.egcm[gs], pt - 64,
-                                            kPrepThreads - 64);
-                    }
-                } else {
+                if constexpr (!kKda) {   // (KDA tiles stay as built; see MMA4 / MMA6)
                     tile_bf16_to_f16(QK + 8192, 8192, pt - 64, kPrepThreads - 64);           // K, block 0
                     tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
                 }
                 tile_bf16_to_f16(Vt, kVBytes, pt - 64, kPrepThreads - 64);
             }
             named_sync(kBarPrep, kPrepThreads);
+            }   // c >= 0
             // Below-diagonal blocks, one warp per 16-column block i (warps 0..2):
             //   T_{R,i} = -T_{R,R} sum_{k=i}^{R-1} A_{R,k} T_{k,i},   R = i+1 .. 3,
             // each 16x16x16 product as two m16n8k16 fp16 warp MMAs (fp32 accumulate),
             // operands fetched with ldmatrix (row-major A blocks, transposed B blocks).
             if (warp < 3) {
+                if (c >= 0) {
                 const int i = warp, g = lane >> 2, t4 = lane & 3;
                 const int lr = lane & 15, lc = 8 * (lane >> 4);   // ldmatrix row / column of this lane
                 __half *X = X16 + 16 * 24 * warp;                  // 16x16 fp16 scratch, row stride 24
@@ -681,6 +708,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                     __syncwarp();
                 }
+                }   // c >= 0
             } else if (warp == kIssuer / 32) {
                 // look-ahead: MMA1 of chunk c + 1 into D1 (read by P4 above)
                 if constexpr (kKda) {
@@ -704,10 +732,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 }
                 if constexpr (kKda) {   // warps 4-7: KDA operands of chunk c + 1
-                    if (c + 1 < nchunks) {
-                        build_wait_tiles(c + 1);
-                        kda_build(c + 1);
-                    }
+                    if (c + 1 < nchunks) kda_build(c + 1, Gn);
                     named_sync(kBarBuildIssue, 160);
                 }
             }
@@ -715,6 +740,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!prep_vote(pt == 0 && c >= 1 ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs)
                                              : true))
                 break;
+            if (c < 0) continue;
 
             // ---- P6: stacked operands AV = [P Tu ; Tu] and AK = [-P Tw ; Tw] (fp16, K-major).
             //      Rows 64..127 straight from T; rows 0..63 from P T by fp16 warp MMAs
@@ -798,9 +824,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int k = 0; k < kC / 16; ++k)
                     umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(av_s, 128, k), mnmajor_desc(v_s, 64, k),
                               id_m128_n64_mn, k > 0);
-                for (int k = 0; k < kC / 16; ++k)
-                    umma_bf16(tbase + (s ? kColDK1 : kColDK0), kmajor_desc(ak_s, 128, k),
-                              mnmajor_desc(k_s, 128, k), id_m128_n128_mn, k > 0);
+                if constexpr (kKda) {   // [[I, -P Tw], [0, Tw]] [Q^ ; K^] = [Q~ ; W]
+                    const uint32_t akc_s = smem_u32(sm + LY::akc);
+                    for (int k = 0; k < 2 * kC / 16; ++k)
+                        umma_bf16(tbase + (s ? kColDK1 : kColDK0), kmajor_desc(akc_s, 128, k),
+                                  mnmajor_desc(qk_s, 128, k), id_m128_n128_mn, k > 0);
+                } else {
+                    for (int k = 0; k < kC / 16; ++k)
+                        umma_bf16(tbase + (s ? kColDK1 : kColDK0), kmajor_desc(ak_s, 128, k),
+                                  mnmajor_desc(k_s, 128, k), id_m128_n128_mn, k > 0);
+                }
                 umma_commit(&S.bar_ready[s]);
             }
         }
@@ -856,21 +889,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint8_t *QK = sm + LY::qk + (c % kStages) * kQKBytes;
             const uint32_t k_s = smem_u32(QK) + 8192;
 
-            // ---- S1: MMA3 / MMA4 of chunk c complete (RV[s] = [P U' ; U'], DK[s] = [-P W ; W])
+            // ---- S1: MMA3 / MMA4 of chunk c complete (RV[s] = [P U' ; U'], DK[s] = [-P W ; W],
+            //      KDA: [Q~ ; W])
             if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
             tc_fence_after();
+            // KDA: MMA3 / MMA4 have read V, Q^ and K^, and MMA6 takes K~ from the side
+            // tile: the ring stage of chunk c is free already
+            if (kKda && st == 0 && c + kStages < nchunks) issue_load(c + kStages);
             const int gs = c % 3;
             const float gC = S.gC[gs];
             const bool top = st < 64;
             const float egc = top ? 0.f : S.egc[gs][st - 64];
 
             // ---- S2: A5 = [Q~ ; -W] (row st): Q~ = Diag(e^{g}) Q - P W on the top rows
-            //      (Q read from the bf16 tile as loaded), -W on the bottom rows, packed as
+            //      (Q read from the bf16 tile as loaded; KDA: MMA4 formed Q~), -W on the
+            //      bottom rows, packed as
             //      fp16 pairs into the first 64 columns of DK[s] -- the MMA5 A operand,
             //      read from tensor memory.  Each thread rewrites only columns of its own
             //      lane that it has already read.
             {
-                const float er = kKda ? 1.f : (top ? S.eg[gs][st] : 0.f);   // KDA: Q^ holds e^{G} already
+                const float er = top ? S.eg[gs][st] : 0.f;
                 const uint32_t dk_col = tbase + lane_base + (s ? kColDK1 : kColDK0);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
@@ -881,14 +919,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tmem_ld16(dk_col + 64 * kb + cc, v);
                         tmem_ld16(dk_col + 64 * kb + cc + 16, v + 16);
                         tmem_ld_wait();
+                        if constexpr (kKda) {
+                            // KDA: the tiles hold Q e^{G-m}, K e^{G-m}, so MMA4 gave [Q~ ; W] Diag(e^{-m})
+                            const float4 *emq = reinterpret_cast<const float4 *>(&S.em[gs][64 * kb + cc]);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 e4 = emq[q];
+                                v[4 * q] *= e4.x; v[4 * q + 1] *= e4.y; v[4 * q + 2] *= e4.z; v[4 * q + 3] *= e4.w;
+                            }
+                        }
                         if (top) {
+                            if constexpr (!kKda) {   // KDA: MMA4 formed Q~ itself
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                float qv[8];
-                                if constexpr (kKda) ld_row8_f16(qblk, st, cc + j, qv);
-                                else ld_row8_bf16(qblk, st, cc + j, qv);
+                                for (int j = 0; j < 32; j += 8) {
+                                    float qv[8];
+                                    ld_row8_bf16(qblk, st, cc + j, qv);
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) v[j + i] += er * qv[i];
+                                    for (int i = 0; i < 8; ++i) v[j + i] += er * qv[i];
+                                }
                             }
                         } else {
 #pragma unroll
@@ -957,11 +1005,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 umma_commit(&S.bar_smma);
             }
             if (!wait_smma()) break;
+            if (kKda && st == 0) mbar_arrive(&S.bar_kbfree[c & 1]);
             // the tiles of chunk c are no longer read by anyone: fetch chunk c + stages into them
-            if (st == 0 && c + kStages < nchunks) issue_load(c + kStages);
+            if (!kKda && st == 0 && c + kStages < nchunks) issue_load(c + kStages);
 
             // ---- S6: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
             const float gCr = kKda ? S.egC[gs][st] : gC;   // KDA: decay of key channel st
+            // KDA: the side tile holds K e^{m-G} = K~ Diag(e^{m-G_C}) per channel, row st of D6
+            const float d6s = kKda ? S.egcm[gs][st] : 1.f;
 #pragma unroll
             for (int n = 0; n < kDVS; n += 32) {
                 float v[32];
@@ -970,7 +1021,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    Hreg[n + i] = gCr * Hreg[n + i] + v[i];
+                    Hreg[n + i] = gCr * Hreg[n + i] + d6s * v[i];
                     v[i] = Hreg[n + i];
                 }
                 st_row16(HB, st, n, v);
@@ -1013,8 +1064,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 bool chunk_tc_supported(const ChunkArgs &a)
 {
+    // KDA reads its per-channel log-gates as float4: the gate tensor must be 16-byte aligned
+    const bool kda_ok = a.mode == LDN_KDA && ((uintptr_t)a.gate & 15u) == 0;
     return a.dtype == LDN_BF16 && a.dk == kDK && a.dv % kDVS == 0 && a.chunk == kC &&
-           (a.mode == LDN_DELTANET || a.mode == LDN_GDN || a.mode == LDN_KDA);
+           (a.mode == LDN_DELTANET || a.mode == LDN_GDN || kda_ok);
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)

@@ -96,15 +96,18 @@ int ldn_chunk_fwd(const void *q, const void *k, const void *v, const float *beta
                   void *stream);
 
 /* Same as ldn_chunk_fwd with an explicit kernel family (ldn_variant).
- * LDN_VARIANT_TENSOR with dtype LDN_F32 returns LDN_ERR_UNSUPPORTED. */
+ * The tensor-core kernel takes bf16 inputs with dk = 128, dv a multiple of 64,
+ * chunk = 64, any mode; for KDA it also needs a 16-byte aligned gate tensor.
+ * LDN_VARIANT_TENSOR outside these returns LDN_ERR_UNSUPPORTED. */
 int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v, const float *beta,
                           const float *gate, const float *S0, void *out, float *S_final,
                           int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
                           int variant, void *stream);
 
-/* Which kernel family LDN_VARIANT_AUTO runs for these sizes: returns
- * LDN_VARIANT_SIMT or LDN_VARIANT_TENSOR, or -LDN_ERR_* for arguments that
- * ldn_chunk_fwd would reject.  Pure host function: touches no device. */
+/* Which kernel family LDN_VARIANT_AUTO runs for these sizes (for KDA, given a
+ * 16-byte aligned gate tensor): returns LDN_VARIANT_SIMT or LDN_VARIANT_TENSOR,
+ * or -LDN_ERR_* for arguments that ldn_chunk_fwd would reject.  Pure host
+ * function: touches no device. */
 int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype);
 
 /*
