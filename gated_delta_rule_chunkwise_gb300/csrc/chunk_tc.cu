@@ -143,6 +143,7 @@ struct Small {
     alignas(16) float em[3][kDK];
     alignas(16) float egcm[3][kDK];
     alignas(16) float egC[3][kDK];
+    float kxm[kDK];           // KDA build: log-decay prefix at row 31, handed from the rows 0-31 warps
     float stg_beta[2][kC];    // beta / log-gate of the next chunk, prefetched by cp.async
     float stg_gate[2][kC];
 };
@@ -373,15 +374,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // entry by entry instead (kflag).  The gate prefix does not need the tiles:
         // it is formed while they are still landing.  Warp 4 calls this after the
         // serial warps released gate slot cc % 3.
-        // thread = 8 key channels (ch0..ch0+7) x 8 consecutive rows (r0..r0+7); the 8
-        // row groups of a channel group are 8 consecutive lanes.  The log-gates are
-        // loaded (into G) a phase ahead of the rest, so their latency is hidden.
-        const int kt = pt - 128, kch0 = 8 * (4 * (kt >> 5) + ((lane >> 3) & 3)), krg = lane & 7;
+        // thread = 8 key channels (ch0..ch0+7) x 8 consecutive rows (r0..r0+7).  Build warp
+        // w covers channel block w & 1 and rows 32 (w >> 1) .. + 31; in a warp, lane & 7 is
+        // the channel group and lane >> 3 the row group, so the 8 lanes of each
+        // shared-memory phase touch 8 different 16-byte columns of one row (no bank
+        // conflict under the 128-byte swizzle).  The log-gates are loaded (into G) a phase
+        // ahead of the rest, so their latency is hidden.
+        const int kw = warp - 4, kch0 = 64 * (kw & 1) + 8 * (lane & 7), krh = kw >> 1, krgl = lane >> 3;
+        const int kr0 = 32 * krh + 8 * krgl;
         auto kda_load_gates = [&](int cc, float (&G)[8][8]) {
             const int tb = cc * kC, LL = min(kC, T - tb);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int r = 8 * krg + i;
+                const int r = kr0 + i;
                 float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
                 if (r < LL) {   // rows past T: zero
                     const float4 *src =
@@ -394,8 +399,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         };
         auto kda_build = [&](int cc, float (&G)[8][8]) {
-            const int ch0 = kch0, rg = krg, r0 = 8 * rg, ls = cc % kStages, gs = cc % 3;
-            // inclusive prefix over the rows: within the thread, then across the row groups
+            const int ch0 = kch0, r0 = kr0, ls = cc % kStages, gs = cc % 3;
+            // inclusive prefix over the rows: within the thread, across the 4 row groups of
+            // the warp, then (rows 32-63) plus the prefix at row 31 from the other warp
 #pragma unroll
             for (int i = 1; i < 8; ++i)
 #pragma unroll
@@ -405,15 +411,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int j = 0; j < 8; ++j) {
                 float inc = G[7][j];
 #pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, inc, o, 8);
-                    if (rg >= o) inc += y;
+                for (int o = 1; o < 4; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, inc, 8 * o);
+                    if (krgl >= o) inc += y;
                 }
                 const float excl = inc - G[7][j];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) G[i][j] += excl;
-                m[j] = __shfl_sync(0xffffffffu, G[7][j], (lane & ~7) + 3);    // row 31
-                gc[j] = __shfl_sync(0xffffffffu, G[7][j], (lane & ~7) + 7);   // row 63
+                gc[j] = __shfl_sync(0xffffffffu, inc, (lane & 7) + 24);   // this half's last row
+            }
+            if (krh == 0 && krgl == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) S.kxm[ch0 + j] = gc[j];       // prefix at row 31
+            }
+            named_sync(kBarBuild, 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (krh == 0) {
+                    m[j] = gc[j];
+                } else {
+                    m[j] = S.kxm[ch0 + j];
+                    gc[j] += m[j];   // row 63
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) G[i][j] += m[j];
+                }
             }
             bool wide = false;
 #pragma unroll
@@ -424,7 +445,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (lane == 0) S.kflag[gs][warp - 4] = any ? 1 : 0;
             named_sync(kBarBuild, 128);
             const bool exact = (S.kflag[gs][0] | S.kflag[gs][1] | S.kflag[gs][2] | S.kflag[gs][3]) != 0;
-            if (rg == 0) {   // per-channel factors the serial warps apply to MMA4 / MMA6 results
+            if (krh == 1 && krgl == 0) {   // per-channel factors the serial warps apply to MMA4 / MMA6 results
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     S.egC[gs][ch0 + j] = expf(gc[j]);
