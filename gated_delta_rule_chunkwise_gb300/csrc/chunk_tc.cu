@@ -436,11 +436,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int i = 0; i < 8; ++i) G[i][j] += m[j];
                 }
             }
+            // span check, and G <- e^{G - m} (the row-side factor; formed before the wait for
+            // the tiles so that it overlaps it; |G - m| <= kKdaMaxSpan whenever it is used)
             bool wide = false;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) wide |= !(fabsf(G[i][j] - m[j]) <= kKdaMaxSpan);   // NaN: entry-wise
+                for (int j = 0; j < 8; ++j) {
+                    const float d = G[i][j] - m[j];
+                    wide |= !(fabsf(d) <= kKdaMaxSpan);   // NaN: entry-wise
+                    G[i][j] = __expf(d);
+                }
             const bool any = __any_sync(0xffffffffu, wide);
             if (lane == 0) S.kflag[gs][warp - 4] = any ? 1 : 0;
             named_sync(kBarBuild, 128);
@@ -468,9 +474,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const int r = r0 + i;
                     float ep[8], en[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {   // |G - m| <= kKdaMaxSpan; rounded to fp16 below
-                        ep[j] = __expf(G[i][j] - m[j]);
-                        en[j] = __expf(m[j] - G[i][j]);
+                    for (int j = 0; j < 8; ++j) {   // e^{G-m} and e^{m-G}, rounded to fp16 below
+                        ep[j] = G[i][j];
+                        en[j] = __fdividef(1.f, G[i][j]);
                     }
                     uint4 *qp = reinterpret_cast<uint4 *>(qk + sw128_offset(r, col));
                     uint4 *kp = reinterpret_cast<uint4 *>(qk + sw128_offset(64 + r, col));
