@@ -5,12 +5,14 @@ kernels of lib/libldn.so.  There is no CPU fallback: if the library has not
 been built, or no GPU is present, the calls raise.
 
 Two layers:
-  * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_decode_step``,
+  * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
+    ``ldn_chunk_fwd_workspace_size``, ``ldn_decode_step``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
   * ``chunk_fwd`` and ``decode_step``: the same calls on torch CUDA tensors,
-    with shape / dtype checks and output allocation (torch is used for device
-    memory and the current stream only).
+    with shape / dtype checks and allocation of outputs and of the split
+    variant's workspace (torch is used for device memory and the current
+    stream only).
 """
 from __future__ import annotations
 
@@ -24,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libldn.so")
 LDN_DELTANET, LDN_GDN, LDN_KDA = 0, 1, 2
 LDN_F32, LDN_BF16 = 0, 1
 LDN_OK, LDN_ERR_INVALID_ARG, LDN_ERR_UNSUPPORTED, LDN_ERR_CUDA, LDN_ERR_TIMEOUT = 0, 1, 2, 3, 4
-LDN_VARIANT_AUTO, LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR = 0, 1, 2
+LDN_VARIANT_AUTO, LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR, LDN_VARIANT_SPLIT = 0, 1, 2, 3
 
 MODES = {"deltanet": LDN_DELTANET, "gdn": LDN_GDN, "kda": LDN_KDA}
 
@@ -45,6 +47,8 @@ _SIGNATURES = {
     "ldn_chunk_fwd": ([_P] * 8 + [_I] * 8 + [_P], _I),
     "ldn_chunk_fwd_variant": ([_P] * 8 + [_I] * 9 + [_P], _I),
     "ldn_chunk_fwd_select": ([_I] * 5, _I),
+    "ldn_chunk_fwd_ws": ([_P] * 8 + [_I] * 9 + [_P, ctypes.c_size_t, _P], _I),
+    "ldn_chunk_fwd_workspace_size": ([_I] * 8, ctypes.c_size_t),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
     "ldn_get_device_status": ([_P], _I),
     "ldn_status_string": ([_I], ctypes.c_char_p),
@@ -89,6 +93,16 @@ def ldn_chunk_fwd_variant(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv
 
 def ldn_chunk_fwd_select(dk, dv, chunk, mode, dtype):
     return load().ldn_chunk_fwd_select(dk, dv, chunk, mode, dtype)
+
+
+def ldn_chunk_fwd_ws(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, variant,
+                     workspace, workspace_bytes, stream):
+    return load().ldn_chunk_fwd_ws(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                                   variant, workspace, workspace_bytes, stream)
+
+
+def ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, dtype):
+    return load().ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, dtype)
 
 
 def ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream):
@@ -161,12 +175,15 @@ def _check(t, name, shape=None, dtype=None):
 
 
 def chunk_fwd(q, k, v, beta, gate=None, S0=None, *, mode, chunk=64, out=None, S_final=None,
-              want_state=True, variant=LDN_VARIANT_AUTO, stream=None):
+              want_state=True, variant=LDN_VARIANT_AUTO, workspace=None, stream=None):
     """Chunkwise forward on torch CUDA tensors (see ldn_chunk_fwd in include/ldn.h).
 
     q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16, same dtype);
     beta [B,T,H] float32; gate [B,T,H] (gdn) or [B,T,H,dk] (kda) float32;
-    S0 [B,H,dk,dv] float32 or None.  Returns (out, S_final or None)."""
+    S0 [B,H,dk,dv] float32 or None.  Returns (out, S_final or None).
+    `workspace`: a uint8 CUDA tensor for the split variant, or None; with
+    variant=LDN_VARIANT_SPLIT and no workspace one of the required size
+    (ldn_chunk_fwd_workspace_size) is allocated."""
     import torch
     mode = MODES.get(mode, mode)
     B, T, H, dk = q.shape
@@ -184,9 +201,18 @@ def chunk_fwd(q, k, v, beta, gate=None, S0=None, *, mode, chunk=64, out=None, S_
     if S_final is None and want_state:
         S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     _check(S_final, "S_final", (B, H, dk, dv), torch.float32)
-    st = ldn_chunk_fwd_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S0),
-                               _ptr(out), _ptr(S_final), B, T, H, dk, dv, chunk, mode,
-                               _dtype_code(q), variant, _stream_handle(stream))
+    if variant == LDN_VARIANT_SPLIT and workspace is None:
+        need = ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, _dtype_code(q))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace is not None:
+        _check(workspace, "workspace", dtype=torch.uint8)
+        st = ldn_chunk_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S0), _ptr(out),
+                              _ptr(S_final), B, T, H, dk, dv, chunk, mode, _dtype_code(q), variant,
+                              _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    else:
+        st = ldn_chunk_fwd_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S0),
+                                   _ptr(out), _ptr(S_final), B, T, H, dk, dv, chunk, mode,
+                                   _dtype_code(q), variant, _stream_handle(stream))
     if st != LDN_OK:
         raise LdnError(st, "ldn_chunk_fwd")
     return out, S_final

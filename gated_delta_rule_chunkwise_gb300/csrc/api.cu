@@ -50,15 +50,24 @@ static int validate_common(int mode, int dtype, int dk, int dv)
     return LDN_OK;
 }
 
-extern "C" int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v, const float *beta,
-                                     const float *gate, const float *S0, void *out, float *S_final,
-                                     int B, int T, int H, int dk, int dv, int chunk, int mode,
-                                     int dtype, int variant, void *stream)
+// Workspace bytes of the split variant (0: it does not take these sizes).
+static size_t split_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)
+{
+    if (T < 1 || B < 1 || H < 1) return 0;
+    ChunkArgs a{};
+    a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = B; a.T = T; a.H = H;
+    if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return 0;
+    return (size_t)B * H * (size_t)((T + chunk - 1) / chunk) * split_unit_bytes(dv);
+}
+
+static int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *beta, const float *gate,
+                          const float *S0, void *out, float *S_final, int B, int T, int H, int dk, int dv,
+                          int chunk, int mode, int dtype, int variant, void *ws, size_t ws_bytes, void *stream)
 {
     int st = validate_common(mode, dtype, dk, dv);
     if (st != LDN_OK) return st;
     if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
-    if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_TENSOR) return LDN_ERR_INVALID_ARG;
+    if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_SPLIT) return LDN_ERR_INVALID_ARG;
     if (chunk != 64) return LDN_ERR_UNSUPPORTED;
     // Sizes: token-head count and state element count must stay well inside int64
     // and the grid limits.
@@ -83,13 +92,45 @@ extern "C" int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v
 
     ChunkArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S0, out, S_final,
                 B, T, H, dk, dv, chunk, mode, dtype, nullptr};
+    const bool tc = dtype == LDN_BF16 && chunk_tc_supported(a);
+    const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype) : 0;
+    const bool ws_ok = ws && aligned(ws, 256) && need > 0 && ws_bytes >= need;
     if (variant == LDN_VARIANT_AUTO)
-        variant = (dtype == LDN_BF16 && chunk_tc_supported(a)) ? LDN_VARIANT_TENSOR : LDN_VARIANT_SIMT;
-    if (variant == LDN_VARIANT_TENSOR && !chunk_tc_supported(a)) return LDN_ERR_UNSUPPORTED;
+        variant = !tc ? LDN_VARIANT_SIMT : (ws_ok ? LDN_VARIANT_SPLIT : LDN_VARIANT_TENSOR);
+    if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT) && !tc) return LDN_ERR_UNSUPPORTED;
+    if (variant == LDN_VARIANT_SPLIT && !ws_ok) return LDN_ERR_INVALID_ARG;
     a.status = status_word_ptr();
     if (!a.status) return LDN_ERR_CUDA;
-    const cudaError_t err = variant == LDN_VARIANT_TENSOR ? launch_chunk_tc(a, s) : launch_chunk_simt(a, s);
+    cudaError_t err;
+    if (variant == LDN_VARIANT_SPLIT) err = launch_chunk_split(a, (uint8_t *)ws, s);
+    else if (variant == LDN_VARIANT_TENSOR) err = launch_chunk_tc(a, s);
+    else err = launch_chunk_simt(a, s);
     return err == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
+extern "C" int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v, const float *beta,
+                                     const float *gate, const float *S0, void *out, float *S_final,
+                                     int B, int T, int H, int dk, int dv, int chunk, int mode,
+                                     int dtype, int variant, void *stream)
+{
+    if (variant == LDN_VARIANT_SPLIT) return LDN_ERR_INVALID_ARG;   // needs a workspace: ldn_chunk_fwd_ws
+    return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, variant,
+                          nullptr, 0, stream);
+}
+
+extern "C" int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *beta,
+                                const float *gate, const float *S0, void *out, float *S_final,
+                                int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                                int variant, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, variant,
+                          workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)
+{
+    if (validate_common(mode, dtype, dk, dv) != LDN_OK || chunk != 64) return 0;
+    return split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype);
 }
 
 extern "C" int ldn_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,

@@ -1,0 +1,276 @@
+// State kernel of the split variant: the chunk-to-chunk recurrence, reading
+// every chunk's state-independent operands from the workspace written by the
+// preparation kernel (chunk_tc_kernel<MODE, true>).
+//
+// With H = S^T ([dk][dv]) the incoming state of a chunk, the workspace holds
+// A5 = [Q~ ; -W] (fp16, 128 x dk, swizzled K-major: the exact shared-memory
+// image of the MMA A operand), RV = [P U' ; U'] (fp16, 128 x 64 per dv slice),
+// K~ = K scaled by e^{g_C - g} (fp16, 64 x dk) and e^{g_C} per key channel, so
+// that for every chunk (chunk algebra derived from the per-token rules of the
+// linear-attention notes, Sec. 2.3-2.5):
+//   [O ; U] = RV + A5 H          (one M = 128 tcgen05.mma chain: MMA5)
+//   H      <- Diag(e^{g_C}) H + K~^T U                      (MMA6)
+// and O (rows 0..63) is the chunk's output.
+//
+// One CTA per (b, h, 64-wide slice of dv), 128 threads: thread = TMEM lane =
+// row of the fp32 state slice, held in registers.  The operands of three
+// chunks are in flight at once (1-D bulk copies into a shared-memory ring).
+// Every wait is bounded (2 s); a timeout sets LDN_ERR_TIMEOUT, in-flight work
+// is drained with bounded waits, TMEM is freed and the CTA returns.
+#include "ldn_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace ldn {
+namespace {
+using namespace sm100;
+
+constexpr int kC = 64;
+constexpr int kDK = 128;
+constexpr int kDVS = 64;
+constexpr int kThreads = 128;
+constexpr int kStages = 3;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kBar = 1;
+// stage: A5 image | RV slice | K~ | e^{g_C}
+constexpr uint32_t kOA5 = 0, kORV = 32768, kOKT = 49152, kOEG = 65536;
+constexpr uint32_t kStageTx = 65536 + 512;
+constexpr uint32_t kStageBytes = 66560;                   // 1024-aligned
+constexpr uint32_t kOffHB = kStages * kStageBytes;        // H fp16, MN-major 128 x 64
+constexpr uint32_t kOffUB = kOffHB + 16384;               // U fp16, MN-major 64 x 64
+constexpr uint32_t kOffBars = kOffUB + 8192;
+constexpr uint32_t kSmemBytes = kOffBars + 128 + 1024;
+constexpr uint32_t kColD5 = 0, kColD6 = 64, kTmemCols = 128;
+static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b)
+{
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ void st_row16(uint8_t *block, int row, int col, const float *v)
+{
+    *reinterpret_cast<uint4 *>(block + sw128_offset(row, col)) =
+        make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
+    *reinterpret_cast<uint4 *>(block + sw128_offset(row, col + 8)) =
+        make_uint4(pack_h2(v[8], v[9]), pack_h2(v[10], v[11]), pack_h2(v[12], v[13]), pack_h2(v[14], v[15]));
+}
+// 1-D bulk copy global -> shared, completing `bytes` of transactions on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat16 *__restrict__ out, float *S_final,
+                   int T, int H, int dv, int *status)
+{
+    extern __shared__ uint8_t dsmem[];
+    uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
+    uint8_t *HB = sm + kOffHB, *UB = sm + kOffUB;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBars);   // [kStages]
+    uint64_t *smma = full + kStages;
+    uint64_t *drain = smma + 1;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int fail;
+
+    const int st = threadIdx.x, warp = st >> 5;
+    const int slices = dv / kDVS;
+    const int unit = blockIdx.x / slices, sl = blockIdx.x % slices;
+    const int b = unit / H, h = unit % H, n0 = sl * kDVS;
+    const int nchunks = (T + kC - 1) / kC;
+    const size_t ub = split_unit_bytes(dv);
+    const uint8_t *base = ws + (size_t)unit * nchunks * ub;
+    const uint32_t lane_base = (32u * (uint32_t)warp) << 16;
+
+    if (st == 0) {
+        for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
+        mbar_init(smma, 1);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        fail = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_s, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_s;
+
+    int pending[kStages] = {-1, -1, -1};   // chunk last loaded into stage ls (thread 0)
+    auto issue_load = [&](int c) {
+        const int s = c % kStages;
+        uint8_t *stg = sm + s * kStageBytes;
+        const uint8_t *u = base + (size_t)c * ub;
+        pending[s] = c;
+        mbar_arrive_expect_tx(&full[s], kStageTx);
+        bulk_load(stg + kOA5, u, 32768, &full[s]);
+        bulk_load(stg + kORV, u + kSplitRvOff + (size_t)sl * 16384, 16384, &full[s]);
+        bulk_load(stg + kOKT, u + split_kt_off(dv), 16384, &full[s]);
+        bulk_load(stg + kOEG, u + split_eg_off(dv), 512, &full[s]);
+    };
+    if (st == 0)
+        for (int c = 0; c < kStages && c < nchunks; ++c) issue_load(c);
+
+    auto vote = [&](bool ok) -> bool {   // same decision in every thread
+        const bool bad = named_sync_or(kBar, kThreads, !ok || fail != 0);
+        if (bad && st == 0) fail = 1;
+        return !bad;
+    };
+    uint32_t sphase = 0;
+    auto wait_smma = [&]() -> bool {
+        const bool ok = (st == 0) ? mbar_wait(smma, sphase, kWaitNs) : true;
+        sphase ^= 1u;
+        const bool r = vote(ok);
+        tc_fence_after();
+        return r;
+    };
+    const uint32_t id_mma5 = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);   // A K-major, B MN-major
+    const uint32_t id_mma6 = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);   // both MN-major
+
+    float Hreg[kDVS];
+    {
+        const float *src = S0 ? S0 + ((size_t)unit * kDK + st) * dv + n0 : nullptr;
+#pragma unroll
+        for (int n = 0; n < kDVS; n += 4) {
+            const float4 x = src ? *reinterpret_cast<const float4 *>(src + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+            Hreg[n] = x.x; Hreg[n + 1] = x.y; Hreg[n + 2] = x.z; Hreg[n + 3] = x.w;
+        }
+#pragma unroll
+        for (int n = 0; n < kDVS; n += 16) st_row16(HB, st, n, &Hreg[n]);
+    }
+    fence_proxy_async_smem();
+    named_sync(kBar, kThreads);
+
+    const bool top = st < 64;
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages, t0 = c * kC, L = min(kC, T - t0);
+        uint8_t *stg = sm + s * kStageBytes;
+        if (!vote(st == 0 ? mbar_wait(&full[s], (c / kStages) & 1, kWaitNs) : true)) break;
+
+        // ---- MMA5: D5 = [Q~ ; -W] H
+        if (st == 0) {
+            tc_fence_after();
+            const uint32_t a5_s = smem_u32(stg + kOA5), hb_s = smem_u32(HB);
+            for (int k = 0; k < kDK / 16; ++k)
+                umma_bf16(tbase + kColD5, kmajor_desc(a5_s, 128, k), mnmajor_desc(hb_s, 128, k), id_mma5, k > 0);
+            umma_commit(smma);
+        }
+        if (!wait_smma()) break;
+
+        // ---- O = P U' + Q~ H (rows 0..63) -> out; U = U' - W H (rows 64..127) -> UB
+        {
+            const uint8_t *rv = stg + kORV;
+#pragma unroll
+            for (int n = 0; n < kDVS; n += 32) {
+                float v[32];
+                tmem_ld16(tbase + lane_base + kColD5 + n, v);
+                tmem_ld16(tbase + lane_base + kColD5 + n + 16, v + 16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(rv + sw128_offset(st, n + 8 * q));
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&w);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __half22float2(h2[i]);
+                        v[8 * q + 2 * i] += f.x;
+                        v[8 * q + 2 * i + 1] += f.y;
+                    }
+                }
+                if (top) {
+                    if (st < L) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + st) * H + h) * dv + n0 + n);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pack_bf2(v[8 * q], v[8 * q + 1]), pack_bf2(v[8 * q + 2], v[8 * q + 3]),
+                                                pack_bf2(v[8 * q + 4], v[8 * q + 5]), pack_bf2(v[8 * q + 6], v[8 * q + 7]));
+                    }
+                } else {
+                    st_row16(UB, st - 64, n, v);
+                    st_row16(UB, st - 64, n + 16, v + 16);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(kBar, kThreads);
+
+        // ---- MMA6: D6 = K~^T U
+        if (st == 0) {
+            tc_fence_after();
+            const uint32_t kt_s = smem_u32(stg + kOKT), ub_s = smem_u32(UB);
+            for (int k = 0; k < kC / 16; ++k)
+                umma_bf16(tbase + kColD6, mnmajor_desc(kt_s, 64, k), mnmajor_desc(ub_s, 64, k), id_mma6, k > 0);
+            umma_commit(smma);
+        }
+        if (!wait_smma()) break;
+
+        // ---- H <- e^{g_C} H + K~^T U (row st), fp16 copy for the next MMA5
+        {
+            const float g = reinterpret_cast<const float *>(stg + kOEG)[st];
+#pragma unroll
+            for (int n = 0; n < kDVS; n += 32) {
+                float v[32];
+                tmem_ld16(tbase + lane_base + kColD6 + n, v);
+                tmem_ld16(tbase + lane_base + kColD6 + n + 16, v + 16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    Hreg[n + i] = g * Hreg[n + i] + v[i];
+                    v[i] = Hreg[n + i];
+                }
+                st_row16(HB, st, n, v);
+                st_row16(HB, st, n + 16, v + 16);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(kBar, kThreads);
+        // every reader of stage s is done (MMA5, the RV read, MMA6, e^{g_C}): chunk c + 3 goes there
+        if (st == 0 && c + kStages < nchunks) issue_load(c + kStages);
+    }
+
+    if (fail == 0 && S_final) {
+        float *dst = S_final + ((size_t)unit * kDK + st) * dv + n0;
+#pragma unroll
+        for (int n = 0; n < kDVS; n += 4)
+            *reinterpret_cast<float4 *>(dst + n) = make_float4(Hreg[n], Hreg[n + 1], Hreg[n + 2], Hreg[n + 3]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (fail && st == 0) {
+        // drain: the MMAs issued by this thread, then the loads still in flight (bounded)
+        atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        umma_commit(drain);
+        mbar_wait(drain, 0, kWaitNs / 4);
+        for (int s = 0; s < kStages; ++s)
+            if (pending[s] >= 0) mbar_wait(&full[s], (pending[s] / kStages) & 1, kWaitNs / 4);
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDVS));
+    cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    chunk_state_kernel<<<grid, kThreads, kSmemBytes, st>>>(ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H,
+                                                           a.dv, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace ldn

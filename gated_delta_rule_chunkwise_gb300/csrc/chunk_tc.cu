@@ -77,12 +77,17 @@ constexpr float kMaxLogSpan = 60.f;                // factored decay limit (e^60
 constexpr float kKdaMaxSpan = 8.f;                 // KDA: fp16 factors e^{+-(G - m)} stay below e^8
 
 // TMEM columns (fp32, 128 lanes).
-constexpr uint32_t kColD1 = 0;      // 64   MMA1
-constexpr uint32_t kColDK1 = 64;    // 128  MMA4, stage 1; then the MMA5 A operand (fp16 pairs, 64)
-constexpr uint32_t kColDK0 = 192;   // 128  MMA4, stage 0; likewise
-constexpr uint32_t kColRV = 320;    // 2 x 64  MMA3 / MMA5 (double-buffered)
-constexpr uint32_t kColD6 = 448;    // 64   MMA6
+// Fused kernel: D1 0 (64, MMA1), DK 64 / 192 (2 x 128, MMA4 by stage; then the
+// MMA5 A operand as fp16 pairs), RV 320 (2 x 64, MMA3 / MMA5), D6 448 (64, MMA6).
+// Preparation kernel of the split variant: D1 0, DK 64 (128, one buffer), RV
+// 192 (2 x dv <= 2 x 128, MMA3 over the whole dv).
+constexpr uint32_t kColD1 = 0;
+constexpr uint32_t kColD6 = 448;
 constexpr uint32_t kTmemCols = 512;
+template <bool SPLIT>
+__device__ __forceinline__ uint32_t col_dk(int s) { return SPLIT ? 64u : (s ? 64u : 192u); }
+template <bool SPLIT>
+__device__ __forceinline__ uint32_t col_rv(int s) { return SPLIT ? 192u + 128u * s : 320u + 64u * s; }
 
 // Shared memory (bytes from a 1024-aligned base).
 constexpr uint32_t kQKBytes = 2 * 16384;      // [Q;K], 2 blocks of 128 rows x 128 B
@@ -94,19 +99,20 @@ constexpr int kMaxStages = 3;
 
 // Input tiles sit in a ring (chunk c in stage c % stages): three stages for
 // DeltaNet / Gated DeltaNet; two for KDA, whose two side tiles take the room.
-template <int MODE>
+template <int MODE, bool SPLIT = false>
 struct Layout {
     static constexpr bool kda = MODE == LDN_KDA;
     static constexpr int stages = kda ? 2 : 3;
+    static constexpr uint32_t vbytes = SPLIT ? 2 * kVBytes : kVBytes;  // V slice (split: all of dv <= 128)
     static constexpr uint32_t qk = 0;                              // stages x [Q;K]
-    static constexpr uint32_t v = qk + stages * kQKBytes;          // stages x V slice
-    static constexpr uint32_t kb = v + stages * kVBytes;           // KDA: 2 x side tile
+    static constexpr uint32_t v = qk + stages * kQKBytes;          // stages x V
+    static constexpr uint32_t kb = v + stages * vbytes;            // KDA: 2 x side tile
     static constexpr uint32_t akc = kb + (kda ? 2 * kKBBytes : 0); // KDA: [I ; 0] K-major 128 x 64 (16 KB, constant)
     static constexpr uint32_t ak = akc + (kda ? 16384 : 0);        // [-P Tw ; Tw] K-major 128 x 64 (16 KB)
     static constexpr uint32_t av = ak + 16384;                     // [P Tu ; Tu] K-major 128 x 64  (16 KB)
     static constexpr uint32_t hb = av + 16384;                     // H fp16, MN-major 128 x 64     (16 KB)
-    static constexpr uint32_t ub = hb + 16384;                     // U~ fp16, MN-major 64 x 64     (8 KB)
-    static constexpr uint32_t a16 = ub + 8192;                     // fp16 A [64][72]
+    static constexpr uint32_t ub = hb + (SPLIT ? 0 : 16384);       // U~ fp16, MN-major 64 x 64     (8 KB)
+    static constexpr uint32_t a16 = ub + (SPLIT ? 0 : 8192);       // fp16 A [64][72]
     static constexpr uint32_t p16 = a16 + 64 * kLd16 * 2;          // fp16 P [64][72]
     static constexpr uint32_t t16 = p16 + 64 * kLd16 * 2;          // fp16 T [64][72]
     static constexpr uint32_t x = t16 + 64 * kLd16 * 2;            // fp16 16x16 scratch per chain warp [3][16][24]
@@ -125,6 +131,8 @@ struct Small {
     uint64_t bar_rvfree[2];   // serial finished reading RV[s] and DK[s]
     uint64_t bar_drain[2];    // failure path: last commit of each MMA issuer
     uint64_t bar_kbfree[2];   // KDA: MMA6 of chunk c finished reading side tile c & 1
+    uint64_t bar_dkfree[2];   // split: the epilogue has read DK of chunk c (DK has one buffer)
+    uint64_t bar_stgfree[2];  // split: the workspace stores of chunk c have read their staging (AV / AK)
     uint32_t tmem_base;
     int fail;
     // Per-chunk gate data, slot = chunk % 3: written one chunk ahead by the gate
@@ -198,18 +206,21 @@ __device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int t, i
     }
 }
 
-template <int MODE>
+// SPLIT = false: the fused kernel, one CTA per (b, h, 64-wide dv slice) over the whole sequence.
+// SPLIT = true: the preparation kernel of the split variant, one CTA per (b, h, range of
+// `cpr` chunks) over the whole dv; its serial warps write the chunk operands to `ws`.
+template <int MODE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ beta,
                 const float *__restrict__ gate, const float *S0, __nv_bfloat16 *__restrict__ out,
-                float *S_final, int T, int H, int dv, int *status)
+                float *S_final, int T, int H, int dv, int *status, uint8_t *__restrict__ ws, int cpr)
 {
     extern __shared__ uint8_t dsmem[];
     // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
     // array so that every access below stays a shared-memory access.
     uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
-    using LY = Layout<MODE>;
+    using LY = Layout<MODE, SPLIT>;
     constexpr int kStages = LY::stages;
     constexpr bool kKda = MODE == LDN_KDA;
     Small &S = *reinterpret_cast<Small *>(sm + LY::small);
@@ -222,11 +233,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t *KB = sm + LY::kb;   // KDA side tiles (chunk c in KB + (c & 1) * kKBBytes)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slices = dv / kDVS;
+    const int nchunks_all = (T + kC - 1) / kC;
+    const int slices = SPLIT ? (nchunks_all + cpr - 1) / cpr : dv / kDVS;   // split: chunk ranges
     const int unit = blockIdx.x / slices;
     const int b = unit / H, h = unit % H;
-    const int n0 = (blockIdx.x % slices) * kDVS;
-    const int nchunks = (T + kC - 1) / kC;
+    const int n0 = SPLIT ? 0 : (blockIdx.x % slices) * kDVS;
+    // chunk c of this CTA is chunk cb + c of the sequence
+    const int cb = SPLIT ? (blockIdx.x % slices) * cpr : 0;
+    const int nchunks = SPLIT ? min(cpr, nchunks_all - cb) : nchunks_all;
     const uint32_t quad = (uint32_t)(warp & 3);          // TMEM lane quadrant of this warp
     const uint32_t lane_base = (32u * quad) << 16;
 
@@ -242,6 +256,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&S.bar_rvfree[1], 1);
         mbar_init(&S.bar_kbfree[0], 1);
         mbar_init(&S.bar_kbfree[1], 1);
+        mbar_init(&S.bar_dkfree[0], 1);
+        mbar_init(&S.bar_dkfree[1], 1);
+        mbar_init(&S.bar_stgfree[0], 1);
+        mbar_init(&S.bar_stgfree[1], 1);
         fence_mbar_init();
         S.fail = 0;
         tma_prefetch_desc(&tm_q);
@@ -288,7 +306,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // beta and log-gates of chunk cc into staging slot cc & 1 (gate warp; rows
         // past T read as zero), asynchronously so the loads overlap a whole chunk.
         auto prefetch_gates = [&](int cc) {
-            const int tt0 = cc * kC, LL = min(kC, T - tt0);
+            const int tt0 = (cb + cc) * kC, LL = min(kC, T - tt0);
             for (int r = lane; r < kC; r += 32) {
                 const bool ok = r < LL;
                 const size_t i = ok ? ((size_t)b * T + tt0 + r) * H + h : 0;
@@ -383,7 +401,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int kw = warp - 4, kch0 = 64 * (kw & 1) + 8 * (lane & 7), krh = kw >> 1, krgl = lane >> 3;
         const int kr0 = 32 * krh + 8 * krgl;
         auto kda_load_gates = [&](int cc, float (&G)[8][8]) {
-            const int tb = cc * kC, LL = min(kC, T - tb);
+            const int tb = (cb + cc) * kC, LL = min(kC, T - tb);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int r = kr0 + i;
@@ -549,7 +567,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int cp = c < 0 ? 0 : c;
             const int s = cp & 1, ls = cp % kStages, gs = cp % 3;
             uint8_t *QK = sm + LY::qk + ls * kQKBytes;
-            uint8_t *Vt = sm + LY::v + ls * kVBytes;
+            uint8_t *Vt = sm + LY::v + ls * LY::vbytes;
             const uint32_t qk_s = smem_u32(QK), k_s = qk_s + 8192, v_s = smem_u32(Vt);
 
             const bool kexact = kKda && c >= 0 && kda_exact(c);
@@ -564,13 +582,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // ---- P4 (KDA, decay span beyond the fp16 factors): A and P entry by entry.
                     // AV / AK, free once MMA3 / MMA4 of chunk c - 1 completed, hold the fp32
                     // per-channel log-decay prefix G [64][128] meanwhile.
-                    if (!prep_vote(pt == 0 && c >= 1 ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1,
-                                                                 kWaitNs)
-                                                     : true))
+                    if (!prep_vote(pt == 0 && c >= 1
+                                       ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs) &&
+                                             (!SPLIT || mbar_wait(&S.bar_stgfree[(c - 1) & 1], ((c - 1) >> 1) & 1,
+                                                                  kWaitNs))
+                                       : true))
                         break;
                     float *Gs = reinterpret_cast<float *>(AK);
                     if (pt < kDK) {
-                        const int tb = c * kC, LL = min(kC, T - tb);
+                        const int tb = (cb + c) * kC, LL = min(kC, T - tb);
                         const float *gp = gate + (((size_t)b * T + tb) * H + h) * kDK + pt;
                         float acc = 0.f;
                         for (int r = 0; r < kC; ++r) {
@@ -688,7 +708,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tile_bf16_to_f16(QK + 8192, 8192, pt - 64, kPrepThreads - 64);           // K, block 0
                     tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
                 }
-                tile_bf16_to_f16(Vt, kVBytes, pt - 64, kPrepThreads - 64);
+                tile_bf16_to_f16(Vt, SPLIT ? dv / kDVS * kVBytes : kVBytes, pt - 64, kPrepThreads - 64);
             }
             named_sync(kBarPrep, kPrepThreads);
             }   // c >= 0
@@ -749,8 +769,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // The serial warps have read the accumulators and gate slot of chunk
                     // c - 2 (needed before MMA3 / MMA4 of chunk c overwrite RV[s], DK[s],
                     // and before slot (c + 1) % 3 = (c - 2) % 3 is rewritten).
+                    // (Split: DK has one buffer, so its chunk c - 1 must have been read too.)
                     bool ok = true;
                     if (c >= 2 && lane == 0) ok = mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs);
+                    if (SPLIT && c >= 1 && lane == 0)
+                        ok = ok && mbar_wait(&S.bar_dkfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) {
                         if (lane == 0) S.fail = 1;
@@ -764,8 +787,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
             // MMA3 / MMA4 of chunk c - 1 have finished reading AV / AK before they are rewritten
-            if (!prep_vote(pt == 0 && c >= 1 ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs)
-                                             : true))
+            // (split: and the workspace stores of chunk c - 1, staged there, have read them)
+            if (!prep_vote(pt == 0 && c >= 1
+                               ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs) &&
+                                     (!SPLIT || mbar_wait(&S.bar_stgfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs))
+                               : true))
                 break;
             if (c < 0) continue;
 
@@ -848,17 +874,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (issuer) {
                 tc_fence_after();
                 const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(AK);
-                for (int k = 0; k < kC / 16; ++k)
-                    umma_bf16(tbase + kColRV + 64 * s, kmajor_desc(av_s, 128, k), mnmajor_desc(v_s, 64, k),
-                              id_m128_n64_mn, k > 0);
+                for (int j = 0; j < (SPLIT ? dv / kDVS : 1); ++j)   // split: all of dv, 64 columns at a time
+                    for (int k = 0; k < kC / 16; ++k)
+                        umma_bf16(tbase + col_rv<SPLIT>(s) + 64 * j, kmajor_desc(av_s, 128, k),
+                                  mnmajor_desc(v_s + j * kVBytes, 64, k), id_m128_n64_mn, k > 0);
                 if constexpr (kKda) {   // [[I, -P Tw], [0, Tw]] [Q^ ; K^] = [Q~ ; W]
                     const uint32_t akc_s = smem_u32(sm + LY::akc);
                     for (int k = 0; k < 2 * kC / 16; ++k)
-                        umma_bf16(tbase + (s ? kColDK1 : kColDK0), kmajor_desc(akc_s, 128, k),
+                        umma_bf16(tbase + col_dk<SPLIT>(s), kmajor_desc(akc_s, 128, k),
                                   mnmajor_desc(qk_s, 128, k), id_m128_n128_mn, k > 0);
                 } else {
                     for (int k = 0; k < kC / 16; ++k)
-                        umma_bf16(tbase + (s ? kColDK1 : kColDK0), kmajor_desc(ak_s, 128, k),
+                        umma_bf16(tbase + col_dk<SPLIT>(s), kmajor_desc(ak_s, 128, k),
                                   mnmajor_desc(k_s, 128, k), id_m128_n128_mn, k > 0);
                 }
                 umma_commit(&S.bar_ready[s]);
@@ -883,17 +910,169 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         auto issue_load = [&](int c) {
             const int ls = c % kStages;
             uint8_t *qk = sm + LY::qk + ls * kQKBytes;
-            uint8_t *vv = sm + LY::v + ls * kVBytes;
+            uint8_t *vv = sm + LY::v + ls * LY::vbytes;
             pending[ls] = c;
-            mbar_arrive_expect_tx(&S.bar_load[ls], 2 * 16384 + 8192);
+            mbar_arrive_expect_tx(&S.bar_load[ls], 2 * 16384 + (SPLIT ? dv / kDVS : 1) * 8192);
             for (int kb = 0; kb < 2; ++kb) {
-                tma_load_4d(qk + kb * 16384, &tm_q, &S.bar_load[ls], kb * 64, h, c * kC, b);
-                tma_load_4d(qk + kb * 16384 + 8192, &tm_k, &S.bar_load[ls], kb * 64, h, c * kC, b);
+                tma_load_4d(qk + kb * 16384, &tm_q, &S.bar_load[ls], kb * 64, h, (cb + c) * kC, b);
+                tma_load_4d(qk + kb * 16384 + 8192, &tm_k, &S.bar_load[ls], kb * 64, h, (cb + c) * kC, b);
             }
-            tma_load_4d(vv, &tm_v, &S.bar_load[ls], n0, h, c * kC, b);
+            if constexpr (SPLIT) {   // all of dv, one 64-column box each
+                for (int j = 0; j < dv / kDVS; ++j)
+                    tma_load_4d(vv + j * kVBytes, &tm_v, &S.bar_load[ls], j * kDVS, h, (cb + c) * kC, b);
+            } else {
+                tma_load_4d(vv, &tm_v, &S.bar_load[ls], n0, h, (cb + c) * kC, b);
+            }
         };
         if (st == 0)
             for (int c = 0; c < kStages && c < nchunks; ++c) issue_load(c);
+        if constexpr (SPLIT) {
+        // ---- preparation kernel: the chunk's operands of the state step go to the workspace.
+        // They are staged in shared memory that is free at this point -- K~ in the chunk's
+        // V tile, [Q~ ; -W] over the chunk's [Q ; K] tile (row by row, after K~ has read K),
+        // [P U' ; U'] in AV / AK (until P6 of a later chunk, which waits for stgfree) -- in
+        // the images the state kernel uses, and leave in three bulk copies.
+        const size_t ubytes = split_unit_bytes(dv);
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1, gs = c % 3, ls = c % kStages;
+            uint8_t *QK = sm + LY::qk + ls * kQKBytes;
+            uint8_t *Vt = sm + LY::v + ls * LY::vbytes;
+            if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
+            tc_fence_after();
+            uint8_t *u = ws + ((size_t)unit * nchunks_all + cb + c) * ubytes;
+            const bool top = st < 64;
+            // (1) DK -> [Q~ ; -W] row st in registers (packed fp16); DK is handed back at once
+            uint32_t a5w[2][2][16];
+            {
+                const float er = top ? S.eg[gs][st] : 0.f;
+                const uint32_t dk_col = tbase + lane_base + col_dk<SPLIT>(s);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    const uint8_t *qblk = QK + kb * 16384;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int cc = 32 * hf;
+                        float v[32];
+                        tmem_ld16(dk_col + 64 * kb + cc, v);
+                        tmem_ld16(dk_col + 64 * kb + cc + 16, v + 16);
+                        tmem_ld_wait();
+                        if constexpr (kKda) {   // MMA4 gave [Q~ ; W] Diag(e^{-m})
+                            const float4 *emq = reinterpret_cast<const float4 *>(&S.em[gs][64 * kb + cc]);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 e4 = emq[q];
+                                v[4 * q] *= e4.x; v[4 * q + 1] *= e4.y; v[4 * q + 2] *= e4.z; v[4 * q + 3] *= e4.w;
+                            }
+                        }
+                        if (top) {
+                            if constexpr (!kKda) {
+#pragma unroll
+                                for (int j = 0; j < 32; j += 8) {
+                                    float qv[8];
+                                    ld_row8_bf16(qblk, st, cc + j, qv);
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) v[j + i] += er * qv[i];
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = -v[i];
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) a5w[kb][hf][i] = pack_h2(v[2 * i], v[2 * i + 1]);
+                    }
+                }
+            }
+            // (2) RV -> [P U' ; U'] staged in AV / AK (one swizzled 128 x 64 block per slice)
+            {
+                const uint32_t rv_col = tbase + lane_base + col_rv<SPLIT>(s);
+                for (int n = 0; n < dv; n += 32) {
+                    float v[32];
+                    tmem_ld16(rv_col + n, v);
+                    tmem_ld16(rv_col + n + 16, v + 16);
+                    tmem_ld_wait();
+                    uint8_t *blk = AK + (n / kDVS) * 16384;   // AK, AV are adjacent
+                    st_row16(blk, st, n % kDVS, v);
+                    st_row16(blk, st, n % kDVS + 16, v + 16);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarSerial, kSerialThreads);
+            if (warp == 8) {   // (3) warp 8: send [P U' ; U'], then give AV / AK back
+                if (lane == 0) {
+                    mbar_arrive(&S.bar_dkfree[s]);   // DK has been read (one buffer)
+                    bulk_store(u + kSplitRvOff, AK, (uint32_t)(dv / kDVS) * 16384);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                __syncwarp();
+                // the staging overwrote the constant zero blocks of AV / AK: restore them
+                for (int e = lane; e < 6 * 16 * 2 * 2; e += 32) {
+                    const int blkid = e / 64, rem = e % 64;
+                    const int R = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
+                    const int i = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
+                    const int rr = 16 * R + (rem >> 2), cc = 16 * i + 8 * ((rem >> 1) & 1);
+                    *reinterpret_cast<uint4 *>(((rem & 1) ? AK : AV) + sw128_offset(rr, cc)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.bar_stgfree[s]);
+            }
+            // (4) K~ = K e^{g_C - g} -> V tile, 2 blocks of 64 rows (thread: row st & 63, half st >> 6)
+            {
+                const int r = st & 63, kb = st >> 6;
+#pragma unroll
+                for (int c8 = 0; c8 < 64; c8 += 8) {
+                    const uint8_t *src = kKda ? KB + (c & 1) * kKBBytes + kb * 8192 + sw128_offset(r, c8)
+                                              : QK + kb * 16384 + sw128_offset(64 + r, c8);
+                    uint4 w = *reinterpret_cast<const uint4 *>(src);
+                    uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&x[i]));
+                        const int ch = 64 * kb + c8 + 2 * i;
+                        const float f0 = kKda ? S.egcm[gs][ch] : S.egc[gs][r];
+                        const float f1 = kKda ? S.egcm[gs][ch + 1] : S.egc[gs][r];
+                        x[i] = pack_h2(f.x * f0, f.y * f1);
+                    }
+                    *reinterpret_cast<uint4 *>(Vt + kb * 8192 + sw128_offset(r, c8)) = make_uint4(x[0], x[1], x[2], x[3]);
+                }
+                // e^{g_C} per key channel, straight to the workspace
+                if (st >= 64) {
+                    float *eg = reinterpret_cast<float *>(u + split_eg_off(dv));
+                    const int ch = 2 * (st - 64);
+                    *reinterpret_cast<float2 *>(eg + ch) = make_float2(kKda ? S.egC[gs][ch] : S.gC[gs],
+                                                                       kKda ? S.egC[gs][ch + 1] : S.gC[gs]);
+                }
+            }
+            named_sync(kBarSerial, kSerialThreads);   // K rows read: [Q~ ; -W] may replace them
+            // (5) [Q~ ; -W] row st over row st of the [Q ; K] tile (same swizzled geometry)
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4 *>(QK + kb * 16384 + sw128_offset(st, 32 * hf + 8 * q)) =
+                            make_uint4(a5w[kb][hf][4 * q], a5w[kb][hf][4 * q + 1], a5w[kb][hf][4 * q + 2],
+                                       a5w[kb][hf][4 * q + 3]);
+            fence_proxy_async_smem();
+            named_sync(kBarSerial, kSerialThreads);
+            if (st == 0) {
+                bulk_store(u, QK, 32768);
+                bulk_store(u + split_kt_off(dv), Vt, 16384);
+                bulk_commit();
+                bulk_wait_read_all();   // the tile stage may be reloaded from here on
+                // RV of chunk c and gate slot c % 3 are read (RV has two buffers)
+                mbar_arrive(&S.bar_rvfree[s]);
+                if (kKda) mbar_arrive(&S.bar_kbfree[c & 1]);
+                if (c + kStages < nchunks) issue_load(c + kStages);
+            }
+        }
+        if (st == 0) bulk_wait_all();   // the workspace is complete before the CTA leaves
+        } else {
         const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);   // MMA5
         const uint32_t id_m128_n64_amn = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);  // MMA6
 
@@ -912,7 +1091,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         named_sync(kBarSerial, kSerialThreads);
 
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1, t0 = c * kC, L = min(kC, T - t0);
+            const int s = c & 1, t0 = (cb + c) * kC, L = min(kC, T - t0);
             const uint8_t *QK = sm + LY::qk + (c % kStages) * kQKBytes;
             const uint32_t k_s = smem_u32(QK) + 8192;
 
@@ -936,7 +1115,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             //      lane that it has already read.
             {
                 const float er = top ? S.eg[gs][st] : 0.f;
-                const uint32_t dk_col = tbase + lane_base + (s ? kColDK1 : kColDK0);
+                const uint32_t dk_col = tbase + lane_base + col_dk<SPLIT>(s);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     const uint8_t *qblk = QK + kb * 16384;   // Q rows 0..63 of this column block
@@ -983,9 +1162,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // ---- S3: MMA5: RV[s] += [Q~ ; -W] H0  -> O (rows 0..63), U (rows 64..127)
             if (st == 0) {
                 tc_fence_after();
-                const uint32_t a5_t = tbase + (s ? kColDK1 : kColDK0), hb_s = smem_u32(HB);
+                const uint32_t a5_t = tbase + col_dk<SPLIT>(s), hb_s = smem_u32(HB);
                 for (int k = 0; k < kDK / 16; ++k)
-                    umma_ts(tbase + kColRV + 64 * s, a5_t + 8 * k, mnmajor_desc(hb_s, 128, k), id_m128_n64_mn, 1);
+                    umma_ts(tbase + col_rv<SPLIT>(s), a5_t + 8 * k, mnmajor_desc(hb_s, 128, k), id_m128_n64_mn, 1);
                 umma_commit(&S.bar_smma);
             }
             if (!wait_smma()) break;
@@ -996,8 +1175,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int n = 0; n < kDVS; n += 32) {
                     float v[32];
-                    tmem_ld16(tbase + lane_base + kColRV + 64 * s + n, v);
-                    tmem_ld16(tbase + lane_base + kColRV + 64 * s + n + 16, v + 16);
+                    tmem_ld16(tbase + lane_base + col_rv<SPLIT>(s) + n, v);
+                    tmem_ld16(tbase + lane_base + col_rv<SPLIT>(s) + n + 16, v + 16);
                     tmem_ld_wait();
                     if (top) {
                         if (r < L) {
@@ -1065,6 +1244,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int n = 0; n < kDVS; n += 4)
                 *reinterpret_cast<float4 *>(dst + n) = make_float4(Hreg[n], Hreg[n + 1], Hreg[n + 2], Hreg[n + 3]);
         }
+        }   // !SPLIT
     }
 
     tc_fence_before();
@@ -1097,27 +1277,57 @@ bool chunk_tc_supported(const ChunkArgs &a)
            (a.mode == LDN_DELTANET || a.mode == LDN_GDN || kda_ok);
 }
 
-cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
+namespace {
+int sm_count()
+{
+    static int sms[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms[dev] = 0;
+    return sms[dev];
+}
+
+template <bool SPLIT>
+cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 {
     CUtensorMap tq, tk, tv;
     if (!make_tmap_bf16_4d(&tq, a.q, kDK, a.H, a.T, a.B, 64, kC) ||
         !make_tmap_bf16_4d(&tk, a.k, kDK, a.H, a.T, a.B, 64, kC) ||
         !make_tmap_bf16_4d(&tv, a.v, a.dv, a.H, a.T, a.B, 64, kC))
         return cudaErrorInvalidValue;
-    const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDVS));
+    int cpr = 0;
+    long long grid = (long long)a.B * a.H * (a.dv / kDVS);
+    if (SPLIT) {
+        // chunk ranges per sequence so that the CTAs fill the SMs once (one CTA per SM)
+        const int nchunks = (a.T + kC - 1) / kC;
+        const long long heads = (long long)a.B * a.H;
+        const int sms = sm_count();
+        int nranges = (int)max(1LL, min((long long)nchunks, sms > 0 ? sms / heads : 1LL));
+        cpr = (nchunks + nranges - 1) / nranges;
+        nranges = (nchunks + cpr - 1) / cpr;
+        grid = heads * nranges;
+    }
     auto go = [&](auto kern, uint32_t smem) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out, a.S_final,
-                                           a.T, a.H, a.dv, a.status);
-        return cudaSuccess;
+        kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
+                                                     a.S_final, a.T, a.H, a.dv, a.status, ws, cpr);
+        return cudaGetLastError();
     };
-    cudaError_t e;
-    if (a.mode == LDN_GDN) e = go(chunk_tc_kernel<LDN_GDN>, Layout<LDN_GDN>::bytes);
-    else if (a.mode == LDN_KDA) e = go(chunk_tc_kernel<LDN_KDA>, Layout<LDN_KDA>::bytes);
-    else e = go(chunk_tc_kernel<LDN_DELTANET>, Layout<LDN_DELTANET>::bytes);
+    if (a.mode == LDN_GDN) return go(chunk_tc_kernel<LDN_GDN, SPLIT>, Layout<LDN_GDN, SPLIT>::bytes);
+    if (a.mode == LDN_KDA) return go(chunk_tc_kernel<LDN_KDA, SPLIT>, Layout<LDN_KDA, SPLIT>::bytes);
+    return go(chunk_tc_kernel<LDN_DELTANET, SPLIT>, Layout<LDN_DELTANET, SPLIT>::bytes);
+}
+}  // namespace
+
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) { return launch_tc<false>(a, nullptr, st); }
+
+cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
+{
+    cudaError_t e = launch_tc<true>(a, ws, st);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_chunk_state(a, ws, st);
 }
 
 }  // namespace ldn

@@ -31,11 +31,22 @@ struct DecodeArgs {
     int *status;
 };
 
+// Split variant: workspace bytes per (b, h, chunk) -- [Q~ ; -W] (32 KiB), [P U' ; U']
+// per 64-column slice of dv (16 KiB each), K~ (16 KiB), e^{g_C} per key channel
+// (512 B); layout described in include/ldn.h.
+__host__ __device__ constexpr size_t split_unit_bytes(int dv) { return 32768 + (size_t)(dv / 64) * 16384 + 16384 + 512; }
+constexpr size_t kSplitRvOff = 32768;
+__host__ __device__ constexpr size_t split_kt_off(int dv) { return 32768 + (size_t)(dv / 64) * 16384; }
+__host__ __device__ constexpr size_t split_eg_off(int dv) { return split_kt_off(dv) + 16384; }
+
 // Launchers: return cudaSuccess or the launch error.  Arguments are validated
 // by the caller (api.cu).
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs &a);
+// Split variant: preparation kernel (chunk_tc.cu) then state kernel (chunk_state.cu).
+cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
+cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 int *status_word_ptr();   // address of the device status word on the current device
 cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cudaStream_t stream);

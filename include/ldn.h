@@ -19,10 +19,12 @@
  * Conventions shared by every entry point
  *   - Pointers q, k, v, beta, gate, S0, S, out, S_final are DEVICE pointers to
  *     contiguous, row-major arrays.  Alignment: ldn_chunk_fwd needs q, k, v,
- *     out, S0 and S_final 16-byte aligned; ldn_decode_step needs S 16-byte
+ *     out, S0 and S_final 16-byte aligned (and the workspace of ldn_chunk_fwd_ws
+ *     256-byte aligned); ldn_decode_step needs S 16-byte
  *     aligned and q, k, v, out aligned to their element size; beta and gate
- *     are 4-byte aligned everywhere.  The caller owns every buffer; the
- *     library allocates no device memory per call.
+ *     are 4-byte aligned everywhere.  The caller owns every buffer (and the
+ *     workspace of the split variant); the library allocates no device memory
+ *     per call.
  *   - Gates are natural-log decays: alpha_t = exp(gate), a_t = exp(gate[c]).
  *     A positive log-gate is accepted (it is not clamped); beta is not clamped.
  *   - q is not scaled and q, k are not normalised by the library (scale = 1).
@@ -40,11 +42,13 @@
 #ifndef LDN_H
 #define LDN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-#define LDN_VERSION 1
+#define LDN_VERSION 2
 
 typedef enum { LDN_DELTANET = 0, LDN_GDN = 1, LDN_KDA = 2 } ldn_mode;
 
@@ -63,7 +67,8 @@ typedef enum {
 typedef enum {
     LDN_VARIANT_AUTO = 0,   /* bf16 -> tensor-core kernel, fp32 -> fp32 SIMT kernel */
     LDN_VARIANT_SIMT = 1,   /* fp32 CUDA-core kernel, either dtype                 */
-    LDN_VARIANT_TENSOR = 2  /* tcgen05 / TMEM kernel, bf16 only                     */
+    LDN_VARIANT_TENSOR = 2, /* tcgen05 / TMEM kernel, bf16 only                     */
+    LDN_VARIANT_SPLIT = 3   /* tcgen05, two kernels through a workspace (see below) */
 } ldn_variant;
 
 /*
@@ -109,6 +114,40 @@ int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v, const flo
  * or -LDN_ERR_* for arguments that ldn_chunk_fwd would reject.  Pure host
  * function: touches no device. */
 int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype);
+
+/*
+ * The split variant runs the chunkwise forward as two kernels: the first forms,
+ * for every chunk in parallel, everything that does not depend on the state
+ * (the UT/WY transform and the intra-chunk products) and writes it to a
+ * device workspace; the second runs the chunk-to-chunk state recurrence from
+ * it.  It takes the same inputs as the tensor-core variant and returns the
+ * same results (equal up to floating-point rounding to the fused kernel).
+ *
+ * Workspace contents, per (b, h, chunk), in this order (all 16-byte aligned):
+ *   [Q~ ; -W] fp16, 128 x dk in the swizzled K-major layout of the state
+ *   step's MMA operand (32 KiB); [P U' ; U'] fp16 per 64-column slice of dv
+ *   (16 KiB each); K~ = K Diag-scaled by e^{g_C - g} fp16 (16 KiB); e^{g_C}
+ *   per key channel fp32 (512 B).
+ *
+ * ldn_chunk_fwd_workspace_size: bytes of workspace the split variant needs for
+ * these sizes, or 0 when it does not take them.  Pure host function.
+ */
+size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype);
+
+/*
+ * ldn_chunk_fwd_ws -- ldn_chunk_fwd with an explicit kernel family and a
+ * caller-owned device workspace (256-byte aligned, at least
+ * ldn_chunk_fwd_workspace_size bytes; its contents on entry do not matter and
+ * on return are unspecified).  LDN_VARIANT_SPLIT without a large enough
+ * workspace returns LDN_ERR_INVALID_ARG; LDN_VARIANT_AUTO takes the split
+ * variant when it supports the call and the workspace suffices, and otherwise
+ * behaves as ldn_chunk_fwd_variant(..., LDN_VARIANT_AUTO, ...).  Calls on
+ * different streams need different workspaces.
+ */
+int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *beta,
+                     const float *gate, const float *S0, void *out, float *S_final,
+                     int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                     int variant, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * ldn_decode_step -- one recurrent step for every (b, h), state updated in place.

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert ldn.ldn_version() == 1
+    assert ldn.ldn_version() == 2
     for st in range(5):
         assert isinstance(ldn.ldn_status_string(st), str) and ldn.ldn_status_string(st)
     assert "unknown" in ldn.ldn_status_string(99)
@@ -122,3 +122,26 @@ def test_select_reports_kernel_family(lib):
     assert ldn.ldn_chunk_fwd_select(96, 128, 64, 1, ldn.LDN_BF16) == -ldn.LDN_ERR_UNSUPPORTED
     assert ldn.ldn_chunk_fwd_select(128, 128, 32, 1, ldn.LDN_BF16) == -ldn.LDN_ERR_UNSUPPORTED
     assert ldn.ldn_chunk_fwd_select(128, 128, 64, 5, ldn.LDN_BF16) == -ldn.LDN_ERR_INVALID_ARG
+
+
+def test_split_workspace_size_is_per_chunk_operands(lib):
+    """[Q~;-W] 32 KiB + [P U';U'] 16 KiB per 64-column slice + K~ 16 KiB + e^{g_C} 512 B
+    per (b, h, chunk); 0 where the split variant does not apply."""
+    per = lambda dv: 32768 + (dv // 64) * 16384 + 16384 + 512
+    assert ldn.ldn_chunk_fwd_workspace_size(4, 2048, 16, 128, 128, 64, 1, 1) == 4 * 16 * 32 * per(128)
+    assert ldn.ldn_chunk_fwd_workspace_size(1, 65, 3, 128, 64, 64, 2, 1) == 3 * 2 * per(64)
+    assert ldn.ldn_chunk_fwd_workspace_size(1, 64, 1, 128, 128, 64, 0, 0) == 0   # fp32: no tensor path
+    assert ldn.ldn_chunk_fwd_workspace_size(1, 64, 1, 64, 128, 64, 1, 1) == 0    # dk = 64
+    assert ldn.ldn_chunk_fwd_workspace_size(1, 0, 1, 128, 128, 64, 1, 1) == 0    # empty sequence
+    assert ldn.ldn_chunk_fwd_workspace_size(1, 64, 1, 128, 128, 32, 1, 1) == 0   # chunk != 64
+
+
+def test_split_without_workspace_is_rejected(lib):
+    """The split variant needs a workspace: without one (or with too small a one) the
+    call is rejected before anything is enqueued."""
+    fake = 1 << 20   # never dereferenced: the checks come first
+    args = [fake] * 5 + [0, fake, 0, 1, 64, 1, 128, 128, 64, 1, 1]
+    assert ldn.ldn_chunk_fwd_variant(*args, ldn.LDN_VARIANT_SPLIT, 0) == ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_chunk_fwd_ws(*args, ldn.LDN_VARIANT_SPLIT, 0, 0, 0) == ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_chunk_fwd_ws(*args, ldn.LDN_VARIANT_SPLIT, 1 << 20, 16, 0) == ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_chunk_fwd_ws(*args, ldn.LDN_VARIANT_SPLIT, (1 << 20) + 8, 1 << 30, 0) == ldn.LDN_ERR_INVALID_ARG

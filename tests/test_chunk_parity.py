@@ -170,11 +170,41 @@ def test_kda_all_chunks_entrywise():
     check(w, ldn.LDN_VARIANT_TENSOR)
 
 
+# ---- split variant: parallel chunk preparation into a workspace, then the state chain ----
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("B,T,H,dv,s0", [(2, 200, 3, 128, True), (1, 64, 2, 64, False), (1, 1, 1, 128, True),
+                                         (1, 700, 1, 128, True), (2, 333, 2, 64, True)])
+def test_split_variant_parity(mode, B, T, H, dv, s0):
+    w = wl.make_chunk(BASE[mode], B=B, T=T, H=H, dk=128, dv=dv, mode=mode, dtype="bf16", s0=s0)
+    check(w, ldn.LDN_VARIANT_SPLIT)
+
+
+def test_split_variant_kda_strong_gates():
+    """Entry-wise chunks (spans beyond the fp16 factors) through the split variant."""
+    w = wl.make_chunk(BASE[2], B=1, T=320, H=2, s0=True)
+    g = w.gate.copy()
+    g[:, 64:192, :, 5] = -1.2
+    g[:, 256:300, 1, 100] = -0.9
+    w.gate = g.astype(np.float32)
+    check(w, ldn.LDN_VARIANT_SPLIT)
+
+
+def test_split_equals_fused_up_to_rounding():
+    """Same inputs through both tensor-core variants: same result up to rounding."""
+    w = wl.make_chunk(BASE[1], B=2, T=500, H=4, s0=True)
+    o1, s1 = run_gpu(w, ldn.LDN_VARIANT_TENSOR)
+    o2, s2 = run_gpu(w, ldn.LDN_VARIANT_SPLIT)
+    # Both outputs are bf16-rounded independently, so they may differ by one bf16 ulp
+    # (up to 2^-7 of the value) on top of the difference of the unrounded values.
+    ulp_excess = np.maximum(np.abs(o2 - o1) - 2.0 ** -7 * np.abs(o1), 0.0).max() / np.sqrt(np.mean(o1 ** 2))
+    assert ulp_excess < 1e-2 and rel_err(s2, s1) < 1e-2
+
+
 # ---- full-size workloads in the benchmark's launch configuration, sampled ----
-def _sampled(name, picks, **over):
+def _sampled(name, picks, variant=ldn.LDN_VARIANT_AUTO, **over):
     import torch
     w = wl.make_chunk(name, **over)
-    o, s = run_gpu(w)
+    o, s = run_gpu(w, variant)
     for b, h in picks:
         sub = wl.Workload(name=w.name, mode=w.mode, dtype=w.dtype, B=1, T=w.T, H=1, dk=w.dk, dv=w.dv,
                           q=w.q[b:b + 1, :, h:h + 1], k=w.k[b:b + 1, :, h:h + 1], v=w.v[b:b + 1, :, h:h + 1],
@@ -198,3 +228,10 @@ def test_full_kda_bf16_b8_t4096_sampled():
 
 def test_full_gdn_long_t65536_sampled():
     _sampled("gdn_bf16_long_b1_t65536_h16_d128", [(0, 5)])
+
+
+@pytest.mark.parametrize("name,picks", [("gdn_bf16_b4_t2048_h16_d128", [(0, 0), (3, 15)]),
+                                        ("kda_bf16_b8_t4096_h16_d128", [(7, 12)]),
+                                        ("gdn_bf16_long_b1_t65536_h16_d128", [(0, 5)])])
+def test_full_workloads_split_variant_sampled(name, picks):
+    _sampled(name, picks, ldn.LDN_VARIANT_SPLIT)
