@@ -284,12 +284,17 @@ def run_ours(args):
     S_final = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
     P = lambda x: 0 if x is None else x.data_ptr()
     args_ptrs = (P(t["q"]), P(t["k"]), P(t["v"]), P(t["beta"]), P(t["gate"]), P(t["S0"]), P(out), P(S_final))
+    # workspace of the split variant (allocated by torch; the library allocates nothing)
+    ws_bytes = ldn.ldn_chunk_fwd_workspace_size(w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, dtype_code)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    chosen = args.variant if args.variant != ldn.LDN_VARIANT_AUTO else \
+        ldn.ldn_chunk_fwd_select_ws(w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, dtype_code, ws_bytes)
 
     def step():
-        st = ldn.ldn_chunk_fwd_variant(*args_ptrs, w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, dtype_code,
-                                       args.variant, sh)
+        st = ldn.ldn_chunk_fwd_ws(*args_ptrs, w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, dtype_code,
+                                  args.variant, ws.data_ptr(), ws_bytes, sh)
         if st != ldn.LDN_OK:
-            raise ldn.LdnError(st, "ldn_chunk_fwd")
+            raise ldn.LdnError(st, "ldn_chunk_fwd_ws")
 
     for _ in range(max(3, args.warmup)):
         flush_l2()
@@ -309,7 +314,7 @@ def run_ours(args):
     barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    launches = args.steps
+    launches = args.steps * (2 if chosen == ldn.LDN_VARIANT_SPLIT else 1)
     if ldn.device_status() != ldn.LDN_OK:
         raise RuntimeError("device status not ok after the timed region")
     per = [e0.elapsed_time(e1) for e0, e1 in evs]
@@ -319,10 +324,8 @@ def run_ours(args):
     nbytes = chunk_bytes(w.B, w.T, w.H, w.dk, w.dv, el, w.mode, False, True)
     flops = chunk_flops(w.B, w.T, w.H, w.dk, w.dv)
     achieved_gbs = nbytes / (ms / 1e3) / 1e9
-    from_variant = "tcgen05" if (args.variant == ldn.LDN_VARIANT_TENSOR or
-                                 (args.variant == ldn.LDN_VARIANT_AUTO and w.dtype == "bf16" and
-                                  _tc_enabled(ldn))) else "simt"
-    src = ["chunk_tc.cu"] if from_variant == "tcgen05" else ["chunk_simt.cu"]
+    from_variant = {ldn.LDN_VARIANT_TENSOR: "tcgen05", ldn.LDN_VARIANT_SPLIT: "split"}.get(chosen, "simt")
+    src = {"tcgen05": ["chunk_tc.cu"], "split": ["chunk_tc.cu", "chunk_state.cu"]}.get(from_variant, ["chunk_simt.cu"])
     kernel_key = f"chunk_{from_variant}:{args.workload}"
     src_hash = kernel_source_hash(src)
     traffic = recorded_traffic(kernel_key, src_hash)
@@ -361,7 +364,7 @@ def run_ours(args):
             e2e_step()
             e1.record(stream)
         barrier()
-        launches += args.steps
+        launches += args.steps * (2 if chosen == ldn.LDN_VARIANT_SPLIT else 1)
         ems = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in ee))
         e2e = {"value": world * tokens / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems}
@@ -380,10 +383,15 @@ def run_ours(args):
             optr = (P(ot["q"]), P(ot["k"]), P(ot["v"]), P(ot["beta"]), P(ot["gate"]), P(ot["S0"]), P(oout), P(osf))
             odt = ldn.LDN_BF16 if ow.dtype == "bf16" else ldn.LDN_F32
 
+            ows_bytes = ldn.ldn_chunk_fwd_workspace_size(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt)
+            ows = torch.empty(max(ows_bytes, 256), dtype=torch.uint8, device="cuda")
+            ochosen = ldn.ldn_chunk_fwd_select_ws(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt, ows_bytes)
+
             def ostep():
-                st_ = ldn.ldn_chunk_fwd(*optr, ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt, sh)
+                st_ = ldn.ldn_chunk_fwd_ws(*optr, ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt,
+                                           ldn.LDN_VARIANT_AUTO, ows.data_ptr(), ows_bytes, sh)
                 if st_ != ldn.LDN_OK:
-                    raise ldn.LdnError(st_, "ldn_chunk_fwd")
+                    raise ldn.LdnError(st_, "ldn_chunk_fwd_ws")
 
             ostep()
             oev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
@@ -393,14 +401,14 @@ def run_ours(args):
                 ostep()
                 e1.record(stream)
             barrier()
-            launches += 4
+            launches += 4 * (2 if ochosen == ldn.LDN_VARIANT_SPLIT else 1)
             oms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in oev))
             ob = chunk_bytes(ow.B, ow.T, ow.H, ow.dk, ow.dv, oel, ow.mode, ow.S0 is not None, True)
-            kern = "tcgen05" if ldn.ldn_chunk_fwd_select(ow.dk, ow.dv, 64, ow.mode, odt) == ldn.LDN_VARIANT_TENSOR else "simt"
+            kern = {ldn.LDN_VARIANT_TENSOR: "tcgen05", ldn.LDN_VARIANT_SPLIT: "split"}.get(ochosen, "simt")
             others[name] = {"tokens_per_s": world * ow.B * ow.T / (oms / 1e3), "ms_per_launch": oms,
                             "kernel": f"chunk_{kern}", "algorithmic_bytes": ob,
                             "hbm_frac": ob / (oms / 1e3) / 1e9 / hbm_peak}
-            del ot, oout, osf
+            del ot, oout, osf, ows
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("other workloads: device status not ok")
 
@@ -478,11 +486,6 @@ def run_ours(args):
     return 0
 
 
-def _tc_enabled(ldn):
-    """Whether the library's automatic choice for bf16 GDN is the tensor-core kernel."""
-    return ldn.ldn_chunk_fwd_select(128, 128, 64, ldn.LDN_GDN, ldn.LDN_BF16) == ldn.LDN_VARIANT_TENSOR
-
-
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,7 +493,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 SIMT fp32, 2 tcgen05")
+    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 SIMT fp32, 2 tcgen05 fused, 3 split")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

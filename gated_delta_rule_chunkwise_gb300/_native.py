@@ -49,6 +49,7 @@ _SIGNATURES = {
     "ldn_chunk_fwd_select": ([_I] * 5, _I),
     "ldn_chunk_fwd_ws": ([_P] * 8 + [_I] * 9 + [_P, ctypes.c_size_t, _P], _I),
     "ldn_chunk_fwd_workspace_size": ([_I] * 8, ctypes.c_size_t),
+    "ldn_chunk_fwd_select_ws": ([_I] * 8 + [ctypes.c_size_t], _I),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
     "ldn_get_device_status": ([_P], _I),
     "ldn_status_string": ([_I], ctypes.c_char_p),
@@ -103,6 +104,10 @@ def ldn_chunk_fwd_ws(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chu
 
 def ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, dtype):
     return load().ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, dtype)
+
+
+def ldn_chunk_fwd_select_ws(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes):
+    return load().ldn_chunk_fwd_select_ws(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes)
 
 
 def ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream):

@@ -96,7 +96,8 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype) : 0;
     const bool ws_ok = ws && aligned(ws, 256) && need > 0 && ws_bytes >= need;
     if (variant == LDN_VARIANT_AUTO)
-        variant = !tc ? LDN_VARIANT_SIMT : (ws_ok ? LDN_VARIANT_SPLIT : LDN_VARIANT_TENSOR);
+        variant = !tc ? LDN_VARIANT_SIMT
+                      : (ws_ok && chunk_split_preferred(a) ? LDN_VARIANT_SPLIT : LDN_VARIANT_TENSOR);
     if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT) && !tc) return LDN_ERR_UNSUPPORTED;
     if (variant == LDN_VARIANT_SPLIT && !ws_ok) return LDN_ERR_INVALID_ARG;
     a.status = status_word_ptr();
@@ -125,6 +126,21 @@ extern "C" int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, con
 {
     return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, variant,
                           workspace, workspace_bytes, stream);
+}
+
+extern "C" int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                                       size_t workspace_bytes)
+{
+    const int st = validate_common(mode, dtype, dk, dv);
+    if (st != LDN_OK) return -st;
+    if (chunk != 64) return -LDN_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || T < 0) return -LDN_ERR_INVALID_ARG;
+    ChunkArgs a{};
+    a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = B; a.T = T; a.H = H;
+    if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return LDN_VARIANT_SIMT;
+    const size_t need = split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype);
+    return (need > 0 && workspace_bytes >= need && chunk_split_preferred(a)) ? LDN_VARIANT_SPLIT
+                                                                             : LDN_VARIANT_TENSOR;
 }
 
 extern "C" size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)

@@ -54,6 +54,8 @@
 // Every mbarrier wait is bounded in time (2 s); a timeout sets LDN_ERR_TIMEOUT
 // in the status word, both roles abandon their loops, in-flight copies and
 // MMAs are drained with bounded waits, TMEM is freed and the CTA returns.
+#include <algorithm>
+
 #include "ldn_internal.cuh"
 #include "sm100_ptx.cuh"
 #include "tma_host.cuh"
@@ -1322,6 +1324,29 @@ cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 }  // namespace
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) { return launch_tc<false>(a, nullptr, st); }
+
+// Which tensor-core variant is expected to be faster: a cost model in waves of
+// CTAs (one CTA per SM) x chunks per CTA x measured time per chunk on GB300 --
+// fused 4.4 us (GDN / DeltaNet) or 7.9 us (KDA); split preparation 5.0 / 10.9 us
+// and state step 2.0 us.  The fused kernel wins when its CTAs fill the SMs
+// once; the split variant when they do not (few sequences) or need several
+// waves (its preparation and state steps are cheaper than a fused chunk step).
+bool chunk_split_preferred(const ChunkArgs &a)
+{
+    const int sms = sm_count();
+    if (sms <= 0) return false;
+    const bool kda = a.mode == LDN_KDA;
+    const double t_fused = kda ? 7.9 : 4.4, t_prep = kda ? 10.9 : 5.0, t_state = 2.0;
+    const long long heads = (long long)a.B * a.H, nchunks = (a.T + kC - 1) / kC;
+    const long long slices = heads * (a.dv / kDVS);
+    const long long waves_f = (slices + sms - 1) / sms;
+    const long long nranges = std::max(1LL, std::min(nchunks, sms / heads));
+    const long long cpr = (nchunks + nranges - 1) / nranges;
+    const long long waves_p = (heads * ((nchunks + cpr - 1) / cpr) + sms - 1) / sms;
+    const double fused = (double)waves_f * nchunks * t_fused;
+    const double split = (double)waves_p * cpr * t_prep + (double)waves_f * nchunks * t_state;
+    return split < fused;
+}
 
 cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 {

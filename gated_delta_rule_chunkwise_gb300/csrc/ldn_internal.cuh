@@ -47,6 +47,7 @@ bool chunk_tc_supported(const ChunkArgs &a);
 // Split variant: preparation kernel (chunk_tc.cu) then state kernel (chunk_state.cu).
 cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
 cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream_t stream);
+bool chunk_split_preferred(const ChunkArgs &a);   // expected faster than the fused kernel
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 int *status_word_ptr();   // address of the device status word on the current device
 cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cudaStream_t stream);

@@ -140,14 +140,24 @@ size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chu
  * ldn_chunk_fwd_workspace_size bytes; its contents on entry do not matter and
  * on return are unspecified).  LDN_VARIANT_SPLIT without a large enough
  * workspace returns LDN_ERR_INVALID_ARG; LDN_VARIANT_AUTO takes the split
- * variant when it supports the call and the workspace suffices, and otherwise
- * behaves as ldn_chunk_fwd_variant(..., LDN_VARIANT_AUTO, ...).  Calls on
- * different streams need different workspaces.
+ * variant when it supports the call, the workspace suffices and a cost model of
+ * the two tensor-core variants (CTA waves x chunks x measured per-chunk times)
+ * expects it to be faster -- typically when B*H*dv/64 leaves SMs idle or needs
+ * several waves -- and otherwise behaves as ldn_chunk_fwd_variant(...,
+ * LDN_VARIANT_AUTO, ...).  Calls on different streams need different workspaces.
  */
 int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *beta,
                      const float *gate, const float *S0, void *out, float *S_final,
                      int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
                      int variant, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Which kernel family ldn_chunk_fwd_ws(..., LDN_VARIANT_AUTO, ...) runs for these
+ * sizes and a workspace of workspace_bytes (pointers assumed aligned): returns
+ * LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR or LDN_VARIANT_SPLIT, or -LDN_ERR_* for
+ * arguments that would be rejected.  Host function; it reads the SM count of
+ * the current device. */
+int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                            size_t workspace_bytes);
 
 /*
  * ldn_decode_step -- one recurrent step for every (b, h), state updated in place.
