@@ -126,13 +126,14 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
         if (bad && st == 0) fail = 1;
         return !bad;
     };
+    // MMA completion: every thread polls the commit barrier itself (no role-wide
+    // barrier on this path); a timeout only marks the CTA failed, and the vote at
+    // the start of the next chunk takes every thread out of the loop together.
     uint32_t sphase = 0;
-    auto wait_smma = [&]() -> bool {
-        const bool ok = (st == 0) ? mbar_wait(smma, sphase, kWaitNs) : true;
+    auto wait_smma = [&]() {
+        if (!mbar_wait(smma, sphase, kWaitNs)) fail = 1;
         sphase ^= 1u;
-        const bool r = vote(ok);
         tc_fence_after();
-        return r;
     };
     const uint32_t id_mma5 = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);   // A K-major, B MN-major
     const uint32_t id_mma6 = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);   // both MN-major
@@ -165,7 +166,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
                 umma_bf16(tbase + kColD5, kmajor_desc(a5_s, 128, k), mnmajor_desc(hb_s, 128, k), id_mma5, k > 0);
             umma_commit(smma);
         }
-        if (!wait_smma()) break;
+        wait_smma();
 
         // ---- O = P U' + Q~ H (rows 0..63) -> out; U = U' - W H (rows 64..127) -> UB
         {
@@ -213,7 +214,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
                 umma_bf16(tbase + kColD6, mnmajor_desc(kt_s, 64, k), mnmajor_desc(ub_s, 64, k), id_mma6, k > 0);
             umma_commit(smma);
         }
-        if (!wait_smma()) break;
+        wait_smma();
 
         // ---- H <- e^{g_C} H + K~^T U (row st), fp16 copy for the next MMA5
         {

@@ -1328,7 +1328,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) { return launch
 // Which tensor-core variant is expected to be faster: a cost model in waves of
 // CTAs (one CTA per SM) x chunks per CTA x measured time per chunk on GB300 --
 // fused 4.4 us (GDN / DeltaNet) or 7.9 us (KDA); split preparation 5.0 / 10.9 us
-// and state step 2.0 us.  The fused kernel wins when its CTAs fill the SMs
+// and state step 1.7 us.  The fused kernel wins when its CTAs fill the SMs
 // once; the split variant when they do not (few sequences) or need several
 // waves (its preparation and state steps are cheaper than a fused chunk step).
 bool chunk_split_preferred(const ChunkArgs &a)
@@ -1336,7 +1336,7 @@ bool chunk_split_preferred(const ChunkArgs &a)
     const int sms = sm_count();
     if (sms <= 0) return false;
     const bool kda = a.mode == LDN_KDA;
-    const double t_fused = kda ? 7.9 : 4.4, t_prep = kda ? 10.9 : 5.0, t_state = 2.0;
+    const double t_fused = kda ? 7.9 : 4.4, t_prep = kda ? 10.9 : 5.0, t_state = 1.7;
     const long long heads = (long long)a.B * a.H, nchunks = (a.T + kC - 1) / kC;
     const long long slices = heads * (a.dv / kDVS);
     const long long waves_f = (slices + sms - 1) / sms;
