@@ -31,6 +31,8 @@ constexpr int kThreads = 128;
 constexpr int kStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kBar = 1;
+constexpr uint32_t kBarU = 2;             // threads 64..127 (the U rows): MMA6 waits only for them
+constexpr int kIssuer6 = 64;
 // stage: A5 image | RV slice | K~ | e^{g_C}
 constexpr uint32_t kOA5 = 0, kORV = 32768, kOKT = 49152, kOEG = 65536;
 constexpr uint32_t kStageTx = 65536 + 512;
@@ -38,7 +40,7 @@ constexpr uint32_t kStageBytes = 66560;                   // 1024-aligned
 constexpr uint32_t kOffHB = kStages * kStageBytes;        // H fp16, MN-major 128 x 64
 constexpr uint32_t kOffUB = kOffHB + 16384;               // U fp16, MN-major 64 x 64
 constexpr uint32_t kOffBars = kOffUB + 8192;
-constexpr uint32_t kSmemBytes = kOffBars + 128 + 1024;
+constexpr uint32_t kSmemBytes = kOffBars + 128 + 1024;   // bars: full[3], smma, drain[2]
 constexpr uint32_t kColD5 = 0, kColD6 = 64, kTmemCols = 128;
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 
@@ -77,7 +79,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     uint8_t *HB = sm + kOffHB, *UB = sm + kOffUB;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBars);   // [kStages]
     uint64_t *smma = full + kStages;
-    uint64_t *drain = smma + 1;
+    uint64_t *drain = smma + 1;   // [2]: one per MMA-issuing thread (0, kIssuer6)
     __shared__ uint32_t tmem_base_s;
     __shared__ int fail;
 
@@ -93,7 +95,8 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     if (st == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
         mbar_init(smma, 1);
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         fence_mbar_init();
         fail = 0;
     }
@@ -202,12 +205,16 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
                 }
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_sync(kBar, kThreads);
+        // MMA6 reads U only: the U rows' threads meet without the O rows' threads,
+        // whose output stores overlap MMA6
+        if (!top) {
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarU, kThreads - 64);
+        }
 
         // ---- MMA6: D6 = K~^T U
-        if (st == 0) {
+        if (st == kIssuer6) {
             tc_fence_after();
             const uint32_t kt_s = smem_u32(stg + kOKT), ub_s = smem_u32(UB);
             for (int k = 0; k < kC / 16; ++k)
@@ -249,13 +256,15 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     }
     tc_fence_before();
     __syncthreads();
-    if (fail && st == 0) {
+    if (fail && (st == 0 || st == kIssuer6)) {
         // drain: the MMAs issued by this thread, then the loads still in flight (bounded)
-        atomicOr(status, 1 << LDN_ERR_TIMEOUT);
-        umma_commit(drain);
-        mbar_wait(drain, 0, kWaitNs / 4);
-        for (int s = 0; s < kStages; ++s)
-            if (pending[s] >= 0) mbar_wait(&full[s], (pending[s] / kStages) & 1, kWaitNs / 4);
+        const int i = st == 0 ? 0 : 1;
+        if (st == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        umma_commit(&drain[i]);
+        mbar_wait(&drain[i], 0, kWaitNs / 4);
+        if (st == 0)
+            for (int s = 0; s < kStages; ++s)
+                if (pending[s] >= 0) mbar_wait(&full[s], (pending[s] / kStages) & 1, kWaitNs / 4);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);

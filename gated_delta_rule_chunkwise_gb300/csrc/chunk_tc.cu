@@ -789,12 +789,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
             // MMA3 / MMA4 of chunk c - 1 have finished reading AV / AK before they are rewritten
-            // (split: and the workspace stores of chunk c - 1, staged there, have read them)
-            if (!prep_vote(pt == 0 && c >= 1
-                               ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs) &&
-                                     (!SPLIT || mbar_wait(&S.bar_stgfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs))
-                               : true))
-                break;
+            // (split: and the workspace stores of chunk c - 1, staged there, have read them).
+            // A timeout only marks the CTA failed; the vote at the next chunk's start takes
+            // every prep thread out of the loop together.
+            if (pt == 0 && c >= 1 &&
+                !(mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs) &&
+                  (!SPLIT || mbar_wait(&S.bar_stgfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs))))
+                S.fail = 1;
+            named_sync(kBarPrep, kPrepThreads);
             if (c < 0) continue;
 
             // ---- P6: stacked operands AV = [P Tu ; Tu] and AK = [-P Tw ; Tw] (fp16, K-major).
@@ -902,12 +904,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (bad && st == 0) S.fail = 1;
             return !bad;
         };
+        // MMA completion: every serial thread polls the commit barrier itself; a timeout
+        // marks the CTA failed and the vote at the next chunk's start ends the loop.
         auto wait_smma = [&]() -> bool {
-            const bool ok = (st == 0) ? mbar_wait(&S.bar_smma, sphase, kWaitNs) : true;
+            if (!mbar_wait(&S.bar_smma, sphase, kWaitNs)) S.fail = 1;
             sphase ^= 1u;
-            const bool r = serial_vote(ok);
             tc_fence_after();
-            return r;
+            return true;
         };
         auto issue_load = [&](int c) {
             const int ls = c % kStages;
@@ -1327,24 +1330,25 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) { return launch
 
 // Which tensor-core variant is expected to be faster: a cost model in waves of
 // CTAs (one CTA per SM) x chunks per CTA x measured time per chunk on GB300 --
-// fused 4.4 us (GDN / DeltaNet) or 7.9 us (KDA); split preparation 5.0 / 10.9 us
-// and state step 1.7 us.  The fused kernel wins when its CTAs fill the SMs
-// once; the split variant when they do not (few sequences) or need several
-// waves (its preparation and state steps are cheaper than a fused chunk step).
+// fused 4.0 us (GDN / DeltaNet) or 7.9 us (KDA); split preparation 5.4 / 10.8 us
+// and state step 1.6 us -- plus a fixed 10 us (one launch) or 20 us (two
+// launches and the preparation pipeline's fill).  The fused kernel wins when its
+// CTAs fill the SMs once; the split variant when they do not (few sequences) or
+// need several waves (its preparation and state steps are cheaper per chunk).
 bool chunk_split_preferred(const ChunkArgs &a)
 {
     const int sms = sm_count();
     if (sms <= 0) return false;
     const bool kda = a.mode == LDN_KDA;
-    const double t_fused = kda ? 7.9 : 4.4, t_prep = kda ? 10.9 : 5.0, t_state = 1.7;
+    const double t_fused = kda ? 7.9 : 4.0, t_prep = kda ? 10.8 : 5.4, t_state = 1.6;
     const long long heads = (long long)a.B * a.H, nchunks = (a.T + kC - 1) / kC;
     const long long slices = heads * (a.dv / kDVS);
     const long long waves_f = (slices + sms - 1) / sms;
     const long long nranges = std::max(1LL, std::min(nchunks, sms / heads));
     const long long cpr = (nchunks + nranges - 1) / nranges;
     const long long waves_p = (heads * ((nchunks + cpr - 1) / cpr) + sms - 1) / sms;
-    const double fused = (double)waves_f * nchunks * t_fused;
-    const double split = (double)waves_p * cpr * t_prep + (double)waves_f * nchunks * t_state;
+    const double fused = 10.0 + (double)waves_f * nchunks * t_fused;
+    const double split = 20.0 + (double)waves_p * cpr * t_prep + (double)waves_f * nchunks * t_state;
     return split < fused;
 }
 
