@@ -39,6 +39,7 @@ EXTRA_WORKLOADS = ("kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d12
 DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000")
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
+MODE_NAME = {0: "deltanet", 1: "gdn", 2: "kda"}
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -205,7 +206,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded recipe, no dataset)",
             "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": 64, "mode": "gdn"},
+                       "chunk": 64, "mode": MODE_NAME[w.mode]},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -471,7 +472,7 @@ def run_ours(args):
             "data": "synthetic (seeded numpy recipe: L2-normalised Gaussian q,k; Gaussian v; sigmoid beta; "
                     "-0.1*softplus log-decay); no dataset",
             "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": 64, "mode": "gdn", "kernel": f"chunk_{from_variant}",
+                       "chunk": 64, "mode": MODE_NAME[w.mode], "kernel": f"chunk_{from_variant}",
                        "l2": "flushed before every timed launch (512 MiB write, then 512 MiB read of another buffer: cold and clean)",
                        "parallelism": f"replica x{world} (independent sequences per GPU)"},
             "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
