@@ -6,7 +6,7 @@ been built, or no GPU is present, the calls raise.
 
 Two layers:
   * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
-    ``ldn_chunk_fwd_workspace_size``, ``ldn_decode_step``,
+    ``ldn_chunk_fwd_workspace_size``, ``ldn_chunk_fwd_noalloc``, ``ldn_decode_step``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
   * ``chunk_fwd`` and ``decode_step``: the same calls on torch CUDA tensors,
@@ -50,6 +50,7 @@ _SIGNATURES = {
     "ldn_chunk_fwd_ws": ([_P] * 8 + [_I] * 9 + [_P, ctypes.c_size_t, _P], _I),
     "ldn_chunk_fwd_workspace_size": ([_I] * 8, ctypes.c_size_t),
     "ldn_chunk_fwd_select_ws": ([_I] * 8 + [ctypes.c_size_t], _I),
+    "ldn_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 9 + [_P], _I),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
     "ldn_get_device_status": ([_P], _I),
     "ldn_status_string": ([_I], ctypes.c_char_p),
@@ -108,6 +109,12 @@ def ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, dtype):
 
 def ldn_chunk_fwd_select_ws(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes):
     return load().ldn_chunk_fwd_select_ws(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes)
+
+
+def ldn_chunk_fwd_noalloc(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                          variant, stream):
+    return load().ldn_chunk_fwd_noalloc(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk,
+                                        mode, dtype, variant, stream)
 
 
 def ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream):

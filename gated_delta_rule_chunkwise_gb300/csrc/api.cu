@@ -60,10 +60,13 @@ static size_t split_workspace_bytes(int B, int T, int H, int dk, int dv, int chu
     return (size_t)B * H * (size_t)((T + chunk - 1) / chunk) * split_unit_bytes(dv);
 }
 
-static int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *beta, const float *gate,
-                          const float *S0, void *out, float *S_final, int B, int T, int H, int dk, int dv,
-                          int chunk, int mode, int dtype, int variant, void *ws, size_t ws_bytes, void *stream)
+// Argument checks shared by the chunk entry points (everything but the
+// workspace).  On LDN_OK, *tc says whether the tensor-core kernels take the call.
+static int check_chunk_args(const void *q, const void *k, const void *v, const float *beta, const float *gate,
+                            const float *S0, const void *out, const float *S_final, int B, int T, int H, int dk,
+                            int dv, int chunk, int mode, int dtype, int variant, bool *tc)
 {
+    *tc = false;
     int st = validate_common(mode, dtype, dk, dv);
     if (st != LDN_OK) return st;
     if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
@@ -71,15 +74,12 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (chunk != 64) return LDN_ERR_UNSUPPORTED;
     // Sizes: token-head count and state element count must stay well inside int64
     // and the grid limits.
-    const long long units = (long long)B * H;
-    if (units > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
+    if ((long long)B * H > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
     if ((long long)B * T * H * (dk > dv ? dk : dv) > (1LL << 40)) return LDN_ERR_UNSUPPORTED;
-    cudaStream_t s = (cudaStream_t)stream;
     if (T == 0) {
         if (S0 && !aligned16(S0)) return LDN_ERR_INVALID_ARG;
         if (S_final && !aligned16(S_final)) return LDN_ERR_INVALID_ARG;
-        if (!S_final) return LDN_OK;
-        return launch_copy_state(S0, S_final, units * dk * dv, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+        return LDN_OK;
     }
     if (!q || !k || !v || !beta || !out) return LDN_ERR_INVALID_ARG;
     if (mode != LDN_DELTANET && !gate) return LDN_ERR_INVALID_ARG;
@@ -89,16 +89,35 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     for (const void *p : vec_ptrs)
         if (p && !aligned16(p)) return LDN_ERR_INVALID_ARG;
     if (!aligned(beta, 4) || (gate && !aligned(gate, 4))) return LDN_ERR_INVALID_ARG;
+    ChunkArgs a{};
+    a.gate = mode == LDN_DELTANET ? nullptr : gate;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype;
+    *tc = dtype == LDN_BF16 && chunk_tc_supported(a);
+    if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT) && !*tc) return LDN_ERR_UNSUPPORTED;
+    return LDN_OK;
+}
 
+static int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *beta, const float *gate,
+                          const float *S0, void *out, float *S_final, int B, int T, int H, int dk, int dv,
+                          int chunk, int mode, int dtype, int variant, void *ws, size_t ws_bytes, void *stream)
+{
+    bool tc = false;
+    const int st = check_chunk_args(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                                    variant, &tc);
+    if (st != LDN_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        if (!S_final) return LDN_OK;
+        return launch_copy_state(S0, S_final, (long long)B * H * dk * dv, s) == cudaSuccess ? LDN_OK
+                                                                                            : LDN_ERR_CUDA;
+    }
     ChunkArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S0, out, S_final,
                 B, T, H, dk, dv, chunk, mode, dtype, nullptr};
-    const bool tc = dtype == LDN_BF16 && chunk_tc_supported(a);
     const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype) : 0;
     const bool ws_ok = ws && aligned(ws, 256) && need > 0 && ws_bytes >= need;
     if (variant == LDN_VARIANT_AUTO)
         variant = !tc ? LDN_VARIANT_SIMT
                       : (ws_ok && chunk_split_preferred(a) ? LDN_VARIANT_SPLIT : LDN_VARIANT_TENSOR);
-    if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT) && !tc) return LDN_ERR_UNSUPPORTED;
     if (variant == LDN_VARIANT_SPLIT && !ws_ok) return LDN_ERR_INVALID_ARG;
     a.status = status_word_ptr();
     if (!a.status) return LDN_ERR_CUDA;
@@ -126,6 +145,94 @@ extern "C" int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, con
 {
     return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, variant,
                           workspace, workspace_bytes, stream);
+}
+
+// Split variant through the library's static scratch.  The call is cut into
+// pieces whose workspace fits the scratch: groups of whole sequences when one
+// sequence fits, else chunk-aligned runs of tokens of one sequence, the state
+// carried from run to run through S_final (or, without one, a state slot at
+// the top of the scratch).  Pieces run in stream order and reuse the scratch.
+extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *beta,
+                                     const float *gate, const float *S0, void *out, float *S_final,
+                                     int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                                     int variant, void *stream)
+{
+    if (variant != LDN_VARIANT_AUTO && variant != LDN_VARIANT_SPLIT)
+        return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                              variant, nullptr, 0, stream);
+    bool tc = false;
+    int st = check_chunk_args(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                              variant, &tc);
+    if (st != LDN_OK) return st;
+    if (T == 0 || !tc)   // state copy, or the SIMT kernel: no scratch
+        return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                              LDN_VARIANT_AUTO, nullptr, 0, stream);
+    ChunkArgs whole{};
+    whole.gate = mode == LDN_DELTANET ? nullptr : gate;
+    whole.B = B; whole.T = T; whole.H = H; whole.dk = dk; whole.dv = dv; whole.chunk = chunk;
+    whole.mode = mode; whole.dtype = dtype;
+    if (variant == LDN_VARIANT_AUTO && !chunk_split_preferred(whole))
+        return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                              LDN_VARIANT_TENSOR, nullptr, 0, stream);
+
+    // Plan: nb sequences per piece, or (nb == 0) runs of tpc chunks of one sequence.
+    const size_t cap = kStaticScratchBytes;
+    const size_t unit = split_unit_bytes(dv);
+    const long long nch = (T + chunk - 1) / chunk;
+    const size_t per_seq = (size_t)H * nch * unit;
+    const size_t state_elems = (size_t)H * dk * dv;
+    int nb = 0;
+    long long tpc = 0;
+    size_t carry_bytes = 0;
+    if (per_seq <= cap) {
+        nb = (int)((size_t)B < cap / per_seq ? (size_t)B : cap / per_seq);
+    } else {
+        carry_bytes = S_final ? 0 : (state_elems * sizeof(float) + 255) / 256 * 256;
+        if (carry_bytes < cap) tpc = (long long)((cap - carry_bytes) / ((size_t)H * unit));
+        if (tpc == 0)
+            return variant == LDN_VARIANT_SPLIT
+                       ? LDN_ERR_UNSUPPORTED
+                       : chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode,
+                                        dtype, LDN_VARIANT_TENSOR, nullptr, 0, stream);
+    }
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *scr = nullptr;
+    size_t scr_bytes = 0;
+    int dev = 0;
+    if (static_scratch_acquire(s, &scr, &scr_bytes, &dev) != cudaSuccess) return LDN_ERR_CUDA;
+    const size_t el = dtype == LDN_BF16 ? 2 : 4;
+    const size_t gate_w = mode == LDN_KDA ? (size_t)dk : 1;
+    // One piece: sequences b0 .. b0+np-1, tokens t0 .. t0+len-1 (t0 > 0 only when np == 1).
+    auto piece = [&](int b0, int np, int t0, int len, const float *s0, float *sf, size_t ws_bytes) {
+        const size_t tok = ((size_t)b0 * T + t0) * H;   // token-head offset of (b0, t0)
+        return chunk_fwd_impl((const uint8_t *)q + tok * dk * el, (const uint8_t *)k + tok * dk * el,
+                              (const uint8_t *)v + tok * dv * el, beta + tok, gate ? gate + tok * gate_w : nullptr,
+                              s0, (uint8_t *)out + tok * dv * el, sf, np, len, H, dk, dv, chunk, mode, dtype,
+                              LDN_VARIANT_SPLIT, scr, ws_bytes, stream);
+    };
+    st = LDN_OK;
+    if (nb > 0) {
+        for (int b0 = 0; b0 < B && st == LDN_OK; b0 += nb) {
+            const int np = B - b0 < nb ? B - b0 : nb;
+            st = piece(b0, np, 0, T, S0 ? S0 + (size_t)b0 * state_elems : nullptr,
+                       S_final ? S_final + (size_t)b0 * state_elems : nullptr, cap);
+        }
+    } else {
+        const long long run = tpc * chunk;
+        for (int b = 0; b < B && st == LDN_OK; ++b) {
+            float *carry = S_final ? S_final + (size_t)b * state_elems : (float *)(scr + cap - carry_bytes);
+            for (long long t0 = 0; t0 < T && st == LDN_OK; t0 += run) {
+                const int len = (int)(T - t0 < run ? T - t0 : run);
+                const float *s0 = t0 == 0 ? (S0 ? S0 + (size_t)b * state_elems : nullptr) : carry;
+                float *sf = t0 + len >= T ? (S_final ? S_final + (size_t)b * state_elems : nullptr) : carry;
+                st = piece(b, 1, (int)t0, len, s0, sf, cap - carry_bytes);
+            }
+        }
+    }
+    const cudaError_t rel = static_scratch_release(s, dev);
+    if (st == LDN_OK && rel != cudaSuccess) st = LDN_ERR_CUDA;
+    return st;
 }
 
 extern "C" int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,

@@ -50,6 +50,12 @@ cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream
 bool chunk_split_preferred(const ChunkArgs &a);   // expected faster than the fused kernel
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 int *status_word_ptr();   // address of the device status word on the current device
+// Library-owned split-variant scratch of ldn_chunk_fwd_noalloc (static_scratch.cu).
+// acquire() locks the current device's scratch and orders `s` after its previous
+// user; release() records the end of this use on `s` and unlocks.
+constexpr size_t kStaticScratchBytes = (size_t)256 << 20;
+cudaError_t static_scratch_acquire(cudaStream_t s, uint8_t **ptr, size_t *bytes, int *device);
+cudaError_t static_scratch_release(cudaStream_t s, int device);
 cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cudaStream_t stream);
 
 // Loads of q/k/v in either element type, widened to fp32.

@@ -24,7 +24,7 @@
  *     aligned and q, k, v, out aligned to their element size; beta and gate
  *     are 4-byte aligned everywhere.  The caller owns every buffer (and the
  *     workspace of the split variant); the library allocates no device memory
- *     per call.
+ *     per call (ldn_chunk_fwd_noalloc uses one static library-owned array).
  *   - Gates are natural-log decays: alpha_t = exp(gate), a_t = exp(gate[c]).
  *     A positive log-gate is accepted (it is not clamped); beta is not clamped.
  *   - q is not scaled and q, k are not normalised by the library (scale = 1).
@@ -158,6 +158,41 @@ int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *b
  * the current device. */
 int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
                             size_t workspace_bytes);
+
+/*
+ * ldn_chunk_fwd_noalloc -- ldn_chunk_fwd_ws without a caller workspace.
+ * The pages have no counterpart to this entry: it is a convenience of this
+ * library for callers that cannot provide device memory.
+ *
+ * The split variant runs through a library-owned device array of 256 MiB per
+ * device (a static __device__ array, backed when the library's module holding
+ * it first loads, at the latest at the first call); no device memory is
+ * allocated per call.  A call whose workspace does not fit is cut into pieces
+ * that do: groups of whole sequences, or, when one sequence alone needs more,
+ * runs of whole chunks of one sequence with the state carried between runs in
+ * S_final (or in a slot of the array when S_final is NULL).  The pieces are
+ * enqueued on `stream` one after another; the result equals that of
+ * ldn_chunk_fwd_ws with the split variant up to floating-point rounding (the
+ * kernels and per-chunk arithmetic are the same).
+ *
+ * Arguments, layouts, alignment and error behaviour are those of
+ * ldn_chunk_fwd_variant, with LDN_VARIANT_SPLIT also accepted.
+ * LDN_VARIANT_AUTO runs the split variant where ldn_chunk_fwd_ws with an
+ * unlimited workspace would, otherwise the fused tensor-core or the SIMT
+ * kernel; LDN_VARIANT_SPLIT returns LDN_ERR_UNSUPPORTED when the call cannot
+ * be cut to fit (H so large that one chunk of all heads exceeds the array).
+ * LDN_VARIANT_SIMT and LDN_VARIANT_TENSOR touch no scratch.
+ *
+ * Calls share the array: calls on different streams are ordered on the
+ * device by an event the library records after each call (a host lock covers
+ * the enqueue).  During stream capture that event is not used, so replays of
+ * a captured graph must be ordered by the caller with other users of the
+ * array.  The host lock makes the call thread-safe.
+ */
+int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *beta,
+                          const float *gate, const float *S0, void *out, float *S_final,
+                          int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                          int variant, void *stream);
 
 /*
  * ldn_decode_step -- one recurrent step for every (b, h), state updated in place.

@@ -145,3 +145,40 @@ def test_split_without_workspace_is_rejected(lib):
     assert ldn.ldn_chunk_fwd_ws(*args, ldn.LDN_VARIANT_SPLIT, 0, 0, 0) == ldn.LDN_ERR_INVALID_ARG
     assert ldn.ldn_chunk_fwd_ws(*args, ldn.LDN_VARIANT_SPLIT, 1 << 20, 16, 0) == ldn.LDN_ERR_INVALID_ARG
     assert ldn.ldn_chunk_fwd_ws(*args, ldn.LDN_VARIANT_SPLIT, (1 << 20) + 8, 1 << 30, 0) == ldn.LDN_ERR_INVALID_ARG
+
+
+def _noalloc(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, gate=FAKE, S0=None, out=FAKE, S_final=None,
+             B=1, T=64, H=1, dk=64, dv=64, chunk=64, mode=1, dtype=1, variant=0, stream=None)
+    a.update(kw)
+    return ldn.ldn_chunk_fwd_noalloc(a["q"], a["k"], a["v"], a["beta"], a["gate"], a["S0"], a["out"],
+                                     a["S_final"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"],
+                                     a["mode"], a["dtype"], a["variant"], a["stream"])
+
+
+@pytest.mark.parametrize("variant", [ldn.LDN_VARIANT_AUTO, ldn.LDN_VARIANT_SPLIT])
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(out=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None, mode=2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 4), ldn.LDN_ERR_INVALID_ARG),
+    (dict(S_final=FAKE + 8), ldn.LDN_ERR_INVALID_ARG),
+    (dict(beta=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(mode=3), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dtype=2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(B=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(T=-1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dk=96), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(chunk=32), ldn.LDN_ERR_UNSUPPORTED),
+])
+def test_noalloc_rejects_bad_arguments(lib, kw, want, variant):
+    """The no-allocation entry checks its arguments like the others, before it takes
+    the scratch or enqueues anything."""
+    assert _noalloc(variant=variant, **kw) == want
+
+
+def test_noalloc_split_outside_the_tensor_kernels_is_unsupported(lib):
+    assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=64) == ldn.LDN_ERR_UNSUPPORTED   # dk = 64
+    assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=128, dtype=0) == ldn.LDN_ERR_UNSUPPORTED   # fp32
+    assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=128, mode=2, gate=FAKE + 4) == ldn.LDN_ERR_UNSUPPORTED
+    assert _noalloc(variant=4) == ldn.LDN_ERR_INVALID_ARG
