@@ -40,6 +40,7 @@ DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
 MODE_NAME = {0: "deltanet", 1: "gdn", 2: "kda"}
+KERNEL_NAME = {2: "tcgen05", 3: "split", 4: "pair"}   # LDN_VARIANT_* -> kernel family in the JSON line
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -325,8 +326,9 @@ def run_ours(args):
     nbytes = chunk_bytes(w.B, w.T, w.H, w.dk, w.dv, el, w.mode, False, True)
     flops = chunk_flops(w.B, w.T, w.H, w.dk, w.dv)
     achieved_gbs = nbytes / (ms / 1e3) / 1e9
-    from_variant = {ldn.LDN_VARIANT_TENSOR: "tcgen05", ldn.LDN_VARIANT_SPLIT: "split"}.get(chosen, "simt")
-    src = {"tcgen05": ["chunk_tc.cu"], "split": ["chunk_tc.cu", "chunk_state.cu"]}.get(from_variant, ["chunk_simt.cu"])
+    from_variant = KERNEL_NAME.get(chosen, "simt")
+    src = {"tcgen05": ["chunk_tc.cu"], "pair": ["chunk_tc.cu"],
+           "split": ["chunk_tc.cu", "chunk_state.cu"]}.get(from_variant, ["chunk_simt.cu"])
     kernel_key = f"chunk_{from_variant}:{args.workload}"
     src_hash = kernel_source_hash(src)
     traffic = recorded_traffic(kernel_key, src_hash)
@@ -405,7 +407,7 @@ def run_ours(args):
             launches += 4 * (2 if ochosen == ldn.LDN_VARIANT_SPLIT else 1)
             oms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in oev))
             ob = chunk_bytes(ow.B, ow.T, ow.H, ow.dk, ow.dv, oel, ow.mode, ow.S0 is not None, True)
-            kern = {ldn.LDN_VARIANT_TENSOR: "tcgen05", ldn.LDN_VARIANT_SPLIT: "split"}.get(ochosen, "simt")
+            kern = KERNEL_NAME.get(ochosen, "simt")
             others[name] = {"tokens_per_s": world * ow.B * ow.T / (oms / 1e3), "ms_per_launch": oms,
                             "kernel": f"chunk_{kern}", "algorithmic_bytes": ob,
                             "hbm_frac": ob / (oms / 1e3) / 1e9 / hbm_peak}
@@ -494,7 +496,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 SIMT fp32, 2 tcgen05 fused, 3 split")
+    ap.add_argument("--variant", type=int, default=0,
+                    help="0 auto, 1 SIMT fp32, 2 tcgen05 fused, 3 split, 4 tcgen05 cluster pair")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

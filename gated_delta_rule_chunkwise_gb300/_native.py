@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libldn.so")
 LDN_DELTANET, LDN_GDN, LDN_KDA = 0, 1, 2
 LDN_F32, LDN_BF16 = 0, 1
 LDN_OK, LDN_ERR_INVALID_ARG, LDN_ERR_UNSUPPORTED, LDN_ERR_CUDA, LDN_ERR_TIMEOUT = 0, 1, 2, 3, 4
-LDN_VARIANT_AUTO, LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR, LDN_VARIANT_SPLIT = 0, 1, 2, 3
+LDN_VARIANT_AUTO, LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR, LDN_VARIANT_SPLIT, LDN_VARIANT_PAIR = 0, 1, 2, 3, 4
 
 MODES = {"deltanet": LDN_DELTANET, "gdn": LDN_GDN, "kda": LDN_KDA}
 

@@ -70,7 +70,7 @@ static int check_chunk_args(const void *q, const void *k, const void *v, const f
     int st = validate_common(mode, dtype, dk, dv);
     if (st != LDN_OK) return st;
     if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
-    if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_SPLIT) return LDN_ERR_INVALID_ARG;
+    if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_PAIR) return LDN_ERR_INVALID_ARG;
     if (chunk != 64) return LDN_ERR_UNSUPPORTED;
     // Sizes: token-head count and state element count must stay well inside int64
     // and the grid limits.
@@ -93,7 +93,9 @@ static int check_chunk_args(const void *q, const void *k, const void *v, const f
     a.gate = mode == LDN_DELTANET ? nullptr : gate;
     a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype;
     *tc = dtype == LDN_BF16 && chunk_tc_supported(a);
-    if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT) && !*tc) return LDN_ERR_UNSUPPORTED;
+    if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT || variant == LDN_VARIANT_PAIR) && !*tc)
+        return LDN_ERR_UNSUPPORTED;
+    if (variant == LDN_VARIANT_PAIR && !chunk_pair_supported(a)) return LDN_ERR_UNSUPPORTED;
     return LDN_OK;
 }
 
@@ -115,14 +117,13 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
                 B, T, H, dk, dv, chunk, mode, dtype, nullptr};
     const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype) : 0;
     const bool ws_ok = ws && aligned(ws, 256) && need > 0 && ws_bytes >= need;
-    if (variant == LDN_VARIANT_AUTO)
-        variant = !tc ? LDN_VARIANT_SIMT
-                      : (ws_ok && chunk_split_preferred(a) ? LDN_VARIANT_SPLIT : LDN_VARIANT_TENSOR);
+    if (variant == LDN_VARIANT_AUTO) variant = !tc ? LDN_VARIANT_SIMT : chunk_tc_pick(a, ws_ok);
     if (variant == LDN_VARIANT_SPLIT && !ws_ok) return LDN_ERR_INVALID_ARG;
     a.status = status_word_ptr();
     if (!a.status) return LDN_ERR_CUDA;
     cudaError_t err;
     if (variant == LDN_VARIANT_SPLIT) err = launch_chunk_split(a, (uint8_t *)ws, s);
+    else if (variant == LDN_VARIANT_PAIR) err = launch_chunk_pair(a, s);
     else if (variant == LDN_VARIANT_TENSOR) err = launch_chunk_tc(a, s);
     else err = launch_chunk_simt(a, s);
     return err == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
@@ -171,9 +172,12 @@ extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v
     whole.gate = mode == LDN_DELTANET ? nullptr : gate;
     whole.B = B; whole.T = T; whole.H = H; whole.dk = dk; whole.dv = dv; whole.chunk = chunk;
     whole.mode = mode; whole.dtype = dtype;
-    if (variant == LDN_VARIANT_AUTO && !chunk_split_preferred(whole))
-        return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
-                              LDN_VARIANT_TENSOR, nullptr, 0, stream);
+    if (variant == LDN_VARIANT_AUTO) {
+        const int pick = chunk_tc_pick(whole, true);
+        if (pick != LDN_VARIANT_SPLIT)
+            return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
+                                  pick, nullptr, 0, stream);
+    }
 
     // Plan: nb sequences per piece, or (nb == 0) runs of tpc chunks of one sequence.
     const size_t cap = kStaticScratchBytes;
@@ -193,7 +197,7 @@ extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v
             return variant == LDN_VARIANT_SPLIT
                        ? LDN_ERR_UNSUPPORTED
                        : chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode,
-                                        dtype, LDN_VARIANT_TENSOR, nullptr, 0, stream);
+                                        dtype, chunk_tc_pick(whole, false), nullptr, 0, stream);
     }
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -246,8 +250,7 @@ extern "C" int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int 
     a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = B; a.T = T; a.H = H;
     if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return LDN_VARIANT_SIMT;
     const size_t need = split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype);
-    return (need > 0 && workspace_bytes >= need && chunk_split_preferred(a)) ? LDN_VARIANT_SPLIT
-                                                                             : LDN_VARIANT_TENSOR;
+    return chunk_tc_pick(a, need > 0 && workspace_bytes >= need);
 }
 
 extern "C" size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)

@@ -174,35 +174,32 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
         // ---- O = P U' + Q~ H (rows 0..63) -> out; U = U' - W H (rows 64..127) -> UB
         {
             const uint8_t *rv = stg + kORV;
+            float v[kDVS];   // the whole slice row in one TMEM round trip
 #pragma unroll
-            for (int n = 0; n < kDVS; n += 32) {
-                float v[32];
-                tmem_ld16(tbase + lane_base + kColD5 + n, v);
-                tmem_ld16(tbase + lane_base + kColD5 + n + 16, v + 16);
-                tmem_ld_wait();
+            for (int q = 0; q < kDVS / 16; ++q) tmem_ld16(tbase + lane_base + kColD5 + 16 * q, v + 16 * q);
+            tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(rv + sw128_offset(st, n + 8 * q));
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&w);
+            for (int q = 0; q < kDVS / 8; ++q) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(rv + sw128_offset(st, 8 * q));
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&w);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = __half22float2(h2[i]);
-                        v[8 * q + 2 * i] += f.x;
-                        v[8 * q + 2 * i + 1] += f.y;
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __half22float2(h2[i]);
+                    v[8 * q + 2 * i] += f.x;
+                    v[8 * q + 2 * i + 1] += f.y;
                 }
-                if (top) {
-                    if (st < L) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + st) * H + h) * dv + n0 + n);
+            }
+            if (top) {
+                if (st < L) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + st) * H + h) * dv + n0);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(pack_bf2(v[8 * q], v[8 * q + 1]), pack_bf2(v[8 * q + 2], v[8 * q + 3]),
-                                                pack_bf2(v[8 * q + 4], v[8 * q + 5]), pack_bf2(v[8 * q + 6], v[8 * q + 7]));
-                    }
-                } else {
-                    st_row16(UB, st - 64, n, v);
-                    st_row16(UB, st - 64, n + 16, v + 16);
+                    for (int q = 0; q < kDVS / 8; ++q)
+                        dst[q] = make_uint4(pack_bf2(v[8 * q], v[8 * q + 1]), pack_bf2(v[8 * q + 2], v[8 * q + 3]),
+                                            pack_bf2(v[8 * q + 4], v[8 * q + 5]), pack_bf2(v[8 * q + 6], v[8 * q + 7]));
                 }
+            } else {
+#pragma unroll
+                for (int n = 0; n < kDVS; n += 16) st_row16(UB, st - 64, n, v + n);
             }
         }
         // MMA6 reads U only: the U rows' threads meet without the O rows' threads,
@@ -226,20 +223,17 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
         // ---- H <- e^{g_C} H + K~^T U (row st), fp16 copy for the next MMA5
         {
             const float g = reinterpret_cast<const float *>(stg + kOEG)[st];
+            float v[kDVS];
 #pragma unroll
-            for (int n = 0; n < kDVS; n += 32) {
-                float v[32];
-                tmem_ld16(tbase + lane_base + kColD6 + n, v);
-                tmem_ld16(tbase + lane_base + kColD6 + n + 16, v + 16);
-                tmem_ld_wait();
+            for (int q = 0; q < kDVS / 16; ++q) tmem_ld16(tbase + lane_base + kColD6 + 16 * q, v + 16 * q);
+            tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    Hreg[n + i] = g * Hreg[n + i] + v[i];
-                    v[i] = Hreg[n + i];
-                }
-                st_row16(HB, st, n, v);
-                st_row16(HB, st, n + 16, v + 16);
+            for (int i = 0; i < kDVS; ++i) {
+                Hreg[i] = g * Hreg[i] + v[i];
+                v[i] = Hreg[i];
             }
+#pragma unroll
+            for (int n = 0; n < kDVS; n += 16) st_row16(HB, st, n, v + n);
         }
         fence_proxy_async_smem();
         tc_fence_before();

@@ -51,6 +51,20 @@
 // result within a few 1e-3 of the exact recurrence on a max-error / RMS scale.
 // Inputs and intermediates must stay below the fp16 range (65504).
 //
+// Pair variant (DeltaNet / Gated DeltaNet, dv = 128): the two dv slices of a
+// (b, h) run as a cluster of two CTAs, and the state-independent preparation,
+// which the fused kernel repeats in both, is split between them by chunk
+// parity.  After P6 the preparing CTA copies [P Tu ; Tu], [-P Tw ; Tw] (32 KB)
+// into the peer's AV / AK with one shared::cluster bulk copy; the peer's serial
+// warps convert its own k / v tiles of that chunk and issue MMA3 / MMA4 while
+// MMA6 of the previous chunk runs.  AV / AK are then written by the two CTAs in
+// turn, chunk by chunk: a barrier per chunk parity counts the MMA3 / MMA4
+// commits of both CTAs (one multicast commit each) before either writes the
+// next chunk's operands.  Waits on barriers the peer completes use the
+// CTA-scope try_wait like every other wait (the arrival and the transaction
+// count carry the ordering); a cluster-scope acquire in the poll loop slowed
+// the whole SM.
+//
 // Every mbarrier wait is bounded in time (2 s); a timeout sets LDN_ERR_TIMEOUT
 // in the status word, both roles abandon their loops, in-flight copies and
 // MMAs are drained with bounded waits, TMEM is freed and the CTA returns.
@@ -135,8 +149,12 @@ struct Small {
     uint64_t bar_kbfree[2];   // KDA: MMA6 of chunk c finished reading side tile c & 1
     uint64_t bar_dkfree[2];   // split: the epilogue has read DK of chunk c (DK has one buffer)
     uint64_t bar_stgfree[2];  // split: the workspace stores of chunk c have read their staging (AV / AK)
+    uint64_t bar_recv;        // pair: the peer's [P Tu ; Tu], [-P Tw ; Tw] of a chunk landed in AV / AK
+    uint64_t bar_avakread[2]; // pair: MMA3 / MMA4 of chunk c read AV / AK in both CTAs (2 arrivals)
+    uint64_t bar_fin;         // pair: the last commit of both MMA issuers of both CTAs (4 arrivals)
     uint32_t tmem_base;
     int fail;
+    uint32_t sent, recvd;     // pair: operand transfers issued to / consumed from the peer
     // Per-chunk gate data, slot = chunk % 3: written one chunk ahead by the gate
     // warp, read by the prep warps and (eg, egc, gC) by the serial warps.
     int exact[3];             // per-entry exponentials for this chunk
@@ -208,10 +226,15 @@ __device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int t, i
     }
 }
 
-// SPLIT = false: the fused kernel, one CTA per (b, h, 64-wide dv slice) over the whole sequence.
-// SPLIT = true: the preparation kernel of the split variant, one CTA per (b, h, range of
+// KIND kFused: the fused kernel, one CTA per (b, h, 64-wide dv slice) over the whole sequence.
+// KIND kSplit: the preparation kernel of the split variant, one CTA per (b, h, range of
 // `cpr` chunks) over the whole dv; its serial warps write the chunk operands to `ws`.
-template <int MODE, bool SPLIT>
+// KIND kPair: the fused kernel with the two dv slices of a (b, h) (dv = 128) as a cluster of
+// two CTAs that share the state-independent preparation: CTA r prepares chunks r, r + 2, ...
+// and copies their [P Tu ; Tu], [-P Tw ; Tw] into the peer's shared memory, whose serial
+// warps issue MMA3 / MMA4 for those chunks themselves (DeltaNet / Gated DeltaNet).
+constexpr int kFused = 0, kSplit = 1, kPair = 2;
+template <int MODE, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ beta,
@@ -222,6 +245,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
     // array so that every access below stays a shared-memory access.
     uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
+    constexpr bool SPLIT = KIND == kSplit, PAIR = KIND == kPair;
+    static_assert(!PAIR || MODE != LDN_KDA, "the pair kernel takes DeltaNet / Gated DeltaNet");
     using LY = Layout<MODE, SPLIT>;
     constexpr int kStages = LY::stages;
     constexpr bool kKda = MODE == LDN_KDA;
@@ -245,6 +270,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int nchunks = SPLIT ? min(cpr, nchunks_all - cb) : nchunks_all;
     const uint32_t quad = (uint32_t)(warp & 3);          // TMEM lane quadrant of this warp
     const uint32_t lane_base = (32u * quad) << 16;
+    // pair: cluster rank = dv slice (blockIdx.x % 2); the peer is the other slice of (b, h)
+    const int prank = PAIR ? (int)(blockIdx.x & 1) : 0;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&S.bar_load[i], 1);
@@ -262,8 +289,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&S.bar_dkfree[1], 1);
         mbar_init(&S.bar_stgfree[0], 1);
         mbar_init(&S.bar_stgfree[1], 1);
+        mbar_init(&S.bar_recv, 1);
+        mbar_init(&S.bar_avakread[0], 2);
+        mbar_init(&S.bar_avakread[1], 2);
+        mbar_init(&S.bar_fin, 4);
         fence_mbar_init();
         S.fail = 0;
+        S.sent = S.recvd = 0;
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
@@ -274,6 +306,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // the peer's barriers exist before anything reaches them
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
     int pending[kMaxStages] = {-1, -1, -1};   // chunk last loaded into ring stage ls (serial thread 0)
@@ -563,19 +596,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         named_sync(kBarPrep, kPrepThreads);
 
-        // Iteration c = -1 runs only the look-ahead part (gates, operands and MMA1 of
-        // chunk 0), so that code exists once.
-        for (int c = -1; c < nchunks; ++c) {
-            const int cp = c < 0 ? 0 : c;
+        // The chunks this CTA prepares: every chunk, or (pair) every other one from its
+        // rank on.  Iteration c = c0 - step runs only the look-ahead part (gates,
+        // operands and MMA1 of chunk c0), so that code exists once.
+        constexpr int kStep = PAIR ? 2 : 1;
+        const int c0 = prank;
+        for (int c = c0 - kStep; c < nchunks; c += kStep) {
+            const int cn = c + kStep;     // the next chunk this CTA prepares
+            const bool run = c >= c0;
+            const int cp = run ? c : c0;
             const int s = cp & 1, ls = cp % kStages, gs = cp % 3;
             uint8_t *QK = sm + LY::qk + ls * kQKBytes;
             uint8_t *Vt = sm + LY::v + ls * LY::vbytes;
             const uint32_t qk_s = smem_u32(QK), k_s = qk_s + 8192, v_s = smem_u32(Vt);
 
-            const bool kexact = kKda && c >= 0 && kda_exact(c);
+            const bool kexact = kKda && run && kda_exact(c);
             float Gn[8][8];   // KDA, warps 4-7: log-gates of chunk c + 1
-            if (kKda && warp >= 4 && c + 1 < nchunks) kda_load_gates(c + 1, Gn);
-            if (c >= 0) {
+            if (kKda && warp >= 4 && cn < nchunks) kda_load_gates(cn, Gn);
+            if (run) {
             // ---- P1: MMA1 of chunk c (issued while chunk c - 1 was prepared) complete
             if (!wait_pmma()) break;
 
@@ -660,30 +698,43 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float frr = S.fr[gs][r] * (isP ? 1.f : S.beta[gs][r]), gr = S.g[gs][r];
                 const float br = isP ? 1.f : S.beta[gs][r];
                 const bool exact = MODE == LDN_GDN && S.exact[gs] != 0;
-                float v[32];
-                tmem_ld16(tbase + lane_base + kColD1 + 32 * half, v);
-                tmem_ld16(tbase + lane_base + kColD1 + 32 * half + 16, v + 16);
-                tmem_ld_wait();
-                if (exact) {   // log-decay span too wide for the factored form: one exp per entry
+                __half *dst = (isP ? P16 : A16) + r * kLd16 + 32 * half;
+                if (exact) {
+                    // log-decay span too wide for the factored form: one exp per entry.  A rare
+                    // path, kept compact (16 columns per pass, the pass loop not unrolled)
+#pragma unroll 1
+                    for (int q = 0; q < 2; ++q) {
+                        float w[16];
+                        tmem_ld16(tbase + lane_base + kColD1 + 32 * half + 16 * q, w);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int j = 32 * half + i;
-                        const bool keep = isP ? (j <= r) : (j < r);
-                        v[i] = keep ? v[i] * br * expf(gr - S.g[gs][j]) : 0.f;
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = 32 * half + 16 * q + i;
+                            const bool keep = isP ? (j <= r) : (j < r);
+                            w[i] = keep ? w[i] * br * expf(gr - S.g[gs][j]) : 0.f;
+                        }
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 16 * q);
+                        d4[0] = make_uint4(pack_h2(w[0], w[1]), pack_h2(w[2], w[3]), pack_h2(w[4], w[5]), pack_h2(w[6], w[7]));
+                        d4[1] = make_uint4(pack_h2(w[8], w[9]), pack_h2(w[10], w[11]), pack_h2(w[12], w[13]),
+                                           pack_h2(w[14], w[15]));
                     }
                 } else {
+                    float v[32];
+                    tmem_ld16(tbase + lane_base + kColD1 + 32 * half, v);
+                    tmem_ld16(tbase + lane_base + kColD1 + 32 * half + 16, v + 16);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int j = 32 * half + i;
                         const bool keep = isP ? (j <= r) : (j < r);
                         v[i] = keep ? (frr * v[i]) * S.fc[gs][j] : 0.f;
                     }
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>((isP ? P16 : A16) + r * kLd16 + 32 * half);
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    dst[q4] = make_uint4(pack_h2(v[8 * q4], v[8 * q4 + 1]), pack_h2(v[8 * q4 + 2], v[8 * q4 + 3]),
-                                         pack_h2(v[8 * q4 + 4], v[8 * q4 + 5]), pack_h2(v[8 * q4 + 6], v[8 * q4 + 7]));
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        d4[q4] = make_uint4(pack_h2(v[8 * q4], v[8 * q4 + 1]), pack_h2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                                            pack_h2(v[8 * q4 + 4], v[8 * q4 + 5]), pack_h2(v[8 * q4 + 6], v[8 * q4 + 7]));
+                }
             }
             tc_fence_before();   // D1 has been read: the next MMA1 may overwrite it
             named_sync(kBarPrep, kPrepThreads);
@@ -713,13 +764,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tile_bf16_to_f16(Vt, SPLIT ? dv / kDVS * kVBytes : kVBytes, pt - 64, kPrepThreads - 64);
             }
             named_sync(kBarPrep, kPrepThreads);
-            }   // c >= 0
+            }   // run
             // Below-diagonal blocks, one warp per 16-column block i (warps 0..2):
             //   T_{R,i} = -T_{R,R} sum_{k=i}^{R-1} A_{R,k} T_{k,i},   R = i+1 .. 3,
             // each 16x16x16 product as two m16n8k16 fp16 warp MMAs (fp32 accumulate),
             // operands fetched with ldmatrix (row-major A blocks, transposed B blocks).
             if (warp < 3) {
-                if (c >= 0) {
+                if (run) {
                 const int i = warp, g = lane >> 2, t4 = lane & 3;
                 const int lr = lane & 15, lc = 8 * (lane >> 4);   // ldmatrix row / column of this lane
                 __half *X = X16 + 16 * 24 * warp;                  // 16x16 fp16 scratch, row stride 24
@@ -757,14 +808,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                     __syncwarp();
                 }
-                }   // c >= 0
+                }   // run
             } else if (warp == kIssuer / 32) {
-                // look-ahead: MMA1 of chunk c + 1 into D1 (read by P4 above)
+                // look-ahead: MMA1 of the next chunk into D1 (read by P4 above)
                 if constexpr (kKda) {
                     named_sync(kBarBuildIssue, 160);   // operands of chunk c + 1 built
-                    if (issuer && c + 1 < nchunks) kda_issue_mma1(c + 1);
+                    if (issuer && cn < nchunks) kda_issue_mma1(cn);
                 } else {
-                    if (issuer && c + 1 < nchunks && !issue_mma1(c + 1)) S.fail = 1;
+                    // (pair: after P9 instead -- chunk c + 2's tiles land only once the serial
+                    // warps have finished chunk c - 1)
+                    if (!PAIR && issuer && cn < nchunks && !issue_mma1(cn)) S.fail = 1;
                 }
             } else {
                 if (warp == kGateWarp) {
@@ -779,25 +832,31 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) {
                         if (lane == 0) S.fail = 1;
-                    } else if (c + 1 < nchunks) {
-                        compute_gates(c + 1);
+                    } else if (c + 1 < nchunks && c + 1 >= 0) {
+                        compute_gates(c + 1);   // pair: the peer's chunk (its gates are needed here too)
                     }
                 }
                 if constexpr (kKda) {   // warps 4-7: KDA operands of chunk c + 1
-                    if (c + 1 < nchunks) kda_build(c + 1, Gn);
+                    if (cn < nchunks) kda_build(cn, Gn);
                     named_sync(kBarBuildIssue, 160);
                 }
             }
             // MMA3 / MMA4 of chunk c - 1 have finished reading AV / AK before they are rewritten
-            // (split: and the workspace stores of chunk c - 1, staged there, have read them).
+            // (split: and the workspace stores of chunk c - 1, staged there, have read them;
+            // pair: in both CTAs, since this CTA's AV / AK go to the peer's as well).
             // A timeout only marks the CTA failed; the vote at the next chunk's start takes
             // every prep thread out of the loop together.
-            if (pt == 0 && c >= 1 &&
-                !(mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs) &&
-                  (!SPLIT || mbar_wait(&S.bar_stgfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs))))
-                S.fail = 1;
+            if (pt == 0 && run && c >= 1) {
+                bool ok;
+                if constexpr (PAIR)
+                    ok = mbar_wait(&S.bar_avakread[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs);
+                else
+                    ok = mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs) &&
+                         (!SPLIT || mbar_wait(&S.bar_stgfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs));
+                if (!ok) S.fail = 1;
+            }
             named_sync(kBarPrep, kPrepThreads);
-            if (c < 0) continue;
+            if (run) {
 
             // ---- P6: stacked operands AV = [P Tu ; Tu] and AK = [-P Tw ; Tw] (fp16, K-major).
             //      Rows 64..127 straight from T; rows 0..63 from P T by fp16 warp MMAs
@@ -893,6 +952,32 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                   mnmajor_desc(k_s, 128, k), id_m128_n128_mn, k > 0);
                 }
                 umma_commit(&S.bar_ready[s]);
+                if constexpr (PAIR) {
+                    // both CTAs learn when these MMAs have read AV / AK; the same operands go
+                    // to the peer's AV / AK (its MMA3 / MMA4 of chunk c - 1 have read them)
+                    umma_commit_mc(&S.bar_avakread[s], 0x3);
+                    const uint32_t peer = (uint32_t)(prank ^ 1);
+                    const uint32_t rbar = mapa_shared(smem_u32(&S.bar_recv), peer);
+                    mbar_remote_arrive_expect_tx(rbar, 2 * 16384);
+                    bulk_copy_to_peer(mapa_shared(smem_u32(AK), peer), AK, 2 * 16384, rbar);   // AK, AV adjacent
+                    S.sent += 1;
+                }
+            }
+            }   // run
+            if constexpr (PAIR) {
+                // MMA1 of the next chunk this CTA prepares, and its gates, into the slot of
+                // chunk c - 1 (which the serial warps have finished with once its RV was read)
+                if (issuer && cn < nchunks && !issue_mma1(cn)) S.fail = 1;
+                if (warp == kGateWarp && cn < nchunks) {
+                    bool ok = true;
+                    if (c >= 1 && lane == 0) ok = mbar_wait(&S.bar_rvfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) {
+                        if (lane == 0) S.fail = 1;
+                    } else {
+                        compute_gates(cn);
+                    }
+                }
             }
         }
     } else {
@@ -1078,8 +1163,42 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (st == 0) bulk_wait_all();   // the workspace is complete before the CTA leaves
         } else {
-        const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);   // MMA5
+        const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16);   // MMA5 (pair: and MMA3)
         const uint32_t id_m128_n64_amn = idesc_f16kind_f32(128, 64, 1, 1, kMmaF16);  // MMA6
+        const uint32_t id_m128_n128_mn = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16); // pair: MMA4
+        // Pair: chunk cc was prepared by the peer.  Its [P Tu ; Tu], [-P Tw ; Tw] arrive
+        // in AV / AK; this CTA's k and v tiles of the chunk become fp16 here (the prep
+        // warps convert only their own chunks' tiles); MMA3 / MMA4 follow as the prep
+        // warps would issue them, and their commit is the chunk's "ready".  RV / DK of
+        // this parity were last read by chunk cc - 2, finished before chunk cc - 1.
+        auto pair_service = [&](int cc) {
+            const int ls2 = cc % kStages, s2 = cc & 1;
+            uint8_t *QK2 = sm + LY::qk + ls2 * kQKBytes;
+            uint8_t *V2 = sm + LY::v + ls2 * LY::vbytes;
+            if (!mbar_wait(&S.bar_load[ls2], (cc / kStages) & 1, kWaitNs)) S.fail = 1;
+            tile_bf16_to_f16(QK2 + 8192, 8192, st, kSerialThreads);           // K, block 0
+            tile_bf16_to_f16(QK2 + 16384 + 8192, 8192, st, kSerialThreads);   // K, block 1
+            tile_bf16_to_f16(V2, kVBytes, st, kSerialThreads);
+            fence_proxy_async_smem();
+            named_sync(kBarSerial, kSerialThreads);
+            if (st == 0) {
+                if (mbar_wait(&S.bar_recv, (cc >> 1) & 1, kWaitNs))
+                    S.recvd += 1;
+                else
+                    S.fail = 1;
+                tc_fence_after();
+                const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(AK);
+                const uint32_t v2_s = smem_u32(V2), k2_s = smem_u32(QK2) + 8192;
+                for (int k = 0; k < kC / 16; ++k)
+                    umma_bf16(tbase + col_rv<SPLIT>(s2), kmajor_desc(av_s, 128, k), mnmajor_desc(v2_s, 64, k),
+                              id_m128_n64_mn, k > 0);
+                for (int k = 0; k < kC / 16; ++k)
+                    umma_bf16(tbase + col_dk<SPLIT>(s2), kmajor_desc(ak_s, 128, k), mnmajor_desc(k2_s, 128, k),
+                              id_m128_n128_mn, k > 0);
+                umma_commit(&S.bar_ready[s2]);
+                umma_commit_mc(&S.bar_avakread[s2], 0x3);
+            }
+        };
 
         float Hreg[kDVS];
         {
@@ -1094,6 +1213,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         fence_proxy_async_smem();
         named_sync(kBarSerial, kSerialThreads);
+        if (PAIR && prank == 1) pair_service(0);
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, t0 = (cb + c) * kC, L = min(kC, T - t0);
@@ -1121,7 +1241,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             {
                 const float er = top ? S.eg[gs][st] : 0.f;
                 const uint32_t dk_col = tbase + lane_base + col_dk<SPLIT>(s);
-#pragma unroll
+#pragma unroll 1   // (code size: both roles' loops must stay in the instruction cache)
                 for (int kb = 0; kb < 2; ++kb) {
                     const uint8_t *qblk = QK + kb * 16384;   // Q rows 0..63 of this column block
 #pragma unroll
@@ -1177,27 +1297,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // ---- S4: O -> global (bf16); U~ = Diag(e^{g_C - g}) U -> UB
             {
                 const int r = top ? st : st - 64;
+                float v[kDVS];   // the whole slice row in one TMEM round trip
 #pragma unroll
-                for (int n = 0; n < kDVS; n += 32) {
-                    float v[32];
-                    tmem_ld16(tbase + lane_base + col_rv<SPLIT>(s) + n, v);
-                    tmem_ld16(tbase + lane_base + col_rv<SPLIT>(s) + n + 16, v + 16);
-                    tmem_ld_wait();
-                    if (top) {
-                        if (r < L) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * H + h) * dv + n0 + n);
+                for (int q = 0; q < kDVS / 16; ++q) tmem_ld16(tbase + lane_base + col_rv<SPLIT>(s) + 16 * q, v + 16 * q);
+                tmem_ld_wait();
+                if (top) {
+                    if (r < L) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * H + h) * dv + n0);
 #pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4)
-                                dst[q4] = make_uint4(pack_bf2(v[8 * q4], v[8 * q4 + 1]), pack_bf2(v[8 * q4 + 2], v[8 * q4 + 3]),
-                                                     pack_bf2(v[8 * q4 + 4], v[8 * q4 + 5]),
-                                                     pack_bf2(v[8 * q4 + 6], v[8 * q4 + 7]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= egc;
-                        st_row16(UB, r, n, v);
-                        st_row16(UB, r, n + 16, v + 16);
+                        for (int q4 = 0; q4 < kDVS / 8; ++q4)
+                            dst[q4] = make_uint4(pack_bf2(v[8 * q4], v[8 * q4 + 1]), pack_bf2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                                                 pack_bf2(v[8 * q4 + 4], v[8 * q4 + 5]),
+                                                 pack_bf2(v[8 * q4 + 6], v[8 * q4 + 7]));
                     }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kDVS; ++i) v[i] *= egc;
+#pragma unroll
+                    for (int n = 0; n < kDVS; n += 16) st_row16(UB, r, n, v + n);
                 }
             }
             fence_proxy_async_smem();
@@ -1215,6 +1332,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                               id_m128_n64_amn, k > 0);
                 umma_commit(&S.bar_smma);
             }
+            // pair: the next chunk is the peer's -- its MMA3 / MMA4 go in while MMA6 runs
+            if (PAIR && c + 1 < nchunks && ((c + 1) & 1) != prank) pair_service(c + 1);
             if (!wait_smma()) break;
             if (kKda && st == 0) mbar_arrive(&S.bar_kbfree[c & 1]);
             // the tiles of chunk c are no longer read by anyone: fetch chunk c + stages into them
@@ -1224,19 +1343,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float gCr = kKda ? S.egC[gs][st] : gC;   // KDA: decay of key channel st
             // KDA: the side tile holds K e^{m-G} = K~ Diag(e^{m-G_C}) per channel, row st of D6
             const float d6s = kKda ? S.egcm[gs][st] : 1.f;
+            {
+                float v[kDVS];
 #pragma unroll
-            for (int n = 0; n < kDVS; n += 32) {
-                float v[32];
-                tmem_ld16(tbase + lane_base + kColD6 + n, v);
-                tmem_ld16(tbase + lane_base + kColD6 + n + 16, v + 16);
+                for (int q = 0; q < kDVS / 16; ++q) tmem_ld16(tbase + lane_base + kColD6 + 16 * q, v + 16 * q);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    Hreg[n + i] = gCr * Hreg[n + i] + d6s * v[i];
-                    v[i] = Hreg[n + i];
+                for (int i = 0; i < kDVS; ++i) {
+                    Hreg[i] = gCr * Hreg[i] + d6s * v[i];
+                    v[i] = Hreg[i];
                 }
-                st_row16(HB, st, n, v);
-                st_row16(HB, st, n + 16, v + 16);
+#pragma unroll
+                for (int n = 0; n < kDVS; n += 16) st_row16(HB, st, n, v + n);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1268,6 +1386,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int ls = 0; ls < kStages; ++ls)
                 if (pending[ls] >= 0) mbar_wait(&S.bar_load[ls], (pending[ls] / kStages) & 1, kWaitNs / 4);
     }
+    if constexpr (PAIR) {
+        // Nothing of the peer may still be on its way here when this CTA leaves.  Each
+        // MMA issuer of both CTAs ends with a commit that arrives in both: the commits of
+        // an issuer arrive in order, so once all four have, so have the earlier ones on
+        // bar_avakread.  Then, after a failure, an operand transfer the peer issued that
+        // was never waited for.
+        if (tid == kIssuer || tid == kPrepThreads) umma_commit_mc(&S.bar_fin, 0x3);
+        if (tid == 0 && !mbar_wait(&S.bar_fin, 0, S.fail ? kWaitNs / 4 : kWaitNs) && !S.fail) {
+            S.fail = 1;
+            atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        }
+        __syncthreads();
+        cluster_sync();
+        if (tid == 0) {
+            const uint32_t peer_sent = ld_shared_cluster_u32(mapa_shared(smem_u32(&S.sent), (uint32_t)(prank ^ 1)));
+            if (peer_sent > S.recvd) mbar_wait(&S.bar_recv, S.recvd & 1, kWaitNs / 4);
+        }
+        __syncthreads();
+        cluster_sync();   // the peer has read this CTA's counter
+    }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
@@ -1293,9 +1431,10 @@ int sm_count()
     return sms[dev];
 }
 
-template <bool SPLIT>
+template <int KIND>
 cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 {
+    constexpr bool SPLIT = KIND == kSplit, PAIR = KIND == kPair;
     CUtensorMap tq, tk, tv;
     if (!make_tmap_bf16_4d(&tq, a.q, kDK, a.H, a.T, a.B, 64, kC) ||
         !make_tmap_bf16_4d(&tk, a.k, kDK, a.H, a.T, a.B, 64, kC) ||
@@ -1316,45 +1455,80 @@ cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
     auto go = [&](auto kern, uint32_t smem) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        if (PAIR) {   // clusters of the two dv slices of a (b, h): consecutive blocks
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)grid);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
+                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr);
+        }
         kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
                                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr);
         return cudaGetLastError();
     };
-    if (a.mode == LDN_GDN) return go(chunk_tc_kernel<LDN_GDN, SPLIT>, Layout<LDN_GDN, SPLIT>::bytes);
-    if (a.mode == LDN_KDA) return go(chunk_tc_kernel<LDN_KDA, SPLIT>, Layout<LDN_KDA, SPLIT>::bytes);
-    return go(chunk_tc_kernel<LDN_DELTANET, SPLIT>, Layout<LDN_DELTANET, SPLIT>::bytes);
+    if (a.mode == LDN_GDN) return go(chunk_tc_kernel<LDN_GDN, KIND>, Layout<LDN_GDN, SPLIT>::bytes);
+    if constexpr (!PAIR)
+        if (a.mode == LDN_KDA) return go(chunk_tc_kernel<LDN_KDA, KIND>, Layout<LDN_KDA, SPLIT>::bytes);
+    return go(chunk_tc_kernel<LDN_DELTANET, KIND>, Layout<LDN_DELTANET, SPLIT>::bytes);
 }
 }  // namespace
 
-cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) { return launch_tc<false>(a, nullptr, st); }
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) { return launch_tc<kFused>(a, nullptr, st); }
 
-// Which tensor-core variant is expected to be faster: a cost model in waves of
-// CTAs (one CTA per SM) x chunks per CTA x measured time per chunk on GB300 --
-// fused 4.0 us (GDN / DeltaNet) or 7.9 us (KDA); split preparation 5.4 / 10.8 us
-// and state step 1.6 us -- plus a fixed 10 us (one launch) or 20 us (two
-// launches and the preparation pipeline's fill).  The fused kernel wins when its
-// CTAs fill the SMs once; the split variant when they do not (few sequences) or
-// need several waves (its preparation and state steps are cheaper per chunk).
-bool chunk_split_preferred(const ChunkArgs &a)
+bool chunk_pair_supported(const ChunkArgs &a)
 {
+    return chunk_tc_supported(a) && a.mode != LDN_KDA && a.dv == 2 * kDVS;
+}
+
+cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t st) { return launch_tc<kPair>(a, nullptr, st); }
+
+// Which tensor-core variant is expected to be fastest: a cost model in waves of
+// CTAs (one CTA per SM) x chunks per CTA x measured time per chunk on GB300 --
+// fused 4.0 us (GDN / DeltaNet) or 7.9 us (KDA); pair 5.0 us (measured: each
+// CTA's preparation waits for tiles that a third ring stage frees only late, and
+// runs slower beside the busier serial warps); split preparation 5.4 /
+// 10.8 us and state step 1.6 us -- plus a fixed 10 us (one launch) or 20 us (two
+// launches and the preparation pipeline's fill).  The fused and pair kernels win
+// when their CTAs fill the SMs once; the split variant when they do not (few
+// sequences) or need several waves.
+int chunk_tc_pick(const ChunkArgs &a, bool split_ok)
+{
+    const bool pair_ok = chunk_pair_supported(a);
     const int sms = sm_count();
-    if (sms <= 0) return false;
+    if (sms <= 0) return pair_ok ? LDN_VARIANT_PAIR : LDN_VARIANT_TENSOR;
     const bool kda = a.mode == LDN_KDA;
-    const double t_fused = kda ? 7.9 : 4.0, t_prep = kda ? 10.8 : 5.4, t_state = 1.6;
+    const double t_fused = kda ? 7.9 : 4.0, t_pair = 5.0, t_prep = kda ? 10.8 : 5.4, t_state = 1.6;
     const long long heads = (long long)a.B * a.H, nchunks = (a.T + kC - 1) / kC;
     const long long slices = heads * (a.dv / kDVS);
     const long long waves_f = (slices + sms - 1) / sms;
     const long long nranges = std::max(1LL, std::min(nchunks, sms / heads));
     const long long cpr = (nchunks + nranges - 1) / nranges;
     const long long waves_p = (heads * ((nchunks + cpr - 1) / cpr) + sms - 1) / sms;
-    const double fused = 10.0 + (double)waves_f * nchunks * t_fused;
-    const double split = 20.0 + (double)waves_p * cpr * t_prep + (double)waves_f * nchunks * t_state;
-    return split < fused;
+    int best = LDN_VARIANT_TENSOR;
+    double cost = 10.0 + (double)waves_f * nchunks * t_fused;
+    if (pair_ok) {
+        const double pair = 10.0 + (double)waves_f * nchunks * t_pair;
+        if (pair < cost) { cost = pair; best = LDN_VARIANT_PAIR; }
+    }
+    if (split_ok) {
+        const double split = 20.0 + (double)waves_p * cpr * t_prep + (double)waves_f * nchunks * t_state;
+        if (split < cost) { cost = split; best = LDN_VARIANT_SPLIT; }
+    }
+    return best;
 }
 
 cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 {
-    cudaError_t e = launch_tc<true>(a, ws, st);
+    cudaError_t e = launch_tc<kSplit>(a, ws, st);
     if (e != cudaSuccess) return e;
     return launch_chunk_state(a, ws, st);
 }

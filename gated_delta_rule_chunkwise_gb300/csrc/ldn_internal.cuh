@@ -47,7 +47,9 @@ bool chunk_tc_supported(const ChunkArgs &a);
 // Split variant: preparation kernel (chunk_tc.cu) then state kernel (chunk_state.cu).
 cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
 cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream_t stream);
-bool chunk_split_preferred(const ChunkArgs &a);   // expected faster than the fused kernel
+int chunk_tc_pick(const ChunkArgs &a, bool split_ok);   // fastest tensor-core LDN_VARIANT_* by a cost model
+bool chunk_pair_supported(const ChunkArgs &a);    // the cluster-pair kernel takes these arguments
+cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 int *status_word_ptr();   // address of the device status word on the current device
 // Library-owned split-variant scratch of ldn_chunk_fwd_noalloc (static_scratch.cu).

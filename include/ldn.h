@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define LDN_VERSION 2
+#define LDN_VERSION 3
 
 typedef enum { LDN_DELTANET = 0, LDN_GDN = 1, LDN_KDA = 2 } ldn_mode;
 
@@ -68,7 +68,8 @@ typedef enum {
     LDN_VARIANT_AUTO = 0,   /* bf16 -> tensor-core kernel, fp32 -> fp32 SIMT kernel */
     LDN_VARIANT_SIMT = 1,   /* fp32 CUDA-core kernel, either dtype                 */
     LDN_VARIANT_TENSOR = 2, /* tcgen05 / TMEM kernel, bf16 only                     */
-    LDN_VARIANT_SPLIT = 3   /* tcgen05, two kernels through a workspace (see below) */
+    LDN_VARIANT_SPLIT = 3,  /* tcgen05, two kernels through a workspace (see below) */
+    LDN_VARIANT_PAIR = 4    /* tcgen05, two CTAs per (b, h) sharing the preparation */
 } ldn_variant;
 
 /*
@@ -103,16 +104,24 @@ int ldn_chunk_fwd(const void *q, const void *k, const void *v, const float *beta
 /* Same as ldn_chunk_fwd with an explicit kernel family (ldn_variant).
  * The tensor-core kernel takes bf16 inputs with dk = 128, dv a multiple of 64,
  * chunk = 64, any mode; for KDA it also needs a 16-byte aligned gate tensor.
- * LDN_VARIANT_TENSOR outside these returns LDN_ERR_UNSUPPORTED. */
+ * LDN_VARIANT_TENSOR outside these returns LDN_ERR_UNSUPPORTED.
+ * LDN_VARIANT_PAIR is the same computation for DeltaNet and Gated DeltaNet with
+ * dv = 128: the two 64-column halves of dv of each (b, h) run as a cluster of
+ * two thread blocks that split the state-independent part of every chunk
+ * between them (each prepares every other chunk and hands its operands to the
+ * other through distributed shared memory); its results are bit-identical to
+ * LDN_VARIANT_TENSOR.  Outside those sizes it returns LDN_ERR_UNSUPPORTED.
+ * LDN_VARIANT_AUTO takes the tensor-core kernel (fused or pair, by a cost model
+ * in the same units as ldn_chunk_fwd_ws's) whenever one supports the call. */
 int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v, const float *beta,
                           const float *gate, const float *S0, void *out, float *S_final,
                           int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
                           int variant, void *stream);
 
 /* Which kernel family LDN_VARIANT_AUTO runs for these sizes (for KDA, given a
- * 16-byte aligned gate tensor): returns LDN_VARIANT_SIMT or LDN_VARIANT_TENSOR,
- * or -LDN_ERR_* for arguments that ldn_chunk_fwd would reject.  Pure host
- * function: touches no device. */
+ * 16-byte aligned gate tensor): returns LDN_VARIANT_SIMT or LDN_VARIANT_TENSOR
+ * (the tensor-core family: fused or pair kernel), or -LDN_ERR_* for arguments
+ * that ldn_chunk_fwd would reject.  Pure host function: touches no device. */
 int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype);
 
 /*
@@ -141,8 +150,8 @@ size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chu
  * on return are unspecified).  LDN_VARIANT_SPLIT without a large enough
  * workspace returns LDN_ERR_INVALID_ARG; LDN_VARIANT_AUTO takes the split
  * variant when it supports the call, the workspace suffices and a cost model of
- * the two tensor-core variants (CTA waves x chunks x measured per-chunk times)
- * expects it to be faster -- typically when B*H*dv/64 leaves SMs idle or needs
+ * the tensor-core variants (CTA waves x chunks x measured per-chunk times)
+ * expects it to be fastest -- typically when B*H*dv/64 leaves SMs idle or needs
  * several waves -- and otherwise behaves as ldn_chunk_fwd_variant(...,
  * LDN_VARIANT_AUTO, ...).  Calls on different streams need different workspaces.
  */
@@ -153,7 +162,7 @@ int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *b
 
 /* Which kernel family ldn_chunk_fwd_ws(..., LDN_VARIANT_AUTO, ...) runs for these
  * sizes and a workspace of workspace_bytes (pointers assumed aligned): returns
- * LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR or LDN_VARIANT_SPLIT, or -LDN_ERR_* for
+ * LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR, LDN_VARIANT_PAIR or LDN_VARIANT_SPLIT, or -LDN_ERR_* for
  * arguments that would be rejected.  Host function; it reads the SM count of
  * the current device. */
 int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
@@ -181,7 +190,7 @@ int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int 
  * unlimited workspace would, otherwise the fused tensor-core or the SIMT
  * kernel; LDN_VARIANT_SPLIT returns LDN_ERR_UNSUPPORTED when the call cannot
  * be cut to fit (H so large that one chunk of all heads exceeds the array).
- * LDN_VARIANT_SIMT and LDN_VARIANT_TENSOR touch no scratch.
+ * LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR and LDN_VARIANT_PAIR touch no scratch.
  *
  * Calls share the array: calls on different streams are ordered on the
  * device by an event the library records after each call (a host lock covers

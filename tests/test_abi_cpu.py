@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert ldn.ldn_version() == 2
+    assert ldn.ldn_version() == 3
     for st in range(5):
         assert isinstance(ldn.ldn_status_string(st), str) and ldn.ldn_status_string(st)
     assert "unknown" in ldn.ldn_status_string(99)
@@ -181,4 +181,13 @@ def test_noalloc_split_outside_the_tensor_kernels_is_unsupported(lib):
     assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=64) == ldn.LDN_ERR_UNSUPPORTED   # dk = 64
     assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=128, dtype=0) == ldn.LDN_ERR_UNSUPPORTED   # fp32
     assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=128, mode=2, gate=FAKE + 4) == ldn.LDN_ERR_UNSUPPORTED
-    assert _noalloc(variant=4) == ldn.LDN_ERR_INVALID_ARG
+    assert _noalloc(variant=5) == ldn.LDN_ERR_INVALID_ARG
+
+
+def test_pair_variant_outside_its_sizes_is_unsupported(lib):
+    """The cluster-pair kernel takes DeltaNet / Gated DeltaNet, bf16, dk = dv = 128."""
+    assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=128, dv=128, mode=2) == ldn.LDN_ERR_UNSUPPORTED   # KDA
+    assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=128, dv=64) == ldn.LDN_ERR_UNSUPPORTED            # one slice
+    assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=64, dv=128) == ldn.LDN_ERR_UNSUPPORTED
+    assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=128, dv=128, dtype=0) == ldn.LDN_ERR_UNSUPPORTED  # fp32
+    assert _chunk(variant=5) == ldn.LDN_ERR_INVALID_ARG

@@ -200,6 +200,33 @@ def test_split_equals_fused_up_to_rounding():
     assert ulp_excess < 1e-2 and rel_err(s2, s1) < 1e-2
 
 
+# ---- cluster-pair variant (two CTAs per (b, h) share the preparation) ----
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("B,T,H,s0", [(1, 64, 1, False), (2, 65, 3, True), (1, 1, 2, True), (2, 500, 4, True),
+                                      (1, 1000, 2, False), (3, 128, 5, True)])
+def test_pair_variant_parity(mode, B, T, H, s0):
+    w = wl.make_chunk(BASE[mode], dtype="bf16", B=B, T=T, H=H, dk=128, dv=128, s0=s0)
+    check(w, ldn.LDN_VARIANT_PAIR)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_pair_equals_fused_bitwise(mode):
+    """The pair's CTAs compute every chunk's operands with the fused kernel's arithmetic
+    (the peer's copy is the same bits), so the results are identical."""
+    w = wl.make_chunk(BASE[mode], dtype="bf16", B=2, T=777, H=3, dk=128, dv=128, s0=True)
+    o1, s1 = run_gpu(w, ldn.LDN_VARIANT_TENSOR)
+    o2, s2 = run_gpu(w, ldn.LDN_VARIANT_PAIR)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+def test_pair_strong_gates_entrywise_chunks():
+    """Gated DeltaNet chunks whose log-decay span exceeds the factored form, in both CTAs'
+    chunks (even and odd)."""
+    w = wl.make_chunk(BASE[1], B=1, T=256, H=2, s0=True)
+    w.gate = (w.gate * 40.0).astype(np.float32)
+    check(w, ldn.LDN_VARIANT_PAIR)
+
+
 # ---- full-size workloads in the benchmark's launch configuration, sampled ----
 def _sampled(name, picks, variant=ldn.LDN_VARIANT_AUTO, **over):
     import torch
@@ -235,3 +262,9 @@ def test_full_gdn_long_t65536_sampled():
                                         ("gdn_bf16_long_b1_t65536_h16_d128", [(0, 5)])])
 def test_full_workloads_split_variant_sampled(name, picks):
     _sampled(name, picks, ldn.LDN_VARIANT_SPLIT)
+
+
+@pytest.mark.parametrize("name,picks", [("gdn_bf16_b4_t2048_h16_d128", [(0, 0), (2, 9), (3, 15)]),
+                                        ("gdn_bf16_long_b1_t8192_h16_d128", [(0, 5)])])
+def test_full_workloads_pair_variant_sampled(name, picks):
+    _sampled(name, picks, ldn.LDN_VARIANT_PAIR)
