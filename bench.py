@@ -36,6 +36,7 @@ METRIC = "tokens/s chunkwise GDN fwd (H=16,dk=dv=128) + % roofline; decode GB/s"
 WORKLOAD = "gdn_bf16_b4_t2048_h16_d128"
 EXTRA_WORKLOADS = ("kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
                    "gdn_bf16_long_b1_t65536_h16_d128", "deltanet_fp32_b1_t256_h1_d64")
+PROLOGUE_WORKLOADS = ("gdn_prologue_bf16_b4_t2048_h16_d128_w4", "kda_prologue_bf16_b8_t4096_h16_d128_w4")
 DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000")
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
@@ -60,6 +61,24 @@ def chunk_flops(B, T, H, dk, dv, C=64):
     """Algorithmic flops of the chunk form per token-head, causal halves counted
     once: 6 dk dv (state read/write products) + C (3 dk + 2 dv) + C^2 / 3."""
     return B * T * H * (6 * dk * dv + C * (3 * dk + 2 * dv) + C * C / 3)
+
+
+def el_bytes_of(dtype):
+    return 2 if dtype == "bf16" else 4
+
+
+def prologue_bytes(B, T, H, dk, dv, el_bytes, mode, width):
+    """Algorithmic bytes of ldn_prologue: q, k, v read and written once, beta logit
+    and beta, the gate input and output, the convolution weights."""
+    n = B * T * H
+    qkv = 2 * n * (2 * dk + dv) * el_bytes
+    gate = 0 if mode == 0 else 2 * n * 4 * (dk if mode == 2 else 1)
+    return qkv + 2 * n * 4 + gate + 4 * H * (2 * dk + dv) * width
+
+
+def rmsnorm_bytes(B, T, H, dv, el_bytes):
+    """Algorithmic bytes of ldn_rmsnorm_gated: o and the gate read, y written."""
+    return 3 * B * T * H * dv * el_bytes + 4 * dv
 
 
 def decode_bytes(B, H, dk, dv, mode):
@@ -415,6 +434,62 @@ def run_ours(args):
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("other workloads: device status not ok")
 
+    # ---------------- prologue and epilogue around the path (bandwidth) ----------------
+    around = None
+    if not args.no_extra:
+        around = {}
+        for name in PROLOGUE_WORKLOADS:
+            p = wl.make_prologue(name, seed=rank)
+            el = torch.bfloat16 if p["dtype"] == "bf16" else torch.float32
+            dev = lambda x, dt=torch.float32: None if x is None else torch.from_numpy(x).to("cuda", dt)
+            pi = {k_: dev(p[k_], el) for k_ in ("q_in", "k_in", "v_in", "o", "g")}
+            pf = {k_: dev(p[k_]) for k_ in ("conv_q", "conv_k", "conv_v", "beta_logit", "gate_z", "gate_a", "gate_b", "gain")}
+            B_, T_, H_, dk_, dv_ = p["B"], p["T"], p["H"], p["dk"], p["dv"]
+            qo = torch.empty((B_, T_, H_, dk_), dtype=el, device="cuda")
+            ko, vo = torch.empty_like(qo), torch.empty((B_, T_, H_, dv_), dtype=el, device="cuda")
+            bo = torch.empty((B_, T_, H_), dtype=torch.float32, device="cuda")
+            go_ = torch.empty(tuple(p["gate_z"].shape), dtype=torch.float32, device="cuda")
+            yo = torch.empty_like(pi["o"])
+            dt_ = ldn.LDN_BF16 if p["dtype"] == "bf16" else ldn.LDN_F32
+            P_ = lambda x: 0 if x is None else x.data_ptr()
+
+            def pro():
+                st_ = ldn.ldn_prologue(P_(pi["q_in"]), P_(pi["k_in"]), P_(pi["v_in"]), P_(pf["conv_q"]),
+                                       P_(pf["conv_k"]), P_(pf["conv_v"]), p["width"], P_(pf["beta_logit"]),
+                                       P_(pf["gate_z"]), P_(pf["gate_a"]), P_(pf["gate_b"]), P_(qo), P_(ko), P_(vo),
+                                       P_(bo), P_(go_), B_, T_, H_, dk_, dv_, p["mode"], dt_, 1e-6, sh)
+                if st_ != ldn.LDN_OK:
+                    raise ldn.LdnError(st_, "ldn_prologue")
+
+            def epi():
+                st_ = ldn.ldn_rmsnorm_gated(P_(pi["o"]), P_(pi["g"]), P_(pf["gain"]), P_(yo), B_, T_, H_, dv_, dt_,
+                                            1e-6, sh)
+                if st_ != ldn.LDN_OK:
+                    raise ldn.LdnError(st_, "ldn_rmsnorm_gated")
+
+            res = {}
+            for what, fn, nb_, nl in (("prologue", pro, prologue_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(p["dtype"]),
+                                                                       p["mode"], p["width"]), 2 if dk_ == dv_ else 3),
+                                      ("rmsnorm_gated", epi, rmsnorm_bytes(B_, T_, H_, dv_, el_bytes_of(p["dtype"])), 1)):
+                for _ in range(3):
+                    fn()
+                barrier()
+                evs_ = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+                for e0, e1 in evs_:
+                    flush_l2()
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                barrier()
+                ms_ = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs_))
+                launches += nl * (3 + len(evs_))
+                res[what] = {"us_per_call": ms_ * 1e3, "algorithmic_bytes": nb_, "GB/s": nb_ / (ms_ / 1e3) / 1e9,
+                             "frac_hbm": nb_ / (ms_ / 1e3) / 1e9 / hbm_peak, "launches_per_call": nl}
+            around[name] = res
+            del pi, pf, qo, ko, vo, bo, go_, yo
+        if ldn.device_status() != ldn.LDN_OK:
+            raise RuntimeError("prologue / epilogue: device status not ok")
+
     # ---------------- decode step (bandwidth) ----------------
     decode = None
     if not args.no_decode:
@@ -478,7 +553,7 @@ def run_ours(args):
                        "l2": "flushed before every timed launch (512 MiB write, then 512 MiB read of another buffer: cold and clean)",
                        "parallelism": f"replica x{world} (independent sequences per GPU)"},
             "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
-            "other_workloads": others,
+            "other_workloads": others, "prologue_epilogue": around,
             "wall_s_timed_region": wall, "decode": decode}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)

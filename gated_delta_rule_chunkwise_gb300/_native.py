@@ -7,6 +7,7 @@ been built, or no GPU is present, the calls raise.
 Two layers:
   * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
     ``ldn_chunk_fwd_workspace_size``, ``ldn_chunk_fwd_noalloc``, ``ldn_decode_step``,
+    ``ldn_prologue``, ``ldn_rmsnorm_gated``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
   * ``chunk_fwd`` and ``decode_step``: the same calls on torch CUDA tensors,
@@ -52,6 +53,8 @@ _SIGNATURES = {
     "ldn_chunk_fwd_select_ws": ([_I] * 8 + [ctypes.c_size_t], _I),
     "ldn_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 9 + [_P], _I),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
+    "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
+    "ldn_rmsnorm_gated": ([_P] * 4 + [_I] * 5 + [ctypes.c_float, _P], _I),
     "ldn_get_device_status": ([_P], _I),
     "ldn_status_string": ([_I], ctypes.c_char_p),
     "ldn_version": ([], _I),
@@ -119,6 +122,16 @@ def ldn_chunk_fwd_noalloc(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv
 
 def ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream):
     return load().ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream)
+
+
+def ldn_prologue(q_in, k_in, v_in, conv_q, conv_k, conv_v, width, beta_logit, gate_z, gate_a, gate_b,
+                 q, k, v, beta, gate, B, T, H, dk, dv, mode, dtype, eps, stream):
+    return load().ldn_prologue(q_in, k_in, v_in, conv_q, conv_k, conv_v, width, beta_logit, gate_z, gate_a, gate_b,
+                               q, k, v, beta, gate, B, T, H, dk, dv, mode, dtype, eps, stream)
+
+
+def ldn_rmsnorm_gated(o, g, weight, y, B, T, H, dv, dtype, eps, stream):
+    return load().ldn_rmsnorm_gated(o, g, weight, y, B, T, H, dv, dtype, eps, stream)
 
 
 def ldn_get_device_status(stream):

@@ -301,6 +301,78 @@ extern "C" int ldn_decode_step(const void *q, const void *k, const void *v, cons
     return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+extern "C" int ldn_prologue(const void *q_in, const void *k_in, const void *v_in, const float *conv_q,
+                            const float *conv_k, const float *conv_v, int width, const float *beta_logit,
+                            const float *gate_z, const float *gate_a, const float *gate_b, void *q, void *k,
+                            void *v, float *beta, float *gate, int B, int T, int H, int dk, int dv, int mode,
+                            int dtype, float eps, void *stream)
+{
+    const int st = validate_common(mode, dtype, dk, dv);
+    if (st != LDN_OK) return st;
+    if (B < 1 || H < 1 || T < 0 || !(eps >= 0.f) || eps > 1e30f) return LDN_ERR_INVALID_ARG;
+    if (width < 1) return LDN_ERR_INVALID_ARG;
+    if (width > 8) return LDN_ERR_UNSUPPORTED;
+    if ((long long)B * T * H * (dk > dv ? dk : dv) > (1LL << 40)) return LDN_ERR_UNSUPPORTED;
+    if (T == 0) return LDN_OK;
+    const bool gated = mode != LDN_DELTANET;
+    const void *must[] = {q_in, k_in, v_in, conv_q, conv_k, conv_v, beta_logit, q, k, v, beta};
+    for (const void *p : must)
+        if (!p) return LDN_ERR_INVALID_ARG;
+    if (gated && (!gate_z || !gate_a || !gate_b || !gate)) return LDN_ERR_INVALID_ARG;
+    const void *vec[] = {q_in, k_in, v_in, q, k, v};   // 16-byte rows
+    for (const void *p : vec)
+        if (!aligned16(p)) return LDN_ERR_INVALID_ARG;
+    const void *f4[] = {conv_q, conv_k, conv_v, beta_logit, beta};
+    for (const void *p : f4)
+        if (!aligned(p, 4)) return LDN_ERR_INVALID_ARG;
+    if (gated) {
+        const bool kda = mode == LDN_KDA;   // per-channel gates move as float4
+        for (const void *p : {(const void *)gate_z, (const void *)gate_b, (const void *)gate})
+            if (!aligned(p, kda ? 16 : 4)) return LDN_ERR_INVALID_ARG;
+        if (!aligned(gate_a, 4)) return LDN_ERR_INVALID_ARG;
+    }
+    const size_t el = dtype == LDN_BF16 ? 2 : 4, ntok = (size_t)B * T * H;
+    const size_t nk = ntok * dk * el, nv = ntok * dv * el, nb = ntok * 4, ng = gated ? ntok * 4 * (mode == LDN_KDA ? dk : 1) : 0;
+    const void *ins[] = {q_in, k_in, v_in, beta_logit, gated ? gate_z : nullptr};
+    const size_t nins[] = {nk, nk, nv, nb, ng};
+    const void *outs[] = {q, k, v, beta, gated ? gate : nullptr};
+    const size_t nouts[] = {nk, nk, nv, nb, ng};
+    for (int i = 0; i < 5; ++i)
+        for (int j = 0; j < 5; ++j)
+            if (overlaps(ins[i], nins[i], outs[j], nouts[j])) return LDN_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
+        for (int j = i + 1; j < 5; ++j)
+            if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return LDN_ERR_INVALID_ARG;
+    PrologueArgs a{q_in, k_in, v_in, conv_q, conv_k, conv_v, beta_logit, gated ? gate_z : nullptr,
+                   gated ? gate_a : nullptr, gated ? gate_b : nullptr, q, k, v, beta, gated ? gate : nullptr,
+                   B, T, H, dk, dv, width, mode, dtype, eps};
+    return launch_prologue(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
+extern "C" int ldn_rmsnorm_gated(const void *o, const void *g, const float *weight, void *y, int B, int T, int H,
+                                 int dv, int dtype, float eps, void *stream)
+{
+    if (dtype != LDN_F32 && dtype != LDN_BF16) return LDN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 0 || dv < 1 || !(eps >= 0.f) || eps > 1e30f) return LDN_ERR_INVALID_ARG;
+    if (!supported_dim(dv)) return LDN_ERR_UNSUPPORTED;
+    if ((long long)B * T * H * dv > (1LL << 40)) return LDN_ERR_UNSUPPORTED;
+    if (T == 0) return LDN_OK;
+    if (!o || !g || !weight || !y) return LDN_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(g) || !aligned16(y) || !aligned(weight, 4)) return LDN_ERR_INVALID_ARG;
+    const size_t n = (size_t)B * T * H * dv * (dtype == LDN_BF16 ? 2 : 4);
+    if (overlaps(g, n, y, n)) return LDN_ERR_INVALID_ARG;   // y may replace o, not g
+    if (o != y && overlaps(o, n, y, n)) return LDN_ERR_INVALID_ARG;
+    RmsNormArgs a{o, g, weight, y, B, T, H, dv, dtype, eps};
+    return launch_rmsnorm_gated(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
 extern "C" int ldn_get_device_status(void *stream)
 {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LDN_ERR_CUDA;

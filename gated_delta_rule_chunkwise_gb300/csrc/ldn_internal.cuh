@@ -31,6 +31,25 @@ struct DecodeArgs {
     int *status;
 };
 
+// Prologue / epilogue around the chunkwise path (prologue.cu).
+struct PrologueArgs {
+    const void *q_in, *k_in, *v_in;
+    const float *conv_q, *conv_k, *conv_v;
+    const float *beta_logit, *gate_z, *gate_a, *gate_b;
+    void *q, *k, *v;
+    float *beta, *gate;
+    int B, T, H, dk, dv, width, mode, dtype;
+    float eps;
+};
+
+struct RmsNormArgs {
+    const void *o, *g;
+    const float *weight;
+    void *y;
+    int B, T, H, dv, dtype;
+    float eps;
+};
+
 // Split variant: workspace bytes per (b, h, chunk) -- [Q~ ; -W] (32 KiB), [P U' ; U']
 // per 64-column slice of dv (16 KiB each), K~ (16 KiB), e^{g_C} per key channel
 // (512 B); layout described in include/ldn.h.
@@ -51,6 +70,8 @@ int chunk_tc_pick(const ChunkArgs &a, bool split_ok);   // fastest tensor-core L
 bool chunk_pair_supported(const ChunkArgs &a);    // the cluster-pair kernel takes these arguments
 cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream);
+cudaError_t launch_rmsnorm_gated(const RmsNormArgs &a, cudaStream_t stream);
 int *status_word_ptr();   // address of the device status word on the current device
 // Library-owned split-variant scratch of ldn_chunk_fwd_noalloc (static_scratch.cu).
 // acquire() locks the current device's scratch and orders `s` after its previous

@@ -134,3 +134,51 @@ def make_decode(name: str = "gdn_decode_b64_h16_dk128_dv128_steps1000", seed: in
                                     r["dv"], True, r["B"])
     return Workload(name=name, mode=r["mode"], dtype=r["dtype"], B=r["B"], T=r["steps"], H=r["H"],
                     dk=r["dk"], dv=r["dv"], q=q, k=k, v=v, beta=beta, gate=gate, S0=S0, decode=True)
+
+
+# ---- prologue / epilogue inputs ------------------------------------------------
+# Recipe: numpy Generator(PCG64(seed)), draws in this order: q_in, k_in, v_in
+# ~ N(0, 1) (projection outputs); conv weights ~ N(0, 1/W) per (channel, tap)
+# for q, k, v; beta logits ~ N(0, 1); gate noise z ~ N(0, 1) per (b, t, h)
+# (Gated DeltaNet) or (b, t, h, c) (KDA); a_h = exp(N(0, 0.5^2)) > 0 per head;
+# bias b ~ N(0, 0.5^2) per head (GDN) or per head and key channel (KDA); then the
+# epilogue's output o ~ N(0, 1), output gate g ~ N(0, 1) and gain ~ 1 + N(0, 0.1^2)
+# per value channel.  For bf16 the q/k/v inputs, o and g are rounded to bf16.
+
+PROLOGUE_WORKLOADS = {
+    "gdn_prologue_bf16_b4_t2048_h16_d128_w4": dict(mode=MODE_GDN, dtype="bf16", B=4, T=2048, H=16, dk=128, dv=128, width=4),
+    "kda_prologue_bf16_b8_t4096_h16_d128_w4": dict(mode=MODE_KDA, dtype="bf16", B=8, T=4096, H=16, dk=128, dv=128, width=4),
+}
+
+
+def make_prologue(name: str = "gdn_prologue_bf16_b4_t2048_h16_d128_w4", seed: int = 0, **over) -> dict:
+    """Inputs of ldn_prologue and ldn_rmsnorm_gated as float32 numpy arrays (bf16
+    values exact in fp32), plus the sizes."""
+    r = dict(PROLOGUE_WORKLOADS[name]); r.update(over)
+    B, T, H, dk, dv, W, mode = r["B"], r["T"], r["H"], r["dk"], r["dv"], r["width"], r["mode"]
+    rng = np.random.default_rng(seed)
+    f32 = np.float32
+    qi = rng.standard_normal((B, T, H, dk), dtype=f32)
+    ki = rng.standard_normal((B, T, H, dk), dtype=f32)
+    vi = rng.standard_normal((B, T, H, dv), dtype=f32)
+    sc = f32(1.0 / np.sqrt(W))
+    cq = (rng.standard_normal((H * dk, W), dtype=f32) * sc).astype(f32)
+    ck = (rng.standard_normal((H * dk, W), dtype=f32) * sc).astype(f32)
+    cv = (rng.standard_normal((H * dv, W), dtype=f32) * sc).astype(f32)
+    bl = rng.standard_normal((B, T, H), dtype=f32)
+    gz = ga = gb = None
+    if mode == MODE_GDN:
+        gz = rng.standard_normal((B, T, H), dtype=f32)
+        ga = np.exp(rng.standard_normal(H, dtype=f32) * f32(0.5)).astype(f32)
+        gb = (rng.standard_normal(H, dtype=f32) * f32(0.5)).astype(f32)
+    elif mode == MODE_KDA:
+        gz = rng.standard_normal((B, T, H, dk), dtype=f32)
+        ga = np.exp(rng.standard_normal(H, dtype=f32) * f32(0.5)).astype(f32)
+        gb = (rng.standard_normal((H, dk), dtype=f32) * f32(0.5)).astype(f32)
+    o = rng.standard_normal((B, T, H, dv), dtype=f32)
+    g = rng.standard_normal((B, T, H, dv), dtype=f32)
+    gain = (1.0 + rng.standard_normal(dv, dtype=f32) * f32(0.1)).astype(f32)
+    if r["dtype"] == "bf16":
+        qi, ki, vi, o, g = round_bf16(qi), round_bf16(ki), round_bf16(vi), round_bf16(o), round_bf16(g)
+    return dict(r, name=name, q_in=qi, k_in=ki, v_in=vi, conv_q=cq, conv_k=ck, conv_v=cv, beta_logit=bl,
+                gate_z=gz, gate_a=ga, gate_b=gb, o=o, g=g, gain=gain)

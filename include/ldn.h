@@ -204,6 +204,48 @@ int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
                           int variant, void *stream);
 
 /*
+ * ldn_prologue -- the input steps before the chunkwise forward (the model-zoo
+ * page's DeltaNet, KDA and Gated DeltaNet entries; the Residual Linear
+ * Attention notes, Sec. 3.2-3.4 and Fig. 1; the backend notes name
+ * causal_conv1d with SiLU):
+ *   q = l2norm(silu(conv_q * q_in)),  k = l2norm(silu(conv_k * k_in)),
+ *   v = silu(conv_v * v_in),  beta = sigmoid(beta_logit),
+ *   gate = -gate_a[h] * softplus(gate_z + gate_b)          (log alpha, Mamba2 style)
+ * "conv *" is a depthwise causal convolution along t of width `width` (1..8):
+ * out[b,t,h,c] = sum_i w[h*d + c][width-1-i] * x[b,t-i,h,c], zero before t = 0
+ * (no state carried in from an earlier call).  l2norm divides each (b,t,h) row
+ * by sqrt(sum of squares + eps).  Arithmetic in fp32; outputs in `dtype`.
+ *   q_in, k_in, q, k [B][T][H][dk] and v_in, v [B][T][H][dv] of `dtype`
+ *   conv_q, conv_k [H*dk][width], conv_v [H*dv][width] fp32
+ *   beta_logit, beta [B][T][H] fp32
+ *   mode GDN: gate_z, gate [B][T][H]; gate_a, gate_b [H]
+ *   mode KDA: gate_z, gate [B][T][H][dk]; gate_a [H]; gate_b [H][dk]
+ *   mode DELTANET: gate_z, gate_a, gate_b and gate are ignored (may be NULL)
+ * The outputs are the inputs ldn_chunk_fwd takes.  They must not overlap any
+ * input or each other (LDN_ERR_INVALID_ARG).  Alignment: q/k/v in and out
+ * 16-byte; KDA gate_z, gate_b and gate 16-byte; the rest 4-byte.  dk, dv in
+ * {64, 128}; width > 8 returns LDN_ERR_UNSUPPORTED; eps >= 0.  Asynchronous on
+ * `stream`; two kernel launches (three when dk != dv).
+ */
+int ldn_prologue(const void *q_in, const void *k_in, const void *v_in, const float *conv_q, const float *conv_k,
+                 const float *conv_v, int width, const float *beta_logit, const float *gate_z, const float *gate_a,
+                 const float *gate_b, void *q, void *k, void *v, float *beta, float *gate, int B, int T, int H,
+                 int dk, int dv, int mode, int dtype, float eps, void *stream);
+
+/*
+ * ldn_rmsnorm_gated -- the output epilogue (the model-zoo page's Gated DeltaNet
+ * entry: the output goes through RMSNorm, a gain and a SiLU gate; the backend
+ * notes name rms_norm_gated):
+ *   y = o / sqrt(mean_c o_c^2 + eps) * weight * silu(g)
+ * per (b,t,h) row of dv values, fp32 arithmetic.
+ *   o, g, y [B][T][H][dv] of `dtype` (16-byte aligned); weight [dv] fp32 (the
+ *   gain, shared by the heads).  y may be o (in place) but must not overlap g.
+ * dv in {64, 128}; eps >= 0.  Asynchronous on `stream`; one kernel launch.
+ */
+int ldn_rmsnorm_gated(const void *o, const void *g, const float *weight, void *y, int B, int T, int H, int dv,
+                      int dtype, float eps, void *stream);
+
+/*
  * ldn_decode_step -- one recurrent step for every (b, h), state updated in place.
  *
  * For one token per sequence it forms the decayed state S' = alpha S (GDN),

@@ -191,3 +191,69 @@ def test_pair_variant_outside_its_sizes_is_unsupported(lib):
     assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=64, dv=128) == ldn.LDN_ERR_UNSUPPORTED
     assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=128, dv=128, dtype=0) == ldn.LDN_ERR_UNSUPPORTED  # fp32
     assert _chunk(variant=5) == ldn.LDN_ERR_INVALID_ARG
+
+
+def _prologue(**kw):
+    a = dict(q_in=FAKE, k_in=FAKE + (1 << 22), v_in=FAKE + (2 << 22), conv_q=FAKE + (3 << 22), conv_k=FAKE + (3 << 22),
+             conv_v=FAKE + (3 << 22), width=4, beta_logit=FAKE + (4 << 22), gate_z=FAKE + (5 << 22),
+             gate_a=FAKE + (6 << 22), gate_b=FAKE + (6 << 22), q=FAKE + (8 << 22), k=FAKE + (9 << 22),
+             v=FAKE + (10 << 22), beta=FAKE + (11 << 22), gate=FAKE + (12 << 22), B=1, T=64, H=2, dk=128, dv=128,
+             mode=1, dtype=1, eps=1e-6, stream=None)
+    a.update(kw)
+    return ldn.ldn_prologue(a["q_in"], a["k_in"], a["v_in"], a["conv_q"], a["conv_k"], a["conv_v"], a["width"],
+                            a["beta_logit"], a["gate_z"], a["gate_a"], a["gate_b"], a["q"], a["k"], a["v"],
+                            a["beta"], a["gate"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["mode"], a["dtype"],
+                            a["eps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(width=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(width=9), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(eps=-1.0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dk=96), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(mode=4), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q_in=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(conv_v=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(beta=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate_z=None), ldn.LDN_ERR_INVALID_ARG),          # GDN needs its gate inputs
+    (dict(gate=None, mode=2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q=FAKE + (8 << 22) + 8), ldn.LDN_ERR_INVALID_ARG),   # misaligned row
+    (dict(gate_z=FAKE + (5 << 22) + 4, mode=2), ldn.LDN_ERR_INVALID_ARG),   # KDA gates move as float4
+    (dict(q=FAKE), ldn.LDN_ERR_INVALID_ARG),                # output over its own input
+    (dict(v=FAKE + (1 << 22) + 64), ldn.LDN_ERR_INVALID_ARG),   # output inside another input
+    (dict(k=FAKE + (8 << 22) + 1024), ldn.LDN_ERR_INVALID_ARG),  # outputs overlapping each other
+    (dict(B=0), ldn.LDN_ERR_INVALID_ARG),
+])
+def test_prologue_rejects_bad_arguments(lib, kw, want):
+    assert _prologue(**kw) == want
+
+
+def test_prologue_zero_length_and_deltanet_gates_need_no_pointers(lib):
+    assert _prologue(T=0, q_in=None, q=None) == ldn.LDN_OK   # nothing to do, nothing launched
+    # DeltaNet ignores the gate pointers: NULL gate inputs pass the checks (the rejection
+    # tested here is the misaligned q, which comes after them)
+    assert _prologue(mode=0, gate_z=None, gate_a=None, gate_b=None, gate=None, q=FAKE + (8 << 22) + 8) == \
+        ldn.LDN_ERR_INVALID_ARG
+
+
+def _rms(**kw):
+    a = dict(o=FAKE, g=FAKE + (1 << 22), weight=FAKE + (2 << 22), y=FAKE + (3 << 22), B=1, T=64, H=2, dv=128,
+             dtype=1, eps=1e-6, stream=None)
+    a.update(kw)
+    return ldn.ldn_rmsnorm_gated(a["o"], a["g"], a["weight"], a["y"], a["B"], a["T"], a["H"], a["dv"], a["dtype"],
+                                 a["eps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(y=FAKE + (1 << 22)), ldn.LDN_ERR_INVALID_ARG),     # y over the gate
+    (dict(y=FAKE + 512), ldn.LDN_ERR_INVALID_ARG),           # y partly over o
+    (dict(o=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(o=FAKE + 8), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dv=96), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(dtype=3), ldn.LDN_ERR_INVALID_ARG),
+    (dict(eps=-0.5), ldn.LDN_ERR_INVALID_ARG),
+    (dict(T=-1), ldn.LDN_ERR_INVALID_ARG),
+])
+def test_rmsnorm_gated_rejects_bad_arguments(lib, kw, want):
+    assert _rms(**kw) == want
