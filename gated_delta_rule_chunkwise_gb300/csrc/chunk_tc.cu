@@ -86,6 +86,7 @@ constexpr int kSerialThreads = 128;
 constexpr int kThreads = kPrepThreads + kSerialThreads;
 constexpr uint32_t kBarPrep = 1, kBarSerial = 2;   // named barrier ids
 constexpr uint32_t kBarBuild = 3, kBarBuildIssue = 4;   // KDA operand build (warps 4-7; + issuer warp 3)
+constexpr uint32_t kBarChain = 5, kBarChain2 = 6;       // levels of the block inverse (warps 0-2; 0-1)
 constexpr int kIssuer = 96;                        // prep thread issuing every prep MMA (warp 3)
 constexpr int kGateWarp = 4;                       // prep warp computing gate prefixes
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
@@ -131,7 +132,7 @@ struct Layout {
     static constexpr uint32_t a16 = ub + (SPLIT ? 0 : 8192);       // fp16 A [64][72]
     static constexpr uint32_t p16 = a16 + 64 * kLd16 * 2;          // fp16 P [64][72]
     static constexpr uint32_t t16 = p16 + 64 * kLd16 * 2;          // fp16 T [64][72]
-    static constexpr uint32_t x = t16 + 64 * kLd16 * 2;            // fp16 16x16 scratch per chain warp [3][16][24]
+    static constexpr uint32_t x = t16 + 64 * kLd16 * 2;            // fp16 16x16 scratch of the block inverse [4][16][24]
     static constexpr uint32_t small = x + 3072;
     static constexpr uint32_t bytes = small + kSmallBytes + 1024;
     static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
@@ -765,48 +766,78 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             named_sync(kBarPrep, kPrepThreads);
             }   // run
-            // Below-diagonal blocks, one warp per 16-column block i (warps 0..2):
-            //   T_{R,i} = -T_{R,R} sum_{k=i}^{R-1} A_{R,k} T_{k,i},   R = i+1 .. 3,
-            // each 16x16x16 product as two m16n8k16 fp16 warp MMAs (fp32 accumulate),
-            // operands fetched with ldmatrix (row-major A blocks, transposed B blocks).
+            // Below-diagonal blocks by halves (warps 0..2).  With T_TL, T_BR the inverses of
+            // the top-left and bottom-right 32x32 diagonal blocks, T_BL = -T_BR M with
+            // M = A_BL T_TL, in three levels:
+            //   (1) T10 = -T11 A10 T00, T32 = -T33 A32 T22, M01 = A21 T11, M11 = A31 T11;
+            //   (2) M00 = A20 T00 + A21 T10, M10 = A30 T00 + A31 T10,
+            //       T21 = -T22 M01, T31 = -(T32 M01 + T33 M11);
+            //   (3) T20 = -T22 M00, T30 = -(T32 M00 + T33 M10).
+            // Four dependent block products on the longest path (a substitution column by
+            // column has six).  Each 16x16x16 product is two m16n8k16 fp16 warp MMAs (fp32
+            // accumulate) with ldmatrix operands (row-major A blocks, transposed B blocks);
+            // intermediate products and M are fp16 16x16 blocks in the X scratch (4 slots,
+            // row stride 24).
             if (warp < 3) {
                 if (run) {
-                const int i = warp, g = lane >> 2, t4 = lane & 3;
+                const int g = lane >> 2, t4 = lane & 3;
                 const int lr = lane & 15, lc = 8 * (lane >> 4);   // ldmatrix row / column of this lane
-                __half *X = X16 + 16 * 24 * warp;                  // 16x16 fp16 scratch, row stride 24
-                for (int R = i + 1; R < 4; ++R) {
-                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int kb = i; kb < R; ++kb) {
-                        uint32_t a[4], bq[4];
-                        ldsm_x4(a, A16 + (16 * R + lr) * kLd16 + 16 * kb + lc);
-                        ldsm_x4_trans(bq, T16 + (16 * kb + lr) * kLd16 + 16 * i + lc);
-                        mma_f16_16x8x16(acc[0], a, bq);
-                        mma_f16_16x8x16(acc[1], a, bq + 2);
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        *reinterpret_cast<uint32_t *>(X + g * 24 + 8 * nt + 2 * t4) = pack_h2(acc[nt][0], acc[nt][1]);
-                        *reinterpret_cast<uint32_t *>(X + (g + 8) * 24 + 8 * nt + 2 * t4) =
-                            pack_h2(acc[nt][2], acc[nt][3]);
-                    }
-                    __syncwarp();
-                    float tacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    {
-                        uint32_t a[4], bq[4];
-                        ldsm_x4(a, T16 + (16 * R + lr) * kLd16 + 16 * R + lc);
-                        ldsm_x4_trans(bq, X + lr * 24 + lc);
-                        mma_f16_16x8x16(tacc[0], a, bq);
-                        mma_f16_16x8x16(tacc[1], a, bq + 2);
-                    }
+                auto Ab = [&](int R, int C) { return A16 + 16 * R * kLd16 + 16 * C; };
+                auto Tb = [&](int R, int C) { return T16 + 16 * R * kLd16 + 16 * C; };
+                auto Xb = [&](int slot) { return X16 + 16 * 24 * slot; };
+                auto mma_blk = [&](float (&acc)[2][4], const __half *a, int lda, const __half *bm, int ldb) {
+                    uint32_t af[4], bq[4];
+                    ldsm_x4(af, a + lr * lda + lc);
+                    ldsm_x4_trans(bq, bm + lr * ldb + lc);
+                    mma_f16_16x8x16(acc[0], af, bq);
+                    mma_f16_16x8x16(acc[1], af, bq + 2);
+                };
+                auto st_blk = [&](__half *dst, int ld, const float (&acc)[2][4], float sgn) {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int rr = 16 * R + g + 8 * hh, cc = 16 * i + 8 * nt + 2 * t4;
-                            const float t0v = -tacc[nt][2 * hh], t1v = -tacc[nt][2 * hh + 1];
-                            *reinterpret_cast<uint32_t *>(T16 + rr * kLd16 + cc) = pack_h2(t0v, t1v);
-                        }
+                        for (int hh = 0; hh < 2; ++hh)
+                            *reinterpret_cast<uint32_t *>(dst + (g + 8 * hh) * ld + 8 * nt + 2 * t4) =
+                                pack_h2(sgn * acc[nt][2 * hh], sgn * acc[nt][2 * hh + 1]);
+                };
+                // ---- level 1
+                if (warp < 2) {   // T10 (warp 0), T32 (warp 1): X = A_{r,r-1} T_{r-1,r-1}, then -T_rr X
+                    const int r = warp == 0 ? 1 : 3;
+                    float acc[2][4] = {};
+                    mma_blk(acc, Ab(r, r - 1), kLd16, Tb(r - 1, r - 1), kLd16);
+                    st_blk(Xb(warp), 24, acc, 1.f);
                     __syncwarp();
+                    float t[2][4] = {};
+                    mma_blk(t, Tb(r, r), kLd16, Xb(warp), 24);
+                    st_blk(Tb(r, r - 1), kLd16, t, -1.f);
+                } else {          // M01 = A21 T11, M11 = A31 T11
+                    float m01[2][4] = {}, m11[2][4] = {};
+                    mma_blk(m01, Ab(2, 1), kLd16, Tb(1, 1), kLd16);
+                    mma_blk(m11, Ab(3, 1), kLd16, Tb(1, 1), kLd16);
+                    st_blk(Xb(2), 24, m01, 1.f);
+                    st_blk(Xb(3), 24, m11, 1.f);
+                }
+                named_sync(kBarChain, 96);
+                // ---- level 2
+                if (warp < 2) {   // M00 (warp 0), M10 (warp 1) = A_r0 T00 + A_r1 T10, r = 2, 3
+                    const int r = 2 + warp;
+                    float acc[2][4] = {};
+                    mma_blk(acc, Ab(r, 0), kLd16, Tb(0, 0), kLd16);
+                    mma_blk(acc, Ab(r, 1), kLd16, Tb(1, 0), kLd16);
+                    st_blk(Xb(warp), 24, acc, 1.f);   // over this warp's level-1 scratch
+                    named_sync(kBarChain2, 64);
+                    // ---- level 3: T20 = -T22 M00 (warp 0), T30 = -(T32 M00 + T33 M10) (warp 1)
+                    float t[2][4] = {};
+                    mma_blk(t, Tb(2 + warp, 2), kLd16, Xb(0), 24);
+                    if (warp == 1) mma_blk(t, Tb(3, 3), kLd16, Xb(1), 24);
+                    st_blk(Tb(2 + warp, 0), kLd16, t, -1.f);
+                } else {          // T21 = -T22 M01, T31 = -(T32 M01 + T33 M11)
+                    float t21[2][4] = {}, t31[2][4] = {};
+                    mma_blk(t21, Tb(2, 2), kLd16, Xb(2), 24);
+                    mma_blk(t31, Tb(3, 2), kLd16, Xb(2), 24);
+                    mma_blk(t31, Tb(3, 3), kLd16, Xb(3), 24);
+                    st_blk(Tb(2, 1), kLd16, t21, -1.f);
+                    st_blk(Tb(3, 1), kLd16, t31, -1.f);
                 }
                 }   // run
             } else if (warp == kIssuer / 32) {
