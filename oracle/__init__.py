@@ -15,7 +15,10 @@ Attention notes (Sec. 1.2), closed forms for orthonormal / axis keys, the
 linear-attention limit, orthogonal invariance and per-value-channel
 independence from the state-reduction notes (Sec. 2.5, Prop. 3.1), the rank
 bound (Eq. 3), the contraction of (I - beta k k^T), state passing, and a brute
-force by explicit matrix products at d = 4, T = 8.
+force by explicit matrix products at d = 4, T = 8.  Gated DeltaNet-2 (Sec. 2.6) is
+pinned in tests/test_gdn2_oracle_pins.py: its reduction to KDA, the erase-off /
+write-on additive limit, the exact write with unit keys, and a brute force through
+the notes' matrix expansion.
 """
 from __future__ import annotations
 
@@ -32,7 +35,7 @@ _LIB_PATH = os.path.join(_HERE, "libldn_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-MODE_DELTANET, MODE_GDN, MODE_KDA = 0, 1, 2
+MODE_DELTANET, MODE_GDN, MODE_KDA, MODE_GDN2 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -59,6 +62,9 @@ def _load():
             f = lib.ldn_oracle_fwd
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)]
+            g2 = lib.ldn_oracle_fwd_gdn2
+            g2.restype = ctypes.c_int
+            g2.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int)]
             lib.ldn_oracle_default_threads.restype = ctypes.c_int
             lib.ldn_oracle_default_threads.argtypes = []
             _lib = lib
@@ -118,6 +124,40 @@ def fwd(q, k, v, beta, gate=None, S0=None, mode=MODE_DELTANET, nthreads=0,
     if return_threads:
         return out, sf, int(used.value)
     return out, sf
+
+
+def fwd_gdn2(q, k, v, erase, write, gate, S0=None, nthreads=0, want_state=True):
+    """Gated DeltaNet-2 token recurrence in fp64 (linear-attention notes, Sec. 2.6,
+    Eqs. 21-24): per-key-channel decay, erase direction e = erase * k, write
+    target z = write * v, outer product with k.
+
+    q, k, erase, gate (log-decay): [B, T, H, dk]; v, write: [B, T, H, dv];
+    S0: [B, H, dk, dv] or None.  Returns (o, S_final or None) as in ``fwd``."""
+    q, k, v = _f32(q, "q"), _f32(k, "k"), _f32(v, "v")
+    erase, write, gate = _f32(erase, "erase"), _f32(write, "write"), _f32(gate, "gate")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or erase.shape != q.shape or gate.shape != q.shape or v.shape[:3] != (B, T, H) \
+            or write.shape != v.shape:
+        raise ValueError("oracle: inconsistent shapes")
+    S0 = _f32(S0, "S0")
+    if S0 is not None and S0.shape != (B, H, dk, dv):
+        raise ValueError("oracle: S0 must be [B, H, dk, dv]")
+    out = np.empty((B, T, H, dv), dtype=np.float64)
+    sf = np.empty((B, H, dk, dv), dtype=np.float64) if want_state else None
+    used = ctypes.c_int(0)
+    rc = _load().ldn_oracle_fwd_gdn2(_ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(gate), _ptr(S0),
+                                     _ptr(out), _ptr(sf), B, T, H, dk, dv, int(nthreads), ctypes.byref(used))
+    if rc != 0:
+        raise RuntimeError(f"ldn_oracle_fwd_gdn2 failed with {rc}")
+    return out, sf
+
+
+def decode_gdn2(q, k, v, erase, write, gate, S0, nthreads=0):
+    """Consecutive Gated DeltaNet-2 decode steps: inputs [steps, B, H, d]."""
+    tr = lambda a: None if a is None else np.ascontiguousarray(np.swapaxes(np.asarray(a), 0, 1))
+    o, sf = fwd_gdn2(tr(q), tr(k), tr(v), tr(erase), tr(write), tr(gate), S0, nthreads=nthreads)
+    return np.ascontiguousarray(np.swapaxes(o, 0, 1)), sf
 
 
 def decode(q, k, v, beta, gate, S0, mode=MODE_GDN, nthreads=0):

@@ -22,6 +22,10 @@
  *     Sec. 2.5, Eqs. 18-20     KDA: D = Diag(a) multiplies W on the RIGHT
  *                              (key-feature side): vbar = W_{i-1} D k,
  *                              W_i = W_{i-1} D + beta (v - vbar) k^T
+ *     Sec. 2.6, Eqs. 21-24     Gated DeltaNet-2: the erase and the write get
+ *                              their own gates: Wt = W_{i-1} D, e = b * k,
+ *                              z = w * v (elementwise), r = z - Wt e,
+ *                              W_i = Wt + r k^T (the outer product keeps k)
  *   "Reading notes: State reduction by key/query channel pruning",
  *     Sec. 2.1, Eqs. 1-2       the same DeltaNet update in S notation.
  *
@@ -49,9 +53,11 @@
 #define LDN_ORACLE_MODE_DELTANET 0
 #define LDN_ORACLE_MODE_GDN 1
 #define LDN_ORACLE_MODE_KDA 2
+#define LDN_ORACLE_MODE_GDN2 3
 
 typedef struct {
     const float *q, *k, *v, *beta, *gate, *S0;
+    const float *erase, *write; /* Gated DeltaNet-2: b [B][T][H][dk], w [B][T][H][dv] */
     double *out, *S_final;
     int B, T, H, dk, dv, mode;
     int next_unit; /* shared work counter, protected by lock */
@@ -79,13 +85,16 @@ static void run_unit(const job_t *J, int unit, double *W, double *pred)
         const float *q = J->q + tok * dk;
         const float *k = J->k + tok * dk;
         const float *v = J->v + tok * dv;
-        const double beta = (double)J->beta[tok];
+        const int gdn2 = J->mode == LDN_ORACLE_MODE_GDN2;
+        const double beta = gdn2 ? 1.0 : (double)J->beta[tok];
+        const float *eb = gdn2 ? J->erase + tok * dk : NULL;   /* e = b * k */
+        const float *ww = gdn2 ? J->write + tok * dv : NULL;   /* z = w * v */
 
         /* Forget step: scalar alpha (Eqs. 15-17) or W <- W Diag(a) (Eqs. 18-20). */
         if (J->mode == LDN_ORACLE_MODE_GDN) {
             const double alpha = exp((double)J->gate[tok]);
             for (size_t e = 0; e < (size_t)dk * dv; ++e) W[e] *= alpha;
-        } else if (J->mode == LDN_ORACLE_MODE_KDA) {
+        } else if (J->mode == LDN_ORACLE_MODE_KDA || gdn2) {
             const float *g = J->gate + tok * dk;
             for (int c = 0; c < dk; ++c) {
                 const double a = exp((double)g[c]);
@@ -93,15 +102,19 @@ static void run_unit(const job_t *J, int unit, double *W, double *pred)
             }
         }
 
-        /* Prediction of the (decayed) memory for the current key, Eq. 9. */
+        /* Prediction of the (decayed) memory for the current key, Eq. 9
+           (Gated DeltaNet-2: along the erase direction e = b * k, Eq. 23). */
         for (int i = 0; i < dv; ++i) {
             double s = 0.0;
-            for (int c = 0; c < dk; ++c) s += W[(size_t)i * dk + c] * (double)k[c];
+            for (int c = 0; c < dk; ++c)
+                s += W[(size_t)i * dk + c] * (gdn2 ? (double)eb[c] * (double)k[c] : (double)k[c]);
             pred[i] = s;
         }
-        /* Write the error along the key, Eq. 10: W += beta (v - pred) k^T. */
+        /* Write the error along the key, Eq. 10: W += beta (v - pred) k^T
+           (Gated DeltaNet-2, Eq. 24: W += (w * v - pred) k^T). */
         for (int i = 0; i < dv; ++i) {
-            const double r = beta * ((double)v[i] - pred[i]);
+            const double target = gdn2 ? (double)ww[i] * (double)v[i] : (double)v[i];
+            const double r = beta * (target - pred[i]);
             for (int c = 0; c < dk; ++c) W[(size_t)i * dk + c] += r * (double)k[c];
         }
         /* Read the updated memory with the query, Eq. 8. */
@@ -139,6 +152,8 @@ static void *worker(void *arg)
     return NULL;
 }
 
+static int run_job(job_t *J, int nthreads, int *threads_used);
+
 /* Number of host threads ldn_oracle_fwd uses for nthreads <= 0. */
 int ldn_oracle_default_threads(void)
 {
@@ -169,10 +184,40 @@ int ldn_oracle_fwd(const float *q, const float *k, const float *v,
 
     job_t J;
     J.q = q; J.k = k; J.v = v; J.beta = beta; J.gate = gate; J.S0 = S0;
+    J.erase = NULL; J.write = NULL;
     J.out = out; J.S_final = S_final;
     J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv; J.mode = mode;
+    return run_job(&J, nthreads, threads_used);
+}
+
+/*
+ * ldn_oracle_fwd_gdn2: the Gated DeltaNet-2 recurrence (Sec. 2.6, Eqs. 21-24)
+ * for every (batch, head) pair.  As ldn_oracle_fwd, with the write strength
+ * beta replaced by the erase gate b [B][T][H][dk] (e = b * k) and the write
+ * gate w [B][T][H][dv] (z = w * v); gate is the per-key-channel log-decay
+ * [B][T][H][dk].
+ */
+int ldn_oracle_fwd_gdn2(const float *q, const float *k, const float *v,
+                        const float *erase, const float *write, const float *gate, const float *S0,
+                        double *out, double *S_final, int B, int T, int H, int dk, int dv,
+                        int nthreads, int *threads_used)
+{
+    if (!q || !k || !v || !erase || !write || !gate || !out) return -1;
+    if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1) return -1;
+    job_t J;
+    J.q = q; J.k = k; J.v = v; J.beta = NULL; J.gate = gate; J.S0 = S0;
+    J.erase = erase; J.write = write;
+    J.out = out; J.S_final = S_final;
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv; J.mode = LDN_ORACLE_MODE_GDN2;
+    return run_job(&J, nthreads, threads_used);
+}
+
+static int run_job(job_t *J_, int nthreads, int *threads_used)
+{
+    job_t J = *J_;
     J.next_unit = 0;
     pthread_mutex_init(&J.lock, NULL);
+    const int B = J.B, H = J.H;
 
     int units = B * H;
     if (nthreads <= 0) nthreads = ldn_oracle_default_threads();

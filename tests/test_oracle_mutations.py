@@ -32,8 +32,13 @@ MUTANTS = {
     "s0_orientation": ("W[(size_t)i * dk + c] = (double)s0[(size_t)c * dv + i];",
                        "W[(size_t)i * dk + c] = (double)s0[(size_t)i * dk + c];"),
     # the prediction uses the query instead of the key
-    "predict_with_query": ("for (int c = 0; c < dk; ++c) s += W[(size_t)i * dk + c] * (double)k[c];\n            pred[i] = s;",
-                           "for (int c = 0; c < dk; ++c) s += W[(size_t)i * dk + c] * (double)q[c];\n            pred[i] = s;"),
+    "predict_with_query": ("s += W[(size_t)i * dk + c] * (gdn2 ? (double)eb[c] * (double)k[c] : (double)k[c]);",
+                           "s += W[(size_t)i * dk + c] * (gdn2 ? (double)eb[c] * (double)k[c] : (double)q[c]);"),
+    # Gated DeltaNet-2: the erase gate is not applied to the prediction direction
+    "gdn2_no_erase": ("(gdn2 ? (double)eb[c] * (double)k[c] : (double)k[c])", "(double)k[c]"),
+    # Gated DeltaNet-2: the write gate is not applied to the value
+    "gdn2_no_write": ("const double target = gdn2 ? (double)ww[i] * (double)v[i] : (double)v[i];",
+                      "const double target = (double)v[i];"),
 }
 
 
@@ -49,6 +54,7 @@ def test_pins_catch_mutant(name, tmp_path):
                     "-D_POSIX_C_SOURCE=200809L", str(mutant_c), "-o", str(lib), "-lm"], check=True)
     env = dict(os.environ, LDN_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_gdn2_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
