@@ -35,12 +35,13 @@ sys.path.insert(0, ROOT)
 METRIC = "tokens/s chunkwise GDN fwd (H=16,dk=dv=128) + % roofline; decode GB/s"
 WORKLOAD = "gdn_bf16_b4_t2048_h16_d128"
 EXTRA_WORKLOADS = ("kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
-                   "gdn_bf16_long_b1_t65536_h16_d128", "deltanet_fp32_b1_t256_h1_d64")
+                   "gdn_bf16_long_b1_t65536_h16_d128", "deltanet_fp32_b1_t256_h1_d64", "gdn2_bf16_b8_t4096_h16_d128")
 PROLOGUE_WORKLOADS = ("gdn_prologue_bf16_b4_t2048_h16_d128_w4", "kda_prologue_bf16_b8_t4096_h16_d128_w4")
-DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000")
+DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000",
+                    "gdn2_decode_b64_h16_dk128_dv128_steps1000")
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
-MODE_NAME = {0: "deltanet", 1: "gdn", 2: "kda"}
+MODE_NAME = {0: "deltanet", 1: "gdn", 2: "kda", 3: "gdn2"}
 KERNEL_NAME = {2: "tcgen05", 3: "split", 4: "pair"}   # LDN_VARIANT_* -> kernel family in the JSON line
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -49,10 +50,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # algorithmic work
 def chunk_bytes(B, T, H, dk, dv, el_bytes, mode, s0, s_final):
     """Bytes a chunk forward must move at least: q, k, v read, o written,
-    beta and gate read (fp32), initial / final state (fp32)."""
+    beta and gate read (fp32; Gated DeltaNet-2: erase, write and gate), initial /
+    final state (fp32)."""
     n = B * T * H
-    gate = 0 if mode == 0 else (4 if mode == 1 else 4 * dk)
-    b = n * (el_bytes * (2 * dk + 2 * dv) + 4 + gate)
+    gates = {0: 4, 1: 8, 2: 4 + 4 * dk, 3: 8 * dk + 4 * dv}[mode]
+    b = n * (el_bytes * (2 * dk + 2 * dv) + gates)
     st = B * H * dk * dv * 4
     return b + (st if s0 else 0) + (st if s_final else 0)
 
@@ -82,8 +84,9 @@ def rmsnorm_bytes(B, T, H, dv, el_bytes):
 
 
 def decode_bytes(B, H, dk, dv, mode):
-    gate = 0 if mode == 0 else (4 if mode == 1 else 4 * dk)
-    return B * H * (2 * dk * dv * 4 + 2 * dk * 4 + 2 * dv * 4 + 4 + gate)
+    """State read and written, q, k, v, out (fp32) and the gates of one step."""
+    gates = {0: 4, 1: 8, 2: 4 + 4 * dk, 3: 8 * dk + 4 * dv}[mode]
+    return B * H * (2 * dk * dv * 4 + 2 * dk * 4 + 2 * dv * 4 + gates)
 
 
 def load_peaks():
@@ -404,16 +407,22 @@ def run_ours(args):
             osf = torch.empty((ow.B, ow.H, ow.dk, ow.dv), dtype=torch.float32, device="cuda")
             optr = (P(ot["q"]), P(ot["k"]), P(ot["v"]), P(ot["beta"]), P(ot["gate"]), P(ot["S0"]), P(oout), P(osf))
             odt = ldn.LDN_BF16 if ow.dtype == "bf16" else ldn.LDN_F32
+            g2 = ow.mode == wl.MODE_GDN2
 
-            ows_bytes = ldn.ldn_chunk_fwd_workspace_size(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt)
+            ows_bytes = 0 if g2 else ldn.ldn_chunk_fwd_workspace_size(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt)
             ows = torch.empty(max(ows_bytes, 256), dtype=torch.uint8, device="cuda")
-            ochosen = ldn.ldn_chunk_fwd_select_ws(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt, ows_bytes)
+            ochosen = ldn.LDN_VARIANT_SIMT if g2 else ldn.ldn_chunk_fwd_select_ws(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64,
+                                                                                   ow.mode, odt, ows_bytes)
 
             def ostep():
-                st_ = ldn.ldn_chunk_fwd_ws(*optr, ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt,
-                                           ldn.LDN_VARIANT_AUTO, ows.data_ptr(), ows_bytes, sh)
+                if g2:
+                    st_ = ldn.ldn_chunk_fwd_gdn2(optr[0], optr[1], optr[2], P(ot["erase"]), P(ot["write"]), optr[4],
+                                                 optr[5], optr[6], optr[7], ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, odt, sh)
+                else:
+                    st_ = ldn.ldn_chunk_fwd_ws(*optr, ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt,
+                                               ldn.LDN_VARIANT_AUTO, ows.data_ptr(), ows_bytes, sh)
                 if st_ != ldn.LDN_OK:
-                    raise ldn.LdnError(st_, "ldn_chunk_fwd_ws")
+                    raise ldn.LdnError(st_, "ldn_chunk_fwd_gdn2" if g2 else "ldn_chunk_fwd_ws")
 
             ostep()
             oev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
@@ -501,13 +510,19 @@ def run_ours(args):
             S = td["S0"].clone()
             o = torch.empty((d.B, d.H, d.dv), dtype=torch.float32, device="cuda")
             steps = d.T
-            ptr = [(td["q"][i].data_ptr(), td["k"][i].data_ptr(), td["v"][i].data_ptr(), td["beta"][i].data_ptr(),
-                    td["gate"][i].data_ptr()) for i in range(steps)]
+            g2 = d.mode == wl.MODE_GDN2
+            ptr = [(td["q"][i].data_ptr(), td["k"][i].data_ptr(), td["v"][i].data_ptr(),
+                    td["erase"][i].data_ptr() if g2 else td["beta"][i].data_ptr(), td["gate"][i].data_ptr(),
+                    td["write"][i].data_ptr() if g2 else 0) for i in range(steps)]
 
             def dstep(i):
-                qp, kp, vp, bp, gp = ptr[i]
-                st = ldn.ldn_decode_step(qp, kp, vp, bp, gp, S.data_ptr(), o.data_ptr(), d.B, d.H, d.dk, d.dv,
-                                         d.mode, ldn.LDN_F32, sh)
+                qp, kp, vp, bp, gp, wp = ptr[i]
+                if g2:
+                    st = ldn.ldn_decode_step_gdn2(qp, kp, vp, bp, wp, gp, S.data_ptr(), o.data_ptr(), d.B, d.H, d.dk,
+                                                  d.dv, ldn.LDN_F32, sh)
+                else:
+                    st = ldn.ldn_decode_step(qp, kp, vp, bp, gp, S.data_ptr(), o.data_ptr(), d.B, d.H, d.dk, d.dv,
+                                             d.mode, ldn.LDN_F32, sh)
                 if st != ldn.LDN_OK:
                     raise ldn.LdnError(st, "ldn_decode_step")
 

@@ -7,10 +7,11 @@ been built, or no GPU is present, the calls raise.
 Two layers:
   * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
     ``ldn_chunk_fwd_workspace_size``, ``ldn_chunk_fwd_noalloc``, ``ldn_decode_step``,
-    ``ldn_prologue``, ``ldn_rmsnorm_gated``,
+    ``ldn_chunk_fwd_gdn2``, ``ldn_decode_step_gdn2``, ``ldn_prologue``, ``ldn_rmsnorm_gated``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
-  * ``chunk_fwd`` and ``decode_step``: the same calls on torch CUDA tensors,
+  * ``chunk_fwd``, ``decode_step``, ``chunk_fwd_gdn2`` and ``decode_step_gdn2``:
+    the same calls on torch CUDA tensors,
     with shape / dtype checks and allocation of outputs and of the split
     variant's workspace (torch is used for device memory and the current
     stream only).
@@ -24,7 +25,7 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libldn.so")
 
-LDN_DELTANET, LDN_GDN, LDN_KDA = 0, 1, 2
+LDN_DELTANET, LDN_GDN, LDN_KDA, LDN_GDN2 = 0, 1, 2, 3
 LDN_F32, LDN_BF16 = 0, 1
 LDN_OK, LDN_ERR_INVALID_ARG, LDN_ERR_UNSUPPORTED, LDN_ERR_CUDA, LDN_ERR_TIMEOUT = 0, 1, 2, 3, 4
 LDN_VARIANT_AUTO, LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR, LDN_VARIANT_SPLIT, LDN_VARIANT_PAIR = 0, 1, 2, 3, 4
@@ -53,6 +54,8 @@ _SIGNATURES = {
     "ldn_chunk_fwd_select_ws": ([_I] * 8 + [ctypes.c_size_t], _I),
     "ldn_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 9 + [_P], _I),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
+    "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 7 + [_P], _I),
+    "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
     "ldn_rmsnorm_gated": ([_P] * 4 + [_I] * 5 + [ctypes.c_float, _P], _I),
     "ldn_get_device_status": ([_P], _I),
@@ -122,6 +125,15 @@ def ldn_chunk_fwd_noalloc(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv
 
 def ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream):
     return load().ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream)
+
+
+def ldn_chunk_fwd_gdn2(q, k, v, erase, write, gate, S0, out, S_final, B, T, H, dk, dv, chunk, dtype, stream):
+    return load().ldn_chunk_fwd_gdn2(q, k, v, erase, write, gate, S0, out, S_final, B, T, H, dk, dv, chunk,
+                                     dtype, stream)
+
+
+def ldn_decode_step_gdn2(q, k, v, erase, write, gate, S, out, B, H, dk, dv, dtype, stream):
+    return load().ldn_decode_step_gdn2(q, k, v, erase, write, gate, S, out, B, H, dk, dv, dtype, stream)
 
 
 def ldn_prologue(q_in, k_in, v_in, conv_q, conv_k, conv_v, width, beta_logit, gate_z, gate_a, gate_b,
@@ -264,6 +276,53 @@ def decode_step(q, k, v, beta, gate, S, *, mode, out=None, stream=None):
                          B, H, dk, dv, mode, _dtype_code(q), _stream_handle(stream))
     if st != LDN_OK:
         raise LdnError(st, "ldn_decode_step")
+    return out
+
+
+def chunk_fwd_gdn2(q, k, v, erase, write, gate, S0=None, *, chunk=64, out=None, S_final=None, want_state=True,
+                   stream=None):
+    """Gated DeltaNet-2 chunkwise forward on torch CUDA tensors (ldn_chunk_fwd_gdn2).
+
+    q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16); erase, gate [B,T,H,dk]
+    and write [B,T,H,dv] float32; S0 [B,H,dk,dv] float32 or None.
+    Returns (out, S_final or None)."""
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q"); _check(k, "k", q.shape, q.dtype); _check(v, "v", (B, T, H, dv), q.dtype)
+    _check(erase, "erase", (B, T, H, dk), torch.float32); _check(write, "write", (B, T, H, dv), torch.float32)
+    _check(gate, "gate", (B, T, H, dk), torch.float32)
+    _check(S0, "S0", (B, H, dk, dv), torch.float32)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", (B, T, H, dv), q.dtype)
+    if S_final is None and want_state:
+        S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check(S_final, "S_final", (B, H, dk, dv), torch.float32)
+    st = ldn_chunk_fwd_gdn2(_ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(gate), _ptr(S0), _ptr(out),
+                            _ptr(S_final), B, T, H, dk, dv, chunk, _dtype_code(q), _stream_handle(stream))
+    if st != LDN_OK:
+        raise LdnError(st, "ldn_chunk_fwd_gdn2")
+    return out, S_final
+
+
+def decode_step_gdn2(q, k, v, erase, write, gate, S, *, out=None, stream=None):
+    """One Gated DeltaNet-2 step on torch CUDA tensors; S [B,H,dk,dv] float32 is
+    updated in place.  q, k, erase, gate [B,H,dk]; v, write [B,H,dv]."""
+    import torch
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q"); _check(k, "k", q.shape, q.dtype); _check(v, "v", (B, H, dv), q.dtype)
+    _check(erase, "erase", (B, H, dk), torch.float32); _check(write, "write", (B, H, dv), torch.float32)
+    _check(gate, "gate", (B, H, dk), torch.float32)
+    _check(S, "S", (B, H, dk, dv), torch.float32)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", (B, H, dv), q.dtype)
+    st = ldn_decode_step_gdn2(_ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(gate), _ptr(S), _ptr(out),
+                              B, H, dk, dv, _dtype_code(q), _stream_handle(stream))
+    if st != LDN_OK:
+        raise LdnError(st, "ldn_decode_step_gdn2")
     return out
 
 

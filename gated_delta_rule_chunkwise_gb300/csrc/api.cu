@@ -41,6 +41,8 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 static bool supported_dim(int d) { return d == 64 || d == 128; }
 
+// Mode LDN_GDN2 takes erase and write gates in place of beta and has entry
+// points of its own; the beta-gated entry points reject it.
 static int validate_common(int mode, int dtype, int dk, int dv)
 {
     if (mode < LDN_DELTANET || mode > LDN_KDA) return LDN_ERR_INVALID_ARG;
@@ -306,6 +308,61 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
     if (!a || !b || na == 0 || nb == 0) return false;
     const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
     return x < y + nb && y < x + na;
+}
+
+// Gated DeltaNet-2: the KDA checks with the erase gate b (shaped like k) and
+// the write gate w (shaped like v) in place of beta.
+extern "C" int ldn_chunk_fwd_gdn2(const void *q, const void *k, const void *v, const float *erase,
+                                  const float *write, const float *gate, const float *S0, void *out, float *S_final,
+                                  int B, int T, int H, int dk, int dv, int chunk, int dtype, void *stream)
+{
+    int st = validate_common(LDN_KDA, dtype, dk, dv);
+    if (st != LDN_OK) return st;
+    if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
+    if (chunk != 64) return LDN_ERR_UNSUPPORTED;
+    if ((long long)B * H > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
+    if ((long long)B * T * H * (dk > dv ? dk : dv) > (1LL << 40)) return LDN_ERR_UNSUPPORTED;
+    if ((S0 && !aligned16(S0)) || (S_final && !aligned16(S_final))) return LDN_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        if (!S_final) return LDN_OK;
+        return launch_copy_state(S0, S_final, (long long)B * H * dk * dv, s) == cudaSuccess ? LDN_OK
+                                                                                            : LDN_ERR_CUDA;
+    }
+    if (!q || !k || !v || !erase || !write || !gate || !out) return LDN_ERR_INVALID_ARG;
+    const void *vec_ptrs[] = {q, k, v, out};
+    for (const void *p : vec_ptrs)
+        if (!aligned16(p)) return LDN_ERR_INVALID_ARG;
+    if (!aligned(erase, 4) || !aligned(write, 4) || !aligned(gate, 4)) return LDN_ERR_INVALID_ARG;
+    ChunkArgs a{q, k, v, nullptr, gate, S0, out, S_final, B, T, H, dk, dv, chunk, LDN_GDN2, dtype, nullptr};
+    a.erase = erase;
+    a.write = write;
+    a.status = status_word_ptr();
+    if (!a.status) return LDN_ERR_CUDA;
+    return launch_chunk_simt(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
+extern "C" int ldn_decode_step_gdn2(const void *q, const void *k, const void *v, const float *erase,
+                                    const float *write, const float *gate, float *S, void *out,
+                                    int B, int H, int dk, int dv, int dtype, void *stream)
+{
+    int st = validate_common(LDN_KDA, dtype, dk, dv);
+    if (st != LDN_OK) return st;
+    if (B < 1 || H < 1) return LDN_ERR_INVALID_ARG;
+    if ((long long)B * H > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !erase || !write || !gate || !S || !out) return LDN_ERR_INVALID_ARG;
+    const uintptr_t el = dtype == LDN_BF16 ? 2 : 4;
+    if (!aligned16(S)) return LDN_ERR_INVALID_ARG;
+    const void *el_ptrs[] = {q, k, v, out};
+    for (const void *p : el_ptrs)
+        if (!aligned(p, el)) return LDN_ERR_INVALID_ARG;
+    if (!aligned(erase, 4) || !aligned(write, 4) || !aligned(gate, 4)) return LDN_ERR_INVALID_ARG;
+    int *sw = status_word_ptr();
+    if (!sw) return LDN_ERR_CUDA;
+    DecodeArgs a{q, k, v, nullptr, gate, S, out, B, H, dk, dv, LDN_GDN2, dtype, sw};
+    a.erase = erase;
+    a.write = write;
+    return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 
 extern "C" int ldn_prologue(const void *q_in, const void *k_in, const void *v_in, const float *conv_q,

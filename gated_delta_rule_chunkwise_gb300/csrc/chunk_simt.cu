@@ -16,6 +16,11 @@
 //   O   = P U' + (Q^ - P W) H0                     (chunk output)
 //   H1  = Diag(e^{g_C}) H0 + K~^T (U' - W H0)      (state passed on)
 // Only the last two lines depend on H0; everything else is per chunk.
+// Gated DeltaNet-2 (linear-attention notes, Sec. 2.6, Eqs. 21-24) has the same
+// form with the erase direction e = b * k in place of beta k on the row side of
+// A and in W, and the write target z = w * v in place of beta V (the write
+// direction, P, O and the state update keep k); it runs the KDA path with those
+// three substitutions made where the tiles are loaded.
 //
 // Work split: one CTA per (b, h, 32-column slice of dv); columns of H are
 // independent (state-reduction notes, Sec. 2.5).  The dk-side work (A, W, P)
@@ -45,8 +50,10 @@ __global__ void __launch_bounds__(kThreads)
 chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
                   const float *__restrict__ beta, const float *__restrict__ gate,
                   const float *S0, TIn *__restrict__ out, float *S_final,  // S0 may alias S_final
-                  int T, int H, int dv)
+                  int T, int H, int dv, const float *__restrict__ erase, const float *__restrict__ write)
 {
+    constexpr bool kG2 = MODE == LDN_GDN2;
+    constexpr bool kChan = MODE == LDN_KDA || kG2;   // per-key-channel decay
     using L = SimtSmem<DK>;
     extern __shared__ float smem[];
     float *Qs = smem;                         // [C][LDK]  Q -> Q^ -> Q^ - P W
@@ -87,14 +94,15 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
                 kv = load_in(k, i);
             }
             Qs[r * L::LDK + c] = qv;
-            Ks[r * L::LDK + c] = kv;
+            Ks[r * L::LDK + c] = (kG2 && r < Lr) ? erase[(((size_t)b * T + t0 + r) * H + h) * DK + c] * kv : kv;
             Kc[r * L::LDK + c] = kv;
         }
         for (int e = tid; e < kC * kDVS; e += kThreads) {
             const int r = e / kDVS, n = e % kDVS;
-            Vs[r * L::LDV + n] = r < Lr ? load_in(v, (((size_t)b * T + t0 + r) * H + h) * dv + col0 + n) : 0.f;
+            const size_t vi = (((size_t)b * T + t0 + r) * H + h) * dv + col0 + n;
+            Vs[r * L::LDV + n] = r < Lr ? (kG2 ? write[vi] * load_in(v, vi) : load_in(v, vi)) : 0.f;
         }
-        if (tid < kC) bs[tid] = tid < Lr ? beta[((size_t)b * T + t0 + tid) * H + h] : 0.f;
+        if (tid < kC) bs[tid] = tid < Lr ? (kG2 ? 1.f : beta[((size_t)b * T + t0 + tid) * H + h]) : 0.f;
         if (MODE == LDN_GDN && tid == 0) {
             float g = 0.f;
             for (int r = 0; r < kC; ++r) {
@@ -109,7 +117,7 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
         //    Qs = Q e^{g-m}, Ks = K e^{g-m}, Kc = K e^{m-g}; the factors of the
         //    kept (lower-triangular) products multiply to e^{g_r - g_j} <= 1
         //    while each factor stays within e^{|g_C|/2}.
-        if (MODE == LDN_KDA) {
+        if (kChan) {
             if (tid < DK) {
                 const int c = tid;
                 float g = 0.f, m = 0.f;
@@ -151,7 +159,7 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
             const int r = e / DK, c = e % DK;
             float f = bs[r];
             if (MODE == LDN_GDN) f *= expf(gr[r]);
-            if (MODE == LDN_KDA) f *= expf(gm[c]);
+            if (kChan) f *= expf(gm[c]);
             Ks[r * L::LDK + c] *= f;
         }
         for (int e = tid; e < kC * kDVS; e += kThreads) {
@@ -196,7 +204,7 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
                 Kc[r * L::LDK + c] *= fk;
             }
         }
-        if (tid < DK) gC[tid] = MODE == LDN_GDN ? expf(gr[kC - 1]) : MODE == LDN_KDA ? expf(gCl[tid]) : 1.0f;
+        if (tid < DK) gC[tid] = MODE == LDN_GDN ? expf(gr[kC - 1]) : kChan ? expf(gCl[tid]) : 1.0f;
         __syncthreads();
 
         // 7. Q~ = Q^ - P W  (row r only reads its own row of Q^).
@@ -253,7 +261,8 @@ cudaError_t launch_mode(const ChunkArgs &a, cudaStream_t st)
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDVS));
     kern<<<grid, kThreads, smem, st>>>((const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, a.beta,
-                                       a.gate, a.S0, (TIn *)a.out, a.S_final, a.T, a.H, a.dv);
+                                       a.gate, a.S0, (TIn *)a.out, a.S_final, a.T, a.H, a.dv, a.erase,
+                                       a.write);
     return cudaGetLastError();
 }
 
@@ -263,6 +272,7 @@ cudaError_t launch_dk(const ChunkArgs &a, cudaStream_t st)
     switch (a.mode) {
     case LDN_DELTANET: return launch_mode<DK, TIn, LDN_DELTANET>(a, st);
     case LDN_GDN: return launch_mode<DK, TIn, LDN_GDN>(a, st);
+    case LDN_GDN2: return launch_mode<DK, TIn, LDN_GDN2>(a, st);
     default: return launch_mode<DK, TIn, LDN_KDA>(a, st);
     }
 }

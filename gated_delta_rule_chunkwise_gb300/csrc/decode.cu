@@ -10,6 +10,9 @@
 //   H  <- H' + k r^T                              (in place)
 // Decay before the error follows the linear-attention notes, Sec. 2.4 Eqs.
 // 15-17; the KDA decay acts on the key rows of H (Sec. 2.5, Eqs. 18-20).
+// Gated DeltaNet-2 (Sec. 2.6, Eqs. 21-24) keeps the KDA decay, predicts along
+// the erase direction e = b * k (p = H'^T e) and writes z = w * v:
+// r = z - p, with no beta; the write direction and the read stay k and q.
 //
 // Work split: one CTA of 128 threads per (b, h, DVC-column slice of dv).
 // Columns are independent (each value channel is its own linear system,
@@ -33,12 +36,15 @@ template <int DK, int DVC, typename TIn, int MODE>
 __global__ void __launch_bounds__(kDecThreads)
 decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
               const float *__restrict__ beta, const float *__restrict__ gate,
-              float *__restrict__ S, TIn *__restrict__ out, int dv)
+              float *__restrict__ S, TIn *__restrict__ out, int dv,
+              const float *__restrict__ erase, const float *__restrict__ write)
 {
+    constexpr bool kG2 = MODE == LDN_GDN2;
+    constexpr bool kChan = MODE == LDN_KDA || kG2;
     constexpr int TPR = DVC / 4;               // threads per row (float4 each)
     constexpr int RP = kDecThreads / TPR;      // rows per pass
     constexpr int RPT = DK / RP;               // rows held per thread
-    __shared__ float qs[DK], ks[DK], as[DK];
+    __shared__ float qs[DK], ks[DK], as[DK], es[kG2 ? DK : 1];
     __shared__ __align__(16) float red_p[RP][DVC];
     __shared__ __align__(16) float red_s[RP][DVC];
     __shared__ __align__(16) float rs[DVC];
@@ -65,7 +71,8 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
         const float kv = load_in(k, (size_t)unit * DK + tid);
         qs[tid] = qv;
         ks[tid] = kv;
-        if (MODE == LDN_KDA) as[tid] = expf(gate[(size_t)unit * DK + tid]);
+        if (kChan) as[tid] = expf(gate[(size_t)unit * DK + tid]);
+        if (kG2) es[tid] = erase[(size_t)unit * DK + tid] * kv;
         kq = qv * kv;
     }
 #pragma unroll
@@ -78,9 +85,9 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int row = rg + i * RP;
-        const float d = (MODE == LDN_KDA) ? as[row] : alpha;
+        const float d = kChan ? as[row] : alpha;
         if (MODE != LDN_DELTANET) { h[i].x *= d; h[i].y *= d; h[i].z *= d; h[i].w *= d; }
-        const float kr = ks[row], qr = qs[row];
+        const float kr = kG2 ? es[row] : ks[row], qr = qs[row];
         p.x += h[i].x * kr; p.y += h[i].y * kr; p.z += h[i].z * kr; p.w += h[i].w * kr;
         s.x += h[i].x * qr; s.y += h[i].y * qr; s.z += h[i].z * qr; s.w += h[i].w * qr;
     }
@@ -95,7 +102,7 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
 #pragma unroll
         for (int w = 0; w < kDecThreads / 32; ++w) kqt += kq_part[w];
         const size_t vi = (size_t)unit * dv + col0 + tid;
-        const float r = beta[unit] * (load_in(v, vi) - pp);
+        const float r = kG2 ? write[vi] * load_in(v, vi) - pp : beta[unit] * (load_in(v, vi) - pp);
         rs[tid] = r;
         store_out(out, vi, ss + r * kqt);
     }
@@ -117,15 +124,20 @@ cudaError_t launch_cfg(const DecodeArgs &a, cudaStream_t st)
     const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / DVC));
     const TIn *q = (const TIn *)a.q, *k = (const TIn *)a.k, *v = (const TIn *)a.v;
     TIn *o = (TIn *)a.out;
+    const float *eb = a.erase, *wb = a.write;
     switch (a.mode) {
     case LDN_DELTANET:
-        decode_kernel<DK, DVC, TIn, LDN_DELTANET><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        decode_kernel<DK, DVC, TIn, LDN_DELTANET><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv,
+                                                                                 eb, wb);
         break;
     case LDN_GDN:
-        decode_kernel<DK, DVC, TIn, LDN_GDN><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        decode_kernel<DK, DVC, TIn, LDN_GDN><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv, eb, wb);
+        break;
+    case LDN_GDN2:
+        decode_kernel<DK, DVC, TIn, LDN_GDN2><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv, eb, wb);
         break;
     default:
-        decode_kernel<DK, DVC, TIn, LDN_KDA><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv);
+        decode_kernel<DK, DVC, TIn, LDN_KDA><<<grid, kDecThreads, 0, st>>>(q, k, v, a.beta, a.gate, a.S, o, a.dv, eb, wb);
         break;
     }
     return cudaGetLastError();

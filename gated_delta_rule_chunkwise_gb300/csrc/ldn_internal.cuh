@@ -20,6 +20,7 @@ struct ChunkArgs {
     float *S_final;
     int B, T, H, dk, dv, chunk, mode, dtype;
     int *status;
+    const float *erase = nullptr, *write = nullptr;   // Gated DeltaNet-2: b [B][T][H][dk], w [B][T][H][dv]
 };
 
 struct DecodeArgs {
@@ -29,6 +30,7 @@ struct DecodeArgs {
     void *out;
     int B, H, dk, dv, mode, dtype;
     int *status;
+    const float *erase = nullptr, *write = nullptr;   // Gated DeltaNet-2: b [B][H][dk], w [B][H][dv]
 };
 
 // Prologue / epilogue around the chunkwise path (prologue.cu).

@@ -13,6 +13,11 @@ Recipe (every named workload):
     KDA log-decay g = -softplus(N(0, 1) + b_h) * 0.1 per (b, t, h, c) with one
     b_h ~ N(0, 0.5^2) per head (0.5 read as the standard deviation);
   * S0 ~ N(0, 0.02^2) where the workload has a nonzero initial state, else none;
+  * Gated DeltaNet-2 draws everything KDA draws (its beta is then dropped), the
+    same per-channel log-decay, and after S0 an erase gate b = sigmoid(N(0, 1))
+    per (b, t, h, c) and a write gate w = sigmoid(N(0, 1)) per (b, t, h, i):
+    gates in (0, 1) like beta, the plainest reading of the notes' channel-wise
+    gates (they fix no range);
   * for bf16 workloads q, k, v are rounded to bf16 (round to nearest even)
     AFTER normalisation; beta, gates and states stay fp32.
 Arrays are returned as float32 numpy arrays holding exactly the values the
@@ -25,7 +30,7 @@ from typing import Optional
 
 import numpy as np
 
-MODE_DELTANET, MODE_GDN, MODE_KDA = 0, 1, 2
+MODE_DELTANET, MODE_GDN, MODE_KDA, MODE_GDN2 = 0, 1, 2, 3
 
 # name -> recipe.  Sizes are the benchmark workloads; tests shrink them with overrides.
 CHUNK_WORKLOADS = {
@@ -35,10 +40,13 @@ CHUNK_WORKLOADS = {
     "gdn_bf16_long_b1_t8192_h16_d128": dict(mode=MODE_GDN, dtype="bf16", B=1, T=8192, H=16, dk=128, dv=128, s0=True),
     "gdn_bf16_long_b1_t32768_h16_d128": dict(mode=MODE_GDN, dtype="bf16", B=1, T=32768, H=16, dk=128, dv=128, s0=True),
     "gdn_bf16_long_b1_t65536_h16_d128": dict(mode=MODE_GDN, dtype="bf16", B=1, T=65536, H=16, dk=128, dv=128, s0=True),
+    "gdn2_bf16_b8_t4096_h16_d128": dict(mode=MODE_GDN2, dtype="bf16", B=8, T=4096, H=16, dk=128, dv=128, s0=False),
 }
 DECODE_WORKLOADS = {
     "gdn_decode_b64_h16_dk128_dv128_steps1000": dict(mode=MODE_GDN, dtype="f32", B=64, H=16, dk=128, dv=128, steps=1000),
     "gdn_decode_b64_h16_dk64_dv128_steps1000": dict(mode=MODE_GDN, dtype="f32", B=64, H=16, dk=64, dv=128, steps=1000),
+    "gdn2_decode_b64_h16_dk128_dv128_steps1000": dict(mode=MODE_GDN2, dtype="f32", B=64, H=16, dk=128, dv=128,
+                                                      steps=1000),
 }
 
 
@@ -75,11 +83,13 @@ class Workload:
     q: np.ndarray           # chunk: [B,T,H,dk]   decode: [steps,B,H,dk]
     k: np.ndarray
     v: np.ndarray
-    beta: np.ndarray
+    beta: Optional[np.ndarray]   # None for Gated DeltaNet-2
     gate: Optional[np.ndarray]
     S0: Optional[np.ndarray]  # [B,H,dk,dv]
     chunk: int = 64
     decode: bool = False
+    erase: Optional[np.ndarray] = None   # Gated DeltaNet-2: erase gate, shaped like k
+    write: Optional[np.ndarray] = None   # Gated DeltaNet-2: write gate, shaped like v
 
     @property
     def tokens(self) -> int:
@@ -91,7 +101,8 @@ class Workload:
         el = torch.bfloat16 if self.dtype == "bf16" else torch.float32
         cv = lambda a, dt: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dt)
         return dict(q=cv(self.q, el), k=cv(self.k, el), v=cv(self.v, el), beta=cv(self.beta, torch.float32),
-                    gate=cv(self.gate, torch.float32), S0=cv(self.S0, torch.float32))
+                    gate=cv(self.gate, torch.float32), S0=cv(self.S0, torch.float32),
+                    erase=cv(self.erase, torch.float32), write=cv(self.write, torch.float32))
 
 
 def _draw(rng, lead, mode, dtype, H, dk, dv, s0, B):
@@ -101,17 +112,21 @@ def _draw(rng, lead, mode, dtype, H, dk, dv, s0, B):
     k = _l2norm(rng.standard_normal((*lead, H, dk), dtype=f32))
     v = rng.standard_normal((*lead, H, dv), dtype=f32)
     beta = _sigmoid(rng.standard_normal((*lead, H), dtype=f32))
-    gate = None
+    gate = erase = write = None
     if mode == MODE_GDN:
         gate = (-_softplus(rng.standard_normal((*lead, H), dtype=f32)) * f32(0.1)).astype(f32)
-    elif mode == MODE_KDA:
+    elif mode in (MODE_KDA, MODE_GDN2):
         noise = rng.standard_normal((*lead, H, dk), dtype=f32)
         b_h = (rng.standard_normal(H, dtype=f32) * f32(0.5)).astype(f32)
         gate = (-_softplus(noise + b_h[:, None]) * f32(0.1)).astype(f32)
     S0 = (rng.standard_normal((B, H, dk, dv), dtype=f32) * f32(0.02)).astype(f32) if s0 else None
+    if mode == MODE_GDN2:
+        erase = _sigmoid(rng.standard_normal((*lead, H, dk), dtype=f32))
+        write = _sigmoid(rng.standard_normal((*lead, H, dv), dtype=f32))
+        beta = None
     if dtype == "bf16":
         q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)
-    return q, k, v, beta, gate, S0
+    return q, k, v, beta, gate, S0, erase, write
 
 
 def make_chunk(name: str = "gdn_bf16_b4_t2048_h16_d128", seed: int = 0, **over) -> Workload:
@@ -119,10 +134,10 @@ def make_chunk(name: str = "gdn_bf16_b4_t2048_h16_d128", seed: int = 0, **over) 
     dtype, s0) shrink or vary it while keeping the recipe."""
     r = dict(CHUNK_WORKLOADS[name]); r.update(over)
     rng = np.random.default_rng(seed)
-    q, k, v, beta, gate, S0 = _draw(rng, (r["B"], r["T"]), r["mode"], r["dtype"], r["H"], r["dk"],
-                                    r["dv"], r["s0"], r["B"])
+    q, k, v, beta, gate, S0, erase, write = _draw(rng, (r["B"], r["T"]), r["mode"], r["dtype"], r["H"], r["dk"],
+                                                  r["dv"], r["s0"], r["B"])
     return Workload(name=name, mode=r["mode"], dtype=r["dtype"], B=r["B"], T=r["T"], H=r["H"],
-                    dk=r["dk"], dv=r["dv"], q=q, k=k, v=v, beta=beta, gate=gate, S0=S0)
+                    dk=r["dk"], dv=r["dv"], q=q, k=k, v=v, beta=beta, gate=gate, S0=S0, erase=erase, write=write)
 
 
 def make_decode(name: str = "gdn_decode_b64_h16_dk128_dv128_steps1000", seed: int = 0, **over) -> Workload:
@@ -130,10 +145,11 @@ def make_decode(name: str = "gdn_decode_b64_h16_dk128_dv128_steps1000", seed: in
     [steps, B, H, .] in one go, from a random S0 ~ N(0, 0.02^2)."""
     r = dict(DECODE_WORKLOADS[name]); r.update(over)
     rng = np.random.default_rng(seed)
-    q, k, v, beta, gate, S0 = _draw(rng, (r["steps"], r["B"]), r["mode"], r["dtype"], r["H"], r["dk"],
-                                    r["dv"], True, r["B"])
+    q, k, v, beta, gate, S0, erase, write = _draw(rng, (r["steps"], r["B"]), r["mode"], r["dtype"], r["H"],
+                                                  r["dk"], r["dv"], True, r["B"])
     return Workload(name=name, mode=r["mode"], dtype=r["dtype"], B=r["B"], T=r["steps"], H=r["H"],
-                    dk=r["dk"], dv=r["dv"], q=q, k=k, v=v, beta=beta, gate=gate, S0=S0, decode=True)
+                    dk=r["dk"], dv=r["dv"], q=q, k=k, v=v, beta=beta, gate=gate, S0=S0, decode=True,
+                    erase=erase, write=write)
 
 
 # ---- prologue / epilogue inputs ------------------------------------------------

@@ -48,9 +48,11 @@
 extern "C" {
 #endif
 
-#define LDN_VERSION 3
+#define LDN_VERSION 4
 
-typedef enum { LDN_DELTANET = 0, LDN_GDN = 1, LDN_KDA = 2 } ldn_mode;
+/* LDN_GDN2 (Gated DeltaNet-2) is taken only by the *_gdn2 entry points, which
+ * carry its two gates; every beta-gated entry point rejects it. */
+typedef enum { LDN_DELTANET = 0, LDN_GDN = 1, LDN_KDA = 2, LDN_GDN2 = 3 } ldn_mode;
 
 /* Element type of q, k, v and out.  beta, gate and every state are fp32. */
 typedef enum { LDN_F32 = 0, LDN_BF16 = 1 } ldn_dtype;
@@ -262,6 +264,42 @@ int ldn_rmsnorm_gated(const void *o, const void *g, const float *weight, void *y
 int ldn_decode_step(const void *q, const void *k, const void *v, const float *beta,
                     const float *gate, float *S, void *out,
                     int B, int H, int dk, int dv, int mode, int dtype, void *stream);
+
+/*
+ * Gated DeltaNet-2 (linear-attention notes, Sec. 2.6, Eqs. 21-24): the erase
+ * and the write of the delta rule get gates of their own in place of the one
+ * beta, both channel-wise, on top of the KDA per-key-channel decay:
+ *   S_t = S_{t-1} Diag(a_t) (I - e_t k_t^T) + z_t k_t^T,   e_t = b_t * k_t,
+ *   z_t = w_t * v_t (element-wise),   o_t = S_t q_t.
+ * The prediction is taken along e_t, the write goes along k_t.  With
+ * b_t = beta_t 1 and w_t = beta_t 1 it is KDA.  Gate values are used as given
+ * (the library applies no sigmoid to them).
+ *
+ * ldn_chunk_fwd_gdn2 -- chunkwise forward of that recurrence over a whole
+ * sequence (the chunk form of ldn_chunk_fwd with e_t in place of beta_t k_t on
+ * the prediction side and z_t in place of beta_t v_t; fp32 CUDA-core kernel).
+ *   q, k     [B][T][H][dk] dtype      v, out [B][T][H][dv] dtype
+ *   erase    [B][T][H][dk] fp32       write  [B][T][H][dv] fp32
+ *   gate     [B][T][H][dk] fp32 (log a_t)
+ *   S0, S_final, B, T, H, dk, dv, chunk, dtype, alignment (q, k, v, out, S0,
+ *   S_final 16-byte; erase, write, gate 4-byte), T = 0 and errors as for
+ *   ldn_chunk_fwd.
+ */
+int ldn_chunk_fwd_gdn2(const void *q, const void *k, const void *v, const float *erase, const float *write,
+                       const float *gate, const float *S0, void *out, float *S_final, int B, int T, int H,
+                       int dk, int dv, int chunk, int dtype, void *stream);
+
+/*
+ * ldn_decode_step_gdn2 -- one Gated DeltaNet-2 step for every (b, h), state
+ * updated in place: S' = S Diag(a), p = S' e, s = S' q, r = z - p,
+ * o = s + r (k^T q), S <- S' + r k^T.
+ *   q, k, erase, gate [B][H][dk]      v, out, write [B][H][dv]
+ *   (q, k, v, out of dtype; erase, write, gate fp32 4-byte aligned)
+ *   S [B][H][dk][dv] fp32 16-byte aligned; B, H >= 1; dk, dv in {64, 128}.
+ */
+int ldn_decode_step_gdn2(const void *q, const void *k, const void *v, const float *erase, const float *write,
+                         const float *gate, float *S, void *out, int B, int H, int dk, int dv, int dtype,
+                         void *stream);
 
 /* Synchronises `stream`, then reads and clears the device status word on the
  * current device.  Returns LDN_OK, LDN_ERR_TIMEOUT (a kernel abandoned a

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert ldn.ldn_version() == 3
+    assert ldn.ldn_version() == 4
     for st in range(5):
         assert isinstance(ldn.ldn_status_string(st), str) and ldn.ldn_status_string(st)
     assert "unknown" in ldn.ldn_status_string(99)
@@ -107,6 +107,65 @@ def _decode(**kw):
 ])
 def test_decode_rejects_bad_arguments(lib, kw, want):
     assert _decode(**kw) == want
+
+
+def _chunk_gdn2(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, erase=FAKE, write=FAKE, gate=FAKE, S0=None, out=FAKE, S_final=None,
+             B=1, T=64, H=1, dk=64, dv=64, chunk=64, dtype=1, stream=None)
+    a.update(kw)
+    return ldn.ldn_chunk_fwd_gdn2(a["q"], a["k"], a["v"], a["erase"], a["write"], a["gate"], a["S0"], a["out"],
+                                  a["S_final"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"], a["dtype"],
+                                  a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(erase=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(write=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None), ldn.LDN_ERR_INVALID_ARG),            # the decay is part of the rule
+    (dict(out=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 4), ldn.LDN_ERR_INVALID_ARG),
+    (dict(S_final=FAKE + 8), ldn.LDN_ERR_INVALID_ARG),
+    (dict(erase=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(write=FAKE + 1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dtype=5), ldn.LDN_ERR_INVALID_ARG),
+    (dict(B=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(T=-1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dk=96), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(chunk=128), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(T=0, q=None, erase=None, write=None, gate=None, out=None), ldn.LDN_OK),   # no state asked: nothing to do
+])
+def test_chunk_gdn2_rejects_bad_arguments(lib, kw, want):
+    assert _chunk_gdn2(**kw) == want
+
+
+def _decode_gdn2(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, erase=FAKE, write=FAKE, gate=FAKE, S=FAKE, out=FAKE, B=1, H=1, dk=64,
+             dv=64, dtype=0, stream=None)
+    a.update(kw)
+    return ldn.ldn_decode_step_gdn2(a["q"], a["k"], a["v"], a["erase"], a["write"], a["gate"], a["S"], a["out"],
+                                    a["B"], a["H"], a["dk"], a["dv"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(S=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(erase=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(write=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(S=FAKE + 4), ldn.LDN_ERR_INVALID_ARG),
+    (dict(k=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(write=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(H=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dv=256), ldn.LDN_ERR_UNSUPPORTED),
+])
+def test_decode_gdn2_rejects_bad_arguments(lib, kw, want):
+    assert _decode_gdn2(**kw) == want
+
+
+def test_beta_gated_entry_points_reject_the_gdn2_mode(lib):
+    assert _decode(mode=ldn.LDN_GDN2) == ldn.LDN_ERR_INVALID_ARG
+    assert _chunk(mode=ldn.LDN_GDN2) == ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_chunk_fwd_select(64, 64, 64, ldn.LDN_GDN2, 1) == -ldn.LDN_ERR_INVALID_ARG
 
 
 def test_binding_without_library_fails_loudly(tmp_path, monkeypatch):

@@ -43,7 +43,7 @@ def test_decode_parity(mode, dtype, dk, dv):
     assert rel_err(S, rs) <= TOL[dtype]
 
 
-@pytest.mark.parametrize("name", sorted(wl.DECODE_WORKLOADS))
+@pytest.mark.parametrize("name", sorted(n for n, r in wl.DECODE_WORKLOADS.items() if r["mode"] != wl.MODE_GDN2))
 def test_decode_full_1000_steps_sampled(name):
     """Full batch 64 x 16 heads, 1000 consecutive tokens; sampled heads vs the oracle."""
     w = wl.make_decode(name)

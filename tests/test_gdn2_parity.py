@@ -1,0 +1,130 @@
+"""GPU parity of the Gated DeltaNet-2 entry points (ldn_chunk_fwd_gdn2,
+ldn_decode_step_gdn2) against the fp64 oracle, element by element, with the
+tolerances of the other modes: max|gpu - oracle| / RMS(oracle) within 1e-4 for
+fp32 inputs and 2e-2 for bf16 inputs (fp32 state).  Sizes span several
+64-token chunks and a ragged tail."""
+import numpy as np
+import pytest
+
+import gated_delta_rule_chunkwise_gb300 as ldn
+from gated_delta_rule_chunkwise_gb300 import workloads as wl
+from tests._helpers import TOL, out_err, rel_err
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+CHUNK = "gdn2_bf16_b8_t4096_h16_d128"
+DECODE = "gdn2_decode_b64_h16_dk128_dv128_steps1000"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gated_delta_rule_chunkwise_gb300 import build
+    build.build()
+    ldn.load()
+
+
+def run_chunk(w, S0=True):
+    import torch
+    t = w.torch_inputs("cuda")
+    out, sf = ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], t["erase"], t["write"], t["gate"], t["S0"] if S0 else None)
+    assert ldn.device_status() == ldn.LDN_OK
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), sf.cpu().numpy()
+
+
+def check_chunk(w):
+    o, s = run_chunk(w)
+    ro, rs = oracle.fwd_gdn2(w.q, w.k, w.v, w.erase, w.write, w.gate, w.S0)
+    eo, es = out_err(o, ro, w.dtype), rel_err(s, rs)
+    assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], f"out {eo:.3g} state {es:.3g}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_chunk_parity_dtypes_dims(dtype, dk, dv):
+    check_chunk(wl.make_chunk(CHUNK, B=2, T=200, H=3, dk=dk, dv=dv, dtype=dtype, s0=True))
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 129])
+def test_chunk_parity_lengths(T):
+    check_chunk(wl.make_chunk(CHUNK, B=1, T=T, H=2, s0=(T % 2 == 1)))
+
+
+def test_chunk_with_both_gates_beta_matches_the_kda_kernel():
+    """b = beta 1 and w = beta 1 turn the rule into KDA: the GDN2 entry point must
+    agree with the KDA path of ldn_chunk_fwd (SIMT kernel) on the same inputs."""
+    import torch
+    k = wl.make_chunk("kda_bf16_b8_t4096_h16_d128", B=2, T=150, H=2, dtype="f32", s0=True)
+    t = k.torch_inputs("cuda")
+    erase = t["beta"][..., None].expand(*t["beta"].shape, k.dk).contiguous()
+    write = t["beta"][..., None].expand(*t["beta"].shape, k.dv).contiguous()
+    o2, s2 = ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], erase, write, t["gate"], t["S0"])
+    ok, sk = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"], mode=ldn.LDN_KDA,
+                           variant=ldn.LDN_VARIANT_SIMT)
+    torch.cuda.synchronize()
+    assert rel_err(o2.cpu().numpy(), ok.cpu().numpy()) <= 1e-5
+    assert rel_err(s2.cpu().numpy(), sk.cpu().numpy()) <= 1e-5
+
+
+def test_chunk_erase_off_is_additive():
+    """b = 0: nothing is erased, the state only decays and accumulates w v k^T."""
+    w = wl.make_chunk(CHUNK, B=1, T=130, H=2, dtype="f32", s0=True)
+    w.erase = np.zeros_like(w.erase)
+    check_chunk(w)
+
+
+def test_chunk_zero_length_copies_state():
+    import torch
+    w = wl.make_chunk(CHUNK, B=2, T=3, H=2, s0=True)
+    t = w.torch_inputs("cuda")
+    S_final = torch.full_like(t["S0"], 7.0)
+    st = ldn.ldn_chunk_fwd_gdn2(0, 0, 0, 0, 0, 0, t["S0"].data_ptr(), 0, S_final.data_ptr(), 2, 0, 2, 128, 128,
+                                64, 1, torch.cuda.current_stream().cuda_stream)
+    assert st == ldn.LDN_OK
+    torch.cuda.synchronize()
+    assert torch.equal(S_final, t["S0"])
+
+
+def test_chunk_full_workload_sampled():
+    """B=8, T=4096, H=16, d=128 bf16 in one call; sampled (b, h) against the oracle."""
+    w = wl.make_chunk(CHUNK)
+    o, s = run_chunk(w, S0=False)
+    for b, h in [(0, 0), (5, 11), (7, 15)]:
+        sl = lambda a: a[b:b + 1, :, h:h + 1]
+        ro, rs = oracle.fwd_gdn2(sl(w.q), sl(w.k), sl(w.v), sl(w.erase), sl(w.write), sl(w.gate), None)
+        assert out_err(o[b:b + 1, :, h:h + 1], ro, "bf16") <= TOL["bf16"]
+        assert rel_err(s[b:b + 1, h:h + 1], rs) <= TOL["bf16"]
+
+
+def run_decode(w):
+    import torch
+    t = w.torch_inputs("cuda")
+    S = t["S0"].clone()
+    outs = [ldn.decode_step_gdn2(t["q"][i], t["k"][i], t["v"][i], t["erase"][i], t["write"][i], t["gate"][i], S)
+            for i in range(w.T)]
+    assert ldn.device_status() == ldn.LDN_OK
+    return torch.stack(outs).float().cpu().numpy(), S.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (64, 64), (128, 64)])
+def test_decode_parity(dtype, dk, dv):
+    w = wl.make_decode(DECODE, B=3, H=5, dk=dk, dv=dv, steps=24, dtype=dtype)
+    o, S = run_decode(w)
+    ro, rs = oracle.decode_gdn2(w.q, w.k, w.v, w.erase, w.write, w.gate, w.S0)
+    assert out_err(o, ro, dtype) <= TOL[dtype]
+    assert rel_err(S, rs) <= TOL[dtype]
+
+
+def test_decode_full_1000_steps_sampled():
+    """B=64 x H=16, 1000 consecutive tokens; sampled heads against the oracle."""
+    w = wl.make_decode(DECODE)
+    o, S = run_decode(w)
+    for b, h in [(0, 0), (17, 9), (63, 15)]:
+        sl = lambda a: a[:, b:b + 1, h:h + 1]
+        ro, rs = oracle.decode_gdn2(sl(w.q), sl(w.k), sl(w.v), sl(w.erase), sl(w.write), sl(w.gate),
+                                    w.S0[b:b + 1, h:h + 1])
+        assert rel_err(o[:, b:b + 1, h:h + 1], ro) <= TOL["f32"]
+        assert rel_err(S[b:b + 1, h:h + 1], rs) <= TOL["f32"]
+    assert np.all(np.isfinite(o))

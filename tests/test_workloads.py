@@ -40,3 +40,15 @@ def test_decode_recipe():
     d = wl.make_decode("gdn_decode_b64_h16_dk64_dv128_steps1000", B=2, H=3, steps=5)
     assert d.q.shape == (5, 2, 3, 64) and d.v.shape == (5, 2, 3, 128)
     assert d.gate.shape == (5, 2, 3) and d.S0.shape == (2, 3, 64, 128)
+
+
+def test_gdn2_recipe():
+    w = wl.make_chunk("gdn2_bf16_b8_t4096_h16_d128", B=2, T=5, H=3, dk=64, dv=128)
+    assert w.beta is None and w.erase.shape == (2, 5, 3, 64) and w.write.shape == (2, 5, 3, 128)
+    assert np.all((w.erase > 0) & (w.erase < 1)) and np.all((w.write > 0) & (w.write < 1))
+    assert w.gate.shape == (2, 5, 3, 64) and np.all(w.gate < 0)
+    kda = wl.make_chunk("kda_bf16_b8_t4096_h16_d128", B=2, T=5, H=3, dk=64, dv=128)
+    np.testing.assert_array_equal(w.q, kda.q)          # same draws up to the extra gates
+    np.testing.assert_array_equal(w.gate, kda.gate)
+    d = wl.make_decode("gdn2_decode_b64_h16_dk128_dv128_steps1000", B=2, H=3, steps=4)
+    assert d.erase.shape == (4, 2, 3, 128) and d.write.shape == (4, 2, 3, 128) and d.beta is None
