@@ -411,13 +411,14 @@ def run_ours(args):
 
             ows_bytes = 0 if g2 else ldn.ldn_chunk_fwd_workspace_size(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt)
             ows = torch.empty(max(ows_bytes, 256), dtype=torch.uint8, device="cuda")
-            ochosen = ldn.LDN_VARIANT_SIMT if g2 else ldn.ldn_chunk_fwd_select_ws(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64,
-                                                                                   ow.mode, odt, ows_bytes)
+            ochosen = ldn.ldn_chunk_fwd_select_ws(ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt,
+                                                  (1 << 64) - 1 if g2 else ows_bytes)
 
             def ostep():
                 if g2:
                     st_ = ldn.ldn_chunk_fwd_gdn2(optr[0], optr[1], optr[2], P(ot["erase"]), P(ot["write"]), optr[4],
-                                                 optr[5], optr[6], optr[7], ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, odt, sh)
+                                                 optr[5], optr[6], optr[7], ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, odt,
+                                                 ldn.LDN_VARIANT_AUTO, sh)
                 else:
                     st_ = ldn.ldn_chunk_fwd_ws(*optr, ow.B, ow.T, ow.H, ow.dk, ow.dv, 64, ow.mode, odt,
                                                ldn.LDN_VARIANT_AUTO, ows.data_ptr(), ows_bytes, sh)

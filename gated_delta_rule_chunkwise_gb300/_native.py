@@ -54,7 +54,7 @@ _SIGNATURES = {
     "ldn_chunk_fwd_select_ws": ([_I] * 8 + [ctypes.c_size_t], _I),
     "ldn_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 9 + [_P], _I),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
-    "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 7 + [_P], _I),
+    "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 8 + [_P], _I),
     "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
     "ldn_rmsnorm_gated": ([_P] * 4 + [_I] * 5 + [ctypes.c_float, _P], _I),
@@ -127,9 +127,10 @@ def ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stre
     return load().ldn_decode_step(q, k, v, beta, gate, S, out, B, H, dk, dv, mode, dtype, stream)
 
 
-def ldn_chunk_fwd_gdn2(q, k, v, erase, write, gate, S0, out, S_final, B, T, H, dk, dv, chunk, dtype, stream):
+def ldn_chunk_fwd_gdn2(q, k, v, erase, write, gate, S0, out, S_final, B, T, H, dk, dv, chunk, dtype, variant,
+                       stream):
     return load().ldn_chunk_fwd_gdn2(q, k, v, erase, write, gate, S0, out, S_final, B, T, H, dk, dv, chunk,
-                                     dtype, stream)
+                                     dtype, variant, stream)
 
 
 def ldn_decode_step_gdn2(q, k, v, erase, write, gate, S, out, B, H, dk, dv, dtype, stream):
@@ -280,7 +281,7 @@ def decode_step(q, k, v, beta, gate, S, *, mode, out=None, stream=None):
 
 
 def chunk_fwd_gdn2(q, k, v, erase, write, gate, S0=None, *, chunk=64, out=None, S_final=None, want_state=True,
-                   stream=None):
+                   variant=LDN_VARIANT_AUTO, stream=None):
     """Gated DeltaNet-2 chunkwise forward on torch CUDA tensors (ldn_chunk_fwd_gdn2).
 
     q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16); erase, gate [B,T,H,dk]
@@ -300,7 +301,7 @@ def chunk_fwd_gdn2(q, k, v, erase, write, gate, S0=None, *, chunk=64, out=None, 
         S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     _check(S_final, "S_final", (B, H, dk, dv), torch.float32)
     st = ldn_chunk_fwd_gdn2(_ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(gate), _ptr(S0), _ptr(out),
-                            _ptr(S_final), B, T, H, dk, dv, chunk, _dtype_code(q), _stream_handle(stream))
+                            _ptr(S_final), B, T, H, dk, dv, chunk, _dtype_code(q), variant, _stream_handle(stream))
     if st != LDN_OK:
         raise LdnError(st, "ldn_chunk_fwd_gdn2")
     return out, S_final

@@ -42,10 +42,10 @@ static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)
 static bool supported_dim(int d) { return d == 64 || d == 128; }
 
 // Mode LDN_GDN2 takes erase and write gates in place of beta and has entry
-// points of its own; the beta-gated entry points reject it.
-static int validate_common(int mode, int dtype, int dk, int dv)
+// points of its own (g2 = true); the beta-gated entry points reject it.
+static int validate_common(int mode, int dtype, int dk, int dv, bool g2 = false)
 {
-    if (mode < LDN_DELTANET || mode > LDN_KDA) return LDN_ERR_INVALID_ARG;
+    if (g2 ? mode != LDN_GDN2 : (mode < LDN_DELTANET || mode > LDN_KDA)) return LDN_ERR_INVALID_ARG;
     if (dtype != LDN_F32 && dtype != LDN_BF16) return LDN_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1) return LDN_ERR_INVALID_ARG;
     if (!supported_dim(dk) || !supported_dim(dv)) return LDN_ERR_UNSUPPORTED;
@@ -53,23 +53,29 @@ static int validate_common(int mode, int dtype, int dk, int dv)
 }
 
 // Workspace bytes of the split variant (0: it does not take these sizes).
+// (Pointers are taken as aligned: a Gated DeltaNet-2 call gets stand-in gates here.)
 static size_t split_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)
 {
     if (T < 1 || B < 1 || H < 1) return 0;
+    alignas(16) static const float kAligned[4] = {0.f, 0.f, 0.f, 0.f};
     ChunkArgs a{};
     a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = B; a.T = T; a.H = H;
+    a.erase = a.write = kAligned;
     if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return 0;
     return (size_t)B * H * (size_t)((T + chunk - 1) / chunk) * split_unit_bytes(dv);
 }
 
 // Argument checks shared by the chunk entry points (everything but the
 // workspace).  On LDN_OK, *tc says whether the tensor-core kernels take the call.
+// Gated DeltaNet-2 (mode LDN_GDN2) passes its erase and write gates, beta unused.
 static int check_chunk_args(const void *q, const void *k, const void *v, const float *beta, const float *gate,
                             const float *S0, const void *out, const float *S_final, int B, int T, int H, int dk,
-                            int dv, int chunk, int mode, int dtype, int variant, bool *tc)
+                            int dv, int chunk, int mode, int dtype, int variant, bool *tc,
+                            const float *erase = nullptr, const float *write = nullptr)
 {
     *tc = false;
-    int st = validate_common(mode, dtype, dk, dv);
+    const bool g2 = mode == LDN_GDN2;
+    int st = validate_common(mode, dtype, dk, dv, g2 && erase && write);
     if (st != LDN_OK) return st;
     if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
     if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_PAIR) return LDN_ERR_INVALID_ARG;
@@ -83,16 +89,19 @@ static int check_chunk_args(const void *q, const void *k, const void *v, const f
         if (S_final && !aligned16(S_final)) return LDN_ERR_INVALID_ARG;
         return LDN_OK;
     }
-    if (!q || !k || !v || !beta || !out) return LDN_ERR_INVALID_ARG;
+    if (!q || !k || !v || (!g2 && !beta) || !out) return LDN_ERR_INVALID_ARG;
     if (mode != LDN_DELTANET && !gate) return LDN_ERR_INVALID_ARG;
+    if (g2 && (!aligned(erase, 4) || !aligned(write, 4))) return LDN_ERR_INVALID_ARG;
     // Tiles of q, k, v, out and the states move in 16-byte vectors (TMA,
     // float4); beta and gates are read as scalars.
     const void *vec_ptrs[] = {q, k, v, S0, out, S_final};
     for (const void *p : vec_ptrs)
         if (p && !aligned16(p)) return LDN_ERR_INVALID_ARG;
-    if (!aligned(beta, 4) || (gate && !aligned(gate, 4))) return LDN_ERR_INVALID_ARG;
+    if ((!g2 && !aligned(beta, 4)) || (gate && !aligned(gate, 4))) return LDN_ERR_INVALID_ARG;
     ChunkArgs a{};
     a.gate = mode == LDN_DELTANET ? nullptr : gate;
+    a.erase = erase;
+    a.write = write;
     a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype;
     *tc = dtype == LDN_BF16 && chunk_tc_supported(a);
     if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT || variant == LDN_VARIANT_PAIR) && !*tc)
@@ -103,11 +112,12 @@ static int check_chunk_args(const void *q, const void *k, const void *v, const f
 
 static int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *beta, const float *gate,
                           const float *S0, void *out, float *S_final, int B, int T, int H, int dk, int dv,
-                          int chunk, int mode, int dtype, int variant, void *ws, size_t ws_bytes, void *stream)
+                          int chunk, int mode, int dtype, int variant, void *ws, size_t ws_bytes, void *stream,
+                          const float *erase = nullptr, const float *write = nullptr)
 {
     bool tc = false;
     const int st = check_chunk_args(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
-                                    variant, &tc);
+                                    variant, &tc, erase, write);
     if (st != LDN_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (T == 0) {
@@ -117,6 +127,8 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     }
     ChunkArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S0, out, S_final,
                 B, T, H, dk, dv, chunk, mode, dtype, nullptr};
+    a.erase = erase;
+    a.write = write;
     const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype) : 0;
     const bool ws_ok = ws && aligned(ws, 256) && need > 0 && ws_bytes >= need;
     if (variant == LDN_VARIANT_AUTO) variant = !tc ? LDN_VARIANT_SIMT : chunk_tc_pick(a, ws_ok);
@@ -155,30 +167,31 @@ extern "C" int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, con
 // sequence fits, else chunk-aligned runs of tokens of one sequence, the state
 // carried from run to run through S_final (or, without one, a state slot at
 // the top of the scratch).  Pieces run in stream order and reuse the scratch.
-extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *beta,
-                                     const float *gate, const float *S0, void *out, float *S_final,
-                                     int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
-                                     int variant, void *stream)
+static int noalloc_impl(const void *q, const void *k, const void *v, const float *beta, const float *gate,
+                        const float *S0, void *out, float *S_final, int B, int T, int H, int dk, int dv, int chunk,
+                        int mode, int dtype, int variant, void *stream, const float *erase, const float *write)
 {
     if (variant != LDN_VARIANT_AUTO && variant != LDN_VARIANT_SPLIT)
         return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
-                              variant, nullptr, 0, stream);
+                              variant, nullptr, 0, stream, erase, write);
     bool tc = false;
     int st = check_chunk_args(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
-                              variant, &tc);
+                              variant, &tc, erase, write);
     if (st != LDN_OK) return st;
     if (T == 0 || !tc)   // state copy, or the SIMT kernel: no scratch
         return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
-                              LDN_VARIANT_AUTO, nullptr, 0, stream);
+                              LDN_VARIANT_AUTO, nullptr, 0, stream, erase, write);
     ChunkArgs whole{};
     whole.gate = mode == LDN_DELTANET ? nullptr : gate;
+    whole.erase = erase;
+    whole.write = write;
     whole.B = B; whole.T = T; whole.H = H; whole.dk = dk; whole.dv = dv; whole.chunk = chunk;
     whole.mode = mode; whole.dtype = dtype;
     if (variant == LDN_VARIANT_AUTO) {
         const int pick = chunk_tc_pick(whole, true);
         if (pick != LDN_VARIANT_SPLIT)
             return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
-                                  pick, nullptr, 0, stream);
+                                  pick, nullptr, 0, stream, erase, write);
     }
 
     // Plan: nb sequences per piece, or (nb == 0) runs of tpc chunks of one sequence.
@@ -199,7 +212,7 @@ extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v
             return variant == LDN_VARIANT_SPLIT
                        ? LDN_ERR_UNSUPPORTED
                        : chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode,
-                                        dtype, chunk_tc_pick(whole, false), nullptr, 0, stream);
+                                        dtype, chunk_tc_pick(whole, false), nullptr, 0, stream, erase, write);
     }
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -208,14 +221,15 @@ extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v
     int dev = 0;
     if (static_scratch_acquire(s, &scr, &scr_bytes, &dev) != cudaSuccess) return LDN_ERR_CUDA;
     const size_t el = dtype == LDN_BF16 ? 2 : 4;
-    const size_t gate_w = mode == LDN_KDA ? (size_t)dk : 1;
+    const size_t gate_w = mode == LDN_KDA || mode == LDN_GDN2 ? (size_t)dk : 1;
     // One piece: sequences b0 .. b0+np-1, tokens t0 .. t0+len-1 (t0 > 0 only when np == 1).
     auto piece = [&](int b0, int np, int t0, int len, const float *s0, float *sf, size_t ws_bytes) {
         const size_t tok = ((size_t)b0 * T + t0) * H;   // token-head offset of (b0, t0)
         return chunk_fwd_impl((const uint8_t *)q + tok * dk * el, (const uint8_t *)k + tok * dk * el,
-                              (const uint8_t *)v + tok * dv * el, beta + tok, gate ? gate + tok * gate_w : nullptr,
-                              s0, (uint8_t *)out + tok * dv * el, sf, np, len, H, dk, dv, chunk, mode, dtype,
-                              LDN_VARIANT_SPLIT, scr, ws_bytes, stream);
+                              (const uint8_t *)v + tok * dv * el, beta ? beta + tok : nullptr,
+                              gate ? gate + tok * gate_w : nullptr, s0, (uint8_t *)out + tok * dv * el, sf, np, len,
+                              H, dk, dv, chunk, mode, dtype, LDN_VARIANT_SPLIT, scr, ws_bytes, stream,
+                              erase ? erase + tok * dk : nullptr, write ? write + tok * dv : nullptr);
     };
     st = LDN_OK;
     if (nb > 0) {
@@ -241,15 +255,27 @@ extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v
     return st;
 }
 
+extern "C" int ldn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *beta,
+                                     const float *gate, const float *S0, void *out, float *S_final,
+                                     int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                                     int variant, void *stream)
+{
+    if (mode == LDN_GDN2) return LDN_ERR_INVALID_ARG;
+    return noalloc_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, variant, stream,
+                        nullptr, nullptr);
+}
+
 extern "C" int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
                                        size_t workspace_bytes)
 {
-    const int st = validate_common(mode, dtype, dk, dv);
+    const int st = validate_common(mode, dtype, dk, dv, mode == LDN_GDN2);
     if (st != LDN_OK) return -st;
     if (chunk != 64) return -LDN_ERR_UNSUPPORTED;
     if (B < 1 || H < 1 || T < 0) return -LDN_ERR_INVALID_ARG;
+    alignas(16) static const float kAligned[4] = {0.f, 0.f, 0.f, 0.f};   // stand-in gates (aligned)
     ChunkArgs a{};
     a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = B; a.T = T; a.H = H;
+    a.erase = a.write = kAligned;
     if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return LDN_VARIANT_SIMT;
     const size_t need = split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype);
     return chunk_tc_pick(a, need > 0 && workspace_bytes >= need);
@@ -311,35 +337,17 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 }
 
 // Gated DeltaNet-2: the KDA checks with the erase gate b (shaped like k) and
-// the write gate w (shaped like v) in place of beta.
+// the write gate w (shaped like v) in place of beta; kernel choice and the
+// split variant's scratch as in ldn_chunk_fwd_noalloc.
 extern "C" int ldn_chunk_fwd_gdn2(const void *q, const void *k, const void *v, const float *erase,
                                   const float *write, const float *gate, const float *S0, void *out, float *S_final,
-                                  int B, int T, int H, int dk, int dv, int chunk, int dtype, void *stream)
+                                  int B, int T, int H, int dk, int dv, int chunk, int dtype, int variant,
+                                  void *stream)
 {
-    int st = validate_common(LDN_KDA, dtype, dk, dv);
-    if (st != LDN_OK) return st;
-    if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
-    if (chunk != 64) return LDN_ERR_UNSUPPORTED;
-    if ((long long)B * H > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
-    if ((long long)B * T * H * (dk > dv ? dk : dv) > (1LL << 40)) return LDN_ERR_UNSUPPORTED;
-    if ((S0 && !aligned16(S0)) || (S_final && !aligned16(S_final))) return LDN_ERR_INVALID_ARG;
-    cudaStream_t s = (cudaStream_t)stream;
-    if (T == 0) {
-        if (!S_final) return LDN_OK;
-        return launch_copy_state(S0, S_final, (long long)B * H * dk * dv, s) == cudaSuccess ? LDN_OK
-                                                                                            : LDN_ERR_CUDA;
-    }
-    if (!q || !k || !v || !erase || !write || !gate || !out) return LDN_ERR_INVALID_ARG;
-    const void *vec_ptrs[] = {q, k, v, out};
-    for (const void *p : vec_ptrs)
-        if (!aligned16(p)) return LDN_ERR_INVALID_ARG;
-    if (!aligned(erase, 4) || !aligned(write, 4) || !aligned(gate, 4)) return LDN_ERR_INVALID_ARG;
-    ChunkArgs a{q, k, v, nullptr, gate, S0, out, S_final, B, T, H, dk, dv, chunk, LDN_GDN2, dtype, nullptr};
-    a.erase = erase;
-    a.write = write;
-    a.status = status_word_ptr();
-    if (!a.status) return LDN_ERR_CUDA;
-    return launch_chunk_simt(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+    if (T > 0 && (!erase || !write)) return LDN_ERR_INVALID_ARG;
+    alignas(16) static const float kNone[4] = {0.f, 0.f, 0.f, 0.f};   // T = 0: no gate is read
+    return noalloc_impl(q, k, v, nullptr, gate, S0, out, S_final, B, T, H, dk, dv, chunk, LDN_GDN2, dtype, variant,
+                        stream, erase ? erase : kNone, write ? write : kNone);
 }
 
 extern "C" int ldn_decode_step_gdn2(const void *q, const void *k, const void *v, const float *erase,

@@ -65,6 +65,13 @@
 // count carry the ordering); a cluster-scope acquire in the poll loop slowed
 // the whole SM.
 //
+// Gated DeltaNet-2 (linear-attention notes, Sec. 2.6, Eqs. 21-24) runs the KDA
+// form with three substitutions where the operands are formed: the K rows of the
+// [Q ; K] tile (the prediction side: A's rows and W) carry the erase direction
+// b * K e^{G-m} instead of K e^{G-m}, beta is 1, and the V tile is multiplied by
+// the write gate w in its fp16 conversion.  The side tile (the write direction,
+// P's columns and the state update) keeps K.
+//
 // Every mbarrier wait is bounded in time (2 s); a timeout sets LDN_ERR_TIMEOUT
 // in the status word, both roles abandon their loops, in-flight copies and
 // MMAs are drained with bounded waits, TMEM is freed and the CTA returns.
@@ -118,7 +125,7 @@ constexpr int kMaxStages = 3;
 // DeltaNet / Gated DeltaNet; two for KDA, whose two side tiles take the room.
 template <int MODE, bool SPLIT = false>
 struct Layout {
-    static constexpr bool kda = MODE == LDN_KDA;
+    static constexpr bool kda = MODE == LDN_KDA || MODE == LDN_GDN2;   // per-channel decay
     static constexpr int stages = kda ? 2 : 3;
     static constexpr uint32_t vbytes = SPLIT ? 2 * kVBytes : kVBytes;  // V slice (split: all of dv <= 128)
     static constexpr uint32_t qk = 0;                              // stages x [Q;K]
@@ -212,6 +219,33 @@ __device__ __forceinline__ void ld_row8_bf16(const uint8_t *block, int row, int 
     }
 }
 
+// In-place bf16 -> fp16 conversion of a V tile (64-column blocks of 64 rows, 128-byte
+// swizzle) by `n` threads, each value multiplied by the write gate w of its token and
+// value channel (Gated DeltaNet-2).  wrow = w of the tile's row 0, column 0 (row stride
+// ldw floats, 16-byte aligned); rows at or past `rows` are zero in the tile and stay so.
+__device__ __forceinline__ void tile_v_gated_to_f16(uint8_t *p, int bytes, int t, int n, const float *wrow,
+                                                    size_t ldw, int rows)
+{
+    for (int o = t * 16; o < bytes; o += n * 16) {
+        const int blk = o >> 13, r = (o >> 7) & 63, c8 = ((((o >> 4) & 7) ^ (r & 7)) << 3) + 64 * blk;
+        uint4 u = *reinterpret_cast<const uint4 *>(p + o);
+        float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;
+        if (r < rows) {
+            const float4 *src = reinterpret_cast<const float4 *>(wrow + (size_t)r * ldw + c8);
+            w0 = __ldg(src);
+            w1 = __ldg(src + 1);
+        }
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[i]));
+            w[i] = pack_h2(f.x * wv[2 * i], f.y * wv[2 * i + 1]);
+        }
+        *reinterpret_cast<uint4 *>(p + o) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // In-place bf16 -> fp16 conversion of `bytes` of a tile by `n` threads.
 __device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int t, int n)
 {
@@ -240,17 +274,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ beta,
                 const float *__restrict__ gate, const float *S0, __nv_bfloat16 *__restrict__ out,
-                float *S_final, int T, int H, int dv, int *status, uint8_t *__restrict__ ws, int cpr)
+                float *S_final, int T, int H, int dv, int *status, uint8_t *__restrict__ ws, int cpr,
+                const float *__restrict__ erase, const float *__restrict__ write)
 {
     extern __shared__ uint8_t dsmem[];
     // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
     // array so that every access below stays a shared-memory access.
     uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
     constexpr bool SPLIT = KIND == kSplit, PAIR = KIND == kPair;
-    static_assert(!PAIR || MODE != LDN_KDA, "the pair kernel takes DeltaNet / Gated DeltaNet");
+    constexpr bool kG2 = MODE == LDN_GDN2;                 // Gated DeltaNet-2: erase / write gates
+    constexpr bool kKda = MODE == LDN_KDA || kG2;          // per-key-channel decay
+    static_assert(!PAIR || !kKda, "the pair kernel takes DeltaNet / Gated DeltaNet");
     using LY = Layout<MODE, SPLIT>;
     constexpr int kStages = LY::stages;
-    constexpr bool kKda = MODE == LDN_KDA;
     Small &S = *reinterpret_cast<Small *>(sm + LY::small);
     __half *A16 = reinterpret_cast<__half *>(sm + LY::a16);
     __half *P16 = reinterpret_cast<__half *>(sm + LY::p16);
@@ -346,7 +382,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int r = lane; r < kC; r += 32) {
                 const bool ok = r < LL;
                 const size_t i = ok ? ((size_t)b * T + tt0 + r) * H + h : 0;
-                cp_async4(&S.stg_beta[cc & 1][r], beta + i, ok ? 4u : 0u);
+                if (!kG2) cp_async4(&S.stg_beta[cc & 1][r], beta + i, ok ? 4u : 0u);
                 if (MODE == LDN_GDN) cp_async4(&S.stg_gate[cc & 1][r], gate + i, ok ? 4u : 0u);
             }
             cp_async_commit();
@@ -358,7 +394,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             cp_async_wait<0>();          // chunk cc's staged beta / gates
             __syncwarp();
             const int r0 = 2 * lane, r1 = r0 + 1;
-            const float b0 = S.stg_beta[sg][r0], b1 = S.stg_beta[sg][r1];
+            const float b0 = kG2 ? 1.f : S.stg_beta[sg][r0], b1 = kG2 ? 1.f : S.stg_beta[sg][r1];
             const float a0 = MODE == LDN_GDN ? S.stg_gate[sg][r0] : 0.f;
             const float a1 = MODE == LDN_GDN ? S.stg_gate[sg][r1] : 0.f;
             __syncwarp();
@@ -523,14 +559,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 uint8_t *qk = sm + LY::qk + ls * kQKBytes + (ch0 >> 6) * 16384;
                 uint8_t *kbt = KB + (cc & 1) * kKBBytes + (ch0 >> 6) * 8192;
                 const int col = ch0 & 63;
+                const int tb = (cb + cc) * kC, LL = min(kC, T - tb);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int r = r0 + i;
-                    float ep[8], en[8];
+                    float ep[8], en[8], eb[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {   // e^{G-m} and e^{m-G}, rounded to fp16 below
                         ep[j] = G[i][j];
                         en[j] = __fdividef(1.f, G[i][j]);
+                        eb[j] = ep[j];
+                    }
+                    if (kG2 && r < LL) {   // the K rows carry b * K e^{G-m} (rows past T: K is zero)
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(erase + (((size_t)b * T + tb + r) * H + h) * kDK + ch0);
+                        const float4 lo = __ldg(src), hi = __ldg(src + 1);
+                        eb[0] *= lo.x; eb[1] *= lo.y; eb[2] *= lo.z; eb[3] *= lo.w;
+                        eb[4] *= hi.x; eb[5] *= hi.y; eb[6] *= hi.z; eb[7] *= hi.w;
                     }
                     uint4 *qp = reinterpret_cast<uint4 *>(qk + sw128_offset(r, col));
                     uint4 *kp = reinterpret_cast<uint4 *>(qk + sw128_offset(64 + r, col));
@@ -543,7 +588,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int u = 0; u < 4; ++u) {
                         const float2 qf = __bfloat1622float2(q2[u]), kf = __bfloat1622float2(k2[u]);
                         wq[u] = pack_h2(qf.x * ep[2 * u], qf.y * ep[2 * u + 1]);
-                        wk[u] = pack_h2(kf.x * ep[2 * u], kf.y * ep[2 * u + 1]);
+                        wk[u] = pack_h2(kf.x * eb[2 * u], kf.y * eb[2 * u + 1]);
                         wb[u] = pack_h2(kf.x * en[2 * u], kf.y * en[2 * u + 1]);
                     }
                     *qp = make_uint4(wq[0], wq[1], wq[2], wq[3]);
@@ -641,7 +686,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     named_sync(kBarPrep, kPrepThreads);
                     {   // A_rj = beta_r sum_ch k_r k_j e^{G_r - G_j} (j < r); P_rj = sum_ch q_r k_j e^{G_r - G_j} (j <= r)
+                        // (Gated DeltaNet-2: b_r * k_r in place of beta_r k_r)
                         const int isA = pt >> 7, r = (pt >> 1) & 63, j0 = 32 * (pt & 1);
+                        const int tbe = (cb + c) * kC, LLe = min(kC, T - tbe);
+                        const float *erow = kG2 && isA && r < LLe ? erase + (((size_t)b * T + tbe + r) * H + h) * kDK
+                                                                  : nullptr;
                         const int jmax = isA ? r - 1 : r;
                         float acc[32];
 #pragma unroll
@@ -650,8 +699,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             for (int ch = 0; ch < kDK; ++ch) {
                                 const uint8_t *blk = QK + (ch >> 6) * 16384;
                                 const int col = ch & 63;
-                                const float xr = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                float xr = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                                     blk + sw128_offset(isA ? 64 + r : r, col)));
+                                if (kG2 && isA) xr *= erow ? __ldg(erow + ch) : 0.f;
                                 const float gr = Gs[r * kDK + ch];
 #pragma unroll
                                 for (int i = 0; i < 32; ++i) {
@@ -671,10 +721,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                                                              j0 + i + 1 <= jmax ? acc[i + 1] * sc : 0.f);
                     }
                     named_sync(kBarPrep, kPrepThreads);
-                    {   // Q^ = Q e^{G}, K^ = K e^{G} in place; K~ = K e^{G_C - G} into the side tile
+                    {   // Q^ = Q e^{G}, K^ = K e^{G} (GDN2: b * K e^{G}) in place; K~ = K e^{G_C - G}
+                        // into the side tile
                         uint8_t *kbt = KB + (c & 1) * kKBBytes;
+                        const int tbe = (cb + c) * kC, LLe = min(kC, T - tbe);
                         for (int e = pt; e < kC * kDK; e += kPrepThreads) {
                             const int r = e >> 7, ch = e & 127, col = ch & 63;
+                            const float bv = !kG2 ? 1.f
+                                             : r < LLe ? __ldg(erase + (((size_t)b * T + tbe + r) * H + h) * kDK + ch)
+                                                       : 0.f;
                             uint8_t *blk = QK + (ch >> 6) * 16384;
                             const float gv = Gs[r * kDK + ch], gcv = Gs[(kC - 1) * kDK + ch];
                             uint8_t *qp = blk + sw128_offset(r, col), *kp = blk + sw128_offset(64 + r, col);
@@ -682,7 +737,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kp));
                             const float eg = expf(gv);
                             *reinterpret_cast<__half *>(qp) = __float2half_rn(qv * eg);
-                            *reinterpret_cast<__half *>(kp) = __float2half_rn(kv * eg);
+                            *reinterpret_cast<__half *>(kp) = __float2half_rn(bv * kv * eg);
                             *reinterpret_cast<__half *>(kbt + (ch >> 6) * 8192 + sw128_offset(r, col)) =
                                 __float2half_rn(kv * expf(gcv - gv));
                         }
@@ -762,7 +817,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tile_bf16_to_f16(QK + 8192, 8192, pt - 64, kPrepThreads - 64);           // K, block 0
                     tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
                 }
-                tile_bf16_to_f16(Vt, SPLIT ? dv / kDVS * kVBytes : kVBytes, pt - 64, kPrepThreads - 64);
+                const int vbytes = SPLIT ? dv / kDVS * kVBytes : kVBytes;
+                if constexpr (kG2) {   // z = w * v
+                    const int tb = (cb + c) * kC;
+                    tile_v_gated_to_f16(Vt, vbytes, pt - 64, kPrepThreads - 64,
+                                        write + (((size_t)b * T + tb) * H + h) * dv + n0, (size_t)H * dv,
+                                        min(kC, T - tb));
+                } else {
+                    tile_bf16_to_f16(Vt, vbytes, pt - 64, kPrepThreads - 64);
+                }
             }
             named_sync(kBarPrep, kPrepThreads);
             }   // run
@@ -1445,10 +1508,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 bool chunk_tc_supported(const ChunkArgs &a)
 {
-    // KDA reads its per-channel log-gates as float4: the gate tensor must be 16-byte aligned
-    const bool kda_ok = a.mode == LDN_KDA && ((uintptr_t)a.gate & 15u) == 0;
+    // KDA reads its per-channel log-gates as float4: the gate tensor must be 16-byte
+    // aligned; so must Gated DeltaNet-2's erase and write gates
+    const bool a16 = ((uintptr_t)a.gate & 15u) == 0;
+    const bool kda_ok = a.mode == LDN_KDA && a16;
+    const bool g2_ok = a.mode == LDN_GDN2 && a16 && a.erase && a.write && ((uintptr_t)a.erase & 15u) == 0 &&
+                       ((uintptr_t)a.write & 15u) == 0;
     return a.dtype == LDN_BF16 && a.dk == kDK && a.dv % kDVS == 0 && a.chunk == kC &&
-           (a.mode == LDN_DELTANET || a.mode == LDN_GDN || kda_ok);
+           (a.mode == LDN_DELTANET || a.mode == LDN_GDN || kda_ok || g2_ok);
 }
 
 namespace {
@@ -1500,15 +1567,18 @@ cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
-                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr);
+                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase, a.write);
         }
         kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
-                                                     a.S_final, a.T, a.H, a.dv, a.status, ws, cpr);
+                                                     a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase,
+                                                     a.write);
         return cudaGetLastError();
     };
     if (a.mode == LDN_GDN) return go(chunk_tc_kernel<LDN_GDN, KIND>, Layout<LDN_GDN, SPLIT>::bytes);
-    if constexpr (!PAIR)
+    if constexpr (!PAIR) {
         if (a.mode == LDN_KDA) return go(chunk_tc_kernel<LDN_KDA, KIND>, Layout<LDN_KDA, SPLIT>::bytes);
+        if (a.mode == LDN_GDN2) return go(chunk_tc_kernel<LDN_GDN2, KIND>, Layout<LDN_GDN2, SPLIT>::bytes);
+    }
     return go(chunk_tc_kernel<LDN_DELTANET, KIND>, Layout<LDN_DELTANET, SPLIT>::bytes);
 }
 }  // namespace
@@ -1517,7 +1587,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) { return launch
 
 bool chunk_pair_supported(const ChunkArgs &a)
 {
-    return chunk_tc_supported(a) && a.mode != LDN_KDA && a.dv == 2 * kDVS;
+    return chunk_tc_supported(a) && (a.mode == LDN_DELTANET || a.mode == LDN_GDN) && a.dv == 2 * kDVS;
 }
 
 cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t st) { return launch_tc<kPair>(a, nullptr, st); }
@@ -1536,7 +1606,7 @@ int chunk_tc_pick(const ChunkArgs &a, bool split_ok)
     const bool pair_ok = chunk_pair_supported(a);
     const int sms = sm_count();
     if (sms <= 0) return pair_ok ? LDN_VARIANT_PAIR : LDN_VARIANT_TENSOR;
-    const bool kda = a.mode == LDN_KDA;
+    const bool kda = a.mode == LDN_KDA || a.mode == LDN_GDN2;
     const double t_fused = kda ? 7.9 : 4.0, t_pair = 5.0, t_prep = kda ? 10.8 : 5.4, t_state = 1.6;
     const long long heads = (long long)a.B * a.H, nchunks = (a.T + kC - 1) / kC;
     const long long slices = heads * (a.dv / kDVS);

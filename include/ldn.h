@@ -163,7 +163,9 @@ int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *b
                      int variant, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Which kernel family ldn_chunk_fwd_ws(..., LDN_VARIANT_AUTO, ...) runs for these
- * sizes and a workspace of workspace_bytes (pointers assumed aligned): returns
+ * sizes and a workspace of workspace_bytes (pointers assumed aligned; mode
+ * LDN_GDN2 answers for ldn_chunk_fwd_gdn2, whose split variant has the
+ * library's array, given as workspace_bytes = SIZE_MAX): returns
  * LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR, LDN_VARIANT_PAIR or LDN_VARIANT_SPLIT, or -LDN_ERR_* for
  * arguments that would be rejected.  Host function; it reads the SM count of
  * the current device. */
@@ -276,18 +278,24 @@ int ldn_decode_step(const void *q, const void *k, const void *v, const float *be
  * (the library applies no sigmoid to them).
  *
  * ldn_chunk_fwd_gdn2 -- chunkwise forward of that recurrence over a whole
- * sequence (the chunk form of ldn_chunk_fwd with e_t in place of beta_t k_t on
- * the prediction side and z_t in place of beta_t v_t; fp32 CUDA-core kernel).
+ * sequence: the chunk form of ldn_chunk_fwd with e_t in place of beta_t k_t on
+ * the prediction side (the rows of A and W) and z_t in place of beta_t v_t.
  *   q, k     [B][T][H][dk] dtype      v, out [B][T][H][dv] dtype
  *   erase    [B][T][H][dk] fp32       write  [B][T][H][dv] fp32
  *   gate     [B][T][H][dk] fp32 (log a_t)
- *   S0, S_final, B, T, H, dk, dv, chunk, dtype, alignment (q, k, v, out, S0,
- *   S_final 16-byte; erase, write, gate 4-byte), T = 0 and errors as for
- *   ldn_chunk_fwd.
+ *   S0, S_final, B, T, H, dk, dv, chunk, dtype, T = 0 and errors as for
+ *   ldn_chunk_fwd.  Alignment: q, k, v, out, S0, S_final 16-byte; erase,
+ *   write, gate 4-byte.
+ * `variant` and the kernel families are those of ldn_chunk_fwd_noalloc (the
+ * split variant through the same library-owned array): the tensor-core
+ * kernels take bf16 inputs with dk = 128, dv a multiple of 64 and erase, write
+ * and gate 16-byte aligned (LDN_VARIANT_PAIR is not offered: it returns
+ * LDN_ERR_UNSUPPORTED); LDN_VARIANT_SIMT runs the fp32 CUDA-core kernel for
+ * either dtype; LDN_VARIANT_AUTO picks as for KDA.
  */
 int ldn_chunk_fwd_gdn2(const void *q, const void *k, const void *v, const float *erase, const float *write,
                        const float *gate, const float *S0, void *out, float *S_final, int B, int T, int H,
-                       int dk, int dv, int chunk, int dtype, void *stream);
+                       int dk, int dv, int chunk, int dtype, int variant, void *stream);
 
 /*
  * ldn_decode_step_gdn2 -- one Gated DeltaNet-2 step for every (b, h), state

@@ -111,11 +111,11 @@ def test_decode_rejects_bad_arguments(lib, kw, want):
 
 def _chunk_gdn2(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, erase=FAKE, write=FAKE, gate=FAKE, S0=None, out=FAKE, S_final=None,
-             B=1, T=64, H=1, dk=64, dv=64, chunk=64, dtype=1, stream=None)
+             B=1, T=64, H=1, dk=64, dv=64, chunk=64, dtype=1, variant=0, stream=None)
     a.update(kw)
     return ldn.ldn_chunk_fwd_gdn2(a["q"], a["k"], a["v"], a["erase"], a["write"], a["gate"], a["S0"], a["out"],
                                   a["S_final"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"], a["dtype"],
-                                  a["stream"])
+                                  a["variant"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -134,6 +134,11 @@ def _chunk_gdn2(**kw):
     (dict(dk=96), ldn.LDN_ERR_UNSUPPORTED),
     (dict(chunk=128), ldn.LDN_ERR_UNSUPPORTED),
     (dict(T=0, q=None, erase=None, write=None, gate=None, out=None), ldn.LDN_OK),   # no state asked: nothing to do
+    (dict(variant=7), ldn.LDN_ERR_INVALID_ARG),
+    (dict(variant=ldn.LDN_VARIANT_PAIR, dk=128, dv=128), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(variant=ldn.LDN_VARIANT_TENSOR, dtype=0, dk=128), ldn.LDN_ERR_UNSUPPORTED),   # tensor cores: bf16
+    (dict(variant=ldn.LDN_VARIANT_TENSOR, dk=128, erase=FAKE + 4), ldn.LDN_ERR_UNSUPPORTED),   # float4 gates
+    (dict(variant=ldn.LDN_VARIANT_SPLIT, dk=64), ldn.LDN_ERR_UNSUPPORTED),
 ])
 def test_chunk_gdn2_rejects_bad_arguments(lib, kw, want):
     assert _chunk_gdn2(**kw) == want
@@ -165,6 +170,9 @@ def test_decode_gdn2_rejects_bad_arguments(lib, kw, want):
 def test_beta_gated_entry_points_reject_the_gdn2_mode(lib):
     assert _decode(mode=ldn.LDN_GDN2) == ldn.LDN_ERR_INVALID_ARG
     assert _chunk(mode=ldn.LDN_GDN2) == ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_chunk_fwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 64, 1, 128, 128, 64,
+                                     ldn.LDN_GDN2, 1, 0, None) == ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_chunk_fwd_workspace_size(1, 64, 1, 128, 128, 64, ldn.LDN_GDN2, 1) == 0
     assert ldn.ldn_chunk_fwd_select(64, 64, 64, ldn.LDN_GDN2, 1) == -ldn.LDN_ERR_INVALID_ARG
 
 
@@ -316,3 +324,13 @@ def _rms(**kw):
 ])
 def test_rmsnorm_gated_rejects_bad_arguments(lib, kw, want):
     assert _rms(**kw) == want
+
+
+def test_select_answers_for_gdn2(lib):
+    """The kernel family ldn_chunk_fwd_gdn2 runs: tensor-core families for bf16 with
+    dk = 128, the CUDA-core kernel otherwise; never the pair kernel."""
+    big = (1 << 64) - 1
+    assert ldn.ldn_chunk_fwd_select_ws(1, 64, 1, 64, 64, 64, ldn.LDN_GDN2, 1, big) == ldn.LDN_VARIANT_SIMT
+    assert ldn.ldn_chunk_fwd_select_ws(1, 64, 1, 128, 128, 64, ldn.LDN_GDN2, 0, big) == ldn.LDN_VARIANT_SIMT
+    fam = ldn.ldn_chunk_fwd_select_ws(8, 4096, 16, 128, 128, 64, ldn.LDN_GDN2, 1, big)
+    assert fam in (ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SPLIT)

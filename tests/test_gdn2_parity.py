@@ -24,17 +24,21 @@ def _built():
     ldn.load()
 
 
-def run_chunk(w, S0=True):
+def run_chunk(w, S0=True, variant=ldn.LDN_VARIANT_AUTO):
     import torch
     t = w.torch_inputs("cuda")
-    out, sf = ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], t["erase"], t["write"], t["gate"], t["S0"] if S0 else None)
+    out, sf = ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], t["erase"], t["write"], t["gate"], t["S0"] if S0 else None,
+                                 variant=variant)
     assert ldn.device_status() == ldn.LDN_OK
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), sf.cpu().numpy()
 
 
-def check_chunk(w):
-    o, s = run_chunk(w)
+VARIANTS = [ldn.LDN_VARIANT_SIMT, ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SPLIT]
+
+
+def check_chunk(w, variant=ldn.LDN_VARIANT_AUTO):
+    o, s = run_chunk(w, variant=variant)
     ro, rs = oracle.fwd_gdn2(w.q, w.k, w.v, w.erase, w.write, w.gate, w.S0)
     eo, es = out_err(o, ro, w.dtype), rel_err(s, rs)
     assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], f"out {eo:.3g} state {es:.3g}"
@@ -43,12 +47,69 @@ def check_chunk(w):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
 def test_chunk_parity_dtypes_dims(dtype, dk, dv):
-    check_chunk(wl.make_chunk(CHUNK, B=2, T=200, H=3, dk=dk, dv=dv, dtype=dtype, s0=True))
+    w = wl.make_chunk(CHUNK, B=2, T=200, H=3, dk=dk, dv=dv, dtype=dtype, s0=True)
+    check_chunk(w)
+    check_chunk(w, ldn.LDN_VARIANT_SIMT)
 
 
 @pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 129])
-def test_chunk_parity_lengths(T):
-    check_chunk(wl.make_chunk(CHUNK, B=1, T=T, H=2, s0=(T % 2 == 1)))
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_chunk_parity_lengths(T, variant):
+    check_chunk(wl.make_chunk(CHUNK, B=1, T=T, H=2, s0=(T % 2 == 1)), variant)
+
+
+@pytest.mark.parametrize("variant", [ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SPLIT])
+@pytest.mark.parametrize("B,T,H,dv,s0", [(2, 200, 3, 128, True), (1, 64, 2, 64, False), (1, 700, 1, 128, True),
+                                         (2, 333, 2, 64, True), (1, 1, 1, 128, True)])
+def test_chunk_tensor_core_variants(variant, B, T, H, dv, s0):
+    """The tcgen05 kernels: K rows carry b * K, beta = 1, V enters as w * V."""
+    check_chunk(wl.make_chunk(CHUNK, B=B, T=T, H=H, dv=dv, s0=s0), variant)
+
+
+@pytest.mark.parametrize("variant", [ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SPLIT])
+def test_chunk_strong_channel_gates_entrywise_chunks(variant):
+    """Chunks whose per-channel decay span leaves the fp16 factors are formed entry
+    by entry (erase gate applied per entry there); the others through the MMA."""
+    w = wl.make_chunk(CHUNK, B=1, T=320, H=2, s0=True)
+    g = w.gate.copy()
+    g[:, 64:192, :, 5] = -1.2
+    g[:, 256:300, 1, 100] = -0.9
+    w.gate = g.astype(np.float32)
+    check_chunk(w, variant)
+    w.gate = np.full_like(w.gate, -0.6)   # every chunk entry by entry
+    check_chunk(w, variant)
+
+
+def test_chunk_tensor_core_erase_and_write_extremes():
+    """b = 0 on some tokens (nothing erased), w = 0 on others (nothing written),
+    b = w = 1 on the rest: the gates reach the operands they belong to."""
+    w = wl.make_chunk(CHUNK, B=1, T=250, H=2, s0=True)
+    w.erase[:, 10:80] = 0.0
+    w.write[:, 60:140] = 0.0
+    w.erase[:, 200:] = 1.0
+    w.write[:, 200:] = 1.0
+    for variant in VARIANTS:
+        check_chunk(w, variant)
+
+
+def test_chunk_tensor_core_with_both_gates_beta_matches_kda():
+    """The same reduction through the tensor-core kernels (fused and split): the
+    GDN2 and KDA builds differ only in where beta enters, so the two agree to the
+    fp16 operand rounding."""
+    import torch
+    k = wl.make_chunk("kda_bf16_b8_t4096_h16_d128", B=2, T=260, H=2, s0=True)
+    t = k.torch_inputs("cuda")
+    erase = t["beta"][..., None].expand(*t["beta"].shape, k.dk).contiguous()
+    write = t["beta"][..., None].expand(*t["beta"].shape, k.dv).contiguous()
+    for variant in (ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SPLIT):
+        o2, s2 = ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], erase, write, t["gate"], t["S0"], variant=variant)
+        ok, sk = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"], mode=ldn.LDN_KDA,
+                               variant=variant)
+        torch.cuda.synchronize()
+        ro, rs = oracle.fwd(k.q, k.k, k.v, k.beta, k.gate, k.S0, mode=oracle.MODE_KDA)
+        assert out_err(o2.float().cpu().numpy(), ro, "bf16") <= TOL["bf16"]
+        assert rel_err(s2.cpu().numpy(), rs) <= TOL["bf16"]
+        assert rel_err(o2.float().cpu().numpy(), ok.float().cpu().numpy()) <= 1e-2
 
 
 def test_chunk_with_both_gates_beta_matches_the_kda_kernel():
@@ -59,7 +120,8 @@ def test_chunk_with_both_gates_beta_matches_the_kda_kernel():
     t = k.torch_inputs("cuda")
     erase = t["beta"][..., None].expand(*t["beta"].shape, k.dk).contiguous()
     write = t["beta"][..., None].expand(*t["beta"].shape, k.dv).contiguous()
-    o2, s2 = ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], erase, write, t["gate"], t["S0"])
+    o2, s2 = ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], erase, write, t["gate"], t["S0"],
+                                variant=ldn.LDN_VARIANT_SIMT)
     ok, sk = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"], mode=ldn.LDN_KDA,
                            variant=ldn.LDN_VARIANT_SIMT)
     torch.cuda.synchronize()
@@ -86,10 +148,11 @@ def test_chunk_zero_length_copies_state():
     assert torch.equal(S_final, t["S0"])
 
 
-def test_chunk_full_workload_sampled():
+@pytest.mark.parametrize("variant", [ldn.LDN_VARIANT_AUTO, ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SIMT])
+def test_chunk_full_workload_sampled(variant):
     """B=8, T=4096, H=16, d=128 bf16 in one call; sampled (b, h) against the oracle."""
     w = wl.make_chunk(CHUNK)
-    o, s = run_chunk(w, S0=False)
+    o, s = run_chunk(w, S0=False, variant=variant)
     for b, h in [(0, 0), (5, 11), (7, 15)]:
         sl = lambda a: a[b:b + 1, :, h:h + 1]
         ro, rs = oracle.fwd_gdn2(sl(w.q), sl(w.k), sl(w.v), sl(w.erase), sl(w.write), sl(w.gate), None)
