@@ -145,7 +145,7 @@ def test_chunk_zero_length_copies_state():
     t = w.torch_inputs("cuda")
     S_final = torch.full_like(t["S0"], 7.0)
     st = ldn.ldn_chunk_fwd_gdn2(0, 0, 0, 0, 0, 0, t["S0"].data_ptr(), 0, S_final.data_ptr(), 2, 0, 2, 128, 128,
-                                64, 1, torch.cuda.current_stream().cuda_stream)
+                                64, 1, ldn.LDN_VARIANT_AUTO, torch.cuda.current_stream().cuda_stream)
     assert st == ldn.LDN_OK
     torch.cuda.synchronize()
     assert torch.equal(S_final, t["S0"])
