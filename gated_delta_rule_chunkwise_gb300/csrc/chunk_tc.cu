@@ -223,24 +223,36 @@ __device__ __forceinline__ void ld_row8_bf16(const uint8_t *block, int row, int 
 // swizzle) by `n` threads, each value multiplied by the write gate w of its token and
 // value channel (Gated DeltaNet-2).  wrow = w of the tile's row 0, column 0 (row stride
 // ldw floats, 16-byte aligned); rows at or past `rows` are zero in the tile and stay so.
+// A thread converts at most NMAX 16-byte groups (NMAX * n * 16 >= bytes); all its gate
+// loads are issued before the first is used, so their latencies overlap.
+template <int NMAX>
 __device__ __forceinline__ void tile_v_gated_to_f16(uint8_t *p, int bytes, int t, int n, const float *wrow,
                                                     size_t ldw, int rows)
 {
-    for (int o = t * 16; o < bytes; o += n * 16) {
+    float4 wv[NMAX][2];
+#pragma unroll
+    for (int i = 0; i < NMAX; ++i) {
+        const int o = (t + i * n) * 16;
         const int blk = o >> 13, r = (o >> 7) & 63, c8 = ((((o >> 4) & 7) ^ (r & 7)) << 3) + 64 * blk;
-        uint4 u = *reinterpret_cast<const uint4 *>(p + o);
-        float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;
-        if (r < rows) {
+        wv[i][0] = wv[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (o < bytes && r < rows) {
             const float4 *src = reinterpret_cast<const float4 *>(wrow + (size_t)r * ldw + c8);
-            w0 = __ldg(src);
-            w1 = __ldg(src + 1);
+            wv[i][0] = __ldg(src);
+            wv[i][1] = __ldg(src + 1);
         }
-        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    }
+#pragma unroll
+    for (int i = 0; i < NMAX; ++i) {
+        const int o = (t + i * n) * 16;
+        if (o >= bytes) break;
+        const uint4 u = *reinterpret_cast<const uint4 *>(p + o);
+        const float g[8] = {wv[i][0].x, wv[i][0].y, wv[i][0].z, wv[i][0].w,
+                            wv[i][1].x, wv[i][1].y, wv[i][1].z, wv[i][1].w};
         uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[i]));
-            w[i] = pack_h2(f.x * wv[2 * i], f.y * wv[2 * i + 1]);
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[j]));
+            w[j] = pack_h2(f.x * g[2 * j], f.y * g[2 * j + 1]);
         }
         *reinterpret_cast<uint4 *>(p + o) = make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -559,7 +571,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 uint8_t *qk = sm + LY::qk + ls * kQKBytes + (ch0 >> 6) * 16384;
                 uint8_t *kbt = KB + (cc & 1) * kKBBytes + (ch0 >> 6) * 8192;
                 const int col = ch0 & 63;
+                // Gated DeltaNet-2: the K rows carry b * K e^{G-m}; the erase gates of a row
+                // are loaded four rows ahead of their use (rows past T: K is zero there)
                 const int tb = (cb + cc) * kC, LL = min(kC, T - tb);
+                const float *erow = kG2 ? erase + (((size_t)b * T + tb + r0) * H + h) * kDK + ch0 : nullptr;
+                constexpr int kAhead = kG2 ? 4 : 1;
+                float4 eq[kAhead][2];
+                auto erase_load = [&](int i, float4 (&d)[2]) {
+                    d[0] = d[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (kG2 && r0 + i < LL) {
+                        const float4 *src = reinterpret_cast<const float4 *>(erow + (size_t)i * H * kDK);
+                        d[0] = __ldg(src);
+                        d[1] = __ldg(src + 1);
+                    }
+                };
+                if constexpr (kG2) {
+#pragma unroll
+                    for (int i = 0; i < kAhead; ++i) erase_load(i, eq[i]);
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int r = r0 + i;
@@ -570,12 +599,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         en[j] = __fdividef(1.f, G[i][j]);
                         eb[j] = ep[j];
                     }
-                    if (kG2 && r < LL) {   // the K rows carry b * K e^{G-m} (rows past T: K is zero)
-                        const float4 *src =
-                            reinterpret_cast<const float4 *>(erase + (((size_t)b * T + tb + r) * H + h) * kDK + ch0);
-                        const float4 lo = __ldg(src), hi = __ldg(src + 1);
+                    if constexpr (kG2) {
+                        const float4 lo = eq[i % kAhead][0], hi = eq[i % kAhead][1];
                         eb[0] *= lo.x; eb[1] *= lo.y; eb[2] *= lo.z; eb[3] *= lo.w;
                         eb[4] *= hi.x; eb[5] *= hi.y; eb[6] *= hi.z; eb[7] *= hi.w;
+                        if (i + kAhead < 8) erase_load(i + kAhead, eq[i % kAhead]);
                     }
                     uint4 *qp = reinterpret_cast<uint4 *>(qk + sw128_offset(r, col));
                     uint4 *kp = reinterpret_cast<uint4 *>(qk + sw128_offset(64 + r, col));
@@ -818,11 +846,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
                 }
                 const int vbytes = SPLIT ? dv / kDVS * kVBytes : kVBytes;
-                if constexpr (kG2) {   // z = w * v
+                if constexpr (kG2) {   // z = w * v (split: dv <= 128, so 16 KB at most)
                     const int tb = (cb + c) * kC;
-                    tile_v_gated_to_f16(Vt, vbytes, pt - 64, kPrepThreads - 64,
-                                        write + (((size_t)b * T + tb) * H + h) * dv + n0, (size_t)H * dv,
-                                        min(kC, T - tb));
+                    constexpr int kNV = ((SPLIT ? 2 : 1) * (int)kVBytes / 16 + kPrepThreads - 65) / (kPrepThreads - 64);
+                    tile_v_gated_to_f16<kNV>(Vt, vbytes, pt - 64, kPrepThreads - 64,
+                                             write + (((size_t)b * T + tb) * H + h) * dv + n0, (size_t)H * dv,
+                                             min(kC, T - tb));
                 } else {
                     tile_bf16_to_f16(Vt, vbytes, pt - 64, kPrepThreads - 64);
                 }
