@@ -399,6 +399,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             cp_async_commit();
         };
+        // Gated DeltaNet-2: the erase and write gate rows of chunk cc into L2 (gate warp,
+        // one bulk prefetch per row and gate), well before the build and the V
+        // conversion load them.
+        auto prefetch_g2_rows = [&](int cc) {
+            if constexpr (kG2) {
+                const int tb = (cb + cc) * kC, LL = min(kC, T - tb);
+                for (int r = lane; r < LL; r += 32) {
+                    const size_t tok = ((size_t)b * T + tb + r) * H + h;
+                    bulk_prefetch_l2(erase + tok * kDK, kDK * 4);
+                    bulk_prefetch_l2(write + tok * dv + n0, (SPLIT ? dv : kDVS) * 4);
+                }
+            }
+        };
         // Gate prefix and decay factors of chunk cc into slot cc % 3 (gate warp, two
         // rows per lane); then the staging of chunk cc + 1 is started.
         auto compute_gates = [&](int cc) {
@@ -411,6 +424,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float a1 = MODE == LDN_GDN ? S.stg_gate[sg][r1] : 0.f;
             __syncwarp();
             if (cc + 1 < nchunks) prefetch_gates(cc + 1);
+            if (cc + 1 < nchunks) prefetch_g2_rows(cc + 1);
             float incl = a0 + a1;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -645,7 +659,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             umma_commit(&S.bar_pmma);
         };
-        if (warp == kGateWarp) prefetch_gates(0);
+        if (warp == kGateWarp) {
+            prefetch_gates(0);
+            prefetch_g2_rows(0);
+            if (nchunks > 1) prefetch_g2_rows(1);
+        }
         // The strictly-upper 16x16 blocks of T and of the top halves of AV / AK
         // (the blocks of P T above the diagonal) are zero for every chunk and
         // nothing else writes them: clear them once.
