@@ -18,7 +18,10 @@ bound (Eq. 3), the contraction of (I - beta k k^T), state passing, and a brute
 force by explicit matrix products at d = 4, T = 8.  Gated DeltaNet-2 (Sec. 2.6) is
 pinned in tests/test_gdn2_oracle_pins.py: its reduction to KDA, the erase-off /
 write-on additive limit, the exact write with unit keys, and a brute force through
-the notes' matrix expansion.
+the notes' matrix expansion.  The backward (``bwd``, the reverse-mode derivative
+of the same recurrence) is pinned in tests/test_bwd_oracle_pins.py by central
+finite differences of the forward oracle on every input and the initial state,
+and by the exact linearity identities of the recurrence in (v, S0) and in q.
 """
 from __future__ import annotations
 
@@ -65,6 +68,9 @@ def _load():
             g2 = lib.ldn_oracle_fwd_gdn2
             g2.restype = ctypes.c_int
             g2.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int)]
+            bw = lib.ldn_oracle_bwd
+            bw.restype = ctypes.c_int
+            bw.argtypes = [ctypes.c_void_p] * 14 + [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)]
             lib.ldn_oracle_default_threads.restype = ctypes.c_int
             lib.ldn_oracle_default_threads.argtypes = []
             _lib = lib
@@ -124,6 +130,42 @@ def fwd(q, k, v, beta, gate=None, S0=None, mode=MODE_DELTANET, nthreads=0,
     if return_threads:
         return out, sf, int(used.value)
     return out, sf
+
+
+def bwd(q, k, v, beta, gate, S0, dout, dS_final=None, mode=MODE_DELTANET, nthreads=0):
+    """Reverse-mode gradients of L = sum <dout, o> + <dS_final, S_T> through the
+    token recurrence of ``fwd`` (fp64, state history kept; see ldn_oracle.c).
+
+    Shapes as ``fwd``; dout [B, T, H, dv]; dS_final [B, H, dk, dv] or None.
+    Returns a dict of float64 arrays: dq, dk [B,T,H,dk], dv [B,T,H,dv],
+    dbeta [B,T,H], dgate (shape of gate; None for DeltaNet), dS0 [B,H,dk,dv]."""
+    q, k, v, beta = _f32(q, "q"), _f32(k, "k"), _f32(v, "v"), _f32(beta, "beta")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, T, H) or beta.shape != (B, T, H):
+        raise ValueError("oracle: inconsistent shapes")
+    if mode == MODE_DELTANET:
+        gate = None
+    else:
+        gate = _f32(gate, "gate")
+        want = (B, T, H) if mode == MODE_GDN else (B, T, H, dk)
+        if gate is None or gate.shape != want:
+            raise ValueError(f"oracle: gate must have shape {want}")
+    S0 = _f32(S0, "S0")
+    dout, dS_final = _f32(dout, "dout"), _f32(dS_final, "dS_final")
+    if dout.shape != v.shape:
+        raise ValueError("oracle: dout must be shaped like v")
+    if S0 is not None and S0.shape != (B, H, dk, dv) or dS_final is not None and dS_final.shape != (B, H, dk, dv):
+        raise ValueError("oracle: states must be [B, H, dk, dv]")
+    g = dict(dq=np.empty((B, T, H, dk)), dk=np.empty((B, T, H, dk)), dv=np.empty((B, T, H, dv)),
+             dbeta=np.empty((B, T, H)), dgate=None if gate is None else np.empty(gate.shape),
+             dS0=np.empty((B, H, dk, dv)))
+    rc = _load().ldn_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S0), _ptr(dout),
+                                _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dbeta"]),
+                                _ptr(g["dgate"]), _ptr(g["dS0"]), B, T, H, dk, dv, int(mode), int(nthreads), None)
+    if rc != 0:
+        raise RuntimeError(f"ldn_oracle_bwd failed with {rc}")
+    return g
 
 
 def fwd_gdn2(q, k, v, erase, write, gate, S0=None, nthreads=0, want_state=True):

@@ -39,6 +39,13 @@
  *     H = W^T, laid out [B][H][d_k][d_v] row-major ("K x V" state in the
  *     benchmark's method sources); a NULL initial state means zeros.
  *
+ * Backward (ldn_oracle_bwd): the reverse-mode derivative of the same token
+ * recurrence, step by step in reverse token order, from the full history of
+ * decayed states Wt_t kept by a forward pass (the "first-order backward that
+ * keeps the whole state history" the benchmark's method sources describe for
+ * KDA).  For the loss L = sum_t <dO_t, o_t> + <dS_final, S_T> it returns the
+ * gradient with respect to every input and the initial state.
+ *
  * Inputs are fp32 arrays (bf16 inputs are exactly representable in fp32);
  * every value is widened to double before use and all arithmetic is fp64.
  * Parallelism: independent (batch, head) pairs are spread over POSIX threads;
@@ -59,13 +66,19 @@ typedef struct {
     const float *q, *k, *v, *beta, *gate, *S0;
     const float *erase, *write; /* Gated DeltaNet-2: b [B][T][H][dk], w [B][T][H][dv] */
     double *out, *S_final;
+    /* backward: upstream gradients (dS_final may be NULL) and the input gradients */
+    const float *dout, *dS_final;
+    double *dq, *dk_, *dv_, *dbeta, *dgate, *dS0;
+    int bwd;
     int B, T, H, dk, dv, mode;
     int next_unit; /* shared work counter, protected by lock */
     pthread_mutex_t lock;
 } job_t;
 
-/* One (batch, head) pair: the recurrence over all T tokens. */
-static void run_unit(const job_t *J, int unit, double *W, double *pred)
+/* One (batch, head) pair: the recurrence over all T tokens.  Hist, when not
+   NULL, receives the decayed state Wt of every token (T x dv x dk, for the
+   backward); outputs are written only when J->out is set. */
+static void run_unit(const job_t *J, int unit, double *W, double *pred, double *Hist)
 {
     const int b = unit / J->H, h = unit % J->H;
     const int dk = J->dk, dv = J->dv, H = J->H, T = J->T;
@@ -101,6 +114,7 @@ static void run_unit(const job_t *J, int unit, double *W, double *pred)
                 for (int i = 0; i < dv; ++i) W[(size_t)i * dk + c] *= a;
             }
         }
+        if (Hist) memcpy(Hist + (size_t)t * dk * dv, W, sizeof(double) * (size_t)dk * dv);
 
         /* Prediction of the (decayed) memory for the current key, Eq. 9
            (Gated DeltaNet-2: along the erase direction e = b * k, Eq. 23). */
@@ -118,6 +132,7 @@ static void run_unit(const job_t *J, int unit, double *W, double *pred)
             for (int c = 0; c < dk; ++c) W[(size_t)i * dk + c] += r * (double)k[c];
         }
         /* Read the updated memory with the query, Eq. 8. */
+        if (!J->out) continue;
         double *o = J->out + tok * dv;
         for (int i = 0; i < dv; ++i) {
             double s = 0.0;
@@ -134,21 +149,129 @@ static void run_unit(const job_t *J, int unit, double *W, double *pred)
     }
 }
 
+/*
+ * One (batch, head) pair of the backward.  Forward, per token (as run_unit):
+ *   Wt = W_{t-1} D_t          (D_t = alpha I, Diag(a), or I)
+ *   p  = Wt k,  r = beta (v - p),  W_t = Wt + r k^T,  o = W_t q.
+ * Reverse, with G = dL/dW_t (starting from dS_final^T):
+ *   G += dO_t q^T                   dq_t  = W_t^T dO_t
+ *   dr = G k                        dk_t  = G^T r + Wt^T dp,   dp = -beta dr
+ *   dv_t = beta dr                  dbeta_t = dr . (v - p)
+ *   Gt = G + dp k^T                 (gradient w.r.t. Wt)
+ *   dg_t: KDA sum_i Gt[i][c] Wt[i][c] per channel c; GDN the sum over all
+ *         entries (d alpha / d g = alpha, so these equal dL/dg)
+ *   G <- Gt D_t                     (gradient w.r.t. W_{t-1})
+ * and at the end dS0 = G^T.  Hist holds Wt for every token (T x dv x dk).
+ */
+static void run_unit_bwd(const job_t *J, int unit, double *Hist, double *W, double *G, double *r, double *e,
+                         double *dp)
+{
+    const int b = unit / J->H, h = unit % J->H;
+    const int dk = J->dk, dv = J->dv, H = J->H, T = J->T;
+    const size_t D2 = (size_t)dk * dv;
+
+    /* forward, keeping Wt of every token (outputs not written: J->out is NULL) */
+    run_unit(J, unit, W, r, Hist);
+    /* reverse */
+    if (J->dS_final) {
+        const float *sf = J->dS_final + ((size_t)b * H + h) * D2;
+        for (int c = 0; c < dk; ++c)
+            for (int i = 0; i < dv; ++i) G[(size_t)i * dk + c] = (double)sf[(size_t)c * dv + i];
+    } else {
+        memset(G, 0, sizeof(double) * D2);
+    }
+    for (int t = T - 1; t >= 0; --t) {
+        const size_t tok = ((size_t)b * T + t) * H + h;
+        const float *q = J->q + tok * dk, *k = J->k + tok * dk, *v = J->v + tok * dv;
+        const float *dO = J->dout + tok * dv;
+        const double beta = (double)J->beta[tok];
+        const double *Wt = Hist + (size_t)t * D2;
+        /* r and v - p of this token, and W_t = Wt + r k^T */
+        for (int i = 0; i < dv; ++i) {
+            double p = 0.0;
+            for (int c = 0; c < dk; ++c) p += Wt[(size_t)i * dk + c] * (double)k[c];
+            e[i] = (double)v[i] - p;
+            r[i] = beta * e[i];
+        }
+        for (int i = 0; i < dv; ++i)
+            for (int c = 0; c < dk; ++c) W[(size_t)i * dk + c] = Wt[(size_t)i * dk + c] + r[i] * (double)k[c];
+        /* output read: G += dO q^T, dq = W_t^T dO */
+        double *dq = J->dq + tok * dk;
+        for (int c = 0; c < dk; ++c) {
+            double s = 0.0;
+            for (int i = 0; i < dv; ++i) s += W[(size_t)i * dk + c] * (double)dO[i];
+            dq[c] = s;
+        }
+        for (int i = 0; i < dv; ++i)
+            for (int c = 0; c < dk; ++c) G[(size_t)i * dk + c] += (double)dO[i] * (double)q[c];
+        /* write W_t = Wt + r k^T */
+        double *dkk = J->dk_ + tok * dk, *dvv = J->dv_ + tok * dv;
+        double db = 0.0;
+        for (int i = 0; i < dv; ++i) {
+            double dr = 0.0;
+            for (int c = 0; c < dk; ++c) dr += G[(size_t)i * dk + c] * (double)k[c];
+            dvv[i] = beta * dr;
+            db += dr * e[i];
+            dp[i] = -beta * dr;
+        }
+        J->dbeta[tok] = db;
+        for (int c = 0; c < dk; ++c) {
+            double s = 0.0;
+            for (int i = 0; i < dv; ++i) s += G[(size_t)i * dk + c] * r[i] + Wt[(size_t)i * dk + c] * dp[i];
+            dkk[c] = s;
+        }
+        /* prediction p = Wt k: G <- G + dp k^T is the gradient w.r.t. Wt */
+        for (int i = 0; i < dv; ++i)
+            for (int c = 0; c < dk; ++c) G[(size_t)i * dk + c] += dp[i] * (double)k[c];
+        /* decay Wt = W_{t-1} D_t */
+        if (J->mode == LDN_ORACLE_MODE_GDN) {
+            double s = 0.0;
+            for (size_t x = 0; x < D2; ++x) s += G[x] * Wt[x];
+            J->dgate[tok] = s;
+            const double a_t = exp((double)J->gate[tok]);   /* alpha of this token */
+            for (size_t x = 0; x < D2; ++x) G[x] *= a_t;
+        } else if (J->mode == LDN_ORACLE_MODE_KDA) {
+            const float *g = J->gate + tok * dk;
+            double *dg = J->dgate + tok * dk;
+            for (int c = 0; c < dk; ++c) {
+                double s = 0.0;
+                for (int i = 0; i < dv; ++i) s += G[(size_t)i * dk + c] * Wt[(size_t)i * dk + c];
+                dg[c] = s;
+                const double a = exp((double)g[c]);
+                for (int i = 0; i < dv; ++i) G[(size_t)i * dk + c] *= a;
+            }
+        }
+    }
+    double *ds0 = J->dS0 + ((size_t)b * H + h) * D2;
+    for (int c = 0; c < dk; ++c)
+        for (int i = 0; i < dv; ++i) ds0[(size_t)c * dv + i] = G[(size_t)i * dk + c];
+}
+
 static void *worker(void *arg)
 {
     job_t *J = (job_t *)arg;
-    double *W = (double *)malloc(sizeof(double) * (size_t)J->dk * J->dv);
+    const size_t D2 = (size_t)J->dk * J->dv;
+    double *W = (double *)malloc(sizeof(double) * D2);
     double *pred = (double *)malloc(sizeof(double) * (size_t)J->dv);
-    if (!W || !pred) { free(W); free(pred); return (void *)1; }
+    double *G = J->bwd ? (double *)malloc(sizeof(double) * D2) : NULL;
+    double *e = J->bwd ? (double *)malloc(sizeof(double) * (size_t)J->dv) : NULL;
+    double *dp = J->bwd ? (double *)malloc(sizeof(double) * (size_t)J->dv) : NULL;
+    double *Hist = J->bwd ? (double *)malloc(sizeof(double) * D2 * (size_t)(J->T > 0 ? J->T : 1)) : NULL;
+    if (!W || !pred || (J->bwd && (!G || !e || !dp || !Hist))) {
+        free(W); free(pred); free(G); free(e); free(dp); free(Hist);
+        return (void *)1;
+    }
     for (;;) {
         pthread_mutex_lock(&J->lock);
         const int unit = J->next_unit++;
         pthread_mutex_unlock(&J->lock);
         if (unit >= J->B * J->H) break;
-        run_unit(J, unit, W, pred);
+        if (J->bwd)
+            run_unit_bwd(J, unit, Hist, W, G, pred, e, dp);
+        else
+            run_unit(J, unit, W, pred, NULL);
     }
-    free(W);
-    free(pred);
+    free(W); free(pred); free(G); free(e); free(dp); free(Hist);
     return NULL;
 }
 
@@ -183,9 +306,37 @@ int ldn_oracle_fwd(const float *q, const float *k, const float *v,
     if (mode != LDN_ORACLE_MODE_DELTANET && !gate) return -1;
 
     job_t J;
+    memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v; J.beta = beta; J.gate = gate; J.S0 = S0;
-    J.erase = NULL; J.write = NULL;
     J.out = out; J.S_final = S_final;
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv; J.mode = mode;
+    return run_job(&J, nthreads, threads_used);
+}
+
+/*
+ * ldn_oracle_bwd: gradients of L = sum <dout, o> + <dS_final, S_T> for modes
+ * 0-2 (DeltaNet, Gated DeltaNet, KDA).  Inputs as ldn_oracle_fwd, plus
+ *   dout    [B][T][H][dv] fp32     dS_final [B][H][dk][dv] fp32 or NULL (zero)
+ * Outputs (fp64): dq, dk [B][T][H][dk], dv [B][T][H][dv], dbeta [B][T][H],
+ *   dgate: mode 1 [B][T][H], mode 2 [B][T][H][dk], mode 0 not written (may be
+ *   NULL); dS0 [B][H][dk][dv] (also when S0 is NULL: the gradient at zero).
+ * Memory: T x dk x dv doubles per thread for the state history.
+ */
+int ldn_oracle_bwd(const float *q, const float *k, const float *v, const float *beta, const float *gate,
+                   const float *S0, const float *dout, const float *dS_final, double *dq, double *dk_,
+                   double *dv_, double *dbeta, double *dgate, double *dS0, int B, int T, int H, int dk, int dv,
+                   int mode, int nthreads, int *threads_used)
+{
+    if (!q || !k || !v || !beta || !dout || !dq || !dk_ || !dv_ || !dbeta || !dS0) return -1;
+    if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1) return -1;
+    if (mode < 0 || mode > 2) return -1;
+    if (mode != LDN_ORACLE_MODE_DELTANET && (!gate || !dgate)) return -1;
+    job_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.beta = beta; J.gate = gate; J.S0 = S0;
+    J.dout = dout; J.dS_final = dS_final;
+    J.dq = dq; J.dk_ = dk_; J.dv_ = dv_; J.dbeta = dbeta; J.dgate = dgate; J.dS0 = dS0;
+    J.bwd = 1;
     J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv; J.mode = mode;
     return run_job(&J, nthreads, threads_used);
 }
@@ -205,6 +356,7 @@ int ldn_oracle_fwd_gdn2(const float *q, const float *k, const float *v,
     if (!q || !k || !v || !erase || !write || !gate || !out) return -1;
     if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1) return -1;
     job_t J;
+    memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v; J.beta = NULL; J.gate = gate; J.S0 = S0;
     J.erase = erase; J.write = write;
     J.out = out; J.S_final = S_final;

@@ -39,6 +39,19 @@ MUTANTS = {
     # Gated DeltaNet-2: the write gate is not applied to the value
     "gdn2_no_write": ("const double target = gdn2 ? (double)ww[i] * (double)v[i] : (double)v[i];",
                       "const double target = (double)v[i];"),
+    # backward: the key gradient misses its write term (G^T r)
+    "bwd_dk_no_write": ("s += G[(size_t)i * dk + c] * r[i] + Wt[(size_t)i * dk + c] * dp[i];",
+                        "s += Wt[(size_t)i * dk + c] * dp[i];"),
+    # backward: the prediction's gradient with the wrong sign
+    "bwd_dp_sign": ("dp[i] = -beta * dr;", "dp[i] = beta * dr;"),
+    # backward: the query gradient read from the state before the write
+    "bwd_dq_pre_write": ("for (int i = 0; i < dv; ++i) s += W[(size_t)i * dk + c] * (double)dO[i];",
+                         "for (int i = 0; i < dv; ++i) s += Wt[(size_t)i * dk + c] * (double)dO[i];"),
+    # backward: the state gradient not carried through the scalar decay
+    "bwd_no_decay": ("for (size_t x = 0; x < D2; ++x) G[x] *= a_t;", "(void)a_t;"),
+    # backward: the per-channel decay gradient taken against the state before the decay
+    "bwd_dg_wrong_state": ("for (int i = 0; i < dv; ++i) s += G[(size_t)i * dk + c] * Wt[(size_t)i * dk + c];",
+                           "for (int i = 0; i < dv; ++i) s += G[(size_t)i * dk + c] * Wt[(size_t)i * dk + c] * exp(-(double)g[c]) * 0.5;"),
 }
 
 
@@ -55,6 +68,7 @@ def test_pins_catch_mutant(name, tmp_path):
     env = dict(os.environ, LDN_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_gdn2_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_gdn2_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_bwd_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
