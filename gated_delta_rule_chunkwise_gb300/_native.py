@@ -7,10 +7,11 @@ been built, or no GPU is present, the calls raise.
 Two layers:
   * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
     ``ldn_chunk_fwd_workspace_size``, ``ldn_chunk_fwd_noalloc``, ``ldn_decode_step``,
-    ``ldn_chunk_fwd_gdn2``, ``ldn_decode_step_gdn2``, ``ldn_prologue``, ``ldn_rmsnorm_gated``,
+    ``ldn_chunk_fwd_gdn2``, ``ldn_decode_step_gdn2``, ``ldn_backward``,
+    ``ldn_backward_workspace_size``, ``ldn_prologue``, ``ldn_rmsnorm_gated``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
-  * ``chunk_fwd``, ``decode_step``, ``chunk_fwd_gdn2`` and ``decode_step_gdn2``:
+  * ``chunk_fwd``, ``decode_step``, ``chunk_fwd_gdn2``, ``decode_step_gdn2`` and ``backward``:
     the same calls on torch CUDA tensors,
     with shape / dtype checks and allocation of outputs and of the split
     variant's workspace (torch is used for device memory and the current
@@ -55,6 +56,8 @@ _SIGNATURES = {
     "ldn_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 9 + [_P], _I),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
     "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 8 + [_P], _I),
+    "ldn_backward": ([_P] * 14 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
+    "ldn_backward_workspace_size": ([_I] * 6, ctypes.c_size_t),
     "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
     "ldn_rmsnorm_gated": ([_P] * 4 + [_I] * 5 + [ctypes.c_float, _P], _I),
@@ -135,6 +138,16 @@ def ldn_chunk_fwd_gdn2(q, k, v, erase, write, gate, S0, out, S_final, B, T, H, d
 
 def ldn_decode_step_gdn2(q, k, v, erase, write, gate, S, out, B, H, dk, dv, dtype, stream):
     return load().ldn_decode_step_gdn2(q, k, v, erase, write, gate, S, out, B, H, dk, dv, dtype, stream)
+
+
+def ldn_backward(q, k, v, beta, gate, S0, dout, dS_final, dq, dk, dv, dbeta, dgate, dS0, B, T, H, dk_dim, dv_dim,
+                 mode, dtype, workspace, workspace_bytes, stream):
+    return load().ldn_backward(q, k, v, beta, gate, S0, dout, dS_final, dq, dk, dv, dbeta, dgate, dS0, B, T, H,
+                               dk_dim, dv_dim, mode, dtype, workspace, workspace_bytes, stream)
+
+
+def ldn_backward_workspace_size(B, T, H, dk, dv, mode):
+    return load().ldn_backward_workspace_size(B, T, H, dk, dv, mode)
 
 
 def ldn_prologue(q_in, k_in, v_in, conv_q, conv_k, conv_v, width, beta_logit, gate_z, gate_a, gate_b,
@@ -325,6 +338,44 @@ def decode_step_gdn2(q, k, v, erase, write, gate, S, *, out=None, stream=None):
     if st != LDN_OK:
         raise LdnError(st, "ldn_decode_step_gdn2")
     return out
+
+
+def backward(q, k, v, beta, gate, S0, dout, dS_final=None, *, mode, workspace=None, stream=None):
+    """Gradients of sum <dout, o> + <dS_final, S_T> on torch CUDA tensors (ldn_backward).
+
+    Shapes and dtypes as ``chunk_fwd``; dout like v.  Returns a dict of float32
+    tensors dq, dk, dv, dbeta, dgate (None for DeltaNet), dS0.  `workspace`: a
+    uint8 CUDA tensor of at least ldn_backward_workspace_size bytes, or None to
+    allocate one."""
+    import torch
+    mode = MODES.get(mode, mode)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q"); _check(k, "k", q.shape, q.dtype); _check(v, "v", (B, T, H, dv), q.dtype)
+    _check(dout, "dout", (B, T, H, dv), q.dtype)
+    _check(beta, "beta", (B, T, H), torch.float32)
+    if mode == LDN_DELTANET:
+        gate = None
+    else:
+        _check(gate, "gate", (B, T, H) if mode == LDN_GDN else (B, T, H, dk), torch.float32)
+    _check(S0, "S0", (B, H, dk, dv), torch.float32)
+    _check(dS_final, "dS_final", (B, H, dk, dv), torch.float32)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = dict(dq=torch.empty((B, T, H, dk), **f32), dk=torch.empty((B, T, H, dk), **f32),
+             dv=torch.empty((B, T, H, dv), **f32), dbeta=torch.empty((B, T, H), **f32),
+             dgate=None if gate is None else torch.empty(tuple(gate.shape), **f32),
+             dS0=torch.empty((B, H, dk, dv), **f32))
+    need = ldn_backward_workspace_size(B, T, H, dk, dv, mode)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = ldn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S0), _ptr(dout), _ptr(dS_final),
+                      _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dbeta"]), _ptr(g["dgate"]), _ptr(g["dS0"]),
+                      B, T, H, dk, dv, mode, _dtype_code(q), _ptr(workspace), workspace.numel(),
+                      _stream_handle(stream))
+    if st != LDN_OK:
+        raise LdnError(st, "ldn_backward")
+    return g
 
 
 def device_status(stream=None) -> int:

@@ -438,6 +438,56 @@ extern "C" int ldn_rmsnorm_gated(const void *o, const void *g, const float *weig
     return launch_rmsnorm_gated(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 
+// Backward of the DeltaNet / Gated DeltaNet / KDA recurrence (csrc/backward.cu).
+static int check_bwd_sizes(int B, int T, int H, int dk, int dv, int mode, int dtype)
+{
+    const int st = validate_common(mode, dtype, dk, dv);
+    if (st != LDN_OK) return st;
+    if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
+    if ((long long)B * H * (dv / 32) > (1LL << 24)) return LDN_ERR_UNSUPPORTED;
+    if ((long long)B * T * H * (2LL * dk + dv + 1) * (dv / 32) > (1LL << 40)) return LDN_ERR_UNSUPPORTED;
+    return LDN_OK;
+}
+
+extern "C" size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode)
+{
+    if (check_bwd_sizes(B, T, H, dk, dv, mode, LDN_F32) != LDN_OK) return 0;
+    return bwd_workspace_bytes(B, T, H, dk, dv, mode);
+}
+
+extern "C" int ldn_backward(const void *q, const void *k, const void *v, const float *beta, const float *gate,
+                            const float *S0, const void *dout, const float *dS_final, float *dq, float *dk_out,
+                            float *dv_out, float *dbeta, float *dgate, float *dS0, int B, int T, int H, int dk,
+                            int dv, int mode, int dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int st = check_bwd_sizes(B, T, H, dk, dv, mode, dtype);
+    if (st != LDN_OK) return st;
+    if (!dS0 || !aligned(dS0, 4) || (S0 && !aligned(S0, 4)) || (dS_final && !aligned(dS_final, 4)))
+        return LDN_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0)
+        return launch_copy_state(dS_final, dS0, (long long)B * H * dk * dv, s) == cudaSuccess ? LDN_OK
+                                                                                              : LDN_ERR_CUDA;
+    const bool gated = mode != LDN_DELTANET;
+    const void *must[] = {q, k, v, beta, dout, dq, dk_out, dv_out, dbeta};
+    for (const void *p : must)
+        if (!p) return LDN_ERR_INVALID_ARG;
+    if (gated && (!gate || !dgate)) return LDN_ERR_INVALID_ARG;
+    const uintptr_t el = dtype == LDN_BF16 ? 2 : 4;
+    const void *elp[] = {q, k, v, dout};
+    for (const void *p : elp)
+        if (!aligned(p, el)) return LDN_ERR_INVALID_ARG;
+    const void *f4[] = {beta, dq, dk_out, dv_out, dbeta};
+    for (const void *p : f4)
+        if (!aligned(p, 4)) return LDN_ERR_INVALID_ARG;
+    if (gated && (!aligned(gate, 4) || !aligned(dgate, 4))) return LDN_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16) || workspace_bytes < bwd_workspace_bytes(B, T, H, dk, dv, mode))
+        return LDN_ERR_INVALID_ARG;
+    BwdArgs a{q, k, v, beta, gated ? gate : nullptr, S0, dout, dS_final, dq, dk_out, dv_out, dbeta,
+              gated ? dgate : nullptr, dS0, (float *)workspace, B, T, H, dk, dv, mode, dtype};
+    return launch_backward(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
 extern "C" int ldn_get_device_status(void *stream)
 {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LDN_ERR_CUDA;

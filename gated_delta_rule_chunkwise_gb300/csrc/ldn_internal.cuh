@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <algorithm>
 
 #include "../../include/ldn.h"
 #include "../../include/ldn_diag.h"
@@ -72,6 +73,20 @@ int chunk_tc_pick(const ChunkArgs &a, bool split_ok);   // fastest tensor-core L
 bool chunk_pair_supported(const ChunkArgs &a);    // the cluster-pair kernel takes these arguments
 cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+
+// Backward of the recurrence (csrc/backward.cu).
+struct BwdArgs {
+    const void *q, *k, *v;
+    const float *beta, *gate, *S0;
+    const void *dout;
+    const float *dS_final;
+    float *dq, *dk_out, *dv_out, *dbeta, *dgate, *dS0;
+    float *ws;   // checkpoints, then the per-slice partial sums
+    int B, T, H, dk, dv, mode, dtype;
+};
+size_t bwd_ckpt_floats(int B, int T, int H, int dk, int dv);
+size_t bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int mode);
+cudaError_t launch_backward(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream);
 cudaError_t launch_rmsnorm_gated(const RmsNormArgs &a, cudaStream_t stream);
 int *status_word_ptr();   // address of the device status word on the current device

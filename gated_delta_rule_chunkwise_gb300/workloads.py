@@ -152,6 +152,20 @@ def make_decode(name: str = "gdn_decode_b64_h16_dk128_dv128_steps1000", seed: in
                     erase=erase, write=write)
 
 
+def make_upstream(w: Workload, seed: int = 1, final_state: bool = True):
+    """Upstream gradients for the backward of a chunk workload: dout ~ N(0, 1)
+    shaped like v (rounded to bf16 for bf16 workloads, as the kernels read it in
+    the workload's dtype) and dS_final ~ N(0, 1) [B, H, dk, dv] fp32 (or None),
+    drawn in that order from Generator(PCG64(seed))."""
+    rng = np.random.default_rng(seed)
+    f32 = np.float32
+    dout = rng.standard_normal(w.v.shape, dtype=f32)
+    if w.dtype == "bf16":
+        dout = round_bf16(dout)
+    dsf = rng.standard_normal((w.B, w.H, w.dk, w.dv), dtype=f32) if final_state else None
+    return dout, dsf
+
+
 # ---- prologue / epilogue inputs ------------------------------------------------
 # Recipe: numpy Generator(PCG64(seed)), draws in this order: q_in, k_in, v_in
 # ~ N(0, 1) (projection outputs); conv weights ~ N(0, 1/W) per (channel, tap)

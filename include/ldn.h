@@ -309,6 +309,41 @@ int ldn_decode_step_gdn2(const void *q, const void *k, const void *v, const floa
                          const float *gate, float *S, void *out, int B, int H, int dk, int dv, int dtype,
                          void *stream);
 
+/*
+ * ldn_backward -- gradients of the forward recurrence (modes DeltaNet, GDN,
+ * KDA) for the loss L = sum_t <dout_t, o_t> + <dS_final, S_T>, with respect to
+ * q, k, v, beta, the log-decay gates and the initial state.  It differentiates
+ * the per-token rules of the linear-attention notes (Sec. 2.3-2.5) step by
+ * step in reverse token order.  The states it needs are recomputed from copies
+ * of every eighth state taken by a forward sweep (the benchmark's method
+ * sources keep the whole state history for their KDA backward).  fp32
+ * arithmetic; the result equals the exact gradient up to rounding.
+ *
+ *   q, k, v, beta, gate, S0, B, T, H, dk, dv, mode, dtype as ldn_chunk_fwd
+ *   (mode LDN_GDN2 is not taken: LDN_ERR_INVALID_ARG)
+ *   dout      [B][T][H][dv] dtype      dS_final [B][H][dk][dv] fp32 or NULL (zero)
+ * Outputs, all fp32 and all overwritten:
+ *   dq, dk    [B][T][H][dk]            dv    [B][T][H][dv]      dbeta [B][T][H]
+ *   dgate     the gate's shape (mode DELTANET: ignored, may be NULL)
+ *   dS0       [B][H][dk][dv] (the gradient at S0, or at the zero state when S0 is NULL)
+ *   workspace device memory, 16-byte aligned, at least
+ *             ldn_backward_workspace_size(B, T, H, dk, dv, mode) bytes (state
+ *             copies, then per-32-column partial sums of the dk-side
+ *             gradients); contents on entry do not matter.
+ * Alignment: q, k, v, dout to their element size; every fp32 array 4-byte.
+ * T = 0 writes dS0 = dS_final (or zeros) and nothing else.  Asynchronous on
+ * `stream`: two kernel launches (the recurrence sweeps, then the sum over the
+ * dv slices).
+ */
+int ldn_backward(const void *q, const void *k, const void *v, const float *beta, const float *gate,
+                 const float *S0, const void *dout, const float *dS_final, float *dq, float *dk, float *dv,
+                 float *dbeta, float *dgate, float *dS0, int B, int T, int H, int dk_dim, int dv_dim, int mode,
+                 int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace ldn_backward needs, or 0 for arguments it rejects.  Pure
+ * host function. */
+size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode);
+
 /* Synchronises `stream`, then reads and clears the device status word on the
  * current device.  Returns LDN_OK, LDN_ERR_TIMEOUT (a kernel abandoned a
  * bounded wait and left its outputs incomplete) or LDN_ERR_CUDA. */

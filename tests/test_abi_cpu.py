@@ -334,3 +334,46 @@ def test_select_answers_for_gdn2(lib):
     assert ldn.ldn_chunk_fwd_select_ws(1, 64, 1, 128, 128, 64, ldn.LDN_GDN2, 0, big) == ldn.LDN_VARIANT_SIMT
     fam = ldn.ldn_chunk_fwd_select_ws(8, 4096, 16, 128, 128, 64, ldn.LDN_GDN2, 1, big)
     assert fam in (ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_SPLIT)
+
+
+def _bwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, gate=FAKE, S0=None, dout=FAKE, dsf=None, dq=FAKE, dk=FAKE,
+             dv=FAKE, dbeta=FAKE, dgate=FAKE, dS0=FAKE, B=1, T=64, H=1, dkd=64, dvd=64, mode=1, dtype=1,
+             ws=FAKE, wsb=1 << 40, stream=None)
+    a.update(kw)
+    return ldn.ldn_backward(a["q"], a["k"], a["v"], a["beta"], a["gate"], a["S0"], a["dout"], a["dsf"], a["dq"],
+                            a["dk"], a["dv"], a["dbeta"], a["dgate"], a["dS0"], a["B"], a["T"], a["H"], a["dkd"],
+                            a["dvd"], a["mode"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dout=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dS0=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dgate=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None, mode=2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(ws=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(wsb=1024), ldn.LDN_ERR_INVALID_ARG),              # workspace too small
+    (dict(ws=FAKE + 8), ldn.LDN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dbeta=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(mode=ldn.LDN_GDN2), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dtype=3), ldn.LDN_ERR_INVALID_ARG),
+    (dict(B=0), ldn.LDN_ERR_INVALID_ARG),
+    (dict(dkd=32), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(mode=0, gate=None, dgate=None, q=None), ldn.LDN_ERR_INVALID_ARG),
+])
+def test_backward_rejects_bad_arguments(lib, kw, want):
+    assert _bwd(**kw) == want
+
+
+def test_backward_workspace_size(lib):
+    """State copies (every eighth state of every column) plus per-32-column partial
+    sums of dq, dk, the gate gradient and dbeta."""
+    B, T, H, dk, dv = 2, 70, 3, 128, 64
+    n, nsub, sl = B * T * H, (T + 7) // 8, dv // 32
+    for mode, gw in ((0, 0), (1, 1), (2, dk)):
+        want = 4 * (B * H * dv * nsub * dk + sl * n * (2 * dk + gw + 1))
+        assert ldn.ldn_backward_workspace_size(B, T, H, dk, dv, mode) == want
+    assert ldn.ldn_backward_workspace_size(B, T, H, 96, dv, 1) == 0
+    assert ldn.ldn_backward_workspace_size(B, T, H, dk, dv, ldn.LDN_GDN2) == 0
