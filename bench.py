@@ -37,6 +37,7 @@ WORKLOAD = "gdn_bf16_b4_t2048_h16_d128"
 EXTRA_WORKLOADS = ("kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
                    "gdn_bf16_long_b1_t65536_h16_d128", "deltanet_fp32_b1_t256_h1_d64", "gdn2_bf16_b8_t4096_h16_d128")
 PROLOGUE_WORKLOADS = ("gdn_prologue_bf16_b4_t2048_h16_d128_w4", "kda_prologue_bf16_b8_t4096_h16_d128_w4")
+BACKWARD_WORKLOADS = ("gdn_bf16_b4_t2048_h16_d128", "kda_bf16_b8_t4096_h16_d128")
 DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000",
                     "gdn2_decode_b64_h16_dk128_dv128_steps1000")
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
@@ -81,6 +82,16 @@ def prologue_bytes(B, T, H, dk, dv, el_bytes, mode, width):
 def rmsnorm_bytes(B, T, H, dv, el_bytes):
     """Algorithmic bytes of ldn_rmsnorm_gated: o and the gate read, y written."""
     return 3 * B * T * H * dv * el_bytes + 4 * dv
+
+
+def backward_bytes(B, T, H, dk, dv, el_bytes, mode):
+    """Bytes ldn_backward must move at least: q, k, v and dout read (el_bytes),
+    beta and gate read, dq, dk, dv, dbeta and dgate written (fp32), dS_final read
+    and dS0 written (fp32)."""
+    n = B * T * H
+    gw = {0: 0, 1: 1, 2: dk}[mode]
+    per = el_bytes * (2 * dk + 2 * dv) + 4 * (1 + gw) + 4 * (2 * dk + dv + 1 + gw)
+    return n * per + 2 * B * H * dk * dv * 4
 
 
 def decode_bytes(B, H, dk, dv, mode):
@@ -500,6 +511,51 @@ def run_ours(args):
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("prologue / epilogue: device status not ok")
 
+    # ---------------- backward (gradients of the forward) ----------------
+    backward = None
+    if not args.no_extra:
+        backward = {}
+        for name in BACKWARD_WORKLOADS:
+            bw = wl.make_chunk(name, seed=rank)
+            bt = bw.torch_inputs("cuda")
+            dout_np, dsf_np = wl.make_upstream(bw, seed=rank + 1)
+            bdo = torch.from_numpy(dout_np).to("cuda", bt["q"].dtype)
+            bdsf = torch.from_numpy(dsf_np).cuda()
+            f32 = dict(dtype=torch.float32, device="cuda")
+            B_, T_, H_, dk_, dv_ = bw.B, bw.T, bw.H, bw.dk, bw.dv
+            gq, gk = torch.empty((B_, T_, H_, dk_), **f32), torch.empty((B_, T_, H_, dk_), **f32)
+            gv, gb = torch.empty((B_, T_, H_, dv_), **f32), torch.empty((B_, T_, H_), **f32)
+            gg = torch.empty(tuple(bt["gate"].shape), **f32)
+            gs0 = torch.empty((B_, H_, dk_, dv_), **f32)
+            need = ldn.ldn_backward_workspace_size(B_, T_, H_, dk_, dv_, bw.mode)
+            bws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            bdt = ldn.LDN_BF16 if bw.dtype == "bf16" else ldn.LDN_F32
+
+            def bstep():
+                st_ = ldn.ldn_backward(P(bt["q"]), P(bt["k"]), P(bt["v"]), P(bt["beta"]), P(bt["gate"]), P(bt["S0"]),
+                                       P(bdo), P(bdsf), P(gq), P(gk), P(gv), P(gb), P(gg), P(gs0), B_, T_, H_, dk_,
+                                       dv_, bw.mode, bdt, bws.data_ptr(), need, sh)
+                if st_ != ldn.LDN_OK:
+                    raise ldn.LdnError(st_, "ldn_backward")
+
+            bstep()
+            bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+            for e0, e1 in bev:
+                flush_l2()
+                e0.record(stream)
+                bstep()
+                e1.record(stream)
+            barrier()
+            launches += 2 * (1 + len(bev))
+            bms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in bev))
+            bb = backward_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(bw.dtype), bw.mode)
+            backward[name] = {"ms_per_call": bms, "tokens_per_s": world * B_ * T_ / (bms / 1e3),
+                              "kernels": "bwd_kernel + bwd_reduce_kernel", "algorithmic_bytes": bb,
+                              "hbm_frac": bb / (bms / 1e3) / 1e9 / hbm_peak, "workspace_bytes": need}
+            del bt, bdo, bdsf, gq, gk, gv, gb, gg, gs0, bws
+        if ldn.device_status() != ldn.LDN_OK:
+            raise RuntimeError("backward: device status not ok")
+
     # ---------------- decode step (bandwidth) ----------------
     decode = None
     if not args.no_decode:
@@ -569,7 +625,7 @@ def run_ours(args):
                        "l2": "flushed before every timed launch (512 MiB write, then 512 MiB read of another buffer: cold and clean)",
                        "parallelism": f"replica x{world} (independent sequences per GPU)"},
             "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
-            "other_workloads": others, "prologue_epilogue": around,
+            "other_workloads": others, "prologue_epilogue": around, "backward": backward,
             "wall_s_timed_region": wall, "decode": decode}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
