@@ -17,12 +17,15 @@
 // the rest).
 //
 // Work split: one CTA of 256 threads per (b, h, 32-column slice of dv).  Lane
-// l of warp w owns value column 4w + (l & 3) and the key rows 8j + (l >> 2),
-// j < dk / 8, in registers: reductions over the rows (p, dr) are shuffles
-// across lanes 4 apart, reductions over the columns (dq, dk, dgate, dbeta) are
-// a two-step halving exchange across the 4 lanes of a row group, then
-// shared-memory adds across the 8 warps, then a plain store of the slice's
-// partial sums; a second kernel adds the slices.
+// l of warp w owns value column l and the key rows w * dk/8 + j, j < dk/8, in
+// registers, so every lane of a warp reads the same rows of q, k and the gates
+// (shared-memory broadcasts).  Reductions over the rows (p, dr) are a partial
+// sum per warp, one exchange through a double-buffered shared array and one
+// barrier per token.  Reductions over the columns (dq, dk and the KDA gate
+// gradient, per row) are a reduce-scatter across the 32 lanes of the warp that
+// owns the rows, so each row has one writer and no atomics are needed; the
+// scalar sums (dbeta, the GDN gate gradient) are warp sums.  Each slice stores
+// its partial sums; a second kernel adds the slices.
 //   Phase 1 walks the sequence forward and stores the state before every block
 //   of 8 tokens (workspace).
 //   Phase 2 walks the blocks in reverse: it reloads the block's checkpoint,
@@ -33,40 +36,73 @@
 namespace ldn {
 namespace {
 
-constexpr int kNC = 32;     // value columns per CTA
+constexpr int kNC = 32;     // value columns per CTA (one per lane)
 constexpr int kBT = 256;    // threads per CTA
+constexpr int kNW = kBT / 32;
 constexpr int kSub = 8;     // tokens per recomputed block
 
 template <int DK>
 struct BwdSmem {
-    static constexpr int RPT = DK / 8;                                   // rows per thread
+    static constexpr int RPT = DK / kNW;                                 // rows per thread (and per warp)
     static constexpr size_t ring = (size_t)kSub * RPT * kBT;            // decayed states h'
     static constexpr size_t floats = ring + 3 * kSub * DK /*q, k, a*/ + 2 * kSub * kNC /*v, dO*/ +
-                                     kSub /*beta*/ + 3 * kSub * DK /*sums dq, dk, dg*/ + kSub /*sum dbeta*/;
+                                     kSub /*beta*/ + 3 * kSub * DK /*sums dq, dk, dg*/ + kSub /*sum dbeta*/ +
+                                     kSub * kNW /*GDN gate-gradient warp sums*/ + 2 * kNW * kNC /*row sums*/;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
-// Sum of v[0..N) over the 4 lanes that differ in bits 0-1 (the 4 columns of a
-// row group), by halving exchanges: on return u[0..N/4) holds the sums of rows
-// j = i + (N/2) (lane & 1) + (N/4) ((lane >> 1) & 1).
+// Reduce-scatter of v[0..N) over the 32 lanes of a warp (N = 16 or 8): on
+// return every lane holds the warp-wide sum of one row, row j(lane) (the lanes
+// sharing a row hold the same value); see row_of.
 template <int N>
-__device__ __forceinline__ void sum_over_columns(const float (&v)[N], float (&u)[N / 4], int lane)
+__device__ __forceinline__ float sum_over_lanes(const float (&v)[N], int lane)
 {
-    float h[N / 2];
-    const bool hi1 = lane & 1, hi2 = lane & 2;
+    float a[N / 2];
+    const bool u16 = lane & 16;
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
-        const float send = hi1 ? v[i] : v[i + N / 2];
-        const float keep = hi1 ? v[i + N / 2] : v[i];
-        h[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        const float send = u16 ? v[i] : v[i + N / 2];
+        const float keep = u16 ? v[i + N / 2] : v[i];
+        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
     }
+    float b[N / 4];
+    const bool u8 = lane & 8;
 #pragma unroll
     for (int i = 0; i < N / 4; ++i) {
-        const float send = hi2 ? h[i] : h[i + N / 4];
-        const float keep = hi2 ? h[i + N / 4] : h[i];
-        u[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        const float send = u8 ? a[i] : a[i + N / 4];
+        const float keep = u8 ? a[i + N / 4] : a[i];
+        b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
     }
+    float c[N / 8];
+    const bool u4 = lane & 4;
+#pragma unroll
+    for (int i = 0; i < N / 8; ++i) {
+        const float send = u4 ? b[i] : b[i + N / 8];
+        const float keep = u4 ? b[i + N / 8] : b[i];
+        c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    float x;
+    if constexpr (N == 16) {
+        const bool u2 = lane & 2;
+        x = (u2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, u2 ? c[0] : c[1], 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+    } else {
+        x = c[0];
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+    }
+    return x;
 }
+// The row whose sum lane `lane` holds after sum_over_lanes<N>, and whether it
+// is the lane that stores it.
+template <int N>
+__device__ __forceinline__ int row_of(int lane)
+{
+    const int j = (N / 2) * ((lane >> 4) & 1) + (N / 4) * ((lane >> 3) & 1) + (N / 8) * ((lane >> 2) & 1);
+    return N == 16 ? j + ((lane >> 1) & 1) : j;
+}
+template <int N>
+__device__ __forceinline__ bool row_writer(int lane) { return N == 16 ? (lane & 1) == 0 : (lane & 3) == 0; }
 
 template <int DK, typename TIn, int MODE>
 __global__ void __launch_bounds__(kBT, 1)
@@ -75,7 +111,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
            const TIn *__restrict__ dout, const float *__restrict__ dSf, float *__restrict__ dv_out,
            float *__restrict__ dS0, float *__restrict__ ckpt, float *__restrict__ part, int T, int H, int dv)
 {
-    constexpr int RPT = DK / 8;
+    constexpr int RPT = BwdSmem<DK>::RPT;
     constexpr int GW = MODE == LDN_KDA ? DK : (MODE == LDN_GDN ? 1 : 0);   // gate width
     extern __shared__ float smb[];
     float *ring = smb;                          // [kSub][RPT][kBT]
@@ -89,17 +125,19 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     float *ak = aq + kSub * DK;
     float *ag = ak + kSub * DK;
     float *ab = ag + kSub * DK;                 // [kSub]
+    float *agw = ab + kSub;                     // [kSub][kNW] GDN gate gradient per warp
+    float *red = agw + kSub * kNW;              // [2][kNW][kNC] row-sum exchange
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rg = lane >> 2;                   // row group: rows 8 j + rg
-    const int c = 4 * warp + (lane & 3);        // column within the slice
+    const int r0 = warp * RPT;                  // first key row of this warp
     const int slices = dv / kNC;
     const int unit = blockIdx.x / slices, sl = blockIdx.x % slices;
     const int b = unit / H, h = unit % H;
-    const int col = sl * kNC + c;
+    const int col = sl * kNC + lane;
     const int nsub = (T + kSub - 1) / kSub;
     const size_t N = (size_t)gridDim.x / slices * T;   // token-heads (B * H * T)
     float *myck = ckpt + (size_t)blockIdx.x * nsub * RPT * kBT;
+    int par = 0;                                // parity of the row-sum buffer
 
     auto tok = [&](int t) { return ((size_t)b * T + t) * H + h; };
     // Inputs of block s into shared memory (rows past T: zero, decay 1).
@@ -127,10 +165,21 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
             if (MODE == LDN_GDN) as[tid * DK] = ok ? expf(gate[i]) : 1.f;
         }
         if (grads)
-            for (int e = tid; e < 3 * kSub * DK + kSub; e += kBT) aq[e] = 0.f;   // aq, ak, ag, ab
+            for (int e = tid; e < 3 * kSub * DK + kSub + kSub * kNW; e += kBT) aq[e] = 0.f;   // aq .. agw
     };
     auto decay = [&](int t, int j) -> float {
-        return MODE == LDN_KDA ? as[t * DK + 8 * j + rg] : (MODE == LDN_GDN ? as[t * DK] : 1.f);
+        return MODE == LDN_KDA ? as[t * DK + r0 + j] : (MODE == LDN_GDN ? as[t * DK] : 1.f);
+    };
+    // Sum over the key rows of this thread's column (all warps): one barrier.
+    auto row_sum = [&](float x) -> float {
+        float *rb = red + par * kNW * kNC;
+        rb[warp * kNC + lane] = x;
+        __syncthreads();
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) s += rb[w * kNC + lane];
+        par ^= 1;
+        return s;
     };
     // One forward token step on the thread's state rows; returns r and v - p.
     auto fwd_step = [&](int t, float (&hr)[RPT], float &r, float &e) {
@@ -138,21 +187,19 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
             hr[j] *= decay(t, j);
-            p += hr[j] * ks[t * DK + 8 * j + rg];
+            p += hr[j] * ks[t * DK + r0 + j];
         }
-        p += __shfl_xor_sync(0xffffffffu, p, 4);
-        p += __shfl_xor_sync(0xffffffffu, p, 8);
-        p += __shfl_xor_sync(0xffffffffu, p, 16);
-        e = vs[t * kNC + c] - p;
+        p = row_sum(p);
+        e = vs[t * kNC + lane] - p;
         r = bs[t] * e;
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) hr[j] += ks[t * DK + 8 * j + rg] * r;
+        for (int j = 0; j < RPT; ++j) hr[j] += ks[t * DK + r0 + j] * r;
     };
 
     // ---- phase 1: forward, checkpoint before every block
     float hr[RPT];
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) hr[j] = S0 ? S0[((size_t)unit * DK + 8 * j + rg) * dv + col] : 0.f;
+    for (int j = 0; j < RPT; ++j) hr[j] = S0 ? S0[((size_t)unit * DK + r0 + j) * dv + col] : 0.f;
     for (int s = 0; s < nsub; ++s) {
         __syncthreads();
         stage(s, false);
@@ -169,9 +216,11 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     // ---- phase 2: blocks in reverse
     float g[RPT];
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) g[j] = dSf ? dSf[((size_t)unit * DK + 8 * j + rg) * dv + col] : 0.f;
+    for (int j = 0; j < RPT; ++j) g[j] = dSf ? dSf[((size_t)unit * DK + r0 + j) * dv + col] : 0.f;
     float *pq = part, *pk = pq + (size_t)slices * N * DK, *pg = pk + (size_t)slices * N * DK;
     float *pb = pg + (size_t)slices * N * GW;
+    const int jrow = row_of<RPT>(lane);
+    const bool writer = row_writer<RPT>(lane);
     for (int s = nsub - 1; s >= 0; --s) {
         const int t0 = s * kSub;
         __syncthreads();
@@ -190,54 +239,50 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
 #pragma unroll
         for (int t = kSub - 1; t >= 0; --t) {
             if (t0 + t >= T) continue;   // uniform over the CTA
-            const float dO = ds[t * kNC + c], bt = bs[t];
+            const float dO = ds[t * kNC + lane], bt = bs[t];
             float hp[RPT], vq[RPT], vk[RPT], vg[RPT];
             float dr = 0.f;
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                const int row = 8 * j + rg;
-                const float kr = ks[t * DK + row];
+                const float kr = ks[t * DK + r0 + j];
                 hp[j] = ring[((size_t)t * RPT + j) * kBT + tid];
                 vq[j] = (hp[j] + kr * rr[t]) * dO;       // h_t * dO
-                g[j] += qs[t * DK + row] * dO;
+                g[j] += qs[t * DK + r0 + j] * dO;
                 dr += g[j] * kr;
             }
-            dr += __shfl_xor_sync(0xffffffffu, dr, 4);
-            dr += __shfl_xor_sync(0xffffffffu, dr, 8);
-            dr += __shfl_xor_sync(0xffffffffu, dr, 16);
-            if (rg == 0) dv_out[tok(t0 + t) * dv + col] = bt * dr;
+            dr = row_sum(dr);
+            if (warp == 0) dv_out[tok(t0 + t) * dv + col] = bt * dr;
             const float dp = -bt * dr;
             float gsum = 0.f;
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                const float kr = ks[t * DK + 8 * j + rg];
+                const float kr = ks[t * DK + r0 + j];
                 vk[j] = g[j] * rr[t] + hp[j] * dp;
                 g[j] += kr * dp;                         // dL/dh'
                 vg[j] = g[j] * hp[j];
                 gsum += vg[j];
             }
-            // column sums: dq, dk (and dgate for KDA) per row, dbeta and the GDN dgate per token
-            float uq[RPT / 4], uk[RPT / 4], ug[RPT / 4];
-            sum_over_columns<RPT>(vq, uq, lane);
-            sum_over_columns<RPT>(vk, uk, lane);
-            if (MODE == LDN_KDA) sum_over_columns<RPT>(vg, ug, lane);
-            const int jo = (lane & 1) * (RPT / 2) + ((lane >> 1) & 1) * (RPT / 4);
-#pragma unroll
-            for (int i = 0; i < RPT / 4; ++i) {
-                const int row = 8 * (jo + i) + rg;
-                atomicAdd(&aq[t * DK + row], uq[i]);
-                atomicAdd(&ak[t * DK + row], uk[i]);
-                if (MODE == LDN_KDA) atomicAdd(&ag[t * DK + row], ug[i]);
+            // column sums of this warp's rows: one writer per row
+            const float sq = sum_over_lanes<RPT>(vq, lane);
+            const float sk = sum_over_lanes<RPT>(vk, lane);
+            if (writer) {
+                aq[t * DK + r0 + jrow] = sq;
+                ak[t * DK + r0 + jrow] = sk;
             }
-            float db = rg == 0 ? dr * ee[t] : 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                db += __shfl_xor_sync(0xffffffffu, db, o);
-                if (MODE == LDN_GDN) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+            if (MODE == LDN_KDA) {
+                const float sg = sum_over_lanes<RPT>(vg, lane);
+                if (writer) ag[t * DK + r0 + jrow] = sg;
             }
-            if (lane == 0) {
-                atomicAdd(&ab[t], db);
-                if (MODE == LDN_GDN) atomicAdd(&ag[t * DK], gsum);
+            if (MODE == LDN_GDN) {
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+                if (lane == 0) agw[t * kNW + warp] = gsum;
+            }
+            if (warp == 0) {   // dbeta: every warp holds the same dr; warp 0 sums the columns
+                float db = dr * ee[t];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
+                if (lane == 0) ab[t] = db;
             }
 #pragma unroll
             for (int j = 0; j < RPT; ++j) g[j] *= decay(t, j);   // dL/dh_{t-1}
@@ -255,11 +300,16 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
         if (tid < kSub && t0 + tid < T) {
             const size_t n = tok(t0 + tid);
             pb[(size_t)sl * N + n] = ab[tid];
-            if (MODE == LDN_GDN) pg[(size_t)sl * N + n] = ag[tid * DK];
+            if (MODE == LDN_GDN) {
+                float sg = 0.f;
+#pragma unroll
+                for (int w = 0; w < kNW; ++w) sg += agw[tid * kNW + w];
+                pg[(size_t)sl * N + n] = sg;
+            }
         }
     }
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) dS0[((size_t)unit * DK + 8 * j + rg) * dv + col] = g[j];
+    for (int j = 0; j < RPT; ++j) dS0[((size_t)unit * DK + r0 + j) * dv + col] = g[j];
 }
 
 // Sum of the slices' partial sums: dq, dk [N][dk], dgate [N][gw], dbeta [N].
