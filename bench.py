@@ -638,15 +638,16 @@ def run_ours(args):
 
 def run_profile_case(args):
     """Two untimed calls of one operation on a given shape (a small case for an
-    ncu capture): backward (ldn_backward) or gdn2 (ldn_chunk_fwd_gdn2, auto
-    variant), bf16, d = 128, the workload recipe of the named mode."""
+    ncu capture): backward-gdn / backward-kda (ldn_backward), gdn2
+    (ldn_chunk_fwd_gdn2) or kda (ldn_chunk_fwd_noalloc), automatic variant,
+    bf16, d = 128, the workload recipe of the named mode."""
     import torch
     import gated_delta_rule_chunkwise_gb300 as ldn
     from gated_delta_rule_chunkwise_gb300 import workloads as wl
     ldn.load()
     B, T, H = (int(x) for x in args.shape.split(","))
     name = {"backward-gdn": "gdn_bf16_b4_t2048_h16_d128", "backward-kda": "kda_bf16_b8_t4096_h16_d128",
-            "gdn2": "gdn2_bf16_b8_t4096_h16_d128"}[args.profile]
+            "gdn2": "gdn2_bf16_b8_t4096_h16_d128", "kda": "kda_bf16_b8_t4096_h16_d128"}[args.profile]
     w = wl.make_chunk(name, B=B, T=T, H=H)
     t = w.torch_inputs("cuda")
     if args.profile.startswith("backward"):
@@ -655,9 +656,18 @@ def run_profile_case(args):
         f = torch.from_numpy(dsf).cuda()
         for _ in range(2):
             ldn.backward(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"], d, f, mode=w.mode)
-    else:
+    elif args.profile == "gdn2":
         for _ in range(2):
             ldn.chunk_fwd_gdn2(t["q"], t["k"], t["v"], t["erase"], t["write"], t["gate"], t["S0"])
+    else:
+        out = torch.empty_like(t["v"])
+        for _ in range(2):
+            st = ldn.ldn_chunk_fwd_noalloc(t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(),
+                                           t["beta"].data_ptr(), t["gate"].data_ptr(), 0, out.data_ptr(), 0,
+                                           B, T, H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16, ldn.LDN_VARIANT_AUTO,
+                                           torch.cuda.current_stream().cuda_stream)
+            if st != ldn.LDN_OK:
+                raise ldn.LdnError(st, "ldn_chunk_fwd_noalloc")
     torch.cuda.synchronize()
     st = ldn.device_status()
     print(json.dumps({"profile_case": args.profile, "shape": [B, T, H], "status": st}))
@@ -677,7 +687,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workload lines")
-    ap.add_argument("--profile", choices=["backward-gdn", "backward-kda", "gdn2"],
+    ap.add_argument("--profile", choices=["backward-gdn", "backward-kda", "gdn2", "kda"],
                     help="run one operation twice, untimed, on --shape (a small case for ncu) and exit")
     ap.add_argument("--shape", default="1,2048,16", help="B,T,H for --profile")
     args = ap.parse_args()
