@@ -22,6 +22,11 @@ the notes' matrix expansion.  The backward (``bwd``, the reverse-mode derivative
 of the same recurrence) is pinned in tests/test_bwd_oracle_pins.py by central
 finite differences of the forward oracle on every input and the initial state,
 and by the exact linearity identities of the recurrence in (v, S0) and in q.
+RLA / RDN (``fwd_rla``, Residual Linear Attention notes Sec. 2.2, 2.4) are pinned
+in tests/test_rla_oracle_pins.py: RLA against its closed form (decayed sums of
+the writes, written in numpy), RDN against the composition of the Gated DeltaNet
+oracle for both states, the notes' one-step expansion of the output, and the
+clip bound.
 """
 from __future__ import annotations
 
@@ -68,6 +73,9 @@ def _load():
             g2 = lib.ldn_oracle_fwd_gdn2
             g2.restype = ctypes.c_int
             g2.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int)]
+            rl = lib.ldn_oracle_rla
+            rl.restype = ctypes.c_int
+            rl.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_float] + [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7
             bw = lib.ldn_oracle_bwd
             bw.restype = ctypes.c_int
             bw.argtypes = [ctypes.c_void_p] * 14 + [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)]
@@ -166,6 +174,34 @@ def bwd(q, k, v, beta, gate, S0, dout, dS_final=None, mode=MODE_DELTANET, nthrea
     if rc != 0:
         raise RuntimeError(f"ldn_oracle_bwd failed with {rc}")
     return g
+
+
+def fwd_rla(q, k, v, beta, gamma, gate, clip=1.0, S0=None, R0=None, delta=False, nthreads=0):
+    """Residual Linear Attention (delta=False) or Residual DeltaNet (delta=True) in
+    fp64 (Residual Linear Attention notes, Sec. 2.2 and 2.4; see ldn_oracle.c).
+
+    q, k [B,T,H,dk]; v [B,T,H,dv]; beta, gamma, gate (log alpha) [B,T,H];
+    clip c > 0 (np.inf: none); S0, R0 [B,H,dk,dv] or None.
+    Returns (o [B,T,H,dv], S_final, R_final), all float64."""
+    q, k, v = _f32(q, "q"), _f32(k, "k"), _f32(v, "v")
+    beta, gamma, gate = _f32(beta, "beta"), _f32(gamma, "gamma"), _f32(gate, "gate")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, T, H) or any(a.shape != (B, T, H) for a in (beta, gamma, gate)):
+        raise ValueError("oracle: inconsistent shapes")
+    S0, R0 = _f32(S0, "S0"), _f32(R0, "R0")
+    out = np.empty((B, T, H, dv))
+    sf, rf = np.empty((B, H, dk, dv)), np.empty((B, H, dk, dv))
+    c = float(clip)
+    if not c > 0:
+        raise ValueError("oracle: clip must be > 0")
+    rc = _load().ldn_oracle_rla(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(gate),
+                                ctypes.c_float(np.float32(c) if np.isfinite(c) else np.float32(np.inf)),
+                                _ptr(S0), _ptr(R0), _ptr(out), _ptr(sf), _ptr(rf), B, T, H, dk, dv,
+                                int(bool(delta)), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"ldn_oracle_rla failed with {rc}")
+    return out, sf, rf
 
 
 def fwd_gdn2(q, k, v, erase, write, gate, S0=None, nthreads=0, want_state=True):

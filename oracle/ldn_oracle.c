@@ -364,6 +364,155 @@ int ldn_oracle_fwd_gdn2(const float *q, const float *k, const float *v,
     return run_job(&J, nthreads, threads_used);
 }
 
+/*
+ * Residual Linear Attention (RLA) and Residual DeltaNet (RDN), "Residual Linear
+ * Attention" reading notes, Sec. 2.2 (the boxed final form) and Sec. 2.4.  Per
+ * token, with alpha = exp(gate) and the base state W and residual state R both
+ * d_v x d_k:
+ *   r  = Clip_[-c, c](v - W_{t-1} k)        (the OLD base state, neither decayed
+ *                                            nor written yet; c = INFINITY: no clip)
+ *   o  = alpha W_{t-1} q + gamma R_t q      (the UPDATED residual state)
+ *   RLA: R_t = alpha R_{t-1} + gamma r k^T,  W_t = alpha W_{t-1} + beta v k^T
+ *   RDN: R_t = alpha R_{t-1} (I - gamma k k^T) + gamma r k^T,
+ *        W_t = alpha W_{t-1} (I - beta k k^T) + beta v k^T
+ * The order follows the notes' pseudo-code: residual from the old base state,
+ * update R, output, update W.
+ */
+typedef struct {
+    const float *q, *k, *v, *beta, *gamma, *gate, *S0, *R0;
+    float clip;
+    int delta;   /* 0: RLA (additive updates), 1: RDN (delta updates) */
+    double *out, *S_final, *R_final;
+    int B, T, H, dk, dv;
+    int next_unit;
+    pthread_mutex_t lock;
+} rla_job_t;
+
+static void rla_unit(const rla_job_t *J, int unit, double *W, double *R, double *tmp)
+{
+    const int b = unit / J->H, h = unit % J->H;
+    const int dk = J->dk, dv = J->dv, H = J->H, T = J->T;
+    const size_t D2 = (size_t)dk * dv;
+    const float *init[2] = {J->S0, J->R0};
+    double *st[2] = {W, R};
+    for (int m = 0; m < 2; ++m) {
+        if (init[m]) {
+            const float *s0 = init[m] + ((size_t)b * H + h) * D2;
+            for (int c = 0; c < dk; ++c)
+                for (int i = 0; i < dv; ++i) st[m][(size_t)i * dk + c] = (double)s0[(size_t)c * dv + i];
+        } else {
+            memset(st[m], 0, sizeof(double) * D2);
+        }
+    }
+    const double clip = (double)J->clip;
+    for (int t = 0; t < T; ++t) {
+        const size_t tok = ((size_t)b * T + t) * H + h;
+        const float *q = J->q + tok * dk, *k = J->k + tok * dk, *v = J->v + tok * dv;
+        const double alpha = exp((double)J->gate[tok]), beta = (double)J->beta[tok], gamma = (double)J->gamma[tok];
+        double *o = J->out + tok * dv;
+        /* residual against the old base state; base read alpha W_{t-1} q into o */
+        for (int i = 0; i < dv; ++i) {
+            double pk = 0.0, sq = 0.0;
+            for (int c = 0; c < dk; ++c) {
+                pk += W[(size_t)i * dk + c] * (double)k[c];
+                sq += W[(size_t)i * dk + c] * (double)q[c];
+            }
+            double r = (double)v[i] - pk;
+            if (r > clip) r = clip;
+            if (r < -clip) r = -clip;
+            tmp[i] = r;
+            o[i] = alpha * sq;
+        }
+        /* residual state */
+        for (int i = 0; i < dv; ++i) {
+            double rk = 0.0;
+            for (int c = 0; c < dk; ++c) rk += R[(size_t)i * dk + c] * (double)k[c];
+            const double w = gamma * (tmp[i] - (J->delta ? alpha * rk : 0.0));
+            for (int c = 0; c < dk; ++c) R[(size_t)i * dk + c] = alpha * R[(size_t)i * dk + c] + w * (double)k[c];
+        }
+        /* output: alpha W_{t-1} q + gamma R_t q */
+        for (int i = 0; i < dv; ++i) {
+            double rq = 0.0;
+            for (int c = 0; c < dk; ++c) rq += R[(size_t)i * dk + c] * (double)q[c];
+            o[i] += gamma * rq;
+        }
+        /* base state */
+        for (int i = 0; i < dv; ++i) {
+            double wk = 0.0;
+            for (int c = 0; c < dk; ++c) wk += W[(size_t)i * dk + c] * (double)k[c];
+            const double w = beta * ((double)v[i] - (J->delta ? alpha * wk : 0.0));
+            for (int c = 0; c < dk; ++c) W[(size_t)i * dk + c] = alpha * W[(size_t)i * dk + c] + w * (double)k[c];
+        }
+    }
+    double *fin[2] = {J->S_final, J->R_final};
+    for (int m = 0; m < 2; ++m) {
+        if (!fin[m]) continue;
+        double *sf = fin[m] + ((size_t)b * H + h) * D2;
+        for (int c = 0; c < dk; ++c)
+            for (int i = 0; i < dv; ++i) sf[(size_t)c * dv + i] = st[m][(size_t)i * dk + c];
+    }
+}
+
+static void *rla_worker(void *arg)
+{
+    rla_job_t *J = (rla_job_t *)arg;
+    const size_t D2 = (size_t)J->dk * J->dv;
+    double *W = (double *)malloc(sizeof(double) * D2), *R = (double *)malloc(sizeof(double) * D2);
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)J->dv);
+    if (!W || !R || !tmp) { free(W); free(R); free(tmp); return (void *)1; }
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        const int unit = J->next_unit++;
+        pthread_mutex_unlock(&J->lock);
+        if (unit >= J->B * J->H) break;
+        rla_unit(J, unit, W, R, tmp);
+    }
+    free(W); free(R); free(tmp);
+    return NULL;
+}
+
+/*
+ * ldn_oracle_rla: RLA (delta = 0) or RDN (delta = 1) for every (batch, head).
+ *   q, k [B][T][H][dk]; v [B][T][H][dv]; beta, gamma, gate (log alpha) [B][T][H];
+ *   clip c > 0 (INFINITY: none); S0, R0 [B][H][dk][dv] or NULL (zeros).
+ *   out [B][T][H][dv] fp64; S_final, R_final [B][H][dk][dv] fp64 or NULL.
+ */
+int ldn_oracle_rla(const float *q, const float *k, const float *v, const float *beta, const float *gamma,
+                   const float *gate, float clip, const float *S0, const float *R0, double *out, double *S_final,
+                   double *R_final, int B, int T, int H, int dk, int dv, int delta, int nthreads)
+{
+    if (!q || !k || !v || !beta || !gamma || !gate || !out) return -1;
+    if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1 || !(clip > 0.0f)) return -1;
+    rla_job_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.beta = beta; J.gamma = gamma; J.gate = gate; J.S0 = S0; J.R0 = R0;
+    J.clip = clip; J.delta = delta ? 1 : 0;
+    J.out = out; J.S_final = S_final; J.R_final = R_final;
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv;
+    pthread_mutex_init(&J.lock, NULL);
+    const int units = B * H;
+    if (nthreads <= 0) nthreads = ldn_oracle_default_threads();
+    if (nthreads > units) nthreads = units > 0 ? units : 1;
+    int rc = 0;
+    if (units > 0) {
+        pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+        if (!tid) { pthread_mutex_destroy(&J.lock); return -2; }
+        int started = 0;
+        for (int i = 0; i < nthreads; ++i) {
+            if (pthread_create(&tid[i], NULL, rla_worker, &J) != 0) { rc = -2; break; }
+            ++started;
+        }
+        for (int i = 0; i < started; ++i) {
+            void *ret = NULL;
+            pthread_join(tid[i], &ret);
+            if (ret) rc = -2;
+        }
+        free(tid);
+    }
+    pthread_mutex_destroy(&J.lock);
+    return rc;
+}
+
 static int run_job(job_t *J_, int nthreads, int *threads_used)
 {
     job_t J = *J_;

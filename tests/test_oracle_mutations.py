@@ -39,6 +39,15 @@ MUTANTS = {
     # Gated DeltaNet-2: the write gate is not applied to the value
     "gdn2_no_write": ("const double target = gdn2 ? (double)ww[i] * (double)v[i] : (double)v[i];",
                       "const double target = (double)v[i];"),
+    # RLA / RDN: the residual read from the decayed base state instead of the old one
+    "rla_residual_decayed": ("double r = (double)v[i] - pk;", "double r = (double)v[i] - alpha * pk;"),
+    # RLA / RDN: the correction read without its gamma
+    "rla_output_no_gamma": ("o[i] += gamma * rq;", "o[i] += rq;"),
+    # RLA / RDN: the residual clipped from above only
+    "rla_clip_one_sided": ("if (r < -clip) r = -clip;", "(void)0;"),
+    # RDN: the residual state's delta correction without the decay
+    "rdn_correction_undecayed": ("const double w = gamma * (tmp[i] - (J->delta ? alpha * rk : 0.0));",
+                                 "const double w = gamma * (tmp[i] - (J->delta ? rk : 0.0));"),
     # backward: the key gradient misses its write term (G^T r)
     "bwd_dk_no_write": ("s += G[(size_t)i * dk + c] * r[i] + Wt[(size_t)i * dk + c] * dp[i];",
                         "s += Wt[(size_t)i * dk + c] * dp[i];"),
@@ -69,6 +78,7 @@ def test_pins_catch_mutant(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_gdn2_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_bwd_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_bwd_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_rla_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
