@@ -8,10 +8,12 @@ Two layers:
   * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
     ``ldn_chunk_fwd_workspace_size``, ``ldn_chunk_fwd_noalloc``, ``ldn_decode_step``,
     ``ldn_chunk_fwd_gdn2``, ``ldn_decode_step_gdn2``, ``ldn_backward``,
-    ``ldn_backward_workspace_size``, ``ldn_prologue``, ``ldn_rmsnorm_gated``,
+    ``ldn_backward_workspace_size``, ``ldn_rla_fwd``, ``ldn_rla_workspace_size``, ``ldn_prologue``,
+    ``ldn_rmsnorm_gated``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
-  * ``chunk_fwd``, ``decode_step``, ``chunk_fwd_gdn2``, ``decode_step_gdn2`` and ``backward``:
+  * ``chunk_fwd``, ``decode_step``, ``chunk_fwd_gdn2``, ``decode_step_gdn2``, ``backward`` and
+    ``rla_fwd``:
     the same calls on torch CUDA tensors,
     with shape / dtype checks and allocation of outputs and of the split
     variant's workspace (torch is used for device memory and the current
@@ -57,6 +59,8 @@ _SIGNATURES = {
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
     "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 8 + [_P], _I),
     "ldn_backward": ([_P] * 14 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
+    "ldn_rla_fwd": ([_P] * 6 + [ctypes.c_float] + [_P] * 5 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
+    "ldn_rla_workspace_size": ([_I] * 5, ctypes.c_size_t),
     "ldn_backward_workspace_size": ([_I] * 6, ctypes.c_size_t),
     "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
@@ -148,6 +152,16 @@ def ldn_backward(q, k, v, beta, gate, S0, dout, dS_final, dq, dk, dv, dbeta, dga
 
 def ldn_backward_workspace_size(B, T, H, dk, dv, mode):
     return load().ldn_backward_workspace_size(B, T, H, dk, dv, mode)
+
+
+def ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv, delta, dtype,
+                workspace, workspace_bytes, stream):
+    return load().ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv,
+                              delta, dtype, workspace, workspace_bytes, stream)
+
+
+def ldn_rla_workspace_size(B, T, H, dv, dtype):
+    return load().ldn_rla_workspace_size(B, T, H, dv, dtype)
 
 
 def ldn_prologue(q_in, k_in, v_in, conv_q, conv_k, conv_v, width, beta_logit, gate_z, gate_a, gate_b,
@@ -376,6 +390,33 @@ def backward(q, k, v, beta, gate, S0, dout, dS_final=None, *, mode, workspace=No
     if st != LDN_OK:
         raise LdnError(st, "ldn_backward")
     return g
+
+
+def rla_fwd(q, k, v, beta, gamma, gate, S0=None, R0=None, *, clip=1.0, delta=False, workspace=None, stream=None):
+    """RLA (delta=False) or RDN (delta=True) forward on torch CUDA tensors
+    (ldn_rla_fwd).  q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16); beta,
+    gamma, gate [B,T,H] float32; S0, R0 [B,H,dk,dv] float32 or None.
+    Returns (out, S_final, R_final)."""
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q"); _check(k, "k", q.shape, q.dtype); _check(v, "v", (B, T, H, dv), q.dtype)
+    for name, t in (("beta", beta), ("gamma", gamma), ("gate", gate)):
+        _check(t, name, (B, T, H), torch.float32)
+    _check(S0, "S0", (B, H, dk, dv), torch.float32); _check(R0, "R0", (B, H, dk, dv), torch.float32)
+    out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    sf = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    rf = torch.empty_like(sf)
+    need = ldn_rla_workspace_size(B, T, H, dv, _dtype_code(q))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = ldn_rla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(gate), float(clip), _ptr(S0), _ptr(R0),
+                     _ptr(out), _ptr(sf), _ptr(rf), B, T, H, dk, dv, int(bool(delta)), _dtype_code(q),
+                     _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if st != LDN_OK:
+        raise LdnError(st, "ldn_rla_fwd")
+    return out, sf, rf
 
 
 def device_status(stream=None) -> int:

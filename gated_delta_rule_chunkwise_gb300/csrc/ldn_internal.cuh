@@ -22,7 +22,15 @@ struct ChunkArgs {
     int B, T, H, dk, dv, chunk, mode, dtype;
     int *status;
     const float *erase = nullptr, *write = nullptr;   // Gated DeltaNet-2: b [B][T][H][dk], w [B][T][H][dv]
+    // SIMT kernel, scalar decay: reads of the state before each token's write
+    // (S_{t-1} k_t and alpha_t S_{t-1} q_t, fp32 [B][T][H][dv]) when not NULL
+    float *pk_out = nullptr, *sq_out = nullptr;
 };
+// Internal modes of the SIMT chunk kernel (not in the public enum): the additive
+// update with scalar decay (Residual Linear Attention's states), and Gated
+// DeltaNet with the pre-update reads written.
+constexpr int kModeAdditive = 16;
+constexpr int kModeGdnEmit = 17;
 
 struct DecodeArgs {
     const void *q, *k, *v;
@@ -84,6 +92,20 @@ struct BwdArgs {
     float *ws;   // checkpoints, then the per-slice partial sums
     int B, T, H, dk, dv, mode, dtype;
 };
+// Residual Linear Attention / Residual DeltaNet forward (csrc/rla.cu).
+struct RlaArgs {
+    const void *q, *k, *v;
+    const float *beta, *gamma, *gate, *S0, *R0;
+    float clip;
+    void *out;
+    float *S_final, *R_final;
+    void *ws;
+    int B, T, H, dk, dv, delta, dtype;
+    int *status;
+};
+size_t rla_off(size_t bytes);   // 256-byte rounding of the workspace sections
+size_t rla_workspace_bytes(int B, int T, int H, int dv, int dtype);
+cudaError_t launch_rla(const RlaArgs &a, cudaStream_t stream);
 size_t bwd_ckpt_floats(int B, int T, int H, int dk, int dv);
 size_t bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int mode);
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t stream);

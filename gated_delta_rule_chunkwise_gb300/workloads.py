@@ -152,6 +152,33 @@ def make_decode(name: str = "gdn_decode_b64_h16_dk128_dv128_steps1000", seed: in
                     erase=erase, write=write)
 
 
+# ---- Residual Linear Attention / Residual DeltaNet inputs --------------------------
+# Recipe: the Gated DeltaNet draws in the same order (q, k, v, beta logits, gate
+# noise, S0), then gamma = sigmoid(N(0, 1)) per (b, t, h) and R0 ~ N(0, 0.02^2)
+# when the workload has initial states.  The notes' main experiments clip at
+# c = 1; alpha, beta, gamma follow their parameterisations (Mamba2-style decay,
+# sigmoid strengths).  The pages give RLA no workload of its own: the Gated
+# DeltaNet bench shape stands in.
+RLA_WORKLOADS = {
+    "rla_bf16_b4_t2048_h16_d128": dict(delta=False, dtype="bf16", B=4, T=2048, H=16, dk=128, dv=128, s0=False),
+    "rdn_bf16_b4_t2048_h16_d128": dict(delta=True, dtype="bf16", B=4, T=2048, H=16, dk=128, dv=128, s0=False),
+}
+
+
+def make_rla(name: str = "rdn_bf16_b4_t2048_h16_d128", seed: int = 0, **over) -> dict:
+    """Inputs of ldn_rla_fwd as float32 numpy arrays (bf16 values exact in fp32)."""
+    r = dict(RLA_WORKLOADS[name]); r.update(over)
+    rng = np.random.default_rng(seed)
+    q, k, v, beta, gate, S0, _, _ = _draw(rng, (r["B"], r["T"]), MODE_GDN, r["dtype"], r["H"], r["dk"], r["dv"],
+                                          r["s0"], r["B"])
+    f32 = np.float32
+    gamma = _sigmoid(rng.standard_normal((r["B"], r["T"], r["H"]), dtype=f32))
+    R0 = (rng.standard_normal((r["B"], r["H"], r["dk"], r["dv"]), dtype=f32) * f32(0.02)).astype(f32) \
+        if r["s0"] else None
+    return dict(name=name, delta=r["delta"], dtype=r["dtype"], B=r["B"], T=r["T"], H=r["H"], dk=r["dk"], dv=r["dv"],
+                q=q, k=k, v=v, beta=beta, gamma=gamma, gate=gate, S0=S0, R0=R0, clip=float(r.get("clip", 1.0)))
+
+
 def make_upstream(w: Workload, seed: int = 1, final_state: bool = True):
     """Upstream gradients for the backward of a chunk workload: dout ~ N(0, 1)
     shaped like v (rounded to bf16 for bf16 workloads, as the kernels read it in
