@@ -37,6 +37,7 @@ WORKLOAD = "gdn_bf16_b4_t2048_h16_d128"
 EXTRA_WORKLOADS = ("kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
                    "gdn_bf16_long_b1_t65536_h16_d128", "deltanet_fp32_b1_t256_h1_d64", "gdn2_bf16_b8_t4096_h16_d128")
 PROLOGUE_WORKLOADS = ("gdn_prologue_bf16_b4_t2048_h16_d128_w4", "kda_prologue_bf16_b8_t4096_h16_d128_w4")
+RLA_WORKLOADS = ("rla_bf16_b4_t2048_h16_d128", "rdn_bf16_b4_t2048_h16_d128")
 BACKWARD_WORKLOADS = ("gdn_bf16_b4_t2048_h16_d128", "kda_bf16_b8_t4096_h16_d128")
 DECODE_WORKLOADS = ("gdn_decode_b64_h16_dk128_dv128_steps1000", "gdn_decode_b64_h16_dk64_dv128_steps1000",
                     "gdn2_decode_b64_h16_dk128_dv128_steps1000")
@@ -92,6 +93,12 @@ def backward_bytes(B, T, H, dk, dv, el_bytes, mode):
     gw = {0: 0, 1: 1, 2: dk}[mode]
     per = el_bytes * (2 * dk + 2 * dv) + 4 * (1 + gw) + 4 * (2 * dk + dv + 1 + gw)
     return n * per + 2 * B * H * dk * dv * 4
+
+
+def rla_bytes(B, T, H, dk, dv, el_bytes):
+    """Bytes ldn_rla_fwd must move at least: q, k, v read and o written (el_bytes),
+    beta, gamma and the gate read (fp32), both final states written (fp32)."""
+    return B * T * H * (el_bytes * (2 * dk + 2 * dv) + 12) + 2 * B * H * dk * dv * 4
 
 
 def decode_bytes(B, H, dk, dv, mode):
@@ -556,6 +563,49 @@ def run_ours(args):
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("backward: device status not ok")
 
+    # ---------------- Residual Linear Attention / Residual DeltaNet ----------------
+    rla = None
+    if not args.no_extra:
+        rla = {}
+        for name in RLA_WORKLOADS:
+            rp = wl.make_rla(name, seed=rank)
+            rel = torch.bfloat16 if rp["dtype"] == "bf16" else torch.float32
+            rd = lambda a, dt=torch.float32: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dt)
+            rq, rk, rv = rd(rp["q"], rel), rd(rp["k"], rel), rd(rp["v"], rel)
+            rb, rgm, rgt = rd(rp["beta"]), rd(rp["gamma"]), rd(rp["gate"])
+            B_, T_, H_, dk_, dv_ = rp["B"], rp["T"], rp["H"], rp["dk"], rp["dv"]
+            rout = torch.empty((B_, T_, H_, dv_), dtype=rel, device="cuda")
+            rsf = torch.empty((B_, H_, dk_, dv_), dtype=torch.float32, device="cuda")
+            rrf = torch.empty_like(rsf)
+            rdt = ldn.LDN_BF16 if rp["dtype"] == "bf16" else ldn.LDN_F32
+            rneed = ldn.ldn_rla_workspace_size(B_, T_, H_, dv_, rdt)
+            rws = torch.empty(rneed, dtype=torch.uint8, device="cuda")
+
+            def rstep():
+                st_ = ldn.ldn_rla_fwd(P(rq), P(rk), P(rv), P(rb), P(rgm), P(rgt), rp["clip"], 0, 0, P(rout), P(rsf),
+                                      P(rrf), B_, T_, H_, dk_, dv_, int(rp["delta"]), rdt, rws.data_ptr(), rneed, sh)
+                if st_ != ldn.LDN_OK:
+                    raise ldn.LdnError(st_, "ldn_rla_fwd")
+
+            rstep()
+            rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+            for e0, e1 in rev:
+                flush_l2()
+                e0.record(stream)
+                rstep()
+                e1.record(stream)
+            barrier()
+            launches += 4 * (1 + len(rev))
+            rms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in rev))
+            rbytes = rla_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(rp["dtype"]))
+            stage2 = "chunk_tc_kernel<GDN>" if rp["delta"] else "chunk_simt_kernel<additive>"
+            rla[name] = {"ms_per_call": rms, "tokens_per_s": world * B_ * T_ / (rms / 1e3),
+                         "kernels": f"chunk_simt_kernel (stage 1, pre-update reads) + clip + {stage2} + sum",
+                         "algorithmic_bytes": rbytes, "hbm_frac": rbytes / (rms / 1e3) / 1e9 / hbm_peak}
+            del rq, rk, rv, rb, rgm, rgt, rout, rsf, rrf, rws
+        if ldn.device_status() != ldn.LDN_OK:
+            raise RuntimeError("rla: device status not ok")
+
     # ---------------- decode step (bandwidth) ----------------
     decode = None
     if not args.no_decode:
@@ -625,7 +675,7 @@ def run_ours(args):
                        "l2": "flushed before every timed launch (512 MiB write, then 512 MiB read of another buffer: cold and clean)",
                        "parallelism": f"replica x{world} (independent sequences per GPU)"},
             "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
-            "other_workloads": others, "prologue_epilogue": around, "backward": backward,
+            "other_workloads": others, "prologue_epilogue": around, "backward": backward, "rla": rla,
             "wall_s_timed_region": wall, "decode": decode}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
