@@ -45,8 +45,9 @@ template <int DK>
 struct BwdSmem {
     static constexpr int RPT = DK / kNW;                                 // rows per thread (and per warp)
     static constexpr size_t ring = (size_t)kSub * RPT * kBT;            // decayed states h'
-    static constexpr size_t floats = ring + 3 * kSub * DK /*q, k, a*/ + 2 * kSub * kNC /*v, dO*/ +
-                                     kSub /*beta*/ + 3 * kSub * DK /*sums dq, dk, dg*/ + kSub /*sum dbeta*/ +
+    // one block's inputs: q, k, a [kSub][DK], v, dO [kSub][kNC], beta [kSub] (two buffers)
+    static constexpr size_t stage = 3 * kSub * DK + 2 * kSub * kNC + kSub;
+    static constexpr size_t floats = ring + 2 * stage + 3 * kSub * DK /*sums dq, dk, dg*/ + kSub /*sum dbeta*/ +
                                      kSub * kNW /*GDN gate-gradient warp sums*/ + 2 * kNW * kNC /*row sums*/;
     static constexpr size_t bytes = floats * sizeof(float);
 };
@@ -115,13 +116,19 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     constexpr int GW = MODE == LDN_KDA ? DK : (MODE == LDN_GDN ? 1 : 0);   // gate width
     extern __shared__ float smb[];
     float *ring = smb;                          // [kSub][RPT][kBT]
-    float *qs = ring + BwdSmem<DK>::ring;       // [kSub][DK]
-    float *ks = qs + kSub * DK;                 // [kSub][DK]
-    float *as = ks + kSub * DK;                 // [kSub][DK] decay factor (GDN: [t][0])
-    float *vs = as + kSub * DK;                 // [kSub][kNC]
-    float *ds = vs + kSub * kNC;                // [kSub][kNC] dO
-    float *bs = ds + kSub * kNC;                // [kSub]
-    float *aq = bs + kSub;                      // [kSub][DK] column sums of this CTA
+    float *stg = ring + BwdSmem<DK>::ring;      // 2 x one block's inputs
+    // the current block's inputs (reassigned per block):
+    float *qs, *ks, *as, *vs, *ds, *bs;         // q, k [kSub][DK], decay [kSub][DK] (GDN [t][0]),
+                                                // v, dO [kSub][kNC], beta [kSub]
+    auto use_buffer = [&](int buf) {
+        qs = stg + buf * BwdSmem<DK>::stage;
+        ks = qs + kSub * DK;
+        as = ks + kSub * DK;
+        vs = as + kSub * DK;
+        ds = vs + kSub * kNC;
+        bs = ds + kSub * kNC;
+    };
+    float *aq = stg + 2 * BwdSmem<DK>::stage;   // [kSub][DK] column sums of this CTA
     float *ak = aq + kSub * DK;
     float *ag = ak + kSub * DK;
     float *ab = ag + kSub * DK;                 // [kSub]
@@ -140,32 +147,52 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     int par = 0;                                // parity of the row-sum buffer
 
     auto tok = [&](int t) { return ((size_t)b * T + t) * H + h; };
-    // Inputs of block s into shared memory (rows past T: zero, decay 1).
-    auto stage = [&](int s, bool grads) {
+    // A block's inputs travel global -> registers (issued a block ahead, so their
+    // latency overlaps the current block) -> shared buffer (rows past T: zero, log-decay 0).
+    constexpr int NKQ = kSub * DK / kBT;        // q, k, gate elements per thread
+    static_assert(kSub * kNC == kBT, "one v / dO element per thread");
+    struct Pre { float k[NKQ], q[NKQ], a[NKQ], v, d, b, g; };
+    auto pre_load = [&](int s, bool grads, Pre &P) {
         const int t0 = s * kSub;
-        for (int e = tid; e < kSub * DK; e += kBT) {
-            const int t = e / DK, r = e % DK;
+#pragma unroll
+        for (int x = 0; x < NKQ; ++x) {
+            const int e = tid + x * kBT, t = e / DK, r = e % DK;
             const bool ok = t0 + t < T;
             const size_t i = tok(ok ? t0 + t : 0) * DK + r;
-            ks[e] = ok ? load_in(k, i) : 0.f;
-            if (grads) qs[e] = ok ? load_in(q, i) : 0.f;
-            if (MODE == LDN_KDA) as[e] = ok ? expf(gate[i]) : 1.f;
+            P.k[x] = ok ? load_in(k, i) : 0.f;
+            P.q[x] = grads && ok ? load_in(q, i) : 0.f;
+            P.a[x] = MODE == LDN_KDA && ok ? gate[i] : 0.f;
         }
-        for (int e = tid; e < kSub * kNC; e += kBT) {
-            const int t = e / kNC, n = e % kNC;
+        {
+            const int t = tid / kNC, n = tid % kNC;
             const bool ok = t0 + t < T;
             const size_t i = tok(ok ? t0 + t : 0) * dv + sl * kNC + n;
-            vs[e] = ok ? load_in(v, i) : 0.f;
-            if (grads) ds[e] = ok ? load_in(dout, i) : 0.f;
+            P.v = ok ? load_in(v, i) : 0.f;
+            P.d = grads && ok ? load_in(dout, i) : 0.f;
         }
+        P.b = P.g = 0.f;
+        if (tid < kSub && t0 + tid < T) {
+            const size_t i = tok(t0 + tid);
+            P.b = beta[i];
+            if (MODE == LDN_GDN) P.g = gate[i];
+        }
+    };
+    auto pre_store = [&](int buf, bool grads, const Pre &P) {
+        float *q_ = stg + buf * BwdSmem<DK>::stage, *k_ = q_ + kSub * DK, *a_ = k_ + kSub * DK;
+        float *v_ = a_ + kSub * DK, *d_ = v_ + kSub * kNC, *b_ = d_ + kSub * kNC;
+#pragma unroll
+        for (int x = 0; x < NKQ; ++x) {
+            const int e = tid + x * kBT;
+            k_[e] = P.k[x];
+            if (grads) q_[e] = P.q[x];
+            if (MODE == LDN_KDA) a_[e] = expf(P.a[x]);
+        }
+        v_[tid] = P.v;
+        if (grads) d_[tid] = P.d;
         if (tid < kSub) {
-            const bool ok = t0 + tid < T;
-            const size_t i = tok(ok ? t0 + tid : 0);
-            bs[tid] = ok ? beta[i] : 0.f;
-            if (MODE == LDN_GDN) as[tid * DK] = ok ? expf(gate[i]) : 1.f;
+            b_[tid] = P.b;
+            if (MODE == LDN_GDN) a_[tid * DK] = expf(P.g);
         }
-        if (grads)
-            for (int e = tid; e < 3 * kSub * DK + kSub + kSub * kNW; e += kBT) aq[e] = 0.f;   // aq .. agw
     };
     auto decay = [&](int t, int j) -> float {
         return MODE == LDN_KDA ? as[t * DK + r0 + j] : (MODE == LDN_GDN ? as[t * DK] : 1.f);
@@ -200,10 +227,15 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     float hr[RPT];
 #pragma unroll
     for (int j = 0; j < RPT; ++j) hr[j] = S0 ? S0[((size_t)unit * DK + r0 + j) * dv + col] : 0.f;
+    Pre P;
+    if (nsub > 0) {
+        pre_load(0, false, P);
+        pre_store(0, false, P);
+    }
     for (int s = 0; s < nsub; ++s) {
-        __syncthreads();
-        stage(s, false);
-        __syncthreads();
+        __syncthreads();                        // block s staged; block s - 1 done with the other buffer
+        use_buffer(s & 1);
+        if (s + 1 < nsub) pre_load(s + 1, false, P);
 #pragma unroll
         for (int j = 0; j < RPT; ++j) myck[((size_t)s * RPT + j) * kBT + tid] = hr[j];
 #pragma unroll
@@ -211,6 +243,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
             float r, e;
             fwd_step(t, hr, r, e);
         }
+        if (s + 1 < nsub) pre_store((s + 1) & 1, false, P);
     }
 
     // ---- phase 2: blocks in reverse
@@ -221,13 +254,25 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     float *pb = pg + (size_t)slices * N * GW;
     const int jrow = row_of<RPT>(lane);
     const bool writer = row_writer<RPT>(lane);
+    float hn[RPT];                              // state copy of the next block to run
+    __syncthreads();                            // phase 1's readers are done with both buffers
+    if (nsub > 0) {
+        pre_load(nsub - 1, true, P);
+        pre_store((nsub - 1) & 1, true, P);
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) hn[j] = myck[((size_t)(nsub - 1) * RPT + j) * kBT + tid];
+    }
     for (int s = nsub - 1; s >= 0; --s) {
         const int t0 = s * kSub;
-        __syncthreads();
-        stage(s, true);
-        __syncthreads();
+        __syncthreads();                        // block s staged; block s + 1 flushed
+        use_buffer(s & 1);
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) hr[j] = myck[((size_t)s * RPT + j) * kBT + tid];
+        for (int j = 0; j < RPT; ++j) hr[j] = hn[j];
+        if (s > 0) {
+            pre_load(s - 1, true, P);
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) hn[j] = myck[((size_t)(s - 1) * RPT + j) * kBT + tid];
+        }
         float rr[kSub], ee[kSub];
 #pragma unroll
         for (int t = 0; t < kSub; ++t) {
@@ -307,6 +352,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
                 pg[(size_t)sl * N + n] = sg;
             }
         }
+        if (s > 0) pre_store((s - 1) & 1, true, P);
     }
 #pragma unroll
     for (int j = 0; j < RPT; ++j) dS0[((size_t)unit * DK + r0 + j) * dv + col] = g[j];
