@@ -22,15 +22,6 @@
 // direction, P, O and the state update keep k); it runs the KDA path with those
 // three substitutions made where the tiles are loaded.
 //
-// Residual Linear Attention's base state (Residual Linear Attention notes,
-// Sec. 2.2) is additive: S_t = alpha S_{t-1} + beta v k^T.  Mode kModeAdditive
-// runs it as the same algebra with A = 0 and W = 0 (no prediction is
-// subtracted, U = U' = Diag(beta) V).  With EMIT the kernel also writes, per
-// token, the reads of the state BEFORE the token's write: the undecayed
-// prediction S_{t-1} k_t = e^{g_{t-1}} k_t . H0 + sum_{j<t} (k_t . k_j)
-// e^{g_{t-1} - g_j} u_j and the decayed query read alpha_t S_{t-1} q_t =
-// o_t - (q_t . k_t) u_t (u = the rows of U, the writes), for scalar decay.
-//
 // Work split: one CTA per (b, h, 32-column slice of dv); columns of H are
 // independent (state-reduction notes, Sec. 2.5).  The dk-side work (A, W, P)
 // is repeated per slice.  All operands live in shared memory as fp32; the
@@ -44,32 +35,26 @@ constexpr int kC = 64;           // chunk length
 constexpr int kDVS = 32;         // dv columns per CTA
 constexpr int kThreads = 256;
 
-template <int DK, bool EMIT = false>
+template <int DK>
 struct SimtSmem {
     static constexpr int LDK = DK + 1;   // padded row strides (bank spread)
     static constexpr int LDV = kDVS + 1;
     static constexpr int LDA = kC + 1;
-    static constexpr size_t base = 3 * (size_t)kC * LDK + (size_t)kC * LDV + (size_t)kC * LDA +
-                                   (size_t)DK * LDV + 3 * DK + 2 * kC;
-    // EMIT: raw K, the strictly lower Gram matrix with the exclusive decay, O
-    static constexpr size_t floats = base + (EMIT ? (size_t)kC * LDK + (size_t)kC * LDA + (size_t)kC * LDV : 0);
+    static constexpr size_t floats = 3 * (size_t)kC * LDK + (size_t)kC * LDV + (size_t)kC * LDA +
+                                     (size_t)DK * LDV + 3 * DK + 2 * kC;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
-template <int DK, typename TIn, int MODE, bool EMIT = false>
+template <int DK, typename TIn, int MODE>
 __global__ void __launch_bounds__(kThreads)
 chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
                   const float *__restrict__ beta, const float *__restrict__ gate,
                   const float *S0, TIn *__restrict__ out, float *S_final,  // S0 may alias S_final
-                  int T, int H, int dv, const float *__restrict__ erase, const float *__restrict__ write,
-                  float *__restrict__ pk_out, float *__restrict__ sq_out)
+                  int T, int H, int dv, const float *__restrict__ erase, const float *__restrict__ write)
 {
     constexpr bool kG2 = MODE == LDN_GDN2;
     constexpr bool kChan = MODE == LDN_KDA || kG2;   // per-key-channel decay
-    constexpr bool kAdd = MODE == kModeAdditive;     // additive update, scalar decay
-    constexpr bool kScalar = MODE == LDN_GDN || kAdd;
-    static_assert(!EMIT || kScalar, "pre-update reads are formed for scalar decay only");
-    using L = SimtSmem<DK, EMIT>;
+    using L = SimtSmem<DK>;
     extern __shared__ float smem[];
     float *Qs = smem;                         // [C][LDK]  Q -> Q^ -> Q^ - P W
     float *Ks = Qs + kC * L::LDK;             // [C][LDK]  K -> K^ -> beta K^ -> W
@@ -82,9 +67,6 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
     float *gm = gCl + DK;                     // [DK]      reference g at the middle row (KDA)
     float *bs = gm + DK;                      // [C]       beta (0 on tail rows)
     float *gr = bs + kC;                      // [C]       scalar log-gate prefix (GDN)
-    float *Kr = gr + kC;                      // EMIT [C][LDK] raw K
-    float *Pk = Kr + kC * L::LDK;             // EMIT [C][LDA] (k_r . k_j) e^{g_{r-1} - g_j}, j < r
-    float *Os = Pk + kC * L::LDA;             // EMIT [C][LDV] the chunk's output slice
 
     const int tid = threadIdx.x;
     const int slices = dv / kDVS;
@@ -114,7 +96,6 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
             Qs[r * L::LDK + c] = qv;
             Ks[r * L::LDK + c] = (kG2 && r < Lr) ? erase[(((size_t)b * T + t0 + r) * H + h) * DK + c] * kv : kv;
             Kc[r * L::LDK + c] = kv;
-            if (EMIT) Kr[r * L::LDK + c] = kv;
         }
         for (int e = tid; e < kC * kDVS; e += kThreads) {
             const int r = e / kDVS, n = e % kDVS;
@@ -122,7 +103,7 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
             Vs[r * L::LDV + n] = r < Lr ? (kG2 ? write[vi] * load_in(v, vi) : load_in(v, vi)) : 0.f;
         }
         if (tid < kC) bs[tid] = tid < Lr ? (kG2 ? 1.f : beta[((size_t)b * T + t0 + tid) * H + h]) : 0.f;
-        if (kScalar && tid == 0) {
+        if (MODE == LDN_GDN && tid == 0) {
             float g = 0.f;
             for (int r = 0; r < kC; ++r) {
                 if (r < Lr) g += gate[((size_t)b * T + t0 + r) * H + h];
@@ -165,11 +146,10 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
             float acc = 0.f;
             if (j < r) {
                 for (int c = 0; c < DK; ++c) acc += Ks[r * L::LDK + c] * Kc[j * L::LDK + c];
-                if (EMIT) Pk[r * L::LDA + j] = acc * expf(gr[r - 1] - gr[j]);
                 acc *= bs[r];
-                if (kScalar) acc *= expf(gr[r] - gr[j]);
+                if (MODE == LDN_GDN) acc *= expf(gr[r] - gr[j]);
             }
-            Am[r * L::LDA + j] = kAdd ? 0.f : acc;
+            Am[r * L::LDA + j] = acc;
         }
         __syncthreads();
 
@@ -178,9 +158,9 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
         for (int e = tid; e < kC * DK; e += kThreads) {
             const int r = e / DK, c = e % DK;
             float f = bs[r];
-            if (kScalar) f *= expf(gr[r]);
+            if (MODE == LDN_GDN) f *= expf(gr[r]);
             if (kChan) f *= expf(gm[c]);
-            Ks[r * L::LDK + c] = kAdd ? 0.f : Ks[r * L::LDK + c] * f;   // additive: W = 0
+            Ks[r * L::LDK + c] *= f;
         }
         for (int e = tid; e < kC * kDVS; e += kThreads) {
             const int r = e / kDVS, n = e % kDVS;
@@ -207,7 +187,7 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
             float acc = 0.f;
             if (j <= r) {
                 for (int c = 0; c < DK; ++c) acc += Qs[r * L::LDK + c] * Kc[j * L::LDK + c];
-                if (kScalar) acc *= expf(gr[r] - gr[j]);
+                if (MODE == LDN_GDN) acc *= expf(gr[r] - gr[j]);
             }
             Am[r * L::LDA + j] = acc;
         }
@@ -218,13 +198,13 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
         if (MODE != LDN_DELTANET) {
             for (int e = tid; e < kC * DK; e += kThreads) {
                 const int r = e / DK, c = e % DK;
-                const float fq = kScalar ? expf(gr[r]) : expf(gm[c]);
-                const float fk = kScalar ? expf(gr[kC - 1] - gr[r]) : expf(gCl[c] - gm[c]);
+                const float fq = MODE == LDN_GDN ? expf(gr[r]) : expf(gm[c]);
+                const float fk = MODE == LDN_GDN ? expf(gr[kC - 1] - gr[r]) : expf(gCl[c] - gm[c]);
                 Qs[r * L::LDK + c] *= fq;
                 Kc[r * L::LDK + c] *= fk;
             }
         }
-        if (tid < DK) gC[tid] = kScalar ? expf(gr[kC - 1]) : kChan ? expf(gCl[tid]) : 1.0f;
+        if (tid < DK) gC[tid] = MODE == LDN_GDN ? expf(gr[kC - 1]) : kChan ? expf(gCl[tid]) : 1.0f;
         __syncthreads();
 
         // 7. Q~ = Q^ - P W  (row r only reads its own row of Q^).
@@ -244,7 +224,6 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
             for (int j = 0; j <= r; ++j) acc += Am[r * L::LDA + j] * Vs[j * L::LDV + n];
             for (int c = 0; c < DK; ++c) acc += Qs[r * L::LDK + c] * Hs[c * L::LDV + n];
             store_out(out, (((size_t)b * T + t0 + r) * H + h) * dv + col0 + n, acc);
-            if (EMIT) Os[r * L::LDV + n] = acc;
         }
         __syncthreads();
 
@@ -256,22 +235,6 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
             Vs[r * L::LDV + n] = acc;
         }
         __syncthreads();
-
-        // 8b'. Reads of the state before each token's write (H0 still in Hs).
-        if constexpr (EMIT) {
-            for (int e = tid; e < kC * kDVS; e += kThreads) {
-                const int r = e / kDVS, n = e % kDVS;
-                if (r >= Lr) continue;
-                float pk = 0.f;
-                for (int c = 0; c < DK; ++c) pk += Kr[r * L::LDK + c] * Hs[c * L::LDV + n];
-                pk *= expf(r ? gr[r - 1] : 0.f);
-                for (int j = 0; j < r; ++j) pk += Pk[r * L::LDA + j] * Vs[j * L::LDV + n];
-                const size_t o = (((size_t)b * T + t0 + r) * H + h) * dv + col0 + n;
-                pk_out[o] = pk;
-                sq_out[o] = Os[r * L::LDV + n] - Am[r * L::LDA + r] * Vs[r * L::LDV + n];
-            }
-            __syncthreads();
-        }
 
         // 8c. H1 = Diag(e^{g_C}) H0 + K~^T U.
         for (int e = tid; e < DK * kDVS; e += kThreads) {
@@ -289,17 +252,17 @@ chunk_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
         }
 }
 
-template <int DK, typename TIn, int MODE, bool EMIT = false>
+template <int DK, typename TIn, int MODE>
 cudaError_t launch_mode(const ChunkArgs &a, cudaStream_t st)
 {
-    auto kern = chunk_simt_kernel<DK, TIn, MODE, EMIT>;
-    const size_t smem = SimtSmem<DK, EMIT>::bytes;
+    auto kern = chunk_simt_kernel<DK, TIn, MODE>;
+    const size_t smem = SimtSmem<DK>::bytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDVS));
     kern<<<grid, kThreads, smem, st>>>((const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, a.beta,
                                        a.gate, a.S0, (TIn *)a.out, a.S_final, a.T, a.H, a.dv, a.erase,
-                                       a.write, a.pk_out, a.sq_out);
+                                       a.write);
     return cudaGetLastError();
 }
 
@@ -310,9 +273,6 @@ cudaError_t launch_dk(const ChunkArgs &a, cudaStream_t st)
     case LDN_DELTANET: return launch_mode<DK, TIn, LDN_DELTANET>(a, st);
     case LDN_GDN: return launch_mode<DK, TIn, LDN_GDN>(a, st);
     case LDN_GDN2: return launch_mode<DK, TIn, LDN_GDN2>(a, st);
-    case kModeAdditive:
-        return a.pk_out ? launch_mode<DK, TIn, kModeAdditive, true>(a, st) : launch_mode<DK, TIn, kModeAdditive>(a, st);
-    case kModeGdnEmit: return launch_mode<DK, TIn, LDN_GDN, true>(a, st);
     default: return launch_mode<DK, TIn, LDN_KDA>(a, st);
     }
 }

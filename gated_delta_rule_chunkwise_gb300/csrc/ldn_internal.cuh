@@ -22,15 +22,7 @@ struct ChunkArgs {
     int B, T, H, dk, dv, chunk, mode, dtype;
     int *status;
     const float *erase = nullptr, *write = nullptr;   // Gated DeltaNet-2: b [B][T][H][dk], w [B][T][H][dv]
-    // SIMT kernel, scalar decay: reads of the state before each token's write
-    // (S_{t-1} k_t and alpha_t S_{t-1} q_t, fp32 [B][T][H][dv]) when not NULL
-    float *pk_out = nullptr, *sq_out = nullptr;
 };
-// Internal modes of the SIMT chunk kernel (not in the public enum): the additive
-// update with scalar decay (Residual Linear Attention's states), and Gated
-// DeltaNet with the pre-update reads written.
-constexpr int kModeAdditive = 16;
-constexpr int kModeGdnEmit = 17;
 
 struct DecodeArgs {
     const void *q, *k, *v;
@@ -92,6 +84,19 @@ struct BwdArgs {
     float *ws;   // checkpoints, then the per-slice partial sums
     int B, T, H, dk, dv, mode, dtype;
 };
+// Token-recurrent forward for scalar decay (csrc/recurrent.cu): pre = true writes
+// S_{t-1} k_t and alpha_t S_{t-1} q_t (fp32) per token, pre = false writes S_t q_t
+// (dtype); delta selects the delta rule over the additive one.
+struct RecArgs {
+    const void *q, *k, *v;
+    const float *beta, *gate, *S0;
+    float *S_final, *p_out, *s_out;
+    void *o_out;
+    int B, T, H, dk, dv, dtype;
+    bool delta, pre;
+};
+cudaError_t launch_recurrent(const RecArgs &a, cudaStream_t stream);
+
 // Residual Linear Attention / Residual DeltaNet forward (csrc/rla.cu).
 struct RlaArgs {
     const void *q, *k, *v;

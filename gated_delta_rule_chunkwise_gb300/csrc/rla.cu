@@ -6,11 +6,11 @@
 //   RDN: S_t = alpha S_{t-1}(I - beta k k^T) + beta v k^T,
 //        R_t = alpha R_{t-1}(I - gamma k k^T) + gamma r k^T       (Sec. 2.4)
 //   r_t = Clip_[-c, c](v_t - S_{t-1} k_t),   o_t = alpha_t S_{t-1} q_t + gamma_t R_t q_t
-// (Sec. 2.2, the boxed form).  Stage 1 is the chunk kernel on CUDA cores with
-// the pre-update reads written (S_{t-1} k_t and alpha_t S_{t-1} q_t); the
-// residual kernel clips; stage 2 is the chunk forward with v := r and
-// beta := gamma (the tensor-core kernel for RDN when it takes the sizes); the
-// combine kernel forms o.
+// (Sec. 2.2, the boxed form).  Stage 1 is the token-recurrent kernel writing
+// the reads of the old base state (S_{t-1} k_t and alpha_t S_{t-1} q_t); the
+// residual kernel clips; stage 2 is the residual state with v := r and
+// beta := gamma, read after its update (the tensor-core chunk kernel for RDN when
+// it takes the sizes, else the recurrent kernel); the combine kernel forms o.
 #include "ldn_internal.cuh"
 
 namespace ldn {
@@ -48,22 +48,23 @@ cudaError_t launch_t(const RlaArgs &a, cudaStream_t st)
     float *sq = (float *)(w + rla_off(n * 4));
     TIn *r = (TIn *)(w + 2 * rla_off(n * 4));
     TIn *o2 = (TIn *)(w + 2 * rla_off(n * 4) + rla_off(n * el));
-    // stage 1: base state, pre-update reads (its own output, S_t q_t, is not needed: o2 holds it meanwhile)
-    ChunkArgs s1{a.q, a.k, a.v, a.beta, a.gate, a.S0, o2, a.S_final, a.B, a.T, a.H, a.dk, a.dv, 64,
-                 a.delta ? kModeGdnEmit : kModeAdditive, a.dtype, a.status};
-    s1.pk_out = pk;
-    s1.sq_out = sq;
-    cudaError_t e = launch_chunk_simt(s1, st);
+    // stage 1: base state and the reads of its old value
+    RecArgs s1{a.q, a.k, a.v, a.beta, a.gate, a.S0, a.S_final, pk, sq, nullptr, a.B, a.T, a.H, a.dk, a.dv,
+               a.dtype, a.delta != 0, true};
+    cudaError_t e = launch_recurrent(s1, st);
     if (e != cudaSuccess) return e;
     rla_residual_kernel<TIn><<<stream_blocks(n), 256, 0, st>>>((const TIn *)a.v, pk, r, a.clip, n);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // stage 2: the residual state with values r and write strength gamma
+    // stage 2: the residual state with values r and write strength gamma, read after its update
     ChunkArgs s2{a.q, a.k, r, a.gamma, a.gate, a.R0, o2, a.R_final, a.B, a.T, a.H, a.dk, a.dv, 64,
-                 a.delta ? (int)LDN_GDN : kModeAdditive, a.dtype, a.status};
-    if (a.delta && a.dtype == LDN_BF16 && chunk_tc_supported(s2))
+                 (int)LDN_GDN, a.dtype, a.status};
+    if (a.delta && a.dtype == LDN_BF16 && chunk_tc_supported(s2)) {
         e = launch_chunk_tc(s2, st);
-    else
-        e = launch_chunk_simt(s2, st);
+    } else {
+        RecArgs r2{a.q, a.k, r, a.gamma, a.gate, a.R0, a.R_final, nullptr, nullptr, o2, a.B, a.T, a.H, a.dk, a.dv,
+                   a.dtype, a.delta != 0, false};
+        e = launch_recurrent(r2, st);
+    }
     if (e != cudaSuccess) return e;
     rla_combine_kernel<TIn><<<stream_blocks(n), 256, 0, st>>>(sq, o2, a.gamma, (TIn *)a.out, n, a.dv);
     return cudaGetLastError();

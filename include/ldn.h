@@ -354,11 +354,11 @@ size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode
  *   RDN: R_t = alpha_t R_{t-1}(I - gamma_t k_t k_t^T) + gamma_t r_t k_t^T,
  *        S_t = alpha_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T
  *   o_t = alpha_t S_{t-1} q_t + gamma_t R_t q_t      (the UPDATED residual state)
- * Four launches: the base state by the CUDA-core chunk kernel, which also
- * writes S_{t-1} k_t and alpha_t S_{t-1} q_t; the clip; the residual state by
- * the chunk forward with v := r and beta := gamma (tensor cores for RDN with
- * bf16 inputs, dk = 128); the sum.  r and the stage-2 output are held in the
- * input dtype (bf16 rounds them).
+ * Four launches: the base state by a token-recurrent fp32 kernel that also
+ * writes S_{t-1} k_t and alpha_t S_{t-1} q_t; the clip; the residual state
+ * with v := r and beta := gamma (the tensor-core chunk kernel for RDN with
+ * bf16 inputs and dk = 128, else the recurrent kernel); the sum.  r and the
+ * stage-2 output are held in the input dtype (bf16 rounds them).
  *   q, k [B][T][H][dk], v, out [B][T][H][dv] of dtype (16-byte aligned)
  *   beta, gamma, gate (log alpha) [B][T][H] fp32 (4-byte aligned)
  *   clip c > 0 (INFINITY: no clip)
