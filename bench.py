@@ -553,11 +553,11 @@ def run_ours(args):
                 bstep()
                 e1.record(stream)
             barrier()
-            launches += 2 * (1 + len(bev))
+            launches += 3 * (1 + len(bev))
             bms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in bev))
             bb = backward_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(bw.dtype), bw.mode)
             backward[name] = {"ms_per_call": bms, "tokens_per_s": world * B_ * T_ / (bms / 1e3),
-                              "kernels": "bwd_kernel + bwd_reduce_kernel", "algorithmic_bytes": bb,
+                              "kernels": "bwd_kernel<phase 1> + bwd_kernel<phase 2> + bwd_reduce_kernel", "algorithmic_bytes": bb,
                               "hbm_frac": bb / (bms / 1e3) / 1e9 / hbm_peak, "workspace_bytes": need}
             del bt, bdo, bdsf, gq, gk, gv, gb, gg, gs0, bws
         if ldn.device_status() != ldn.LDN_OK:

@@ -26,8 +26,9 @@
 // owns the rows, so each row has one writer and no atomics are needed; the
 // scalar sums (dbeta, the GDN gate gradient) are warp sums.  Each slice stores
 // its partial sums; a second kernel adds the slices.
-//   Phase 1 walks the sequence forward and stores the state before every block
-//   of 8 tokens (workspace).
+//   Phase 1 (its own launch: small shared memory, several CTAs per SM) walks the
+//   sequence forward and stores the state before every block of 8 tokens
+//   (workspace).
 //   Phase 2 walks the blocks in reverse: it reloads the block's checkpoint,
 //   recomputes the block's decayed states h' into a shared-memory ring
 //   (thread-private slots), then steps the 8 tokens backward.
@@ -41,10 +42,10 @@ constexpr int kBT = 256;    // threads per CTA
 constexpr int kNW = kBT / 32;
 constexpr int kSub = 8;     // tokens per recomputed block
 
-template <int DK>
+template <int DK, int PHASE = 2>
 struct BwdSmem {
     static constexpr int RPT = DK / kNW;                                 // rows per thread (and per warp)
-    static constexpr size_t ring = (size_t)kSub * RPT * kBT;            // decayed states h'
+    static constexpr size_t ring = PHASE == 2 ? (size_t)kSub * RPT * kBT : 0;   // decayed states h'
     // one block's inputs: q, k, a [kSub][DK], v, dO [kSub][kNC], beta [kSub] (two buffers)
     static constexpr size_t stage = 3 * kSub * DK + 2 * kSub * kNC + kSub;
     static constexpr size_t floats = ring + 2 * stage + 3 * kSub * DK /*sums dq, dk, dg*/ + kSub /*sum dbeta*/ +
@@ -105,30 +106,31 @@ __device__ __forceinline__ int row_of(int lane)
 template <int N>
 __device__ __forceinline__ bool row_writer(int lane) { return N == 16 ? (lane & 1) == 0 : (lane & 3) == 0; }
 
-template <int DK, typename TIn, int MODE>
-__global__ void __launch_bounds__(kBT, 1)
+template <int DK, typename TIn, int MODE, int PHASE>
+__global__ void __launch_bounds__(kBT, PHASE == 1 ? 3 : 1)
 bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
            const float *__restrict__ beta, const float *__restrict__ gate, const float *__restrict__ S0,
            const TIn *__restrict__ dout, const float *__restrict__ dSf, float *__restrict__ dv_out,
            float *__restrict__ dS0, float *__restrict__ ckpt, float *__restrict__ part, int T, int H, int dv)
 {
-    constexpr int RPT = BwdSmem<DK>::RPT;
+    using SM = BwdSmem<DK, PHASE>;
+    constexpr int RPT = SM::RPT;
     constexpr int GW = MODE == LDN_KDA ? DK : (MODE == LDN_GDN ? 1 : 0);   // gate width
     extern __shared__ float smb[];
     float *ring = smb;                          // [kSub][RPT][kBT]
-    float *stg = ring + BwdSmem<DK>::ring;      // 2 x one block's inputs
+    float *stg = ring + SM::ring;      // 2 x one block's inputs
     // the current block's inputs (reassigned per block):
     float *qs, *ks, *as, *vs, *ds, *bs;         // q, k [kSub][DK], decay [kSub][DK] (GDN [t][0]),
                                                 // v, dO [kSub][kNC], beta [kSub]
     auto use_buffer = [&](int buf) {
-        qs = stg + buf * BwdSmem<DK>::stage;
+        qs = stg + buf * SM::stage;
         ks = qs + kSub * DK;
         as = ks + kSub * DK;
         vs = as + kSub * DK;
         ds = vs + kSub * kNC;
         bs = ds + kSub * kNC;
     };
-    float *aq = stg + 2 * BwdSmem<DK>::stage;   // [kSub][DK] column sums of this CTA
+    float *aq = stg + 2 * SM::stage;   // [kSub][DK] column sums of this CTA
     float *ak = aq + kSub * DK;
     float *ag = ak + kSub * DK;
     float *ab = ag + kSub * DK;                 // [kSub]
@@ -178,7 +180,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
         }
     };
     auto pre_store = [&](int buf, bool grads, const Pre &P) {
-        float *q_ = stg + buf * BwdSmem<DK>::stage, *k_ = q_ + kSub * DK, *a_ = k_ + kSub * DK;
+        float *q_ = stg + buf * SM::stage, *k_ = q_ + kSub * DK, *a_ = k_ + kSub * DK;
         float *v_ = a_ + kSub * DK, *d_ = v_ + kSub * kNC, *b_ = d_ + kSub * kNC;
 #pragma unroll
         for (int x = 0; x < NKQ; ++x) {
@@ -223,11 +225,12 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
         for (int j = 0; j < RPT; ++j) hr[j] += ks[t * DK + r0 + j] * r;
     };
 
-    // ---- phase 1: forward, checkpoint before every block
     float hr[RPT];
+    Pre P;
+    if constexpr (PHASE == 1) {
+    // ---- phase 1: forward, checkpoint before every block
 #pragma unroll
     for (int j = 0; j < RPT; ++j) hr[j] = S0 ? S0[((size_t)unit * DK + r0 + j) * dv + col] : 0.f;
-    Pre P;
     if (nsub > 0) {
         pre_load(0, false, P);
         pre_store(0, false, P);
@@ -245,7 +248,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
         }
         if (s + 1 < nsub) pre_store((s + 1) & 1, false, P);
     }
-
+    } else {
     // ---- phase 2: blocks in reverse
     float g[RPT];
 #pragma unroll
@@ -255,7 +258,6 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     const int jrow = row_of<RPT>(lane);
     const bool writer = row_writer<RPT>(lane);
     float hn[RPT];                              // state copy of the next block to run
-    __syncthreads();                            // phase 1's readers are done with both buffers
     if (nsub > 0) {
         pre_load(nsub - 1, true, P);
         pre_store((nsub - 1) & 1, true, P);
@@ -356,6 +358,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     }
 #pragma unroll
     for (int j = 0; j < RPT; ++j) dS0[((size_t)unit * DK + r0 + j) * dv + col] = g[j];
+    }
 }
 
 // Sum of the slices' partial sums: dq, dk [N][dk], dgate [N][gw], dbeta [N].
@@ -385,18 +388,22 @@ __global__ void bwd_reduce_kernel(const float *__restrict__ part, float *__restr
 template <int DK, typename TIn, int MODE>
 cudaError_t launch_mode(const BwdArgs &a, cudaStream_t st)
 {
-    auto kern = bwd_kernel<DK, TIn, MODE>;
-    const size_t smem = BwdSmem<DK>::bytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const int slices = a.dv / kNC;
     const unsigned grid = (unsigned)((long long)a.B * a.H * slices);
     float *ckpt = a.ws;
     float *part = ckpt + bwd_ckpt_floats(a.B, a.T, a.H, a.dk, a.dv);
-    kern<<<grid, kBT, smem, st>>>((const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, a.beta, a.gate, a.S0,
-                                  (const TIn *)a.dout, a.dS_final, a.dv_out, a.dS0, ckpt, part, a.T, a.H, a.dv);
-    e = cudaGetLastError();
+    auto k1 = bwd_kernel<DK, TIn, MODE, 1>;
+    auto k2 = bwd_kernel<DK, TIn, MODE, 2>;
+    cudaError_t e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdSmem<DK, 2>::bytes);
     if (e != cudaSuccess) return e;
+    k1<<<grid, kBT, BwdSmem<DK, 1>::bytes, st>>>((const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, a.beta, a.gate,
+                                                  a.S0, (const TIn *)a.dout, a.dS_final, a.dv_out, a.dS0, ckpt, part,
+                                                  a.T, a.H, a.dv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k2<<<grid, kBT, BwdSmem<DK, 2>::bytes, st>>>((const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, a.beta, a.gate,
+                                                  a.S0, (const TIn *)a.dout, a.dS_final, a.dv_out, a.dS0, ckpt, part,
+                                                  a.T, a.H, a.dv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long long N = (long long)a.B * a.T * a.H;
     const int gw = MODE == LDN_KDA ? DK : (MODE == LDN_GDN ? 1 : 0);
     const long long total = N * (2LL * DK + gw + 1);

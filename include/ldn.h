@@ -332,8 +332,8 @@ int ldn_decode_step_gdn2(const void *q, const void *k, const void *v, const floa
  *             gradients); contents on entry do not matter.
  * Alignment: q, k, v, dout to their element size; every fp32 array 4-byte.
  * T = 0 writes dS0 = dS_final (or zeros) and nothing else.  Asynchronous on
- * `stream`: two kernel launches (the recurrence sweeps, then the sum over the
- * dv slices).
+ * `stream`: three kernel launches (the forward sweep that stores the state
+ * copies, the reverse sweep, the sum over the dv slices).
  */
 int ldn_backward(const void *q, const void *k, const void *v, const float *beta, const float *gate,
                  const float *S0, const void *dout, const float *dS_final, float *dq, float *dk, float *dv,
