@@ -6,7 +6,7 @@ import pytest
 
 import gated_delta_rule_chunkwise_gb300 as ldn
 from gated_delta_rule_chunkwise_gb300 import workloads as wl
-from tests._helpers import rel_err
+from tests._helpers import BF16_HALF_ULP, rel_err
 import oracle
 
 pytestmark = pytest.mark.gpu
@@ -36,11 +36,12 @@ def test_autograd_gradients_match_the_oracle(mode, dtype):
     loss.backward()
     ref = oracle.bwd(w.q, w.k, w.v, w.beta, w.gate, w.S0, dout, dsf, mode=mode)
     names = {"q": "dq", "k": "dk", "v": "dv", "beta": "dbeta", "gate": "dgate", "S0": "dS0"}
-    # q, k, v gradients come back in the input dtype (bf16 rounds them by up to 2^-9)
-    tol = {"f32": 1e-3, "bf16": 1e-2}[dtype]
+    # q, k, v gradients come back in the input dtype: bf16 storage rounds them by up to
+    # half a bf16 ulp, measured beyond that rounding as for the bf16 outputs
     for name, gname in names.items():
         if leaves[name] is None:
             assert ref[gname] is None
             continue
-        e = rel_err(leaves[name].grad.float().cpu().numpy(), ref[gname])
-        assert e <= tol, f"{gname}: {e:.3g}"
+        stored = BF16_HALF_ULP if dtype == "bf16" and name in ("q", "k", "v") else 0.0
+        e = rel_err(leaves[name].grad.float().cpu().numpy(), ref[gname], stored)
+        assert e <= 1e-3, f"{gname}: {e:.3g}"
