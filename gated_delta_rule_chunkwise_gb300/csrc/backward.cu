@@ -46,12 +46,10 @@ template <int DK, int PHASE = 2>
 struct BwdSmem {
     static constexpr int RPT = DK / kNW;                                 // rows per thread (and per warp)
     static constexpr size_t ring = PHASE == 2 ? (size_t)kSub * RPT * kBT : 0;   // decayed states h'
-    // one block's inputs: q, k, a [kSub][DK], v, dO [kSub][kNC], beta [kSub]; two buffers
-    // (phase 1) or three (phase 2: the block stepped back, the block recomputed, the block loading)
+    // one block's inputs: q, k, a [kSub][DK], v, dO [kSub][kNC], beta [kSub] (two buffers)
     static constexpr size_t stage = 3 * kSub * DK + 2 * kSub * kNC + kSub;
-    static constexpr int nbuf = PHASE == 2 ? 3 : 2;
-    static constexpr size_t floats = ring + nbuf * stage + 3 * kSub * DK /*sums dq, dk, dg*/ + kSub /*sum dbeta*/ +
-                                     kSub * kNW /*GDN gate-gradient warp sums*/ + 4 * kNW * kNC /*row sums (float2)*/;
+    static constexpr size_t floats = ring + 2 * stage + 3 * kSub * DK /*sums dq, dk, dg*/ + kSub /*sum dbeta*/ +
+                                     kSub * kNW /*GDN gate-gradient warp sums*/ + 2 * kNW * kNC /*row sums*/;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -132,12 +130,12 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
         ds = vs + kSub * kNC;
         bs = ds + kSub * kNC;
     };
-    float *aq = stg + SM::nbuf * SM::stage;     // [kSub][DK] column sums of this CTA
+    float *aq = stg + 2 * SM::stage;   // [kSub][DK] column sums of this CTA
     float *ak = aq + kSub * DK;
     float *ag = ak + kSub * DK;
     float *ab = ag + kSub * DK;                 // [kSub]
     float *agw = ab + kSub;                     // [kSub][kNW] GDN gate gradient per warp
-    float *red = agw + kSub * kNW;              // [2][kNW][kNC] row-sum exchange (phase 2: float2)
+    float *red = agw + kSub * kNW;              // [2][kNW][kNC] row-sum exchange
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r0 = warp * RPT;                  // first key row of this warp
@@ -251,11 +249,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
         if (s + 1 < nsub) pre_store((s + 1) & 1, false, P);
     }
     } else {
-    // ---- phase 2: blocks in reverse.  While block s is stepped backward (its tokens in
-    // reverse), block s - 1 is recomputed forward into the same ring: step i reads the slot
-    // of token 7 - i of block s and then writes token i of block s - 1 into it, so the
-    // token-to-slot map alternates between blocks (slot t, then slot 7 - t).  Both
-    // row sums of a step (dr of the backward, p of the recompute) share one exchange.
+    // ---- phase 2: blocks in reverse
     float g[RPT];
 #pragma unroll
     for (int j = 0; j < RPT; ++j) g[j] = dSf ? dSf[((size_t)unit * DK + r0 + j) * dv + col] : 0.f;
@@ -263,152 +257,82 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     float *pb = pg + (size_t)slices * N * GW;
     const int jrow = row_of<RPT>(lane);
     const bool writer = row_writer<RPT>(lane);
-    struct Bp { const float *q, *k, *a, *v, *d, *b; };
-    auto bufp = [&](int buf) -> Bp {
-        const float *q_ = stg + buf * SM::stage, *k_ = q_ + kSub * DK, *a_ = k_ + kSub * DK;
-        const float *v_ = a_ + kSub * DK, *d_ = v_ + kSub * kNC, *b_ = d_ + kSub * kNC;
-        return Bp{q_, k_, a_, v_, d_, b_};
-    };
-    auto dec = [&](const Bp &B_, int t, int j) -> float {
-        return MODE == LDN_KDA ? B_.a[t * DK + r0 + j] : (MODE == LDN_GDN ? B_.a[t * DK] : 1.f);
-    };
-    float2 *red2 = reinterpret_cast<float2 *>(red);
-    auto xchg = [&](float x, float y) -> float2 {
-        float2 *rb = red2 + par * kNW * kNC;
-        rb[warp * kNC + lane] = make_float2(x, y);
-        __syncthreads();
-        float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) {
-            const float2 z = rb[w * kNC + lane];
-            s2.x += z.x;
-            s2.y += z.y;
-        }
-        par ^= 1;
-        return s2;
-    };
-    auto ck = [&](int s_, int j) { return myck[((size_t)s_ * RPT + j) * kBT + tid]; };
-
-    float rr[kSub], ee[kSub];   // r and v - p of the block being stepped back
-    float h2[RPT];              // running state of the block being recomputed
-    float hn[RPT];              // state copy of the block after that
-    int map = 0;                // token-to-slot map of the block being stepped back
+    float hn[RPT];                              // state copy of the next block to run
     if (nsub > 0) {
         pre_load(nsub - 1, true, P);
-        pre_store((nsub - 1) % 3, true, P);
-        if (nsub > 1) {
-            pre_load(nsub - 2, true, P);
-            pre_store((nsub - 2) % 3, true, P);
-        }
+        pre_store((nsub - 1) & 1, true, P);
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            hr[j] = ck(nsub - 1, j);
-            hn[j] = nsub > 1 ? ck(nsub - 2, j) : 0.f;
-        }
-        __syncthreads();
-        // the last block on its own (slot t)
-        const Bp B_ = bufp((nsub - 1) % 3);
-#pragma unroll
-        for (int t = 0; t < kSub; ++t) {
-            float pp = 0.f;
-#pragma unroll
-            for (int j = 0; j < RPT; ++j) {
-                hr[j] *= dec(B_, t, j);
-                ring[((size_t)t * RPT + j) * kBT + tid] = hr[j];
-                pp += hr[j] * B_.k[t * DK + r0 + j];
-            }
-            const float p_ = xchg(pp, 0.f).x;
-            ee[t] = B_.v[t * kNC + lane] - p_;
-            rr[t] = B_.b[t] * ee[t];
-#pragma unroll
-            for (int j = 0; j < RPT; ++j) hr[j] += B_.k[t * DK + r0 + j] * rr[t];
-        }
+        for (int j = 0; j < RPT; ++j) hn[j] = myck[((size_t)(nsub - 1) * RPT + j) * kBT + tid];
     }
     for (int s = nsub - 1; s >= 0; --s) {
         const int t0 = s * kSub;
-        const bool rec = s > 0;                 // block s - 1 is recomputed meanwhile
-        const Bp Bc = bufp(s % 3), Br = bufp((s + 2) % 3);
+        __syncthreads();                        // block s staged; block s + 1 flushed
+        use_buffer(s & 1);
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) h2[j] = hn[j];
-        if (s >= 2) {
-            pre_load(s - 2, true, P);
+        for (int j = 0; j < RPT; ++j) hr[j] = hn[j];
+        if (s > 0) {
+            pre_load(s - 1, true, P);
 #pragma unroll
-            for (int j = 0; j < RPT; ++j) hn[j] = ck(s - 2, j);
+            for (int j = 0; j < RPT; ++j) hn[j] = myck[((size_t)(s - 1) * RPT + j) * kBT + tid];
         }
-        float rr2[kSub] = {}, ee2[kSub] = {};
+        float rr[kSub], ee[kSub];
 #pragma unroll
-        for (int i = 0; i < kSub; ++i) {
-            const int t = kSub - 1 - i;         // token of block s stepped back
-            const bool ok = t0 + t < T;         // uniform over the CTA
-            const int slot = map ? i : t;       // its slot; token i of block s - 1 goes there next
-            float hp[RPT], vq[RPT];
-            float drp = 0.f;
-            const float dO = Bc.d[t * kNC + lane], bt = Bc.b[t];
-            if (ok) {
+        for (int t = 0; t < kSub; ++t) {
+            // h' of token t is the state after the decay, before the write
 #pragma unroll
-                for (int j = 0; j < RPT; ++j) {
-                    const float kr = Bc.k[t * DK + r0 + j];
-                    hp[j] = ring[((size_t)slot * RPT + j) * kBT + tid];
-                    vq[j] = (hp[j] + kr * rr[t]) * dO;       // h_t * dO
-                    g[j] += Bc.q[t * DK + r0 + j] * dO;
-                    drp += g[j] * kr;
-                }
+            for (int j = 0; j < RPT; ++j) ring[((size_t)t * RPT + j) * kBT + tid] = hr[j] * decay(t, j);
+            fwd_step(t, hr, rr[t], ee[t]);
+        }
+#pragma unroll
+        for (int t = kSub - 1; t >= 0; --t) {
+            if (t0 + t >= T) continue;   // uniform over the CTA
+            const float dO = ds[t * kNC + lane], bt = bs[t];
+            float hp[RPT], vq[RPT], vk[RPT], vg[RPT];
+            float dr = 0.f;
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) {
+                const float kr = ks[t * DK + r0 + j];
+                hp[j] = ring[((size_t)t * RPT + j) * kBT + tid];
+                vq[j] = (hp[j] + kr * rr[t]) * dO;       // h_t * dO
+                g[j] += qs[t * DK + r0 + j] * dO;
+                dr += g[j] * kr;
             }
-            float pp = 0.f;
-            if (rec) {
+            dr = row_sum(dr);
+            if (warp == 0) dv_out[tok(t0 + t) * dv + col] = bt * dr;
+            const float dp = -bt * dr;
+            float gsum = 0.f;
 #pragma unroll
-                for (int j = 0; j < RPT; ++j) {
-                    h2[j] *= dec(Br, i, j);
-                    ring[((size_t)slot * RPT + j) * kBT + tid] = h2[j];
-                    pp += h2[j] * Br.k[i * DK + r0 + j];
-                }
+            for (int j = 0; j < RPT; ++j) {
+                const float kr = ks[t * DK + r0 + j];
+                vk[j] = g[j] * rr[t] + hp[j] * dp;
+                g[j] += kr * dp;                         // dL/dh'
+                vg[j] = g[j] * hp[j];
+                gsum += vg[j];
             }
-            const float2 sums = xchg(drp, pp);
-            if (rec) {
-                ee2[i] = Br.v[i * kNC + lane] - sums.y;
-                rr2[i] = Br.b[i] * ee2[i];
-#pragma unroll
-                for (int j = 0; j < RPT; ++j) h2[j] += Br.k[i * DK + r0 + j] * rr2[i];
+            // column sums of this warp's rows: one writer per row
+            const float sq = sum_over_lanes<RPT>(vq, lane);
+            const float sk = sum_over_lanes<RPT>(vk, lane);
+            if (writer) {
+                aq[t * DK + r0 + jrow] = sq;
+                ak[t * DK + r0 + jrow] = sk;
             }
-            if (ok) {
-                const float dr = sums.x;
-                if (warp == 0) dv_out[tok(t0 + t) * dv + col] = bt * dr;
-                const float dp = -bt * dr;
-                float vk[RPT], vg[RPT];
-                float gsum = 0.f;
-#pragma unroll
-                for (int j = 0; j < RPT; ++j) {
-                    const float kr = Bc.k[t * DK + r0 + j];
-                    vk[j] = g[j] * rr[t] + hp[j] * dp;
-                    g[j] += kr * dp;                         // dL/dh'
-                    vg[j] = g[j] * hp[j];
-                    gsum += vg[j];
-                }
-                // column sums of this warp's rows: one writer per row
-                const float sq = sum_over_lanes<RPT>(vq, lane);
-                const float sk = sum_over_lanes<RPT>(vk, lane);
-                if (writer) {
-                    aq[t * DK + r0 + jrow] = sq;
-                    ak[t * DK + r0 + jrow] = sk;
-                }
-                if (MODE == LDN_KDA) {
-                    const float sg = sum_over_lanes<RPT>(vg, lane);
-                    if (writer) ag[t * DK + r0 + jrow] = sg;
-                }
-                if (MODE == LDN_GDN) {
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
-                    if (lane == 0) agw[t * kNW + warp] = gsum;
-                }
-                if (warp == 0) {   // dbeta: every warp holds the same dr; warp 0 sums the columns
-                    float db = dr * ee[t];
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
-                    if (lane == 0) ab[t] = db;
-                }
-#pragma unroll
-                for (int j = 0; j < RPT; ++j) g[j] *= dec(Bc, t, j);   // dL/dh_{t-1}
+            if (MODE == LDN_KDA) {
+                const float sg = sum_over_lanes<RPT>(vg, lane);
+                if (writer) ag[t * DK + r0 + jrow] = sg;
             }
+            if (MODE == LDN_GDN) {
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+                if (lane == 0) agw[t * kNW + warp] = gsum;
+            }
+            if (warp == 0) {   // dbeta: every warp holds the same dr; warp 0 sums the columns
+                float db = dr * ee[t];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
+                if (lane == 0) ab[t] = db;
+            }
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) g[j] *= decay(t, j);   // dL/dh_{t-1}
         }
         __syncthreads();
         // this slice's partial sums of block s
@@ -430,14 +354,7 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
                 pg[(size_t)sl * N + n] = sg;
             }
         }
-        if (s >= 2) pre_store((s - 2) % 3, true, P);   // the buffer block s + 1 used
-#pragma unroll
-        for (int t = 0; t < kSub; ++t) {
-            rr[t] = rr2[t];
-            ee[t] = ee2[t];
-        }
-        map ^= 1;
-        __syncthreads();   // block s - 2 staged; the sums of block s read before block s - 1 writes them
+        if (s > 0) pre_store((s - 1) & 1, true, P);
     }
 #pragma unroll
     for (int j = 0; j < RPT; ++j) dS0[((size_t)unit * DK + r0 + j) * dv + col] = g[j];
