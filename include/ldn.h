@@ -16,6 +16,20 @@
  * token, written in the prediction-correction form of the Residual Linear
  * Attention notes, Sec. 1.2.
  *
+ * Entry points, in the order below:
+ *   ldn_chunk_fwd, _variant, _select, _ws, _workspace_size, _select_ws, _noalloc
+ *       the chunkwise forward and its kernel families;
+ *   ldn_prologue, ldn_rmsnorm_gated     the steps on either side of it;
+ *   ldn_decode_step                     one recurrent token;
+ *   ldn_chunk_fwd_gdn2, ldn_decode_step_gdn2
+ *       Gated DeltaNet-2 (separate erase and write gates, Sec. 2.6);
+ *   ldn_backward, ldn_backward_workspace_size
+ *       gradients of the forward;
+ *   ldn_rla_fwd, ldn_rla_workspace_size
+ *       Residual Linear Attention / Residual DeltaNet (the Residual Linear
+ *       Attention notes, Sec. 2.2-2.6);
+ *   ldn_get_device_status, ldn_status_string, ldn_version.
+ *
  * Conventions shared by every entry point
  *   - Pointers q, k, v, beta, gate, S0, S, out, S_final are DEVICE pointers to
  *     contiguous, row-major arrays.  Alignment: ldn_chunk_fwd needs q, k, v,
