@@ -610,12 +610,10 @@ def run_ours(args):
             rsf = torch.empty((B_, H_, dk_, dv_), dtype=torch.float32, device="cuda")
             rrf = torch.empty_like(rsf)
             rdt = ldn.LDN_BF16 if rp["dtype"] == "bf16" else ldn.LDN_F32
-            rneed = ldn.ldn_rla_workspace_size(B_, T_, H_, dv_, rdt)
-            rws = torch.empty(rneed, dtype=torch.uint8, device="cuda")
 
             def rstep():
                 st_ = ldn.ldn_rla_fwd(P(rq), P(rk), P(rv), P(rb), P(rgm), P(rgt), rp["clip"], 0, 0, P(rout), P(rsf),
-                                      P(rrf), B_, T_, H_, dk_, dv_, int(rp["delta"]), rdt, rws.data_ptr(), rneed, sh)
+                                      P(rrf), B_, T_, H_, dk_, dv_, int(rp["delta"]), rdt, sh)
                 if st_ != ldn.LDN_OK:
                     raise ldn.LdnError(st_, "ldn_rla_fwd")
 
@@ -627,14 +625,13 @@ def run_ours(args):
                 rstep()
                 e1.record(stream)
             barrier()
-            launches += 4 * (1 + len(rev))
+            launches += 1 + len(rev)
             rms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in rev))
             rbytes = rla_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(rp["dtype"]))
-            stage2 = "chunk_tc_kernel<GDN>" if rp["delta"] else "chunk_simt_kernel<additive>"
             rla[name] = {"ms_per_call": rms, "tokens_per_s": world * B_ * T_ / (rms / 1e3),
-                         "kernels": f"chunk_simt_kernel (stage 1, pre-update reads) + clip + {stage2} + sum",
+                         "kernels": "rla_kernel (both states in one pass)",
                          "algorithmic_bytes": rbytes, "hbm_frac": rbytes / (rms / 1e3) / 1e9 / hbm_peak}
-            del rq, rk, rv, rb, rgm, rgt, rout, rsf, rrf, rws
+            del rq, rk, rv, rb, rgm, rgt, rout, rsf, rrf
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("rla: device status not ok")
 

@@ -8,7 +8,7 @@ Two layers:
   * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
     ``ldn_chunk_fwd_workspace_size``, ``ldn_chunk_fwd_noalloc``, ``ldn_decode_step``,
     ``ldn_chunk_fwd_gdn2``, ``ldn_decode_step_gdn2``, ``ldn_backward``,
-    ``ldn_backward_workspace_size``, ``ldn_rla_fwd``, ``ldn_rla_workspace_size``, ``ldn_prologue``,
+    ``ldn_backward_workspace_size``, ``ldn_rla_fwd``, ``ldn_prologue``,
     ``ldn_rmsnorm_gated``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
@@ -59,8 +59,7 @@ _SIGNATURES = {
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
     "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 8 + [_P], _I),
     "ldn_backward": ([_P] * 14 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
-    "ldn_rla_fwd": ([_P] * 6 + [ctypes.c_float] + [_P] * 5 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
-    "ldn_rla_workspace_size": ([_I] * 5, ctypes.c_size_t),
+    "ldn_rla_fwd": ([_P] * 6 + [ctypes.c_float] + [_P] * 5 + [_I] * 7 + [_P], _I),
     "ldn_backward_workspace_size": ([_I] * 6, ctypes.c_size_t),
     "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
@@ -155,13 +154,9 @@ def ldn_backward_workspace_size(B, T, H, dk, dv, mode):
 
 
 def ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv, delta, dtype,
-                workspace, workspace_bytes, stream):
+                stream):
     return load().ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv,
-                              delta, dtype, workspace, workspace_bytes, stream)
-
-
-def ldn_rla_workspace_size(B, T, H, dv, dtype):
-    return load().ldn_rla_workspace_size(B, T, H, dv, dtype)
+                              delta, dtype, stream)
 
 
 def ldn_prologue(q_in, k_in, v_in, conv_q, conv_k, conv_v, width, beta_logit, gate_z, gate_a, gate_b,
@@ -392,7 +387,7 @@ def backward(q, k, v, beta, gate, S0, dout, dS_final=None, *, mode, workspace=No
     return g
 
 
-def rla_fwd(q, k, v, beta, gamma, gate, S0=None, R0=None, *, clip=1.0, delta=False, workspace=None, stream=None):
+def rla_fwd(q, k, v, beta, gamma, gate, S0=None, R0=None, *, clip=1.0, delta=False, stream=None):
     """RLA (delta=False) or RDN (delta=True) forward on torch CUDA tensors
     (ldn_rla_fwd).  q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16); beta,
     gamma, gate [B,T,H] float32; S0, R0 [B,H,dk,dv] float32 or None.
@@ -407,13 +402,9 @@ def rla_fwd(q, k, v, beta, gamma, gate, S0=None, R0=None, *, clip=1.0, delta=Fal
     out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     sf = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     rf = torch.empty_like(sf)
-    need = ldn_rla_workspace_size(B, T, H, dv, _dtype_code(q))
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    _check(workspace, "workspace", dtype=torch.uint8)
     st = ldn_rla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(gate), float(clip), _ptr(S0), _ptr(R0),
                      _ptr(out), _ptr(sf), _ptr(rf), B, T, H, dk, dv, int(bool(delta)), _dtype_code(q),
-                     _ptr(workspace), workspace.numel(), _stream_handle(stream))
+                     _stream_handle(stream))
     if st != LDN_OK:
         raise LdnError(st, "ldn_rla_fwd")
     return out, sf, rf

@@ -488,16 +488,10 @@ extern "C" int ldn_backward(const void *q, const void *k, const void *v, const f
     return launch_backward(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 
-extern "C" size_t ldn_rla_workspace_size(int B, int T, int H, int dv, int dtype)
-{
-    if (B < 1 || T < 0 || H < 1 || !supported_dim(dv) || (dtype != LDN_F32 && dtype != LDN_BF16)) return 0;
-    return rla_workspace_bytes(B, T, H, dv, dtype);
-}
-
 extern "C" int ldn_rla_fwd(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
                            const float *gate, float clip, const float *S0, const float *R0, void *out,
                            float *S_final, float *R_final, int B, int T, int H, int dk, int dv, int delta,
-                           int dtype, void *workspace, size_t workspace_bytes, void *stream)
+                           int dtype, void *stream)
 {
     const int st = validate_common(LDN_GDN, dtype, dk, dv);
     if (st != LDN_OK) return st;
@@ -514,19 +508,14 @@ extern "C" int ldn_rla_fwd(const void *q, const void *k, const void *v, const fl
         if (R_final && launch_copy_state(R0, R_final, ns, s) != cudaSuccess) return LDN_ERR_CUDA;
         return LDN_OK;
     }
-    const void *must[] = {q, k, v, beta, gamma, gate, out, workspace};
+    const void *must[] = {q, k, v, beta, gamma, gate, out};
     for (const void *p : must)
         if (!p) return LDN_ERR_INVALID_ARG;
     const void *vec[] = {q, k, v, out};
     for (const void *p : vec)
         if (!aligned16(p)) return LDN_ERR_INVALID_ARG;
     if (!aligned(beta, 4) || !aligned(gamma, 4) || !aligned(gate, 4)) return LDN_ERR_INVALID_ARG;
-    if (!aligned(workspace, 256) || workspace_bytes < rla_workspace_bytes(B, T, H, dv, dtype))
-        return LDN_ERR_INVALID_ARG;
-    int *sw = status_word_ptr();
-    if (!sw) return LDN_ERR_CUDA;
-    RlaArgs a{q, k, v, beta, gamma, gate, S0, R0, clip, out, S_final, R_final, workspace,
-              B, T, H, dk, dv, delta, dtype, sw};
+    RlaArgs a{q, k, v, beta, gamma, gate, S0, R0, clip, out, S_final, R_final, B, T, H, dk, dv, delta, dtype};
     return launch_rla(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 

@@ -84,19 +84,6 @@ struct BwdArgs {
     float *ws;   // checkpoints, then the per-slice partial sums
     int B, T, H, dk, dv, mode, dtype;
 };
-// Token-recurrent forward for scalar decay (csrc/recurrent.cu): pre = true writes
-// S_{t-1} k_t and alpha_t S_{t-1} q_t (fp32) per token, pre = false writes S_t q_t
-// (dtype); delta selects the delta rule over the additive one.
-struct RecArgs {
-    const void *q, *k, *v;
-    const float *beta, *gate, *S0;
-    float *S_final, *p_out, *s_out;
-    void *o_out;
-    int B, T, H, dk, dv, dtype;
-    bool delta, pre;
-};
-cudaError_t launch_recurrent(const RecArgs &a, cudaStream_t stream);
-
 // Residual Linear Attention / Residual DeltaNet forward (csrc/rla.cu).
 struct RlaArgs {
     const void *q, *k, *v;
@@ -104,12 +91,8 @@ struct RlaArgs {
     float clip;
     void *out;
     float *S_final, *R_final;
-    void *ws;
     int B, T, H, dk, dv, delta, dtype;
-    int *status;
 };
-size_t rla_off(size_t bytes);   // 256-byte rounding of the workspace sections
-size_t rla_workspace_bytes(int B, int T, int H, int dv, int dtype);
 cudaError_t launch_rla(const RlaArgs &a, cudaStream_t stream);
 size_t bwd_ckpt_floats(int B, int T, int H, int dk, int dv);
 size_t bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int mode);

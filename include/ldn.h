@@ -25,9 +25,9 @@
  *       Gated DeltaNet-2 (separate erase and write gates, Sec. 2.6);
  *   ldn_backward, ldn_backward_workspace_size
  *       gradients of the forward;
- *   ldn_rla_fwd, ldn_rla_workspace_size
+ *   ldn_rla_fwd
  *       Residual Linear Attention / Residual DeltaNet (the Residual Linear
- *       Attention notes, Sec. 2.2-2.6);
+ *       Attention notes, Sec. 2.2-2.4);
  *   ldn_get_device_status, ldn_status_string, ldn_version.
  *
  * Conventions shared by every entry point
@@ -361,34 +361,25 @@ size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode
 /*
  * ldn_rla_fwd -- Residual Linear Attention (delta = 0) or Residual DeltaNet
  * (delta = 1), forward ("Residual Linear Attention" reading notes, Sec. 2.2
- * boxed form, Sec. 2.4, and the two-stage computation of Sec. 2.6):
+ * boxed form, Sec. 2.4):
  *   r_t = Clip_[-c, c](v_t - S_{t-1} k_t)     (the previous base state, before
  *                                             its decay and write)
  *   RLA: R_t = alpha_t R_{t-1} + gamma_t r_t k_t^T,  S_t = alpha_t S_{t-1} + beta_t v_t k_t^T
  *   RDN: R_t = alpha_t R_{t-1}(I - gamma_t k_t k_t^T) + gamma_t r_t k_t^T,
  *        S_t = alpha_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T
  *   o_t = alpha_t S_{t-1} q_t + gamma_t R_t q_t      (the UPDATED residual state)
- * Four launches: the base state by a token-recurrent fp32 kernel that also
- * writes S_{t-1} k_t and alpha_t S_{t-1} q_t; the clip; the residual state
- * with v := r and beta := gamma (the tensor-core chunk kernel for RDN with
- * bf16 inputs and dk = 128, else the recurrent kernel); the sum.  r and the
- * stage-2 output are held in the input dtype (bf16 rounds them).
+ * One launch: both states step together, token by token, in fp32 (the notes'
+ * two-stage computation, Sec. 2.6, is not needed when both states are on chip).
  *   q, k [B][T][H][dk], v, out [B][T][H][dv] of dtype (16-byte aligned)
  *   beta, gamma, gate (log alpha) [B][T][H] fp32 (4-byte aligned)
  *   clip c > 0 (INFINITY: no clip)
  *   S0, R0 [B][H][dk][dv] fp32 or NULL (zeros); S_final, R_final the same
  *   shape or NULL (not written); all 16-byte aligned
- *   workspace 256-byte aligned, at least ldn_rla_workspace_size bytes
  *   dk, dv in {64, 128}; T = 0 copies the initial states to the final ones.
  */
 int ldn_rla_fwd(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
                 const float *gate, float clip, const float *S0, const float *R0, void *out, float *S_final,
-                float *R_final, int B, int T, int H, int dk, int dv, int delta, int dtype, void *workspace,
-                size_t workspace_bytes, void *stream);
-
-/* Bytes of workspace ldn_rla_fwd needs (S_{t-1} k_t and alpha_t S_{t-1} q_t in
- * fp32, r and the stage-2 output in dtype), or 0 for sizes it rejects. */
-size_t ldn_rla_workspace_size(int B, int T, int H, int dv, int dtype);
+                float *R_final, int B, int T, int H, int dk, int dv, int delta, int dtype, void *stream);
 
 /* Synchronises `stream`, then reads and clears the device status word on the
  * current device.  Returns LDN_OK, LDN_ERR_TIMEOUT (a kernel abandoned a

@@ -381,20 +381,17 @@ def test_backward_workspace_size(lib):
 
 def _rla(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, gamma=FAKE, gate=FAKE, clip=1.0, S0=None, R0=None, out=FAKE,
-             sf=None, rf=None, B=1, T=64, H=1, dk=64, dv=64, delta=1, dtype=1, ws=FAKE, wsb=1 << 40, stream=None)
+             sf=None, rf=None, B=1, T=64, H=1, dk=64, dv=64, delta=1, dtype=1, stream=None)
     a.update(kw)
     return ldn.ldn_rla_fwd(a["q"], a["k"], a["v"], a["beta"], a["gamma"], a["gate"], a["clip"], a["S0"], a["R0"],
                            a["out"], a["sf"], a["rf"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["delta"],
-                           a["dtype"], a["ws"], a["wsb"], a["stream"])
+                           a["dtype"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,want", [
     (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
     (dict(gamma=None), ldn.LDN_ERR_INVALID_ARG),
     (dict(gate=None), ldn.LDN_ERR_INVALID_ARG),
-    (dict(ws=None), ldn.LDN_ERR_INVALID_ARG),
-    (dict(wsb=100), ldn.LDN_ERR_INVALID_ARG),
-    (dict(ws=FAKE + 16), ldn.LDN_ERR_INVALID_ARG),          # 256-byte alignment
     (dict(clip=0.0), ldn.LDN_ERR_INVALID_ARG),
     (dict(clip=-1.0), ldn.LDN_ERR_INVALID_ARG),
     (dict(clip=float("nan")), ldn.LDN_ERR_INVALID_ARG),
@@ -404,16 +401,7 @@ def _rla(**kw):
     (dict(gamma=FAKE + 2), ldn.LDN_ERR_INVALID_ARG),
     (dict(dk=96), ldn.LDN_ERR_UNSUPPORTED),
     (dict(dtype=4), ldn.LDN_ERR_INVALID_ARG),
-    (dict(T=0, q=None, out=None, ws=None), ldn.LDN_OK),     # no state asked: nothing to do
+    (dict(T=0, q=None, out=None), ldn.LDN_OK),              # no state asked: nothing to do
 ])
 def test_rla_rejects_bad_arguments(lib, kw, want):
     assert _rla(**kw) == want
-
-
-def test_rla_workspace_size(lib):
-    B, T, H, dv = 2, 70, 3, 128
-    n = B * T * H * dv
-    up = lambda x: (x + 255) // 256 * 256
-    assert ldn.ldn_rla_workspace_size(B, T, H, dv, 1) == 2 * up(4 * n) + 2 * up(2 * n)
-    assert ldn.ldn_rla_workspace_size(B, T, H, dv, 0) == 4 * up(4 * n)
-    assert ldn.ldn_rla_workspace_size(B, T, H, 96, 1) == 0
