@@ -1,5 +1,5 @@
 """GPU parity of ldn_rla_fwd (Residual Linear Attention and Residual DeltaNet,
-two-stage) against the fp64 RLA / RDN oracle, element by element.
+one pass) against the fp64 RLA / RDN oracle, element by element.
 
 Tolerances: fp32 inputs 1e-4; bf16 inputs 2e-2, with the bf16-stored output
 measured beyond its half-ulp rounding as for the other modes (the kernel runs
