@@ -718,13 +718,24 @@ def run_ours(args):
 def run_profile_case(args):
     """Two untimed calls of one operation on a given shape (a small case for an
     ncu capture): backward-gdn / backward-kda (ldn_backward), gdn2
-    (ldn_chunk_fwd_gdn2) or kda (ldn_chunk_fwd_noalloc), automatic variant,
-    bf16, d = 128, the workload recipe of the named mode."""
+    (ldn_chunk_fwd_gdn2), kda (ldn_chunk_fwd_noalloc) or rdn (ldn_rla_fwd),
+    automatic variant, bf16, d = 128, the workload recipe of the named mode."""
+    import numpy as np
     import torch
     import gated_delta_rule_chunkwise_gb300 as ldn
     from gated_delta_rule_chunkwise_gb300 import workloads as wl
     ldn.load()
     B, T, H = (int(x) for x in args.shape.split(","))
+    if args.profile == "rdn":
+        p = wl.make_rla("rdn_bf16_b4_t2048_h16_d128", B=B, T=T, H=H)
+        d = lambda a, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dt)
+        for _ in range(2):
+            ldn.rla_fwd(d(p["q"], torch.bfloat16), d(p["k"], torch.bfloat16), d(p["v"], torch.bfloat16), d(p["beta"]),
+                        d(p["gamma"]), d(p["gate"]), clip=p["clip"], delta=True)
+        torch.cuda.synchronize()
+        st = ldn.device_status()
+        print(json.dumps({"profile_case": args.profile, "shape": [B, T, H], "status": st}))
+        return 0 if st == ldn.LDN_OK else 1
     name = {"backward-gdn": "gdn_bf16_b4_t2048_h16_d128", "backward-kda": "kda_bf16_b8_t4096_h16_d128",
             "gdn2": "gdn2_bf16_b8_t4096_h16_d128", "kda": "kda_bf16_b8_t4096_h16_d128"}[args.profile]
     w = wl.make_chunk(name, B=B, T=T, H=H)
@@ -766,7 +777,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workload lines")
-    ap.add_argument("--profile", choices=["backward-gdn", "backward-kda", "gdn2", "kda"],
+    ap.add_argument("--profile", choices=["backward-gdn", "backward-kda", "gdn2", "kda", "rdn"],
                     help="run one operation twice, untimed, on --shape (a small case for ncu) and exit")
     ap.add_argument("--shape", default="1,2048,16", help="B,T,H for --profile")
     args = ap.parse_args()
