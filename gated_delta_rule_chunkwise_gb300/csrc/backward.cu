@@ -196,8 +196,21 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
             if (MODE == LDN_GDN) a_[tid * DK] = expf(P.g);
         }
     };
-    auto decay = [&](int t, int j) -> float {
-        return MODE == LDN_KDA ? as[t * DK + r0 + j] : (MODE == LDN_GDN ? as[t * DK] : 1.f);
+    // this warp's RPT rows of a [kSub][DK] input at token t (16-byte aligned): vector loads
+    auto rows = [&](const float *base, int t, float (&x)[RPT]) {
+#pragma unroll
+        for (int j = 0; j < RPT; j += 4) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(base + t * DK + r0 + j);
+            x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
+        }
+    };
+    auto decays = [&](int t, float (&x)[RPT]) {
+        if constexpr (MODE == LDN_KDA) {
+            rows(as, t, x);
+        } else {
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) x[j] = MODE == LDN_GDN ? as[t * DK] : 1.f;
+        }
     };
     // Sum over the key rows of this thread's column (all warps): one barrier.
     auto row_sum = [&](float x) -> float {
@@ -212,17 +225,20 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
     };
     // One forward token step on the thread's state rows; returns r and v - p.
     auto fwd_step = [&](int t, float (&hr)[RPT], float &r, float &e) {
+        float kr[RPT], ar[RPT];
+        rows(ks, t, kr);
+        decays(t, ar);
         float p = 0.f;
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
-            hr[j] *= decay(t, j);
-            p += hr[j] * ks[t * DK + r0 + j];
+            hr[j] *= ar[j];
+            p += hr[j] * kr[j];
         }
         p = row_sum(p);
         e = vs[t * kNC + lane] - p;
         r = bs[t] * e;
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) hr[j] += ks[t * DK + r0 + j] * r;
+        for (int j = 0; j < RPT; ++j) hr[j] += kr[j] * r;
     };
 
     float hr[RPT];
@@ -279,23 +295,26 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
 #pragma unroll
         for (int t = 0; t < kSub; ++t) {
             // h' of token t is the state after the decay, before the write
+            float ar[RPT];
+            decays(t, ar);
 #pragma unroll
-            for (int j = 0; j < RPT; ++j) ring[((size_t)t * RPT + j) * kBT + tid] = hr[j] * decay(t, j);
+            for (int j = 0; j < RPT; ++j) ring[((size_t)t * RPT + j) * kBT + tid] = hr[j] * ar[j];
             fwd_step(t, hr, rr[t], ee[t]);
         }
 #pragma unroll
         for (int t = kSub - 1; t >= 0; --t) {
             if (t0 + t >= T) continue;   // uniform over the CTA
             const float dO = ds[t * kNC + lane], bt = bs[t];
-            float hp[RPT], vq[RPT], vk[RPT], vg[RPT];
+            float hp[RPT], vq[RPT], vk[RPT], vg[RPT], kr[RPT], qr[RPT];
+            rows(ks, t, kr);
+            rows(qs, t, qr);
             float dr = 0.f;
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                const float kr = ks[t * DK + r0 + j];
                 hp[j] = ring[((size_t)t * RPT + j) * kBT + tid];
-                vq[j] = (hp[j] + kr * rr[t]) * dO;       // h_t * dO
-                g[j] += qs[t * DK + r0 + j] * dO;
-                dr += g[j] * kr;
+                vq[j] = (hp[j] + kr[j] * rr[t]) * dO;    // h_t * dO
+                g[j] += qr[j] * dO;
+                dr += g[j] * kr[j];
             }
             dr = row_sum(dr);
             if (warp == 0) dv_out[tok(t0 + t) * dv + col] = bt * dr;
@@ -303,9 +322,8 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
             float gsum = 0.f;
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                const float kr = ks[t * DK + r0 + j];
                 vk[j] = g[j] * rr[t] + hp[j] * dp;
-                g[j] += kr * dp;                         // dL/dh'
+                g[j] += kr[j] * dp;                      // dL/dh'
                 vg[j] = g[j] * hp[j];
                 gsum += vg[j];
             }
@@ -331,8 +349,10 @@ bwd_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
                 for (int o = 1; o < 32; o <<= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
                 if (lane == 0) ab[t] = db;
             }
+            float ar[RPT];
+            decays(t, ar);
 #pragma unroll
-            for (int j = 0; j < RPT; ++j) g[j] *= decay(t, j);   // dL/dh_{t-1}
+            for (int j = 0; j < RPT; ++j) g[j] *= ar[j];         // dL/dh_{t-1}
         }
         __syncthreads();
         // this slice's partial sums of block s

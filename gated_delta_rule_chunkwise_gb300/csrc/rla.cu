@@ -116,14 +116,22 @@ rla_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
         const int t0 = s * kSub;
 #pragma unroll
         for (int t = 0; t < kSub; ++t) {
+            // this warp's rows of k_t and q_t (16-byte aligned, contiguous): vector loads
+            float kr[RPT], qr[RPT];
+#pragma unroll
+            for (int j = 0; j < RPT; j += 4) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(ks + t * DK + r0 + j);
+                const float4 q4 = *reinterpret_cast<const float4 *>(qs + t * DK + r0 + j);
+                kr[j] = k4.x; kr[j + 1] = k4.y; kr[j + 2] = k4.z; kr[j + 3] = k4.w;
+                qr[j] = q4.x; qr[j + 1] = q4.y; qr[j + 2] = q4.z; qr[j + 3] = q4.w;
+            }
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                const float kr = ks[t * DK + r0 + j], qr = qs[t * DK + r0 + j];
-                x.x += hs[j] * kr;
-                x.y += hs[j] * qr;
-                x.z += hr[j] * kr;
-                x.w += hr[j] * qr;
+                x.x += hs[j] * kr[j];
+                x.y += hs[j] * qr[j];
+                x.z += hr[j] * kr[j];
+                x.w += hr[j] * qr[j];
             }
             float4 *rb = red + par * kNW * kNC;
             rb[warp * kNC + lane] = x;
@@ -141,9 +149,8 @@ rla_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__re
             const float u = DELTA ? bt * (vv - a * x.x) : bt * vv;
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                const float kr = ks[t * DK + r0 + j];
-                hr[j] = a * hr[j] + wr * kr;
-                hs[j] = a * hs[j] + u * kr;
+                hr[j] = a * hr[j] + wr * kr[j];
+                hs[j] = a * hs[j] + u * kr[j];
             }
             if (warp == 0 && t0 + t < T)
                 store_out(out, tok(t0 + t) * dv + col, a * x.y + gm * (a * x.w + wr * kq[t]));
