@@ -1,6 +1,8 @@
 // Chunkwise forward on the 5th-generation tensor cores (tcgen05, fp16
 // operands, fp32 accumulators in TMEM), fp32 state, for bf16 q/k/v with
-// dk = 128 and dv a multiple of 64; DeltaNet and Gated DeltaNet.
+// dk = 128 and dv a multiple of 64; DeltaNet and Gated DeltaNet (below), KDA
+// (per-channel decay factored about the chunk's row 31, see the KDA operand
+// build) and Gated DeltaNet-2 (KDA with separate erase and write gates).
 //
 // Chunk algebra (exact; derived from the per-token rules of the
 // linear-attention notes, Sec. 2.3-2.4, which give no chunk form).  Memory
@@ -122,7 +124,7 @@ constexpr uint32_t kSmallBytes = 11264;
 constexpr int kMaxStages = 3;
 
 // Input tiles sit in a ring (chunk c in stage c % stages): three stages for
-// DeltaNet / Gated DeltaNet; two for KDA, whose two side tiles take the room.
+// DeltaNet / Gated DeltaNet; two for KDA and Gated DeltaNet-2, whose two side tiles take the room.
 template <int MODE, bool SPLIT = false>
 struct Layout {
     static constexpr bool kda = MODE == LDN_KDA || MODE == LDN_GDN2;   // per-channel decay
