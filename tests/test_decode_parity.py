@@ -55,3 +55,30 @@ def test_decode_full_1000_steps_sampled(name):
         assert rel_err(o[:, b:b + 1, h:h + 1], ro) <= TOL["f32"]
         assert rel_err(S[b:b + 1, h:h + 1], rs) <= TOL["f32"]
     assert np.all(np.isfinite(o))
+
+
+def test_decode_steps_in_a_cuda_graph_match_eager():
+    """ldn_decode_step is capture-safe: 24 steps captured in a CUDA graph and
+    replayed give the same bits as the same steps run eagerly."""
+    import torch
+    w = wl.make_decode("gdn_decode_b64_h16_dk128_dv128_steps1000", B=3, H=5, steps=24, dtype="f32")
+    t = w.torch_inputs("cuda")
+    o_eager, S_eager = run_steps(w)
+    S = t["S0"].clone()
+    outs = [torch.empty((w.B, w.H, w.dv), dtype=torch.float32, device="cuda") for _ in range(w.T)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # first call outside capture (library set-up)
+        ldn.decode_step(t["q"][0], t["k"][0], t["v"][0], t["beta"][0], t["gate"][0], S.clone(), mode=w.mode)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        for i in range(w.T):
+            ldn.decode_step(t["q"][i], t["k"][i], t["v"][i], t["beta"][i], t["gate"][i], S, mode=w.mode, out=outs[i])
+    S.copy_(t["S0"])
+    g.replay()
+    torch.cuda.synchronize()
+    assert ldn.device_status() == ldn.LDN_OK
+    np.testing.assert_array_equal(torch.stack(outs).cpu().numpy(), o_eager)
+    np.testing.assert_array_equal(S.cpu().numpy(), S_eager)
