@@ -194,3 +194,20 @@ def test_decode_full_1000_steps_sampled():
         assert rel_err(o[:, b:b + 1, h:h + 1], ro) <= TOL["f32"]
         assert rel_err(S[b:b + 1, h:h + 1], rs) <= TOL["f32"]
     assert np.all(np.isfinite(o))
+
+
+def test_chunk_split_through_the_library_scratch_in_pieces():
+    """B=2, T=16384, H=16: the split variant's workspace (330 MB per sequence)
+    exceeds the library's 256 MiB array, so the call is cut into token runs with
+    the state carried between them; the erase and write gates must follow every
+    piece's offset.  Sampled (b, h) against the oracle."""
+    import torch
+    w = wl.make_chunk(CHUNK, B=2, T=16384, H=16, s0=True)
+    o, s = run_chunk(w, variant=ldn.LDN_VARIANT_SPLIT)
+    for b, h in [(0, 3), (1, 14)]:
+        sl = lambda a: a[b:b + 1, :, h:h + 1]
+        ro, rs = oracle.fwd_gdn2(sl(w.q), sl(w.k), sl(w.v), sl(w.erase), sl(w.write), sl(w.gate),
+                                 w.S0[b:b + 1, h:h + 1], nthreads=1)
+        assert out_err(o[b:b + 1, :, h:h + 1], ro, "bf16") <= TOL["bf16"]
+        assert rel_err(s[b:b + 1, h:h + 1], rs) <= TOL["bf16"]
+    torch.cuda.empty_cache()
