@@ -39,6 +39,11 @@ MUTANTS = {
     # Gated DeltaNet-2: the write gate is not applied to the value
     "gdn2_no_write": ("const double target = gdn2 ? (double)ww[i] * (double)v[i] : (double)v[i];",
                       "const double target = (double)v[i];"),
+    # GDN2: the write goes along the erase direction e = b * k instead of k (the notes
+    # single this out: the outer product keeps k)
+    "gdn2_write_along_erase": ("for (int c = 0; c < dk; ++c) W[(size_t)i * dk + c] += r * (double)k[c];",
+                               "for (int c = 0; c < dk; ++c) W[(size_t)i * dk + c] += r * (gdn2 ? (double)eb[c] * "
+                               "(double)k[c] : (double)k[c]);"),
     # RLA / RDN: the residual read from the decayed base state instead of the old one
     "rla_residual_decayed": ("double r = (double)v[i] - pk;", "double r = (double)v[i] - alpha * pk;"),
     # RLA / RDN: the correction read without its gamma
