@@ -1,7 +1,6 @@
 """CPU-side checks of the C ABI: the library loads without a GPU, exports
 every entry point include/ldn.h declares, and rejects bad arguments
 synchronously (these paths run before any CUDA call)."""
-import ctypes
 import os
 import re
 
