@@ -26,7 +26,10 @@ RLA / RDN (``fwd_rla``, Residual Linear Attention notes Sec. 2.2, 2.4) are pinne
 in tests/test_rla_oracle_pins.py: RLA against its closed form (decayed sums of
 the writes, written in numpy), RDN against the composition of the Gated DeltaNet
 oracle for both states, the notes' one-step expansion of the output, and the
-clip bound.
+clip bound.  ``ldn_oracle_selftest.c`` (built by ``build`` into an executable
+beside the library) repeats the worked example, the exact write, the brute
+force, the mode reductions and state passing natively, without numpy; the CPU
+suite runs it (tests/test_oracle_selftest_c.py).
 """
 from __future__ import annotations
 
@@ -46,17 +49,35 @@ _lib = None
 MODE_DELTANET, MODE_GDN, MODE_KDA, MODE_GDN2 = 0, 1, 2, 3
 
 
+_SELFTEST_SRC = os.path.join(_HERE, "ldn_oracle_selftest.c")
+SELFTEST_PATH = os.path.join(_HERE, "ldn_oracle_selftest")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-pthread", "-D_POSIX_C_SOURCE=200809L"]
+
+
 def build(force: bool = False) -> str:
     """Compile ldn_oracle.c into libldn_oracle.so beside it (gcc, no fast-math,
-    no FMA contraction, so the fp64 rounding is the same on every host)."""
-    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-           "-pthread", "-D_POSIX_C_SOURCE=200809L", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
+    no FMA contraction, so the fp64 rounding is the same on every host), and the
+    native self-test beside it (``build_selftest``)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    build_selftest(force)
     return _LIB_PATH
+
+
+def build_selftest(force: bool = False, oracle_src: str | None = None, out: str | None = None) -> str:
+    """Compile the native self-test (ldn_oracle_selftest.c, linked with the oracle
+    source under the library's flags) into an executable; ``oracle_src`` and
+    ``out`` let a test build it against a modified copy of the oracle."""
+    src = oracle_src or _SRC
+    out = out or SELFTEST_PATH
+    stale = not os.path.exists(out) or any(os.path.getmtime(out) < os.path.getmtime(f) for f in (src, _SELFTEST_SRC))
+    if force or oracle_src or stale:
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, _SELFTEST_SRC, src, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, out)
+    return out
 
 
 def _load():
