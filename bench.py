@@ -34,7 +34,8 @@ sys.path.insert(0, ROOT)
 METRIC = "tokens/s chunkwise GDN fwd (H=16,dk=dv=128) + % roofline; decode GB/s"
 WORKLOAD = "gdn_bf16_b4_t2048_h16_d128"
 EXTRA_WORKLOADS = ("kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
-                   "gdn_bf16_long_b1_t65536_h16_d128", "deltanet_fp32_b1_t256_h1_d64", "gdn2_bf16_b8_t4096_h16_d128")
+                   "gdn_bf16_long_b1_t32768_h16_d128", "gdn_bf16_long_b1_t65536_h16_d128",
+                   "deltanet_fp32_b1_t256_h1_d64", "gdn2_bf16_b8_t4096_h16_d128")
 PROLOGUE_WORKLOADS = ("gdn_prologue_bf16_b4_t2048_h16_d128_w4", "kda_prologue_bf16_b8_t4096_h16_d128_w4")
 RLA_WORKLOADS = ("rla_bf16_b4_t2048_h16_d128", "rdn_bf16_b4_t2048_h16_d128")
 BACKWARD_WORKLOADS = ("gdn_bf16_b4_t2048_h16_d128", "kda_bf16_b8_t4096_h16_d128")
@@ -189,6 +190,17 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------
 # multi-rank host logic (one process per GPU; no data-path collective)
+L2_NOTE = ("GPU arm: flushed before every timed launch (512 MiB write, then 512 MiB read of another buffer: "
+           "cold and clean); CPU oracle arm: not applicable")
+
+
+def run_config(w, workload, world):
+    """The workload's `config` object, the same keys and values in both arms."""
+    return {"workload": workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": 64,
+            "mode": MODE_NAME[w.mode], "l2": L2_NOTE,
+            "parallelism": f"replica x{world} (independent sequences per GPU)"}
+
+
 def rank_seed(rank: int) -> int:
     """Each rank draws its own independent sequences: the workload is sharded
     by batch (weak scaling), rank r uses seed r."""
@@ -245,8 +257,8 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded recipe, no dataset)",
-            "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": 64, "mode": MODE_NAME[w.mode]},
+            "config": run_config(w, args.workload, int(os.environ.get("WORLD_SIZE", "1"))),
+            "kernel": "fp64 CPU oracle (token-by-token recurrence)",
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -255,8 +267,27 @@ def run_reference(args):
     return 0
 
 
-def cpu_baseline(w):
-    """The oracle as it stands, on this host's cores, over ~10-20 s of work."""
+def parity_record(got, ref, bf16, tol):
+    """Both forms of the parity metric on one tensor: plain max|gpu - oracle| /
+    RMS(oracle), and (bf16-stored results) the error in excess of the 2^-8 |oracle|
+    storage rounding, with the count of elements that are within tol only
+    through that allowance."""
+    import numpy as np
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = max(float(np.sqrt(np.mean(ref * ref))), 1e-30)
+    err = np.abs(got - ref)
+    exc = np.maximum(err - (2.0 ** -8 if bf16 else 0.0) * np.abs(ref), 0.0)
+    return {"plain": float(err.max()) / rms, "excess_over_bf16_rounding": float(exc.max()) / rms,
+            "n_within_tol_only_through_allowance": int(np.count_nonzero((err > tol * rms) & (exc <= tol * rms))),
+            "n_elements": int(ref.size), "tol": tol}
+
+
+def cpu_baseline(w, out=None, S_final=None):
+    """The oracle as it stands, on this host's cores, over ~10-20 s of work.
+    Given the GPU's output and final state for the same workload, also returns
+    their parity against the oracle's result on the same sample (both forms of
+    the metric), else None."""
     import numpy as np
     import oracle
     threads = oracle.default_threads()
@@ -269,13 +300,21 @@ def cpu_baseline(w):
     nh = w.H if units >= w.H else units
     sub = lambda a: None if a is None else np.ascontiguousarray(a[:nb, :, :nh])
     t0 = time.perf_counter()
-    _, _, used = oracle.fwd(sub(w.q), sub(w.k), sub(w.v), sub(w.beta), sub(w.gate), None, mode=w.mode,
-                            return_threads=True)
+    ro, rs, used = oracle.fwd(sub(w.q), sub(w.k), sub(w.v), sub(w.beta), sub(w.gate),
+                              None if w.S0 is None else np.ascontiguousarray(w.S0[:nb, :nh]), mode=w.mode,
+                              return_threads=True)
     dt = time.perf_counter() - t0
     value = (nb * w.T) * (nh / w.H) / dt
-    return {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
-            "sample": f"{nb} of {w.B} sequences x {nh} of {w.H} heads x T={w.T} ({nb * nh * w.T} token-heads, "
-                      f"{dt:.1f} s wall); tokens/s scaled to H={w.H} heads"}
+    sample = f"{nb} of {w.B} sequences x {nh} of {w.H} heads x T={w.T}"
+    base = {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"{sample} ({nb * nh * w.T} token-heads, {dt:.1f} s wall); tokens/s scaled to H={w.H} heads"}
+    par = None
+    if out is not None:
+        tol = 2e-2 if w.dtype == "bf16" else 1e-4
+        par = {"sample": f"{sample}: the timed launch's output and final state against the oracle's",
+               "output": parity_record(out[:nb, :, :nh], ro, w.dtype == "bf16", tol),
+               "final_state": parity_record(S_final[:nb, :nh], rs, False, tol)}
+    return base, par
 
 
 def run_ours(args):
@@ -725,15 +764,12 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded numpy recipe: L2-normalised Gaussian q,k; Gaussian v; sigmoid beta; "
                     "-0.1*softplus log-decay); no dataset",
-            "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": 64, "mode": MODE_NAME[w.mode], "kernel": f"chunk_{from_variant}",
-                       "l2": "flushed before every timed launch (512 MiB write, then 512 MiB read of another buffer: cold and clean)",
-                       "parallelism": f"replica x{world} (independent sequences per GPU)"},
+            "config": run_config(w, args.workload, world), "kernel": f"chunk_{from_variant}",
             "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
             "other_workloads": others, "prologue_epilogue": around, "backward": backward, "rla": rla,
             "wall_s_timed_region": wall, "decode": decode}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"], line["parity"] = cpu_baseline(w, out.float().cpu().numpy(), S_final.cpu().numpy())
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -67,10 +67,6 @@ _SIGNATURES = {
     "ldn_get_device_status": ([_P], _I),
     "ldn_status_string": ([_I], ctypes.c_char_p),
     "ldn_version": ([], _I),
-    "ldn_diag_umma": ([_P] * 3 + [_I] * 6 + [_P], _I),
-    "ldn_diag_umma_tmem_a": ([_P] * 3 + [_I] * 4 + [_P], _I),
-    "ldn_diag_tma_sw128": ([_P] * 2 + [_I] * 4 + [_P], _I),
-    "ldn_diag_wait_timeout": ([ctypes.c_longlong, _P, _P], _I),
 }
 EXPORTS = tuple(_SIGNATURES)
 
@@ -182,22 +178,6 @@ def ldn_status_string(status: int) -> str:
 
 def ldn_version() -> int:
     return load().ldn_version()
-
-
-def ldn_diag_umma(A, B, D, M, N, K, a_mn, b_mn, fmt, stream):
-    return load().ldn_diag_umma(A, B, D, M, N, K, a_mn, b_mn, fmt, stream)
-
-
-def ldn_diag_umma_tmem_a(A, B, D, N, K, b_mn, fmt, stream):
-    return load().ldn_diag_umma_tmem_a(A, B, D, N, K, b_mn, fmt, stream)
-
-
-def ldn_diag_tma_sw128(src, dst, rows, cols, row0, col0, stream):
-    return load().ldn_diag_tma_sw128(src, dst, rows, cols, row0, col0, stream)
-
-
-def ldn_diag_wait_timeout(timeout_ns, waited_ok, stream):
-    return load().ldn_diag_wait_timeout(timeout_ns, waited_ok, stream)
 
 
 # --- torch-tensor convenience layer ---------------------------------------

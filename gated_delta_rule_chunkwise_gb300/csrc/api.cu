@@ -219,7 +219,8 @@ static int noalloc_impl(const void *q, const void *k, const void *v, const float
     uint8_t *scr = nullptr;
     size_t scr_bytes = 0;
     int dev = 0;
-    if (static_scratch_acquire(s, &scr, &scr_bytes, &dev) != cudaSuccess) return LDN_ERR_CUDA;
+    st = static_scratch_acquire(s, &scr, &scr_bytes, &dev);
+    if (st != LDN_OK) return st;
     const size_t el = dtype == LDN_BF16 ? 2 : 4;
     const size_t gate_w = mode == LDN_KDA || mode == LDN_GDN2 ? (size_t)dk : 1;
     // One piece: sequences b0 .. b0+np-1, tokens t0 .. t0+len-1 (t0 > 0 only when np == 1).

@@ -1,15 +1,40 @@
-// Diagnostic entry points (include/ldn_diag.h): check, on tiny matrices, the
-// building blocks the tensor-core kernels rely on -- SWIZZLE_128B placement
-// of TMA loads, shared-memory / instruction descriptors for K-major and
-// MN-major bf16 operands, and the TMEM row layout of M = 64 and M = 128
-// accumulators.  They exist so that tests can pin these encodings directly.
-#include "ldn_internal.cuh"
-#include "sm100_ptx.cuh"
-#include "tma_host.cuh"
+// Diagnostic entry points (include/ldn_diag.h), built into their own library
+// (lib/libldn_diag.so), apart from the product library libldn.so: they check,
+// on tiny matrices, the building blocks the tensor-core kernels rely on --
+// SWIZZLE_128B placement of TMA loads, shared-memory / instruction descriptors
+// for K-major and MN-major 16-bit operands, and the TMEM row layout of M = 64
+// and M = 128 accumulators -- and drive a bounded wait to its limit.  They exist
+// so that tests can pin these encodings and the failure path directly.  This
+// library has a status word of its own (ldn_diag_get_device_status).
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../../include/ldn.h"
+#include "../../../include/ldn_diag.h"
+#include "../sm100_ptx.cuh"
+#include "../tma_host.cuh"
 
 namespace ldn {
+// Status word of the diagnostic kernels (the same encoding as libldn's: bit
+// 1 << LDN_ERR_TIMEOUT set by a kernel that abandoned a bounded wait).
+__device__ int g_diag_status = 0;
+
 namespace {
 using namespace sm100;
+
+int *status_word_ptr()
+{
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_diag_status) != cudaSuccess) return nullptr;
+        addr[dev] = (int *)p;
+    }
+    return addr[dev];
+}
 
 constexpr uint64_t kDiagTimeoutNs = 2000000000ull;   // 2 s
 constexpr float kSentinel = -12345.0f;
@@ -220,6 +245,16 @@ __global__ void diag_timeout_kernel(uint64_t timeout_ns, int *status, int *waite
 }  // namespace ldn
 
 using namespace ldn;
+
+extern "C" int ldn_diag_get_device_status(void *stream)
+{
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LDN_ERR_CUDA;
+    int h = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&h, g_diag_status, sizeof(int)) != cudaSuccess) return LDN_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_diag_status, &zero, sizeof(int)) != cudaSuccess) return LDN_ERR_CUDA;
+    if (h & (1 << LDN_ERR_TIMEOUT)) return LDN_ERR_TIMEOUT;
+    return h ? LDN_ERR_CUDA : LDN_OK;
+}
 
 extern "C" int ldn_diag_wait_timeout(long long timeout_ns, int *waited_ok, void *stream)
 {

@@ -6,7 +6,6 @@
 #include <algorithm>
 
 #include "../../include/ldn.h"
-#include "../../include/ldn_diag.h"
 
 namespace ldn {
 
@@ -102,9 +101,11 @@ cudaError_t launch_rmsnorm_gated(const RmsNormArgs &a, cudaStream_t stream);
 int *status_word_ptr();   // address of the device status word on the current device
 // Library-owned split-variant scratch of ldn_chunk_fwd_noalloc (static_scratch.cu).
 // acquire() locks the current device's scratch and orders `s` after its previous
-// user; release() records the end of this use on `s` and unlocks.
+// user (LDN_OK), or returns LDN_ERR_INVALID_ARG (`s` belongs to another device)
+// or LDN_ERR_UNSUPPORTED (first use on the device during a stream capture);
+// release() records the end of this use on `s` and unlocks.
 constexpr size_t kStaticScratchBytes = (size_t)256 << 20;
-cudaError_t static_scratch_acquire(cudaStream_t s, uint8_t **ptr, size_t *bytes, int *device);
+int static_scratch_acquire(cudaStream_t s, uint8_t **ptr, size_t *bytes, int *device);
 cudaError_t static_scratch_release(cudaStream_t s, int device);
 cudaError_t launch_copy_state(const float *S0, float *S_final, long long n, cudaStream_t stream);
 

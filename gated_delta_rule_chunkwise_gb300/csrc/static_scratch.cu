@@ -2,9 +2,18 @@
 // __device__ array per device, so that the split variant can run without the
 // caller providing (or the library allocating) a workspace.
 //
-// The array lives in this translation unit's own module, which the CUDA
-// runtime loads (and so backs with device memory) only when its symbol is
-// first resolved, i.e. at the first ldn_chunk_fwd_noalloc call on a device.
+// The array lives in this translation unit's own module.  Under lazy module
+// loading (the CUDA default) the runtime loads that module, and so backs the
+// array with device memory, when its symbol is first resolved: at the first
+// call on a device that needs the scratch.  Under CUDA_MODULE_LOADING=EAGER
+// every module loads with the library, so each device the process uses holds
+// the 256 MiB from then on.
+//
+// The first call on a device resolves the address and creates the event
+// below; it must not be made while its stream is being captured into a CUDA
+// graph (it returns LDN_ERR_UNSUPPORTED and enqueues nothing).  The stream
+// must belong to the current device (else LDN_ERR_INVALID_ARG): the lock, the
+// array's address and the event are per device.
 //
 // All calls of a process on one device share the array.  acquire() takes a
 // per-device host lock and makes the caller's stream wait for the event that
@@ -37,33 +46,38 @@ bool capturing(cudaStream_t s)
 
 }  // namespace
 
-cudaError_t static_scratch_acquire(cudaStream_t s, uint8_t **ptr, size_t *bytes, int *device)
+int static_scratch_acquire(cudaStream_t s, uint8_t **ptr, size_t *bytes, int *device)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int dev = 0, sdev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LDN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return LDN_ERR_UNSUPPORTED;
+    if (cudaStreamGetDevice(s, &sdev) != cudaSuccess) return LDN_ERR_INVALID_ARG;
+    if (sdev != dev) return LDN_ERR_INVALID_ARG;
+    const bool cap = capturing(s);
     g_lock[dev].lock();
     if (!g_addr[dev]) {
+        if (cap) {   // set-up (symbol resolution, event creation) stays out of captures
+            g_lock[dev].unlock();
+            return LDN_ERR_UNSUPPORTED;
+        }
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
+        cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g_done[dev], cudaEventDisableTiming);
         if (e != cudaSuccess) {
             g_lock[dev].unlock();
-            return e;
+            return LDN_ERR_CUDA;
         }
         g_addr[dev] = p;
-    } else if (!capturing(s)) {
-        e = cudaStreamWaitEvent(s, g_done[dev], 0);
-        if (e != cudaSuccess) {
+    } else if (!cap) {
+        if (cudaStreamWaitEvent(s, g_done[dev], 0) != cudaSuccess) {
             g_lock[dev].unlock();
-            return e;
+            return LDN_ERR_CUDA;
         }
     }
     *ptr = (uint8_t *)g_addr[dev];
     *bytes = kStaticScratchBytes;
     *device = dev;
-    return cudaSuccess;
+    return LDN_OK;
 }
 
 cudaError_t static_scratch_release(cudaStream_t s, int device)

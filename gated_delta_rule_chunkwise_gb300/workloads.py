@@ -31,6 +31,7 @@ from typing import Optional
 import numpy as np
 
 MODE_DELTANET, MODE_GDN, MODE_KDA, MODE_GDN2 = 0, 1, 2, 3
+MODE_NAMES = {MODE_DELTANET: "deltanet", MODE_GDN: "gdn", MODE_KDA: "kda", MODE_GDN2: "gdn2"}
 
 # name -> recipe.  Sizes are the benchmark workloads; tests shrink them with overrides.
 CHUNK_WORKLOADS = {
@@ -51,10 +52,16 @@ DECODE_WORKLOADS = {
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
-    """fp32 -> nearest bf16 (ties to even), returned as fp32 values (finite inputs)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    """fp32 -> nearest bf16 (ties to even), returned as fp32 values (finite inputs:
+    their bit patterns are at most 0xFF7FFFFF, so adding at most 0x8000 stays
+    inside 32 bits)."""
+    u = np.array(x, dtype=np.float32, copy=True, order="C").view(np.uint32)
+    lsb = u >> np.uint32(16)
+    lsb &= np.uint32(1)
+    lsb += np.uint32(0x7FFF)
+    u += lsb
+    u &= np.uint32(0xFFFF0000)
+    return u.view(np.float32)
 
 
 def _l2norm(x: np.ndarray) -> np.ndarray:

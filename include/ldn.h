@@ -192,15 +192,24 @@ int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int 
  * library for callers that cannot provide device memory.
  *
  * The split variant runs through a library-owned device array of 256 MiB per
- * device (a static __device__ array, backed when the library's module holding
- * it first loads, at the latest at the first call); no device memory is
- * allocated per call.  A call whose workspace does not fit is cut into pieces
- * that do: groups of whole sequences, or, when one sequence alone needs more,
- * runs of whole chunks of one sequence with the state carried between runs in
- * S_final (or in a slot of the array when S_final is NULL).  The pieces are
- * enqueued on `stream` one after another; the result equals that of
- * ldn_chunk_fwd_ws with the split variant up to floating-point rounding (the
- * kernels and per-chunk arithmetic are the same).
+ * device (a static __device__ array); no device memory is allocated per call.
+ * The array is backed with device memory when the module holding it loads:
+ * under lazy module loading (the CUDA default) at the first call on a device
+ * that uses it, under CUDA_MODULE_LOADING=EAGER when the library loads, so that
+ * every device the process uses then holds the 256 MiB.  ldn_chunk_fwd_gdn2's
+ * split variant runs through the same array.  A call whose workspace does not
+ * fit is cut into pieces that do: groups of whole sequences, or, when one
+ * sequence alone needs more, runs of whole chunks of one sequence with the
+ * fp32 state carried between runs in S_final (or in a slot of the array when
+ * S_final is NULL).  The pieces are enqueued on `stream` one after another;
+ * the result is bit-identical to that of ldn_chunk_fwd_ws with the split
+ * variant and a caller workspace (the same kernels on the same operands; the
+ * state passes between pieces in fp32, as between chunks).
+ *
+ * The first call on a device resolves the array's address and creates an
+ * event; it must not be made while `stream` is being captured into a CUDA
+ * graph: such a call returns LDN_ERR_UNSUPPORTED and enqueues nothing.
+ * `stream` must belong to the current device (else LDN_ERR_INVALID_ARG).
  *
  * Arguments, layouts, alignment and error behaviour are those of
  * ldn_chunk_fwd_variant, with LDN_VARIANT_SPLIT also accepted.
@@ -301,7 +310,8 @@ int ldn_decode_step(const void *q, const void *k, const void *v, const float *be
  *   ldn_chunk_fwd.  Alignment: q, k, v, out, S0, S_final 16-byte; erase,
  *   write, gate 4-byte.
  * `variant` and the kernel families are those of ldn_chunk_fwd_noalloc (the
- * split variant through the same library-owned array): the tensor-core
+ * split variant through the same library-owned array, with the same rules on
+ * the first call during a stream capture and on the stream's device): the tensor-core
  * kernels take bf16 inputs with dk = 128, dv a multiple of 64 and erase, write
  * and gate 16-byte aligned (LDN_VARIANT_PAIR is not offered: it returns
  * LDN_ERR_UNSUPPORTED); LDN_VARIANT_SIMT runs the fp32 CUDA-core kernel for

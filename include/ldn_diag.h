@@ -1,12 +1,15 @@
 /*
- * ldn_diag.h -- diagnostic entry points of libldn.
+ * ldn_diag.h -- diagnostic entry points, in a library of their own
+ * (lib/libldn_diag.so, built beside libldn.so; not part of the product ABI).
  *
  * These do not compute the method; they expose, on tiny inputs, the hardware
  * building blocks the tensor-core kernels of ldn.h are made of, so that tests
- * can check each encoding against a plain matrix product.  Pointers are
- * device pointers; calls are asynchronous on `stream`; argument errors return
- * synchronously (LDN_ERR_* of ldn.h); a kernel that abandons a bounded wait
- * sets LDN_ERR_TIMEOUT in the status word read by ldn_get_device_status().
+ * can check each encoding against a plain matrix product, and they drive a
+ * bounded wait to its limit so that tests can check the failure path.
+ * Pointers are device pointers; calls are asynchronous on `stream`; argument
+ * errors return synchronously (LDN_ERR_* of ldn.h); a kernel that abandons a
+ * bounded wait sets LDN_ERR_TIMEOUT in this library's own status word, read
+ * (and cleared) by ldn_diag_get_device_status().
  */
 #ifndef LDN_DIAG_H
 #define LDN_DIAG_H
@@ -53,6 +56,13 @@ int ldn_diag_tma_sw128(const void *src, void *dst, int rows, int cols, int row0,
  * 0 if it timed out.
  */
 int ldn_diag_wait_timeout(long long timeout_ns, int *waited_ok, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the diagnostic kernels' status
+ * word: LDN_OK, LDN_ERR_TIMEOUT (a diagnostic kernel abandoned a bounded wait)
+ * or LDN_ERR_CUDA.
+ */
+int ldn_diag_get_device_status(void *stream);
 
 #ifdef __cplusplus
 }

@@ -18,22 +18,36 @@ def lib():
     return ldn.load()
 
 
-def _declared():
-    names = set()
-    for f in os.listdir(os.path.join(ROOT, "include")):
-        if f.endswith(".h"):
-            txt = open(os.path.join(ROOT, "include", f)).read()
-            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-            names |= set(re.findall(r"\b(ldn_\w+)\s*\(", txt))
-    return names
+def _declared(header):
+    txt = open(os.path.join(ROOT, "include", header)).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return set(re.findall(r"\b(ldn_\w+)\s*\(", txt))
+
+
+def test_headers_are_the_two_libraries():
+    assert sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")) == ["ldn.h",
+                                                                                               "ldn_diag.h"]
 
 
 def test_exports_every_declared_symbol(lib):
-    declared = _declared()
+    declared = _declared("ldn.h")
     assert {"ldn_chunk_fwd", "ldn_decode_step"} <= declared
     for name in declared:
-        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ldn.h but not exported"
     assert set(ldn.EXPORTS) == declared
+
+
+def test_diagnostics_live_in_their_own_library(lib):
+    """include/ldn_diag.h is exported by the test-only libldn_diag.so and by
+    nothing in the product library."""
+    from tests import _diag
+    declared = _declared("ldn_diag.h")
+    assert {"ldn_diag_wait_timeout", "ldn_diag_get_device_status"} <= declared
+    d = _diag.load()
+    for name in declared:
+        assert hasattr(d, name), f"{name} declared in include/ldn_diag.h but not exported"
+        assert not hasattr(lib, name), f"{name} is exported by the product library"
+    assert set(_diag.SIGNATURES) == declared
 
 
 def test_version_and_status_strings(lib):

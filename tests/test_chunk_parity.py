@@ -8,7 +8,7 @@ import pytest
 
 import gated_delta_rule_chunkwise_gb300 as ldn
 from gated_delta_rule_chunkwise_gb300 import workloads as wl
-from tests._helpers import TOL, oracle_chunk, out_err, rel_err
+from tests._helpers import TOL, fmt_parity, oracle_chunk, out_err, parity, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -227,7 +227,7 @@ def test_pair_strong_gates_entrywise_chunks():
     check(w, ldn.LDN_VARIANT_PAIR)
 
 
-# ---- full-size workloads in the benchmark's launch configuration, sampled ----
+# ---- full-size workloads in the benchmark's launch configuration ----
 def _sampled(name, picks, variant=ldn.LDN_VARIANT_AUTO, **over):
     import torch
     w = wl.make_chunk(name, **over)
@@ -245,16 +245,24 @@ def _sampled(name, picks, variant=ldn.LDN_VARIANT_AUTO, **over):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
 
 
-def test_full_gdn_bf16_b4_t2048_sampled():
-    _sampled("gdn_bf16_b4_t2048_h16_d128", [(0, 0), (1, 7), (3, 15)])
+# Every output element and every final-state element of each full-size
+# chunkwise workload (Gated DeltaNet B=4 T=2048; KDA B=8 T=4096; the long
+# Gated DeltaNet sequences T = 8192, 32768, 65536 with S0), computed with the
+# variant the library picks by itself, against the oracle over the whole tensor.
+FULL_WORKLOADS = ["gdn_bf16_b4_t2048_h16_d128", "kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
+                  "gdn_bf16_long_b1_t32768_h16_d128", "gdn_bf16_long_b1_t65536_h16_d128"]
 
 
-def test_full_kda_bf16_b8_t4096_sampled():
-    _sampled("kda_bf16_b8_t4096_h16_d128", [(0, 3), (7, 12)])
-
-
-def test_full_gdn_long_t65536_sampled():
-    _sampled("gdn_bf16_long_b1_t65536_h16_d128", [(0, 5)])
+@pytest.mark.parametrize("name", FULL_WORKLOADS)
+def test_full_workload_whole_tensors(name):
+    w = wl.make_chunk(name)
+    o, s = run_gpu(w)
+    ro, rs = oracle_chunk(w)
+    po, ps = parity(o, ro, w.dtype), parity(s, rs, "f32", tol=TOL[w.dtype])
+    print(f"\n{name}: output: {fmt_parity(po)}; final state: plain {ps['plain']:.3g} over {ps['n']} elements")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
+    assert po["excess"] <= TOL[w.dtype], f"{name}: output {fmt_parity(po)}"
+    assert ps["plain"] <= TOL[w.dtype], f"{name}: final state {ps['plain']:.3g}"
 
 
 @pytest.mark.parametrize("name,picks", [("gdn_bf16_b4_t2048_h16_d128", [(0, 0), (3, 15)]),

@@ -5,7 +5,7 @@ import pytest
 
 import gated_delta_rule_chunkwise_gb300 as ldn
 from gated_delta_rule_chunkwise_gb300 import workloads as wl
-from tests._helpers import TOL, out_err, rel_err
+from tests._helpers import TOL, out_err, parity, rel_err
 import oracle
 
 pytestmark = pytest.mark.gpu
@@ -44,17 +44,16 @@ def test_decode_parity(mode, dtype, dk, dv):
 
 
 @pytest.mark.parametrize("name", sorted(n for n, r in wl.DECODE_WORKLOADS.items() if r["mode"] != wl.MODE_GDN2))
-def test_decode_full_1000_steps_sampled(name):
-    """Full batch 64 x 16 heads, 1000 consecutive tokens; sampled heads vs the oracle."""
+def test_decode_full_1000_steps_whole_tensors(name):
+    """Full batch 64 x 16 heads, 1000 consecutive tokens: every output of every
+    step and every element of the final state against the oracle."""
     w = wl.make_decode(name)
     o, S = run_steps(w)
-    for b, h in [(0, 0), (17, 9), (63, 15)]:
-        ro, rs = oracle.decode(w.q[:, b:b + 1, h:h + 1], w.k[:, b:b + 1, h:h + 1], w.v[:, b:b + 1, h:h + 1],
-                               w.beta[:, b:b + 1, h:h + 1], w.gate[:, b:b + 1, h:h + 1],
-                               w.S0[b:b + 1, h:h + 1], mode=w.mode)
-        assert rel_err(o[:, b:b + 1, h:h + 1], ro) <= TOL["f32"]
-        assert rel_err(S[b:b + 1, h:h + 1], rs) <= TOL["f32"]
+    ro, rs = oracle.decode(w.q, w.k, w.v, w.beta, w.gate, w.S0, mode=w.mode)
+    po, ps = parity(o, ro, "f32"), parity(S, rs, "f32")
+    print(f"\n{name}: outputs plain {po['plain']:.3g} over {po['n']} elements; state plain {ps['plain']:.3g}")
     assert np.all(np.isfinite(o))
+    assert po["plain"] <= TOL["f32"] and ps["plain"] <= TOL["f32"]
 
 
 def test_decode_steps_in_a_cuda_graph_match_eager():

@@ -3,12 +3,14 @@
 Every kernel of the library bounds its waits in time; a wait that runs out
 records LDN_ERR_TIMEOUT in the device status word and the kernel returns
 normally.  The GPU test makes such a wait run out on purpose (an mbarrier
-that nothing arrives on, a 5 ms bound) and checks the status and that the
-context is still usable afterwards.  Argument errors are covered on the CPU
+that nothing arrives on, a 5 ms bound; the waiting kernel is in the test-only
+diagnostic library, which has its own status word) and checks the status and
+that the context, and the product library, are still usable afterwards.  Argument errors are covered on the CPU
 (tests/test_abi_cpu.py)."""
 import pytest
 
 import gated_delta_rule_chunkwise_gb300 as ldn
+from tests import _diag
 
 pytestmark = pytest.mark.gpu
 
@@ -24,12 +26,13 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     import torch
     from gated_delta_rule_chunkwise_gb300 import workloads as wl
     assert ldn.device_status() == ldn.LDN_OK              # clean slate
+    assert _diag.status() == ldn.LDN_OK
     flag = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    st = ldn.ldn_diag_wait_timeout(5_000_000, flag.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    st = _diag.load().ldn_diag_wait_timeout(5_000_000, flag.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert st == ldn.LDN_OK
-    assert ldn.device_status() == ldn.LDN_ERR_TIMEOUT     # recorded ...
+    assert _diag.status() == ldn.LDN_ERR_TIMEOUT          # recorded ...
     assert int(flag.item()) == 0
-    assert ldn.device_status() == ldn.LDN_OK              # ... and cleared by the read
+    assert _diag.status() == ldn.LDN_OK                   # ... and cleared by the read
     # the context is intact: a real call still runs and reports ok
     w = wl.make_chunk("gdn_bf16_b4_t2048_h16_d128", B=1, T=70, H=1)
     t = w.torch_inputs("cuda")
@@ -39,6 +42,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 
 def test_timeout_argument_validation():
-    assert ldn.ldn_diag_wait_timeout(-1, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG
-    assert ldn.ldn_diag_wait_timeout(3_000_000_000, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG
-    assert ldn.ldn_diag_wait_timeout(1000, None, None) == ldn.LDN_ERR_INVALID_ARG
+    d = _diag.load()
+    assert d.ldn_diag_wait_timeout(-1, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG
+    assert d.ldn_diag_wait_timeout(3_000_000_000, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG
+    assert d.ldn_diag_wait_timeout(1000, None, None) == ldn.LDN_ERR_INVALID_ARG

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import gated_delta_rule_chunkwise_gb300 as ldn
+from tests import _diag
 
 pytestmark = pytest.mark.gpu
 
@@ -39,8 +40,8 @@ def test_tma_swizzle_128b_placement(row0, col0):
     src = torch.arange(rows * cols, dtype=torch.int32).remainder(30000).to(torch.int16).view(torch.bfloat16)
     src = src.reshape(rows, cols).cuda().contiguous()
     dst = torch.zeros(8192, dtype=torch.uint8, device="cuda")
-    assert ldn.ldn_diag_tma_sw128(src.data_ptr(), dst.data_ptr(), rows, cols, row0, col0, _stream()) == ldn.LDN_OK
-    assert ldn.device_status() == ldn.LDN_OK
+    assert _diag.load().ldn_diag_tma_sw128(src.data_ptr(), dst.data_ptr(), rows, cols, row0, col0, _stream()) == ldn.LDN_OK
+    assert _diag.status() == ldn.LDN_OK
     got = dst.cpu().numpy().view(np.uint16)
     s = src.view(torch.int16).cpu().numpy().view(np.uint16)
     want = np.zeros(4096, np.uint16)
@@ -68,9 +69,9 @@ def test_umma_f16kind_layouts(M, N, K, a_mn, b_mn, fmt):
     B = torch.randn(N, K, generator=g).to(dt)
     D = torch.empty(128, N, dtype=torch.float32, device="cuda")
     Ad, Bd = A.cuda(), B.cuda()
-    st = ldn.ldn_diag_umma(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, a_mn, b_mn, fmt, _stream())
+    st = _diag.load().ldn_diag_umma(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, a_mn, b_mn, fmt, _stream())
     assert st == ldn.LDN_OK
-    assert ldn.device_status() == ldn.LDN_OK
+    assert _diag.status() == ldn.LDN_OK
     got = D.cpu().numpy().astype(np.float64)
     ref = A.double().numpy() @ B.double().numpy().T
     lane_of = (lambda r: r) if M == 128 else (lambda r: 32 * (r // 16) + r % 16)
@@ -104,8 +105,8 @@ def test_umma_a_operand_in_tmem(N, K, b_mn, fmt):
     B = torch.randn(N, K, generator=g).to(dt)
     D = torch.empty(128, N, dtype=torch.float32, device="cuda")
     Ad, Bd = A.cuda(), B.cuda()
-    assert ldn.ldn_diag_umma_tmem_a(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), N, K, b_mn, fmt, _stream()) == ldn.LDN_OK
-    assert ldn.device_status() == ldn.LDN_OK
+    assert _diag.load().ldn_diag_umma_tmem_a(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), N, K, b_mn, fmt, _stream()) == ldn.LDN_OK
+    assert _diag.status() == ldn.LDN_OK
     got = D.cpu().numpy().astype(np.float64)
     a, b = A.double().numpy(), B.double().numpy()
     ref = a @ b.T

@@ -243,3 +243,46 @@ def test_graph_capture_and_replay():
     assert ldn.device_status() == ldn.LDN_OK
     _same(out, eager_o)
     _same(sf, eager_s)
+
+
+_FIRST_CALL_UNDER_CAPTURE = r"""
+import sys
+sys.path.insert(0, sys.argv[1])
+import torch
+import gated_delta_rule_chunkwise_gb300 as ldn
+from gated_delta_rule_chunkwise_gb300 import workloads as wl
+ldn.load()
+torch.cuda.set_device(0)
+w = wl.make_chunk("gdn_bf16_b4_t2048_h16_d128", B=1, T=200, H=2, s0=True)
+t = w.torch_inputs("cuda")
+out = torch.empty((w.B, w.T, w.H, w.dv), dtype=t["q"].dtype, device="cuda")
+sf = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+args = (t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(), t["beta"].data_ptr(), t["gate"].data_ptr(),
+        t["S0"].data_ptr(), out.data_ptr(), sf.data_ptr(), w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16,
+        ldn.LDN_VARIANT_SPLIT)
+side = torch.cuda.Stream()
+side.wait_stream(torch.cuda.current_stream())
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+    st_cap = ldn.ldn_chunk_fwd_noalloc(*args, side.cuda_stream)
+torch.cuda.synchronize()
+st_eager = ldn.ldn_chunk_fwd_noalloc(*args, torch.cuda.current_stream().cuda_stream)
+torch.cuda.synchronize()
+print(st_cap, st_eager, ldn.device_status())
+"""
+
+
+def test_first_call_under_capture_is_rejected_in_a_fresh_process():
+    """In a fresh process, a first call made while its stream is being captured
+    is refused (LDN_ERR_UNSUPPORTED, nothing enqueued: the capture still ends
+    cleanly); the next call, made eagerly, sets the scratch up and runs."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL_UNDER_CAPTURE, root], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    st_cap, st_eager, dev = (int(x) for x in r.stdout.strip().splitlines()[-1].split())
+    assert st_cap == ldn.LDN_ERR_UNSUPPORTED
+    assert st_eager == ldn.LDN_OK and dev == ldn.LDN_OK
