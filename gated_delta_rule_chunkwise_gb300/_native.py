@@ -32,6 +32,7 @@ LDN_DELTANET, LDN_GDN, LDN_KDA, LDN_GDN2 = 0, 1, 2, 3
 LDN_F32, LDN_BF16 = 0, 1
 LDN_OK, LDN_ERR_INVALID_ARG, LDN_ERR_UNSUPPORTED, LDN_ERR_CUDA, LDN_ERR_TIMEOUT = 0, 1, 2, 3, 4
 LDN_VARIANT_AUTO, LDN_VARIANT_SIMT, LDN_VARIANT_TENSOR, LDN_VARIANT_SPLIT, LDN_VARIANT_PAIR = 0, 1, 2, 3, 4
+LDN_VARIANT_PRESOLVED = 5
 
 MODES = {"deltanet": LDN_DELTANET, "gdn": LDN_GDN, "kda": LDN_KDA}
 
@@ -241,7 +242,7 @@ def chunk_fwd(q, k, v, beta, gate=None, S0=None, *, mode, chunk=64, out=None, S_
     if S_final is None and want_state:
         S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     _check(S_final, "S_final", (B, H, dk, dv), torch.float32)
-    if variant == LDN_VARIANT_SPLIT and workspace is None:
+    if variant in (LDN_VARIANT_SPLIT, LDN_VARIANT_PRESOLVED) and workspace is None:
         need = ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, _dtype_code(q))
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if workspace is not None:

@@ -78,7 +78,7 @@ static int check_chunk_args(const void *q, const void *k, const void *v, const f
     int st = validate_common(mode, dtype, dk, dv, g2 && erase && write);
     if (st != LDN_OK) return st;
     if (B < 1 || H < 1 || T < 0) return LDN_ERR_INVALID_ARG;
-    if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_PAIR) return LDN_ERR_INVALID_ARG;
+    if (variant < LDN_VARIANT_AUTO || variant > LDN_VARIANT_PRESOLVED) return LDN_ERR_INVALID_ARG;
     if (chunk != 64) return LDN_ERR_UNSUPPORTED;
     // Sizes: token-head count and state element count must stay well inside int64
     // and the grid limits.
@@ -104,7 +104,8 @@ static int check_chunk_args(const void *q, const void *k, const void *v, const f
     a.write = write;
     a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype;
     *tc = dtype == LDN_BF16 && chunk_tc_supported(a);
-    if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT || variant == LDN_VARIANT_PAIR) && !*tc)
+    if ((variant == LDN_VARIANT_TENSOR || variant == LDN_VARIANT_SPLIT || variant == LDN_VARIANT_PAIR ||
+         variant == LDN_VARIANT_PRESOLVED) && !*tc)
         return LDN_ERR_UNSUPPORTED;
     if (variant == LDN_VARIANT_PAIR && !chunk_pair_supported(a)) return LDN_ERR_UNSUPPORTED;
     return LDN_OK;
@@ -131,12 +132,15 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     a.write = write;
     const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype) : 0;
     const bool ws_ok = ws && aligned(ws, 256) && need > 0 && ws_bytes >= need;
-    if (variant == LDN_VARIANT_AUTO) variant = !tc ? LDN_VARIANT_SIMT : chunk_tc_pick(a, ws_ok);
+    const bool pre_ok = tc && ws && aligned(ws, 256) && ws_bytes >= presolved_workspace_bytes(B, T, H);
+    if (variant == LDN_VARIANT_AUTO) variant = !tc ? LDN_VARIANT_SIMT : chunk_tc_pick(a, ws_ok, pre_ok);
     if (variant == LDN_VARIANT_SPLIT && !ws_ok) return LDN_ERR_INVALID_ARG;
+    if (variant == LDN_VARIANT_PRESOLVED && !pre_ok) return LDN_ERR_INVALID_ARG;
     a.status = status_word_ptr();
     if (!a.status) return LDN_ERR_CUDA;
     cudaError_t err;
-    if (variant == LDN_VARIANT_SPLIT) err = launch_chunk_split(a, (uint8_t *)ws, s);
+    if (variant == LDN_VARIANT_PRESOLVED) err = launch_chunk_presolved(a, (uint8_t *)ws, s);
+    else if (variant == LDN_VARIANT_SPLIT) err = launch_chunk_split(a, (uint8_t *)ws, s);
     else if (variant == LDN_VARIANT_PAIR) err = launch_chunk_pair(a, s);
     else if (variant == LDN_VARIANT_TENSOR) err = launch_chunk_tc(a, s);
     else err = launch_chunk_simt(a, s);
@@ -148,7 +152,8 @@ extern "C" int ldn_chunk_fwd_variant(const void *q, const void *k, const void *v
                                      int B, int T, int H, int dk, int dv, int chunk, int mode,
                                      int dtype, int variant, void *stream)
 {
-    if (variant == LDN_VARIANT_SPLIT) return LDN_ERR_INVALID_ARG;   // needs a workspace: ldn_chunk_fwd_ws
+    if (variant == LDN_VARIANT_SPLIT || variant == LDN_VARIANT_PRESOLVED)
+        return LDN_ERR_INVALID_ARG;   // needs a workspace: ldn_chunk_fwd_ws
     return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype, variant,
                           nullptr, 0, stream);
 }
@@ -171,7 +176,7 @@ static int noalloc_impl(const void *q, const void *k, const void *v, const float
                         const float *S0, void *out, float *S_final, int B, int T, int H, int dk, int dv, int chunk,
                         int mode, int dtype, int variant, void *stream, const float *erase, const float *write)
 {
-    if (variant != LDN_VARIANT_AUTO && variant != LDN_VARIANT_SPLIT)
+    if (variant != LDN_VARIANT_AUTO && variant != LDN_VARIANT_SPLIT && variant != LDN_VARIANT_PRESOLVED)
         return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
                               variant, nullptr, 0, stream, erase, write);
     bool tc = false;
@@ -187,16 +192,20 @@ static int noalloc_impl(const void *q, const void *k, const void *v, const float
     whole.write = write;
     whole.B = B; whole.T = T; whole.H = H; whole.dk = dk; whole.dv = dv; whole.chunk = chunk;
     whole.mode = mode; whole.dtype = dtype;
+    const int requested = variant;
     if (variant == LDN_VARIANT_AUTO) {
-        const int pick = chunk_tc_pick(whole, true);
-        if (pick != LDN_VARIANT_SPLIT)
+        const int pick = chunk_tc_pick(whole, true, true);
+        if (pick != LDN_VARIANT_SPLIT && pick != LDN_VARIANT_PRESOLVED)
             return chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,
                                   pick, nullptr, 0, stream, erase, write);
+        variant = pick;
     }
 
-    // Plan: nb sequences per piece, or (nb == 0) runs of tpc chunks of one sequence.
+    // Plan: nb sequences per piece, or (nb == 0) runs of tpc chunks of one sequence.  The
+    // workspace per (b, h, chunk) is the split variant's operand image or the pre-solved
+    // variant's X.
     const size_t cap = kStaticScratchBytes;
-    const size_t unit = split_unit_bytes(dv);
+    const size_t unit = variant == LDN_VARIANT_SPLIT ? split_unit_bytes(dv) : presolved_workspace_bytes(1, 64, 1);
     const long long nch = (T + chunk - 1) / chunk;
     const size_t per_seq = (size_t)H * nch * unit;
     const size_t state_elems = (size_t)H * dk * dv;
@@ -208,11 +217,11 @@ static int noalloc_impl(const void *q, const void *k, const void *v, const float
     } else {
         carry_bytes = S_final ? 0 : (state_elems * sizeof(float) + 255) / 256 * 256;
         if (carry_bytes < cap) tpc = (long long)((cap - carry_bytes) / ((size_t)H * unit));
-        if (tpc == 0)
-            return variant == LDN_VARIANT_SPLIT
+        if (tpc == 0)   // one chunk of all heads exceeds the array: a kernel without workspace (AUTO)
+            return requested != LDN_VARIANT_AUTO
                        ? LDN_ERR_UNSUPPORTED
                        : chunk_fwd_impl(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode,
-                                        dtype, chunk_tc_pick(whole, false), nullptr, 0, stream, erase, write);
+                                        dtype, chunk_tc_pick(whole, false, false), nullptr, 0, stream, erase, write);
     }
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -229,7 +238,7 @@ static int noalloc_impl(const void *q, const void *k, const void *v, const float
         return chunk_fwd_impl((const uint8_t *)q + tok * dk * el, (const uint8_t *)k + tok * dk * el,
                               (const uint8_t *)v + tok * dv * el, beta ? beta + tok : nullptr,
                               gate ? gate + tok * gate_w : nullptr, s0, (uint8_t *)out + tok * dv * el, sf, np, len,
-                              H, dk, dv, chunk, mode, dtype, LDN_VARIANT_SPLIT, scr, ws_bytes, stream,
+                              H, dk, dv, chunk, mode, dtype, variant, scr, ws_bytes, stream,
                               erase ? erase + tok * dk : nullptr, write ? write + tok * dv : nullptr);
     };
     st = LDN_OK;
@@ -279,7 +288,8 @@ extern "C" int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int 
     a.erase = a.write = kAligned;
     if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return LDN_VARIANT_SIMT;
     const size_t need = split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype);
-    return chunk_tc_pick(a, need > 0 && workspace_bytes >= need);
+    return chunk_tc_pick(a, need > 0 && workspace_bytes >= need,
+                         T > 0 && workspace_bytes >= presolved_workspace_bytes(B, T, H));
 }
 
 extern "C" size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)

@@ -40,7 +40,7 @@ constexpr uint32_t kStageBytes = 66560;                   // 1024-aligned
 constexpr uint32_t kOffHB = kStages * kStageBytes;        // H fp16, MN-major 128 x 64
 constexpr uint32_t kOffUB = kOffHB + 16384;               // U fp16, MN-major 64 x 64
 constexpr uint32_t kOffBars = kOffUB + 8192;
-constexpr uint32_t kSmemBytes = kOffBars + 128 + 1024;   // bars: full[3], smma, drain[2]
+constexpr uint32_t kSmemBytes = kOffBars + 128 + 1024;   // bars: full[3], smma, drain[2], s6
 constexpr uint32_t kColD5 = 0, kColD6 = 64, kTmemCols = 128;
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 
@@ -61,14 +61,6 @@ __device__ __forceinline__ void st_row16(uint8_t *block, int row, int col, const
     *reinterpret_cast<uint4 *>(block + sw128_offset(row, col + 8)) =
         make_uint4(pack_h2(v[8], v[9]), pack_h2(v[10], v[11]), pack_h2(v[12], v[13]), pack_h2(v[14], v[15]));
 }
-// 1-D bulk copy global -> shared, completing `bytes` of transactions on `bar`.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat16 *__restrict__ out, float *S_final,
@@ -80,6 +72,10 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBars);   // [kStages]
     uint64_t *smma = full + kStages;
     uint64_t *drain = smma + 1;   // [2]: one per MMA-issuing thread (0, kIssuer6)
+    // MMA6 completes on a barrier of its own: its issuer does not wait for the O rows to
+    // have seen MMA5's completion, and one barrier for both would let a late O-row waiter
+    // see two phases pass and wait for a third
+    uint64_t *s6 = drain + 2;
     __shared__ uint32_t tmem_base_s;
     __shared__ int fail;
 
@@ -97,6 +93,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
         mbar_init(smma, 1);
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
+        mbar_init(s6, 1);
         fence_mbar_init();
         fail = 0;
     }
@@ -216,9 +213,10 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
             const uint32_t kt_s = smem_u32(stg + kOKT), ub_s = smem_u32(UB);
             for (int k = 0; k < kC / 16; ++k)
                 umma_bf16(tbase + kColD6, mnmajor_desc(kt_s, 64, k), mnmajor_desc(ub_s, 64, k), id_mma6, k > 0);
-            umma_commit(smma);
+            umma_commit(s6);
         }
-        wait_smma();
+        if (!mbar_wait(s6, (uint32_t)(c & 1), kWaitNs)) fail = 1;
+        tc_fence_after();
 
         // ---- H <- e^{g_C} H + K~^T U (row st), fp16 copy for the next MMA5
         {

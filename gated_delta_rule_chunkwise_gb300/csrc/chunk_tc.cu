@@ -78,6 +78,7 @@
 // in the status word, both roles abandon their loops, in-flight copies and
 // MMAs are drained with bounded waits, TMEM is freed and the CTA returns.
 #include <algorithm>
+#include <cstddef>
 
 #include "ldn_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -96,6 +97,9 @@ constexpr int kThreads = kPrepThreads + kSerialThreads;
 constexpr uint32_t kBarPrep = 1, kBarSerial = 2;   // named barrier ids
 constexpr uint32_t kBarBuild = 3, kBarBuildIssue = 4;   // KDA operand build (warps 4-7; + issuer warp 3)
 constexpr uint32_t kBarChain = 5, kBarChain2 = 6;       // levels of the block inverse (warps 0-2; 0-1)
+constexpr uint32_t kBarU = 7;                           // kFed: the U rows of the serial warps (64 threads)
+constexpr int kIssuerB = 64;                            // kFed: prep thread issuing MMA4 (warp 2)
+constexpr int kIssuer6 = kPrepThreads + 64;             // kFed: serial thread issuing MMA6 (a U row)
 constexpr int kIssuer = 96;                        // prep thread issuing every prep MMA (warp 3)
 constexpr int kGateWarp = 4;                       // prep warp computing gate prefixes
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
@@ -123,39 +127,32 @@ constexpr int kLd16 = 72;                     // fp16 row stride (144 B: ldmatri
 constexpr uint32_t kSmallBytes = 11264;
 constexpr int kMaxStages = 3;
 
-// Input tiles sit in a ring (chunk c in stage c % stages): three stages for
-// DeltaNet / Gated DeltaNet; two for KDA and Gated DeltaNet-2, whose two side tiles take the room.
-template <int MODE, bool SPLIT = false>
-struct Layout {
-    static constexpr bool kda = MODE == LDN_KDA || MODE == LDN_GDN2;   // per-channel decay
-    static constexpr int stages = kda ? 2 : 3;
-    static constexpr uint32_t vbytes = SPLIT ? 2 * kVBytes : kVBytes;  // V slice (split: all of dv <= 128)
-    static constexpr uint32_t qk = 0;                              // stages x [Q;K]
-    static constexpr uint32_t v = qk + stages * kQKBytes;          // stages x V
-    static constexpr uint32_t kb = v + stages * vbytes;            // KDA: 2 x side tile
-    static constexpr uint32_t akc = kb + (kda ? 2 * kKBBytes : 0); // KDA: [I ; 0] K-major 128 x 64 (16 KB, constant)
-    static constexpr uint32_t ak = akc + (kda ? 16384 : 0);        // [-P Tw ; Tw] K-major 128 x 64 (16 KB)
-    static constexpr uint32_t av = ak + 16384;                     // [P Tu ; Tu] K-major 128 x 64  (16 KB)
-    static constexpr uint32_t hb = av + 16384;                     // H fp16, MN-major 128 x 64     (16 KB)
-    static constexpr uint32_t ub = hb + (SPLIT ? 0 : 16384);       // U~ fp16, MN-major 64 x 64     (8 KB)
-    static constexpr uint32_t a16 = ub + (SPLIT ? 0 : 8192);       // fp16 A [64][72]
-    static constexpr uint32_t p16 = a16 + 64 * kLd16 * 2;          // fp16 P [64][72]
-    static constexpr uint32_t t16 = p16 + 64 * kLd16 * 2;          // fp16 T [64][72]
-    static constexpr uint32_t x = t16 + 64 * kLd16 * 2;            // fp16 16x16 scratch of the block inverse [4][16][24]
-    static constexpr uint32_t small = x + 3072;
-    static constexpr uint32_t bytes = small + kSmallBytes + 1024;
-    static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
-    static_assert(small % 16 == 0 && t16 % 16 == 0 && kb % 1024 == 0 && akc % 1024 == 0 && ak % 1024 == 0,
-                  "buffer alignment (16 B vector accesses, 1024 B swizzled tiles)");
-};
+// KIND kFused: the fused kernel, one CTA per (b, h, 64-wide dv slice) over the whole sequence.
+// KIND kSplit: the preparation kernel of the split variant, one CTA per (b, h, range of
+// `cpr` chunks) over the whole dv; its serial warps write the chunk operands to `ws`.
+// KIND kPair: the fused kernel with the two dv slices of a (b, h) (dv = 128) as a cluster of
+// two CTAs that share the state-independent preparation: CTA r prepares chunks r, r + 2, ...
+// and copies their [P Tu ; Tu], [-P Tw ; Tw] into the peer's shared memory, whose serial
+// warps issue MMA3 / MMA4 for those chunks themselves (DeltaNet / Gated DeltaNet).
+// KIND kPrepX and kFed: the two launches of the pre-solved variant.  kPrepX (prep warps
+// only, two CTAs per SM, one CTA per (b, h, range of chunks)) runs MMA1, the operands A
+// and P, the inverse T and P T, and writes X = [P T ; T] (fp16, 128 x 64, the swizzled
+// K-major image of an MMA A operand, 16 KB per (b, h, chunk)) to `ws`.  kFed is the fused
+// kernel whose prep warps read X instead of computing it: they scale it into AV / AK,
+// convert the k / v tiles, issue MMA3 / MMA4 and form the MMA5 operand [Q~ ; -W], so
+// that the serial warps only run the state step.
+constexpr int kFused = 0, kSplit = 1, kPair = 2, kPrepX = 3, kFed = 4;
+constexpr uint32_t kXBytes = 16384;   // X = [P T ; T] per (b, h, chunk)
 
 struct Small {
     uint64_t bar_load[kMaxStages];   // TMA tiles of ring stage ls landed
     uint64_t bar_pmma;        // prep MMA commits
     uint64_t bar_smma;        // serial MMA commits
+    uint64_t bar_s6;          // kFed: MMA6 commits (its issuer does not wait for MMA5's waiters:
+                              // a barrier of its own keeps a late waiter from seeing two phases)
     uint64_t bar_ready[2];    // MMA3 / MMA4 of stage s complete (prep commit)
     uint64_t bar_rvfree[2];   // serial finished reading RV[s] and DK[s]
-    uint64_t bar_drain[2];    // failure path: last commit of each MMA issuer
+    uint64_t bar_drain[4];    // failure path: last commit of each MMA issuer
     uint64_t bar_kbfree[2];   // KDA: MMA6 of chunk c finished reading side tile c & 1
     uint64_t bar_dkfree[2];   // split: the epilogue has read DK of chunk c (DK has one buffer)
     uint64_t bar_stgfree[2];  // split: the workspace stores of chunk c have read their staging (AV / AK)
@@ -172,8 +169,6 @@ struct Small {
     int kflag[3][4];          // KDA: a channel of this chunk exceeds the factored span (one word per build warp)
     alignas(16) float beta[3][kC];
     alignas(16) float g[3][kC];      // inclusive log-decay prefix
-    alignas(16) float fr[3][kC];     // e^{g_r - m}
-    alignas(16) float fc[3][kC];     // e^{m - g_j}
     alignas(16) float eg[3][kC];     // e^{g_r}
     alignas(16) float egc[3][kC];    // e^{g_C - g_r}
     // KDA, per key channel: e^{m}, e^{g_C - m}, e^{g_C} (m, g_C: the channel's
@@ -184,8 +179,47 @@ struct Small {
     float kxm[kDK];           // KDA build: log-decay prefix at row 31, handed from the rows 0-31 warps
     float stg_beta[2][kC];    // beta / log-gate of the next chunk, prefetched by cp.async
     float stg_gate[2][kC];
+    uint64_t bar_x[2];        // kFed: X of chunk c landed in AV[c & 1]
+    // Factors of MMA1's decay ratios (the operand build of A and P): last, so that
+    // kFed, which does not build them, leaves them out of its shared memory.
+    alignas(16) float fr[3][kC];     // e^{g_r - m}
+    alignas(16) float fc[3][kC];     // e^{m - g_j}
 };
 static_assert(sizeof(Small) <= kSmallBytes, "Small does not fit its shared-memory slot");
+constexpr uint32_t kSmallBytesFed = (offsetof(Small, fr) + 127) / 128 * 128;
+
+// Input tiles sit in a ring (chunk c in stage c % stages): three stages for
+// DeltaNet / Gated DeltaNet; two for KDA and Gated DeltaNet-2, whose two side tiles take
+// the room; one [Q ; K] buffer for kPrepX (MMA1 is its only reader, so the next chunk's
+// tiles load while the current chunk is solved).
+template <int MODE, int KIND = kFused>
+struct Layout {
+    static constexpr bool kda = MODE == LDN_KDA || MODE == LDN_GDN2;   // per-channel decay
+    static constexpr bool prepx = KIND == kPrepX, fed = KIND == kFed, split = KIND == kSplit;
+    static constexpr int stages = prepx ? 1 : (kda ? 2 : 3);
+    static constexpr uint32_t vbytes = prepx ? 0 : (split ? 2 * kVBytes : kVBytes);  // V slice (split: all of dv <= 128)
+    static constexpr uint32_t qk = 0;                              // stages x [Q;K]
+    static constexpr uint32_t v = qk + stages * kQKBytes;          // stages x V
+    static constexpr uint32_t kb = v + stages * vbytes;            // KDA: 2 x side tile (kPrepX: 1)
+    static constexpr uint32_t akc = kb + (kda ? (prepx ? 1 : 2) * kKBBytes : 0); // KDA: [I ; 0] K-major 128 x 64 (16 KB, constant)
+    static constexpr uint32_t ak = akc + (kda && !prepx ? 16384 : 0);   // [-P Tw ; Tw] K-major 128 x 64 (16 KB)
+    // [P Tu ; Tu] K-major 128 x 64 (16 KB).  kFed: AK, AV twice (buffer s at ak + 32 KB s);
+    // kPrepX: AV stages X (KDA: AK before it, for the entry-wise path's scratch only).
+    static constexpr uint32_t av = ak + (prepx && !kda ? 0 : 16384);
+    static constexpr uint32_t hb = av + (fed ? 16384 + 32768 : 16384);   // H fp16, MN-major 128 x 64 (16 KB)
+    static constexpr uint32_t ub = hb + (split || prepx ? 0 : 16384);    // U~ fp16, MN-major 64 x 64 (8 KB)
+    static constexpr uint32_t a16 = ub + (split || prepx ? 0 : 8192);    // fp16 A [64][72]
+    static constexpr uint32_t p16 = a16 + (fed ? 0 : 64 * kLd16 * 2);    // fp16 P [64][72]
+    static constexpr uint32_t t16 = p16 + (fed ? 0 : 64 * kLd16 * 2);    // fp16 T [64][72]
+    static constexpr uint32_t x = t16 + (fed ? 0 : 64 * kLd16 * 2);      // fp16 16x16 scratch of the block inverse [4][16][24]
+    static constexpr uint32_t small = x + (fed ? 0 : 3072);
+    static constexpr uint32_t bytes = small + (fed ? kSmallBytesFed : kSmallBytes) + 1024;
+    static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
+    static_assert(!prepx || kda || bytes <= 232448 / 2 - 1024, "kPrepX runs two CTAs per SM (DeltaNet / GDN)");
+    static_assert(small % 16 == 0 && t16 % 16 == 0 && kb % 1024 == 0 && akc % 1024 == 0 && ak % 1024 == 0 &&
+                      av % 1024 == 0,
+                  "buffer alignment (16 B vector accesses, 1024 B swizzled tiles)");
+};
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b)
 {
@@ -275,16 +309,9 @@ __device__ __forceinline__ void tile_bf16_to_f16(uint8_t *p, int bytes, int t, i
     }
 }
 
-// KIND kFused: the fused kernel, one CTA per (b, h, 64-wide dv slice) over the whole sequence.
-// KIND kSplit: the preparation kernel of the split variant, one CTA per (b, h, range of
-// `cpr` chunks) over the whole dv; its serial warps write the chunk operands to `ws`.
-// KIND kPair: the fused kernel with the two dv slices of a (b, h) (dv = 128) as a cluster of
-// two CTAs that share the state-independent preparation: CTA r prepares chunks r, r + 2, ...
-// and copies their [P Tu ; Tu], [-P Tw ; Tw] into the peer's shared memory, whose serial
-// warps issue MMA3 / MMA4 for those chunks themselves (DeltaNet / Gated DeltaNet).
-constexpr int kFused = 0, kSplit = 1, kPair = 2;
 template <int MODE, int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(KIND == kPrepX ? kPrepThreads : kThreads,
+                                  KIND == kPrepX && MODE != LDN_KDA && MODE != LDN_GDN2 ? 2 : 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ beta,
                 const float *__restrict__ gate, const float *S0, __nv_bfloat16 *__restrict__ out,
@@ -299,7 +326,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     constexpr bool kG2 = MODE == LDN_GDN2;                 // Gated DeltaNet-2: erase / write gates
     constexpr bool kKda = MODE == LDN_KDA || kG2;          // per-key-channel decay
     static_assert(!PAIR || !kKda, "the pair kernel takes DeltaNet / Gated DeltaNet");
-    using LY = Layout<MODE, SPLIT>;
+    constexpr bool PREPX = KIND == kPrepX, FED = KIND == kFed;
+    using LY = Layout<MODE, PAIR ? kFused : KIND>;
     constexpr int kStages = LY::stages;
     Small &S = *reinterpret_cast<Small *>(sm + LY::small);
     __half *A16 = reinterpret_cast<__half *>(sm + LY::a16);
@@ -312,13 +340,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nchunks_all = (T + kC - 1) / kC;
-    const int slices = SPLIT ? (nchunks_all + cpr - 1) / cpr : dv / kDVS;   // split: chunk ranges
+    constexpr bool RANGES = SPLIT || PREPX;   // one CTA per (b, h, range of cpr chunks)
+    const int slices = RANGES ? (nchunks_all + cpr - 1) / cpr : dv / kDVS;   // split / prep-X: chunk ranges
     const int unit = blockIdx.x / slices;
     const int b = unit / H, h = unit % H;
-    const int n0 = SPLIT ? 0 : (blockIdx.x % slices) * kDVS;
+    const int n0 = RANGES ? 0 : (blockIdx.x % slices) * kDVS;
     // chunk c of this CTA is chunk cb + c of the sequence
-    const int cb = SPLIT ? (blockIdx.x % slices) * cpr : 0;
-    const int nchunks = SPLIT ? min(cpr, nchunks_all - cb) : nchunks_all;
+    const int cb = RANGES ? (blockIdx.x % slices) * cpr : 0;
+    const int nchunks = RANGES ? min(cpr, nchunks_all - cb) : nchunks_all;
+    constexpr uint32_t kCols = PREPX ? 64u : kTmemCols;   // prep-X: D1 only
     const uint32_t quad = (uint32_t)(warp & 3);          // TMEM lane quadrant of this warp
     const uint32_t lane_base = (32u * quad) << 16;
     // pair: cluster rank = dv slice (blockIdx.x % 2); the peer is the other slice of (b, h)
@@ -326,12 +356,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&S.bar_load[i], 1);
-        mbar_init(&S.bar_pmma, 1);
+        mbar_init(&S.bar_pmma, FED ? 2 : 1);   // kFed: MMA3 and MMA4 come from two threads
         mbar_init(&S.bar_smma, 1);
+        mbar_init(&S.bar_s6, 1);
         mbar_init(&S.bar_ready[0], 1);
         mbar_init(&S.bar_ready[1], 1);
-        mbar_init(&S.bar_drain[0], 1);
-        mbar_init(&S.bar_drain[1], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&S.bar_drain[i], 1);
         mbar_init(&S.bar_rvfree[0], 1);
         mbar_init(&S.bar_rvfree[1], 1);
         mbar_init(&S.bar_kbfree[0], 1);
@@ -344,6 +374,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&S.bar_avakread[0], 2);
         mbar_init(&S.bar_avakread[1], 2);
         mbar_init(&S.bar_fin, 4);
+        mbar_init(&S.bar_x[0], 1);
+        mbar_init(&S.bar_x[1], 1);
         fence_mbar_init();
         S.fail = 0;
         S.sent = S.recvd = 0;
@@ -352,7 +384,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_prefetch_desc(&tm_v);
     }
     if (warp == 0) {
-        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_alloc(&S.tmem_base, kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -360,6 +392,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if constexpr (PAIR) cluster_sync();   // the peer's barriers exist before anything reaches them
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
+    // prep-X: the fed kernel that follows may start its CTAs as SMs free up (it waits for
+    // this grid before reading the workspace)
+    if constexpr (PREPX) griddep_launch_dependents();
     int pending[kMaxStages] = {-1, -1, -1};   // chunk last loaded into ring stage ls (serial thread 0)
 
     if (tid < kPrepThreads) {
@@ -439,8 +474,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             S.beta[gs][r0] = b0; S.beta[gs][r1] = b1;
             S.g[gs][r0] = g0; S.g[gs][r1] = g1;
             if (MODE == LDN_GDN) {
-                S.fr[gs][r0] = expf(g0 - m); S.fr[gs][r1] = expf(g1 - m);
-                S.fc[gs][r0] = expf(m - g0); S.fc[gs][r1] = expf(m - g1);
+                if constexpr (!FED) {   // MMA1's factors (kFed runs no MMA1 and leaves them out)
+                    S.fr[gs][r0] = expf(g0 - m); S.fr[gs][r1] = expf(g1 - m);
+                    S.fc[gs][r0] = expf(m - g0); S.fc[gs][r1] = expf(m - g1);
+                }
                 S.eg[gs][r0] = expf(g0); S.eg[gs][r1] = expf(g1);
                 S.egc[gs][r0] = expf(gc - g0); S.egc[gs][r1] = expf(gc - g1);
                 if (lane == 0) {
@@ -448,7 +485,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     S.exact[gs] = (-m > kMaxLogSpan || m - gc > kMaxLogSpan) ? 1 : 0;
                 }
             } else {
-                S.fr[gs][r0] = S.fr[gs][r1] = S.fc[gs][r0] = S.fc[gs][r1] = 1.f;
+                if constexpr (!FED) S.fr[gs][r0] = S.fr[gs][r1] = S.fc[gs][r0] = S.fc[gs][r1] = 1.f;
                 S.eg[gs][r0] = S.eg[gs][r1] = 1.f;
                 S.egc[gs][r0] = S.egc[gs][r1] = 1.f;
                 if (lane == 0) { S.gC[gs] = 1.f; S.exact[gs] = 0; }
@@ -498,6 +535,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // shared-memory phase touch 8 different 16-byte columns of one row (no bank
         // conflict under the 128-byte swizzle).  The log-gates are loaded (into G) a phase
         // ahead of the rest, so their latency is hidden.
+        // KDA side tile of chunk cc (prep-X keeps one: MMA1 is its only reader)
+        auto side = [&](int cc) -> uint8_t * { return KB + (PREPX ? 0 : (cc & 1) * kKBBytes); };
         const int kw = warp - 4, kch0 = 64 * (kw & 1) + 8 * (lane & 7), krh = kw >> 1, krgl = lane >> 3;
         const int kr0 = 32 * krh + 8 * krgl;
         auto kda_load_gates = [&](int cc, float (&G)[8][8]) {
@@ -578,14 +617,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
             build_wait_tiles(cc);
-            if (cc >= 2) {   // side tile cc & 1: MMA6 of chunk cc - 2 has read it
+            if (!PREPX && cc >= 2) {   // side tile cc & 1: MMA6 of chunk cc - 2 has read it
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait(&S.bar_kbfree[cc & 1], ((cc >> 1) - 1) & 1, kWaitNs);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) S.fail = 1;
             }
             if (!exact) {
                 uint8_t *qk = sm + LY::qk + ls * kQKBytes + (ch0 >> 6) * 16384;
-                uint8_t *kbt = KB + (cc & 1) * kKBBytes + (ch0 >> 6) * 8192;
+                uint8_t *kbt = side(cc) + (ch0 >> 6) * 8192;
                 const int col = ch0 & 63;
                 // Gated DeltaNet-2: the K rows carry b * K e^{G-m}; the erase gates of a row
                 // are loaded four rows ahead of their use (rows past T: K is zero there)
@@ -605,6 +644,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < kAhead; ++i) erase_load(i, eq[i]);
                 }
+                // kFed, KDA: the K^ rows also carry beta (MMA4's A operand is X = [P T ; T] unscaled)
+                float brow[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    brow[i] = FED && !kG2 && r0 + i < LL ? __ldg(beta + ((size_t)b * T + tb + r0 + i) * H + h) : 1.f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int r = r0 + i;
@@ -613,7 +657,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int j = 0; j < 8; ++j) {   // e^{G-m} and e^{m-G}, rounded to fp16 below
                         ep[j] = G[i][j];
                         en[j] = __fdividef(1.f, G[i][j]);
-                        eb[j] = ep[j];
+                        eb[j] = ep[j] * brow[i];
                     }
                     if constexpr (kG2) {
                         const float4 lo = eq[i % kAhead][0], hi = eq[i % kAhead][1];
@@ -654,13 +698,329 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_after();
             if (!kda_exact(cc)) {
                 const uint32_t qk = smem_u32(sm + LY::qk + ls * kQKBytes);
-                const uint32_t kbt = smem_u32(KB + (cc & 1) * kKBBytes);
+                const uint32_t kbt = smem_u32(side(cc));
                 for (int k = 0; k < kDK / 16; ++k)
                     umma_bf16(tbase + kColD1, kmajor_desc(qk, 128, k), kmajor_desc(kbt, 64, k), id_m128_n64_f16,
                               k > 0);
             }
             umma_commit(&S.bar_pmma);
         };
+        // KDA: MMA4 runs over [Q^ ; K^] with A = [[I, -P Tw], [0, Tw]]; its first 64
+        // columns, [I ; 0], are the same for every chunk
+        // (kFed: [-I ; 0], its MMA4 A operand being [[-I, P T], [0, T]])
+        auto init_akc = [&]() {
+            uint8_t *akc = sm + LY::akc;
+            const uint32_t one = FED ? 0xBC00u : 0x3C00u;   // fp16 -1 / +1
+            for (int e = pt; e < 128 * 8; e += kPrepThreads) {
+                const int rr = e >> 3, c8 = 8 * (e & 7);
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                if (rr < 64 && rr >= c8 && rr < c8 + 8) {
+                    const int j = rr - c8;   // the 1.0 sits in half j of this 16-byte group
+                    w[j >> 1] = (j & 1) ? one << 16 : one;
+                }
+                *reinterpret_cast<uint4 *>(akc + sw128_offset(rr, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        };
+        // prep-X: the [Q ; K] tiles of chunk cc into the single buffer (thread 0)
+        auto prepx_load = [&](int cc) {
+            pending[0] = cc;
+            mbar_arrive_expect_tx(&S.bar_load[0], 2 * 16384);
+            uint8_t *qk = sm + LY::qk;
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_4d(qk + kb * 16384, &tm_q, &S.bar_load[0], kb * 64, h, (cb + cc) * kC, b);
+                tma_load_4d(qk + kb * 16384 + 8192, &tm_k, &S.bar_load[0], kb * 64, h, (cb + cc) * kC, b);
+            }
+        };
+        // ---- kFed: the prep warps of the pre-solved variant.  Per chunk: X = [P T ; T] of
+        // the chunk (from the workspace, two chunks ahead into AV[c & 1]) stays as loaded and
+        // is the A operand of MMA3 and MMA4, whose B operands take the diagonal scales (beta V;
+        // Diag(beta e^{g}) K in AK[c & 1]; KDA: the build's K^ rows times beta); the k / v
+        // tiles become fp16; MMA3 / MMA4 give [P U' ; U'] and [P W ; W] (KDA: [-Q~ ; W]); the
+        // MMA5 operand [Q~ ; -W] is formed from MMA4's accumulator in tensor memory and its
+        // arrival on bar_ready is the serial warps' "chunk ready".  GDN / DeltaNet run one
+        // chunk ahead: the conversions and MMA3 / MMA4 of chunk c + 1 go in right after
+        // chunk c is handed over; KDA / GDN2 keep the chunk's steps in order (their look-ahead
+        // operand build waits on the side tile that MMA6 of the chunk before frees).
+        auto fed_prep_loop = [&]() {
+            const uint8_t *xin = ws + (size_t)unit * nchunks_all * kXBytes;
+            auto akb = [&](int sb) -> uint8_t * { return AK + sb * 32768; };   // AK[sb]; AV[sb] = AK[sb] + 16 KB
+            int xpend[2] = {-1, -1};   // issuer: chunk last loaded into AV[sb]
+            auto load_x = [&](int cc) {
+                uint64_t *bar = &S.bar_x[cc & 1];
+                xpend[cc & 1] = cc;
+                mbar_arrive_expect_tx(bar, kXBytes);
+                bulk_load(akb(cc & 1) + 16384, xin + (size_t)cc * kXBytes, kXBytes, bar);
+            };
+            // the tiles and X of chunk cc landed and (cc >= 2) the serial warps released RV / DK
+            // of chunk cc - 2, which MMA3 / MMA4 of chunk cc overwrite (one vote)
+            auto wait_inputs = [&](int cc) -> bool {
+                bool ok = true;
+                if (pt == 0)
+                    ok = mbar_wait(&S.bar_load[cc % kStages], (cc / kStages) & 1, kWaitNs) &&
+                         mbar_wait(&S.bar_x[cc & 1], (cc >> 1) & 1, kWaitNs) &&
+                         (cc < 2 || mbar_wait(&S.bar_rvfree[cc & 1], ((cc >> 1) - 1) & 1, kWaitNs));
+                return prep_vote(ok);
+            };
+            // the operand conversions of chunk c (F2) and MMA3 / MMA4 of chunk c (F3)
+            auto convert = [&](int c) {
+                const int s = c & 1, ls = c % kStages, gs = c % 3;
+                const int t0 = c * kC, L = min(kC, T - t0);
+                uint8_t *QK = sm + LY::qk + ls * kQKBytes;
+                uint8_t *Vt = sm + LY::v + ls * LY::vbytes;
+                uint8_t *AKs = akb(s);
+                const bool kexact = kKda && kda_exact(c);
+                // ---- F2: the B operands take the diagonal scales, X stays as loaded: V rows
+                //      times beta (Gated DeltaNet-2: times w), and (GDN / DeltaNet) the K tile to
+                //      fp16 in place for MMA6 plus K rows times beta e^{g} into AK[s] for MMA4
+                //      (KDA: the build scaled its K^ rows by beta).  One 16-byte group is 8
+                //      channels of one row, so one scale per group.
+                {
+                    // thread pt: K groups pt + 256 j (j < 4, GDN / DeltaNet) and V groups pt + 256 j
+                    // (j < 2); every load is issued before the first store
+                    constexpr int kNK = kKda ? 0 : 4;
+                    uint4 ku[kNK > 0 ? kNK : 1], vu[2];
+#pragma unroll
+                    for (int j = 0; j < kNK; ++j) {
+                        const int i = pt + kPrepThreads * j;
+                        ku[j] = *reinterpret_cast<const uint4 *>(QK + (i >> 9) * 16384 + 8192 + (i & 511) * 16);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) vu[j] = *reinterpret_cast<const uint4 *>(Vt + (pt + kPrepThreads * j) * 16);
+                    float wg[2][8];   // Gated DeltaNet-2: the write gate of the V group's 8 channels
+                    if constexpr (kG2) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int o = (pt + kPrepThreads * j) * 16, r = o >> 7;
+                            const int c8 = 8 * (((o >> 4) ^ r) & 7);
+                            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+                            if (r < L) {
+                                const float4 *src = reinterpret_cast<const float4 *>(
+                                    write + (((size_t)b * T + t0 + r) * H + h) * dv + n0 + c8);
+                                lo = __ldg(src);
+                                hi = __ldg(src + 1);
+                            }
+                            wg[j][0] = lo.x; wg[j][1] = lo.y; wg[j][2] = lo.z; wg[j][3] = lo.w;
+                            wg[j][4] = hi.x; wg[j][5] = hi.y; wg[j][6] = hi.z; wg[j][7] = hi.w;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < kNK; ++j) {
+                        const int i = pt + kPrepThreads * j, kb = i >> 9, o = (i & 511) * 16, r = o >> 7;
+                        const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ku[j]);
+                        const float sc = S.beta[gs][r] * S.eg[gs][r];
+                        uint32_t a[4], bsc[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(k2[e]);
+                            a[e] = pack_h2(f.x, f.y);
+                            bsc[e] = pack_h2(f.x * sc, f.y * sc);
+                        }
+                        *reinterpret_cast<uint4 *>(QK + kb * 16384 + 8192 + o) = make_uint4(a[0], a[1], a[2], a[3]);
+                        *reinterpret_cast<uint4 *>(AKs + kb * 8192 + o) = make_uint4(bsc[0], bsc[1], bsc[2], bsc[3]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {   // beta v (Gated DeltaNet-2: w * v)
+                        const int o = (pt + kPrepThreads * j) * 16, r = o >> 7;
+                        const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&vu[j]);
+                        const float sc = kG2 ? 1.f : S.beta[gs][r];
+                        uint32_t a[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(v2[e]);
+                            a[e] = kG2 ? pack_h2(f.x * wg[j][2 * e], f.y * wg[j][2 * e + 1]) : pack_h2(f.x * sc, f.y * sc);
+                        }
+                        *reinterpret_cast<uint4 *>(Vt + o) = make_uint4(a[0], a[1], a[2], a[3]);
+                    }
+                }
+                if (kexact && pt < kDK) {
+                    // KDA chunk whose decay span exceeds the fp16 factors: Q^ = Q e^{G}, K^ = K e^{G}
+                    // (GDN2: b * K e^{G}) in place and K~ = K e^{G_C - G} into the side tile, unfactored
+                    // (thread = key channel; the build left the tiles as loaded and set e^{m} = 1)
+                    const int ch = pt, col = ch & 63;
+                    uint8_t *blk = QK + (ch >> 6) * 16384;
+                    uint8_t *kbt = side(c) + (ch >> 6) * 8192;
+                    const float *gp = gate + (((size_t)b * T + t0) * H + h) * kDK + ch;
+                    float gC = 0.f;
+                    for (int r = 0; r < kC; ++r)
+                        if (r < L) gC += __ldg(gp + (size_t)r * H * kDK);
+                    float acc = 0.f;
+                    for (int r = 0; r < kC; ++r) {
+                        if (r < L) acc += __ldg(gp + (size_t)r * H * kDK);
+                        // (the erase gate b for Gated DeltaNet-2, beta for KDA)
+                        const float bvv = r >= L ? 0.f
+                                          : kG2 ? __ldg(erase + (((size_t)b * T + t0 + r) * H + h) * kDK + ch)
+                                                : __ldg(beta + ((size_t)b * T + t0 + r) * H + h);
+                        uint8_t *qp = blk + sw128_offset(r, col), *kp = blk + sw128_offset(64 + r, col);
+                        const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qp));
+                        const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kp));
+                        const float eg = expf(acc);
+                        *reinterpret_cast<__half *>(qp) = __float2half_rn(qv * eg);
+                        *reinterpret_cast<__half *>(kp) = __float2half_rn(bvv * kv * eg);
+                        *reinterpret_cast<__half *>(kbt + sw128_offset(r, col)) = __float2half_rn(kv * expf(gC - acc));
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+            };
+            auto issue_mma34 = [&](int c) {
+                const int s = c & 1, ls = c % kStages;
+                uint8_t *QK = sm + LY::qk + ls * kQKBytes;
+                uint8_t *Vt = sm + LY::v + ls * LY::vbytes;
+                uint8_t *AKs = akb(s), *AVs = akb(s) + 16384;
+                const uint32_t qk_s = smem_u32(QK), v_s = smem_u32(Vt);
+                // (two issuing threads: MMA3 from the issuer, MMA4 from thread kIssuerB; each
+                //  commit arrives once on bar_pmma, which counts two)
+                const uint32_t x_s = smem_u32(AVs), ak_s = smem_u32(AKs);
+                if (issuer) {
+                    tc_fence_after();
+                    for (int k = 0; k < kC / 16; ++k)   // X (beta V) = [P U' ; U']
+                        umma_bf16(tbase + col_rv<false>(s), kmajor_desc(x_s, 128, k), mnmajor_desc(v_s, 64, k),
+                                  id_m128_n64_mn, k > 0);
+                    umma_commit(&S.bar_pmma);
+                } else if (pt == kIssuerB) {
+                    tc_fence_after();
+                    if constexpr (kKda) {   // [[-I, P T], [0, T]] [Q^ ; beta K^] = [-Q~ ; W]
+                        const uint32_t akc_s = smem_u32(sm + LY::akc);
+                        for (int k = 0; k < kC / 16; ++k)
+                            umma_bf16(tbase + col_dk<false>(s), kmajor_desc(akc_s, 128, k),
+                                      mnmajor_desc(qk_s, 128, k), id_m128_n128_mn, k > 0);
+                        for (int k = 0; k < kC / 16; ++k)
+                            umma_bf16(tbase + col_dk<false>(s), kmajor_desc(x_s, 128, k),
+                                      mnmajor_desc(qk_s, 128, k + kC / 16), id_m128_n128_mn, 1);
+                    } else {                // X (Diag(beta e^{g}) K) = [P W ; W]
+                        for (int k = 0; k < kC / 16; ++k)
+                            umma_bf16(tbase + col_dk<false>(s), kmajor_desc(x_s, 128, k),
+                                      mnmajor_desc(ak_s, 64, k), id_m128_n128_mn, k > 0);
+                    }
+                    umma_commit(&S.bar_pmma);
+                }
+            };
+            // the gates (KDA: and operands) of chunk cc, formed while MMAs run
+            auto lookahead = [&](int cc) {
+                if (warp == kGateWarp) compute_gates(cc);
+                if (kKda && warp >= 4) {
+                    float Gn[8][8];
+                    kda_load_gates(cc, Gn);
+                    kda_build(cc, Gn);
+                }
+            };
+            // A5 = [Q~ ; -W] (fp16 pairs) into the first 64 columns of DK[c & 1] (F5): Q~ =
+            // Diag(e^{g}) Q - P W on the top rows (KDA: -(MMA4) times e^{m} per channel), -W on
+            // the bottom rows.  Warps w and w + 4 share a lane quadrant and take key channels
+            // 64 (w >> 2) ..; all read before either writes (the packed columns of the second
+            // half overlap the fp32 columns of the first).  Then chunk c is ready.
+            auto form_a5 = [&](int c) {
+                const int s = c & 1, ls = c % kStages, gs = c % 3;
+                uint8_t *QK = sm + LY::qk + ls * kQKBytes;
+                {
+                    const int kb = warp >> 2, row = 32 * quad + lane;
+                    const bool top = row < 64;
+                    const float er = top ? S.eg[gs][row] : 0.f;
+                    const uint32_t dk_col = tbase + lane_base + col_dk<false>(s);
+                    const uint8_t *qblk = QK + kb * 16384;
+                    uint32_t w[32];
+                    float va[64];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) tmem_ld16(dk_col + 64 * kb + 16 * q, va + 16 * q);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int cc = 32 * hf;
+                        float *v = va + cc;
+                        if constexpr (kKda) {
+                            const float4 *emq = reinterpret_cast<const float4 *>(&S.em[gs][64 * kb + cc]);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 e4 = emq[q];
+                                v[4 * q] *= e4.x; v[4 * q + 1] *= e4.y; v[4 * q + 2] *= e4.z; v[4 * q + 3] *= e4.w;
+                            }
+                        }
+                        // MMA4 gave [P W ; W] (GDN / DeltaNet) or [-Q~ ; W] Diag(e^{-m}) (KDA)
+                        if (!kKda && top) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                float qv[8];
+                                ld_row8_bf16(qblk, row, cc + j, qv);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) v[j + i] = er * qv[i] - v[j + i];
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = -v[i];
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[16 * hf + i] = pack_h2(v[2 * i], v[2 * i + 1]);
+                    }
+                    named_sync(kBarPrep, kPrepThreads);
+                    tmem_st16u(dk_col + 32 * kb, w);
+                    tmem_st16u(dk_col + 32 * kb + 16, w + 16);
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                named_sync(kBarPrep, kPrepThreads);
+                if (pt == 0) mbar_arrive(&S.bar_ready[s]);
+            };
+            if (issuer) {
+                griddep_wait();   // the prep-X grid wrote the workspace (its completion and memory)
+                load_x(0);
+                if (nchunks > 1) load_x(1);
+            }
+            if (warp == kGateWarp) {
+                prefetch_gates(0);
+                prefetch_g2_rows(0);
+                if (nchunks > 1) prefetch_g2_rows(1);
+                compute_gates(0);
+            }
+            if constexpr (kKda) {
+                init_akc();
+                if (warp >= 4) {
+                    float G0[8][8];
+                    kda_load_gates(0, G0);
+                    kda_build(0, G0);
+                }
+            }
+            named_sync(kBarPrep, kPrepThreads);
+            if constexpr (kKda) {
+                for (int c = 0; c < nchunks; ++c) {
+                    if (!wait_inputs(c)) break;
+                    convert(c);
+                    named_sync(kBarPrep, kPrepThreads);
+                    issue_mma34(c);
+                    if (c + 1 < nchunks) lookahead(c + 1);
+                    if (!wait_pmma()) break;
+                    form_a5(c);
+                    if (issuer && c + 2 < nchunks) load_x(c + 2);   // MMA3 / MMA4 have read AV[c & 1]
+                }
+            } else {
+                bool live = wait_inputs(0);
+                if (live) {
+                    convert(0);
+                    named_sync(kBarPrep, kPrepThreads);
+                    issue_mma34(0);
+                    if (nchunks > 1) lookahead(1);
+                }
+                for (int c = 0; live && c < nchunks; ++c) {
+                    if (!wait_pmma()) break;          // MMA3 / MMA4 of chunk c complete
+                    form_a5(c);
+                    if (issuer && c + 2 < nchunks) load_x(c + 2);   // they have read AV[c & 1]
+                    if (c + 1 < nchunks) {
+                        if (!wait_inputs(c + 1)) break;
+                        convert(c + 1);
+                        named_sync(kBarPrep, kPrepThreads);
+                        issue_mma34(c + 1);
+                        if (c + 2 < nchunks) lookahead(c + 2);   // slot (c + 2) % 3: chunk c - 1 released
+                    }
+                }
+            }
+            // After a failure: the X loads still in flight land before the CTA leaves
+            if (issuer && S.fail)
+                for (int sb = 0; sb < 2; ++sb)
+                    if (xpend[sb] >= 0) mbar_wait(&S.bar_x[sb], (xpend[sb] >> 1) & 1, kWaitNs / 4);
+        };
+        if constexpr (FED) {
+            fed_prep_loop();
+        } else {
+        if (PREPX && pt == 0) prepx_load(0);
         if (warp == kGateWarp) {
             prefetch_gates(0);
             prefetch_g2_rows(0);
@@ -674,20 +1034,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if ((j >> 4) > (r >> 4)) T16[r * kLd16 + j] = __float2half_rn(0.f);
         }
         zero_upper_avak();
-        if constexpr (kKda) {
-            // KDA: MMA4 runs over [Q^ ; K^] with A = [[I, -P Tw], [0, Tw]]; its first
-            // 64 columns, [I ; 0], are the same for every chunk
-            uint8_t *akc = sm + LY::akc;
-            for (int e = pt; e < 128 * 8; e += kPrepThreads) {
-                const int rr = e >> 3, c8 = 8 * (e & 7);
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
-                if (rr < 64 && rr >= c8 && rr < c8 + 8) {
-                    const int j = rr - c8;   // the 1.0 sits in half j of this 16-byte group
-                    w[j >> 1] = (j & 1) ? 0x3C000000u : 0x00003C00u;
-                }
-                *reinterpret_cast<uint4 *>(akc + sw128_offset(rr, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
+        if constexpr (kKda && !PREPX) init_akc();
         named_sync(kBarPrep, kPrepThreads);
 
         // The chunks this CTA prepares: every chunk, or (pair) every other one from its
@@ -710,13 +1057,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (run) {
             // ---- P1: MMA1 of chunk c (issued while chunk c - 1 was prepared) complete
             if (!wait_pmma()) break;
+            // prep-X: MMA1 has read the tiles -- the next chunk's load into the single buffer
+            // (after the entry-wise A / P of a KDA chunk, which read the tiles too)
+            if (PREPX && pt == 0 && !kexact && c + 1 < nchunks) prepx_load(c + 1);
 
             if constexpr (kKda) {
                 if (kexact) {
                     // ---- P4 (KDA, decay span beyond the fp16 factors): A and P entry by entry.
                     // AV / AK, free once MMA3 / MMA4 of chunk c - 1 completed, hold the fp32
                     // per-channel log-decay prefix G [64][128] meanwhile.
-                    if (!prep_vote(pt == 0 && c >= 1
+                    // (prep-X: the store of chunk c - 1's X has read AV)
+                    if (PREPX && pt == 0) bulk_wait_read_all();
+                    if (!prep_vote(!PREPX && pt == 0 && c >= 1
                                        ? mbar_wait(&S.bar_ready[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs) &&
                                              (!SPLIT || mbar_wait(&S.bar_stgfree[(c - 1) & 1], ((c - 1) >> 1) & 1,
                                                                   kWaitNs))
@@ -769,7 +1121,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                                                              j0 + i + 1 <= jmax ? acc[i + 1] * sc : 0.f);
                     }
                     named_sync(kBarPrep, kPrepThreads);
-                    {   // Q^ = Q e^{G}, K^ = K e^{G} (GDN2: b * K e^{G}) in place; K~ = K e^{G_C - G}
+                    if constexpr (!PREPX) {   // (prep-X runs no MMA4 / MMA6)
+                        // Q^ = Q e^{G}, K^ = K e^{G} (GDN2: b * K e^{G}) in place; K~ = K e^{G_C - G}
                         // into the side tile
                         uint8_t *kbt = KB + (c & 1) * kKBBytes;
                         const int tbe = (cb + c) * kC, LLe = min(kC, T - tbe);
@@ -842,6 +1195,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             tc_fence_before();   // D1 has been read: the next MMA1 may overwrite it
             named_sync(kBarPrep, kPrepThreads);
+            if (PREPX && pt == 0 && kexact && c + 1 < nchunks) prepx_load(c + 1);
 
             // ---- P5: T = (I + A)^{-1}: 16x16 diagonal blocks, then block substitution
             if (pt < 64) {
@@ -860,7 +1214,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     T16[(o + r) * kLd16 + o + col] = __float2half_rn(x[r]);
                 }
             }
-            else {   // the other prep threads convert the k and v tiles to fp16 meanwhile
+            else if constexpr (!PREPX) {   // the other prep threads convert the k and v tiles to fp16 meanwhile
                 if constexpr (!kKda) {   // (KDA tiles stay as built; see MMA4 / MMA6)
                     tile_bf16_to_f16(QK + 8192, 8192, pt - 64, kPrepThreads - 64);           // K, block 0
                     tile_bf16_to_f16(QK + 16384 + 8192, 8192, pt - 64, kPrepThreads - 64);   // K, block 1
@@ -969,7 +1323,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // and before slot (c + 1) % 3 = (c - 2) % 3 is rewritten).
                     // (Split: DK has one buffer, so its chunk c - 1 must have been read too.)
                     bool ok = true;
-                    if (c >= 2 && lane == 0) ok = mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs);
+                    if (!PREPX && c >= 2 && lane == 0) ok = mbar_wait(&S.bar_rvfree[s], ((c >> 1) - 1) & 1, kWaitNs);
                     if (SPLIT && c >= 1 && lane == 0)
                         ok = ok && mbar_wait(&S.bar_dkfree[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -989,7 +1343,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // pair: in both CTAs, since this CTA's AV / AK go to the peer's as well).
             // A timeout only marks the CTA failed; the vote at the next chunk's start takes
             // every prep thread out of the loop together.
-            if (pt == 0 && run && c >= 1) {
+            if (PREPX && pt == 0 && run) bulk_wait_read_all();   // the store of chunk c - 1's X has read AV
+            if (!PREPX && pt == 0 && run && c >= 1) {
                 bool ok;
                 if constexpr (PAIR)
                     ok = mbar_wait(&S.bar_avakread[(c - 1) & 1], ((c - 1) >> 1) & 1, kWaitNs);
@@ -1020,13 +1375,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const float4 bb = bq[2 * h8 + q], ee = eq[2 * h8 + q];
                         const float2 ta = __half22float2(t2[2 * q]), tb = __half22float2(t2[2 * q + 1]);
                         const int i = 8 * h8 + 4 * q;
-                        vu[i] = ta.x * bb.x; vu[i + 1] = ta.y * bb.y; vu[i + 2] = tb.x * bb.z; vu[i + 3] = tb.y * bb.w;
-                        vw[i] = vu[i] * ee.x; vw[i + 1] = vu[i + 1] * ee.y;
-                        vw[i + 2] = vu[i + 2] * ee.z; vw[i + 3] = vu[i + 3] * ee.w;
+                        if constexpr (PREPX) {   // X: T itself
+                            vu[i] = ta.x; vu[i + 1] = ta.y; vu[i + 2] = tb.x; vu[i + 3] = tb.y;
+                        } else {
+                            vu[i] = ta.x * bb.x; vu[i + 1] = ta.y * bb.y; vu[i + 2] = tb.x * bb.z; vu[i + 3] = tb.y * bb.w;
+                            vw[i] = vu[i] * ee.x; vw[i + 1] = vu[i + 1] * ee.y;
+                            vw[i + 2] = vu[i + 2] * ee.z; vw[i + 3] = vu[i + 3] * ee.w;
+                        }
                     }
                 }
                 st_row16(AV, 64 + j, n0c, vu);
-                st_row16(AK, 64 + j, n0c, vw);
+                if constexpr (!PREPX) st_row16(AK, 64 + j, n0c, vw);
             }
             if (warp < 7) {
                 // (R, i) output blocks per warp, balanced by k-block count (20 in all).
@@ -1062,11 +1421,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int hh = 0; hh < 2; ++hh) {
                             const int rr = 16 * R + g + 8 * hh, cc = 16 * i + 8 * nt + 2 * t4;
                             const float p0 = acc[nt][2 * hh], p1 = acc[nt][2 * hh + 1];
-                            const float2 bb = *reinterpret_cast<const float2 *>(&S.beta[gs][cc]);
-                            const float2 ee = *reinterpret_cast<const float2 *>(&S.eg[gs][cc]);
-                            const float u0 = p0 * bb.x, u1 = p1 * bb.y;
-                            *reinterpret_cast<uint32_t *>(AV + sw128_offset(rr, cc)) = pack_h2(u0, u1);
-                            *reinterpret_cast<uint32_t *>(AK + sw128_offset(rr, cc)) = pack_h2(-u0 * ee.x, -u1 * ee.y);
+                            if constexpr (PREPX) {   // X: P T itself
+                                *reinterpret_cast<uint32_t *>(AV + sw128_offset(rr, cc)) = pack_h2(p0, p1);
+                            } else {
+                                const float2 bb = *reinterpret_cast<const float2 *>(&S.beta[gs][cc]);
+                                const float2 ee = *reinterpret_cast<const float2 *>(&S.eg[gs][cc]);
+                                const float u0 = p0 * bb.x, u1 = p1 * bb.y;
+                                *reinterpret_cast<uint32_t *>(AV + sw128_offset(rr, cc)) = pack_h2(u0, u1);
+                                *reinterpret_cast<uint32_t *>(AK + sw128_offset(rr, cc)) = pack_h2(-u0 * ee.x, -u1 * ee.y);
+                            }
                         }
                 }
             }
@@ -1077,7 +1440,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // ---- P9: MMA3 [P Tu ; Tu] V -> RV[s], MMA4 [-P Tw ; Tw] K -> DK[s] (the
             //      gate warp saw the serial warps release both for chunk c - 2); their
             //      commit is the serial warps' "chunk ready".
-            if (issuer) {
+            if constexpr (PREPX) {   // X of chunk c to the workspace (its shared-memory reads are
+                if (pt == 0) {        // waited for before AV is written again)
+                    bulk_store(ws + ((size_t)unit * nchunks_all + cb + c) * kXBytes, AV, kXBytes);
+                    bulk_commit();
+                }
+            } else if (issuer) {
                 tc_fence_after();
                 const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(AK);
                 for (int j = 0; j < (SPLIT ? dv / kDVS : 1); ++j)   // split: all of dv, 64 columns at a time
@@ -1123,6 +1491,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
         }
+        if (PREPX && pt == 0) bulk_wait_all();   // the workspace is complete before the CTA leaves
+        }   // !FED
     } else {
         // ============================== SERIAL ==============================
         const int st = tid - kPrepThreads;   // = TMEM lane = state row
@@ -1374,14 +1744,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float gC = S.gC[gs];
             const bool top = st < 64;
             const float egc = top ? 0.f : S.egc[gs][st - 64];
+            // gate data of this chunk for S6, read now: the slot is released (rvfree) before S6
+            const float gCr = kKda ? S.egC[gs][st] : gC;   // KDA: decay of key channel st
+            // KDA: the side tile holds K e^{m-G} = K~ Diag(e^{m-G_C}) per channel, row st of D6
+            const float d6s = kKda ? S.egcm[gs][st] : 1.f;
 
             // ---- S2: A5 = [Q~ ; -W] (row st): Q~ = Diag(e^{g}) Q - P W on the top rows
             //      (Q read from the bf16 tile as loaded; KDA: MMA4 formed Q~), -W on the
             //      bottom rows, packed as
             //      fp16 pairs into the first 64 columns of DK[s] -- the MMA5 A operand,
             //      read from tensor memory.  Each thread rewrites only columns of its own
-            //      lane that it has already read.
-            {
+            //      lane that it has already read.  (kFed: the prep warps formed it.)
+            if constexpr (!FED) {
                 const float er = top ? S.eg[gs][st] : 0.f;
                 const uint32_t dk_col = tbase + lane_base + col_dk<SPLIT>(s);
 #pragma unroll 1   // (code size: both roles' loops must stay in the instruction cache)
@@ -1422,10 +1796,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tmem_st16u(dk_col + 32 * kb + cc / 2, w);
                     }
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                named_sync(kBarSerial, kSerialThreads);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            named_sync(kBarSerial, kSerialThreads);
 
             // ---- S3: MMA5: RV[s] += [Q~ ; -W] H0  -> O (rows 0..63), U (rows 64..127)
             if (st == 0) {
@@ -1460,32 +1834,50 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int n = 0; n < kDVS; n += 16) st_row16(UB, r, n, v + n);
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(kBarSerial, kSerialThreads);
-            if (st == 0) {
-                mbar_arrive(&S.bar_rvfree[s]);
-                // ---- S5: MMA6: K^T U~ -> D6
+            // ---- S5: MMA6: K^T U~ -> D6.  A = K^T (GDN, DeltaNet: U~ carries the decay) or
+            //      K~^T (KDA, side tile).  kFed: only the U rows meet before it (one of them
+            //      issues it), so the O rows' output stores overlap it.
+            auto issue_mma6 = [&]() {
                 tc_fence_after();
                 const uint32_t ub_s = smem_u32(UB);
-                // A = K^T (GDN, DeltaNet: U~ carries the decay) or K~^T (KDA, side tile)
                 const uint32_t ka_s = kKda ? smem_u32(KB + (c & 1) * kKBBytes) : k_s;
                 for (int k = 0; k < kC / 16; ++k)
                     umma_bf16(tbase + kColD6, mnmajor_desc(ka_s, kKda ? 64 : 128, k), mnmajor_desc(ub_s, 64, k),
                               id_m128_n64_amn, k > 0);
-                umma_commit(&S.bar_smma);
+                umma_commit(FED ? &S.bar_s6 : &S.bar_smma);
+            };
+            if constexpr (FED) {
+                if (!top) {
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    named_sync(kBarU, kSerialThreads - 64);
+                    if (st == 64) issue_mma6();
+                }
+                tc_fence_before();
+                named_sync(kBarSerial, kSerialThreads);   // every row has read RV[s]
+                if (st == 0) mbar_arrive(&S.bar_rvfree[s]);
+            } else {
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_sync(kBarSerial, kSerialThreads);
+                if (st == 0) {
+                    mbar_arrive(&S.bar_rvfree[s]);
+                    issue_mma6();
+                }
             }
             // pair: the next chunk is the peer's -- its MMA3 / MMA4 go in while MMA6 runs
             if (PAIR && c + 1 < nchunks && ((c + 1) & 1) != prank) pair_service(c + 1);
-            if (!wait_smma()) break;
+            if constexpr (FED) {
+                if (!mbar_wait(&S.bar_s6, (uint32_t)(c & 1), kWaitNs)) S.fail = 1;
+                tc_fence_after();
+            } else {
+                if (!wait_smma()) break;
+            }
             if (kKda && st == 0) mbar_arrive(&S.bar_kbfree[c & 1]);
             // the tiles of chunk c are no longer read by anyone: fetch chunk c + stages into them
             if (!kKda && st == 0 && c + kStages < nchunks) issue_load(c + kStages);
 
             // ---- S6: H1 = e^{g_C} H0 + K^T U~ (row st), fp16 copy for the next MMA5
-            const float gCr = kKda ? S.egC[gs][st] : gC;   // KDA: decay of key channel st
-            // KDA: the side tile holds K e^{m-G} = K~ Diag(e^{m-G_C}) per channel, row st of D6
-            const float d6s = kKda ? S.egcm[gs][st] : 1.f;
             {
                 float v[kDVS];
 #pragma unroll
@@ -1520,12 +1912,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // before shared memory and TMEM are released: a commit tracks every
         // earlier MMA of the thread that issues it.
         if (tid == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
-        if (tid == kIssuer || tid == kPrepThreads) {
-            const int i = tid == kIssuer ? 0 : 1;
+        if (tid == kIssuer || tid == kPrepThreads || (FED && (tid == kIssuerB || tid == kIssuer6))) {
+            const int i = tid == kIssuer ? 0 : tid == kPrepThreads ? 1 : tid == kIssuerB ? 2 : 3;
             umma_commit(&S.bar_drain[i]);
             mbar_wait(&S.bar_drain[i], 0, kWaitNs / 4);
         }
-        if (tid == kPrepThreads)
+        if (tid == (PREPX ? 0 : kPrepThreads))   // the thread that issued the tile loads
             for (int ls = 0; ls < kStages; ++ls)
                 if (pending[ls] >= 0) mbar_wait(&S.bar_load[ls], (pending[ls] / kStages) & 1, kWaitNs / 4);
     }
@@ -1550,7 +1942,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         cluster_sync();   // the peer has read this CTA's counter
     }
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+    if (warp == 0) tmem_dealloc(tbase, kCols);
 }
 
 }  // namespace
@@ -1581,7 +1973,8 @@ int sm_count()
 template <int KIND>
 cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 {
-    constexpr bool SPLIT = KIND == kSplit, PAIR = KIND == kPair;
+    constexpr bool SPLIT = KIND == kSplit, PAIR = KIND == kPair, PREPX = KIND == kPrepX;
+    constexpr int LK = PAIR ? kFused : KIND;   // shared-memory plan
     CUtensorMap tq, tk, tv;
     if (!make_tmap_bf16_4d(&tq, a.q, kDK, a.H, a.T, a.B, 64, kC) ||
         !make_tmap_bf16_4d(&tk, a.k, kDK, a.H, a.T, a.B, 64, kC) ||
@@ -1589,19 +1982,39 @@ cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
         return cudaErrorInvalidValue;
     int cpr = 0;
     long long grid = (long long)a.B * a.H * (a.dv / kDVS);
-    if (SPLIT) {
-        // chunk ranges per sequence so that the CTAs fill the SMs once (one CTA per SM)
+    if (SPLIT || PREPX) {
+        // chunk ranges per sequence so that the CTAs fill the SMs once (split: one CTA per
+        // SM; prep-X: two for DeltaNet / Gated DeltaNet, whose plan takes half an SM)
         const int nchunks = (a.T + kC - 1) / kC;
         const long long heads = (long long)a.B * a.H;
-        const int sms = sm_count();
-        int nranges = (int)max(1LL, min((long long)nchunks, sms > 0 ? sms / heads : 1LL));
-        cpr = (nchunks + nranges - 1) / nranges;
+        const bool kda = a.mode == LDN_KDA || a.mode == LDN_GDN2;
+        const long long slots = (long long)sm_count() * (PREPX && !kda ? 2 : 1);
+        long long nranges = max(1LL, min((long long)nchunks, slots > 0 ? slots / heads : 1LL));
+        if (PREPX && slots > 0) {   // ranges of about the same length on every slot
+            const long long per = (heads * nchunks + slots - 1) / slots;
+            nranges = min((long long)nchunks, max(1LL, (nchunks + per - 1) / per));
+        }
+        cpr = (int)((nchunks + nranges - 1) / nranges);
         nranges = (nchunks + cpr - 1) / cpr;
         grid = heads * nranges;
     }
     auto go = [&](auto kern, uint32_t smem) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        if (KIND == kFed) {   // may start while the prep-X grid before it drains (see griddep_wait)
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)grid);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
+                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase, a.write);
+        }
         if (PAIR) {   // clusters of the two dv slices of a (b, h): consecutive blocks
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)grid);
@@ -1618,17 +2031,17 @@ cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
             return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
                                       a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase, a.write);
         }
-        kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
-                                                     a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase,
-                                                     a.write);
+        kern<<<(unsigned)grid, PREPX ? kPrepThreads : kThreads, smem, st>>>(
+            tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.dv, a.status, ws, cpr,
+            a.erase, a.write);
         return cudaGetLastError();
     };
-    if (a.mode == LDN_GDN) return go(chunk_tc_kernel<LDN_GDN, KIND>, Layout<LDN_GDN, SPLIT>::bytes);
+    if (a.mode == LDN_GDN) return go(chunk_tc_kernel<LDN_GDN, KIND>, Layout<LDN_GDN, LK>::bytes);
     if constexpr (!PAIR) {
-        if (a.mode == LDN_KDA) return go(chunk_tc_kernel<LDN_KDA, KIND>, Layout<LDN_KDA, SPLIT>::bytes);
-        if (a.mode == LDN_GDN2) return go(chunk_tc_kernel<LDN_GDN2, KIND>, Layout<LDN_GDN2, SPLIT>::bytes);
+        if (a.mode == LDN_KDA) return go(chunk_tc_kernel<LDN_KDA, KIND>, Layout<LDN_KDA, LK>::bytes);
+        if (a.mode == LDN_GDN2) return go(chunk_tc_kernel<LDN_GDN2, KIND>, Layout<LDN_GDN2, LK>::bytes);
     }
-    return go(chunk_tc_kernel<LDN_DELTANET, KIND>, Layout<LDN_DELTANET, SPLIT>::bytes);
+    return go(chunk_tc_kernel<LDN_DELTANET, KIND>, Layout<LDN_DELTANET, LK>::bytes);
 }
 }  // namespace
 
@@ -1642,27 +2055,33 @@ bool chunk_pair_supported(const ChunkArgs &a)
 cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t st) { return launch_tc<kPair>(a, nullptr, st); }
 
 // Which tensor-core variant is expected to be fastest: a cost model in waves of
-// CTAs (one CTA per SM) x chunks per CTA x measured time per chunk on GB300 --
-// fused 4.0 us (GDN / DeltaNet) or 7.9 us (KDA); pair 5.0 us (measured: each
-// CTA's preparation waits for tiles that a third ring stage frees only late, and
-// runs slower beside the busier serial warps); split preparation 5.4 /
-// 10.8 us and state step 1.6 us -- plus a fixed 10 us (one launch) or 20 us (two
-// launches and the preparation pipeline's fill).  The fused and pair kernels win
-// when their CTAs fill the SMs once; the split variant when they do not (few
-// sequences) or need several waves.
-int chunk_tc_pick(const ChunkArgs &a, bool split_ok)
+// CTAs x chunks per CTA x measured time per chunk on GB300 --
+//   fused: 10 us + waves x chunks x 4.0 us (GDN / DeltaNet) or 7.9 us (KDA);
+//   pair: 10 us + waves x chunks x 5.0 us (measured: each CTA's preparation waits for
+//     tiles that a third ring stage frees only late, and runs slower beside the busier
+//     serial warps);
+//   split: 20 us + preparation waves x chunks per range x 5.4 / 10.8 us + state waves x
+//     chunks x 1.6 us;
+//   pre-solved: 22 us + prep-X chunks per slot x 3.2 / 6.6 us (two / one CTAs per SM) +
+//     waves x chunks x 2.2 / 6.3 us.
+// The fused and pair kernels win when their CTAs fill the SMs once and the sequences are
+// short; the pre-solved variant when many sequences fill the SMs (GDN / DeltaNet); the
+// split variant when few sequences are long, or for KDA.
+int chunk_tc_pick(const ChunkArgs &a, bool split_ok, bool presolved_ok)
 {
     const bool pair_ok = chunk_pair_supported(a);
     const int sms = sm_count();
     if (sms <= 0) return pair_ok ? LDN_VARIANT_PAIR : LDN_VARIANT_TENSOR;
     const bool kda = a.mode == LDN_KDA || a.mode == LDN_GDN2;
     const double t_fused = kda ? 7.9 : 4.0, t_pair = 5.0, t_prep = kda ? 10.8 : 5.4, t_state = 1.6;
+    const double t_px = kda ? 6.6 : 3.2, t_fed = kda ? 6.3 : 2.2;
     const long long heads = (long long)a.B * a.H, nchunks = (a.T + kC - 1) / kC;
     const long long slices = heads * (a.dv / kDVS);
     const long long waves_f = (slices + sms - 1) / sms;
     const long long nranges = std::max(1LL, std::min(nchunks, sms / heads));
     const long long cpr = (nchunks + nranges - 1) / nranges;
     const long long waves_p = (heads * ((nchunks + cpr - 1) / cpr) + sms - 1) / sms;
+    const long long px_slots = (long long)sms * (kda ? 1 : 2);
     int best = LDN_VARIANT_TENSOR;
     double cost = 10.0 + (double)waves_f * nchunks * t_fused;
     if (pair_ok) {
@@ -1673,7 +2092,24 @@ int chunk_tc_pick(const ChunkArgs &a, bool split_ok)
         const double split = 20.0 + (double)waves_p * cpr * t_prep + (double)waves_f * nchunks * t_state;
         if (split < cost) { cost = split; best = LDN_VARIANT_SPLIT; }
     }
+    if (presolved_ok) {
+        const double pre = 22.0 + (double)((heads * nchunks + px_slots - 1) / px_slots) * t_px +
+                           (double)waves_f * nchunks * t_fed;
+        if (pre < cost) { cost = pre; best = LDN_VARIANT_PRESOLVED; }
+    }
     return best;
+}
+
+size_t presolved_workspace_bytes(int B, int T, int H)
+{
+    return (size_t)B * H * (size_t)((T + kC - 1) / kC) * kXBytes;
+}
+
+cudaError_t launch_chunk_presolved(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
+{
+    cudaError_t e = launch_tc<kPrepX>(a, ws, st);
+    if (e != cudaSuccess) return e;
+    return launch_tc<kFed>(a, ws, st);
 }
 
 cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)

@@ -68,7 +68,12 @@ bool chunk_tc_supported(const ChunkArgs &a);
 // Split variant: preparation kernel (chunk_tc.cu) then state kernel (chunk_state.cu).
 cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
 cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream_t stream);
-int chunk_tc_pick(const ChunkArgs &a, bool split_ok);   // fastest tensor-core LDN_VARIANT_* by a cost model
+// Pre-solved variant (chunk_tc.cu): X = [P T ; T] of every chunk into the workspace
+// (presolved_workspace_bytes), then the fused kernel reading it.
+size_t presolved_workspace_bytes(int B, int T, int H);
+cudaError_t launch_chunk_presolved(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
+// fastest tensor-core LDN_VARIANT_* by a cost model, given which workspace variants can run
+int chunk_tc_pick(const ChunkArgs &a, bool split_ok, bool presolved_ok);
 bool chunk_pair_supported(const ChunkArgs &a);    // the cluster-pair kernel takes these arguments
 cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);

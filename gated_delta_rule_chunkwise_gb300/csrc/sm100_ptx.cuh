@@ -241,6 +241,16 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr)
     return v;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Let the grid launched after this one on the stream (with the programmatic
+// stream serialization attribute) start its CTAs now; they wait for this grid's
+// completion and memory with griddep_wait() before they read what it writes.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 // Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
@@ -263,6 +273,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 1-D bulk copy global -> shared (both addresses 16-byte aligned, size a
+// multiple of 16), completing `bytes` of transactions on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 // 1-D bulk copy shared -> global as a bulk async-group of the issuing thread

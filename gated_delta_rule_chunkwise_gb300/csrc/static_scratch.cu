@@ -12,8 +12,10 @@
 // The first call on a device resolves the address and creates the event
 // below; it must not be made while its stream is being captured into a CUDA
 // graph (it returns LDN_ERR_UNSUPPORTED and enqueues nothing).  The stream
-// must belong to the current device (else LDN_ERR_INVALID_ARG): the lock, the
-// array's address and the event are per device.
+// must belong to the current device: the lock, the array's address and the
+// event are per device.  Outside a capture a stream of another device returns
+// LDN_ERR_INVALID_ARG (a capturing stream is not asked for its device: the
+// query would invalidate the capture).
 //
 // All calls of a process on one device share the array.  acquire() takes a
 // per-device host lock and makes the caller's stream wait for the event that
@@ -51,9 +53,9 @@ int static_scratch_acquire(cudaStream_t s, uint8_t **ptr, size_t *bytes, int *de
     int dev = 0, sdev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LDN_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return LDN_ERR_UNSUPPORTED;
-    if (cudaStreamGetDevice(s, &sdev) != cudaSuccess) return LDN_ERR_INVALID_ARG;
-    if (sdev != dev) return LDN_ERR_INVALID_ARG;
     const bool cap = capturing(s);
+    // (querying a capturing stream's device invalidates the capture: checked outside captures)
+    if (!cap && (cudaStreamGetDevice(s, &sdev) != cudaSuccess || sdev != dev)) return LDN_ERR_INVALID_ARG;
     g_lock[dev].lock();
     if (!g_addr[dev]) {
         if (cap) {   // set-up (symbol resolution, event creation) stays out of captures

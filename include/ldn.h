@@ -85,7 +85,8 @@ typedef enum {
     LDN_VARIANT_SIMT = 1,   /* fp32 CUDA-core kernel, either dtype                 */
     LDN_VARIANT_TENSOR = 2, /* tcgen05 / TMEM kernel, bf16 only                     */
     LDN_VARIANT_SPLIT = 3,  /* tcgen05, two kernels through a workspace (see below) */
-    LDN_VARIANT_PAIR = 4    /* tcgen05, two CTAs per (b, h) sharing the preparation */
+    LDN_VARIANT_PAIR = 4,   /* tcgen05, two CTAs per (b, h) sharing the preparation */
+    LDN_VARIANT_PRESOLVED = 5 /* tcgen05, every chunk's UT/WY solve first, through a workspace */
 } ldn_variant;
 
 /*
@@ -209,7 +210,8 @@ int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int 
  * The first call on a device resolves the array's address and creates an
  * event; it must not be made while `stream` is being captured into a CUDA
  * graph: such a call returns LDN_ERR_UNSUPPORTED and enqueues nothing.
- * `stream` must belong to the current device (else LDN_ERR_INVALID_ARG).
+ * `stream` must belong to the current device; outside a stream capture a
+ * stream of another device returns LDN_ERR_INVALID_ARG.
  *
  * Arguments, layouts, alignment and error behaviour are those of
  * ldn_chunk_fwd_variant, with LDN_VARIANT_SPLIT also accepted.

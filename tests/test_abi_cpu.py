@@ -261,7 +261,27 @@ def test_noalloc_split_outside_the_tensor_kernels_is_unsupported(lib):
     assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=64) == ldn.LDN_ERR_UNSUPPORTED   # dk = 64
     assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=128, dtype=0) == ldn.LDN_ERR_UNSUPPORTED   # fp32
     assert _noalloc(variant=ldn.LDN_VARIANT_SPLIT, dk=128, mode=2, gate=FAKE + 4) == ldn.LDN_ERR_UNSUPPORTED
-    assert _noalloc(variant=5) == ldn.LDN_ERR_INVALID_ARG
+    assert _noalloc(variant=ldn.LDN_VARIANT_PRESOLVED, dk=64) == ldn.LDN_ERR_UNSUPPORTED
+    assert _noalloc(variant=ldn.LDN_VARIANT_PRESOLVED, dk=128, dtype=0) == ldn.LDN_ERR_UNSUPPORTED
+    assert _noalloc(variant=6) == ldn.LDN_ERR_INVALID_ARG
+
+
+def test_presolved_variant_needs_a_workspace_and_the_tensor_kernels(lib):
+    """The pre-solved variant runs through a workspace of 16 KiB per (b, h, chunk): without
+    one (ldn_chunk_fwd_variant) or with too small a one it is refused before any CUDA call;
+    outside the tensor-core sizes it is unsupported."""
+    assert _chunk(variant=ldn.LDN_VARIANT_PRESOLVED, dk=128, dv=128) == ldn.LDN_ERR_INVALID_ARG   # no workspace
+    big = 1 << 30
+    for dk, dv, dtype in ((64, 64, 1), (128, 128, 0)):   # not the tensor-core sizes / fp32
+        assert ldn.ldn_chunk_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 64, 1, dk, dv, 64, 1, dtype,
+                                    ldn.LDN_VARIANT_PRESOLVED, FAKE, big, None) == ldn.LDN_ERR_UNSUPPORTED
+    B, T, H = 2, 200, 3
+    need = B * H * ((T + 63) // 64) * 16384
+    assert ldn.ldn_chunk_fwd_workspace_size(B, T, H, 128, 128, 64, 1, 1) >= need   # enough for either variant
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, B, T, H, 128, 128, 64, 1, 1,
+            ldn.LDN_VARIANT_PRESOLVED)
+    assert ldn.ldn_chunk_fwd_ws(*args, FAKE, need - 256, None) == ldn.LDN_ERR_INVALID_ARG      # too small
+    assert ldn.ldn_chunk_fwd_ws(*args, FAKE + 16, need, None) == ldn.LDN_ERR_INVALID_ARG       # not 256-aligned
 
 
 def test_pair_variant_outside_its_sizes_is_unsupported(lib):
@@ -270,7 +290,7 @@ def test_pair_variant_outside_its_sizes_is_unsupported(lib):
     assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=128, dv=64) == ldn.LDN_ERR_UNSUPPORTED            # one slice
     assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=64, dv=128) == ldn.LDN_ERR_UNSUPPORTED
     assert _chunk(variant=ldn.LDN_VARIANT_PAIR, dk=128, dv=128, dtype=0) == ldn.LDN_ERR_UNSUPPORTED  # fp32
-    assert _chunk(variant=5) == ldn.LDN_ERR_INVALID_ARG
+    assert _chunk(variant=6) == ldn.LDN_ERR_INVALID_ARG
 
 
 def _prologue(**kw):

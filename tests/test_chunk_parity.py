@@ -23,11 +23,19 @@ def _built():
     ldn.load()
 
 
-def run_gpu(w, variant=ldn.LDN_VARIANT_AUTO, S0=True, want_state=True):
+def run_gpu(w, variant=ldn.LDN_VARIANT_AUTO, S0=True, want_state=True, workspace=False):
+    """workspace=True: through ldn_chunk_fwd_ws with a workspace of
+    ldn_chunk_fwd_workspace_size bytes, as the benchmark calls it (AUTO may then pick a
+    workspace variant)."""
     import torch
     t = w.torch_inputs("cuda")
+    ws = None
+    if workspace:
+        need = ldn.ldn_chunk_fwd_workspace_size(w.B, w.T, w.H, w.dk, w.dv, 64, w.mode,
+                                                ldn.LDN_BF16 if w.dtype == "bf16" else ldn.LDN_F32)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
     out, sf = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"] if S0 else None,
-                            mode=w.mode, variant=variant, want_state=want_state)
+                            mode=w.mode, variant=variant, want_state=want_state, workspace=ws)
     assert ldn.device_status() == ldn.LDN_OK
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), (None if sf is None else sf.cpu().numpy())
@@ -247,8 +255,9 @@ def _sampled(name, picks, variant=ldn.LDN_VARIANT_AUTO, **over):
 
 # Every output element and every final-state element of each full-size
 # chunkwise workload (Gated DeltaNet B=4 T=2048; KDA B=8 T=4096; the long
-# Gated DeltaNet sequences T = 8192, 32768, 65536 with S0), computed with the
-# variant the library picks by itself, against the oracle over the whole tensor.
+# Gated DeltaNet sequences T = 8192, 32768, 65536 with S0), computed as the
+# benchmark launches it (ldn_chunk_fwd_ws with a workspace, the variant the
+# library picks), against the oracle over the whole tensor.
 FULL_WORKLOADS = ["gdn_bf16_b4_t2048_h16_d128", "kda_bf16_b8_t4096_h16_d128", "gdn_bf16_long_b1_t8192_h16_d128",
                   "gdn_bf16_long_b1_t32768_h16_d128", "gdn_bf16_long_b1_t65536_h16_d128"]
 
@@ -256,7 +265,7 @@ FULL_WORKLOADS = ["gdn_bf16_b4_t2048_h16_d128", "kda_bf16_b8_t4096_h16_d128", "g
 @pytest.mark.parametrize("name", FULL_WORKLOADS)
 def test_full_workload_whole_tensors(name):
     w = wl.make_chunk(name)
-    o, s = run_gpu(w)
+    o, s = run_gpu(w, workspace=True)
     ro, rs = oracle_chunk(w)
     po, ps = parity(o, ro, w.dtype), parity(s, rs, "f32", tol=TOL[w.dtype])
     print(f"\n{name}: output: {fmt_parity(po)}; final state: plain {ps['plain']:.3g} over {ps['n']} elements")
@@ -270,6 +279,12 @@ def test_full_workload_whole_tensors(name):
                                         ("gdn_bf16_long_b1_t65536_h16_d128", [(0, 5)])])
 def test_full_workloads_split_variant_sampled(name, picks):
     _sampled(name, picks, ldn.LDN_VARIANT_SPLIT)
+
+
+@pytest.mark.parametrize("name,picks", [("kda_bf16_b8_t4096_h16_d128", [(0, 3), (7, 12)]),
+                                        ("gdn_bf16_long_b1_t65536_h16_d128", [(0, 5)])])
+def test_full_workloads_presolved_variant_sampled(name, picks):
+    _sampled(name, picks, ldn.LDN_VARIANT_PRESOLVED)
 
 
 @pytest.mark.parametrize("name,picks", [("gdn_bf16_b4_t2048_h16_d128", [(0, 0), (2, 9), (3, 15)]),

@@ -130,7 +130,8 @@ def test_token_runs_of_long_sequences(want_state):
 def test_auto_follows_the_cost_model():
     w = wl.make_chunk(GDN_BASE)
     chosen = ldn.ldn_chunk_fwd_select_ws(w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16, 1 << 62)
-    assert chosen in (ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_PAIR, ldn.LDN_VARIANT_SPLIT)
+    assert chosen in (ldn.LDN_VARIANT_TENSOR, ldn.LDN_VARIANT_PAIR, ldn.LDN_VARIANT_SPLIT,
+                      ldn.LDN_VARIANT_PRESOLVED)
     o, s = run_noalloc(w, ldn.LDN_VARIANT_AUTO)
     ro, rs = run_ref(w, chosen)
     _same(o, ro)
