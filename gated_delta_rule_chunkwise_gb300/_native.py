@@ -61,7 +61,7 @@ _SIGNATURES = {
     "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 8 + [_P], _I),
     "ldn_backward": ([_P] * 14 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
     "ldn_rla_fwd": ([_P] * 6 + [ctypes.c_float] + [_P] * 5 + [_I] * 7 + [_P], _I),
-    "ldn_backward_workspace_size": ([_I] * 6, ctypes.c_size_t),
+    "ldn_backward_workspace_size": ([_I] * 7, ctypes.c_size_t),
     "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
     "ldn_rmsnorm_gated": ([_P] * 4 + [_I] * 5 + [ctypes.c_float, _P], _I),
@@ -146,8 +146,8 @@ def ldn_backward(q, k, v, beta, gate, S0, dout, dS_final, dq, dk, dv, dbeta, dga
                                dk_dim, dv_dim, mode, dtype, workspace, workspace_bytes, stream)
 
 
-def ldn_backward_workspace_size(B, T, H, dk, dv, mode):
-    return load().ldn_backward_workspace_size(B, T, H, dk, dv, mode)
+def ldn_backward_workspace_size(B, T, H, dk, dv, mode, dtype):
+    return load().ldn_backward_workspace_size(B, T, H, dk, dv, mode, dtype)
 
 
 def ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv, delta, dtype,
@@ -355,7 +355,7 @@ def backward(q, k, v, beta, gate, S0, dout, dS_final=None, *, mode, workspace=No
              dv=torch.empty((B, T, H, dv), **f32), dbeta=torch.empty((B, T, H), **f32),
              dgate=None if gate is None else torch.empty(tuple(gate.shape), **f32),
              dS0=torch.empty((B, H, dk, dv), **f32))
-    need = ldn_backward_workspace_size(B, T, H, dk, dv, mode)
+    need = ldn_backward_workspace_size(B, T, H, dk, dv, mode, _dtype_code(q))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check(workspace, "workspace", dtype=torch.uint8)

@@ -4,7 +4,11 @@
 marshalling only: both directions run in the CUDA kernels of libldn.so.
 
 The gradients of q, k and v are returned in their dtype (the kernel computes
-them in fp32); beta, gate and S0 are fp32 throughout.
+them in fp32); beta, gate and S0 are fp32 throughout.  The output's gradient
+reaches backward() in the output's dtype (autograd casts every incoming
+gradient to the dtype of the tensor it belongs to), which is the inputs' dtype:
+ldn_backward takes it in that dtype, and the conversion below only makes the
+layout contiguous.
 """
 from __future__ import annotations
 

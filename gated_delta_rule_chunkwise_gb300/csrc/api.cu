@@ -460,10 +460,18 @@ static int check_bwd_sizes(int B, int T, int H, int dk, int dv, int mode, int dt
     return LDN_OK;
 }
 
-extern "C" size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode)
+// The chunkwise tensor-core backward takes bf16 DeltaNet / Gated DeltaNet at dk = dv = 128;
+// every other call runs the recurrent backward.
+static bool bwd_chunkwise(int dk, int dv, int mode, int dtype)
 {
-    if (check_bwd_sizes(B, T, H, dk, dv, mode, LDN_F32) != LDN_OK) return 0;
-    return bwd_workspace_bytes(B, T, H, dk, dv, mode);
+    return dtype == LDN_BF16 && dk == 128 && dv == 128 && (mode == LDN_DELTANET || mode == LDN_GDN);
+}
+
+extern "C" size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode, int dtype)
+{
+    if (check_bwd_sizes(B, T, H, dk, dv, mode, dtype) != LDN_OK) return 0;
+    return bwd_chunkwise(dk, dv, mode, dtype) ? bwd_chunk_workspace_bytes(B, T, H)
+                                              : bwd_workspace_bytes(B, T, H, dk, dv, mode);
 }
 
 extern "C" int ldn_backward(const void *q, const void *k, const void *v, const float *beta, const float *gate,
@@ -492,10 +500,17 @@ extern "C" int ldn_backward(const void *q, const void *k, const void *v, const f
     for (const void *p : f4)
         if (!aligned(p, 4)) return LDN_ERR_INVALID_ARG;
     if (gated && (!aligned(gate, 4) || !aligned(dgate, 4))) return LDN_ERR_INVALID_ARG;
-    if (!workspace || !aligned(workspace, 16) || workspace_bytes < bwd_workspace_bytes(B, T, H, dk, dv, mode))
-        return LDN_ERR_INVALID_ARG;
+    const bool chunked = bwd_chunkwise(dk, dv, mode, dtype);
+    if (chunked) {   // tensors read as 16-byte rows and through TMA descriptors
+        const void *a16p[] = {q, k, v, dout, dq, dk_out, dv_out};
+        for (const void *p : a16p)
+            if (!aligned16(p)) return LDN_ERR_INVALID_ARG;
+    }
+    const size_t need = chunked ? bwd_chunk_workspace_bytes(B, T, H) : bwd_workspace_bytes(B, T, H, dk, dv, mode);
+    if (!workspace || !aligned(workspace, chunked ? 256 : 16) || workspace_bytes < need) return LDN_ERR_INVALID_ARG;
     BwdArgs a{q, k, v, beta, gated ? gate : nullptr, S0, dout, dS_final, dq, dk_out, dv_out, dbeta,
               gated ? dgate : nullptr, dS0, (float *)workspace, B, T, H, dk, dv, mode, dtype};
+    if (chunked) return launch_backward_chunk(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
     return launch_backward(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 

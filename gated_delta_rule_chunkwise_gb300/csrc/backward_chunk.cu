@@ -1,0 +1,1043 @@
+// Chunkwise backward of DeltaNet and Gated DeltaNet (scalar decay) on the tensor cores:
+// warp-level fp16 MMAs (mma.sync m16n8k16, ldmatrix operands) with fp32 accumulation, for
+// bf16 inputs with dk = dv = 128 and chunks of 64 tokens.
+//
+// The pages state the recurrence per token (linear-attention notes, Sec. 2.3-2.4) and describe
+// a first-order backward that keeps the state history, checked in fp64 (the method-sources
+// page, KDA entry).  The chunk form of the derivative is derived here.  In H = S^T ([dk][dv]),
+// for a chunk of rows r with incoming state H0, g the inclusive prefix of the log-decay,
+// Gamma_rj = e^{g_r - g_j}, ge = e^{g}, gc = e^{g_last - g} and gamma = e^{g_last}, the forward
+// is
+//   A = strict_tril(Diag(beta) (K K^T * Gamma)),   T = (I + A)^-1,
+//   W = T Diag(beta ge) K,   U' = T Diag(beta) V,   U = U' - W H0,
+//   P = tril(Q K^T * Gamma),   O = Diag(ge) Q H0 + P U,   H_C = gamma H0 + K^T Diag(gc) U,
+// and, given dO and dH_C (written dH' below), its reverse is
+//   dU  = Diag(gc) K dH' + P^T dO,       dW = -dU H0^T,
+//   dH0 = gamma dH' + Q^T Diag(ge) dO - W^T dU                      (the chain, kernel 1)
+//   dP  = tril(dO U^T),   dT = dU Vb^T + dW Kb^T  (Vb = Diag(beta) V, Kb = Diag(beta ge) K),
+//   dA  = strict_tril(-T^T dT T^T),   E' = dA * Gamma,   F = dP * Gamma,
+//   dQ  = Diag(ge) dO H0^T + F K,
+//   dK  = Diag(beta) E' K + E'^T Diag(beta) K + F^T Q + Diag(gc) U dH'^T + Diag(beta ge) T^T dW,
+//   dV  = Diag(beta) T^T dU,
+//   dbeta = rowsum(E' * K K^T) + rowsum(V * T^T dU) + ge rowsum(K * T^T dW),
+//   dg  = rowsum(R) - colsum(R) + ge (rowsum(Q * dO H0^T) + beta rowsum(K * T^T dW))
+//         - gc rowsum(K * U dH'^T), and at the last row also + sum(gc rowsum(K * U dH'^T))
+//         + gamma sum(H0 * dH'), with R = Diag(beta) E' * K K^T + F * Q K^T;
+//   the log-decay input's gradient is the reverse cumulative sum of dg within the chunk.
+// (Padded rows past the end of the sequence are zero and carry no decay.)
+//
+// The backward is three steps after a forward pass that stores the state entering every
+// chunk (the fused / pre-solved forward kernels with chunk_states) and X = [P T ; T] of every
+// chunk (the pre-solved variant's solve, whose rows 64..127 are T):
+//   1. bwd_chain_kernel: one CTA per (b, h, 64-wide slice of dv) walks the chunks in reverse
+//      and carries dH in fp32; it stores the dH' of every chunk.
+//   2. bwd_chunk_kernel: one CTA per (b, h, chunk), all in parallel, forms every gradient of
+//      the chunk from its inputs, T, H0 and dH'.
+// Arithmetic: products on fp16 operands (2^-11) with fp32 accumulation; states, gradients and
+// every elementwise step in fp32.  Operands stay in fp16 range when the log-decays are not
+// positive (every Gamma, ge, gc <= 1).
+#include "ldn_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace ldn {
+namespace {
+using namespace sm100;
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr int kLdW = kD + 8;    // fp16 row stride of 128-column tiles (272 B: ldmatrix conflict-free)
+constexpr int kLdN = kC + 8;    // fp16 row stride of 64-column tiles (144 B)
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kXBytes = 16384;  // X = [P T ; T] per (b, h, chunk), the swizzled image the solve writes
+constexpr int kLdO = kD + 8;    // fp32 row stride of the staged gradient rows (544 B)
+constexpr uint64_t kWaitNs = 2000000000ull;   // bound of every wait (2 s)
+static_assert(kStateImgLd == kLdW, "the state images are the shared-memory tiles");
+
+// One operand pair of a product: op(A) [M x K] times op(B) [K x N], fp16 in shared memory.
+// ta: A is stored K x M (element (m, k) at a[k * lda + m]), else M x K (a[m * lda + k]);
+// tb: B is stored N x K (element (k, n) at b[n * ldb + k]), else K x N (b[k * ldb + n]).
+struct Op {
+    const __half *a;
+    int lda;
+    bool ta;
+    const __half *b;
+    int ldb;
+    bool tb;
+    int K;
+};
+
+// Warp grid of an M x N product: the 8 warps as WM x WN, each owning MT x NT adjacent 16 x 16
+// output tiles (a 32 x 32 block for the 64 x 128 and 128 x 64 products, 16 x 32 for 64 x 64),
+// so the A fragments of a k-step serve NT tiles and the B fragments MT tiles.
+template <int M, int N>
+struct WarpGrid {
+    static constexpr int WN = N >= 128 ? 4 : 2, WM = kWarps / WN;
+    static constexpr int MT = M / 16 / WM, NT = N / 16 / WN;
+    static_assert(MT >= 1 && NT >= 1 && MT * 16 * WM == M && NT * 16 * WN == N, "warp grid");
+};
+
+// Origin (m0, n0) of tile i of a warp in an M x N product (the same in every product of that shape).
+template <int M, int N>
+__device__ __forceinline__ int2 tile_origin(int warp, int i)
+{
+    using G = WarpGrid<M, N>;
+    return make_int2(((warp / G::WN) * G::MT + i / G::NT) * 16, ((warp % G::WN) * G::NT + i % G::NT) * 16);
+}
+
+// Out [M x N] = sum over the ops of op(A) op(B).  Warp w computes its tiles i = 0 .. TILES-1
+// (tile_origin) together, every k-step fully unrolled; then calls epi(i, m0, n0, acc) per
+// tile: acc[nt][e] is the element at row m0 + g + 8 (e >> 1), column n0 + 8 nt + 2 t + (e & 1),
+// with g = lane / 4, t = lane % 4 (the mma.sync accumulator layout).
+template <int M, int N, int NOPS, typename Epi>
+__device__ __forceinline__ void cta_mma(const Op (&ops)[NOPS], int warp, int lane, Epi &&epi)
+{
+    using G = WarpGrid<M, N>;
+    const int r = lane & 7, j = lane >> 3;
+    const int2 o0 = tile_origin<M, N>(warp, 0);
+    float acc[G::MT][G::NT][2][4];
+#pragma unroll
+    for (int a = 0; a < G::MT; ++a)
+#pragma unroll
+        for (int b = 0; b < G::NT; ++b)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[a][b][e >> 2][e & 3] = 0.f;
+#pragma unroll
+    for (int o = 0; o < NOPS; ++o) {
+        const Op &op = ops[o];
+#pragma unroll 8
+        for (int k0 = 0; k0 < op.K; k0 += 16) {
+            uint32_t af[G::MT][4], bq[G::NT][4];
+#pragma unroll
+            for (int a = 0; a < G::MT; ++a) {
+                const int m0 = o0.x + 16 * a;
+                if (op.ta)
+                    ldsm_x4_trans(af[a], op.a + (k0 + r + 8 * (j >> 1)) * op.lda + m0 + 8 * (j & 1));
+                else
+                    ldsm_x4(af[a], op.a + (m0 + r + 8 * (j & 1)) * op.lda + k0 + 8 * (j >> 1));
+            }
+#pragma unroll
+            for (int b = 0; b < G::NT; ++b) {
+                const int n0 = o0.y + 16 * b;
+                if (op.tb)
+                    ldsm_x4(bq[b], op.b + (n0 + r + 8 * (j >> 1)) * op.ldb + k0 + 8 * (j & 1));
+                else
+                    ldsm_x4_trans(bq[b], op.b + (k0 + r + 8 * (j & 1)) * op.ldb + n0 + 8 * (j >> 1));
+            }
+#pragma unroll
+            for (int a = 0; a < G::MT; ++a)
+#pragma unroll
+                for (int b = 0; b < G::NT; ++b) {
+                    mma_f16_16x8x16(acc[a][b][0], af[a], bq[b]);
+                    mma_f16_16x8x16(acc[a][b][1], af[a], bq[b] + 2);
+                }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < G::MT; ++a)
+#pragma unroll
+        for (int b = 0; b < G::NT; ++b) epi(a * G::NT + b, o0.x + 16 * a, o0.y + 16 * b, acc[a][b]);
+}
+
+// Row and column of accumulator element e of half nt in a tile at (m0, n0).
+__device__ __forceinline__ int acc_row(int lane, int m0, int e) { return m0 + (lane >> 2) + 8 * (e >> 1); }
+__device__ __forceinline__ int acc_col(int lane, int n0, int nt, int e) { return n0 + 8 * nt + 2 * (lane & 3) + (e & 1); }
+
+// Sum of v over the 4 threads of an accumulator row (lanes 4 g .. 4 g + 3).
+__device__ __forceinline__ float row_quad_sum(float v)
+{
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v;
+}
+
+// bf16 16-byte group -> fp16 16-byte group (times s)
+__device__ __forceinline__ uint4 bf16x8_to_f16(uint4 u, float s = 1.f)
+{
+    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+    __half2 h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        h[i] = __floats2half2_rn(f.x * s, f.y * s);
+    }
+    return *reinterpret_cast<uint4 *>(h);
+}
+
+// Rows of bf16 tiles (128 channels: 16 groups of 16 bytes) into fp16 tiles of stride kLdW:
+// NT tiles of 64 rows each, every load of the thread in flight before the first store.
+template <int NT>
+__device__ __forceinline__ void load_tiles_f16(const __nv_bfloat16 *const (&src)[NT], __half *const (&dst)[NT],
+                                               size_t tok0, int H, int L, int tid)
+{
+    constexpr int kPer = NT * kC * 16 / kThreads;   // 16-byte groups per thread
+    uint4 u[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int e = tid + kThreads * i, which = e / (kC * 16), rr = (e / 16) % kC, part = e % 16;
+        u[i] = rr < L ? __ldg(reinterpret_cast<const uint4 *>(src[which] + (tok0 + (size_t)rr * H) * kD) + part)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int e = tid + kThreads * i, which = e / (kC * 16), rr = (e / 16) % kC, part = e % 16;
+        *reinterpret_cast<uint4 *>(dst[which] + rr * kLdW + 8 * part) = bf16x8_to_f16(u[i]);
+    }
+}
+
+// Rows of a staged fp32 [64][kLdO] tile to the token rows of a [.., H, 128] gradient tensor,
+// a warp per row (32 x 16 bytes), rows past the sequence skipped.
+__device__ __forceinline__ void store_rows(float *__restrict__ dst, const float *src, size_t tok0, int H, int L,
+                                           int tid)
+{
+#pragma unroll 4
+    for (int e = tid; e < kC * 32; e += kThreads) {
+        const int rr = e >> 5, part = e & 31;
+        if (rr < L)
+            *reinterpret_cast<float4 *>(dst + (tok0 + (size_t)rr * H) * kD + 4 * part) =
+                *reinterpret_cast<const float4 *>(src + rr * kLdO + 4 * part);
+    }
+}
+
+// T of a chunk from the solve's X image (rows 64..127, 128-byte swizzled K-major fp16: the
+// 16-byte group p of row `row` holds columns 8 ((p ^ row) & 7) ..), as fp16 tiles of stride
+// kLdN: T itself (optional), T Diag(s1) and (optional) T Diag(s2), s1 / s2 per column.
+__device__ __forceinline__ void load_t(const uint8_t *X, __half *t, __half *t1, const float *s1, __half *t2,
+                                       const float *s2, int tid)
+{
+    uint4 u[kC * 8 / kThreads];
+#pragma unroll
+    for (int i = 0; i < kC * 8 / kThreads; ++i) u[i] = __ldg(reinterpret_cast<const uint4 *>(X + 8192) + tid + kThreads * i);
+#pragma unroll
+    for (int i = 0; i < kC * 8 / kThreads; ++i) {
+        const int e = tid + kThreads * i, j = e >> 3, c8 = 8 * (((e & 7) ^ (64 + j)) & 7);
+        const __half2 *h2 = reinterpret_cast<const __half2 *>(&u[i]);
+        __half2 a[4], b2[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(h2[q]);
+            a[q] = __floats2half2_rn(f.x * s1[c8 + 2 * q], f.y * s1[c8 + 2 * q + 1]);
+            if (t2) b2[q] = __floats2half2_rn(f.x * s2[c8 + 2 * q], f.y * s2[c8 + 2 * q + 1]);
+        }
+        if (t) *reinterpret_cast<uint4 *>(t + j * kLdN + c8) = u[i];
+        *reinterpret_cast<uint4 *>(t1 + j * kLdN + c8) = *reinterpret_cast<uint4 *>(a);
+        if (t2) *reinterpret_cast<uint4 *>(t2 + j * kLdN + c8) = *reinterpret_cast<uint4 *>(b2);
+    }
+}
+
+// Per-chunk gate data: the inclusive log-decay prefix of the chunk's rows (warp 0; rows past
+// the sequence and DeltaNet add nothing), beta.
+template <int MODE>
+__device__ __forceinline__ void chunk_gates(const float *__restrict__ beta, const float *__restrict__ gate,
+                                            size_t tok0, int H, int L, int lane, float *sbeta, float *sg)
+{
+    for (int rr = lane; rr < kC; rr += 32) sbeta[rr] = rr < L ? __ldg(beta + tok0 + (size_t)rr * H) : 0.f;
+    float a0 = 0.f, a1 = 0.f;
+    if (MODE == LDN_GDN) {
+        const int r0 = 2 * lane, r1 = r0 + 1;
+        a0 = r0 < L ? __ldg(gate + tok0 + (size_t)r0 * H) : 0.f;
+        a1 = r1 < L ? __ldg(gate + tok0 + (size_t)r1 * H) : 0.f;
+    }
+    float incl = a0 + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    sg[2 * lane] = incl - a1;
+    sg[2 * lane + 1] = incl;
+}
+
+// =====================================================================================
+// Kernel 1: the chain dH0 = gamma dH' + Q^T Diag(ge) dO - W^T (Diag(gc) K dH' + P^T dO),
+// chunks in reverse, one CTA per (b, h, 64-wide slice of dv), dH in fp32 registers (the
+// warp owns the same 16 x 16 tiles of the 128 x 64 state in every chunk).  The fp16 state
+// image dHs[c] receives the dH' of chunk c (the gradient at the state it leaves); dS0 the
+// gradient at S0.
+struct ChainSmem {
+    static constexpr int q = 0;                                   // Q [64][136] fp16
+    static constexpr int k = q + kC * kLdW * 2;                   // K [64][136]
+    static constexpr int tk = k + kC * kLdW * 2;                  // T Diag(beta ge) [64][72]
+    static constexpr int p = tk + kC * kLdN * 2;                  // P [64][72]
+    static constexpr int w = p + kC * kLdN * 2;                   // W [64][136]
+    static constexpr int dO = w + kC * kLdW * 2;                  // Diag(ge) dO slice [64][72]
+    static constexpr int dOr = dO + kC * kLdN * 2;                // dO slice [64][72]
+    static constexpr int du = dOr + kC * kLdN * 2;                // dU [64][72]
+    static constexpr int dh = du + kC * kLdN * 2;                 // dH' fp16 [128][72]
+    static constexpr int small = dh + kD * kLdN * 2;              // beta, g, ge, gc, beta ge
+    // staging of the next chunk's inputs (cp.async): q, k rows (bf16 [64][128]), the dO
+    // slice (bf16 [64][64]), T (X rows 64..127, swizzled fp16 [64][64]), beta and gate
+    static constexpr int sq = small + 5 * kC * 4;
+    static constexpr int sk = sq + kC * kD * 2;
+    static constexpr int sdo = sk + kC * kD * 2;
+    static constexpr int st = sdo + kC * 64 * 2;
+    static constexpr int sb = st + kC * kC * 2;
+    static constexpr int sgt = sb + kC * 4;
+    static constexpr int bytes = sgt + kC * 4;
+    static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
+};
+
+// Stage chunk c's inputs for the chain (16-byte cp.async; rows past the sequence read as zero).
+__device__ __forceinline__ void chain_prefetch(uint8_t *smc, const __nv_bfloat16 *__restrict__ q,
+                                               const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
+                                               const float *__restrict__ gate, const __nv_bfloat16 *__restrict__ dout,
+                                               const uint8_t *__restrict__ Xc, size_t tok0, int H, int L, int dv,
+                                               int n0, int tid)
+{
+    using SM = ChainSmem;
+    for (int e = tid; e < 2 * kC * 16; e += kThreads) {   // q, k: 16 groups per row
+        const int which = e / (kC * 16), rr = (e / 16) % kC, part = e % 16;
+        const __nv_bfloat16 *src = (which ? k : q) + (tok0 + (size_t)(rr < L ? rr : 0) * H) * kD + 8 * part;
+        cp_async16(smc + (which ? SM::sk : SM::sq) + (rr * 16 + part) * 16, src, rr < L ? 16u : 0u);
+    }
+    for (int e = tid; e < kC * 8; e += kThreads) {        // dO slice: 8 groups per row; T: 8 per row
+        const int rr = e >> 3, part = e & 7;
+        const __nv_bfloat16 *src = dout + (tok0 + (size_t)(rr < L ? rr : 0) * H) * dv + n0 + 8 * part;
+        cp_async16(smc + SM::sdo + e * 16, src, rr < L ? 16u : 0u);
+        cp_async16(smc + SM::st + e * 16, Xc + 8192 + e * 16, 16u);
+    }
+    if (tid < kC) {
+        const int rr = tid;
+        cp_async4(smc + SM::sb + 4 * rr, beta + tok0 + (size_t)(rr < L ? rr : 0) * H, rr < L ? 4u : 0u);
+        if (gate) cp_async4(smc + SM::sgt + 4 * rr, gate + tok0 + (size_t)(rr < L ? rr : 0) * H, rr < L ? 4u : 0u);
+    }
+    cp_async_commit();
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_chain_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                 const float *__restrict__ beta, const float *__restrict__ gate,
+                 const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ dS_final,
+                 const uint8_t *__restrict__ X, __half *__restrict__ dHs, float *__restrict__ dS0, int T, int H, int dv)
+{
+    extern __shared__ __align__(16) uint8_t smc[];
+    using SM = ChainSmem;
+    __half *Qs = reinterpret_cast<__half *>(smc + SM::q), *Ks = reinterpret_cast<__half *>(smc + SM::k);
+    __half *TKs = reinterpret_cast<__half *>(smc + SM::tk), *Ps = reinterpret_cast<__half *>(smc + SM::p);
+    __half *Ws = reinterpret_cast<__half *>(smc + SM::w), *dOs = reinterpret_cast<__half *>(smc + SM::dO);
+    __half *dOr = reinterpret_cast<__half *>(smc + SM::dOr), *dUs = reinterpret_cast<__half *>(smc + SM::du);
+    __half *dHh = reinterpret_cast<__half *>(smc + SM::dh);
+    float *sbeta = reinterpret_cast<float *>(smc + SM::small), *sg = sbeta + kC, *sge = sg + kC, *sgc = sge + kC;
+    float *sbge = sgc + kC;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slices = dv / 64, unit = blockIdx.x / slices, n0 = (blockIdx.x % slices) * 64;
+    const int b = unit / H, h = unit % H;
+    const int nch = (T + kC - 1) / kC;
+
+    // dH' of the last chunk: dS_final (or zero); tile i of this warp: rows / columns of the
+    // accumulator layout (M = 128 dk rows, N = 64 columns: 32 tiles, 4 per warp)
+    float dh[4][2][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int2 og = tile_origin<kD, 64>(warp, i);
+        const int m0 = og.x, c0 = og.y;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                dh[i][nt][e] = dS_final ? dS_final[((size_t)unit * kD + rr) * dv + n0 + cc] : 0.f;
+            }
+    }
+    auto tok_of = [&](int c) { return ((size_t)b * T + (size_t)c * kC) * H + h; };
+    chain_prefetch(smc, q, k, beta, gate, dout, X + ((size_t)unit * nch + nch - 1) * kXBytes, tok_of(nch - 1), H,
+                   min(kC, T - (nch - 1) * kC), dv, n0, tid);
+    for (int c = nch - 1; c >= 0; --c) {
+        cp_async_wait<0>();
+        __syncthreads();
+        // ---- the staged inputs to fp16 tiles; gates (warp 0); dH' (fp32 out, fp16 copy)
+        for (int e = tid; e < 2 * kC * 16; e += kThreads) {
+            const int which = e / (kC * 16), rr = (e / 16) % kC, part = e % 16;
+            const uint4 u = *reinterpret_cast<const uint4 *>(smc + (which ? SM::sk : SM::sq) + (rr * 16 + part) * 16);
+            *reinterpret_cast<uint4 *>((which ? Ks : Qs) + rr * kLdW + 8 * part) = bf16x8_to_f16(u);
+        }
+        if (warp == 0) {
+            const float *gb = reinterpret_cast<const float *>(smc + SM::sb);
+            const float *gg = reinterpret_cast<const float *>(smc + SM::sgt);
+            const int r0 = 2 * lane, r1 = r0 + 1;
+            const float a0 = MODE == LDN_GDN ? gg[r0] : 0.f, a1 = MODE == LDN_GDN ? gg[r1] : 0.f;
+            float incl = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const float gl = __shfl_sync(0xffffffffu, incl, 31);
+            const float g0 = incl - a1, g1 = incl;
+            sg[r0] = g0;
+            sg[r1] = g1;
+            sbeta[r0] = gb[r0];
+            sbeta[r1] = gb[r1];
+            sge[r0] = MODE == LDN_GDN ? expf(g0) : 1.f;
+            sge[r1] = MODE == LDN_GDN ? expf(g1) : 1.f;
+            sgc[r0] = MODE == LDN_GDN ? expf(gl - g0) : 1.f;
+            sgc[r1] = MODE == LDN_GDN ? expf(gl - g1) : 1.f;
+            sbge[r0] = gb[r0] * sge[r0];
+            sbge[r1] = gb[r1] * sge[r1];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int2 og = tile_origin<kD, 64>(warp, i);
+            const int m0 = og.x, c0 = og.y;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    *reinterpret_cast<__half2 *>(dHh + rr * kLdN + cc) =
+                        __floats2half2_rn(dh[i][nt][e], dh[i][nt][e + 1]);
+                }
+        }
+        __syncthreads();
+        // dH' (fp16) into the chunk's state-gradient image, 16-byte rows; T Diag(beta ge) (the
+        // staged swizzled rows); the dO slice, plain and times ge
+        {
+            __half *img = dHs + ((size_t)unit * nch + c) * (kStateImgBytes / 2) + n0;
+#pragma unroll
+            for (int e = tid; e < kD * 8; e += kThreads)
+                *reinterpret_cast<uint4 *>(img + (e >> 3) * kStateImgLd + 8 * (e & 7)) =
+                    *reinterpret_cast<const uint4 *>(dHh + (e >> 3) * kLdN + 8 * (e & 7));
+        }
+        for (int e = tid; e < kC * 8; e += kThreads) {
+            const int j = e >> 3, c8 = 8 * (((e & 7) ^ (64 + j)) & 7);
+            const uint4 u = *reinterpret_cast<const uint4 *>(smc + SM::st + e * 16);
+            const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
+            __half2 a[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const float2 f = __half22float2(h2[qq]);
+                a[qq] = __floats2half2_rn(f.x * sbge[c8 + 2 * qq], f.y * sbge[c8 + 2 * qq + 1]);
+            }
+            *reinterpret_cast<uint4 *>(TKs + j * kLdN + c8) = *reinterpret_cast<uint4 *>(a);
+            const int rr = e >> 3, part = e & 7;
+            const uint4 d = *reinterpret_cast<const uint4 *>(smc + SM::sdo + e * 16);
+            *reinterpret_cast<uint4 *>(dOr + rr * kLdN + 8 * part) = bf16x8_to_f16(d);
+            *reinterpret_cast<uint4 *>(dOs + rr * kLdN + 8 * part) = bf16x8_to_f16(d, sge[rr]);
+        }
+        __syncthreads();
+        if (c > 0)   // the staging buffer is free: the previous chunk's inputs load under this chunk's products
+            chain_prefetch(smc, q, k, beta, gate, dout, X + ((size_t)unit * nch + c - 1) * kXBytes, tok_of(c - 1), H,
+                           kC, dv, n0, tid);
+        // ---- P = tril(Q K^T * Gamma) and W = T Diag(beta ge) K
+        {
+            const Op ops[1] = {{Qs, kLdW, false, Ks, kLdW, true, kD}};
+            cta_mma<kC, kC>(ops, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                        const float gm = MODE == LDN_GDN ? expf(sg[rr] - sg[jj]) : 1.f;
+                        Ps[rr * kLdN + jj] = __float2half_rn(jj <= rr ? acc[nt][e] * gm : 0.f);
+                    }
+            });
+            const Op opw[1] = {{TKs, kLdN, false, Ks, kLdW, false, kC}};
+            cta_mma<kC, kD>(opw, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                        *reinterpret_cast<__half2 *>(Ws + rr * kLdW + cc) = __floats2half2_rn(acc[nt][e], acc[nt][e + 1]);
+                    }
+            });
+        }
+        __syncthreads();
+        // ---- dU = Diag(gc) K dH' + P^T dO
+        {
+            float keep[2][2][4];   // this warp's two dU tiles: (Diag(gc) K dH') then + P^T dO
+            const Op o1[1] = {{Ks, kLdW, false, dHh, kLdN, false, kD}};
+            cta_mma<kC, 64>(o1, warp, lane, [&](int i, int m0, int, float (&acc)[2][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) keep[i][nt][e] = acc[nt][e] * sgc[acc_row(lane, m0, e)];
+            });
+            const Op o2[1] = {{Ps, kLdN, true, dOr, kLdN, false, kC}};
+            cta_mma<kC, 64>(o2, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                        *reinterpret_cast<__half2 *>(dUs + rr * kLdN + cc) =
+                            __floats2half2_rn(keep[i][nt][e] + acc[nt][e], keep[i][nt][e + 1] + acc[nt][e + 1]);
+                    }
+            });
+        }
+        __syncthreads();
+        // ---- dH0 = gamma dH' + Q^T Diag(ge) dO - W^T dU (this warp's tiles, in registers)
+        {
+            const float gam = MODE == LDN_GDN ? expf(sg[kC - 1]) : 1.f;
+            const Op o1[1] = {{Qs, kLdW, true, dOs, kLdN, false, kC}};
+            const Op o2[1] = {{Ws, kLdW, true, dUs, kLdN, false, kC}};
+            float qd[4][2][4];
+            cta_mma<kD, 64>(o1, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) qd[i][nt][e] = acc[nt][e];
+            });
+            cta_mma<kD, 64>(o2, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dh[i][nt][e] = gam * dh[i][nt][e] + qd[i][nt][e] - acc[nt][e];
+            });
+        }
+        // (the next chunk's first barrier orders these reads before its writes)
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int2 og = tile_origin<kD, 64>(warp, i);
+        const int m0 = og.x, c0 = og.y;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                *reinterpret_cast<float2 *>(dS0 + ((size_t)unit * kD + rr) * dv + n0 + cc) =
+                    make_float2(dh[i][nt][e], dh[i][nt][e + 1]);
+            }
+    }
+}
+
+// =====================================================================================
+// Kernel 2: every chunk's gradients, one CTA per (b, h, chunk).  Shared-memory plan (fp16
+// tiles; buffers are reused once their last reader is past):
+//   Q, K, V, dO [64][136] (dO's place takes dW; V and dO's together the staged dK rows), H0
+//   and dH' [128][136] (their places the staged dV and dQ rows), T, T Diag(beta ge) (then X1 = T^T dT, then
+//   E = Diag(beta) E'), T Diag(beta) (then dT, then E'), P (then F) [64][72], W (then dU) and
+//   U [64][136], small vectors.
+struct ChunkSmem {
+    static constexpr int q = 0;
+    static constexpr int k = q + kC * kLdW * 2;
+    static constexpr int v = k + kC * kLdW * 2;
+    static constexpr int dO = v + kC * kLdW * 2;          // then dW
+    static constexpr int h0 = dO + kC * kLdW * 2;         // [128][136]; then dV fp32 [64][136]
+    static constexpr int dh = h0 + kD * kLdW * 2;         // [128][136]; then dQ fp32 [64][136]
+    static constexpr int t = dh + kD * kLdW * 2;
+    static constexpr int tk = t + kC * kLdN * 2;          // T Diag(beta ge); X1; E
+    static constexpr int tv = tk + kC * kLdN * 2;         // T Diag(beta); dT; E'
+    static constexpr int p = tv + kC * kLdN * 2;          // P; F
+    static constexpr int w = p + kC * kLdN * 2;           // -W; dU
+    static constexpr int u = w + kC * kLdW * 2;           // U
+    static constexpr int small = u + kC * kLdW * 2;       // beta, g, ge, gc, beta ge, 8 slots, 5 x [8][64] parts
+    static constexpr int bar = small + (5 * kC + 8 + 5 * kWarps * kC) * 4;   // mbarrier of the state images' copies
+    static constexpr int bytes = bar + 8;
+    static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
+    static_assert(kC * kLdO * 4 <= kD * kLdW * 2 && kC * kLdO * 4 == 2 * kC * kLdW * 2,
+                  "dV / dQ fit a state tile, dK the V and dO tiles");
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
+                 const float *__restrict__ gate, const __nv_bfloat16 *__restrict__ dout,
+                 const uint8_t *__restrict__ X, const __half *__restrict__ Hs, const __half *__restrict__ dHs,
+                 float *__restrict__ dq, float *__restrict__ dk_out, float *__restrict__ dv_out,
+                 float *__restrict__ dbeta, float *__restrict__ dgate, int *status, int T, int H)
+{
+    extern __shared__ __align__(16) uint8_t smk[];
+    using SM = ChunkSmem;
+    __half *Qs = reinterpret_cast<__half *>(smk + SM::q), *Ks = reinterpret_cast<__half *>(smk + SM::k);
+    __half *Vs = reinterpret_cast<__half *>(smk + SM::v), *dOs = reinterpret_cast<__half *>(smk + SM::dO);
+    __half *H0s = reinterpret_cast<__half *>(smk + SM::h0), *dHh = reinterpret_cast<__half *>(smk + SM::dh);
+    __half *Ts = reinterpret_cast<__half *>(smk + SM::t), *TKs = reinterpret_cast<__half *>(smk + SM::tk);
+    __half *TVs = reinterpret_cast<__half *>(smk + SM::tv), *Ps = reinterpret_cast<__half *>(smk + SM::p);
+    __half *Ws = reinterpret_cast<__half *>(smk + SM::w), *Us = reinterpret_cast<__half *>(smk + SM::u);
+    __half *dWs = dOs, *dUs = Ws, *X1s = TKs, *dTs = TVs, *Fs = Ps, *Es = TKs, *Eps = TVs;
+    float *dVo = reinterpret_cast<float *>(smk + SM::h0), *dQo = reinterpret_cast<float *>(smk + SM::dh);
+    float *dKo = reinterpret_cast<float *>(smk + SM::v);
+    float *sbeta = reinterpret_cast<float *>(smk + SM::small), *sg = sbeta + kC, *sge = sg + kC, *sgc = sge + kC;
+    float *sbge = sgc + kC;        // beta ge
+    float *red = sbge + kC;        // [8] per-warp parts of sum(H0 * dH')
+    // per-warp partial sums [8][64] (each written by its own warp in program order, summed over
+    // the warps in a fixed order at the end: the result does not depend on scheduling)
+    float *p_dge = red + 8;        // rowsum(Q * dO H0^T) + beta rowsum(K * T^T dW)  (then times ge)
+    float *p_dgc = p_dge + kWarps * kC;   // rowsum(K * U dH'^T)
+    float *p_db = p_dgc + kWarps * kC;    // dbeta
+    float *p_dgr = p_db + kWarps * kC;    // rowsum(R)
+    float *p_dgk = p_dgr + kWarps * kC;   // -colsum(R)
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float *pw_dge = p_dge + warp * kC, *pw_dgc = p_dgc + warp * kC, *pw_db = p_db + warp * kC;
+    float *pw_dgr = p_dgr + warp * kC, *pw_dgk = p_dgk + warp * kC;
+    const int nch = (T + kC - 1) / kC;
+    const int unit = blockIdx.x / nch, c = blockIdx.x % nch;
+    const int b = unit / H, h = unit % H;
+    const int t0 = c * kC, L = min(kC, T - t0);
+    const size_t tok0 = ((size_t)b * T + t0) * H + h;
+
+    // ---- 0: inputs.  H0 and dH' (the fp16 state images, already in the tiles' layout) by two
+    //      bulk copies; meanwhile q, k, v, dO rows to fp16 (sixteen 16-byte loads per thread in
+    //      flight); T
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smk + SM::bar);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, 2 * (uint32_t)kStateImgBytes);
+        const size_t img = ((size_t)unit * nch + c) * (kStateImgBytes / 2);
+        bulk_load(H0s, Hs + img, (uint32_t)kStateImgBytes, bar);
+        bulk_load(dHh, dHs + img, (uint32_t)kStateImgBytes, bar);
+    }
+    {
+        const __nv_bfloat16 *const src[4] = {q, k, v, dout};
+        __half *const dst[4] = {Qs, Ks, Vs, dOs};
+        load_tiles_f16<4>(src, dst, tok0, H, L, tid);
+    }
+    if (warp == 0) chunk_gates<MODE>(beta, gate, tok0, H, L, lane, sbeta, sg);
+    for (int e = tid; e < 5 * kWarps * kC; e += kThreads) p_dge[e] = 0.f;
+    __syncthreads();   // (also orders the barrier's initialisation before the waits)
+    if (!__syncthreads_and(mbar_wait(bar, 0, kWaitNs))) {
+        // the copies did not land (in some thread's view): report, give them a last bounded
+        // wait, leave the chunk (every thread, the vote being the block's)
+        if (tid == 0) atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        mbar_wait(bar, 0, kWaitNs / 4);
+        return;
+    }
+    // sum(H0 * dH') (the decay gradient's gamma term) from the fp16 tiles
+    float hdh = 0.f;
+#pragma unroll 4
+    for (int e = tid; e < kD * 16; e += kThreads) {
+        const int rr = e >> 4, part = e & 15;
+        const uint4 a = *reinterpret_cast<const uint4 *>(H0s + rr * kLdW + 8 * part);
+        const uint4 d = *reinterpret_cast<const uint4 *>(dHh + rr * kLdW + 8 * part);
+        const __half2 *a2 = reinterpret_cast<const __half2 *>(&a), *d2 = reinterpret_cast<const __half2 *>(&d);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const float2 fa = __half22float2(a2[x]), fd = __half22float2(d2[x]);
+            hdh += fa.x * fd.x + fa.y * fd.y;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hdh += __shfl_xor_sync(0xffffffffu, hdh, o);
+    if (lane == 0) red[warp] = hdh;
+    for (int rr = tid; rr < kC; rr += kThreads) {
+        const float gl = sg[kC - 1];
+        sge[rr] = MODE == LDN_GDN ? expf(sg[rr]) : 1.f;
+        sgc[rr] = MODE == LDN_GDN ? expf(gl - sg[rr]) : 1.f;
+        sbge[rr] = sbeta[rr] * sge[rr];
+    }
+    __syncthreads();
+    load_t(X + ((size_t)unit * nch + c) * kXBytes, Ts, TKs, sbge, TVs, sbeta, tid);
+    __syncthreads();
+    auto gam_of = [&](int rr, int jj) { return MODE == LDN_GDN ? expf(sg[rr] - sg[jj]) : 1.f; };
+
+    // ---- 1: P = tril(Q K^T * Gamma); -W = -T Diag(beta ge) K
+    {
+        const Op op[1] = {{Qs, kLdW, false, Ks, kLdW, true, kD}};
+        cta_mma<kC, kC>(op, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    Ps[rr * kLdN + jj] = __float2half_rn(jj <= rr ? acc[nt][e] * gam_of(rr, jj) : 0.f);
+                }
+        });
+        const Op ow[1] = {{TKs, kLdN, false, Ks, kLdW, false, kC}};
+        cta_mma<kC, kD>(ow, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    *reinterpret_cast<__half2 *>(Ws + rr * kLdW + cc) = __floats2half2_rn(-acc[nt][e], -acc[nt][e + 1]);
+                }
+        });
+    }
+    __syncthreads();
+    // ---- 2: U = T Diag(beta) V + (-W) H0
+    {
+        const Op op[2] = {{TVs, kLdN, false, Vs, kLdW, false, kC}, {Ws, kLdW, false, H0s, kLdW, false, kD}};
+        cta_mma<kC, kD>(op, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    *reinterpret_cast<__half2 *>(Us + rr * kLdW + cc) = __floats2half2_rn(acc[nt][e], acc[nt][e + 1]);
+                }
+        });
+    }
+    __syncthreads();
+    // ---- 3: dU = Diag(gc) K dH' + P^T dO  (into W's place)
+    {
+        float kd[4][2][4];
+        const Op o1[1] = {{Ks, kLdW, false, dHh, kLdW, false, kD}};
+        cta_mma<kC, kD>(o1, warp, lane, [&](int i, int m0, int, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kd[i][nt][e] = acc[nt][e] * sgc[acc_row(lane, m0, e)];
+        });
+        const Op o2[1] = {{Ps, kLdN, true, dOs, kLdW, false, kC}};
+        cta_mma<kC, kD>(o2, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    *reinterpret_cast<__half2 *>(dUs + rr * kLdW + cc) =
+                        __floats2half2_rn(kd[i][nt][e] + acc[nt][e], kd[i][nt][e + 1] + acc[nt][e + 1]);
+                }
+        });
+    }
+    __syncthreads();
+    // ---- 4: dQ-hat = dO H0^T (dQ's first part, and rowsum(Q * dQ-hat)); F = tril(dO U^T) * Gamma
+    float dqa[4][2][4];   // this warp's dQ tiles (M = 64, N = 128)
+    {
+        const Op o1[1] = {{dOs, kLdW, false, H0s, kLdW, true, kD}};
+        cta_mma<kC, kD>(o1, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    const float2 qv = __half22float2(*reinterpret_cast<const __half2 *>(Qs + rr * kLdW + cc));
+                    rs[e >> 1] += acc[nt][e] * qv.x + acc[nt][e + 1] * qv.y;
+                    dqa[i][nt][e] = acc[nt][e] * sge[rr];
+                    dqa[i][nt][e + 1] = acc[nt][e + 1] * sge[rr];
+                }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float s = row_quad_sum(rs[hh]);
+                if ((lane & 3) == 0) pw_dge[m0 + (lane >> 2) + 8 * hh] += s;
+            }
+        });
+        const Op o2[1] = {{dOs, kLdW, false, Us, kLdW, true, kD}};
+        cta_mma<kC, kC>(o2, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    Fs[rr * kLdN + jj] = __float2half_rn(jj <= rr ? acc[nt][e] * gam_of(rr, jj) : 0.f);
+                }
+        });
+    }
+    __syncthreads();
+    // ---- 5: dK's part Diag(gc) U dH'^T (and rowsum(K * U dH'^T)); -dW = dU H0^T into dO's place
+    float dka[4][2][4];   // this warp's dK tiles
+    {
+        const Op o1[1] = {{Us, kLdW, false, dHh, kLdW, true, kD}};
+        cta_mma<kC, kD>(o1, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(Ks + rr * kLdW + cc));
+                    rs[e >> 1] += acc[nt][e] * kv.x + acc[nt][e + 1] * kv.y;
+                    dka[i][nt][e] = acc[nt][e] * sgc[rr];
+                    dka[i][nt][e + 1] = acc[nt][e + 1] * sgc[rr];
+                }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float s = row_quad_sum(rs[hh]);
+                if ((lane & 3) == 0) pw_dgc[m0 + (lane >> 2) + 8 * hh] += s;
+            }
+        });
+        const Op o2[1] = {{dUs, kLdW, false, H0s, kLdW, true, kD}};
+        cta_mma<kC, kD>(o2, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    *reinterpret_cast<__half2 *>(dWs + rr * kLdW + cc) = __floats2half2_rn(-acc[nt][e], -acc[nt][e + 1]);
+                }
+        });
+    }
+    __syncthreads();
+    // ---- 6: dT = dU V^T Diag(beta) + dW K^T Diag(beta ge)  (into T Diag(beta)'s place)
+    {
+        const Op o1[1] = {{dUs, kLdW, false, Vs, kLdW, true, kD}};
+        const Op o2[1] = {{dWs, kLdW, false, Ks, kLdW, true, kD}};
+        float uv[2][2][4];
+        cta_mma<kC, kC>(o1, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) uv[i][nt][e] = acc[nt][e];
+        });
+        __syncthreads();   // T Diag(beta) (read by nothing now) is overwritten below
+        cta_mma<kC, kC>(o2, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    dTs[rr * kLdN + jj] =
+                        __float2half_rn(uv[i][nt][e] * sbeta[jj] + acc[nt][e] * sbeta[jj] * sge[jj]);
+                }
+        });
+    }
+    __syncthreads();
+    // ---- 7: X1 = T^T dT (into T Diag(beta ge)'s place), then dA = strict_tril(-X1 T^T),
+    //      E' = dA * Gamma (into dT's place), E = Diag(beta) E' (into X1's place)
+    {
+        const Op o1[1] = {{Ts, kLdN, true, dTs, kLdN, false, kC}};
+        cta_mma<kC, kC>(o1, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    X1s[rr * kLdN + jj] = __float2half_rn(acc[nt][e]);
+                }
+        });
+        __syncthreads();
+        float da[2][2][4];
+        const Op o2[1] = {{X1s, kLdN, false, Ts, kLdN, true, kC}};
+        cta_mma<kC, kC>(o2, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    da[i][nt][e] = jj < rr ? -acc[nt][e] * gam_of(rr, jj) : 0.f;
+                }
+        });
+        __syncthreads();   // X1 and dT are read: E and E' take their places
+        for (int i = 0; i < 2; ++i) {
+            const int2 og = tile_origin<kC, kC>(warp, i);
+            const int m0 = og.x, c0 = og.y;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    Eps[rr * kLdN + jj] = __float2half_rn(da[i][nt][e]);
+                    Es[rr * kLdN + jj] = __float2half_rn(da[i][nt][e] * sbeta[rr]);
+                }
+        }
+    }
+    __syncthreads();
+    // ---- 8: T^T dU -> dV = Diag(beta) T^T dU (and rowsum(V * T^T dU) into dbeta);
+    //      T^T dW -> dK part Diag(beta ge) T^T dW (and rowsum(K * T^T dW) into dbeta and dge)
+    {
+        const Op o1[1] = {{Ts, kLdN, true, dUs, kLdW, false, kC}};
+        cta_mma<kC, kD>(o1, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    const float2 vv = __half22float2(*reinterpret_cast<const __half2 *>(Vs + rr * kLdW + cc));
+                    rs[e >> 1] += acc[nt][e] * vv.x + acc[nt][e + 1] * vv.y;
+                    *reinterpret_cast<float2 *>(dVo + rr * kLdO + cc) =
+                        make_float2(acc[nt][e] * sbeta[rr], acc[nt][e + 1] * sbeta[rr]);
+                }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float s = row_quad_sum(rs[hh]);
+                if ((lane & 3) == 0) pw_db[m0 + (lane >> 2) + 8 * hh] += s;
+            }
+        });
+        const Op o2[1] = {{Ts, kLdN, true, dWs, kLdW, false, kC}};
+        cta_mma<kC, kD>(o2, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(Ks + rr * kLdW + cc));
+                    rs[e >> 1] += acc[nt][e] * kv.x + acc[nt][e + 1] * kv.y;
+                    dka[i][nt][e] += acc[nt][e] * sbge[rr];
+                    dka[i][nt][e + 1] += acc[nt][e + 1] * sbge[rr];
+                }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float s = row_quad_sum(rs[hh]);
+                if ((lane & 3) == 0) {
+                    const int rr = m0 + (lane >> 2) + 8 * hh;
+                    pw_db[rr] += sge[rr] * s;
+                    pw_dge[rr] += sbeta[rr] * s;
+                }
+            }
+        });
+    }
+    __syncthreads();
+    store_rows(dv_out, dVo, tok0, H, L, tid);
+    // ---- 9: dQ += F K; dK += E K + E^T K + F^T Q, with E = Diag(beta) E' (both terms of A's
+    //      gradient, A = strict_tril(Diag(beta) (K K^T * Gamma)), carry beta on the row side)
+    {
+        const Op o1[1] = {{Fs, kLdN, false, Ks, kLdW, false, kC}};
+        cta_mma<kC, kD>(o1, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dqa[i][nt][e] += acc[nt][e];
+        });
+        const Op o2[3] = {{Es, kLdN, false, Ks, kLdW, false, kC}, {Es, kLdN, true, Ks, kLdW, false, kC},
+                          {Fs, kLdN, true, Qs, kLdW, false, kC}};
+        cta_mma<kC, kD>(o2, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dka[i][nt][e] += acc[nt][e];
+        });
+    }
+    // dQ and dK rows of this chunk, staged (V, dW, dH' are read by nobody now) and stored whole
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int2 og = tile_origin<kC, kD>(warp, i);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const int rr = acc_row(lane, og.x, e), cc = acc_col(lane, og.y, nt, e);
+                *reinterpret_cast<float2 *>(dQo + rr * kLdO + cc) = make_float2(dqa[i][nt][e], dqa[i][nt][e + 1]);
+                *reinterpret_cast<float2 *>(dKo + rr * kLdO + cc) = make_float2(dka[i][nt][e], dka[i][nt][e + 1]);
+            }
+    }
+    __syncthreads();
+    store_rows(dq, dQo, tok0, H, L, tid);
+    store_rows(dk_out, dKo, tok0, H, L, tid);
+    // ---- 10: K K^T (kept), then Q K^T with, in its epilogue, R = Diag(beta) E' * K K^T + F * Q K^T:
+    //       dg += rowsum(R) - colsum(R), dbeta += rowsum(E' * K K^T)
+    {
+        float kk[2][2][4];
+        const Op o1[1] = {{Ks, kLdW, false, Ks, kLdW, true, kD}};
+        cta_mma<kC, kC>(o1, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kk[i][nt][e] = acc[nt][e];
+        });
+        const Op o2[1] = {{Qs, kLdW, false, Ks, kLdW, true, kD}};
+        cta_mma<kC, kC>(o2, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
+            float rsum[2] = {0.f, 0.f}, bsum[2] = {0.f, 0.f}, csum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    const float2 ep = __half22float2(*reinterpret_cast<const __half2 *>(Eps + rr * kLdN + jj));
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(Fs + rr * kLdN + jj));
+                    const float b0 = ep.x * kk[i][nt][e], b1 = ep.y * kk[i][nt][e + 1];
+                    const float r0 = sbeta[rr] * b0 + f.x * acc[nt][e], r1 = sbeta[rr] * b1 + f.y * acc[nt][e + 1];
+                    rsum[e >> 1] += r0 + r1;
+                    bsum[e >> 1] += b0 + b1;
+                    csum[nt][0] += r0;
+                    csum[nt][1] += r1;
+                }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float rs = row_quad_sum(rsum[hh]), bs = row_quad_sum(bsum[hh]);
+                if ((lane & 3) == 0) {
+                    const int rr = m0 + (lane >> 2) + 8 * hh;
+                    if (MODE == LDN_GDN) pw_dgr[rr] += rs;
+                    pw_db[rr] += bs;
+                }
+            }
+            if (MODE == LDN_GDN) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        float cs = csum[nt][x];
+                        cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+                        cs += __shfl_xor_sync(0xffffffffu, cs, 8);
+                        cs += __shfl_xor_sync(0xffffffffu, cs, 16);
+                        if (lane < 4) pw_dgk[c0 + 8 * nt + 2 * lane + x] -= cs;
+                    }
+            }
+        });
+    }
+    __syncthreads();
+    auto sum_warps = [&](const float *part, int rr) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) acc += part[w * kC + rr];
+        return acc;
+    };
+    if (warp == 0) {
+        // dbeta; dg per row, then the log-decay input's gradient = reverse cumulative sum
+        for (int rr = lane; rr < kC; rr += 32)
+            if (rr < L) dbeta[tok0 + (size_t)rr * H] = sum_warps(p_db, rr);
+        if (MODE == LDN_GDN) {
+            float hd = 0.f;
+            for (int i = 0; i < kWarps; ++i) hd += red[i];
+            const float gam = expf(sg[kC - 1]);
+            const int r0 = 2 * lane, r1 = r0 + 1;
+            const float c0 = sum_warps(p_dgc, r0), c1 = sum_warps(p_dgc, r1);
+            float d0 = sum_warps(p_dgr, r0) + sum_warps(p_dgk, r0) + sge[r0] * sum_warps(p_dge, r0) - sgc[r0] * c0;
+            float d1 = sum_warps(p_dgr, r1) + sum_warps(p_dgk, r1) + sge[r1] * sum_warps(p_dge, r1) - sgc[r1] * c1;
+            // the last row also carries gc's and gamma's dependence on g_last
+            float gcs = sgc[r0] * c0 + sgc[r1] * c1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) gcs += __shfl_xor_sync(0xffffffffu, gcs, o);
+            if (lane == 31) d1 += gcs + gam * hd;
+            // reverse cumulative sum over the 64 rows (two per lane)
+            float inc = d0 + d1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, inc, o);
+                if (lane + o < 32) inc += y;
+            }
+            // inc = sum over rows >= r0 of d; row r1's suffix = inc - d0
+            if (r0 < L) dgate[tok0 + (size_t)r0 * H] = inc;
+            if (r1 < L) dgate[tok0 + (size_t)r1 * H] = inc - d0;
+        }
+    }
+}
+
+}  // namespace
+
+bool bwd_chunk_supported(const BwdArgs &a)
+{
+    // q, k, v and dout are read as 16-byte rows (and through TMA descriptors by the forward pass)
+    const bool a16 = (((uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.dout) & 15u) == 0;
+    return a.dtype == LDN_BF16 && a.dk == kD && a.dv == kD && (a.mode == LDN_DELTANET || a.mode == LDN_GDN) && a16;
+}
+
+// Workspace: the solve's X (16 KB per (b, h, chunk)), the states entering every chunk and the
+// state gradients leaving every chunk (fp16 state images, 34 KB each), and the forward pass's
+// output (bf16).
+size_t bwd_chunk_workspace_bytes(int B, int T, int H)
+{
+    const size_t units = (size_t)B * H, nch = (size_t)(T + kC - 1) / kC;
+    return units * nch * (kXBytes + 2 * kStateImgBytes) + (size_t)B * T * H * kD * 2;
+}
+
+cudaError_t launch_backward_chunk(const BwdArgs &a, cudaStream_t s)
+{
+    const size_t units = (size_t)a.B * a.H, nch = (size_t)(a.T + kC - 1) / kC;
+    uint8_t *X = reinterpret_cast<uint8_t *>(a.ws);
+    __half *Hs = reinterpret_cast<__half *>(X + units * nch * kXBytes);
+    __half *dHs = Hs + units * nch * (kStateImgBytes / 2);
+    void *out = dHs + units * nch * (kStateImgBytes / 2);
+    // forward: the solve and the fused kernel with the chunk states
+    ChunkArgs f{a.q, a.k, a.v, a.beta, a.gate, a.S0, out, nullptr, a.B, a.T, a.H, kD, kD, kC, a.mode, a.dtype,
+                status_word_ptr()};
+    f.chunk_states = Hs;
+    if (!f.status) return cudaErrorInvalidValue;
+    cudaError_t e = launch_chunk_presolved(f, X, s);
+    if (e != cudaSuccess) return e;
+    auto k1 = a.mode == LDN_GDN ? bwd_chain_kernel<LDN_GDN> : bwd_chain_kernel<LDN_DELTANET>;
+    auto k2 = a.mode == LDN_GDN ? bwd_chunk_kernel<LDN_GDN> : bwd_chunk_kernel<LDN_DELTANET>;
+    if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, ChainSmem::bytes)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, ChunkSmem::bytes)) != cudaSuccess)
+        return e;
+    k1<<<(unsigned)(units * (kD / 64)), kThreads, ChainSmem::bytes, s>>>(
+        (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, a.beta, a.gate, (const __nv_bfloat16 *)a.dout,
+        a.dS_final, X, dHs, a.dS0, a.T, a.H, kD);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k2<<<(unsigned)(units * nch), kThreads, ChunkSmem::bytes, s>>>(
+        (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v, a.beta, a.gate,
+        (const __nv_bfloat16 *)a.dout, X, Hs, dHs, a.dq, a.dk_out, a.dv_out, a.dbeta, a.dgate, f.status, a.T, a.H);
+    return cudaGetLastError();
+}
+
+}  // namespace ldn

@@ -316,7 +316,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ beta,
                 const float *__restrict__ gate, const float *S0, __nv_bfloat16 *__restrict__ out,
                 float *S_final, int T, int H, int dv, int *status, uint8_t *__restrict__ ws, int cpr,
-                const float *__restrict__ erase, const float *__restrict__ write)
+                const float *__restrict__ erase, const float *__restrict__ write, __half *__restrict__ Hs)
 {
     extern __shared__ uint8_t dsmem[];
     // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
@@ -1744,6 +1744,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float gC = S.gC[gs];
             const bool top = st < 64;
             const float egc = top ? 0.f : S.egc[gs][st - 64];
+            // the state entering this chunk, for the chunkwise backward (row st of the slice, into
+            // the fp16 state image)
+            if (Hs) {
+                __half *dst = Hs + ((size_t)unit * nchunks + c) * (kStateImgBytes / 2) + st * kStateImgLd + n0;
+#pragma unroll
+                for (int n = 0; n < kDVS; n += 8) {
+                    __half2 h[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) h[x] = __floats2half2_rn(Hreg[n + 2 * x], Hreg[n + 2 * x + 1]);
+                    *reinterpret_cast<uint4 *>(dst + n) = *reinterpret_cast<const uint4 *>(h);
+                }
+            }
             // gate data of this chunk for S6, read now: the slot is released (rvfree) before S6
             const float gCr = kKda ? S.egC[gs][st] : gC;   // KDA: decay of key channel st
             // KDA: the side tile holds K e^{m-G} = K~ Diag(e^{m-G_C}) per channel, row st of D6
@@ -2013,7 +2025,7 @@ cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
-                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase, a.write);
+                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase, a.write, a.chunk_states);
         }
         if (PAIR) {   // clusters of the two dv slices of a (b, h): consecutive blocks
             cudaLaunchConfig_t cfg = {};
@@ -2029,11 +2041,11 @@ cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out,
-                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase, a.write);
+                                      a.S_final, a.T, a.H, a.dv, a.status, ws, cpr, a.erase, a.write, a.chunk_states);
         }
         kern<<<(unsigned)grid, PREPX ? kPrepThreads : kThreads, smem, st>>>(
             tq, tk, tv, a.beta, a.gate, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.dv, a.status, ws, cpr,
-            a.erase, a.write);
+            a.erase, a.write, a.chunk_states);
         return cudaGetLastError();
     };
     if (a.mode == LDN_GDN) return go(chunk_tc_kernel<LDN_GDN, KIND>, Layout<LDN_GDN, LK>::bytes);

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 #include <algorithm>
 
@@ -13,6 +14,12 @@ namespace ldn {
 // abandon a bounded wait.  It is a __device__ variable of api.cu (no
 // allocation); api.cu resolves its address per device and hands it to the
 // launchers, and ldn_get_device_status() reads and clears it.
+// State image of the chunkwise backward: per (b, h, chunk) a [128][kStateImgLd] fp16 tile (row
+// i = state row i, 128 values padded to 272 bytes), the layout its shared-memory tiles use, so
+// one bulk copy moves a state.
+constexpr int kStateImgLd = 136;
+constexpr size_t kStateImgBytes = 128 * kStateImgLd * 2;
+
 struct ChunkArgs {
     const void *q, *k, *v;
     const float *beta, *gate, *S0;
@@ -21,6 +28,9 @@ struct ChunkArgs {
     int B, T, H, dk, dv, chunk, mode, dtype;
     int *status;
     const float *erase = nullptr, *write = nullptr;   // Gated DeltaNet-2: b [B][T][H][dk], w [B][T][H][dv]
+    // Pre-solved tensor-core kernels (dk = dv = 128): when set, the state entering every chunk
+    // as the chunkwise backward's fp16 state image (kStateImgBytes per (b, h, chunk))
+    __half *chunk_states = nullptr;
 };
 
 struct DecodeArgs {
@@ -98,6 +108,11 @@ struct RlaArgs {
     int B, T, H, dk, dv, delta, dtype;
 };
 cudaError_t launch_rla(const RlaArgs &a, cudaStream_t stream);
+// Chunkwise backward on the tensor cores (csrc/backward_chunk.cu): DeltaNet / Gated DeltaNet,
+// bf16 inputs, dk = dv = 128, 16-byte aligned q, k, v, dout.
+bool bwd_chunk_supported(const BwdArgs &a);
+size_t bwd_chunk_workspace_bytes(int B, int T, int H);
+cudaError_t launch_backward_chunk(const BwdArgs &a, cudaStream_t stream);
 size_t bwd_ckpt_floats(int B, int T, int H, int dk, int dv);
 size_t bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int mode);
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t stream);

@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define LDN_VERSION 4
+#define LDN_VERSION 5
 
 /* LDN_GDN2 (Gated DeltaNet-2) is taken only by the *_gdn2 entry points, which
  * carry its two gates; every beta-gated entry point rejects it. */
@@ -338,12 +338,19 @@ int ldn_decode_step_gdn2(const void *q, const void *k, const void *v, const floa
 /*
  * ldn_backward -- gradients of the forward recurrence (modes DeltaNet, GDN,
  * KDA) for the loss L = sum_t <dout_t, o_t> + <dS_final, S_T>, with respect to
- * q, k, v, beta, the log-decay gates and the initial state.  It differentiates
- * the per-token rules of the linear-attention notes (Sec. 2.3-2.5) step by
- * step in reverse token order.  The states it needs are recomputed from copies
- * of every eighth state taken by a forward sweep (the benchmark's method
- * sources keep the whole state history for their KDA backward).  fp32
- * arithmetic; the result equals the exact gradient up to rounding.
+ * q, k, v, beta, the log-decay gates and the initial state.  The pages give the
+ * rules per token (linear-attention notes, Sec. 2.3-2.5) and a first-order
+ * backward keeping the state history (the benchmark's method sources, KDA).
+ * Two forms, both equal to the exact gradient up to rounding:
+ *   * chunkwise on the tensor cores, for bf16 DeltaNet and Gated DeltaNet at
+ *     dk = dv = 128: a forward pass that keeps the state entering every chunk of
+ *     64 tokens, the chain of state gradients from chunk to chunk in reverse,
+ *     then every chunk's gradients at once by dense products (fp16 operands,
+ *     fp32 accumulation; the chunk form of the derivative is derived in
+ *     csrc/backward_chunk.cu).  Every log-decay must be <= 0 for its operands
+ *     to stay in fp16 range.  Four launches;
+ *   * otherwise the per-token rules stepped back in reverse token order, in fp32,
+ *     from copies of every eighth state taken by a forward sweep.  Three launches.
  *
  *   q, k, v, beta, gate, S0, B, T, H, dk, dv, mode, dtype as ldn_chunk_fwd
  *   (mode LDN_GDN2 is not taken: LDN_ERR_INVALID_ARG)
@@ -352,23 +359,25 @@ int ldn_decode_step_gdn2(const void *q, const void *k, const void *v, const floa
  *   dq, dk    [B][T][H][dk]            dv    [B][T][H][dv]      dbeta [B][T][H]
  *   dgate     the gate's shape (mode DELTANET: ignored, may be NULL)
  *   dS0       [B][H][dk][dv] (the gradient at S0, or at the zero state when S0 is NULL)
- *   workspace device memory, 16-byte aligned, at least
- *             ldn_backward_workspace_size(B, T, H, dk, dv, mode) bytes (state
- *             copies, then per-32-column partial sums of the dk-side
- *             gradients); contents on entry do not matter.
- * Alignment: q, k, v, dout to their element size; every fp32 array 4-byte.
- * T = 0 writes dS0 = dS_final (or zeros) and nothing else.  Asynchronous on
- * `stream`: three kernel launches (the forward sweep that stores the state
- * copies, the reverse sweep, the sum over the dv slices).
+ *   workspace device memory, at least ldn_backward_workspace_size(B, T, H, dk,
+ *             dv, mode, dtype) bytes, 256-byte aligned for the chunkwise form
+ *             (the forward's per-chunk states and solve, the state gradients)
+ *             and 16-byte aligned otherwise (state copies, then per-32-column
+ *             partial sums of the dk-side gradients); contents on entry do not
+ *             matter.
+ * Alignment: q, k, v, dout to their element size and every fp32 array 4-byte;
+ * the chunkwise form also wants q, k, v, dout, dq, dk, dv 16-byte aligned
+ * (else LDN_ERR_INVALID_ARG).  T = 0 writes dS0 = dS_final (or zeros) and
+ * nothing else.  Asynchronous on `stream`.
  */
 int ldn_backward(const void *q, const void *k, const void *v, const float *beta, const float *gate,
                  const float *S0, const void *dout, const float *dS_final, float *dq, float *dk, float *dv,
                  float *dbeta, float *dgate, float *dS0, int B, int T, int H, int dk_dim, int dv_dim, int mode,
                  int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace ldn_backward needs, or 0 for arguments it rejects.  Pure
- * host function. */
-size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode);
+/* Bytes of workspace ldn_backward needs for these sizes and dtype, or 0 for
+ * arguments it rejects.  Pure host function. */
+size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode, int dtype);
 
 /*
  * ldn_rla_fwd -- Residual Linear Attention (delta = 0) or Residual DeltaNet

@@ -51,7 +51,7 @@ def test_diagnostics_live_in_their_own_library(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert ldn.ldn_version() == 4
+    assert ldn.ldn_version() == 5
     for st in range(5):
         assert isinstance(ldn.ldn_status_string(st), str) and ldn.ldn_status_string(st)
     assert "unknown" in ldn.ldn_status_string(99)
@@ -400,16 +400,39 @@ def test_backward_rejects_bad_arguments(lib, kw, want):
     assert _bwd(**kw) == want
 
 
+def test_chunkwise_backward_wants_aligned_tensors_and_its_workspace(lib):
+    """bf16 Gated DeltaNet at dk = dv = 128 takes the chunkwise backward: 16-byte aligned
+    tensors, a 256-byte aligned workspace of its size; anything less is refused before any
+    CUDA call."""
+    need = ldn.ldn_backward_workspace_size(1, 64, 1, 128, 128, 1, ldn.LDN_BF16)
+    base = dict(dkd=128, dvd=128, dtype=ldn.LDN_BF16, wsb=need)
+    assert _bwd(q=FAKE + 2, **base) == ldn.LDN_ERR_INVALID_ARG
+    assert _bwd(dk=FAKE + 4, **base) == ldn.LDN_ERR_INVALID_ARG
+    assert _bwd(ws=FAKE + 16, **base) == ldn.LDN_ERR_INVALID_ARG
+    assert _bwd(**dict(base, wsb=need - 1)) == ldn.LDN_ERR_INVALID_ARG
+
+
 def test_backward_workspace_size(lib):
-    """State copies (every eighth state of every column) plus per-32-column partial
-    sums of dq, dk, the gate gradient and dbeta."""
+    """Recurrent form: state copies (every eighth state of every column) plus
+    per-32-column partial sums of dq, dk, the gate gradient and dbeta.  Chunkwise form
+    (bf16 DeltaNet / GDN, dk = dv = 128): the solve X (16 KiB per chunk), the states
+    entering and the state gradients leaving every chunk (fp16 images of 128 x 136), the
+    forward's output."""
     B, T, H, dk, dv = 2, 70, 3, 128, 64
     n, nsub, sl = B * T * H, (T + 7) // 8, dv // 32
-    for mode, gw in ((0, 0), (1, 1), (2, dk)):
-        want = 4 * (B * H * dv * nsub * dk + sl * n * (2 * dk + gw + 1))
-        assert ldn.ldn_backward_workspace_size(B, T, H, dk, dv, mode) == want
-    assert ldn.ldn_backward_workspace_size(B, T, H, 96, dv, 1) == 0
-    assert ldn.ldn_backward_workspace_size(B, T, H, dk, dv, ldn.LDN_GDN2) == 0
+    for dtype in (ldn.LDN_F32, ldn.LDN_BF16):
+        for mode, gw in ((0, 0), (1, 1), (2, dk)):
+            want = 4 * (B * H * dv * nsub * dk + sl * n * (2 * dk + gw + 1))
+            assert ldn.ldn_backward_workspace_size(B, T, H, dk, dv, mode, dtype) == want
+    nch = (T + 63) // 64
+    chunked = B * H * nch * (16384 + 2 * 128 * 136 * 2) + n * 128 * 2
+    for mode in (0, 1):
+        assert ldn.ldn_backward_workspace_size(B, T, H, 128, 128, mode, ldn.LDN_BF16) == chunked
+    n, nsub, sl = B * T * H, (T + 7) // 8, 128 // 32
+    assert ldn.ldn_backward_workspace_size(B, T, H, 128, 128, 2, ldn.LDN_BF16) == \
+        4 * (B * H * 128 * nsub * 128 + sl * n * (2 * 128 + 128 + 1))   # KDA: recurrent
+    assert ldn.ldn_backward_workspace_size(B, T, H, 96, dv, 1, 1) == 0
+    assert ldn.ldn_backward_workspace_size(B, T, H, dk, dv, ldn.LDN_GDN2, 1) == 0
 
 
 def _rla(**kw):

@@ -1,11 +1,15 @@
 """GPU parity of ldn_backward (gradients of sum <dout, o> + <dS_final, S_T>)
 against the fp64 backward oracle, element by element.
 
-Tolerance from the arithmetic: the kernel runs the recurrence and its adjoint
-in fp32 (a relative rounding of ~6e-8 per operation, accumulated over the
-sequence and over the sums of up to dv columns), so every gradient must agree
-to 1e-4 of its RMS; the decay-gate gradient, a sum over a full state of
-products whose terms cancel, to 1e-3."""
+Tolerances from the arithmetic.  Recurrent form (fp32 inputs, KDA, and dims
+other than 128 x 128): the kernel runs the recurrence and its adjoint in fp32
+(a relative rounding of ~6e-8 per operation, accumulated over the sequence and
+over the sums of up to dv columns), so every gradient must agree to 1e-4 of its
+RMS; the decay-gate gradient, a sum over a full state of products whose terms
+cancel, to 1e-3.  Chunkwise form (bf16 DeltaNet / Gated DeltaNet, dk = dv =
+128): its products take fp16 operands (2^-11 relative) with fp32 accumulation,
+the precision class of the bf16 forward, so the bf16 target 2e-2 applies
+(measured: below 1e-2)."""
 import numpy as np
 import pytest
 
@@ -18,6 +22,16 @@ pytestmark = pytest.mark.gpu
 
 BASE = {0: "deltanet_fp32_b1_t256_h1_d64", 1: "gdn_bf16_b4_t2048_h16_d128", 2: "kda_bf16_b8_t4096_h16_d128"}
 TOL = {"dq": 1e-4, "dk": 1e-4, "dv": 1e-4, "dbeta": 1e-4, "dgate": 1e-3, "dS0": 1e-4}
+TOL_CHUNKWISE = 2e-2
+
+
+def chunkwise(w) -> bool:
+    """The shapes ldn_backward runs in chunk form."""
+    return w.dtype == "bf16" and w.dk == 128 and w.dv == 128 and w.mode in (0, 1)
+
+
+def tol(w, gname) -> float:
+    return TOL_CHUNKWISE if chunkwise(w) else TOL[gname]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -46,7 +60,7 @@ def check(w, dout, dsf, S0=True, sel=None):
             assert got[name] is None
             continue
         e = rel_err(got[name], r)
-        assert e <= TOL[name], f"{name}: {e:.3g} (mode {w.mode}, {w.dtype}, T={w.T})"
+        assert e <= tol(w, name), f"{name}: {e:.3g} (mode {w.mode}, {w.dtype}, T={w.T})"
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
@@ -102,4 +116,4 @@ def test_backward_full_workload_sampled(name, pairs):
                 continue
             gv = got[gname][b:b + 1, h:h + 1] if gname == "dS0" else got[gname][b:b + 1, :, h:h + 1]
             e = rel_err(gv, r)
-            assert e <= TOL[gname], f"{name} ({b},{h}) {gname}: {e:.3g}"
+            assert e <= tol(w, gname), f"{name} ({b},{h}) {gname}: {e:.3g}"
