@@ -609,9 +609,10 @@ def run_ours(args):
             gv, gb = torch.empty((B_, T_, H_, dv_), **f32), torch.empty((B_, T_, H_), **f32)
             gg = torch.empty(tuple(bt["gate"].shape), **f32)
             gs0 = torch.empty((B_, H_, dk_, dv_), **f32)
-            need = ldn.ldn_backward_workspace_size(B_, T_, H_, dk_, dv_, bw.mode)
-            bws = torch.empty(need, dtype=torch.uint8, device="cuda")
             bdt = ldn.LDN_BF16 if bw.dtype == "bf16" else ldn.LDN_F32
+            need = ldn.ldn_backward_workspace_size(B_, T_, H_, dk_, dv_, bw.mode, bdt)
+            bws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            chunked = bdt == ldn.LDN_BF16 and dk_ == 128 and dv_ == 128 and bw.mode in (0, 1)
 
             def bstep():
                 st_ = ldn.ldn_backward(P(bt["q"]), P(bt["k"]), P(bt["v"]), P(bt["beta"]), P(bt["gate"]), P(bt["S0"]),
@@ -628,12 +629,16 @@ def run_ours(args):
                 bstep()
                 e1.record(stream)
             barrier()
-            launches += 3 * (1 + len(bev))
+            launches += (4 if chunked else 3) * (1 + len(bev))
             bms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in bev))
             bb = backward_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(bw.dtype), bw.mode)
+            kernels = ("chunk_tc_kernel<prep-X> + chunk_tc_kernel<fed> (forward with chunk states) + "
+                       "bwd_chain_kernel + bwd_chunk_kernel" if chunked else
+                       "bwd_kernel<phase 1> + bwd_kernel<phase 2> + bwd_reduce_kernel")
             backward[name] = {"ms_per_call": bms, "tokens_per_s": world * B_ * T_ / (bms / 1e3),
-                              "kernels": "bwd_kernel<phase 1> + bwd_kernel<phase 2> + bwd_reduce_kernel", "algorithmic_bytes": bb,
-                              "hbm_frac": bb / (bms / 1e3) / 1e9 / hbm_peak, "workspace_bytes": need}
+                              "form": "chunkwise" if chunked else "recurrent", "kernels": kernels,
+                              "algorithmic_bytes": bb, "hbm_frac": bb / (bms / 1e3) / 1e9 / hbm_peak,
+                              "workspace_bytes": need}
             del bt, bdo, bdsf, gq, gk, gv, gb, gg, gs0, bws
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("backward: device status not ok")

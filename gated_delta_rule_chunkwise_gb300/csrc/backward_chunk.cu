@@ -27,12 +27,14 @@
 // (Padded rows past the end of the sequence are zero and carry no decay.)
 //
 // The backward is three steps after a forward pass that stores the state entering every
-// chunk (the fused / pre-solved forward kernels with chunk_states) and X = [P T ; T] of every
-// chunk (the pre-solved variant's solve, whose rows 64..127 are T):
-//   1. bwd_chain_kernel: one CTA per (b, h, 64-wide slice of dv) walks the chunks in reverse
-//      and carries dH in fp32; it stores the dH' of every chunk.
-//   2. bwd_chunk_kernel: one CTA per (b, h, chunk), all in parallel, forms every gradient of
-//      the chunk from its inputs, T, H0 and dH'.
+// chunk (the pre-solved forward kernel with chunk_states) and X = [P T ; T] of every chunk
+// (the pre-solved variant's solve, whose rows 64..127 are T):
+//   1. bwd_prep_kernel: one CTA per (b, h, chunk), all in parallel, forms P, -W and the two
+//      chain-independent terms of the state gradient's recursion, dH0 = M dH' + Bc.
+//   2. bwd_chain_kernel: one CTA per (b, h, 64-wide slice of dv) walks the chunks in reverse,
+//      one product per chunk, and carries dH in fp32; it stores the dH' of every chunk.
+//   3. bwd_chunk_kernel: one CTA per (b, h, chunk), all in parallel, forms every gradient of
+//      the chunk from its inputs, T, P, -W, H0 and dH'.
 // Arithmetic: products on fp16 operands (2^-11) with fp32 accumulation; states, gradients and
 // every elementwise step in fp32.  Operands stay in fp16 range when the log-decays are not
 // positive (every Gamma, ge, gc <= 1).
@@ -199,15 +201,16 @@ __device__ __forceinline__ void store_rows(float *__restrict__ dst, const float 
     }
 }
 
-// T of a chunk from the solve's X image (rows 64..127, 128-byte swizzled K-major fp16: the
-// 16-byte group p of row `row` holds columns 8 ((p ^ row) & 7) ..), as fp16 tiles of stride
-// kLdN: T itself (optional), T Diag(s1) and (optional) T Diag(s2), s1 / s2 per column.
-__device__ __forceinline__ void load_t(const uint8_t *X, __half *t, __half *t1, const float *s1, __half *t2,
+// T of a chunk from the rows 64..127 of the solve's X image (128-byte swizzled K-major fp16:
+// the 16-byte group p of row `row` holds columns 8 ((p ^ row) & 7) ..), copied raw to shared
+// memory, as fp16 tiles of stride kLdN: T itself (optional), T Diag(s1) and (optional)
+// T Diag(s2), s1 / s2 per column.
+__device__ __forceinline__ void load_t(const uint8_t *Xt, __half *t, __half *t1, const float *s1, __half *t2,
                                        const float *s2, int tid)
 {
     uint4 u[kC * 8 / kThreads];
 #pragma unroll
-    for (int i = 0; i < kC * 8 / kThreads; ++i) u[i] = __ldg(reinterpret_cast<const uint4 *>(X + 8192) + tid + kThreads * i);
+    for (int i = 0; i < kC * 8 / kThreads; ++i) u[i] = reinterpret_cast<const uint4 *>(Xt)[tid + kThreads * i];
 #pragma unroll
     for (int i = 0; i < kC * 8 / kThreads; ++i) {
         const int e = tid + kThreads * i, j = e >> 3, c8 = 8 * (((e & 7) ^ (64 + j)) & 7);
@@ -249,82 +252,216 @@ __device__ __forceinline__ void chunk_gates(const float *__restrict__ beta, cons
 }
 
 // =====================================================================================
-// Kernel 1: the chain dH0 = gamma dH' + Q^T Diag(ge) dO - W^T (Diag(gc) K dH' + P^T dO),
-// chunks in reverse, one CTA per (b, h, 64-wide slice of dv), dH in fp32 registers (the
-// warp owns the same 16 x 16 tiles of the 128 x 64 state in every chunk).  The fp16 state
-// image dHs[c] receives the dH' of chunk c (the gradient at the state it leaves); dS0 the
-// gradient at S0.
-struct ChainSmem {
-    static constexpr int q = 0;                                   // Q [64][136] fp16
-    static constexpr int k = q + kC * kLdW * 2;                   // K [64][136]
-    static constexpr int tk = k + kC * kLdW * 2;                  // T Diag(beta ge) [64][72]
-    static constexpr int p = tk + kC * kLdN * 2;                  // P [64][72]
-    static constexpr int w = p + kC * kLdN * 2;                   // W [64][136]
-    static constexpr int dO = w + kC * kLdW * 2;                  // Diag(ge) dO slice [64][72]
-    static constexpr int dOr = dO + kC * kLdN * 2;                // dO slice [64][72]
-    static constexpr int du = dOr + kC * kLdN * 2;                // dU [64][72]
-    static constexpr int dh = du + kC * kLdN * 2;                 // dH' fp16 [128][72]
-    static constexpr int small = dh + kD * kLdN * 2;              // beta, g, ge, gc, beta ge
-    // staging of the next chunk's inputs (cp.async): q, k rows (bf16 [64][128]), the dO
-    // slice (bf16 [64][64]), T (X rows 64..127, swizzled fp16 [64][64]), beta and gate
-    static constexpr int sq = small + 5 * kC * 4;
-    static constexpr int sk = sq + kC * kD * 2;
-    static constexpr int sdo = sk + kC * kD * 2;
-    static constexpr int st = sdo + kC * 64 * 2;
-    static constexpr int sb = st + kC * kC * 2;
-    static constexpr int sgt = sb + kC * 4;
-    static constexpr int bytes = sgt + kC * 4;
-    static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
+// Kernel 1: the chain-independent products of every chunk, one CTA per (b, h, chunk), all in
+// parallel.  The reverse chain of the state gradient,
+//   dH0 = gamma dH' + Q^T Diag(ge) dO - W^T dU,   dU = Diag(gc) K dH' + P^T dO,
+// is affine in dH':  dH0 = M dH' + Bc with
+//   M  = gamma I - W^T Diag(gc) K        [dk x dk],
+//   Bc = (Diag(ge) Q - P W)^T dO         [dk x dv]   (Diag(ge) Q - P W is the forward's Q~),
+// so the serial pass is one product per chunk.  Stored per chunk as fp16 images laid out as
+// their consumers' shared-memory tiles: P [64][72] and -W [64][136] (the per-chunk kernel's
+// operands), M and Bc [128][136] (the chain's).
+constexpr size_t kPImg = kC * kLdN * 2;      // 9216 B
+constexpr size_t kWImg = kC * kLdW * 2;      // 17408 B
+constexpr size_t kMImg = kStateImgBytes;     // 34816 B, also Bc's
+
+struct PrepSmem {
+    static constexpr int q = 0;                       // Q, then Q~ [64][136] fp16
+    static constexpr int k = q + kC * kLdW * 2;       // K, then Diag(gc) K
+    static constexpr int dO = k + kC * kLdW * 2;      // dO
+    static constexpr int tk = dO + kC * kLdW * 2;     // T Diag(beta ge) [64][72]
+    static constexpr int p = tk + kC * kLdN * 2;      // T's raw rows, then P [64][72]
+    static constexpr int w = p + kC * kLdN * 2;       // W [64][136]
+    static constexpr int small = w + kC * kLdW * 2;   // beta, g, ge, gc, beta ge
+    static constexpr int bytes = small + 5 * kC * 4;
+    static_assert(2 * bytes <= 232448, "two CTAs per SM");
 };
 
-// Stage chunk c's inputs for the chain (16-byte cp.async; rows past the sequence read as zero).
-__device__ __forceinline__ void chain_prefetch(uint8_t *smc, const __nv_bfloat16 *__restrict__ q,
-                                               const __nv_bfloat16 *__restrict__ k, const float *__restrict__ beta,
-                                               const float *__restrict__ gate, const __nv_bfloat16 *__restrict__ dout,
-                                               const uint8_t *__restrict__ Xc, size_t tok0, int H, int L, int dv,
-                                               int n0, int tid)
-{
-    using SM = ChainSmem;
-    for (int e = tid; e < 2 * kC * 16; e += kThreads) {   // q, k: 16 groups per row
-        const int which = e / (kC * 16), rr = (e / 16) % kC, part = e % 16;
-        const __nv_bfloat16 *src = (which ? k : q) + (tok0 + (size_t)(rr < L ? rr : 0) * H) * kD + 8 * part;
-        cp_async16(smc + (which ? SM::sk : SM::sq) + (rr * 16 + part) * 16, src, rr < L ? 16u : 0u);
-    }
-    for (int e = tid; e < kC * 8; e += kThreads) {        // dO slice: 8 groups per row; T: 8 per row
-        const int rr = e >> 3, part = e & 7;
-        const __nv_bfloat16 *src = dout + (tok0 + (size_t)(rr < L ? rr : 0) * H) * dv + n0 + 8 * part;
-        cp_async16(smc + SM::sdo + e * 16, src, rr < L ? 16u : 0u);
-        cp_async16(smc + SM::st + e * 16, Xc + 8192 + e * 16, 16u);
-    }
-    if (tid < kC) {
-        const int rr = tid;
-        cp_async4(smc + SM::sb + 4 * rr, beta + tok0 + (size_t)(rr < L ? rr : 0) * H, rr < L ? 4u : 0u);
-        if (gate) cp_async4(smc + SM::sgt + 4 * rr, gate + tok0 + (size_t)(rr < L ? rr : 0) * H, rr < L ? 4u : 0u);
-    }
-    cp_async_commit();
-}
-
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-bwd_chain_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                 const float *__restrict__ beta, const float *__restrict__ gate,
-                 const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ dS_final,
-                 const uint8_t *__restrict__ X, __half *__restrict__ dHs, float *__restrict__ dS0, int T, int H, int dv)
+__global__ void __launch_bounds__(kThreads, 2)
+bwd_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                const float *__restrict__ beta, const float *__restrict__ gate,
+                const __nv_bfloat16 *__restrict__ dout, const uint8_t *__restrict__ X, __half *__restrict__ Pimg,
+                __half *__restrict__ Wimg, __half *__restrict__ Mimg, __half *__restrict__ Bimg, int T, int H)
 {
-    extern __shared__ __align__(16) uint8_t smc[];
-    using SM = ChainSmem;
-    __half *Qs = reinterpret_cast<__half *>(smc + SM::q), *Ks = reinterpret_cast<__half *>(smc + SM::k);
-    __half *TKs = reinterpret_cast<__half *>(smc + SM::tk), *Ps = reinterpret_cast<__half *>(smc + SM::p);
-    __half *Ws = reinterpret_cast<__half *>(smc + SM::w), *dOs = reinterpret_cast<__half *>(smc + SM::dO);
-    __half *dOr = reinterpret_cast<__half *>(smc + SM::dOr), *dUs = reinterpret_cast<__half *>(smc + SM::du);
-    __half *dHh = reinterpret_cast<__half *>(smc + SM::dh);
-    float *sbeta = reinterpret_cast<float *>(smc + SM::small), *sg = sbeta + kC, *sge = sg + kC, *sgc = sge + kC;
+    extern __shared__ __align__(16) uint8_t smp[];
+    using SM = PrepSmem;
+    __half *Qs = reinterpret_cast<__half *>(smp + SM::q), *Ks = reinterpret_cast<__half *>(smp + SM::k);
+    __half *dOs = reinterpret_cast<__half *>(smp + SM::dO), *TKs = reinterpret_cast<__half *>(smp + SM::tk);
+    __half *Ps = reinterpret_cast<__half *>(smp + SM::p), *Ws = reinterpret_cast<__half *>(smp + SM::w);
+    float *sbeta = reinterpret_cast<float *>(smp + SM::small), *sg = sbeta + kC, *sge = sg + kC, *sgc = sge + kC;
     float *sbge = sgc + kC;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slices = dv / 64, unit = blockIdx.x / slices, n0 = (blockIdx.x % slices) * 64;
-    const int b = unit / H, h = unit % H;
     const int nch = (T + kC - 1) / kC;
+    const size_t chunk = blockIdx.x;
+    const int unit = blockIdx.x / nch, c = blockIdx.x % nch;
+    const int b = unit / H, h = unit % H;
+    const int t0 = c * kC, L = min(kC, T - t0);
+    const size_t tok0 = ((size_t)b * T + t0) * H + h;
+
+    // ---- 0: T's rows of X (raw, into P's place, cp.async); q, k, dO rows to fp16; gates
+    for (int e = tid; e < kC * 8; e += kThreads)
+        cp_async16(Ps + 8 * e, X + chunk * kXBytes + 8192 + 16 * e, 16u);
+    cp_async_commit();
+    {
+        const __nv_bfloat16 *const src[3] = {q, k, dout};
+        __half *const dst[3] = {Qs, Ks, dOs};
+        load_tiles_f16<3>(src, dst, tok0, H, L, tid);
+    }
+    if (warp == 0) chunk_gates<MODE>(beta, gate, tok0, H, L, lane, sbeta, sg);
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int rr = tid; rr < kC; rr += kThreads) {
+        const float gl = sg[kC - 1];
+        sge[rr] = MODE == LDN_GDN ? expf(sg[rr]) : 1.f;
+        sgc[rr] = MODE == LDN_GDN ? expf(gl - sg[rr]) : 1.f;
+        sbge[rr] = sbeta[rr] * sge[rr];
+    }
+    __syncthreads();
+    load_t(reinterpret_cast<const uint8_t *>(Ps), nullptr, TKs, sbge, nullptr, nullptr, tid);
+    __syncthreads();
+    // ---- 1: P = tril(Q K^T * Gamma); W = T Diag(beta ge) K
+    {
+        const Op op[1] = {{Qs, kLdW, false, Ks, kLdW, true, kD}};
+        cta_mma<kC, kC>(op, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
+                    const float gm = MODE == LDN_GDN ? expf(sg[rr] - sg[jj]) : 1.f;
+                    Ps[rr * kLdN + jj] = __float2half_rn(jj <= rr ? acc[nt][e] * gm : 0.f);
+                }
+        });
+        const Op ow[1] = {{TKs, kLdN, false, Ks, kLdW, false, kC}};
+        cta_mma<kC, kD>(ow, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    *reinterpret_cast<__half2 *>(Ws + rr * kLdW + cc) = __floats2half2_rn(acc[nt][e], acc[nt][e + 1]);
+                }
+        });
+    }
+    __syncthreads();
+    // ---- 2: the P and -W images; Q~ = Diag(ge) Q - P W (in Q's place); Diag(gc) K (in K's place)
+    {
+        const uint4 *ps = reinterpret_cast<const uint4 *>(Ps);
+        uint4 *pd = reinterpret_cast<uint4 *>(Pimg + chunk * (kPImg / 2));
+        for (int e = tid; e < (int)(kPImg / 16); e += kThreads) pd[e] = ps[e];
+        const uint4 *ws = reinterpret_cast<const uint4 *>(Ws);
+        uint4 *wd = reinterpret_cast<uint4 *>(Wimg + chunk * (kWImg / 2));
+        for (int e = tid; e < (int)(kWImg / 16); e += kThreads) {
+            uint4 u = ws[e];
+            u.x ^= 0x80008000u;   // fp16 sign bits: -W
+            u.y ^= 0x80008000u;
+            u.z ^= 0x80008000u;
+            u.w ^= 0x80008000u;
+            wd[e] = u;
+        }
+        const Op o1[1] = {{Ps, kLdN, false, Ws, kLdW, false, kC}};
+        cta_mma<kC, kD>(o1, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    __half2 *qp = reinterpret_cast<__half2 *>(Qs + rr * kLdW + cc);
+                    const float2 qv = __half22float2(*qp);
+                    *qp = __floats2half2_rn(sge[rr] * qv.x - acc[nt][e], sge[rr] * qv.y - acc[nt][e + 1]);
+                }
+        });
+        if (MODE == LDN_GDN)
+            for (int e = tid; e < kC * 16; e += kThreads) {
+                const int rr = e >> 4, part = e & 15;
+                uint4 *kp = reinterpret_cast<uint4 *>(Ks + rr * kLdW + 8 * part);
+                uint4 u = *kp;
+                __half2 *h2 = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float2 f = __half22float2(h2[x]);
+                    h2[x] = __floats2half2_rn(f.x * sgc[rr], f.y * sgc[rr]);
+                }
+                *kp = u;
+            }
+    }
+    __syncthreads();
+    // ---- 3: Bc = Q~^T dO and M = gamma I - W^T Diag(gc) K, each in two 128 x 64 halves staged
+    //      in the place of T Diag(beta ge) and P (read by nobody now; one [128][72] tile) and
+    //      copied to the images as 16-byte row pieces
+    const float gam = MODE == LDN_GDN ? expf(sg[kC - 1]) : 1.f;
+    __half *stg = TKs;
+    static_assert(PrepSmem::p - PrepSmem::tk == kC * kLdN * 2 && 2 * kC * kLdN == kD * kLdN, "staging tile");
+#pragma unroll 1
+    for (int x = 0; x < 4; ++x) {
+        const int hv = x & 1;
+        const bool is_m = x >= 2;
+        __half *img = (is_m ? Mimg : Bimg) + chunk * (kMImg / 2) + 64 * hv;
+        const Op ob[1] = {{Qs, kLdW, true, dOs + 64 * hv, kLdW, false, kC}};
+        const Op om[1] = {{Ws, kLdW, true, Ks + 64 * hv, kLdW, false, kC}};
+        cta_mma<kD, 64>(is_m ? om : ob, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e), gc = cc + 64 * hv;
+                    const float d0 = is_m && rr == gc ? gam : 0.f, d1 = is_m && rr == gc + 1 ? gam : 0.f;
+                    *reinterpret_cast<__half2 *>(stg + rr * kLdN + cc) =
+                        is_m ? __floats2half2_rn(d0 - acc[nt][e], d1 - acc[nt][e + 1])
+                             : __floats2half2_rn(acc[nt][e], acc[nt][e + 1]);
+                }
+        });
+        __syncthreads();
+#pragma unroll
+        for (int e = tid; e < kD * 8; e += kThreads)
+            *reinterpret_cast<uint4 *>(img + (e >> 3) * kStateImgLd + 8 * (e & 7)) =
+                *reinterpret_cast<const uint4 *>(stg + (e >> 3) * kLdN + 8 * (e & 7));
+        __syncthreads();
+    }
+}
+
+// =====================================================================================
+// Kernel 2: the chain dH0 = M dH' + Bc, chunks in reverse, one CTA per (b, h, 64-wide slice
+// of dv), dH in fp32 registers (the warp owns the same 16 x 16 tiles of the 128 x 64 slice
+// in every chunk); M and the Bc slice of the next chunk load by cp.async under the current
+// product.  The fp16 state image dHs[c] receives the dH' of chunk c (the gradient at the
+// state it leaves); dS0 the gradient at S0.
+struct ChainSmem {
+    static constexpr int m = 0;                         // M [2][128][136] fp16 (double buffer)
+    static constexpr int bc = m + 2 * kD * kLdW * 2;    // Bc slice [2][128][72]
+    static constexpr int dh = bc + 2 * kD * kLdN * 2;   // dH' slice [128][72]
+    static constexpr int bytes = dh + kD * kLdN * 2;
+};
+
+__device__ __forceinline__ void chain_prefetch(uint8_t *smc, int buf, const __half *__restrict__ Mimg,
+                                               const __half *__restrict__ Bimg, size_t chunk, int n0, int tid)
+{
+    using SM = ChainSmem;
+    const uint8_t *ms = reinterpret_cast<const uint8_t *>(Mimg + chunk * (kMImg / 2));
+    uint8_t *md = smc + SM::m + buf * (kD * kLdW * 2);
+    for (int e = tid; e < (int)(kMImg / 16); e += kThreads) cp_async16(md + 16 * e, ms + 16 * e, 16u);
+    const __half *bs = Bimg + chunk * (kMImg / 2) + n0;
+    __half *bd = reinterpret_cast<__half *>(smc + SM::bc + buf * (kD * kLdN * 2));
+    for (int e = tid; e < kD * 8; e += kThreads)
+        cp_async16(bd + (e >> 3) * kLdN + 8 * (e & 7), bs + (e >> 3) * kStateImgLd + 8 * (e & 7), 16u);
+    cp_async_commit();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_chain_kernel(const __half *__restrict__ Mimg, const __half *__restrict__ Bimg,
+                 const float *__restrict__ dS_final, __half *__restrict__ dHs, float *__restrict__ dS0, int T,
+                 int H, int dv)
+{
+    extern __shared__ __align__(16) uint8_t smc[];
+    using SM = ChainSmem;
+    __half *dHh = reinterpret_cast<__half *>(smc + SM::dh);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slices = dv / 64, unit = blockIdx.x / slices, n0 = (blockIdx.x % slices) * 64;
+    const int nch = (T + kC - 1) / kC;
+    (void)H;
 
     // dH' of the last chunk: dS_final (or zero); tile i of this warp: rows / columns of the
     // accumulator layout (M = 128 dk rows, N = 64 columns: 32 tiles, 4 per warp)
@@ -332,67 +469,38 @@ bwd_chain_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int2 og = tile_origin<kD, 64>(warp, i);
-        const int m0 = og.x, c0 = og.y;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                const int rr = acc_row(lane, og.x, e), cc = acc_col(lane, og.y, nt, e);
                 dh[i][nt][e] = dS_final ? dS_final[((size_t)unit * kD + rr) * dv + n0 + cc] : 0.f;
             }
     }
-    auto tok_of = [&](int c) { return ((size_t)b * T + (size_t)c * kC) * H + h; };
-    chain_prefetch(smc, q, k, beta, gate, dout, X + ((size_t)unit * nch + nch - 1) * kXBytes, tok_of(nch - 1), H,
-                   min(kC, T - (nch - 1) * kC), dv, n0, tid);
+    chain_prefetch(smc, (nch - 1) & 1, Mimg, Bimg, (size_t)unit * nch + nch - 1, n0, tid);
     for (int c = nch - 1; c >= 0; --c) {
-        cp_async_wait<0>();
-        __syncthreads();
-        // ---- the staged inputs to fp16 tiles; gates (warp 0); dH' (fp32 out, fp16 copy)
-        for (int e = tid; e < 2 * kC * 16; e += kThreads) {
-            const int which = e / (kC * 16), rr = (e / 16) % kC, part = e % 16;
-            const uint4 u = *reinterpret_cast<const uint4 *>(smc + (which ? SM::sk : SM::sq) + (rr * 16 + part) * 16);
-            *reinterpret_cast<uint4 *>((which ? Ks : Qs) + rr * kLdW + 8 * part) = bf16x8_to_f16(u);
-        }
-        if (warp == 0) {
-            const float *gb = reinterpret_cast<const float *>(smc + SM::sb);
-            const float *gg = reinterpret_cast<const float *>(smc + SM::sgt);
-            const int r0 = 2 * lane, r1 = r0 + 1;
-            const float a0 = MODE == LDN_GDN ? gg[r0] : 0.f, a1 = MODE == LDN_GDN ? gg[r1] : 0.f;
-            float incl = a0 + a1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const float gl = __shfl_sync(0xffffffffu, incl, 31);
-            const float g0 = incl - a1, g1 = incl;
-            sg[r0] = g0;
-            sg[r1] = g1;
-            sbeta[r0] = gb[r0];
-            sbeta[r1] = gb[r1];
-            sge[r0] = MODE == LDN_GDN ? expf(g0) : 1.f;
-            sge[r1] = MODE == LDN_GDN ? expf(g1) : 1.f;
-            sgc[r0] = MODE == LDN_GDN ? expf(gl - g0) : 1.f;
-            sgc[r1] = MODE == LDN_GDN ? expf(gl - g1) : 1.f;
-            sbge[r0] = gb[r0] * sge[r0];
-            sbge[r1] = gb[r1] * sge[r1];
-        }
+        const int buf = c & 1;
+        const __half *Ms = reinterpret_cast<const __half *>(smc + SM::m + buf * (kD * kLdW * 2));
+        const __half *Bs = reinterpret_cast<const __half *>(smc + SM::bc + buf * (kD * kLdN * 2));
+        // dH' (fp16): the product's operand and the chunk's state-gradient image
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int2 og = tile_origin<kD, 64>(warp, i);
-            const int m0 = og.x, c0 = og.y;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; e += 2) {
-                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
-                    *reinterpret_cast<__half2 *>(dHh + rr * kLdN + cc) =
-                        __floats2half2_rn(dh[i][nt][e], dh[i][nt][e + 1]);
+                    const int rr = acc_row(lane, og.x, e), cc = acc_col(lane, og.y, nt, e);
+                    *reinterpret_cast<__half2 *>(dHh + rr * kLdN + cc) = __floats2half2_rn(dh[i][nt][e], dh[i][nt][e + 1]);
                 }
         }
+        if (c > 0) {   // the other buffer was last read before the previous chunk's closing barrier
+            chain_prefetch(smc, buf ^ 1, Mimg, Bimg, (size_t)unit * nch + c - 1, n0, tid);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
         __syncthreads();
-        // dH' (fp16) into the chunk's state-gradient image, 16-byte rows; T Diag(beta ge) (the
-        // staged swizzled rows); the dO slice, plain and times ge
         {
             __half *img = dHs + ((size_t)unit * nch + c) * (kStateImgBytes / 2) + n0;
 #pragma unroll
@@ -400,104 +508,29 @@ bwd_chain_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                 *reinterpret_cast<uint4 *>(img + (e >> 3) * kStateImgLd + 8 * (e & 7)) =
                     *reinterpret_cast<const uint4 *>(dHh + (e >> 3) * kLdN + 8 * (e & 7));
         }
-        for (int e = tid; e < kC * 8; e += kThreads) {
-            const int j = e >> 3, c8 = 8 * (((e & 7) ^ (64 + j)) & 7);
-            const uint4 u = *reinterpret_cast<const uint4 *>(smc + SM::st + e * 16);
-            const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
-            __half2 a[4];
+        // ---- dH0 = M dH' + Bc
+        const Op op[1] = {{Ms, kLdW, false, dHh, kLdN, false, kD}};
+        cta_mma<kD, 64>(op, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                const float2 f = __half22float2(h2[qq]);
-                a[qq] = __floats2half2_rn(f.x * sbge[c8 + 2 * qq], f.y * sbge[c8 + 2 * qq + 1]);
-            }
-            *reinterpret_cast<uint4 *>(TKs + j * kLdN + c8) = *reinterpret_cast<uint4 *>(a);
-            const int rr = e >> 3, part = e & 7;
-            const uint4 d = *reinterpret_cast<const uint4 *>(smc + SM::sdo + e * 16);
-            *reinterpret_cast<uint4 *>(dOr + rr * kLdN + 8 * part) = bf16x8_to_f16(d);
-            *reinterpret_cast<uint4 *>(dOs + rr * kLdN + 8 * part) = bf16x8_to_f16(d, sge[rr]);
-        }
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                    const float2 bv = __half22float2(*reinterpret_cast<const __half2 *>(Bs + rr * kLdN + cc));
+                    dh[i][nt][e] = acc[nt][e] + bv.x;
+                    dh[i][nt][e + 1] = acc[nt][e + 1] + bv.y;
+                }
+        });
         __syncthreads();
-        if (c > 0)   // the staging buffer is free: the previous chunk's inputs load under this chunk's products
-            chain_prefetch(smc, q, k, beta, gate, dout, X + ((size_t)unit * nch + c - 1) * kXBytes, tok_of(c - 1), H,
-                           kC, dv, n0, tid);
-        // ---- P = tril(Q K^T * Gamma) and W = T Diag(beta ge) K
-        {
-            const Op ops[1] = {{Qs, kLdW, false, Ks, kLdW, true, kD}};
-            cta_mma<kC, kC>(ops, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
-                        const float gm = MODE == LDN_GDN ? expf(sg[rr] - sg[jj]) : 1.f;
-                        Ps[rr * kLdN + jj] = __float2half_rn(jj <= rr ? acc[nt][e] * gm : 0.f);
-                    }
-            });
-            const Op opw[1] = {{TKs, kLdN, false, Ks, kLdW, false, kC}};
-            cta_mma<kC, kD>(opw, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; e += 2) {
-                        const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
-                        *reinterpret_cast<__half2 *>(Ws + rr * kLdW + cc) = __floats2half2_rn(acc[nt][e], acc[nt][e + 1]);
-                    }
-            });
-        }
-        __syncthreads();
-        // ---- dU = Diag(gc) K dH' + P^T dO
-        {
-            float keep[2][2][4];   // this warp's two dU tiles: (Diag(gc) K dH') then + P^T dO
-            const Op o1[1] = {{Ks, kLdW, false, dHh, kLdN, false, kD}};
-            cta_mma<kC, 64>(o1, warp, lane, [&](int i, int m0, int, float (&acc)[2][4]) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) keep[i][nt][e] = acc[nt][e] * sgc[acc_row(lane, m0, e)];
-            });
-            const Op o2[1] = {{Ps, kLdN, true, dOr, kLdN, false, kC}};
-            cta_mma<kC, 64>(o2, warp, lane, [&](int i, int m0, int c0, float (&acc)[2][4]) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; e += 2) {
-                        const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
-                        *reinterpret_cast<__half2 *>(dUs + rr * kLdN + cc) =
-                            __floats2half2_rn(keep[i][nt][e] + acc[nt][e], keep[i][nt][e + 1] + acc[nt][e + 1]);
-                    }
-            });
-        }
-        __syncthreads();
-        // ---- dH0 = gamma dH' + Q^T Diag(ge) dO - W^T dU (this warp's tiles, in registers)
-        {
-            const float gam = MODE == LDN_GDN ? expf(sg[kC - 1]) : 1.f;
-            const Op o1[1] = {{Qs, kLdW, true, dOs, kLdN, false, kC}};
-            const Op o2[1] = {{Ws, kLdW, true, dUs, kLdN, false, kC}};
-            float qd[4][2][4];
-            cta_mma<kD, 64>(o1, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) qd[i][nt][e] = acc[nt][e];
-            });
-            cta_mma<kD, 64>(o2, warp, lane, [&](int i, int, int, float (&acc)[2][4]) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) dh[i][nt][e] = gam * dh[i][nt][e] + qd[i][nt][e] - acc[nt][e];
-            });
-        }
-        // (the next chunk's first barrier orders these reads before its writes)
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int2 og = tile_origin<kD, 64>(warp, i);
-        const int m0 = og.x, c0 = og.y;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
-                const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
+                const int rr = acc_row(lane, og.x, e), cc = acc_col(lane, og.y, nt, e);
                 *reinterpret_cast<float2 *>(dS0 + ((size_t)unit * kD + rr) * dv + n0 + cc) =
                     make_float2(dh[i][nt][e], dh[i][nt][e + 1]);
             }
@@ -505,12 +538,12 @@ bwd_chain_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
 }
 
 // =====================================================================================
-// Kernel 2: every chunk's gradients, one CTA per (b, h, chunk).  Shared-memory plan (fp16
+// Kernel 3: every chunk's gradients, one CTA per (b, h, chunk).  Shared-memory plan (fp16
 // tiles; buffers are reused once their last reader is past):
-//   Q, K, V, dO [64][136] (dO's place takes dW; V and dO's together the staged dK rows), H0
-//   and dH' [128][136] (their places the staged dV and dQ rows), T, T Diag(beta ge) (then X1 = T^T dT, then
-//   E = Diag(beta) E'), T Diag(beta) (then dT, then E'), P (then F) [64][72], W (then dU) and
-//   U [64][136], small vectors.
+//   Q, K, V, dO [64][136] (dO's place takes dW; V and dO's together the staged dK rows),
+//   H0 and dH' [128][136] (their places the staged dV and dQ rows), T, X1 = T^T dT (then
+//   E = Diag(beta) E'), T Diag(beta) (then dT, then E'), P (then F) [64][72], -W (then dU)
+//   and U (T's raw rows first) [64][136], small vectors.
 struct ChunkSmem {
     static constexpr int q = 0;
     static constexpr int k = q + kC * kLdW * 2;
@@ -519,13 +552,13 @@ struct ChunkSmem {
     static constexpr int h0 = dO + kC * kLdW * 2;         // [128][136]; then dV fp32 [64][136]
     static constexpr int dh = h0 + kD * kLdW * 2;         // [128][136]; then dQ fp32 [64][136]
     static constexpr int t = dh + kD * kLdW * 2;
-    static constexpr int tk = t + kC * kLdN * 2;          // T Diag(beta ge); X1; E
+    static constexpr int tk = t + kC * kLdN * 2;          // X1; E
     static constexpr int tv = tk + kC * kLdN * 2;         // T Diag(beta); dT; E'
     static constexpr int p = tv + kC * kLdN * 2;          // P; F
     static constexpr int w = p + kC * kLdN * 2;           // -W; dU
-    static constexpr int u = w + kC * kLdW * 2;           // U
+    static constexpr int u = w + kC * kLdW * 2;           // T's raw rows; U
     static constexpr int small = u + kC * kLdW * 2;       // beta, g, ge, gc, beta ge, 8 slots, 5 x [8][64] parts
-    static constexpr int bar = small + (5 * kC + 8 + 5 * kWarps * kC) * 4;   // mbarrier of the state images' copies
+    static constexpr int bar = small + (5 * kC + 8 + 5 * kWarps * kC) * 4;   // mbarrier of the bulk copies
     static constexpr int bytes = bar + 8;
     static_assert(bytes <= 232448, "shared memory plan exceeds 227 KB");
     static_assert(kC * kLdO * 4 <= kD * kLdW * 2 && kC * kLdO * 4 == 2 * kC * kLdW * 2,
@@ -538,6 +571,7 @@ bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                  const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
                  const float *__restrict__ gate, const __nv_bfloat16 *__restrict__ dout,
                  const uint8_t *__restrict__ X, const __half *__restrict__ Hs, const __half *__restrict__ dHs,
+                 const __half *__restrict__ Pimg, const __half *__restrict__ Wimg,
                  float *__restrict__ dq, float *__restrict__ dk_out, float *__restrict__ dv_out,
                  float *__restrict__ dbeta, float *__restrict__ dgate, int *status, int T, int H)
 {
@@ -572,17 +606,20 @@ bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
     const int t0 = c * kC, L = min(kC, T - t0);
     const size_t tok0 = ((size_t)b * T + t0) * H + h;
 
-    // ---- 0: inputs.  H0 and dH' (the fp16 state images, already in the tiles' layout) by two
-    //      bulk copies; meanwhile q, k, v, dO rows to fp16 (sixteen 16-byte loads per thread in
-    //      flight); T
+    // ---- 0: inputs.  H0 and dH' (the fp16 state images), P and -W (the prep kernel's images),
+    //      all in the tiles' layout, and T's rows of X (raw, into U's place) by bulk copies;
+    //      meanwhile q, k, v, dO rows to fp16 (sixteen 16-byte loads per thread in flight)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smk + SM::bar);
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar, 2 * (uint32_t)kStateImgBytes);
-        const size_t img = ((size_t)unit * nch + c) * (kStateImgBytes / 2);
-        bulk_load(H0s, Hs + img, (uint32_t)kStateImgBytes, bar);
-        bulk_load(dHh, dHs + img, (uint32_t)kStateImgBytes, bar);
+        mbar_arrive_expect_tx(bar, (uint32_t)(2 * kStateImgBytes + kPImg + kWImg) + 8192u);
+        const size_t chunk = (size_t)unit * nch + c;
+        bulk_load(H0s, Hs + chunk * (kStateImgBytes / 2), (uint32_t)kStateImgBytes, bar);
+        bulk_load(dHh, dHs + chunk * (kStateImgBytes / 2), (uint32_t)kStateImgBytes, bar);
+        bulk_load(Ps, Pimg + chunk * (kPImg / 2), (uint32_t)kPImg, bar);
+        bulk_load(Ws, Wimg + chunk * (kWImg / 2), (uint32_t)kWImg, bar);
+        bulk_load(Us, X + chunk * kXBytes + 8192, 8192u, bar);   // T's rows, raw
     }
     {
         const __nv_bfloat16 *const src[4] = {q, k, v, dout};
@@ -623,34 +660,10 @@ bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
         sbge[rr] = sbeta[rr] * sge[rr];
     }
     __syncthreads();
-    load_t(X + ((size_t)unit * nch + c) * kXBytes, Ts, TKs, sbge, TVs, sbeta, tid);
+    load_t(reinterpret_cast<const uint8_t *>(Us), Ts, TVs, sbeta, nullptr, nullptr, tid);
     __syncthreads();
     auto gam_of = [&](int rr, int jj) { return MODE == LDN_GDN ? expf(sg[rr] - sg[jj]) : 1.f; };
 
-    // ---- 1: P = tril(Q K^T * Gamma); -W = -T Diag(beta ge) K
-    {
-        const Op op[1] = {{Qs, kLdW, false, Ks, kLdW, true, kD}};
-        cta_mma<kC, kC>(op, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int rr = acc_row(lane, m0, e), jj = acc_col(lane, c0, nt, e);
-                    Ps[rr * kLdN + jj] = __float2half_rn(jj <= rr ? acc[nt][e] * gam_of(rr, jj) : 0.f);
-                }
-        });
-        const Op ow[1] = {{TKs, kLdN, false, Ks, kLdW, false, kC}};
-        cta_mma<kC, kD>(ow, warp, lane, [&](int, int m0, int c0, float (&acc)[2][4]) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; e += 2) {
-                    const int rr = acc_row(lane, m0, e), cc = acc_col(lane, c0, nt, e);
-                    *reinterpret_cast<__half2 *>(Ws + rr * kLdW + cc) = __floats2half2_rn(-acc[nt][e], -acc[nt][e + 1]);
-                }
-        });
-    }
-    __syncthreads();
     // ---- 2: U = T Diag(beta) V + (-W) H0
     {
         const Op op[2] = {{TVs, kLdN, false, Vs, kLdW, false, kC}, {Ws, kLdW, false, H0s, kLdW, false, kD}};
@@ -1001,22 +1014,27 @@ bool bwd_chunk_supported(const BwdArgs &a)
     return a.dtype == LDN_BF16 && a.dk == kD && a.dv == kD && (a.mode == LDN_DELTANET || a.mode == LDN_GDN) && a16;
 }
 
-// Workspace: the solve's X (16 KB per (b, h, chunk)), the states entering every chunk and the
-// state gradients leaving every chunk (fp16 state images, 34 KB each), and the forward pass's
-// output (bf16).
+// Workspace per (b, h, chunk): the solve's X (16 KB), the state entering and the state
+// gradient leaving the chunk (fp16 state images, 34 KB each), the prep kernel's P (9 KB), -W
+// (17 KB), M and Bc (34 KB each); and the forward pass's output (bf16).
 size_t bwd_chunk_workspace_bytes(int B, int T, int H)
 {
     const size_t units = (size_t)B * H, nch = (size_t)(T + kC - 1) / kC;
-    return units * nch * (kXBytes + 2 * kStateImgBytes) + (size_t)B * T * H * kD * 2;
+    return units * nch * (kXBytes + 2 * kStateImgBytes + kPImg + kWImg + 2 * kMImg) + (size_t)B * T * H * kD * 2;
 }
 
 cudaError_t launch_backward_chunk(const BwdArgs &a, cudaStream_t s)
 {
     const size_t units = (size_t)a.B * a.H, nch = (size_t)(a.T + kC - 1) / kC;
+    const size_t nc = units * nch;
     uint8_t *X = reinterpret_cast<uint8_t *>(a.ws);
-    __half *Hs = reinterpret_cast<__half *>(X + units * nch * kXBytes);
-    __half *dHs = Hs + units * nch * (kStateImgBytes / 2);
-    void *out = dHs + units * nch * (kStateImgBytes / 2);
+    __half *Hs = reinterpret_cast<__half *>(X + nc * kXBytes);
+    __half *dHs = Hs + nc * (kStateImgBytes / 2);
+    __half *Pimg = dHs + nc * (kStateImgBytes / 2);
+    __half *Wimg = Pimg + nc * (kPImg / 2);
+    __half *Mimg = Wimg + nc * (kWImg / 2);
+    __half *Bimg = Mimg + nc * (kMImg / 2);
+    void *out = Bimg + nc * (kMImg / 2);
     // forward: the solve and the fused kernel with the chunk states
     ChunkArgs f{a.q, a.k, a.v, a.beta, a.gate, a.S0, out, nullptr, a.B, a.T, a.H, kD, kD, kC, a.mode, a.dtype,
                 status_word_ptr()};
@@ -1024,19 +1042,26 @@ cudaError_t launch_backward_chunk(const BwdArgs &a, cudaStream_t s)
     if (!f.status) return cudaErrorInvalidValue;
     cudaError_t e = launch_chunk_presolved(f, X, s);
     if (e != cudaSuccess) return e;
-    auto k1 = a.mode == LDN_GDN ? bwd_chain_kernel<LDN_GDN> : bwd_chain_kernel<LDN_DELTANET>;
+    auto k0 = a.mode == LDN_GDN ? bwd_prep_kernel<LDN_GDN> : bwd_prep_kernel<LDN_DELTANET>;
     auto k2 = a.mode == LDN_GDN ? bwd_chunk_kernel<LDN_GDN> : bwd_chunk_kernel<LDN_DELTANET>;
-    if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, ChainSmem::bytes)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem::bytes)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  ChainSmem::bytes)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, ChunkSmem::bytes)) != cudaSuccess)
         return e;
-    k1<<<(unsigned)(units * (kD / 64)), kThreads, ChainSmem::bytes, s>>>(
-        (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, a.beta, a.gate, (const __nv_bfloat16 *)a.dout,
-        a.dS_final, X, dHs, a.dS0, a.T, a.H, kD);
+    k0<<<(unsigned)nc, kThreads, PrepSmem::bytes, s>>>(
+        (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, a.beta, a.gate, (const __nv_bfloat16 *)a.dout, X,
+        Pimg, Wimg, Mimg, Bimg, a.T, a.H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k2<<<(unsigned)(units * nch), kThreads, ChunkSmem::bytes, s>>>(
+    bwd_chain_kernel<<<(unsigned)(units * (kD / 64)), kThreads, ChainSmem::bytes, s>>>(
+        Mimg, Bimg, a.dS_final, dHs, a.dS0, a.T, a.H, kD);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k2<<<(unsigned)nc, kThreads, ChunkSmem::bytes, s>>>(
         (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v, a.beta, a.gate,
-        (const __nv_bfloat16 *)a.dout, X, Hs, dHs, a.dq, a.dk_out, a.dv_out, a.dbeta, a.dgate, f.status, a.T, a.H);
+        (const __nv_bfloat16 *)a.dout, X, Hs, dHs, Pimg, Wimg, a.dq, a.dk_out, a.dv_out, a.dbeta, a.dgate, f.status,
+        a.T, a.H);
     return cudaGetLastError();
 }
 

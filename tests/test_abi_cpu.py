@@ -415,9 +415,9 @@ def test_chunkwise_backward_wants_aligned_tensors_and_its_workspace(lib):
 def test_backward_workspace_size(lib):
     """Recurrent form: state copies (every eighth state of every column) plus
     per-32-column partial sums of dq, dk, the gate gradient and dbeta.  Chunkwise form
-    (bf16 DeltaNet / GDN, dk = dv = 128): the solve X (16 KiB per chunk), the states
-    entering and the state gradients leaving every chunk (fp16 images of 128 x 136), the
-    forward's output."""
+    (bf16 DeltaNet / GDN, dk = dv = 128), per chunk: the solve X (16 KiB), the state
+    entering and the state gradient leaving it and the chain's two terms M and Bc (fp16
+    images of 128 x 136), P (64 x 72) and -W (64 x 136); and the forward's output."""
     B, T, H, dk, dv = 2, 70, 3, 128, 64
     n, nsub, sl = B * T * H, (T + 7) // 8, dv // 32
     for dtype in (ldn.LDN_F32, ldn.LDN_BF16):
@@ -425,7 +425,7 @@ def test_backward_workspace_size(lib):
             want = 4 * (B * H * dv * nsub * dk + sl * n * (2 * dk + gw + 1))
             assert ldn.ldn_backward_workspace_size(B, T, H, dk, dv, mode, dtype) == want
     nch = (T + 63) // 64
-    chunked = B * H * nch * (16384 + 2 * 128 * 136 * 2) + n * 128 * 2
+    chunked = B * H * nch * (16384 + 4 * 128 * 136 * 2 + 64 * 72 * 2 + 64 * 136 * 2) + n * 128 * 2
     for mode in (0, 1):
         assert ldn.ldn_backward_workspace_size(B, T, H, 128, 128, mode, ldn.LDN_BF16) == chunked
     n, nsub, sl = B * T * H, (T + 7) // 8, 128 // 32
