@@ -11,13 +11,19 @@
 //
 // Each block stages its tile in shared memory with 16-byte cp.async copies
 // (zero-filled outside the sequence; nothing held in registers while the bytes
-// are in flight), then computes from there, so that many small blocks per SM
-// keep HBM busy.  Convolution: a block takes 64 tokens of one (b, h) and one
-// of q, k, v -- the tile holds its W - 1 tokens of halo, so every input row
-// is read once from HBM (and up to W - 1 more times from L2) -- and a group of
-// d/4 lanes (4 channels each) forms one output row: the W taps, SiLU, and for
-// q and k the L2 norm as a shuffle sum over the group.  Blocks are numbered
-// with the head fastest, so neighbouring blocks read neighbouring rows.
+// are in flight), then computes from there, so that several blocks per SM keep
+// HBM busy.  Convolution: a block takes 32 tokens (16 for more than four taps) of
+// a group of heads whose rows make 1 KB, and one of q, k, v -- the tile holds its
+// W - 1 tokens of halo, so every input row is read once from HBM (and up to W - 1
+// more times from L2) -- and a thread owns one 16-byte piece of a row (8 bf16 / 4
+// fp32 channels): the W taps and SiLU in packed fp32x2 arithmetic, and for q and k
+// the L2 norm as a shuffle sum over the head's threads.  The convolution kernel is
+// issue-bound (ncu: 59% of issue slots at 30% occupancy before the packed form),
+// so instructions per element are what the layout minimises.  Blocks are numbered
+// with the head fastest, so neighbouring blocks read neighbouring rows.  The gates
+// (one per (b, t, h)) ride in the convolution launch, each block taking a share
+// while its tile's copies are in flight; KDA's per-channel gates, a stream as large
+// as the convolutions', have a launch of their own.
 // RMSNorm: a block takes 64 consecutive rows of o and the gate.  Arithmetic is
 // fp32; values are stored in the tensor's dtype.
 #include <algorithm>
@@ -65,41 +71,135 @@ __device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
 // log(1 + e^x); for x > 15 the correction log(1 + e^-x) is below fp32 resolution of x
 __device__ __forceinline__ float softplus_f(float x) { return x > 15.f ? x : __logf(1.f + __expf(x)); }
 
-// Up to three convolutions of one row width D in one launch (blockIdx.y picks
-// q, k or v).  y = silu(short_conv(x)), then (norm) divided by sqrt(sum of
-// squares + eps) per row.  x, y [B][T][H][D]; w [H * D][W], tap W - 1 on the
-// current token.
+// beta = sigmoid(logit) over nb values and, when g is given, one gate per (b, t, h):
+// log alpha = -a[h] softplus(z + bias[h]).  A grid-stride loop (start, stride) with
+// four independent elements per thread in flight.
+struct GateArgs {
+    const float *logit;
+    float *beta;
+    const float *z, *a, *bias;
+    float *g;
+    long long nb;
+    int H;
+};
+
+constexpr int kGateUnroll = 4;
+
+__device__ __forceinline__ void gates_work(const GateArgs &ga, long long start, long long stride)
+{
+    for (long long i0 = start; i0 < ga.nb; i0 += kGateUnroll * stride) {
+        float lv[kGateUnroll];
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const long long i = i0 + u * stride;
+            lv[u] = i < ga.nb ? __ldg(ga.logit + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const long long i = i0 + u * stride;
+            if (i < ga.nb) ga.beta[i] = sigmoid_f(lv[u]);
+        }
+    }
+    if (!ga.g) return;
+    for (long long i0 = start; i0 < ga.nb; i0 += kGateUnroll * stride) {
+        float zv[kGateUnroll];
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const long long i = i0 + u * stride;
+            zv[u] = i < ga.nb ? __ldg(ga.z + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const long long i = i0 + u * stride;
+            if (i >= ga.nb) continue;
+            const int h = (int)(i % ga.H);
+            ga.g[i] = -__ldg(ga.a + h) * softplus_f(zv[u] + __ldg(ga.bias + h));
+        }
+    }
+}
+
+// Up to three convolutions of one row width D in one launch (blockIdx.y picks q, k or v),
+// and, when `gates` is set, the gates, spread over all the launch's blocks: y =
+// silu(short_conv(x)), then (norm) divided by sqrt(sum of squares + eps) per row.  x, y
+// [B][T][H][D]; w [H * D][W], tap W - 1 on the current token.
 struct ConvBatch {
     const void *x[3];
     const float *w[3];
     void *y[3];
     int norm[3];
+    int n;
+    int gates;
+    GateArgs ga;
 };
 
 // Convolution tile: kConvTok tokens (plus the W - 1 before them) of a group of
 // HG = 1 KB / (D * element size) consecutive heads, so that each token row of the
-// tile is 1 KB of contiguous memory.  blockIdx.x = (b, run, head group) with the
-// head group fastest, blockIdx.y = the tensor.  One lane group of D/4 lanes (4
-// channels each) per head walks the tile's tokens, sliding a register window of
-// the last WMAX input rows (one shared-memory read per row).
-constexpr int kConvTok = 16;
+// tile is 1 KB of contiguous memory, and the heads' weights.  blockIdx.x = (b, run,
+// head group) with the head group fastest.  A thread owns one 16-byte piece of a head's
+// row (VE channels); the D / VE threads of a head and the heads of the group make a
+// walker of 64 threads, and the block's two walkers take half of the tile's tokens each,
+// sliding a register window of the last WMAX input rows (one shared-memory read per
+// row) through a fully unrolled token loop.
+constexpr int kConvWalk = 2;
+constexpr int kConvThreads = 128;
+// tokens per tile: 32 for up to 4 taps, 16 for up to 8 (static shared memory stays under 48 KB)
+template <int WMAX>
+constexpr int conv_tok() { return WMAX <= 4 ? 32 : 16; }
 
 template <int D, typename TIn>
 constexpr int conv_heads() { return 1024 / (D * (int)sizeof(TIn)); }
-template <int D, typename TIn>
-constexpr int conv_threads() { return conv_heads<D, TIn>() * (D / 4); }
+
+template <typename TIn> struct Vec16;
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void ld(const float *p, float *v)
+    {
+        const float4 x = *reinterpret_cast<const float4 *>(p);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    }
+    static __device__ __forceinline__ void st(float *p, const float *v)
+    {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void ld(const __nv_bfloat16 *p, float *v)
+    {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(b[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void st(__nv_bfloat16 *p, const float *v)
+    {
+        uint4 u;
+        __nv_bfloat162 *b = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) b[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        *reinterpret_cast<uint4 *>(p) = u;
+    }
+};
 
 template <int D, int WMAX, typename TIn>
-__global__ void __launch_bounds__(conv_threads<D, TIn>())
+__global__ void __launch_bounds__(kConvThreads)
 conv_silu_kernel(const ConvBatch cb, int B, int T, int H, int W, float eps)
 {
+    using V = Vec16<TIn>;
+    constexpr int VE = V::N;                          // channels per thread
+    constexpr int L = D / VE;                         // threads per head
     constexpr int HG = conv_heads<D, TIn>();
-    constexpr int kThr = conv_threads<D, TIn>();
+    static_assert(HG * L * kConvWalk == kConvThreads, "two walkers of 64 threads");
+    constexpr int kConvTok = conv_tok<WMAX>();
     constexpr int kRows = kConvTok + WMAX - 1;        // tile rows: tokens t0 - (W-1) ...
     constexpr int kRowElems = HG * D;                 // one token of the head group
-    constexpr int kVec = 16 / sizeof(TIn);            // elements per 16-byte copy
-    constexpr int L = D / 4;                          // lanes per head
+    constexpr int TPW = kConvTok / kConvWalk;         // tokens per walker
     __shared__ __align__(16) TIn tile[kRows * kRowElems];
+    __shared__ __align__(16) float wsm[HG * D * WMAX];
     const int ts = blockIdx.y;   // selected without indexing, so that cb stays in parameter space
     const TIn *x = (const TIn *)(ts == 0 ? cb.x[0] : ts == 1 ? cb.x[1] : cb.x[2]);
     const float *w = ts == 0 ? cb.w[0] : ts == 1 ? cb.w[1] : cb.w[2];
@@ -115,63 +215,89 @@ conv_silu_kernel(const ConvBatch cb, int B, int T, int H, int W, float eps)
     const size_t base = ((size_t)b * T * H + h0) * D;              // token 0, head h0
     const int hvalid = min(HG, H - h0);
     const int tbase = t0 - (W - 1);
-    for (int i = threadIdx.x; i < kRows * (kRowElems / kVec); i += kThr) {
-        const int r = i / (kRowElems / kVec), e = (i % (kRowElems / kVec)) * kVec;
+    for (int i = threadIdx.x; i < kRows * (kRowElems / VE); i += kConvThreads) {
+        const int r = i / (kRowElems / VE), e = (i % (kRowElems / VE)) * VE;
         const int t = tbase + r;
         const bool ok = t >= 0 && t < T && e < hvalid * D;
         cp_async16(&tile[r * kRowElems + e], ok ? x + base + (size_t)t * rs + e : x, ok ? 16u : 0u);
     }
     cp_async_commit();
+    // this block's share of the gates (grid-stride over every block of the launch), while the
+    // tile's copies are in flight
+    if (cb.gates)
+        gates_work(cb.ga, ((long long)blockIdx.y * gridDim.x + blockIdx.x) * kConvThreads + threadIdx.x,
+                   (long long)gridDim.x * gridDim.y * kConvThreads);
+    // the group's weights (in memory W taps per channel, channels of heads h0 ..), stored tap
+    // by tap: wsm[j][channel], so that a thread's VE channels of a tap are 16 / 32 contiguous bytes
+    for (int c = threadIdx.x; c < hvalid * D; c += kConvThreads) {
+        const float *wc = w + ((size_t)h0 * D + c) * W;
+#pragma unroll
+        for (int j = 0; j < WMAX; ++j)
+            if (j < W) wsm[j * kRowElems + c] = __ldg(wc + j);
+    }
 
-    const int lane = threadIdx.x & 31;
-    const int hl = threadIdx.x / L, c0 = 4 * (lane % L), h = h0 + hl;
+    const int walker = threadIdx.x / (HG * L), r = threadIdx.x % (HG * L);
+    const int hl = r / L, c0 = VE * (r % L), h = h0 + hl;
     const bool hok = h < H;
-    float wt[WMAX][4];   // tap j multiplies tile row (output row + j)
+    cp_async_wait<0>();
+    __syncthreads();
+    // channel pairs in packed fp32x2 arithmetic (one instruction per pair)
+    constexpr int VP = VE / 2;
+    float2 wt[WMAX][VP];   // tap j multiplies tile row (output row + j)
 #pragma unroll
     for (int j = 0; j < WMAX; ++j)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) wt[j][i] = (hok && j < W) ? w[(size_t)(h * D + c0 + i) * W + j] : 0.f;
-    cp_async_wait<0>();
-    __syncthreads();
+        for (int i = 0; i < VP; ++i) {
+            const bool on = hok && j < W;
+            wt[j][i] = on ? *reinterpret_cast<const float2 *>(&wsm[j * kRowElems + hl * D + c0 + 2 * i])
+                          : make_float2(0.f, 0.f);
+        }
 
-    const int col = hl * D + c0;
-    float win[WMAX][4];
+    const int col = hl * D + c0, u0 = walker * TPW;
+    float2 win[WMAX][VP];
 #pragma unroll
-    for (int j = 0; j < WMAX - 1; ++j) ld4(&tile[j * kRowElems + col], win[j]);
-    TIn *yp = y + base + (size_t)t0 * rs + col;
-#pragma unroll 4
-    for (int u = 0; u < kConvTok; ++u) {
-        ld4(&tile[(u + WMAX - 1) * kRowElems + col], win[WMAX - 1]);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < WMAX - 1; ++j) V::ld(&tile[(u0 + j) * kRowElems + col], reinterpret_cast<float *>(win[j]));
+    TIn *yp = y + base + (size_t)(t0 + u0) * rs + col;
 #pragma unroll
-        for (int j = 0; j < WMAX; ++j)
+    for (int u = 0; u < TPW; ++u) {
+        V::ld(&tile[(u0 + u + WMAX - 1) * kRowElems + col], reinterpret_cast<float *>(win[WMAX - 1]));
+        float2 acc[VP];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wt[j][i], win[j][i], acc[i]);
+        for (int i = 0; i < VP; ++i) acc[i] = __fmul2_rn(wt[0][i], win[0][i]);
+#pragma unroll
+        for (int j = 1; j < WMAX; ++j)
+#pragma unroll
+            for (int i = 0; i < VP; ++i) acc[i] = __ffma2_rn(wt[j][i], win[j][i], acc[i]);
 #pragma unroll
         for (int j = 0; j < WMAX - 1; ++j)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) win[j][i] = win[j + 1][i];
+            for (int i = 0; i < VP; ++i) win[j][i] = win[j + 1][i];
+        // silu(x) = x / (1 + e^-x)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = silu_f(acc[i]);
+        for (int i = 0; i < VP; ++i) {
+            const float2 d = __fadd2_rn(make_float2(__expf(-acc[i].x), __expf(-acc[i].y)), make_float2(1.f, 1.f));
+            acc[i] = __fmul2_rn(acc[i], make_float2(__fdividef(1.f, d.x), __fdividef(1.f, d.y)));
+        }
         if (norm) {
-            float ss = acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3];
+            float2 s2 = __fmul2_rn(acc[0], acc[0]);
+#pragma unroll
+            for (int i = 1; i < VP; ++i) s2 = __ffma2_rn(acc[i], acc[i], s2);
+            float ss = s2.x + s2.y;
 #pragma unroll
             for (int o = L / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             const float sc = rsqrtf(ss + eps);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] *= sc;
+            for (int i = 0; i < VP; ++i) acc[i] = __fmul2_rn(acc[i], make_float2(sc, sc));
         }
-        if (hok && t0 + u < T) st4(yp, acc);
+        if (hok && t0 + u0 + u < T) V::st(yp, reinterpret_cast<const float *>(acc));
         yp += rs;
     }
 }
 
-// beta = sigmoid(logit) over nb values and, when g is given, log alpha =
-// -a[h] softplus(z + bias) over the gate tensor: PER4 = 0, one gate per (b, t, h)
-// (bias[h]); PER4 = dk / 4, dk per-channel gates per (b, t, h) handled as float4
-// (bias[h][c]).  Each thread takes kGateUnroll independent elements.  Idx is 32-bit
-// unless the tensors need more.
-constexpr int kGateUnroll = 4;
+// The gates as a kernel of their own (KDA: dk per-channel gates per (b, t, h), a stream
+// as large as the convolutions' that wants every block of the GPU): as gates_work, each
+// thread taking kGateUnroll independent elements.  Idx is 32-bit unless the tensors need
+// more.
 
 template <int PER4, typename Idx>
 __global__ void __launch_bounds__(kThreads)
@@ -287,9 +413,10 @@ rmsnorm_gated_kernel(const TIn *__restrict__ o, const TIn *__restrict__ gt, cons
     }
 }
 
-// Convolutions of the tensors in `sel` (all of row width d) in one launch.
+// Convolutions of the tensors in `sel` (all of row width d) in one launch, with the gates
+// when `ga` is given.
 template <typename TIn>
-cudaError_t conv_launch(const PrologueArgs &a, const int *sel, int n, int d, cudaStream_t st)
+cudaError_t conv_launch(const PrologueArgs &a, const int *sel, int n, int d, const GateArgs *ga, cudaStream_t st)
 {
     const void *xs[3] = {a.q_in, a.k_in, a.v_in};
     const float *ws[3] = {a.conv_q, a.conv_k, a.conv_v};
@@ -301,16 +428,18 @@ cudaError_t conv_launch(const PrologueArgs &a, const int *sel, int n, int d, cud
         cb.y[i] = ys[sel[i]];
         cb.norm[i] = sel[i] < 2;   // q and k are L2-normalised
     }
+    cb.n = n;
+    cb.gates = ga != nullptr;
+    if (ga) cb.ga = *ga;
     const int hg = 1024 / (d * (int)sizeof(TIn));   // conv_heads
-    const dim3 grid((unsigned)((long long)a.B * ((a.H + hg - 1) / hg) * ((a.T + kConvTok - 1) / kConvTok)), (unsigned)n);
-    auto go = [&](auto kern, int thr) { kern<<<grid, thr, 0, st>>>(cb, a.B, a.T, a.H, a.width, a.eps); };
     const bool w4 = a.width <= 4;
+    const int tok = w4 ? conv_tok<4>() : conv_tok<8>();
+    const dim3 grid((unsigned)((long long)a.B * ((a.H + hg - 1) / hg) * ((a.T + tok - 1) / tok)), (unsigned)n);
+    auto go = [&](auto kern) { kern<<<grid, kConvThreads, 0, st>>>(cb, a.B, a.T, a.H, a.width, a.eps); };
     if (d == 128)
-        w4 ? go(conv_silu_kernel<128, 4, TIn>, conv_threads<128, TIn>())
-           : go(conv_silu_kernel<128, 8, TIn>, conv_threads<128, TIn>());
+        w4 ? go(conv_silu_kernel<128, 4, TIn>) : go(conv_silu_kernel<128, 8, TIn>);
     else
-        w4 ? go(conv_silu_kernel<64, 4, TIn>, conv_threads<64, TIn>())
-           : go(conv_silu_kernel<64, 8, TIn>, conv_threads<64, TIn>());
+        w4 ? go(conv_silu_kernel<64, 4, TIn>) : go(conv_silu_kernel<64, 8, TIn>);
     return cudaGetLastError();
 }
 
@@ -320,18 +449,25 @@ cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t st)
 {
     if (a.T == 0) return cudaSuccess;
     const bool bf = a.dtype == LDN_BF16;
+    const bool kda = a.mode == LDN_KDA;
+    // one gate per (b, t, h): folded into the convolution launch; KDA's per-channel gates:
+    // their own launch
+    const GateArgs ga{a.beta_logit, a.beta, a.gate_z, a.gate_a, a.gate_b, a.mode == LDN_DELTANET ? nullptr : a.gate,
+                      (long long)a.B * a.T * a.H, a.H};
+    const GateArgs *fold = kda ? nullptr : &ga;
     cudaError_t e;
     if (a.dk == a.dv) {   // q, k, v in one launch
         const int sel[3] = {0, 1, 2};
-        e = bf ? conv_launch<__nv_bfloat16>(a, sel, 3, a.dk, st) : conv_launch<float>(a, sel, 3, a.dk, st);
+        e = bf ? conv_launch<__nv_bfloat16>(a, sel, 3, a.dk, fold, st) : conv_launch<float>(a, sel, 3, a.dk, fold, st);
     } else {
         const int sqk[2] = {0, 1}, sv[1] = {2};
-        e = bf ? conv_launch<__nv_bfloat16>(a, sqk, 2, a.dk, st) : conv_launch<float>(a, sqk, 2, a.dk, st);
+        e = bf ? conv_launch<__nv_bfloat16>(a, sqk, 2, a.dk, fold, st) : conv_launch<float>(a, sqk, 2, a.dk, fold, st);
         if (e == cudaSuccess)
-            e = bf ? conv_launch<__nv_bfloat16>(a, sv, 1, a.dv, st) : conv_launch<float>(a, sv, 1, a.dv, st);
+            e = bf ? conv_launch<__nv_bfloat16>(a, sv, 1, a.dv, nullptr, st)
+                   : conv_launch<float>(a, sv, 1, a.dv, nullptr, st);
     }
-    if (e != cudaSuccess) return e;
-    const long long n4 = (long long)a.B * a.T * a.H * (a.mode == LDN_KDA ? a.dk / 4 : 1);
+    if (e != cudaSuccess || !kda) return e;
+    const long long n4 = (long long)a.B * a.T * a.H * (a.dk / 4);
     return n4 + kThreads * kGateUnroll < (1LL << 31) ? gates_launch<unsigned>(a, st)
                                                       : gates_launch<unsigned long long>(a, st);
 }
