@@ -658,12 +658,16 @@ def run_ours(args):
             rsf = torch.empty((B_, H_, dk_, dv_), dtype=torch.float32, device="cuda")
             rrf = torch.empty_like(rsf)
             rdt = ldn.LDN_BF16 if rp["dtype"] == "bf16" else ldn.LDN_F32
+            rneed = ldn.ldn_rla_fwd_workspace_size(B_, T_, H_, dk_, dv_, int(rp["delta"]), rdt)
+            rws = torch.empty(max(rneed, 1), dtype=torch.uint8, device="cuda")
+            rchunk = rdt == ldn.LDN_BF16 and dk_ == 128 and dv_ == 128
 
             def rstep():
-                st_ = ldn.ldn_rla_fwd(P(rq), P(rk), P(rv), P(rb), P(rgm), P(rgt), rp["clip"], 0, 0, P(rout), P(rsf),
-                                      P(rrf), B_, T_, H_, dk_, dv_, int(rp["delta"]), rdt, sh)
+                st_ = ldn.ldn_rla_fwd_ws(P(rq), P(rk), P(rv), P(rb), P(rgm), P(rgt), rp["clip"], 0, 0, P(rout),
+                                         P(rsf), P(rrf), B_, T_, H_, dk_, dv_, int(rp["delta"]), rdt,
+                                         rws.data_ptr() if rneed else 0, rneed, sh)
                 if st_ != ldn.LDN_OK:
-                    raise ldn.LdnError(st_, "ldn_rla_fwd")
+                    raise ldn.LdnError(st_, "ldn_rla_fwd_ws")
 
             rstep()
             rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
@@ -673,13 +677,16 @@ def run_ours(args):
                 rstep()
                 e1.record(stream)
             barrier()
-            launches += 1 + len(rev)
+            nrl = (3 if rp["delta"] else 1) if rchunk else 1
+            launches += nrl * (1 + len(rev))
             rms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in rev))
             rbytes = rla_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(rp["dtype"]))
+            rkern = ("chunk_tc_kernel<prep-X> x 2 (the solves for beta and gamma) + rla_chunk_kernel<RDN>"
+                     if rp["delta"] else "rla_chunk_kernel<RLA>") if rchunk else "rla_kernel (both states in one pass)"
             rla[name] = {"ms_per_call": rms, "tokens_per_s": world * B_ * T_ / (rms / 1e3),
-                         "kernels": "rla_kernel (both states in one pass)",
+                         "form": "chunkwise" if rchunk else "recurrent", "kernels": rkern, "workspace_bytes": rneed,
                          "algorithmic_bytes": rbytes, "hbm_frac": rbytes / (rms / 1e3) / 1e9 / hbm_peak}
-            del rq, rk, rv, rb, rgm, rgt, rout, rsf, rrf
+            del rq, rk, rv, rb, rgm, rgt, rout, rsf, rrf, rws
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("rla: device status not ok")
 

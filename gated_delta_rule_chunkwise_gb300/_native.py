@@ -8,7 +8,8 @@ Two layers:
   * ``ldn_chunk_fwd``, ``ldn_chunk_fwd_variant``, ``ldn_chunk_fwd_ws``,
     ``ldn_chunk_fwd_workspace_size``, ``ldn_chunk_fwd_noalloc``, ``ldn_decode_step``,
     ``ldn_chunk_fwd_gdn2``, ``ldn_decode_step_gdn2``, ``ldn_backward``,
-    ``ldn_backward_workspace_size``, ``ldn_rla_fwd``, ``ldn_prologue``,
+    ``ldn_backward_workspace_size``, ``ldn_rla_fwd``, ``ldn_rla_fwd_ws``,
+    ``ldn_rla_fwd_workspace_size``, ``ldn_prologue``,
     ``ldn_rmsnorm_gated``,
     ``ldn_get_device_status``, ``ldn_status_string``, ``ldn_version``: the C
     entry points under the same names, taking raw integer pointers;
@@ -62,6 +63,8 @@ _SIGNATURES = {
     "ldn_backward": ([_P] * 14 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
     "ldn_rla_fwd": ([_P] * 6 + [ctypes.c_float] + [_P] * 5 + [_I] * 7 + [_P], _I),
     "ldn_backward_workspace_size": ([_I] * 7, ctypes.c_size_t),
+    "ldn_rla_fwd_ws": ([_P] * 6 + [ctypes.c_float] + [_P] * 5 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
+    "ldn_rla_fwd_workspace_size": ([_I] * 7, ctypes.c_size_t),
     "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
     "ldn_rmsnorm_gated": ([_P] * 4 + [_I] * 5 + [ctypes.c_float, _P], _I),
@@ -154,6 +157,16 @@ def ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final,
                 stream):
     return load().ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv,
                               delta, dtype, stream)
+
+
+def ldn_rla_fwd_ws(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv, delta, dtype,
+                   workspace, workspace_bytes, stream):
+    return load().ldn_rla_fwd_ws(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv,
+                                 delta, dtype, workspace, workspace_bytes, stream)
+
+
+def ldn_rla_fwd_workspace_size(B, T, H, dk, dv, delta, dtype):
+    return load().ldn_rla_fwd_workspace_size(B, T, H, dk, dv, delta, dtype)
 
 
 def ldn_prologue(q_in, k_in, v_in, conv_q, conv_k, conv_v, width, beta_logit, gate_z, gate_a, gate_b,
@@ -368,10 +381,12 @@ def backward(q, k, v, beta, gate, S0, dout, dS_final=None, *, mode, workspace=No
     return g
 
 
-def rla_fwd(q, k, v, beta, gamma, gate, S0=None, R0=None, *, clip=1.0, delta=False, stream=None):
+def rla_fwd(q, k, v, beta, gamma, gate, S0=None, R0=None, *, clip=1.0, delta=False, workspace=True, stream=None):
     """RLA (delta=False) or RDN (delta=True) forward on torch CUDA tensors
-    (ldn_rla_fwd).  q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16); beta,
-    gamma, gate [B,T,H] float32; S0, R0 [B,H,dk,dv] float32 or None.
+    (ldn_rla_fwd_ws).  q, k [B,T,H,dk], v [B,T,H,dv] (float32 or bfloat16); beta,
+    gamma, gate [B,T,H] float32; S0, R0 [B,H,dk,dv] float32 or None.  With
+    workspace=True the workspace ldn_rla_fwd_workspace_size asks for is allocated
+    (Residual DeltaNet then takes the chunk form); False passes none.
     Returns (out, S_final, R_final)."""
     import torch
     B, T, H, dk = q.shape
@@ -383,9 +398,11 @@ def rla_fwd(q, k, v, beta, gamma, gate, S0=None, R0=None, *, clip=1.0, delta=Fal
     out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     sf = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     rf = torch.empty_like(sf)
-    st = ldn_rla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(gate), float(clip), _ptr(S0), _ptr(R0),
-                     _ptr(out), _ptr(sf), _ptr(rf), B, T, H, dk, dv, int(bool(delta)), _dtype_code(q),
-                     _stream_handle(stream))
+    need = ldn_rla_fwd_workspace_size(B, T, H, dk, dv, int(bool(delta)), _dtype_code(q)) if workspace else 0
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+    st = ldn_rla_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(gate), float(clip), _ptr(S0),
+                        _ptr(R0), _ptr(out), _ptr(sf), _ptr(rf), B, T, H, dk, dv, int(bool(delta)), _dtype_code(q),
+                        _ptr(ws), need, _stream_handle(stream))
     if st != LDN_OK:
         raise LdnError(st, "ldn_rla_fwd")
     return out, sf, rf

@@ -514,10 +514,27 @@ extern "C" int ldn_backward(const void *q, const void *k, const void *v, const f
     return launch_backward(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 
+extern "C" size_t ldn_rla_fwd_workspace_size(int B, int T, int H, int dk, int dv, int delta, int dtype)
+{
+    if (validate_common(LDN_GDN, dtype, dk, dv) != LDN_OK || B < 1 || H < 1 || T < 1 || (delta != 0 && delta != 1))
+        return 0;
+    if (dtype != LDN_BF16 || dk != 128 || dv != 128) return 0;   // the chunk form's shapes
+    return rla_chunk_workspace_bytes(B, T, H, delta);
+}
+
 extern "C" int ldn_rla_fwd(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
                            const float *gate, float clip, const float *S0, const float *R0, void *out,
                            float *S_final, float *R_final, int B, int T, int H, int dk, int dv, int delta,
                            int dtype, void *stream)
+{
+    return ldn_rla_fwd_ws(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv, delta,
+                          dtype, nullptr, 0, stream);
+}
+
+extern "C" int ldn_rla_fwd_ws(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                              const float *gate, float clip, const float *S0, const float *R0, void *out,
+                              float *S_final, float *R_final, int B, int T, int H, int dk, int dv, int delta,
+                              int dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
     const int st = validate_common(LDN_GDN, dtype, dk, dv);
     if (st != LDN_OK) return st;
@@ -542,6 +559,13 @@ extern "C" int ldn_rla_fwd(const void *q, const void *k, const void *v, const fl
         if (!aligned16(p)) return LDN_ERR_INVALID_ARG;
     if (!aligned(beta, 4) || !aligned(gamma, 4) || !aligned(gate, 4)) return LDN_ERR_INVALID_ARG;
     RlaArgs a{q, k, v, beta, gamma, gate, S0, R0, clip, out, S_final, R_final, B, T, H, dk, dv, delta, dtype};
+    if (workspace && !aligned(workspace, 256)) return LDN_ERR_INVALID_ARG;
+    // chunk form: bf16, dk = dv = 128; Residual DeltaNet also needs the workspace for its solves
+    if (rla_chunk_supported(a)) {
+        const size_t need = rla_chunk_workspace_bytes(B, T, H, delta);
+        if (need == 0 || (workspace && workspace_bytes >= need))
+            return launch_rla_chunk(a, workspace, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+    }
     return launch_rla(a, s) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 

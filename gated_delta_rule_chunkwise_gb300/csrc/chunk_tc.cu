@@ -2124,6 +2124,11 @@ cudaError_t launch_chunk_presolved(const ChunkArgs &a, uint8_t *ws, cudaStream_t
     return launch_tc<kFed>(a, ws, st);
 }
 
+cudaError_t launch_chunk_solve(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
+{
+    return launch_tc<kPrepX>(a, ws, st);
+}
+
 cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 {
     cudaError_t e = launch_tc<kSplit>(a, ws, st);

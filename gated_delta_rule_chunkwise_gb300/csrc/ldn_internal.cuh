@@ -82,6 +82,9 @@ cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream
 // (presolved_workspace_bytes), then the fused kernel reading it.
 size_t presolved_workspace_bytes(int B, int T, int H);
 cudaError_t launch_chunk_presolved(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
+// The pre-solved variant's solve alone: X = [P T ; T] of every chunk into ws (16 KB per
+// (b, h, chunk), rows 64..127 are T = (I + strict_tril(Diag(beta) (K K^T * Gamma)))^-1).
+cudaError_t launch_chunk_solve(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
 // fastest tensor-core LDN_VARIANT_* by a cost model, given which workspace variants can run
 int chunk_tc_pick(const ChunkArgs &a, bool split_ok, bool presolved_ok);
 bool chunk_pair_supported(const ChunkArgs &a);    // the cluster-pair kernel takes these arguments
@@ -108,6 +111,12 @@ struct RlaArgs {
     int B, T, H, dk, dv, delta, dtype;
 };
 cudaError_t launch_rla(const RlaArgs &a, cudaStream_t stream);
+// Chunk form of the same (csrc/rla_chunk.cu): bf16 inputs, dk = dv = 128, 16-byte aligned
+// q, k, v, out.  Residual DeltaNet needs a workspace of rla_chunk_workspace_bytes (the
+// solves for beta and gamma); Residual Linear Attention none.
+bool rla_chunk_supported(const RlaArgs &a);
+size_t rla_chunk_workspace_bytes(int B, int T, int H, int delta);
+cudaError_t launch_rla_chunk(const RlaArgs &a, void *ws, cudaStream_t stream);
 // Chunkwise backward on the tensor cores (csrc/backward_chunk.cu): DeltaNet / Gated DeltaNet,
 // bf16 inputs, dk = dv = 128, 16-byte aligned q, k, v, dout.
 bool bwd_chunk_supported(const BwdArgs &a);

@@ -25,7 +25,7 @@
  *       Gated DeltaNet-2 (separate erase and write gates, Sec. 2.6);
  *   ldn_backward, ldn_backward_workspace_size
  *       gradients of the forward;
- *   ldn_rla_fwd
+ *   ldn_rla_fwd, ldn_rla_fwd_ws, ldn_rla_fwd_workspace_size
  *       Residual Linear Attention / Residual DeltaNet (the Residual Linear
  *       Attention notes, Sec. 2.2-2.4);
  *   ldn_get_device_status, ldn_status_string, ldn_version.
@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define LDN_VERSION 5
+#define LDN_VERSION 6
 
 /* LDN_GDN2 (Gated DeltaNet-2) is taken only by the *_gdn2 entry points, which
  * carry its two gates; every beta-gated entry point rejects it. */
@@ -389,8 +389,12 @@ size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode
  *   RDN: R_t = alpha_t R_{t-1}(I - gamma_t k_t k_t^T) + gamma_t r_t k_t^T,
  *        S_t = alpha_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T
  *   o_t = alpha_t S_{t-1} q_t + gamma_t R_t q_t      (the UPDATED residual state)
- * One launch: both states step together, token by token, in fp32 (the notes'
- * two-stage computation, Sec. 2.6, is not needed when both states are on chip).
+ * Two forms.  Chunk form (bf16, dk = dv = 128; for Residual DeltaNet only with a
+ * workspace, see ldn_rla_fwd_ws): the notes' two-stage computation (Sec. 2.6) in
+ * chunks of 64 tokens, both states carried chunk to chunk in fp32 and every
+ * product on the tensor cores (fp16 operands, fp32 accumulation); Residual
+ * DeltaNet's two UT solves (for beta and for gamma) run first.  Recurrent form
+ * (every other case): both states step together, token by token, in fp32.
  *   q, k [B][T][H][dk], v, out [B][T][H][dv] of dtype (16-byte aligned)
  *   beta, gamma, gate (log alpha) [B][T][H] fp32 (4-byte aligned)
  *   clip c > 0 (INFINITY: no clip)
@@ -401,6 +405,21 @@ size_t ldn_backward_workspace_size(int B, int T, int H, int dk, int dv, int mode
 int ldn_rla_fwd(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
                 const float *gate, float clip, const float *S0, const float *R0, void *out, float *S_final,
                 float *R_final, int B, int T, int H, int dk, int dv, int delta, int dtype, void *stream);
+
+/* ldn_rla_fwd with a caller-owned DEVICE workspace (256-byte aligned, or NULL):
+ * Residual DeltaNet takes the chunk form when workspace_bytes is at least
+ * ldn_rla_fwd_workspace_size(...) (its solves, 32 KiB per (b, h, chunk)), the
+ * recurrent form otherwise; everything else as ldn_rla_fwd.  The workspace is
+ * written, not read, and must not be used by other work until the call's kernels
+ * have finished on `stream`. */
+int ldn_rla_fwd_ws(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                   const float *gate, float clip, const float *S0, const float *R0, void *out, float *S_final,
+                   float *R_final, int B, int T, int H, int dk, int dv, int delta, int dtype, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace ldn_rla_fwd_ws uses for these sizes (0: none needed, or a
+ * shape without the chunk form).  Pure host function. */
+size_t ldn_rla_fwd_workspace_size(int B, int T, int H, int dk, int dv, int delta, int dtype);
 
 /* Synchronises `stream`, then reads and clears the device status word on the
  * current device.  Returns LDN_OK, LDN_ERR_TIMEOUT (a kernel abandoned a

@@ -51,7 +51,7 @@ def test_diagnostics_live_in_their_own_library(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert ldn.ldn_version() == 5
+    assert ldn.ldn_version() == 6
     for st in range(5):
         assert isinstance(ldn.ldn_status_string(st), str) and ldn.ldn_status_string(st)
     assert "unknown" in ldn.ldn_status_string(99)
@@ -461,3 +461,24 @@ def _rla(**kw):
 ])
 def test_rla_rejects_bad_arguments(lib, kw, want):
     assert _rla(**kw) == want
+
+
+def test_rla_workspace_size(lib):
+    """Chunk form (bf16, dk = dv = 128): Residual DeltaNet's two solves, 16 KiB per
+    (b, h, chunk) each; Residual Linear Attention and the recurrent shapes need none."""
+    B, T, H = 2, 130, 3
+    nch = (T + 63) // 64
+    assert ldn.ldn_rla_fwd_workspace_size(B, T, H, 128, 128, 1, ldn.LDN_BF16) == 2 * B * H * nch * 16384
+    assert ldn.ldn_rla_fwd_workspace_size(B, T, H, 128, 128, 0, ldn.LDN_BF16) == 0
+    assert ldn.ldn_rla_fwd_workspace_size(B, T, H, 128, 128, 1, ldn.LDN_F32) == 0
+    assert ldn.ldn_rla_fwd_workspace_size(B, T, H, 64, 128, 1, ldn.LDN_BF16) == 0
+    assert ldn.ldn_rla_fwd_workspace_size(B, 0, H, 128, 128, 1, ldn.LDN_BF16) == 0
+    assert ldn.ldn_rla_fwd_workspace_size(B, T, H, 128, 128, 2, ldn.LDN_BF16) == 0
+
+
+def test_rla_ws_wants_an_aligned_workspace(lib):
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, None, FAKE, None, None, 1, 64, 1, 128, 128, 1,
+            ldn.LDN_BF16)
+    assert ldn.ldn_rla_fwd_ws(*args, FAKE + 16, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_rla_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, None, None, FAKE, None, None, 1, 64, 1, 128,
+                              128, 1, ldn.LDN_BF16, FAKE, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG

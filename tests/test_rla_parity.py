@@ -1,9 +1,12 @@
-"""GPU parity of ldn_rla_fwd (Residual Linear Attention and Residual DeltaNet,
-one pass) against the fp64 RLA / RDN oracle, element by element.
+"""GPU parity of ldn_rla_fwd / ldn_rla_fwd_ws (Residual Linear Attention and
+Residual DeltaNet) against the fp64 RLA / RDN oracle, element by element, in
+both forms: the chunk form (bf16, dk = dv = 128; Residual DeltaNet with a
+workspace) and the recurrent form (every other case, and Residual DeltaNet
+without a workspace).
 
 Tolerances: fp32 inputs 1e-4; bf16 inputs 2e-2, with the bf16-stored output
-measured beyond its half-ulp rounding as for the other modes (the kernel runs
-both states in fp32)."""
+measured beyond its half-ulp rounding as for the other modes (both forms carry
+the states in fp32; the chunk form's products take fp16 operands)."""
 import numpy as np
 import pytest
 
@@ -24,19 +27,19 @@ def _built():
     ldn.load()
 
 
-def run(p):
+def run(p, workspace=True):
     import torch
     el = torch.bfloat16 if p["dtype"] == "bf16" else torch.float32
     d = lambda a, dt=torch.float32: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dt)
     out, sf, rf = ldn.rla_fwd(d(p["q"], el), d(p["k"], el), d(p["v"], el), d(p["beta"]), d(p["gamma"]), d(p["gate"]),
-                              d(p["S0"]), d(p["R0"]), clip=p["clip"], delta=p["delta"])
+                              d(p["S0"]), d(p["R0"]), clip=p["clip"], delta=p["delta"], workspace=workspace)
     assert ldn.device_status() == ldn.LDN_OK
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), sf.cpu().numpy(), rf.cpu().numpy()
 
 
-def check(p):
-    o, sf, rf = run(p)
+def check(p, workspace=True):
+    o, sf, rf = run(p, workspace)
     ro, rsf, rrf = oracle.fwd_rla(p["q"], p["k"], p["v"], p["beta"], p["gamma"], p["gate"], clip=p["clip"],
                                   S0=p["S0"], R0=p["R0"], delta=p["delta"])
     tol = TOL[p["dtype"]]
@@ -90,3 +93,24 @@ def test_rla_rdn_full_workload_whole_tensors(delta):
     print(f"\n{BASE[delta]}: output: {fmt_parity(po)}; states plain {ps['plain']:.3g} / {pr['plain']:.3g}")
     assert po["excess"] <= TOL["bf16"]
     assert ps["plain"] <= TOL["bf16"] and pr["plain"] <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("delta", [False, True])
+def test_rla_rdn_both_forms(delta):
+    """The same bf16 128 x 128 inputs through the chunk form and (Residual DeltaNet
+    without a workspace) the recurrent form; fp32 inputs take the recurrent form."""
+    p = wl.make_rla(BASE[delta], B=2, T=300, H=2, s0=True)
+    check(p, workspace=True)
+    if delta:
+        check(p, workspace=False)
+    check(wl.make_rla(BASE[delta], B=2, T=300, H=2, dtype="f32", s0=True))
+
+
+@pytest.mark.parametrize("delta", [False, True])
+def test_rla_rdn_strong_decay(delta):
+    """Log-decays of -6 per token: the decay factors across a chunk underflow fp32
+    (e^-378); every factor is formed from a difference of log prefixes, so none
+    overflows, and the states of a chunk's start are forgotten by its end."""
+    p = wl.make_rla(BASE[delta], B=1, T=200, H=2, s0=True)
+    p["gate"] = np.full_like(p["gate"], -6.0)
+    check(p)
