@@ -764,6 +764,38 @@ def run_ours(args):
             graph_ms = max_over_ranks(g0.elapsed_time(g1) / steps)
             del cg
             launches += 3 * steps
+            # the same steps in one ldn_decode_steps call (state read and written once per call)
+            multi = None
+            if not g2:
+                mo = torch.empty((steps, d.B, d.H, d.dv), dtype=torch.float32, device="cuda")
+
+                def mstep():
+                    st = ldn.ldn_decode_steps(td["q"].data_ptr(), td["k"].data_ptr(), td["v"].data_ptr(),
+                                              td["beta"].data_ptr(), td["gate"].data_ptr(), S.data_ptr(), mo.data_ptr(),
+                                              steps, d.B, d.H, d.dk, d.dv, d.mode, ldn.LDN_F32, sh)
+                    if st != ldn.LDN_OK:
+                        raise ldn.LdnError(st, "ldn_decode_steps")
+
+                S.copy_(td["S0"])
+                mstep()
+                mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+                for e0, e1 in mev:
+                    S.copy_(td["S0"])
+                    flush_l2()
+                    e0.record(stream)
+                    mstep()
+                    e1.record(stream)
+                barrier()
+                m_ms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in mev))
+                launches += 1 + len(mev)
+                per_tok = d.B * d.H * (2 * d.dk * 4 + 2 * d.dv * 4 + {0: 4, 1: 8, 2: 4 + 4 * d.dk}[d.mode])
+                mbytes = 2 * d.B * d.H * d.dk * d.dv * 4 + steps * per_tok
+                multi = {"steps_per_call": steps, "ms_per_call": m_ms, "us_per_step": m_ms * 1e3 / steps,
+                         "tokens_per_s": world * d.B * steps / (m_ms / 1e3), "kernels": "decode_steps_kernel",
+                         "algorithmic_bytes": mbytes, "hbm_frac": mbytes / (m_ms / 1e3) / 1e9 / hbm_peak,
+                         "note": "ldn_decode_steps (opt-in): all steps in one launch, the state on chip between "
+                                 "steps; bound by the per-step barriers, not HBM; L2 flushed before each call"}
+                del mo
             if ldn.device_status() != ldn.LDN_OK:
                 raise RuntimeError("decode: device status not ok")
             db = decode_bytes(d.B, d.H, d.dk, d.dv, d.mode)
@@ -773,7 +805,7 @@ def run_ours(args):
                             "warm_back_to_back": {"us_per_step": warm_ms * 1e3, "GB/s": db / (warm_ms / 1e3) / 1e9},
                             "cuda_graph": {"us_per_step": graph_ms * 1e3, "GB/s": db / (graph_ms / 1e3) / 1e9,
                                            "note": "all steps replayed from one captured graph, L2 not flushed"},
-                            "tokens_per_s": world * d.B / (cold_ms / 1e3)}
+                            "tokens_per_s": world * d.B / (cold_ms / 1e3), "multi_step": multi}
             del td, S, o, ptr
 
     line = {"impl": "ours", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -65,6 +65,7 @@ _SIGNATURES = {
     "ldn_backward_workspace_size": ([_I] * 7, ctypes.c_size_t),
     "ldn_rla_fwd_ws": ([_P] * 6 + [ctypes.c_float] + [_P] * 5 + [_I] * 7 + [_P, ctypes.c_size_t, _P], _I),
     "ldn_rla_fwd_workspace_size": ([_I] * 7, ctypes.c_size_t),
+    "ldn_decode_steps": ([_P] * 7 + [_I] * 7 + [_P], _I),
     "ldn_decode_step_gdn2": ([_P] * 8 + [_I] * 5 + [_P], _I),
     "ldn_prologue": ([_P] * 6 + [_I] + [_P] * 9 + [_I] * 7 + [ctypes.c_float, _P], _I),
     "ldn_rmsnorm_gated": ([_P] * 4 + [_I] * 5 + [ctypes.c_float, _P], _I),
@@ -157,6 +158,10 @@ def ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final,
                 stream):
     return load().ldn_rla_fwd(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv,
                               delta, dtype, stream)
+
+
+def ldn_decode_steps(q, k, v, beta, gate, S, out, n_steps, B, H, dk, dv, mode, dtype, stream):
+    return load().ldn_decode_steps(q, k, v, beta, gate, S, out, n_steps, B, H, dk, dv, mode, dtype, stream)
 
 
 def ldn_rla_fwd_ws(q, k, v, beta, gamma, gate, clip, S0, R0, out, S_final, R_final, B, T, H, dk, dv, delta, dtype,
@@ -293,6 +298,31 @@ def decode_step(q, k, v, beta, gate, S, *, mode, out=None, stream=None):
                          B, H, dk, dv, mode, _dtype_code(q), _stream_handle(stream))
     if st != LDN_OK:
         raise LdnError(st, "ldn_decode_step")
+    return out
+
+
+def decode_steps(q, k, v, beta, gate, S, *, mode, out=None, stream=None):
+    """n consecutive recurrent steps in one launch (ldn_decode_steps) on torch CUDA
+    tensors; S [B,H,dk,dv] float32 is updated in place.  q, k [n,B,H,dk], v [n,B,H,dv];
+    beta [n,B,H]; gate [n,B,H] / [n,B,H,dk].  Returns out [n,B,H,dv]."""
+    import torch
+    mode = MODES.get(mode, mode)
+    n, B, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q"); _check(k, "k", q.shape, q.dtype); _check(v, "v", (n, B, H, dv), q.dtype)
+    _check(beta, "beta", (n, B, H), torch.float32)
+    if mode == LDN_DELTANET:
+        gate = None
+    else:
+        _check(gate, "gate", (n, B, H) if mode == LDN_GDN else (n, B, H, dk), torch.float32)
+    _check(S, "S", (B, H, dk, dv), torch.float32)
+    if out is None:
+        out = torch.empty((n, B, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", (n, B, H, dv), q.dtype)
+    st = ldn_decode_steps(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gate), _ptr(S), _ptr(out), n,
+                          B, H, dk, dv, mode, _dtype_code(q), _stream_handle(stream))
+    if st != LDN_OK:
+        raise LdnError(st, "ldn_decode_steps")
     return out
 
 

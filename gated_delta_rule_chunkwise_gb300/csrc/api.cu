@@ -340,6 +340,30 @@ extern "C" int ldn_decode_step(const void *q, const void *k, const void *v, cons
     return launch_decode(a, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
 }
 
+extern "C" int ldn_decode_steps(const void *q, const void *k, const void *v, const float *beta,
+                                const float *gate, float *S, void *out, int n_steps,
+                                int B, int H, int dk, int dv, int mode, int dtype, void *stream)
+{
+    if (mode == LDN_GDN2) return LDN_ERR_UNSUPPORTED;   // its step is ldn_decode_step_gdn2
+    int st = validate_common(mode, dtype, dk, dv);
+    if (st != LDN_OK) return st;
+    if (B < 1 || H < 1 || n_steps < 0) return LDN_ERR_INVALID_ARG;
+    if ((long long)B * H > (1LL << 24) || (long long)n_steps * B * H * (dk > dv ? dk : dv) > (1LL << 40))
+        return LDN_ERR_UNSUPPORTED;
+    if (!S) return LDN_ERR_INVALID_ARG;
+    if (n_steps == 0) return LDN_OK;
+    if (!q || !k || !v || !beta || !out) return LDN_ERR_INVALID_ARG;
+    if (mode != LDN_DELTANET && !gate) return LDN_ERR_INVALID_ARG;
+    const uintptr_t el = dtype == LDN_BF16 ? 2 : 4;
+    if (!aligned16(S)) return LDN_ERR_INVALID_ARG;
+    const void *el_ptrs[] = {q, k, v, out};
+    for (const void *p : el_ptrs)
+        if (!aligned(p, el)) return LDN_ERR_INVALID_ARG;
+    if (!aligned(beta, 4) || (gate && !aligned(gate, 4))) return LDN_ERR_INVALID_ARG;
+    DecodeArgs a{q, k, v, beta, mode == LDN_DELTANET ? nullptr : gate, S, out, B, H, dk, dv, mode, dtype, nullptr};
+    return launch_decode_steps(a, n_steps, (cudaStream_t)stream) == cudaSuccess ? LDN_OK : LDN_ERR_CUDA;
+}
+
 static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 {
     if (!a || !b || na == 0 || nb == 0) return false;

@@ -90,6 +90,8 @@ int chunk_tc_pick(const ChunkArgs &a, bool split_ok, bool presolved_ok);
 bool chunk_pair_supported(const ChunkArgs &a);    // the cluster-pair kernel takes these arguments
 cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+// nsteps consecutive steps in one launch (DeltaNet, Gated DeltaNet, KDA); inputs [nsteps][B][H][..].
+cudaError_t launch_decode_steps(const DecodeArgs &a, int nsteps, cudaStream_t stream);
 
 // Backward of the recurrence (csrc/backward.cu).
 struct BwdArgs {

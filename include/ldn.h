@@ -20,7 +20,7 @@
  *   ldn_chunk_fwd, _variant, _select, _ws, _workspace_size, _select_ws, _noalloc
  *       the chunkwise forward and its kernel families;
  *   ldn_prologue, ldn_rmsnorm_gated     the steps on either side of it;
- *   ldn_decode_step                     one recurrent token;
+ *   ldn_decode_step, ldn_decode_steps                     one recurrent token;
  *   ldn_chunk_fwd_gdn2, ldn_decode_step_gdn2
  *       Gated DeltaNet-2 (separate erase and write gates, Sec. 2.6);
  *   ldn_backward, ldn_backward_workspace_size
@@ -291,6 +291,22 @@ int ldn_rmsnorm_gated(const void *o, const void *g, const float *weight, void *y
 int ldn_decode_step(const void *q, const void *k, const void *v, const float *beta,
                     const float *gate, float *S, void *out,
                     int B, int H, int dk, int dv, int mode, int dtype, void *stream);
+
+/*
+ * ldn_decode_steps -- n_steps consecutive ldn_decode_step calls on the same
+ * sequences in one launch (DeltaNet, Gated DeltaNet, KDA), for inputs known in
+ * advance (several tokens of one sequence taken in recurrent form).  Each step is
+ * the arithmetic of ldn_decode_step; the state slices stay on chip between the
+ * steps, so S is read once and written once per call.
+ *   q, k  [n_steps][B][H][dk] dtype     v, out [n_steps][B][H][dv] dtype
+ *   beta  [n_steps][B][H] fp32          gate   GDN [n_steps][B][H], KDA
+ *                                              [n_steps][B][H][dk] fp32, DN ignored
+ *   S     [B][H][dk][dv] fp32, read and overwritten in place (16-byte aligned)
+ *   n_steps >= 0 (0: nothing to do); B, H >= 1; dk, dv in {64, 128}.
+ * LDN_ERR_UNSUPPORTED for Gated DeltaNet-2 (its step is ldn_decode_step_gdn2).
+ */
+int ldn_decode_steps(const void *q, const void *k, const void *v, const float *beta, const float *gate, float *S,
+                     void *out, int n_steps, int B, int H, int dk, int dv, int mode, int dtype, void *stream);
 
 /*
  * Gated DeltaNet-2 (linear-attention notes, Sec. 2.6, Eqs. 21-24): the erase

@@ -482,3 +482,21 @@ def test_rla_ws_wants_an_aligned_workspace(lib):
     assert ldn.ldn_rla_fwd_ws(*args, FAKE + 16, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG
     assert ldn.ldn_rla_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, None, None, FAKE, None, None, 1, 64, 1, 128,
                               128, 1, ldn.LDN_BF16, FAKE, 1 << 20, None) == ldn.LDN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(S=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(S=FAKE + 8), ldn.LDN_ERR_INVALID_ARG),
+    (dict(gate=None), ldn.LDN_ERR_INVALID_ARG),
+    (dict(n=-1), ldn.LDN_ERR_INVALID_ARG),
+    (dict(mode=ldn.LDN_GDN2), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(dk=96), ldn.LDN_ERR_UNSUPPORTED),
+    (dict(n=0, q=None, v=None, out=None), ldn.LDN_OK),   # nothing to do
+])
+def test_decode_steps_rejects_bad_arguments(lib, kw, want):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, gate=FAKE, S=FAKE, out=FAKE, n=4, B=1, H=1, dk=64, dv=64,
+             mode=ldn.LDN_GDN, dtype=ldn.LDN_F32)
+    a.update(kw)
+    assert ldn.ldn_decode_steps(a["q"], a["k"], a["v"], a["beta"], a["gate"], a["S"], a["out"], a["n"], a["B"],
+                                a["H"], a["dk"], a["dv"], a["mode"], a["dtype"], None) == want
