@@ -572,7 +572,8 @@ def run_ours(args):
 
             res = {}
             for what, fn, nb_, nl in (("prologue", pro, prologue_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(p["dtype"]),
-                                                                       p["mode"], p["width"]), 2 if dk_ == dv_ else 3),
+                                                                       p["mode"], p["width"]),
+                                                                       (1 if dk_ == dv_ else 2) + (p["mode"] == 2)),
                                       ("rmsnorm_gated", epi, rmsnorm_bytes(B_, T_, H_, dv_, el_bytes_of(p["dtype"])), 1)):
                 for _ in range(3):
                     fn()
@@ -828,30 +829,44 @@ def run_ours(args):
 
 def run_profile_case(args):
     """Two untimed calls of one operation on a given shape (a small case for an
-    ncu capture): backward-gdn / backward-kda (ldn_backward), gdn2
-    (ldn_chunk_fwd_gdn2), kda (ldn_chunk_fwd_noalloc) or rdn (ldn_rla_fwd),
-    automatic variant, bf16, d = 128, the workload recipe of the named mode."""
+    ncu capture): gdn (ldn_chunk_fwd_ws, the variant the cost model picks, as
+    the timed step runs it), backward-gdn / backward-kda (ldn_backward), gdn2
+    (ldn_chunk_fwd_gdn2), kda (ldn_chunk_fwd_noalloc), rla / rdn
+    (ldn_rla_fwd_ws), automatic variant, bf16, d = 128, the workload recipe of
+    the named mode."""
     import numpy as np
     import torch
     import gated_delta_rule_chunkwise_gb300 as ldn
     from gated_delta_rule_chunkwise_gb300 import workloads as wl
     ldn.load()
     B, T, H = (int(x) for x in args.shape.split(","))
-    if args.profile == "rdn":
-        p = wl.make_rla("rdn_bf16_b4_t2048_h16_d128", B=B, T=T, H=H)
+    if args.profile in ("rla", "rdn"):
+        p = wl.make_rla(f"{args.profile}_bf16_b4_t2048_h16_d128", B=B, T=T, H=H)
         d = lambda a, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dt)
         for _ in range(2):
             ldn.rla_fwd(d(p["q"], torch.bfloat16), d(p["k"], torch.bfloat16), d(p["v"], torch.bfloat16), d(p["beta"]),
-                        d(p["gamma"]), d(p["gate"]), clip=p["clip"], delta=True)
+                        d(p["gamma"]), d(p["gate"]), clip=p["clip"], delta=p["delta"])
         torch.cuda.synchronize()
         st = ldn.device_status()
         print(json.dumps({"profile_case": args.profile, "shape": [B, T, H], "status": st}))
         return 0 if st == ldn.LDN_OK else 1
     name = {"backward-gdn": "gdn_bf16_b4_t2048_h16_d128", "backward-kda": "kda_bf16_b8_t4096_h16_d128",
-            "gdn2": "gdn2_bf16_b8_t4096_h16_d128", "kda": "kda_bf16_b8_t4096_h16_d128"}[args.profile]
+            "gdn2": "gdn2_bf16_b8_t4096_h16_d128", "kda": "kda_bf16_b8_t4096_h16_d128",
+            "gdn": "gdn_bf16_b4_t2048_h16_d128"}[args.profile]
     w = wl.make_chunk(name, B=B, T=T, H=H)
     t = w.torch_inputs("cuda")
-    if args.profile.startswith("backward"):
+    if args.profile == "gdn":
+        out = torch.empty_like(t["v"])
+        wsb = ldn.ldn_chunk_fwd_workspace_size(B, T, H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16)
+        wsp = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        var = ldn.ldn_chunk_fwd_select_ws(B, T, H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16, wsb)
+        for _ in range(2):
+            st = ldn.ldn_chunk_fwd_ws(t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(), t["beta"].data_ptr(),
+                                      t["gate"].data_ptr(), 0, out.data_ptr(), 0, B, T, H, w.dk, w.dv, 64, w.mode,
+                                      ldn.LDN_BF16, var, wsp.data_ptr(), wsb, torch.cuda.current_stream().cuda_stream)
+            if st != ldn.LDN_OK:
+                raise ldn.LdnError(st, "ldn_chunk_fwd_ws")
+    elif args.profile.startswith("backward"):
         dout, dsf = wl.make_upstream(w)
         d = torch.from_numpy(dout).to("cuda", t["q"].dtype)
         f = torch.from_numpy(dsf).cuda()
@@ -888,7 +903,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workload lines")
-    ap.add_argument("--profile", choices=["backward-gdn", "backward-kda", "gdn2", "kda", "rdn"],
+    ap.add_argument("--profile", choices=["gdn", "backward-gdn", "backward-kda", "gdn2", "kda", "rla", "rdn"],
                     help="run one operation twice, untimed, on --shape (a small case for ncu) and exit")
     ap.add_argument("--shape", default="1,2048,16", help="B,T,H for --profile")
     args = ap.parse_args()
