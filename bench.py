@@ -530,9 +530,13 @@ def run_ours(args):
             oms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in oev))
             ob = chunk_bytes(ow.B, ow.T, ow.H, ow.dk, ow.dv, oel, ow.mode, ow.S0 is not None, True)
             kern = KERNEL_NAME.get(ochosen, "simt")
+            osrc = {"tcgen05": ["chunk_tc.cu"], "pair": ["chunk_tc.cu"], "presolved": ["chunk_tc.cu"],
+                    "split": ["chunk_tc.cu", "chunk_state.cu"]}.get(kern, ["chunk_simt.cu"])
+            otraffic = recorded_traffic(f"chunk_{kern}:{name}", kernel_source_hash(osrc))
             others[name] = {"tokens_per_s": world * ow.B * ow.T / (oms / 1e3), "ms_per_launch": oms,
                             "kernel": f"chunk_{kern}", "algorithmic_bytes": ob,
-                            "hbm_frac": ob / (oms / 1e3) / 1e9 / hbm_peak}
+                            "hbm_frac": ob / (oms / 1e3) / 1e9 / hbm_peak, "traffic": otraffic,
+                            "traffic_over_algorithmic": None if otraffic is None else otraffic / ob}
             del ot, oout, osf, ows
         if ldn.device_status() != ldn.LDN_OK:
             raise RuntimeError("other workloads: device status not ok")
