@@ -94,3 +94,19 @@ def test_chunkwise_backward_is_deterministic():
     for n in a:
         if a[n] is not None:
             assert np.array_equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_chunkwise_backward_strong_decay_and_many_heads(mode):
+    """Log-decays of -6 per token (a chunk's decay products underflow fp32: every
+    factor is a difference of log prefixes, at most 1) and 32 heads in one call."""
+    w = wl.make_chunk(BASE[mode], B=2, T=130, H=32, mode=mode, s0=True)
+    if w.gate is not None:
+        w.gate[...] = -6.0
+    dout, dsf = wl.make_upstream(w)
+    got = run_bwd(w, dout, dsf, S0=True)
+    ref = oracle.bwd(w.q, w.k, w.v, w.beta, w.gate, w.S0, dout, dsf, mode=mode)
+    for name, g in got.items():
+        if g is not None:
+            assert np.all(np.isfinite(g)), name
+    compare(got, ref, f"mode {mode} strong decay")
