@@ -153,10 +153,12 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     named_sync(kBar, kThreads);
 
     const bool top = st < 64;
-    for (int c = 0; c < nchunks; ++c) {
+    // one vote per chunk, taken at the barrier that ends the chunk: thread 0 first waits for
+    // the next chunk's operands, so every thread leaves the loop at the same chunk
+    bool go = nchunks > 0 && vote(st == 0 ? mbar_wait(&full[0], 0, kWaitNs) : true);
+    for (int c = 0; go && c < nchunks; ++c) {
         const int s = c % kStages, t0 = c * kC, L = min(kC, T - t0);
         uint8_t *stg = sm + s * kStageBytes;
-        if (!vote(st == 0 ? mbar_wait(&full[s], (c / kStages) & 1, kWaitNs) : true)) break;
 
         // ---- MMA5: D5 = [Q~ ; -W] H
         if (st == 0) {
@@ -165,6 +167,9 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
             for (int k = 0; k < kDK / 16; ++k)
                 umma_bf16(tbase + kColD5, kmajor_desc(a5_s, 128, k), mnmajor_desc(hb_s, 128, k), id_mma5, k > 0);
             umma_commit(smma);
+            // every reader of chunk c - 1's stage was done at the vote that ended it: chunk c + 2
+            // goes there (issued behind this chunk's first product, off its critical path)
+            if (c >= 1 && c + 2 < nchunks) issue_load(c + 2);
         }
         wait_smma();
 
@@ -235,9 +240,8 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        named_sync(kBar, kThreads);
-        // every reader of stage s is done (MMA5, the RV read, MMA6, e^{g_C}): chunk c + 3 goes there
-        if (st == 0 && c + kStages < nchunks) issue_load(c + kStages);
+        const int cn = c + 1;
+        go = vote(st == 0 && cn < nchunks ? mbar_wait(&full[cn % kStages], (cn / kStages) & 1, kWaitNs) : true);
     }
 
     if (fail == 0 && S_final) {
