@@ -1728,14 +1728,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         named_sync(kBarSerial, kSerialThreads);
         if (PAIR && prank == 1) pair_service(0);
 
-        for (int c = 0; c < nchunks; ++c) {
+        // ---- S1: MMA3 / MMA4 of chunk c complete (RV[s] = [P U' ; U'], DK[s] = [-P W ; W],
+        //      KDA: [Q~ ; W]).  One vote per chunk, taken at the barrier that ends the chunk
+        //      before (thread 0 first waits for this chunk's ready barrier), so every thread
+        //      leaves the loop at the same chunk.
+        bool go = nchunks > 0 && serial_vote(st == 0 ? mbar_wait(&S.bar_ready[0], 0, kWaitNs) : true);
+        for (int c = 0; go && c < nchunks; ++c) {
             const int s = c & 1, t0 = (cb + c) * kC, L = min(kC, T - t0);
             const uint8_t *QK = sm + LY::qk + (c % kStages) * kQKBytes;
             const uint32_t k_s = smem_u32(QK) + 8192;
-
-            // ---- S1: MMA3 / MMA4 of chunk c complete (RV[s] = [P U' ; U'], DK[s] = [-P W ; W],
-            //      KDA: [Q~ ; W])
-            if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
             tc_fence_after();
             // KDA: MMA3 / MMA4 have read V, Q^ and K^, and MMA6 takes K~ from the side
             // tile: the ring stage of chunk c is free already
@@ -1905,7 +1906,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(kBarSerial, kSerialThreads);
+            const int cn = c + 1;
+            go = serial_vote(st == 0 && cn < nchunks ? mbar_wait(&S.bar_ready[cn & 1], (cn >> 1) & 1, kWaitNs) : true);
         }
 
         if (S.fail == 0 && S_final) {
