@@ -46,6 +46,15 @@ FALLBACK_HBM_GBS = 6800.0
 MODE_NAME = {0: "deltanet", 1: "gdn", 2: "kda", 3: "gdn2"}
 KERNEL_NAME = {2: "tcgen05", 3: "split", 4: "pair", 5: "presolved"}   # LDN_VARIANT_* -> kernel family in the JSON line
 TWO_LAUNCH = (3, 5)   # variants that make two launches per call (split, pre-solved)
+
+
+def chunk_launches(chosen, B, T, H, dk, dv, mode, dt, ws_bytes):
+    """Kernel launches of one chunkwise forward call: the split variant makes four when it
+    cuts long sequences into segments (maps, scan, outputs after the preparation)."""
+    import gated_delta_rule_chunkwise_gb300 as ldn
+    if chosen == 3 and ldn.ldn_chunk_fwd_split_segments(B, T, H, dk, dv, 64, mode, dt, ws_bytes) >= 3:
+        return 4
+    return 2 if chosen in TWO_LAUNCH else 1
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -395,7 +404,8 @@ def run_ours(args):
     barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    launches = args.steps * (2 if chosen in TWO_LAUNCH else 1)
+    per_call = chunk_launches(chosen, w.B, w.T, w.H, w.dk, w.dv, w.mode, dtype_code, ws_bytes)
+    launches = args.steps * per_call
     if ldn.device_status() != ldn.LDN_OK:
         raise RuntimeError("device status not ok after the timed region")
     per = [e0.elapsed_time(e1) for e0, e1 in evs]
@@ -480,7 +490,7 @@ def run_ours(args):
         e1.record(s_down)
         torch.cuda.synchronize()
         barrier()
-        launches += args.steps * (2 if chosen in TWO_LAUNCH else 1)
+        launches += args.steps * per_call
         ems = max_over_ranks(e0.elapsed_time(e1) / args.steps)
         e2e = {"value": world * tokens / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems,
@@ -526,7 +536,9 @@ def run_ours(args):
                 ostep()
                 e1.record(stream)
             barrier()
-            launches += 4 * (2 if ochosen in TWO_LAUNCH else 1)
+            onl = (2 if ochosen in TWO_LAUNCH else 1) if g2 else chunk_launches(ochosen, ow.B, ow.T, ow.H, ow.dk,
+                                                                                 ow.dv, ow.mode, odt, ows_bytes)
+            launches += 4 * onl
             oms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in oev))
             ob = chunk_bytes(ow.B, ow.T, ow.H, ow.dk, ow.dv, oel, ow.mode, ow.S0 is not None, True)
             kern = KERNEL_NAME.get(ochosen, "simt")
@@ -534,7 +546,7 @@ def run_ours(args):
                     "split": ["chunk_tc.cu", "chunk_state.cu"]}.get(kern, ["chunk_simt.cu"])
             otraffic = recorded_traffic(f"chunk_{kern}:{name}", kernel_source_hash(osrc))
             others[name] = {"tokens_per_s": world * ow.B * ow.T / (oms / 1e3), "ms_per_launch": oms,
-                            "kernel": f"chunk_{kern}", "algorithmic_bytes": ob,
+                            "kernel": f"chunk_{kern}", "launches_per_call": onl, "algorithmic_bytes": ob,
                             "hbm_frac": ob / (oms / 1e3) / 1e9 / hbm_peak, "traffic": otraffic,
                             "traffic_over_algorithmic": None if otraffic is None else otraffic / ob}
             del ot, oout, osf, ows

@@ -57,6 +57,7 @@ _SIGNATURES = {
     "ldn_chunk_fwd_ws": ([_P] * 8 + [_I] * 9 + [_P, ctypes.c_size_t, _P], _I),
     "ldn_chunk_fwd_workspace_size": ([_I] * 8, ctypes.c_size_t),
     "ldn_chunk_fwd_select_ws": ([_I] * 8 + [ctypes.c_size_t], _I),
+    "ldn_chunk_fwd_split_segments": ([_I] * 8 + [ctypes.c_size_t], _I),
     "ldn_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 9 + [_P], _I),
     "ldn_decode_step": ([_P] * 7 + [_I] * 6 + [_P], _I),
     "ldn_chunk_fwd_gdn2": ([_P] * 9 + [_I] * 8 + [_P], _I),
@@ -122,6 +123,10 @@ def ldn_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, mode, dtype):
 
 def ldn_chunk_fwd_select_ws(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes):
     return load().ldn_chunk_fwd_select_ws(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes)
+
+
+def ldn_chunk_fwd_split_segments(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes):
+    return load().ldn_chunk_fwd_split_segments(B, T, H, dk, dv, chunk, mode, dtype, workspace_bytes)
 
 
 def ldn_chunk_fwd_noalloc(q, k, v, beta, gate, S0, out, S_final, B, T, H, dk, dv, chunk, mode, dtype,

@@ -52,9 +52,12 @@ static int validate_common(int mode, int dtype, int dk, int dv, bool g2 = false)
     return LDN_OK;
 }
 
-// Workspace bytes of the split variant (0: it does not take these sizes).
+// Workspace bytes of the split variant (0: it does not take these sizes): the operand images
+// (`base` true: all the variant needs) and, for long sequences, the sequence split's states and
+// maps (chunk_state.cu).
 // (Pointers are taken as aligned: a Gated DeltaNet-2 call gets stand-in gates here.)
-static size_t split_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)
+static size_t split_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                                    bool base = false)
 {
     if (T < 1 || B < 1 || H < 1) return 0;
     alignas(16) static const float kAligned[4] = {0.f, 0.f, 0.f, 0.f};
@@ -62,7 +65,8 @@ static size_t split_workspace_bytes(int B, int T, int H, int dk, int dv, int chu
     a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = B; a.T = T; a.H = H;
     a.erase = a.write = kAligned;
     if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return 0;
-    return (size_t)B * H * (size_t)((T + chunk - 1) / chunk) * split_unit_bytes(dv);
+    const int nch = (T + chunk - 1) / chunk;
+    return (size_t)B * H * (size_t)nch * split_unit_bytes(dv) + (base ? 0 : split_seg_bytes(B * H, nch, dv));
 }
 
 // Argument checks shared by the chunk entry points (everything but the
@@ -130,7 +134,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
                 B, T, H, dk, dv, chunk, mode, dtype, nullptr};
     a.erase = erase;
     a.write = write;
-    const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype) : 0;
+    const size_t need = tc ? split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype, true) : 0;
     const bool ws_ok = ws && aligned(ws, 256) && need > 0 && ws_bytes >= need;
     const bool pre_ok = tc && ws && aligned(ws, 256) && ws_bytes >= presolved_workspace_bytes(B, T, H);
     if (variant == LDN_VARIANT_AUTO) variant = !tc ? LDN_VARIANT_SIMT : chunk_tc_pick(a, ws_ok, pre_ok);
@@ -140,7 +144,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (!a.status) return LDN_ERR_CUDA;
     cudaError_t err;
     if (variant == LDN_VARIANT_PRESOLVED) err = launch_chunk_presolved(a, (uint8_t *)ws, s);
-    else if (variant == LDN_VARIANT_SPLIT) err = launch_chunk_split(a, (uint8_t *)ws, s);
+    else if (variant == LDN_VARIANT_SPLIT) err = launch_chunk_split(a, (uint8_t *)ws, ws_bytes, s);
     else if (variant == LDN_VARIANT_PAIR) err = launch_chunk_pair(a, s);
     else if (variant == LDN_VARIANT_TENSOR) err = launch_chunk_tc(a, s);
     else err = launch_chunk_simt(a, s);
@@ -235,6 +239,8 @@ static int noalloc_impl(const void *q, const void *k, const void *v, const float
     // One piece: sequences b0 .. b0+np-1, tokens t0 .. t0+len-1 (t0 > 0 only when np == 1).
     auto piece = [&](int b0, int np, int t0, int len, const float *s0, float *sf, size_t ws_bytes) {
         const size_t tok = ((size_t)b0 * T + t0) * H;   // token-head offset of (b0, t0)
+        if (variant == LDN_VARIANT_SPLIT)   // the operand images alone: no sequence split here
+            ws_bytes = std::min(ws_bytes, (size_t)np * H * (size_t)((len + chunk - 1) / chunk) * unit);
         return chunk_fwd_impl((const uint8_t *)q + tok * dk * el, (const uint8_t *)k + tok * dk * el,
                               (const uint8_t *)v + tok * dv * el, beta ? beta + tok : nullptr,
                               gate ? gate + tok * gate_w : nullptr, s0, (uint8_t *)out + tok * dv * el, sf, np, len,
@@ -287,9 +293,22 @@ extern "C" int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int 
     a.dk = dk; a.dv = dv; a.chunk = chunk; a.mode = mode; a.dtype = dtype; a.B = B; a.T = T; a.H = H;
     a.erase = a.write = kAligned;
     if (dtype != LDN_BF16 || !chunk_tc_supported(a)) return LDN_VARIANT_SIMT;
-    const size_t need = split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype);
+    const size_t need = split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype, true);
     return chunk_tc_pick(a, need > 0 && workspace_bytes >= need,
                          T > 0 && workspace_bytes >= presolved_workspace_bytes(B, T, H));
+}
+
+extern "C" int ldn_chunk_fwd_split_segments(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                                            size_t workspace_bytes)
+{
+    const int st = validate_common(mode, dtype, dk, dv, mode == LDN_GDN2);
+    if (st != LDN_OK) return -st;
+    if (chunk != 64) return -LDN_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || T < 0) return -LDN_ERR_INVALID_ARG;
+    const size_t base = split_workspace_bytes(B, T, H, dk, dv, chunk, mode, dtype, true);
+    if (base == 0) return 0;
+    const int nch = (T + chunk - 1) / chunk, nseg = split_segments(B * H, nch, dv);
+    return nseg >= 3 && workspace_bytes >= base + split_seg_bytes(B * H, nch, dv) ? nseg : 1;
 }
 
 extern "C" size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype)

@@ -62,9 +62,22 @@ __device__ __forceinline__ void st_row16(uint8_t *block, int row, int col, const
         make_uint4(pack_h2(v[8], v[9]), pack_h2(v[10], v[11]), pack_h2(v[12], v[13]), pack_h2(v[14], v[15]));
 }
 
+// Sequence split (`pass` 1 and 2; dv = 128): the chunks of each (b, h) form `nseg` segments of
+// `cps` chunks.  Pass 1, per (b, h): segment 0 from S0 with its outputs (its final state is
+// the state entering segment 1), and for every segment s = 1 .. nseg-2 its affine map
+// H_out = M_s H_in + N_s: N_s from a zero state, M_s (dk x dk) from the identity with the U'
+// term dropped, no outputs.  A scan then gives every segment its incoming state, and pass 2
+// runs segments 1 .. nseg-1 from them with their outputs (the last one writes S_final).  Pass
+// 0 is the whole sequence from S0.  `seg` holds, per (b, h), the states entering the segments
+// and the maps: [3 nseg][dk][128] fp32 (seg_slot()).
+__host__ __device__ constexpr size_t seg_slot(int unit, int nseg, int kind, int s)
+{   // kind 0: state entering segment s; 1: N_s; 2: M_s
+    return (((size_t)unit * 3 * nseg + (size_t)kind * nseg + s) * kDK) * 128;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat16 *__restrict__ out, float *S_final,
-                   int T, int H, int dv, int *status)
+                   int T, int H, int dv, int *status, int pass, int nseg, int cps, float *seg)
 {
     extern __shared__ uint8_t dsmem[];
     uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
@@ -81,11 +94,26 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
 
     const int st = threadIdx.x, warp = st >> 5;
     const int slices = dv / kDVS;
-    const int unit = blockIdx.x / slices, sl = blockIdx.x % slices;
-    const int b = unit / H, h = unit % H, n0 = sl * kDVS;
     const int nchunks = (T + kC - 1) / kC;
+    // this CTA's job: (b, h), dv slice, chunk range, initial state, whether U' and outputs count,
+    // where the final state goes
+    const int jobs = pass == 0 ? slices : pass == 1 ? 2 + 4 * (nseg - 2) : 2 * (nseg - 1);
+    const int unit = blockIdx.x / jobs, j = blockIdx.x % jobs;
+    int sl = j % 2, sg = 0, kind = 0;   // kind 0: a run with outputs; 1: N map; 2: M map
+    if (pass == 0) sl = j;
+    else if (pass == 1 && j >= 2) { sg = 1 + (j - 2) / 4; kind = 1 + ((j - 2) % 4) / 2; }
+    else if (pass == 2) sg = 1 + j / 2;
+    const int cs = pass == 0 ? 0 : sg * cps, ce = pass == 0 ? nchunks : min(nchunks, (sg + 1) * cps);
+    const int nloc = ce - cs;
+    const bool use_rv = kind != 2, write_out = kind == 0;
+    const int b = unit / H, h = unit % H, n0 = sl * kDVS;
     const size_t ub = split_unit_bytes(dv);
-    const uint8_t *base = ws + (size_t)unit * nchunks * ub;
+    const uint8_t *base = ws + ((size_t)unit * nchunks + cs) * ub;   // operands of the CTA's first chunk
+    const float *init = pass == 0 || (pass == 1 && sg == 0) ? (S0 ? S0 + (size_t)unit * kDK * dv : nullptr)
+                        : pass == 2 ? seg + seg_slot(unit, nseg, 0, sg) : nullptr;
+    float *fin = pass == 0 ? (S_final ? S_final + (size_t)unit * kDK * dv : nullptr)
+                 : pass == 1 ? seg + seg_slot(unit, nseg, sg == 0 ? 0 : kind, sg == 0 ? 1 : sg)
+                 : sg == nseg - 1 ? (S_final ? S_final + (size_t)unit * kDK * dv : nullptr) : nullptr;
     const uint32_t lane_base = (32u * (uint32_t)warp) << 16;
 
     if (st == 0) {
@@ -119,7 +147,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
         bulk_load(stg + kOEG, u + split_eg_off(dv), 512, &full[s]);
     };
     if (st == 0)
-        for (int c = 0; c < kStages && c < nchunks; ++c) issue_load(c);
+        for (int c = 0; c < kStages && c < nloc; ++c) issue_load(c);
 
     auto vote = [&](bool ok) -> bool {   // same decision in every thread
         const bool bad = named_sync_or(kBar, kThreads, !ok || fail != 0);
@@ -140,12 +168,15 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
 
     float Hreg[kDVS];
     {
-        const float *src = S0 ? S0 + ((size_t)unit * kDK + st) * dv + n0 : nullptr;
+        const float *src = init ? init + (size_t)st * dv + n0 : nullptr;
 #pragma unroll
         for (int n = 0; n < kDVS; n += 4) {
             const float4 x = src ? *reinterpret_cast<const float4 *>(src + n) : make_float4(0.f, 0.f, 0.f, 0.f);
             Hreg[n] = x.x; Hreg[n + 1] = x.y; Hreg[n + 2] = x.z; Hreg[n + 3] = x.w;
         }
+        if (kind == 2)   // M map: columns n0 .. n0 + 63 of the identity
+#pragma unroll
+            for (int n = 0; n < kDVS; ++n) Hreg[n] = st == n0 + n ? 1.f : 0.f;
 #pragma unroll
         for (int n = 0; n < kDVS; n += 16) st_row16(HB, st, n, &Hreg[n]);
     }
@@ -155,9 +186,9 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     const bool top = st < 64;
     // one vote per chunk, taken at the barrier that ends the chunk: thread 0 first waits for
     // the next chunk's operands, so every thread leaves the loop at the same chunk
-    bool go = nchunks > 0 && vote(st == 0 ? mbar_wait(&full[0], 0, kWaitNs) : true);
-    for (int c = 0; go && c < nchunks; ++c) {
-        const int s = c % kStages, t0 = c * kC, L = min(kC, T - t0);
+    bool go = nloc > 0 && vote(st == 0 ? mbar_wait(&full[0], 0, kWaitNs) : true);
+    for (int lc = 0; go && lc < nloc; ++lc) {   // lc: the chunk's place in the CTA's range
+        const int c = cs + lc, s = lc % kStages, t0 = c * kC, L = min(kC, T - t0);
         uint8_t *stg = sm + s * kStageBytes;
 
         // ---- MMA5: D5 = [Q~ ; -W] H
@@ -169,7 +200,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
             umma_commit(smma);
             // every reader of chunk c - 1's stage was done at the vote that ended it: chunk c + 2
             // goes there (issued behind this chunk's first product, off its critical path)
-            if (c >= 1 && c + 2 < nchunks) issue_load(c + 2);
+            if (lc >= 1 && lc + 2 < nloc) issue_load(lc + 2);
         }
         wait_smma();
 
@@ -181,7 +212,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
             for (int q = 0; q < kDVS / 16; ++q) tmem_ld16(tbase + lane_base + kColD5 + 16 * q, v + 16 * q);
             tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < kDVS / 8; ++q) {
+            for (int q = 0; q < kDVS / 8 && use_rv; ++q) {
                 const uint4 w = *reinterpret_cast<const uint4 *>(rv + sw128_offset(st, 8 * q));
                 const __half2 *h2 = reinterpret_cast<const __half2 *>(&w);
 #pragma unroll
@@ -192,7 +223,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
                 }
             }
             if (top) {
-                if (st < L) {
+                if (write_out && st < L) {
                     uint4 *dst = reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + st) * H + h) * dv + n0);
 #pragma unroll
                     for (int q = 0; q < kDVS / 8; ++q)
@@ -220,7 +251,7 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
                 umma_bf16(tbase + kColD6, mnmajor_desc(kt_s, 64, k), mnmajor_desc(ub_s, 64, k), id_mma6, k > 0);
             umma_commit(s6);
         }
-        if (!mbar_wait(s6, (uint32_t)(c & 1), kWaitNs)) fail = 1;
+        if (!mbar_wait(s6, (uint32_t)(lc & 1), kWaitNs)) fail = 1;
         tc_fence_after();
 
         // ---- H <- e^{g_C} H + K~^T U (row st), fp16 copy for the next MMA5
@@ -240,12 +271,12 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        const int cn = c + 1;
-        go = vote(st == 0 && cn < nchunks ? mbar_wait(&full[cn % kStages], (cn / kStages) & 1, kWaitNs) : true);
+        const int cn = lc + 1;
+        go = vote(st == 0 && cn < nloc ? mbar_wait(&full[cn % kStages], (cn / kStages) & 1, kWaitNs) : true);
     }
 
-    if (fail == 0 && S_final) {
-        float *dst = S_final + ((size_t)unit * kDK + st) * dv + n0;
+    if (fail == 0 && fin) {
+        float *dst = fin + (size_t)st * dv + n0;
 #pragma unroll
         for (int n = 0; n < kDVS; n += 4)
             *reinterpret_cast<float4 *>(dst + n) = make_float4(Hreg[n], Hreg[n + 1], Hreg[n + 2], Hreg[n + 3]);
@@ -266,16 +297,99 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
+// The scan of the sequence split: seg(0, s) = M_{s-1} seg(0, s-1) + N_{s-1}, s = 2 .. nseg-1, in
+// fp32.  One CTA of 256 threads per ((b, h), 16-column slice of the state): its slice of each
+// state depends only on its slice of the one before, so the CTA runs its steps alone.  M sits
+// in shared memory with rows padded to 129 words (a warp reads one column of 32 rows without
+// bank conflicts), the incoming slice as it is; thread = (row, 8 columns).
+constexpr int kScanLd = kDK + 1;
+constexpr int kScanSmem = (kDK * kScanLd + kDK * 16) * 4;
+
+__global__ void __launch_bounds__(256) seg_scan_kernel(float *seg, int nseg)
+{
+    extern __shared__ __align__(16) float ssm[];
+    float *Ms = ssm, *Xs = ssm + kDK * kScanLd;
+    const int unit = blockIdx.x >> 3, c0 = (blockIdx.x & 7) * 16, tid = threadIdx.x;
+    const int r = tid & 127, cc = 8 * (tid >> 7);
+    for (int s = 2; s < nseg; ++s) {
+        const float *M = seg + seg_slot(unit, nseg, 2, s - 1), *N = seg + seg_slot(unit, nseg, 1, s - 1);
+        const float *X = seg + seg_slot(unit, nseg, 0, s - 1);
+        float *Y = seg + seg_slot(unit, nseg, 0, s);
+        __syncthreads();   // the previous step's reads of Ms and Xs are done; its writes of X are seen
+        for (int e = tid; e < kDK * kDK / 4; e += 256) {
+            const float4 m = reinterpret_cast<const float4 *>(M)[e];
+            float *d = Ms + (e >> 5) * kScanLd + 4 * (e & 31);
+            d[0] = m.x; d[1] = m.y; d[2] = m.z; d[3] = m.w;
+        }
+        for (int e = tid; e < kDK * 4; e += 256)
+            reinterpret_cast<float4 *>(Xs)[e] = *reinterpret_cast<const float4 *>(X + (e >> 2) * 128 + c0 + 4 * (e & 3));
+        __syncthreads();
+        float acc[8];
+        {
+            const float4 n0 = *reinterpret_cast<const float4 *>(N + r * 128 + c0 + cc);
+            const float4 n1 = *reinterpret_cast<const float4 *>(N + r * 128 + c0 + cc + 4);
+            acc[0] = n0.x; acc[1] = n0.y; acc[2] = n0.z; acc[3] = n0.w;
+            acc[4] = n1.x; acc[5] = n1.y; acc[6] = n1.z; acc[7] = n1.w;
+        }
+#pragma unroll 8
+        for (int kk = 0; kk < kDK; ++kk) {
+            const float m = Ms[r * kScanLd + kk];
+            const float4 x0 = *reinterpret_cast<const float4 *>(Xs + kk * 16 + cc);
+            const float4 x1 = *reinterpret_cast<const float4 *>(Xs + kk * 16 + cc + 4);
+            acc[0] = fmaf(m, x0.x, acc[0]); acc[1] = fmaf(m, x0.y, acc[1]);
+            acc[2] = fmaf(m, x0.z, acc[2]); acc[3] = fmaf(m, x0.w, acc[3]);
+            acc[4] = fmaf(m, x1.x, acc[4]); acc[5] = fmaf(m, x1.y, acc[5]);
+            acc[6] = fmaf(m, x1.z, acc[6]); acc[7] = fmaf(m, x1.w, acc[7]);
+        }
+        *reinterpret_cast<float4 *>(Y + r * 128 + c0 + cc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(Y + r * 128 + c0 + cc + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream_t st)
+int split_segments(int units, int nchunks, int dv)
 {
-    const unsigned grid = (unsigned)((long long)a.B * a.H * (a.dv / kDVS));
+    if (dv != 128 || units < 1) return 1;
+    const int sms = sm_count();
+    if (sms <= 0 || sms / units < 6) return 1;
+    int nseg = (sms / units - 2) / 4 + 2;   // pass 1 takes 2 + 4 (nseg - 2) CTAs per (b, h): one wave
+    nseg = std::min(nseg, std::min(8, nchunks / 16));
+    return nseg >= 3 ? nseg : 1;
+}
+
+size_t split_seg_bytes(int units, int nchunks, int dv)
+{
+    const int nseg = split_segments(units, nchunks, dv);
+    return nseg >= 3 ? (size_t)units * 3 * nseg * kDK * 128 * 4 : 0;
+}
+
+cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, size_t ws_bytes, cudaStream_t st)
+{
+    const int units = a.B * a.H, nch = (a.T + kC - 1) / kC;
     cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    chunk_state_kernel<<<grid, kThreads, kSmemBytes, st>>>(ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H,
-                                                           a.dv, a.status);
+    const size_t base = (size_t)units * nch * split_unit_bytes(a.dv);
+    const int nseg = split_segments(units, nch, a.dv);
+    const size_t extra = split_seg_bytes(units, nch, a.dv);
+    if (nseg >= 3 && ws_bytes >= base + extra) {
+        float *seg = reinterpret_cast<float *>(const_cast<uint8_t *>(ws) + base);
+        const int cps = (nch + nseg - 1) / nseg;
+        chunk_state_kernel<<<(unsigned)(units * (2 + 4 * (nseg - 2))), kThreads, kSmemBytes, st>>>(
+            ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.dv, a.status, 1, nseg, cps, seg);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem)) !=
+            cudaSuccess)
+            return e;
+        seg_scan_kernel<<<(unsigned)(units * 8), 256, kScanSmem, st>>>(seg, nseg);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        chunk_state_kernel<<<(unsigned)(units * 2 * (nseg - 1)), kThreads, kSmemBytes, st>>>(
+            ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.dv, a.status, 2, nseg, cps, seg);
+        return cudaGetLastError();
+    }
+    chunk_state_kernel<<<(unsigned)(units * (a.dv / kDVS)), kThreads, kSmemBytes, st>>>(
+        ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.dv, a.status, 0, 1, nch, nullptr);
     return cudaGetLastError();
 }
 

@@ -1973,7 +1973,6 @@ bool chunk_tc_supported(const ChunkArgs &a)
            (a.mode == LDN_DELTANET || a.mode == LDN_GDN || kda_ok || g2_ok);
 }
 
-namespace {
 int sm_count()
 {
     static int sms[64] = {0};
@@ -1984,6 +1983,7 @@ int sm_count()
     return sms[dev];
 }
 
+namespace {
 template <int KIND>
 cudaError_t launch_tc(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
 {
@@ -2075,7 +2075,8 @@ cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t st) { return laun
 //     tiles that a third ring stage frees only late, and runs slower beside the busier
 //     serial warps);
 //   split: 20 us + preparation waves x chunks per range x 5.4 / 10.8 us + state waves x
-//     chunks x 1.6 us;
+//     chunks x 1.6 us (with a sequence split: 10 us + 2 x chunks per segment x 1.6 us + 3 us
+//     per scan step);
 //   pre-solved: 22 us + prep-X chunks per slot x 3.2 / 6.6 us (two / one CTAs per SM) +
 //     waves x chunks x 2.2 / 6.3 us.
 // The fused and pair kernels win when their CTAs fill the SMs once and the sequences are
@@ -2103,7 +2104,12 @@ int chunk_tc_pick(const ChunkArgs &a, bool split_ok, bool presolved_ok)
         if (pair < cost) { cost = pair; best = LDN_VARIANT_PAIR; }
     }
     if (split_ok) {
-        const double split = 20.0 + (double)waves_p * cpr * t_prep + (double)waves_f * nchunks * t_state;
+        // a sequence split runs the state recurrence twice over segments of cps chunks, with a
+        // scan of 3 us per segment between (chunk_state.cu)
+        const int nseg = split_segments((int)heads, (int)nchunks, a.dv);
+        const double state = nseg >= 3 ? 10.0 + 2.0 * ((nchunks + nseg - 1) / nseg) * t_state + 3.0 * (nseg - 2)
+                                        : (double)waves_f * nchunks * t_state;
+        const double split = 20.0 + (double)waves_p * cpr * t_prep + state;
         if (split < cost) { cost = split; best = LDN_VARIANT_SPLIT; }
     }
     if (presolved_ok) {
@@ -2131,11 +2137,11 @@ cudaError_t launch_chunk_solve(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
     return launch_tc<kPrepX>(a, ws, st);
 }
 
-cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t st)
+cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, size_t ws_bytes, cudaStream_t st)
 {
     cudaError_t e = launch_tc<kSplit>(a, ws, st);
     if (e != cudaSuccess) return e;
-    return launch_chunk_state(a, ws, st);
+    return launch_chunk_state(a, ws, ws_bytes, st);
 }
 
 }  // namespace ldn

@@ -76,8 +76,16 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs &a);
 // Split variant: preparation kernel (chunk_tc.cu) then state kernel (chunk_state.cu).
-cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, cudaStream_t stream);
-cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, cudaStream_t stream);
+// ws_bytes >= the operand images (units x chunks x split_unit_bytes); with split_seg_bytes()
+// more, long sequences are cut into segments that run side by side (chunk_state.cu).
+cudaError_t launch_chunk_split(const ChunkArgs &a, uint8_t *ws, size_t ws_bytes, cudaStream_t stream);
+cudaError_t launch_chunk_state(const ChunkArgs &a, const uint8_t *ws, size_t ws_bytes, cudaStream_t stream);
+// Segments per (b, h) of the split variant's state kernel (1: no split), and the fp32 bytes
+// they need beyond the operand images (0 when there is no split).
+int split_segments(int units, int nchunks, int dv);
+size_t split_seg_bytes(int units, int nchunks, int dv);
+// Streaming multiprocessors of the current device (0 if it cannot be read).
+int sm_count();
 // Pre-solved variant (chunk_tc.cu): X = [P T ; T] of every chunk into the workspace
 // (presolved_workspace_bytes), then the fused kernel reading it.
 size_t presolved_workspace_bytes(int B, int T, int H);

@@ -17,7 +17,7 @@
  * Attention notes, Sec. 1.2.
  *
  * Entry points, in the order below:
- *   ldn_chunk_fwd, _variant, _select, _ws, _workspace_size, _select_ws, _noalloc
+ *   ldn_chunk_fwd, _variant, _select, _ws, _workspace_size, _select_ws, _split_segments, _noalloc
  *       the chunkwise forward and its kernel families;
  *   ldn_prologue, ldn_rmsnorm_gated     the steps on either side of it;
  *   ldn_decode_step, ldn_decode_steps                     one recurrent token;
@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define LDN_VERSION 6
+#define LDN_VERSION 7
 
 /* LDN_GDN2 (Gated DeltaNet-2) is taken only by the *_gdn2 entry points, which
  * carry its two gates; every beta-gated entry point rejects it. */
@@ -155,8 +155,21 @@ int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype);
  *   (16 KiB each); K~ = K Diag-scaled by e^{g_C - g} fp16 (16 KiB); e^{g_C}
  *   per key channel fp32 (512 B).
  *
+ * Sequence split: when few (b, h) are long (dv = 128, at least 48 chunks each,
+ * and B*H at most a sixth of the SM count), the state recurrence of each (b, h)
+ * is cut into nseg = 3 .. 8 segments that run side by side: every segment's
+ * affine map H_out = M H_in + N (M dk x dk, N dk x dv, fp32) is formed from the
+ * operand images, a scan gives every segment its incoming state, and the
+ * segments then run again from those states with their outputs.  This takes
+ * B*H*3*nseg*dk*dv*4 more bytes after the operand images (segment states and
+ * maps, fp32); with only the operand images the recurrence runs unsplit.  The
+ * two forms agree up to fp32 rounding of the maps.
+ *
  * ldn_chunk_fwd_workspace_size: bytes of workspace the split variant needs for
- * these sizes, or 0 when it does not take them.  Pure host function.
+ * these sizes (the operand images, plus the sequence split's states and maps
+ * where it applies), or 0 when it does not take them.  Host function; whether
+ * the sequence split applies depends on the SM count of the current device
+ * (none when no device can be read).
  */
 size_t ldn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype);
 
@@ -187,6 +200,16 @@ int ldn_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *b
 int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
                             size_t workspace_bytes);
 
+/* Segments per (b, h) into which ldn_chunk_fwd_ws's split variant cuts the state
+ * recurrence for these sizes and a workspace of workspace_bytes (the sequence
+ * split above): nseg >= 3, or 1 when it runs unsplit (the variant then makes
+ * two launches; split, four: the preparation, the segments' maps, the scan and
+ * the segments' outputs).  -LDN_ERR_* for arguments ldn_chunk_fwd_ws would
+ * reject, 0 when the split variant does not take these sizes.  Host function;
+ * it reads the SM count of the current device. */
+int ldn_chunk_fwd_split_segments(int B, int T, int H, int dk, int dv, int chunk, int mode, int dtype,
+                                 size_t workspace_bytes);
+
 /*
  * ldn_chunk_fwd_noalloc -- ldn_chunk_fwd_ws without a caller workspace.
  * The pages have no counterpart to this entry: it is a convenience of this
@@ -204,8 +227,9 @@ int ldn_chunk_fwd_select_ws(int B, int T, int H, int dk, int dv, int chunk, int 
  * fp32 state carried between runs in S_final (or in a slot of the array when
  * S_final is NULL).  The pieces are enqueued on `stream` one after another;
  * the result is bit-identical to that of ldn_chunk_fwd_ws with the split
- * variant and a caller workspace (the same kernels on the same operands; the
- * state passes between pieces in fp32, as between chunks).
+ * variant and a caller workspace of the operand images alone (the same kernels
+ * on the same operands; the state passes between pieces in fp32, as between
+ * chunks).  The sequence split is not used here.
  *
  * The first call on a device resolves the array's address and creates an
  * event; it must not be made while `stream` is being captured into a CUDA

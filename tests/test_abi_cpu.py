@@ -51,7 +51,7 @@ def test_diagnostics_live_in_their_own_library(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert ldn.ldn_version() == 6
+    assert ldn.ldn_version() == 7
     for st in range(5):
         assert isinstance(ldn.ldn_status_string(st), str) and ldn.ldn_status_string(st)
     assert "unknown" in ldn.ldn_status_string(99)
@@ -214,6 +214,19 @@ def test_split_workspace_size_is_per_chunk_operands(lib):
     assert ldn.ldn_chunk_fwd_workspace_size(1, 64, 1, 64, 128, 64, 1, 1) == 0    # dk = 64
     assert ldn.ldn_chunk_fwd_workspace_size(1, 0, 1, 128, 128, 64, 1, 1) == 0    # empty sequence
     assert ldn.ldn_chunk_fwd_workspace_size(1, 64, 1, 128, 128, 32, 1, 1) == 0   # chunk != 64
+
+
+def test_split_segments_answers_without_a_device(lib):
+    """With no device the SM count is unknown: the recurrence runs unsplit (1), the
+    workspace is the operand images alone; 0 where the split variant does not apply,
+    -LDN_ERR_* for rejected arguments."""
+    big = (1 << 64) - 1
+    assert ldn.ldn_chunk_fwd_split_segments(1, 65536, 16, 128, 128, 64, 1, 1, big) == 1
+    assert ldn.ldn_chunk_fwd_workspace_size(1, 65536, 16, 128, 128, 64, 1, 1) == 16 * 1024 * (32768 + 2 * 16384 + 16896)
+    assert ldn.ldn_chunk_fwd_split_segments(1, 64, 1, 128, 128, 64, 0, 0, big) == 0    # fp32: no split variant
+    assert ldn.ldn_chunk_fwd_split_segments(1, 64, 1, 128, 128, 32, 1, 1, big) == -ldn.LDN_ERR_UNSUPPORTED
+    assert ldn.ldn_chunk_fwd_split_segments(0, 64, 1, 128, 128, 64, 1, 1, big) == -ldn.LDN_ERR_INVALID_ARG
+    assert ldn.ldn_chunk_fwd_split_segments(1, 64, 1, 128, 128, 64, 7, 1, big) == -ldn.LDN_ERR_INVALID_ARG
 
 
 def test_split_without_workspace_is_rejected(lib):

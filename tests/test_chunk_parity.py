@@ -208,6 +208,57 @@ def test_split_equals_fused_up_to_rounding():
     assert ulp_excess < 1e-2 and rel_err(s2, s1) < 1e-2
 
 
+# ---- split variant with the sequence split: long (b, h) cut into segments run side by side ----
+def _segments(w, ws_bytes):
+    return ldn.ldn_chunk_fwd_split_segments(w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16, ws_bytes)
+
+
+def _base_bytes(w):
+    """The operand images alone (no room for the segment states and maps)."""
+    return w.B * w.H * ((w.T + 63) // 64) * (32768 + (w.dv // 64) * 16384 + 16896)
+
+
+@pytest.mark.parametrize("mode,B,T,H,s0,nseg", [(1, 1, 8192 + 37, 1, True, 8), (1, 1, 64 * 60 + 5, 2, True, 3),
+                                                (2, 1, 5000, 3, True, 4), (0, 2, 4000, 2, False, 3),
+                                                (1, 1, 64 * 112, 1, False, 7)])
+def test_sequence_split_parity(mode, B, T, H, s0, nseg):
+    """Segment counts 3 .. 8, ragged last chunk and uneven last segment, with and without
+    S0, every mode; the whole output and final state against the oracle."""
+    w = wl.make_chunk(BASE[mode], B=B, T=T, H=H, dk=128, dv=128, mode=mode, dtype="bf16", s0=s0)
+    need = ldn.ldn_chunk_fwd_workspace_size(w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16)
+    assert need > _base_bytes(w) and _segments(w, need) == nseg
+    o, s = run_gpu(w, ldn.LDN_VARIANT_SPLIT, S0=s0, workspace=True)
+    ro, rs = oracle_chunk(w)
+    eo, es = out_err(o, ro, w.dtype), rel_err(s, rs)
+    assert eo <= TOL["bf16"] and es <= TOL["bf16"], f"nseg {nseg}: out {eo:.3g} state {es:.3g}"
+
+
+def test_sequence_split_matches_unsplit_recurrence():
+    """The same call with a workspace of the operand images alone runs the recurrence
+    unsplit: both forms agree up to rounding (the maps compose in fp32), and without a
+    final state asked for."""
+    import torch
+    w = wl.make_chunk(BASE[1], B=1, T=6000, H=2, s0=True)
+    t = w.torch_inputs("cuda")
+    base = _base_bytes(w)
+    need = ldn.ldn_chunk_fwd_workspace_size(w.B, w.T, w.H, w.dk, w.dv, 64, w.mode, ldn.LDN_BF16)
+    assert _segments(w, need) >= 3 and _segments(w, base) == 1
+    res = []
+    for nbytes in (base, need):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        o, sf = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"], mode=w.mode,
+                              variant=ldn.LDN_VARIANT_SPLIT, workspace=ws)
+        o2, sf2 = ldn.chunk_fwd(t["q"], t["k"], t["v"], t["beta"], t["gate"], t["S0"], mode=w.mode,
+                                variant=ldn.LDN_VARIANT_SPLIT, want_state=False, workspace=ws)
+        torch.cuda.synchronize()
+        assert ldn.device_status() == ldn.LDN_OK and sf2 is None
+        assert torch.equal(o, o2)
+        res.append((o.float().cpu().numpy(), sf.cpu().numpy()))
+    (o1, s1), (o2, s2) = res
+    ulp_excess = np.maximum(np.abs(o2 - o1) - 2.0 ** -7 * np.abs(o1), 0.0).max() / np.sqrt(np.mean(o1 ** 2))
+    assert ulp_excess < 1e-2 and rel_err(s2, s1) < 1e-2
+
+
 # ---- cluster-pair variant (two CTAs per (b, h) share the preparation) ----
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("B,T,H,s0", [(1, 64, 1, False), (2, 65, 3, True), (1, 1, 2, True), (2, 500, 4, True),
