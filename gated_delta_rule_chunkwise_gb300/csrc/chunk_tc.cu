@@ -2074,9 +2074,9 @@ cudaError_t launch_chunk_pair(const ChunkArgs &a, cudaStream_t st) { return laun
 //   pair: 10 us + waves x chunks x 5.0 us (measured: each CTA's preparation waits for
 //     tiles that a third ring stage frees only late, and runs slower beside the busier
 //     serial warps);
-//   split: 20 us + preparation waves x chunks per range x 5.4 / 10.8 us + state waves x
-//     chunks x 1.6 us (with a sequence split: 10 us + 2 x chunks per segment x 1.6 us + 3 us
-//     per scan step);
+//   split: 20 us + preparation waves x chunks per range x 5.4 / 10.8 us + state waves (one
+//     CTA per (b, h)) x chunks x 1.6 us (with a sequence split: 10 us + 2 x chunks per segment
+//     x 1.6 us + 4 us per scan step);
 //   pre-solved: 22 us + prep-X chunks per slot x 3.2 / 6.6 us (two / one CTAs per SM) +
 //     waves x chunks x 2.2 / 6.3 us.
 // The fused and pair kernels win when their CTAs fill the SMs once and the sequences are
@@ -2107,8 +2107,8 @@ int chunk_tc_pick(const ChunkArgs &a, bool split_ok, bool presolved_ok)
         // a sequence split runs the state recurrence twice over segments of cps chunks, with a
         // scan of 3 us per segment between (chunk_state.cu)
         const int nseg = split_segments((int)heads, (int)nchunks, a.dv);
-        const double state = nseg >= 3 ? 10.0 + 2.0 * ((nchunks + nseg - 1) / nseg) * t_state + 3.0 * (nseg - 2)
-                                        : (double)waves_f * nchunks * t_state;
+        const double state = nseg >= 3 ? 10.0 + 2.0 * ((nchunks + nseg - 1) / nseg) * t_state + 4.0 * (nseg - 2)
+                                        : (double)((heads + sms - 1) / sms) * nchunks * t_state;
         const double split = 20.0 + (double)waves_p * cpr * t_prep + state;
         if (split < cost) { cost = split; best = LDN_VARIANT_SPLIT; }
     }

@@ -156,8 +156,8 @@ int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype);
  *   per key channel fp32 (512 B).
  *
  * Sequence split: when few (b, h) are long (dv = 128, at least 48 chunks each,
- * and B*H at most a sixth of the SM count), the state recurrence of each (b, h)
- * is cut into nseg = 3 .. 8 segments that run side by side: every segment's
+ * and B*H at most a fifth of the SM count), the state recurrence of each (b, h)
+ * is cut into nseg = 3 .. 16 segments that run side by side: every segment's
  * affine map H_out = M H_in + N (M dk x dk, N dk x dv, fp32) is formed from the
  * operand images, a scan gives every segment its incoming state, and the
  * segments then run again from those states with their outputs.  This takes
