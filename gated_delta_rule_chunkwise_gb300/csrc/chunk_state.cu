@@ -351,6 +351,286 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
     if (warp == 0) tmem_dealloc(tbase, P::kTmemCols);
 }
 
+// dv = 128: the same recurrence transposed, so that the lanes of tensor memory are dv columns
+// and any warp may take any rows of [O ; U] (D^T = H^T [Q~ ; -W]^T, the H^T and U^T operands
+// in tensor memory):
+//   [O ; U]^T = RV^T + H^T A5^T       (MMA5: A = H^T in TMEM, B = the A5 image, K-major)
+//   H^T      <- H^T Diag(e^{g_C}) + U^T K~   (MMA6: A = U^T in TMEM, B = the K~ image, MN-major)
+// The workspace's RV part holds RV^T for dv = 128 (block 0 = (P U')^T, block 1 = U'^T, rows =
+// dv columns).  256 threads: lane n = dv column, warp half hh; in the epilogue half 0 forms U^T
+// (one warp on every SM sub-partition: the step's critical path) and half 1 the output; in the
+// state update half hh holds key channels 64 hh .. 64 hh + 63 of row n of H^T.  A5 lands in a
+// two-stage ring, RV^T | K~ | e^{g_C} in a three-stage one, each part loaded two chunks ahead.
+struct PlanT {
+    static constexpr int kThreads = 256;
+    static constexpr int kAStages = 2, kBStages = 3;
+    static constexpr uint32_t kA = 32768;                          // A5 image
+    static constexpr uint32_t kORV = 0, kOKT = 32768, kOEG = 49152;   // within a B stage
+    static constexpr uint32_t kTxB = 32768 + 16384 + 512;
+    static constexpr uint32_t kB = 50176;                          // B stage, 1024-aligned
+    static constexpr uint32_t kOffB = kAStages * kA;
+    static constexpr uint32_t kOffBars = kOffB + kBStages * kB;
+    static constexpr uint32_t kSmemBytes = kOffBars + 128 + 1024;   // bars: a[2], b[3], smma, s6, drain[2]
+    // tensor memory: D5^T, D6^T (fp32, 128 columns each), H^T (fp16 pairs, 64), U^T (fp16 pairs, 32)
+    static constexpr uint32_t kColD5 = 0, kColD6 = 128, kColH = 256, kColU = 320, kTmemCols = 512;
+    static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+    static_assert(kOKT == split_kt_off(128) - kSplitRvOff && kOEG == split_eg_off(128) - kSplitRvOff,
+                  "B stage must mirror the workspace image");
+};
+
+__device__ __forceinline__ void pack_h16(const float *v, uint32_t *w)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_h2(v[2 * i], v[2 * i + 1]);
+}
+
+__global__ void __launch_bounds__(PlanT::kThreads, 1)
+chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat16 *__restrict__ out,
+                     float *S_final, int T, int H, int *status, int pass, int nseg, int cps, float *seg)
+{
+    using P = PlanT;
+    constexpr int kThreads = P::kThreads, dv = 128;
+    extern __shared__ uint8_t dsmem[];
+    uint8_t *sm = dsmem + ((1024u - (smem_u32(dsmem) & 1023u)) & 1023u);
+    uint64_t *full_a = reinterpret_cast<uint64_t *>(sm + P::kOffBars);   // [kAStages]: A5
+    uint64_t *full_b = full_a + P::kAStages;                             // [kBStages]: RV^T | K~ | e^{g_C}
+    uint64_t *smma = full_b + P::kBStages;
+    uint64_t *s6 = smma + 1;
+    uint64_t *drain = s6 + 1;   // [2]: unused slot kept for the layout; thread 0 issues every MMA
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int fail;
+
+    const int st = threadIdx.x, warp = st >> 5;
+    const int n = st & 127, hh = st >> 7;   // dv column (TMEM lane), warp half
+    const int nchunks = (T + kC - 1) / kC;
+    const int jobs = seg_jobs(pass, nseg);
+    const int unit = blockIdx.x / jobs, j = blockIdx.x % jobs;
+    int sg = 0, kind = 0;   // kind 0: a run with outputs; 1: N map; 2: M map
+    if (pass == 1 && j >= 1) { sg = 1 + (j - 1) / 2; kind = 1 + (j - 1) % 2; }
+    else if (pass == 2) sg = 1 + j;
+    const int cs = pass == 0 ? 0 : sg * cps, ce = pass == 0 ? nchunks : min(nchunks, (sg + 1) * cps);
+    const int nloc = ce - cs;
+    const bool use_rv = kind != 2, write_out = kind == 0;
+    const int b = unit / H, h = unit % H;
+    const size_t ub = split_unit_bytes(dv);
+    const uint8_t *base = ws + ((size_t)unit * nchunks + cs) * ub;
+    const float *init = pass == 0 || (pass == 1 && sg == 0) ? (S0 ? S0 + (size_t)unit * kDK * dv : nullptr)
+                        : pass == 2 ? seg + seg_slot(unit, nseg, 0, sg) : nullptr;
+    float *fin = pass == 0 ? (S_final ? S_final + (size_t)unit * kDK * dv : nullptr)
+                 : pass == 1 ? seg + seg_slot(unit, nseg, sg == 0 ? 0 : kind, sg == 0 ? 1 : sg)
+                 : sg == nseg - 1 ? (S_final ? S_final + (size_t)unit * kDK * dv : nullptr) : nullptr;
+    const uint32_t lane_base = (32u * (uint32_t)(warp & 3)) << 16;
+
+    if (st == 0) {
+        for (int i = 0; i < P::kAStages; ++i) mbar_init(&full_a[i], 1);
+        for (int i = 0; i < P::kBStages; ++i) mbar_init(&full_b[i], 1);
+        mbar_init(smma, 1);
+        mbar_init(s6, 1);
+        mbar_init(&drain[0], 1);
+        fence_mbar_init();
+        fail = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_s, P::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_s;
+    const uint32_t trow = tbase + lane_base;   // this warp's lanes
+
+    int pend_a[P::kAStages] = {-1, -1}, pend_b[P::kBStages] = {-1, -1, -1};   // thread 0
+    // A map (no outputs) loads only what its U rows use: the -W rows of A5 (rows 64..127 of
+    // both 64-column K blocks), U'^T (RV^T block 1; none for M), K~ and e^{g_C}.  What it leaves
+    // stale feeds only the O columns of its products, which it never reads.
+    auto load_a = [&](int c) {
+        const int s = c % P::kAStages;
+        uint8_t *d = sm + s * P::kA;
+        const uint8_t *u = base + (size_t)c * ub;
+        pend_a[s] = c;
+        if (write_out) {
+            mbar_arrive_expect_tx(&full_a[s], P::kA);
+            bulk_load(d, u, P::kA, &full_a[s]);
+        } else {
+            mbar_arrive_expect_tx(&full_a[s], P::kA / 2);
+            bulk_load(d + 8192, u + 8192, 8192, &full_a[s]);
+            bulk_load(d + 16384 + 8192, u + 16384 + 8192, 8192, &full_a[s]);
+        }
+    };
+    auto load_b = [&](int c) {
+        const int s = c % P::kBStages;
+        uint8_t *d = sm + P::kOffB + s * P::kB;
+        const uint8_t *u = base + (size_t)c * ub + kSplitRvOff;
+        pend_b[s] = c;
+        if (write_out) {
+            mbar_arrive_expect_tx(&full_b[s], P::kTxB);
+            bulk_load(d, u, P::kTxB, &full_b[s]);
+        } else {
+            mbar_arrive_expect_tx(&full_b[s], (use_rv ? 16384 : 0) + 16384 + 512);
+            if (use_rv) bulk_load(d + 16384, u + 16384, 16384, &full_b[s]);
+            bulk_load(d + P::kOKT, u + P::kOKT, 16384 + 512, &full_b[s]);
+        }
+    };
+    if (st == 0)
+        for (int c = 0; c < 2 && c < nloc; ++c) {
+            load_a(c);
+            load_b(c);
+        }
+
+    auto vote = [&](bool ok) -> bool {   // same decision in every thread
+        const bool bad = named_sync_or(kBar, kThreads, !ok || fail != 0);
+        if (bad && st == 0) fail = 1;
+        return !bad;
+    };
+    uint32_t sphase = 0;
+    auto wait_smma = [&]() {
+        if (!mbar_wait(smma, sphase, kWaitNs)) fail = 1;
+        sphase ^= 1u;
+        tc_fence_after();
+    };
+    const uint32_t id_mma5 = idesc_f16kind_f32(128, 128, 0, 0, kMmaF16);   // A (TMEM) K-major, B K-major
+    const uint32_t id_mma6 = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16);   // B MN-major
+
+    // H^T row n, key channels 64 hh .. 64 hh + 63 (fp32, registers); fp16 copy in TMEM
+    float Hreg[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        const int k = 64 * hh + i;
+        Hreg[i] = kind == 2 ? (n == k ? 1.f : 0.f) : init ? init[(size_t)k * dv + n] : 0.f;
+    }
+    {
+        uint32_t w[32];
+        pack_h16(Hreg, w);
+        pack_h16(Hreg + 32, w + 16);
+        tmem_st16u(trow + P::kColH + 32 * hh, w);
+        tmem_st16u(trow + P::kColH + 32 * hh + 16, w + 16);
+        tmem_st_wait();
+    }
+    tc_fence_before();
+
+    // one vote per chunk, taken at the barrier that ends the chunk: thread 0 first waits for
+    // the next chunk's A5, so every thread leaves the loop at the same chunk
+    bool go = nloc > 0 && vote(st == 0 ? mbar_wait(&full_a[0], 0, kWaitNs) : true);
+    for (int lc = 0; go && lc < nloc; ++lc) {
+        const int c = cs + lc, t0 = c * kC, L = min(kC, T - t0);
+        const int sa = lc % P::kAStages, sb = lc % P::kBStages;
+        const uint8_t *stb = sm + P::kOffB + sb * P::kB;
+
+        // ---- MMA5: D5^T = H^T A5^T
+        if (st == 0) {
+            tc_fence_after();
+            const uint32_t a5_s = smem_u32(sm + sa * P::kA);
+            for (int k = 0; k < kDK / 16; ++k)
+                umma_ts(tbase + P::kColD5, tbase + P::kColH + 8 * k, kmajor_desc(a5_s, 128, k), id_mma5, k > 0);
+            umma_commit(smma);
+            // the B part of chunk lc + 2 goes where chunk lc - 1's was: every reader of it was
+            // done at the vote that ended chunk lc - 1
+            if (lc + 2 < nloc) load_b(lc + 2);
+        }
+        wait_smma();
+        if (st == 0 && lc + 2 < nloc) load_a(lc + 2);   // MMA5 has read this chunk's A5
+
+        if (!mbar_wait(&full_b[sb], (uint32_t)(lc / P::kBStages) & 1u, kWaitNs)) fail = 1;
+        {
+            // half 0: U^T = U'^T - (W H)^T (columns 64..127); half 1: O^T (columns 0..63)
+            const uint8_t *rv = stb + P::kORV + (hh ? 0 : 16384);
+            float v[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(trow + P::kColD5 + (hh ? 0 : 64) + 16 * q, v + 16 * q);
+            tmem_ld_wait();
+            if (use_rv) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(rv + sw128_offset(n, 8 * q));
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&w);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __half22float2(h2[i]);
+                        v[8 * q + 2 * i] += f.x;
+                        v[8 * q + 2 * i + 1] += f.y;
+                    }
+                }
+            }
+            if (hh == 0) {
+                uint32_t w[32];
+                pack_h16(v, w);
+                pack_h16(v + 32, w + 16);
+                tmem_st16u(trow + P::kColU, w);
+                tmem_st16u(trow + P::kColU + 16, w + 16);
+                tmem_st_wait();
+                tc_fence_before();
+                named_sync(kBarU, kThreads / 2);
+                // ---- MMA6: D6^T = U^T K~
+                if (st == 0) {
+                    tc_fence_after();
+                    const uint32_t kt_s = smem_u32(stb + P::kOKT);
+                    for (int k = 0; k < kC / 16; ++k)
+                        umma_ts(tbase + P::kColD6, tbase + P::kColU + 8 * k, mnmajor_desc(kt_s, 64, k), id_mma6,
+                                k > 0);
+                    umma_commit(s6);
+                }
+            } else if (write_out) {
+                __nv_bfloat16 *dst = out + (((size_t)b * T + t0) * H + h) * dv + n;
+                const size_t rs = (size_t)H * dv;
+#pragma unroll
+                for (int t = 0; t < 64; ++t)
+                    if (t < L) dst[t * rs] = __float2bfloat16_rn(v[t]);
+            }
+        }
+        if (!mbar_wait(s6, (uint32_t)(lc & 1), kWaitNs)) fail = 1;
+        tc_fence_after();
+
+        // ---- H^T <- H^T Diag(e^{g_C}) + D6^T (key channels 64 hh ..), fp16 copy for the next MMA5
+        {
+            const float4 *eg = reinterpret_cast<const float4 *>(stb + P::kOEG) + 16 * hh;
+            float v[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(trow + P::kColD6 + 64 * hh + 16 * q, v + 16 * q);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 g = eg[q];
+                Hreg[4 * q] = g.x * Hreg[4 * q] + v[4 * q];
+                Hreg[4 * q + 1] = g.y * Hreg[4 * q + 1] + v[4 * q + 1];
+                Hreg[4 * q + 2] = g.z * Hreg[4 * q + 2] + v[4 * q + 2];
+                Hreg[4 * q + 3] = g.w * Hreg[4 * q + 3] + v[4 * q + 3];
+            }
+            uint32_t w[32];
+            pack_h16(Hreg, w);
+            pack_h16(Hreg + 32, w + 16);
+            tmem_st16u(trow + P::kColH + 32 * hh, w);
+            tmem_st16u(trow + P::kColH + 32 * hh + 16, w + 16);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        const int cn = lc + 1;
+        go = vote(st == 0 && cn < nloc
+                      ? mbar_wait(&full_a[cn % P::kAStages], (uint32_t)(cn / P::kAStages) & 1u, kWaitNs)
+                      : true);
+    }
+
+    if (fail == 0 && fin)
+#pragma unroll
+        for (int i = 0; i < 64; ++i) fin[(size_t)(64 * hh + i) * dv + n] = Hreg[i];
+    tc_fence_before();
+    __syncthreads();
+    if (fail && st == 0) {
+        // drain: the MMAs this thread issued, then the loads still in flight (bounded)
+        atomicOr(status, 1 << LDN_ERR_TIMEOUT);
+        umma_commit(&drain[0]);
+        mbar_wait(&drain[0], 0, kWaitNs / 4);
+        for (int s = 0; s < P::kAStages; ++s)
+            if (pend_a[s] >= 0)
+                mbar_wait(&full_a[s], (uint32_t)(pend_a[s] / P::kAStages) & 1u, kWaitNs / 4);
+        for (int s = 0; s < P::kBStages; ++s)
+            if (pend_b[s] >= 0)
+                mbar_wait(&full_b[s], (uint32_t)(pend_b[s] / P::kBStages) & 1u, kWaitNs / 4);
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, P::kTmemCols);
+}
+
 // The scan of the sequence split: seg(0, s) = M_{s-1} seg(0, s-1) + N_{s-1}, s = 2 .. nseg-1, in
 // fp32.  One CTA of 256 threads per ((b, h), 16-column slice of the state): its slice of each
 // state depends only on its slice of the one before, which it keeps in shared memory, so the
@@ -447,13 +727,14 @@ namespace {
 template <int NS>
 cudaError_t launch_state(const ChunkArgs &a, const uint8_t *ws, size_t ws_bytes, cudaStream_t st)
 {
-    using P = Plan<NS>;
     const int units = a.B * a.H, nch = (a.T + kC - 1) / kC;
-    cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)P::kSmemBytes);
+    auto kern = NS == 2 ? chunk_state_t_kernel : chunk_state_kernel<1>;
+    const uint32_t threads = NS == 2 ? PlanT::kThreads : Plan<1>::kThreads;
+    const uint32_t smem = NS == 2 ? PlanT::kSmemBytes : Plan<1>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     auto run = [&](int pass, int nseg, int cps, float *seg) {
-        chunk_state_kernel<NS><<<(unsigned)(units * seg_jobs(pass, nseg)), P::kThreads, P::kSmemBytes, st>>>(
+        kern<<<(unsigned)(units * seg_jobs(pass, nseg)), threads, smem, st>>>(
             ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.status, pass, nseg, cps, seg);
         return cudaGetLastError();
     };

@@ -423,6 +423,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t id_m128_n64 = idesc_f16kind_f32(128, 64, 0, 0, kMmaBF16);   // MMA1 (bf16)
         const uint32_t id_m128_n64_mn = idesc_f16kind_f32(128, 64, 0, 1, kMmaF16); // MMA3
         const uint32_t id_m128_n128_mn = idesc_f16kind_f32(128, 128, 0, 1, kMmaF16);// MMA4
+        const uint32_t id_m128_n128_amn = idesc_f16kind_f32(128, 128, 1, 0, kMmaF16);// split MMA3, dv = 128
 
         // beta and log-gates of chunk cc into staging slot cc & 1 (gate warp; rows
         // past T read as zero), asynchronously so the loads overlap a whole chunk.
@@ -1448,10 +1449,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             } else if (issuer) {
                 tc_fence_after();
                 const uint32_t av_s = smem_u32(AV), ak_s = smem_u32(AK);
-                for (int j = 0; j < (SPLIT ? dv / kDVS : 1); ++j)   // split: all of dv, 64 columns at a time
+                if (SPLIT && dv == 2 * kDVS) {   // split, dv = 128: RV^T = V^T [P Tu ; Tu]^T (lane = dv column)
                     for (int k = 0; k < kC / 16; ++k)
-                        umma_bf16(tbase + col_rv<SPLIT>(s) + 64 * j, kmajor_desc(av_s, 128, k),
-                                  mnmajor_desc(v_s + j * kVBytes, 64, k), id_m128_n64_mn, k > 0);
+                        umma_bf16(tbase + col_rv<SPLIT>(s), mnmajor_desc(v_s, 64, k), kmajor_desc(av_s, 128, k),
+                                  id_m128_n128_amn, k > 0);
+                } else {
+                    for (int j = 0; j < (SPLIT ? dv / kDVS : 1); ++j)   // split: all of dv, 64 columns at a time
+                        for (int k = 0; k < kC / 16; ++k)
+                            umma_bf16(tbase + col_rv<SPLIT>(s) + 64 * j, kmajor_desc(av_s, 128, k),
+                                      mnmajor_desc(v_s + j * kVBytes, 64, k), id_m128_n64_mn, k > 0);
+                }
                 if constexpr (kKda) {   // [[I, -P Tw], [0, Tw]] [Q^ ; K^] = [Q~ ; W]
                     const uint32_t akc_s = smem_u32(sm + LY::akc);
                     for (int k = 0; k < 2 * kC / 16; ++k)
@@ -1586,7 +1593,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 }
             }
-            // (2) RV -> [P U' ; U'] staged in AV / AK (one swizzled 128 x 64 block per slice)
+            // (2) RV -> [P U' ; U'] staged in AV / AK (one swizzled 128 x 64 block per slice); for
+            //     dv = 128 its transpose, lane = dv column: block 0 = (P U')^T, block 1 = U'^T
             {
                 const uint32_t rv_col = tbase + lane_base + col_rv<SPLIT>(s);
                 for (int n = 0; n < dv; n += 32) {

@@ -152,8 +152,9 @@ int ldn_chunk_fwd_select(int dk, int dv, int chunk, int mode, int dtype);
  * Workspace contents, per (b, h, chunk), in this order (all 16-byte aligned):
  *   [Q~ ; -W] fp16, 128 x dk in the swizzled K-major layout of the state
  *   step's MMA operand (32 KiB); [P U' ; U'] fp16 per 64-column slice of dv
- *   (16 KiB each); K~ = K Diag-scaled by e^{g_C - g} fp16 (16 KiB); e^{g_C}
- *   per key channel fp32 (512 B).
+ *   (16 KiB each; for dv = 128 its transpose, two swizzled 128 x 64 blocks
+ *   (P U')^T and U'^T with one row per dv column); K~ = K Diag-scaled by
+ *   e^{g_C - g} fp16 (16 KiB); e^{g_C} per key channel fp32 (512 B).
  *
  * Sequence split: when few (b, h) are long (dv = 128, at least 48 chunks each,
  * and B*H at most a fifth of the SM count), the state recurrence of each (b, h)
