@@ -24,6 +24,7 @@
 // returns.
 #include "ldn_internal.cuh"
 #include "sm100_ptx.cuh"
+#include "tma_host.cuh"
 
 namespace ldn {
 namespace {
@@ -358,25 +359,30 @@ chunk_state_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat1
 //   H^T      <- H^T Diag(e^{g_C}) + U^T K~   (MMA6: A = U^T in TMEM, B = the K~ image, MN-major)
 // The workspace's RV part holds RV^T for dv = 128 (block 0 = (P U')^T, block 1 = U'^T, rows =
 // dv columns).  256 threads: lane n = dv column, warp half hh; in the epilogue half 0 forms U^T
-// (one warp on every SM sub-partition: the step's critical path) and half 1 the output; in the
+// (one warp on every SM sub-partition: the step's critical path) and half 1 the output, staged
+// in shared memory in the output tensor's swizzled tile layout and sent by one TMA store; in the
 // state update half hh holds key channels 64 hh .. 64 hh + 63 of row n of H^T.  A5 lands in a
-// two-stage ring, RV^T | K~ | e^{g_C} in a three-stage one, each part loaded two chunks ahead.
+// two-stage ring, RV^T | K~ (and e^{g_C}, in a ring of its own) in a three-stage one, each part
+// loaded two chunks ahead.
 struct PlanT {
     static constexpr int kThreads = 256;
     static constexpr int kAStages = 2, kBStages = 3;
     static constexpr uint32_t kA = 32768;                          // A5 image
-    static constexpr uint32_t kORV = 0, kOKT = 32768, kOEG = 49152;   // within a B stage
-    static constexpr uint32_t kTxB = 32768 + 16384 + 512;
-    static constexpr uint32_t kB = 50176;                          // B stage, 1024-aligned
+    static constexpr uint32_t kORV = 0, kOKT = 32768;              // within a B stage
+    static constexpr uint32_t kB = 49152;                          // B stage: RV^T | K~
+    static constexpr uint32_t kTxB = kB + 512;                     // and e^{g_C}
     static constexpr uint32_t kOffB = kAStages * kA;
-    static constexpr uint32_t kOffBars = kOffB + kBStages * kB;
+    static constexpr uint32_t kOffO = kOffB + kBStages * kB;       // output tile: 2 blocks of 64 x 64 bf16
+    static constexpr uint32_t kOffEG = kOffO + 16384;              // e^{g_C}: [kBStages][128] fp32
+    static constexpr uint32_t kOffBars = kOffEG + kBStages * 512;
     static constexpr uint32_t kSmemBytes = kOffBars + 128 + 1024;   // bars: a[2], b[3], smma, s6, drain[2]
     // tensor memory: D5^T, D6^T (fp32, 128 columns each), H^T (fp16 pairs, 64), U^T (fp16 pairs, 32)
     static constexpr uint32_t kColD5 = 0, kColD6 = 128, kColH = 256, kColU = 320, kTmemCols = 512;
     static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
-    static_assert(kOKT == split_kt_off(128) - kSplitRvOff && kOEG == split_eg_off(128) - kSplitRvOff,
+    static_assert(kOKT == split_kt_off(128) - kSplitRvOff && kB == split_eg_off(128) - kSplitRvOff,
                   "B stage must mirror the workspace image");
 };
+constexpr uint32_t kBarO = 3;   // the output half's threads: the tile is complete before its store
 
 __device__ __forceinline__ void pack_h16(const float *v, uint32_t *w)
 {
@@ -385,7 +391,7 @@ __device__ __forceinline__ void pack_h16(const float *v, uint32_t *w)
 }
 
 __global__ void __launch_bounds__(PlanT::kThreads, 1)
-chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloat16 *__restrict__ out,
+chunk_state_t_kernel(const __grid_constant__ CUtensorMap tm_out, const uint8_t *__restrict__ ws, const float *S0,
                      float *S_final, int T, int H, int *status, int pass, int nseg, int cps, float *seg)
 {
     using P = PlanT;
@@ -440,7 +446,9 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
     const uint32_t tbase = tmem_base_s;
     const uint32_t trow = tbase + lane_base;   // this warp's lanes
 
-    int pend_a[P::kAStages] = {-1, -1}, pend_b[P::kBStages] = {-1, -1, -1};   // thread 0
+    // loads are issued by kLoader (a U-half thread idle while MMA6 runs), not by the MMA issuer
+    constexpr int kLoader = 96;
+    int pend_a[P::kAStages] = {-1, -1}, pend_b[P::kBStages] = {-1, -1, -1};   // kLoader
     // A map (no outputs) loads only what its U rows use: the -W rows of A5 (rows 64..127 of
     // both 64-column K blocks), U'^T (RV^T block 1; none for M), K~ and e^{g_C}.  What it leaves
     // stale feeds only the O columns of its products, which it never reads.
@@ -463,20 +471,34 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
         uint8_t *d = sm + P::kOffB + s * P::kB;
         const uint8_t *u = base + (size_t)c * ub + kSplitRvOff;
         pend_b[s] = c;
+        mbar_arrive_expect_tx(&full_b[s], write_out ? P::kTxB : (use_rv ? 16384 : 0) + 16384 + 512);
         if (write_out) {
-            mbar_arrive_expect_tx(&full_b[s], P::kTxB);
-            bulk_load(d, u, P::kTxB, &full_b[s]);
+            bulk_load(d, u, P::kB, &full_b[s]);
         } else {
-            mbar_arrive_expect_tx(&full_b[s], (use_rv ? 16384 : 0) + 16384 + 512);
             if (use_rv) bulk_load(d + 16384, u + 16384, 16384, &full_b[s]);
-            bulk_load(d + P::kOKT, u + P::kOKT, 16384 + 512, &full_b[s]);
+            bulk_load(d + P::kOKT, u + P::kOKT, 16384, &full_b[s]);
+        }
+        bulk_load(sm + P::kOffEG + s * 512, u + P::kB, 512, &full_b[s]);
+    };
+    // chunk images four ahead are pulled into L2, so that the loads into the rings meet L2
+    auto prefetch = [&](int c) {
+        const uint8_t *u = base + (size_t)c * ub;
+        if (write_out) {
+            bulk_prefetch_l2(u, (uint32_t)ub);
+        } else {
+            bulk_prefetch_l2(u + 8192, 8192);
+            bulk_prefetch_l2(u + 16384 + 8192, 8192);
+            if (use_rv) bulk_prefetch_l2(u + kSplitRvOff + 16384, 16384);
+            bulk_prefetch_l2(u + kSplitRvOff + P::kOKT, 16384 + 512);
         }
     };
-    if (st == 0)
+    if (st == kLoader) {
         for (int c = 0; c < 2 && c < nloc; ++c) {
             load_a(c);
             load_b(c);
         }
+        for (int c = 2; c < 4 && c < nloc; ++c) prefetch(c);
+    }
 
     auto vote = [&](bool ok) -> bool {   // same decision in every thread
         const bool bad = named_sync_or(kBar, kThreads, !ok || fail != 0);
@@ -513,7 +535,7 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
     // the next chunk's A5, so every thread leaves the loop at the same chunk
     bool go = nloc > 0 && vote(st == 0 ? mbar_wait(&full_a[0], 0, kWaitNs) : true);
     for (int lc = 0; go && lc < nloc; ++lc) {
-        const int c = cs + lc, t0 = c * kC, L = min(kC, T - t0);
+        const int c = cs + lc, t0 = c * kC;
         const int sa = lc % P::kAStages, sb = lc % P::kBStages;
         const uint8_t *stb = sm + P::kOffB + sb * P::kB;
 
@@ -524,12 +546,14 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
             for (int k = 0; k < kDK / 16; ++k)
                 umma_ts(tbase + P::kColD5, tbase + P::kColH + 8 * k, kmajor_desc(a5_s, 128, k), id_mma5, k > 0);
             umma_commit(smma);
-            // the B part of chunk lc + 2 goes where chunk lc - 1's was: every reader of it was
-            // done at the vote that ended chunk lc - 1
+        }
+        // while MMA5 runs: the B part of chunk lc + 2 goes where chunk lc - 1's was (every reader
+        // of it was done at the vote that ended chunk lc - 1); chunk lc + 4 into L2
+        if (st == kLoader) {
             if (lc + 2 < nloc) load_b(lc + 2);
+            if (lc + 4 < nloc) prefetch(lc + 4);
         }
         wait_smma();
-        if (st == 0 && lc + 2 < nloc) load_a(lc + 2);   // MMA5 has read this chunk's A5
 
         if (!mbar_wait(&full_b[sb], (uint32_t)(lc / P::kBStages) & 1u, kWaitNs)) fail = 1;
         {
@@ -561,6 +585,7 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
                 tmem_st_wait();
                 tc_fence_before();
                 named_sync(kBarU, kThreads / 2);
+                if (st == kLoader && lc + 2 < nloc) load_a(lc + 2);   // where this chunk's A5 was
                 // ---- MMA6: D6^T = U^T K~
                 if (st == 0) {
                     tc_fence_after();
@@ -571,11 +596,19 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
                     umma_commit(s6);
                 }
             } else if (write_out) {
-                __nv_bfloat16 *dst = out + (((size_t)b * T + t0) * H + h) * dv + n;
-                const size_t rs = (size_t)H * dv;
+                // column n of the 64 x 128 output tile (rows past T are not stored); the store
+                // of the chunk before finished reading the tile before the vote that ended it
+                uint8_t *blk = sm + P::kOffO + (n >> 6) * 8192;
 #pragma unroll
                 for (int t = 0; t < 64; ++t)
-                    if (t < L) dst[t * rs] = __float2bfloat16_rn(v[t]);
+                    *reinterpret_cast<__nv_bfloat16 *>(blk + sw128_offset(t, n & 63)) = __float2bfloat16_rn(v[t]);
+                fence_proxy_async_smem();
+                named_sync(kBarO, kThreads / 2);
+                if (st == 128) {
+                    tma_store_4d(&tm_out, sm + P::kOffO, 0, h, t0, b);
+                    tma_store_4d(&tm_out, sm + P::kOffO + 8192, 64, h, t0, b);
+                    bulk_commit();
+                }
             }
         }
         if (!mbar_wait(s6, (uint32_t)(lc & 1), kWaitNs)) fail = 1;
@@ -583,7 +616,7 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
 
         // ---- H^T <- H^T Diag(e^{g_C}) + D6^T (key channels 64 hh ..), fp16 copy for the next MMA5
         {
-            const float4 *eg = reinterpret_cast<const float4 *>(stb + P::kOEG) + 16 * hh;
+            const float4 *eg = reinterpret_cast<const float4 *>(sm + P::kOffEG + sb * 512) + 16 * hh;
             float v[64];
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld16(trow + P::kColD6 + 64 * hh + 16 * q, v + 16 * q);
@@ -604,6 +637,7 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
             tmem_st_wait();
         }
         tc_fence_before();
+        if (st == 128 && write_out) bulk_wait_read_all();   // the output tile may be written again
         const int cn = lc + 1;
         go = vote(st == 0 && cn < nloc
                       ? mbar_wait(&full_a[cn % P::kAStages], (uint32_t)(cn / P::kAStages) & 1u, kWaitNs)
@@ -613,13 +647,15 @@ chunk_state_t_kernel(const uint8_t *__restrict__ ws, const float *S0, __nv_bfloa
     if (fail == 0 && fin)
 #pragma unroll
         for (int i = 0; i < 64; ++i) fin[(size_t)(64 * hh + i) * dv + n] = Hreg[i];
+    if (st == 128) bulk_wait_all();   // the output stores are done
     tc_fence_before();
     __syncthreads();
-    if (fail && st == 0) {
-        // drain: the MMAs this thread issued, then the loads still in flight (bounded)
+    if (fail && st == 0) {   // drain: the MMAs this thread issued (bounded)
         atomicOr(status, 1 << LDN_ERR_TIMEOUT);
         umma_commit(&drain[0]);
         mbar_wait(&drain[0], 0, kWaitNs / 4);
+    }
+    if (fail && st == kLoader) {   // drain: the loads still in flight (bounded)
         for (int s = 0; s < P::kAStages; ++s)
             if (pend_a[s] >= 0)
                 mbar_wait(&full_a[s], (uint32_t)(pend_a[s] / P::kAStages) & 1u, kWaitNs / 4);
@@ -728,14 +764,22 @@ template <int NS>
 cudaError_t launch_state(const ChunkArgs &a, const uint8_t *ws, size_t ws_bytes, cudaStream_t st)
 {
     const int units = a.B * a.H, nch = (a.T + kC - 1) / kC;
-    auto kern = NS == 2 ? chunk_state_t_kernel : chunk_state_kernel<1>;
-    const uint32_t threads = NS == 2 ? PlanT::kThreads : Plan<1>::kThreads;
+    CUtensorMap tm_out;   // dv = 128: [B][T][H][dv] bf16 in 64 x 64 tiles (128-byte swizzle)
+    if (NS == 2 && !make_tmap_bf16_4d(&tm_out, a.out, 128, a.H, a.T, a.B, 64, kC)) return cudaErrorInvalidValue;
     const uint32_t smem = NS == 2 ? PlanT::kSmemBytes : Plan<1>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = NS == 2 ? cudaFuncSetAttribute(chunk_state_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem)
+                            : cudaFuncSetAttribute(chunk_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
     if (e != cudaSuccess) return e;
     auto run = [&](int pass, int nseg, int cps, float *seg) {
-        kern<<<(unsigned)(units * seg_jobs(pass, nseg)), threads, smem, st>>>(
-            ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.status, pass, nseg, cps, seg);
+        const unsigned grid = (unsigned)(units * seg_jobs(pass, nseg));
+        if (NS == 2)
+            chunk_state_t_kernel<<<grid, PlanT::kThreads, smem, st>>>(tm_out, ws, a.S0, a.S_final, a.T, a.H,
+                                                                      a.status, pass, nseg, cps, seg);
+        else
+            chunk_state_kernel<1><<<grid, Plan<1>::kThreads, smem, st>>>(
+                ws, a.S0, (__nv_bfloat16 *)a.out, a.S_final, a.T, a.H, a.status, pass, nseg, cps, seg);
         return cudaGetLastError();
     };
     const size_t base = (size_t)units * nch * split_unit_bytes(a.dv);

@@ -275,6 +275,17 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// 4-D tiled store from shared memory as a bulk async-group of the issuing thread (elements
+// outside the tensor are not written); commit, then wait for the group's reads before the
+// shared-memory tile is written again.
+__device__ __forceinline__ void tma_store_4d(const void *tmap, const void *src, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+                 : "memory");
+}
+
 // 1-D bulk copy global -> shared (both addresses 16-byte aligned, size a
 // multiple of 16), completing `bytes` of transactions on `bar`.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
