@@ -1549,6 +1549,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint8_t *Vt = sm + LY::v + ls * LY::vbytes;
             if (!serial_vote(st == 0 ? mbar_wait(&S.bar_ready[s], (c >> 1) & 1, kWaitNs) : true)) break;
             tc_fence_after();
+            if (kStages >= 3 && st == 0 && c >= 1) {   // chunk c - 1's stores have read its tile stage
+                bulk_wait_read_all();
+                if (c - 1 + kStages < nchunks) issue_load(c - 1 + kStages);
+            }
             uint8_t *u = ws + ((size_t)unit * nchunks_all + cb + c) * ubytes;
             const bool top = st < 64;
             // (1) DK -> [Q~ ; -W] row st in registers (packed fp16); DK is handed back at once
@@ -1675,11 +1679,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 bulk_store(u, QK, 32768);
                 bulk_store(u + split_kt_off(dv), Vt, 16384);
                 bulk_commit();
-                bulk_wait_read_all();   // the tile stage may be reloaded from here on
+                // With three tile stages the stage is reloaded after the next chunk's vote,
+                // once these stores have read it.  With two (KDA, GDN2) the chunk after next
+                // must be in flight before that vote: the next chunk's MMA1 precedes this
+                // chunk's "ready" there.
+                if constexpr (kStages < 3) {
+                    bulk_wait_read_all();
+                    if (c + kStages < nchunks) issue_load(c + kStages);
+                }
                 // RV of chunk c and gate slot c % 3 are read (RV has two buffers)
                 mbar_arrive(&S.bar_rvfree[s]);
                 if (kKda) mbar_arrive(&S.bar_kbfree[c & 1]);
-                if (c + kStages < nchunks) issue_load(c + kStages);
             }
         }
         if (st == 0) bulk_wait_all();   // the workspace is complete before the CTA leaves
