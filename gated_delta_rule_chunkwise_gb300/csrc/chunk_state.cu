@@ -12,9 +12,11 @@
 //   H      <- Diag(e^{g_C}) H + K~^T U                      (MMA6)
 // and O (rows 0..63) is the chunk's output.
 //
-// One CTA per (b, h) over the whole dv (an N = 128 product costs what an N = 64
-// one does), 128 threads per 64-wide dv slice: thread = (row of the fp32 state,
-// dv slice), the row's slice held in registers.  The operands of a chunk land in
+// chunk_state_kernel<NS>: one CTA per (b, h) over the whole dv = 64 NS, 128 threads
+// per 64-wide dv slice: thread = (row of the fp32 state, dv slice), the row's slice
+// held in registers.  It runs dv = 64 (NS = 1); dv = 128 runs the transposed kernel
+// further below (chunk_state_t_kernel), whose epilogue work spreads over every SM
+// sub-partition instead of the two that own the U rows' lanes.  The operands of a chunk land in
 // a two-stage ring in two parts with a barrier each: A5 (read by MMA5 at the
 // start of the chunk) and RV | K~ | e^{g_C} (read later in the chunk).  A5 of
 // chunk c + 2 is loaded as soon as MMA5 of chunk c has read its slot, the rest of
