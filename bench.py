@@ -48,6 +48,21 @@ KERNEL_NAME = {2: "tcgen05", 3: "split", 4: "pair", 5: "presolved"}   # LDN_VARI
 TWO_LAUNCH = (3, 5)   # variants that make two launches per call (split, pre-solved)
 
 
+def noalloc_pieces(B, T, H, dv, chosen):
+    """Pieces a call with S_final through the library's 256 MiB array is cut into (groups
+    of whole sequences, or runs of chunks of one sequence), as the C header states for the
+    no-allocation entry and Gated DeltaNet-2."""
+    cap = 256 << 20
+    unit = 32768 + (dv // 64) * 16384 + 16896 if chosen == 3 else 16384
+    nch = (T + 63) // 64
+    per_seq = H * nch * unit
+    if per_seq <= cap:
+        nb = min(B, cap // per_seq)
+        return (B + nb - 1) // nb
+    tpc = cap // (H * unit)   # runs of chunks (S_final given: the state is carried in it)
+    return B * ((nch + tpc - 1) // tpc)
+
+
 def chunk_launches(chosen, B, T, H, dk, dv, mode, dt, ws_bytes):
     """Kernel launches of one chunkwise forward call: the split variant makes four when it
     cuts long sequences into segments (maps, scan, outputs after the preparation)."""
@@ -536,8 +551,8 @@ def run_ours(args):
                 ostep()
                 e1.record(stream)
             barrier()
-            onl = (2 if ochosen in TWO_LAUNCH else 1) if g2 else chunk_launches(ochosen, ow.B, ow.T, ow.H, ow.dk,
-                                                                                 ow.dv, ow.mode, odt, ows_bytes)
+            onl = ((2 * noalloc_pieces(ow.B, ow.T, ow.H, ow.dv, ochosen) if ochosen in TWO_LAUNCH else 1) if g2
+                   else chunk_launches(ochosen, ow.B, ow.T, ow.H, ow.dk, ow.dv, ow.mode, odt, ows_bytes))
             launches += 4 * onl
             oms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in oev))
             ob = chunk_bytes(ow.B, ow.T, ow.H, ow.dk, ow.dv, oel, ow.mode, ow.S0 is not None, True)
@@ -646,11 +661,11 @@ def run_ours(args):
                 bstep()
                 e1.record(stream)
             barrier()
-            launches += (4 if chunked else 3) * (1 + len(bev))
+            launches += (5 if chunked else 3) * (1 + len(bev))
             bms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in bev))
             bb = backward_bytes(B_, T_, H_, dk_, dv_, el_bytes_of(bw.dtype), bw.mode)
             kernels = ("chunk_tc_kernel<prep-X> + chunk_tc_kernel<fed> (forward with chunk states) + "
-                       "bwd_chain_kernel + bwd_chunk_kernel" if chunked else
+                       "bwd_prep_kernel + bwd_chain_kernel + bwd_chunk_kernel" if chunked else
                        "bwd_kernel<phase 1> + bwd_kernel<phase 2> + bwd_reduce_kernel")
             backward[name] = {"ms_per_call": bms, "tokens_per_s": world * B_ * T_ / (bms / 1e3),
                               "form": "chunkwise" if chunked else "recurrent", "kernels": kernels,
